@@ -1,0 +1,431 @@
+// Host arbitrary-precision naturals for the reconstruction stage.
+#include "bigint.h"
+
+#include <algorithm>
+#include <cstring>
+
+namespace es {
+namespace big {
+
+using u128 = unsigned __int128;
+
+void trim(Nat& a) {
+  while (!a.empty() && a.back() == 0) a.pop_back();
+}
+bool is_zero(const Nat& a) { return a.empty(); }
+int cmp(const Nat& a, const Nat& b) {
+  if (a.size() != b.size()) return a.size() < b.size() ? -1 : 1;
+  for (size_t i = a.size(); i-- > 0;)
+    if (a[i] != b[i]) return a[i] < b[i] ? -1 : 1;
+  return 0;
+}
+size_t bitlen(const Nat& a) {
+  return a.empty() ? 0 : 64 * (a.size() - 1) + (64 - (size_t)__builtin_clzll(a.back()));
+}
+Nat from_u64(uint64_t v) { return v ? Nat{v} : Nat{}; }
+
+bool le_pow2(const Nat& a, size_t k) {
+  size_t bl = bitlen(a);
+  if (bl <= k) return true;
+  if (bl > k + 1) return false;
+  // bl == k + 1: a <= 2^k iff a == 2^k
+  size_t w = k / 64;
+  if (a[w] != (limb(1) << (k % 64))) return false;
+  for (size_t i = 0; i < w; ++i)
+    if (a[i]) return false;
+  return true;
+}
+
+void add_in(Nat& a, const Nat& b) {
+  if (a.size() < b.size()) a.resize(b.size(), 0);
+  limb carry = 0;
+  for (size_t i = 0; i < b.size(); ++i) {
+    u128 s = (u128)a[i] + b[i] + carry;
+    a[i] = (limb)s;
+    carry = (limb)(s >> 64);
+  }
+  for (size_t i = b.size(); carry && i < a.size(); ++i) {
+    a[i] += 1;
+    carry = (a[i] == 0);
+  }
+  if (carry) a.push_back(1);
+}
+Nat add(const Nat& a, const Nat& b) {
+  Nat r = a;
+  add_in(r, b);
+  return r;
+}
+
+void sub_in(Nat& a, const Nat& b) {
+  limb borrow = 0;
+  for (size_t i = 0; i < b.size(); ++i) {
+    limb x = a[i], y = b[i];
+    limb t1 = x - y, b1 = x < y;
+    limb t2 = t1 - borrow, b2 = t1 < borrow;
+    a[i] = t2;
+    borrow = b1 | b2;
+  }
+  for (size_t i = b.size(); borrow && i < a.size(); ++i) {
+    borrow = (a[i] == 0);
+    a[i] -= 1;
+  }
+  trim(a);
+}
+Nat sub(const Nat& a, const Nat& b) {
+  Nat r = a;
+  sub_in(r, b);
+  return r;
+}
+
+// r[0 .. an+bn) = a * b (r zeroed by the caller)
+static void mul_school(limb* r, const limb* a, size_t an, const limb* b, size_t bn) {
+  for (size_t i = 0; i < an; ++i) {
+    limb ai = a[i], carry = 0;
+    for (size_t j = 0; j < bn; ++j) {
+      u128 t = (u128)ai * b[j] + r[i + j] + carry;
+      r[i + j] = (limb)t;
+      carry = (limb)(t >> 64);
+    }
+    r[i + bn] = carry;
+  }
+}
+
+static limb add_into(limb* r, size_t rn, const limb* a, size_t an) {  // r += a, returns carry out of rn
+  limb carry = 0;
+  size_t i = 0;
+  for (; i < an; ++i) {
+    u128 s = (u128)r[i] + a[i] + carry;
+    r[i] = (limb)s;
+    carry = (limb)(s >> 64);
+  }
+  for (; carry && i < rn; ++i) {
+    r[i] += 1;
+    carry = (r[i] == 0);
+  }
+  return carry;
+}
+static void sub_into(limb* r, size_t rn, const limb* a, size_t an) {  // r -= a (r >= a)
+  limb borrow = 0;
+  size_t i = 0;
+  for (; i < an; ++i) {
+    limb x = r[i], y = a[i];
+    limb t1 = x - y, b1 = x < y;
+    limb t2 = t1 - borrow, b2 = t1 < borrow;
+    r[i] = t2;
+    borrow = b1 | b2;
+  }
+  for (; borrow && i < rn; ++i) {
+    borrow = (r[i] == 0);
+    r[i] -= 1;
+  }
+}
+
+constexpr size_t kKaraThreshold = 40;
+
+// r[0 .. 2n) = a[0..n) * b[0..n)
+static void kara(limb* r, const limb* a, const limb* b, size_t n) {
+  if (n < kKaraThreshold) {
+    std::fill(r, r + 2 * n, 0);
+    mul_school(r, a, n, b, n);
+    return;
+  }
+  size_t h = n / 2, hh = n - h;
+  std::fill(r, r + 2 * n, 0);
+  std::vector<limb> z0(2 * h), z2(2 * hh);
+  kara(z0.data(), a, b, h);
+  kara(z2.data(), a + h, b + h, hh);
+  std::vector<limb> sa(hh + 1, 0), sb(hh + 1, 0);
+  std::copy(a + h, a + n, sa.begin());
+  std::copy(b + h, b + n, sb.begin());
+  sa[hh] = add_into(sa.data(), hh, a, h);
+  sb[hh] = add_into(sb.data(), hh, b, h);
+  std::vector<limb> z1(2 * (hh + 1));
+  kara(z1.data(), sa.data(), sb.data(), hh + 1);
+  sub_into(z1.data(), z1.size(), z0.data(), z0.size());
+  sub_into(z1.data(), z1.size(), z2.data(), z2.size());
+  std::copy(z0.begin(), z0.end(), r);
+  std::copy(z2.begin(), z2.end(), r + 2 * h);
+  size_t z1n = z1.size();
+  while (z1n && z1[z1n - 1] == 0) --z1n;
+  add_into(r + h, 2 * n - h, z1.data(), z1n);
+}
+
+Nat mul(const Nat& a, const Nat& b) {
+  if (a.empty() || b.empty()) return {};
+  const Nat& x = a.size() <= b.size() ? a : b;
+  const Nat& y = a.size() <= b.size() ? b : a;
+  size_t n = x.size(), m = y.size();
+  Nat r(n + m, 0);
+  if (n < kKaraThreshold) {
+    mul_school(r.data(), x.data(), n, y.data(), m);
+  } else {
+    std::vector<limb> t(2 * n);
+    for (size_t off = 0; off < m; off += n) {
+      size_t len = std::min(n, m - off);
+      if (len == n) {
+        kara(t.data(), x.data(), y.data() + off, n);
+        add_into(r.data() + off, n + m - off, t.data(), 2 * n);
+      } else {
+        Nat part(y.begin() + off, y.begin() + off + len), xx = x;
+        trim(part);
+        Nat p = mul(xx, part);
+        add_into(r.data() + off, n + m - off, p.data(), p.size());
+      }
+    }
+  }
+  trim(r);
+  return r;
+}
+
+Nat mul_small(const Nat& a, limb s) {
+  if (a.empty() || s == 0) return {};
+  Nat r(a.size() + 1);
+  limb carry = 0;
+  for (size_t i = 0; i < a.size(); ++i) {
+    u128 t = (u128)a[i] * s + carry;
+    r[i] = (limb)t;
+    carry = (limb)(t >> 64);
+  }
+  r[a.size()] = carry;
+  trim(r);
+  return r;
+}
+
+void mul_small_add_in(Nat& a, const limb* s, int slen, const limb* addv, int alen) {
+  size_t an = a.size();
+  Nat r(an + slen + 1, 0);
+  if (an) mul_school(r.data(), a.data(), an, s, (size_t)slen);
+  add_into(r.data(), r.size(), addv, (size_t)alen);
+  trim(r);
+  a.swap(r);
+}
+
+Nat shl(const Nat& a, size_t bits) {
+  if (a.empty()) return {};
+  size_t w = bits / 64, b = bits % 64;
+  Nat r(a.size() + w + 1, 0);
+  for (size_t i = 0; i < a.size(); ++i) {
+    r[i + w] |= a[i] << b;
+    if (b) r[i + w + 1] |= a[i] >> (64 - b);
+  }
+  trim(r);
+  return r;
+}
+
+Nat shr(const Nat& a, size_t bits) {
+  size_t w = bits / 64, b = bits % 64;
+  if (w >= a.size()) return {};
+  Nat r(a.size() - w, 0);
+  for (size_t i = 0; i < r.size(); ++i) {
+    r[i] = a[i + w] >> b;
+    if (b && i + w + 1 < a.size()) r[i] |= a[i + w + 1] << (64 - b);
+  }
+  trim(r);
+  return r;
+}
+
+// Knuth, TAOCP vol. 2, 4.3.1, Algorithm D, with 64-bit limbs.
+void divmod(const Nat& u, const Nat& v, Nat* q, Nat* r) {
+  const size_t n = v.size(), mlen = u.size();
+  if (cmp(u, v) < 0) {
+    if (q) q->clear();
+    if (r) *r = u;
+    return;
+  }
+  if (n == 1) {
+    const limb d = v[0];
+    Nat qq(mlen);
+    u128 rem = 0;
+    for (size_t i = mlen; i-- > 0;) {
+      u128 cur = (rem << 64) | u[i];
+      qq[i] = (limb)(cur / d);
+      rem = cur % d;
+    }
+    trim(qq);
+    if (q) q->swap(qq);
+    if (r) *r = from_u64((limb)rem);
+    return;
+  }
+  const int s = __builtin_clzll(v.back());
+  Nat vn(n), un(mlen + 1);
+  for (size_t i = n - 1; i > 0; --i) vn[i] = (v[i] << s) | (s ? v[i - 1] >> (64 - s) : 0);
+  vn[0] = v[0] << s;
+  un[mlen] = s ? u[mlen - 1] >> (64 - s) : 0;
+  for (size_t i = mlen - 1; i > 0; --i) un[i] = (u[i] << s) | (s ? u[i - 1] >> (64 - s) : 0);
+  un[0] = u[0] << s;
+  Nat qq(mlen - n + 1, 0);
+  const limb vtop = vn[n - 1], vsec = vn[n - 2];
+  for (ptrdiff_t j = (ptrdiff_t)(mlen - n); j >= 0; --j) {
+    u128 num = ((u128)un[j + n] << 64) | un[j + n - 1];
+    u128 qhat = num / vtop, rhat = num % vtop;
+    while ((qhat >> 64) != 0 || qhat * vsec > ((rhat << 64) | un[j + n - 2])) {
+      qhat -= 1;
+      rhat += vtop;
+      if ((rhat >> 64) != 0) break;
+    }
+    limb borrow = 0, carry = 0;
+    const limb qh = (limb)qhat;
+    for (size_t i = 0; i < n; ++i) {
+      u128 p = (u128)qh * vn[i] + carry;
+      carry = (limb)(p >> 64);
+      limb pl = (limb)p, x = un[i + j];
+      limb t1 = x - pl, b1 = x < pl;
+      limb t2 = t1 - borrow, b2 = t1 < borrow;
+      un[i + j] = t2;
+      borrow = b1 | b2;
+    }
+    limb x = un[j + n];
+    limb t1 = x - carry, b1 = x < carry;
+    limb t2 = t1 - borrow, b2 = t1 < borrow;
+    un[j + n] = t2;
+    limb qfinal = qh;
+    if (b1 | b2) {  // went negative: add back once
+      qfinal -= 1;
+      limb c = 0;
+      for (size_t i = 0; i < n; ++i) {
+        u128 sum = (u128)un[i + j] + vn[i] + c;
+        un[i + j] = (limb)sum;
+        c = (limb)(sum >> 64);
+      }
+      un[j + n] += c;
+    }
+    qq[(size_t)j] = qfinal;
+  }
+  if (q) {
+    trim(qq);
+    q->swap(qq);
+  }
+  if (r) {
+    Nat rr(n);
+    for (size_t i = 0; i < n; ++i) rr[i] = (un[i] >> s) | (s ? un[i + 1] << (64 - s) : 0);
+    trim(rr);
+    r->swap(rr);
+  }
+}
+
+// ------------------------------------------------------------ Lehmer
+static uint64_t bits_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^64
+  size_t w = sh / 64, b = sh % 64;
+  uint64_t lo = w < x.size() ? x[w] : 0, hi = w + 1 < x.size() ? x[w + 1] : 0;
+  return b ? (lo >> b) | (hi << (64 - b)) : lo;
+}
+
+// A x + B y for cofactors of opposite signs (or a zero one); the result is
+// known to be non-negative.
+static Nat comb(int64_t A, const Nat& x, int64_t B, const Nat& y) {
+  if (A >= 0 && B >= 0) {
+    Nat t = mul_small(x, (limb)A);
+    add_in(t, mul_small(y, (limb)B));
+    return t;
+  }
+  if (A >= 0) {
+    Nat t = mul_small(x, (limb)A);
+    sub_in(t, mul_small(y, (limb)(-B)));
+    return t;
+  }
+  Nat t = mul_small(y, (limb)B);
+  sub_in(t, mul_small(x, (limb)(-A)));
+  return t;
+}
+
+static inline limb uabs(int64_t v) { return v < 0 ? (limb)(-v) : (limb)v; }
+
+// Shared loop: r0 >= r1; stops when r1 <= 2^nbits (or r1 == 0 when nbits < 0).
+static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits) {
+  auto done = [&](const Nat& x) { return nbits < 0 ? x.empty() : le_pow2(x, (size_t)nbits); };
+  bool single_only = false;
+  const size_t nb = nbits < 0 ? 0 : (size_t)nbits;
+  while (!done(r1)) {
+    size_t bl1 = bitlen(r1);
+    if (!single_only && r1.size() >= 3 && bl1 > nb + 200) {
+      const bool guard = bl1 < nb + 400;
+      Nat s0, s1, sT0, sT1;
+      size_t ssteps = *steps;
+      if (guard) {
+        s0 = r0;
+        s1 = r1;
+        if (T0) {
+          sT0 = *T0;
+          sT1 = *T1;
+        }
+      }
+      const size_t sh = bitlen(r0) - 62;
+      int64_t a = (int64_t)bits_at(r0, sh), b = (int64_t)bits_at(r1, sh);
+      int64_t A = 1, B = 0, C = 0, D = 1;
+      size_t k = 0;
+      for (;;) {
+        if (b + C <= 0 || b + D <= 0) break;
+        int64_t q1 = (a + A) / (b + C), q2 = (a + B) / (b + D);
+        if (q1 != q2) break;
+        int64_t t = A - q1 * C;
+        A = C;
+        C = t;
+        t = B - q1 * D;
+        B = D;
+        D = t;
+        t = a - q1 * b;
+        a = b;
+        b = t;
+        ++k;
+      }
+      if (B != 0) {
+        Nat n0 = comb(A, r0, B, r1), n1 = comb(C, r0, D, r1);
+        r0.swap(n0);
+        r1.swap(n1);
+        if (T0) {
+          Nat m0 = mul_small(*T0, uabs(A)), m1 = mul_small(*T0, uabs(C));
+          add_in(m0, mul_small(*T1, uabs(B)));
+          add_in(m1, mul_small(*T1, uabs(D)));
+          T0->swap(m0);
+          T1->swap(m1);
+        }
+        *steps += k;
+        if (guard && done(r1)) {  // overshot the stopping point: redo singly
+          r0.swap(s0);
+          r1.swap(s1);
+          if (T0) {
+            T0->swap(sT0);
+            T1->swap(sT1);
+          }
+          *steps = ssteps;
+          single_only = true;
+        }
+        continue;
+      }
+    }
+    // one division step
+    Nat q, rem;
+    divmod(r0, r1, &q, &rem);
+    r0.swap(r1);
+    r1.swap(rem);
+    if (T0) {
+      Nat t = mul(q, *T1);
+      add_in(t, *T0);
+      T0->swap(*T1);
+      T1->swap(t);
+    }
+    ++*steps;
+  }
+}
+
+bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den) {
+  Nat r0 = M, r1 = u, T0, T1 = from_u64(1);
+  size_t steps = 0;
+  euclid(r0, r1, &T0, &T1, &steps, (long)nbits);
+  if (T1.empty()) return false;
+  *num = r1;
+  *num_neg = (steps & 1) && !r1.empty();
+  *den = T1;
+  return true;
+}
+
+Nat gcd(const Nat& a, const Nat& b) {
+  Nat r0 = a, r1 = b;
+  if (cmp(r0, r1) < 0) r0.swap(r1);
+  size_t steps = 0;
+  euclid(r0, r1, nullptr, nullptr, &steps, -1);
+  return r0;
+}
+
+}  // namespace big
+}  // namespace es

@@ -1,0 +1,41 @@
+// Minimal arbitrary-precision naturals for the host reconstruction stage
+// (64-bit limbs, little-endian, no leading zero limbs; zero = empty).
+// Schoolbook and Karatsuba multiplication, Knuth's Algorithm D division,
+// Lehmer's extended Euclid.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+namespace es {
+namespace big {
+
+using limb = uint64_t;
+using Nat = std::vector<limb>;
+
+void trim(Nat& a);
+int cmp(const Nat& a, const Nat& b);
+size_t bitlen(const Nat& a);
+bool is_zero(const Nat& a);
+Nat from_u64(uint64_t v);
+Nat add(const Nat& a, const Nat& b);
+Nat sub(const Nat& a, const Nat& b);  // a >= b
+void add_in(Nat& a, const Nat& b);
+void sub_in(Nat& a, const Nat& b);  // a >= b
+Nat mul(const Nat& a, const Nat& b);
+Nat mul_small(const Nat& a, limb s);
+void mul_small_add_in(Nat& a, const limb* s, int slen, const limb* add, int alen);  // a = a*s + add
+void divmod(const Nat& u, const Nat& v, Nat* q, Nat* r);                            // v != 0
+Nat shl(const Nat& a, size_t bits);
+Nat shr(const Nat& a, size_t bits);
+// a <= 2^k
+bool le_pow2(const Nat& a, size_t k);
+
+// Extended Euclid on (r0 = M, r1 = u) stopped at the first remainder <= 2^nbits
+// (Wang's rational reconstruction).  Returns den = |t| and num = r with its
+// sign (num_neg), or false when no remainder ever gets that small.
+bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den);
+Nat gcd(const Nat& a, const Nat& b);
+
+}  // namespace big
+}  // namespace es

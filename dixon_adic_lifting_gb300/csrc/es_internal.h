@@ -1,0 +1,114 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/es.h"
+
+namespace es {
+
+// ---------------------------------------------------------------- errors
+void set_last_error(const std::string& s);
+// Records the CUDA error (if any) and returns ES_ERR_CUDA / ES_OK.
+es_status cuda_status(int cuda_err, const char* where);
+
+#define ES_CHECK(expr)                     \
+  do {                                     \
+    es_status _st = (expr);                \
+    if (_st != ES_OK) return _st;          \
+  } while (0)
+
+// ---------------------------------------------------------------- workspace
+// Grow-only device workspace of the current device, carved into regions by
+// a Layout.  Each region starts on a 256-byte boundary.
+struct Layout {
+  size_t total = 0;
+  size_t add(size_t bytes) {
+    size_t off = total;
+    total += (bytes + 255) / 256 * 256;
+    return off;
+  }
+};
+
+// Ensures the current device's workspace holds at least `bytes`; returns its
+// base in *base.  max_bytes != 0 caps the size (ES_ERR_NOMEM beyond it).
+es_status workspace_get(size_t bytes, size_t max_bytes, bool inject_nomem, char** base);
+
+// Stream to use for a caller-given handle (NULL -> the library's stream).
+void* resolve_stream(void* user_stream);
+
+// Current device's SM count (cached).
+int sm_count();
+
+// Row-stride of the int8 residue matrices: n rounded up to 16 bytes.
+inline int64_t padded_ld(int64_t n) { return (n + 15) / 16 * 16; }
+
+// ---------------------------------------------------------------- range
+// Device statistics of A and b used by the range check and the bounds.
+struct Stats {
+  uint64_t max_abs_a;   // max |A_ij| (|-2^63| = 2^63 as uint64)
+  int zero_row;         // some row of A is zero
+  double log2_d;        // sum_i 0.5 log2 ||a_i||^2
+  double log2_n;        // sum_i 0.5 log2 (||a_i||^2 + max_k b_ik^2)
+};
+es_status compute_stats(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, char* scratch,
+                        void* stream, Stats* out);
+// scratch bytes compute_stats needs
+size_t stats_scratch_bytes(int64_t n);
+bool in_range(int64_t n, uint64_t max_abs_a);
+
+// Bounds and step count from Stats and the good-prime flags.
+void plan_from_stats(const Stats& s, const uint8_t* good, int64_t* num_bits, int64_t* den_bits, int32_t* m);
+
+// ---------------------------------------------------------------- stages
+// Residues of `count` int64 values for all 53 primes: out[j*ostride + i].
+es_status launch_residues(const int64_t* src, int64_t count, int8_t* out, int64_t ostride, void* stream);
+// Residues of A [n, n] into W [53][n][ld] (balanced, padding zero).
+es_status launch_residues_matrix(const int64_t* A, int64_t n, int64_t ld, int8_t* W, void* stream);
+
+// Batched modular inverse: A_dev -> B [53][n][ld], good [53] (device).
+size_t inverse_scratch_bytes(int64_t n);
+es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev, char* scratch,
+                      void* stream);
+
+// Kernel accounting: every launch site adds to the launch counter; the lift
+// optionally brackets each launch of its product kernel with CUDA events.
+void count_launch(int64_t k = 1);
+int64_t launch_count();
+struct KernelTiming {
+  bool events = false;       // bracket each product-kernel launch with events
+  int64_t launches = 0;      // product-kernel launches
+  double ms = 0.0;           // their summed event time
+  double bytes_per_launch = 0.0;
+};
+
+// Lift: m steps -> digits [m][n*c][6].
+size_t lift_scratch_bytes(int64_t n, int64_t c, int E, bool a32);
+es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
+                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                   void* stream, KernelTiming* kt = nullptr);
+
+// ---------------------------------------------------------------- solution
+struct Solution {
+  int64_t n = 0, c = 0, limbs = 0;
+  std::vector<uint64_t> num;  // [n*c*limbs]
+  std::vector<uint64_t> den;  // [limbs]
+  double ms[ES_NUM_PHASES] = {0, 0, 0, 0, 0, 0};
+  int32_t m = 0;
+  int32_t primes_used = 0;
+  int64_t launches = 0;
+  KernelTiming top;
+};
+
+// Host reconstruction (recon.cpp).  digits [m][n*c][6].
+es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,
+                      int64_t num_bits, int64_t den_bits, int threads, bool inject_fault, Solution* out);
+
+}  // namespace es
+
+struct es_solution {
+  es::Solution s;
+};

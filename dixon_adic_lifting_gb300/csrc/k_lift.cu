@@ -1,0 +1,474 @@
+// The Dixon lift: m steps of
+//     x_i = B r_i mod P      (per prime: Y_j = B_j R_j, exact int32, then mod q_j)
+//     balanced CRT of the E' residues into one base-P digit x_i
+//     r_{i+1} = (r_i - A x_i) P^{-1} mod 2^64   (one signed 64-bit limb)
+// exact-solve card, §Method: "the lift (per-step per-prime products as one
+// batched INT8 GEMM, CRT reconstruction of the wide digit, and the residual
+// update in one limb as (r_i - A x_i) P^{-1} mod 2^64, P odd)", with the
+// range n * max|A_ij| < 2^63 keeping the residual in one limb and K = n <=
+// 2^17 keeping the int32 accumulator exact (2^17 * 125^2 < 2^31).
+//
+// Device buffers of one lift:
+//   B     int8   [53][n][ld]       inverses (ld = n rounded up to 16), only good primes read
+//   R     int8   [E'][c][ld]       balanced residues of r_i, column-major per prime, zero padded
+//   V     int8   [E'][n*c]         balanced residues of x_i
+//   r     int64  [2][n*c]          residual (double buffer)
+//   xl    uint64 [n*c]             x_i mod 2^64
+//   D     uint64 [m][n*c][6]       the digits
+//   A32   int32  [n][n]            A narrowed when max|A| < 2^31 (else A int64 is read)
+//   K     LiftConst                CRT / residual constants of the good prime set
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <vector>
+
+#include "es_common.cuh"
+#include "es_internal.h"
+
+namespace es {
+
+struct LiftConst {
+  int32_t E;                      // number of good primes
+  int32_t pidx[kNumPrimes];       // their indices in the prime table, ascending
+  ModQ mq[kNumPrimes];            // reduction constants, compact order
+  uint32_t w[kNumPrimes];         // (P'/q)^{-1} mod q
+  uint64_t tfix[kNumPrimes];      // floor(2^50 / q)
+  uint32_t Mq[kNumPrimes][kCrtWords];  // P'/q, 32-bit little-endian words
+  uint32_t P[kCrtWords];          // P'
+  uint32_t Phalf[kCrtWords];      // (P' - 1) / 2
+  uint64_t Pinv64;                // P'^{-1} mod 2^64
+};
+
+// ------------------------------------------------------------ host constants
+namespace {
+// little-endian 32-bit word arithmetic on kCrtWords words
+void w_mul_small(uint32_t* x, uint32_t s) {
+  uint64_t carry = 0;
+  for (int l = 0; l < kCrtWords; ++l) {
+    uint64_t t = (uint64_t)x[l] * s + carry;
+    x[l] = (uint32_t)t;
+    carry = t >> 32;
+  }
+}
+uint32_t w_mod_small(const uint32_t* x, uint32_t q) {
+  uint64_t r = 0;
+  for (int l = kCrtWords - 1; l >= 0; --l) r = ((r << 32) | x[l]) % q;
+  return (uint32_t)r;
+}
+uint32_t inv_small(uint32_t a, uint32_t q) {  // extended Euclid, a != 0 mod q
+  int64_t t0 = 0, t1 = 1, r0 = q, r1 = a % q;
+  while (r1) {
+    int64_t qq = r0 / r1, tmp = r0 - qq * r1;
+    r0 = r1;
+    r1 = tmp;
+    tmp = t0 - qq * t1;
+    t0 = t1;
+    t1 = tmp;
+  }
+  return (uint32_t)((t0 % (int64_t)q + q) % q);
+}
+}  // namespace
+
+void build_lift_const(const uint8_t* good, LiftConst* K) {
+  std::memset(K, 0, sizeof(*K));
+  int E = 0;
+  for (int j = 0; j < kNumPrimes; ++j)
+    if (good[j]) K->pidx[E++] = j;
+  K->E = E;
+  uint32_t P[kCrtWords] = {1};
+  for (int e = 0; e < E; ++e) w_mul_small(P, kPrimes[K->pidx[e]]);
+  std::memcpy(K->P, P, sizeof(P));
+  // (P - 1) / 2 (P odd)
+  uint32_t h[kCrtWords];
+  std::memcpy(h, P, sizeof(P));
+  h[0] -= 1;
+  for (int l = 0; l < kCrtWords; ++l) h[l] = (h[l] >> 1) | (l + 1 < kCrtWords ? (h[l + 1] << 31) : 0);
+  std::memcpy(K->Phalf, h, sizeof(h));
+  for (int e = 0; e < E; ++e) {
+    uint32_t q = kPrimes[K->pidx[e]];
+    K->mq[e] = make_modq(q);
+    uint32_t Mq[kCrtWords] = {1};
+    for (int f = 0; f < E; ++f)
+      if (f != e) w_mul_small(Mq, kPrimes[K->pidx[f]]);
+    std::memcpy(K->Mq[e], Mq, sizeof(Mq));
+    K->w[e] = inv_small(w_mod_small(Mq, q), q);
+    K->tfix[e] = (1ull << 50) / q;
+  }
+  // P^{-1} mod 2^64 by Newton's iteration x <- x (2 - P x) (P x = 1 mod 8 for x = P)
+  uint64_t p64 = (uint64_t)P[0] | ((uint64_t)P[1] << 32), x = p64;
+  for (int it = 0; it < 6; ++it) x *= 2 - p64 * x;
+  K->Pinv64 = x;
+}
+
+// ------------------------------------------------------------ kernels
+// r0 = b, R = residues of b.  Thread per entry, row fastest.
+__global__ void k_lift_init(const int64_t* __restrict__ b, int64_t n, int64_t c, int64_t ld,
+                            const LiftConst* __restrict__ K, int64_t* __restrict__ r, int8_t* __restrict__ R) {
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n * c) return;
+  int64_t row = t % n, col = t / n;
+  int64_t v = b[row * c + col];
+  r[row * c + col] = v;
+  const int E = K->E;
+  for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+}
+
+// c == 1: V[e][i] = bal(sum_k B_j[i][k] R_e[k]).  Grid (n/32, E'), 8 warps x 4 rows.
+__global__ void __launch_bounds__(256) k_lift_gemv(const int8_t* __restrict__ B, const int8_t* __restrict__ R,
+                                                   int64_t n, int64_t ld, const LiftConst* __restrict__ K,
+                                                   int8_t* __restrict__ V) {
+  const int e = blockIdx.y;
+  const int j = K->pidx[e];
+  const ModQ m = K->mq[e];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row0 = (int64_t)blockIdx.x * 32 + warp * 4;
+  const int8_t* Bj = B + (int64_t)j * n * ld;
+  const int4* Re = reinterpret_cast<const int4*>(R + (int64_t)e * ld);
+  const int64_t chunks = ld / 16;
+  int32_t acc[4] = {0, 0, 0, 0};
+  const int4* rows[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    int64_t i = row0 + u < n ? row0 + u : n - 1;  // clamp; result discarded
+    rows[u] = reinterpret_cast<const int4*>(Bj + i * ld);
+  }
+  for (int64_t k = lane; k < chunks; k += 32) {
+    int4 rv = __ldg(Re + k);
+    int4 bv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) bv[u] = __ldg(rows[u] + k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc[u] = __dp4a(bv[u].x, rv.x, acc[u]);
+      acc[u] = __dp4a(bv[u].y, rv.y, acc[u]);
+      acc[u] = __dp4a(bv[u].z, rv.z, acc[u]);
+      acc[u] = __dp4a(bv[u].w, rv.w, acc[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+  if (lane < 4) {
+    int64_t i = row0 + lane;
+    int32_t a = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+    if (i < n) V[(int64_t)e * n + i] = (int8_t)reduce_bal(a, m);
+  }
+}
+
+// general c: V[e][i*c + col] = bal(sum_k B_j[i][k] R_e[col][k]).
+// CTA tile 64 rows x 64 columns, K in chunks of 64 bytes, dp4a.
+__global__ void __launch_bounds__(256) k_lift_gemm(const int8_t* __restrict__ B, const int8_t* __restrict__ R,
+                                                   int64_t n, int64_t c, int64_t ld,
+                                                   const LiftConst* __restrict__ K, int8_t* __restrict__ V) {
+  const int e = blockIdx.z;
+  const int j = K->pidx[e];
+  const ModQ m = K->mq[e];
+  const int64_t row0 = (int64_t)blockIdx.y * 64, col0 = (int64_t)blockIdx.x * 64;
+  const int8_t* Bj = B + (int64_t)j * n * ld;
+  const int8_t* Re = R + (int64_t)e * c * ld;
+  __shared__ int32_t As[64][17];
+  __shared__ int32_t Bs[64][17];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  int32_t acc[4][4] = {};
+  for (int64_t k0 = 0; k0 < ld; k0 += 64) {
+    {
+      int r = tid >> 2, cch = tid & 3;
+      int64_t i = row0 + r, kk = k0 + 16 * cch;
+      int4 v = make_int4(0, 0, 0, 0);
+      if (i < n && kk < ld) v = *reinterpret_cast<const int4*>(Bj + i * ld + kk);
+      As[r][cch * 4 + 0] = v.x;
+      As[r][cch * 4 + 1] = v.y;
+      As[r][cch * 4 + 2] = v.z;
+      As[r][cch * 4 + 3] = v.w;
+      int64_t col = col0 + r;
+      int4 u = make_int4(0, 0, 0, 0);
+      if (col < c && kk < ld) u = *reinterpret_cast<const int4*>(Re + col * ld + kk);
+      Bs[r][cch * 4 + 0] = u.x;
+      Bs[r][cch * 4 + 1] = u.y;
+      Bs[r][cch * 4 + 2] = u.z;
+      Bs[r][cch * 4 + 3] = u.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 16; ++w) {
+      int32_t a[4], bb[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = As[ty * 4 + r][w];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) bb[u] = Bs[tx + 16 * u][w];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[r][u] = __dp4a(a[r], bb[u], acc[r][u]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    int64_t i = row0 + ty * 4 + r;
+    if (i >= n) continue;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      int64_t col = col0 + tx + 16 * u;
+      if (col < c) V[(int64_t)e * n * c + i * c + col] = (int8_t)reduce_bal(acc[r][u], m);
+    }
+  }
+}
+
+// Balanced CRT of one entry: x = sum_e c_e (P'/q_e) - t P', c_e = v_e w_e mod q_e,
+// t = floor(sum_e c_e / q_e) estimated in 2^-50 fixed point (exact or one too
+// small), one conditional subtraction of P', then the balanced shift.
+__global__ void __launch_bounds__(128) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
+                                                  const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
+                                                  uint64_t* __restrict__ xl) {
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= nc) return;
+  const int E = K->E;
+  uint64_t acc[kCrtWords];
+#pragma unroll
+  for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
+  uint64_t tf = 0;
+  for (int e = 0; e < E; ++e) {
+    const ModQ m = K->mq[e];
+    int32_t v = V[(int64_t)e * nc + t];
+    uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
+    uint32_t ce = barrett(vu * K->w[e], m);
+    tf += (uint64_t)ce * K->tfix[e];
+#pragma unroll
+    for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+  }
+  uint32_t S[kCrtWords];
+  uint64_t carry = 0;
+#pragma unroll
+  for (int l = 0; l < kCrtWords; ++l) {
+    uint64_t s = acc[l] + carry;
+    S[l] = (uint32_t)s;
+    carry = s >> 32;
+  }
+  // x = S - tq P'
+  const uint32_t tq = (uint32_t)(tf >> 50);
+  uint64_t mc = 0;
+  int64_t borrow = 0;
+#pragma unroll
+  for (int l = 0; l < kCrtWords; ++l) {
+    uint64_t prod = (uint64_t)tq * K->P[l] + mc;
+    mc = prod >> 32;
+    int64_t d = (int64_t)S[l] - (int64_t)(uint32_t)prod + borrow;
+    S[l] = (uint32_t)d;
+    borrow = d >> 32;  // 0 or -1
+  }
+  // if S >= P' subtract once
+  bool ge = true;
+#pragma unroll
+  for (int l = kCrtWords - 1; l >= 0; --l) {
+    // lexicographic compare from the top, branch-free
+    if (S[l] != K->P[l]) {
+      ge = S[l] > K->P[l];
+      break;
+    }
+  }
+  if (ge) {
+    borrow = 0;
+#pragma unroll
+    for (int l = 0; l < kCrtWords; ++l) {
+      int64_t d = (int64_t)S[l] - (int64_t)K->P[l] + borrow;
+      S[l] = (uint32_t)d;
+      borrow = d >> 32;
+    }
+  }
+  // balanced: if S > (P'-1)/2 then S -= P' (mod 2^384)
+  bool gt = false;
+#pragma unroll
+  for (int l = kCrtWords - 1; l >= 0; --l) {
+    if (S[l] != K->Phalf[l]) {
+      gt = S[l] > K->Phalf[l];
+      break;
+    }
+  }
+  if (gt) {
+    borrow = 0;
+#pragma unroll
+    for (int l = 0; l < kCrtWords; ++l) {
+      int64_t d = (int64_t)S[l] - (int64_t)K->P[l] + borrow;
+      S[l] = (uint32_t)d;
+      borrow = d >> 32;
+    }
+  }
+  uint64_t* out = D + t * kDigitLimbs;
+#pragma unroll
+  for (int l = 0; l < kDigitLimbs; ++l) out[l] = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
+  xl[t] = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+}
+
+template <typename AT>
+__device__ __forceinline__ uint64_t mac64(uint64_t acc, AT a, uint64_t x) {
+  return acc + (uint64_t)(int64_t)a * x;
+}
+
+// c == 1: r'[i] = (r[i] - sum_k A[i][k] xl[k]) Pinv mod 2^64 and its residues.  Warp per row.
+template <typename AT>
+__global__ void __launch_bounds__(256) k_lift_resid_gemv(const AT* __restrict__ A, const uint64_t* __restrict__ xl,
+                                                         const int64_t* __restrict__ r, int64_t n, int64_t ld,
+                                                         const LiftConst* __restrict__ K,
+                                                         int64_t* __restrict__ rn, int8_t* __restrict__ R) {
+  const int lane = threadIdx.x & 31;
+  const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= n) return;
+  const AT* Ai = A + i * n;
+  uint64_t s = 0;
+  for (int64_t k = lane; k < n; k += 32) s = mac64(s, Ai[k], __ldg(xl + k));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const int64_t v = (int64_t)(((uint64_t)r[i] - s) * K->Pinv64);
+  if (lane == 0) rn[i] = v;
+  const int E = K->E;
+  for (int e = lane; e < E; e += 32) R[(int64_t)e * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+}
+
+// general c: tile 32 rows x 32 columns; thread (tx = row, ty = 4 columns).
+template <typename AT>
+__global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ A, const uint64_t* __restrict__ xl,
+                                                         const int64_t* __restrict__ r, int64_t n, int64_t c,
+                                                         int64_t ld, const LiftConst* __restrict__ K,
+                                                         int64_t* __restrict__ rn, int8_t* __restrict__ R) {
+  __shared__ int64_t As[32][33];
+  __shared__ uint64_t Xs[32][33];
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int64_t row0 = (int64_t)blockIdx.y * 32, col0 = (int64_t)blockIdx.x * 32;
+  uint64_t acc[4] = {0, 0, 0, 0};
+  for (int64_t k0 = 0; k0 < n; k0 += 32) {
+    for (int idx = tid; idx < 32 * 32; idx += 256) {
+      int rr = idx >> 5, kk = idx & 31;
+      int64_t i = row0 + rr, k = k0 + kk;
+      As[rr][kk] = (i < n && k < n) ? (int64_t)A[i * n + k] : 0;
+      int64_t col = col0 + kk;  // reuse: Xs[k][col]
+      int64_t kr = k0 + rr;
+      Xs[rr][kk] = (kr < n && col < c) ? xl[kr * c + col] : 0;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      int64_t a = As[tx][kk];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[u] += (uint64_t)a * Xs[kk][ty * 4 + u];
+    }
+    __syncthreads();
+  }
+  const int64_t i = row0 + tx;
+  if (i >= n) return;
+  const int E = K->E;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    int64_t col = col0 + ty * 4 + u;
+    if (col >= c) continue;
+    int64_t v = (int64_t)(((uint64_t)r[i * c + col] - acc[u]) * K->Pinv64);
+    rn[i * c + col] = v;
+    for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+  }
+}
+
+__global__ void k_narrow_a(const int64_t* __restrict__ A, int64_t count, int32_t* __restrict__ A32) {
+  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < count) A32[t] = (int32_t)A[t];
+}
+
+// ------------------------------------------------------------ driver
+namespace {
+struct LiftLayout {
+  size_t K, R, V, r, xl, A32, total;
+};
+LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
+  int64_t ld = padded_ld(n);
+  Layout L;
+  LiftLayout o;
+  o.K = L.add(sizeof(LiftConst));
+  o.R = L.add((size_t)E * c * ld);
+  o.V = L.add((size_t)E * n * c);
+  o.r = L.add((size_t)2 * n * c * 8);
+  o.xl = L.add((size_t)n * c * 8);
+  o.A32 = a32 ? L.add((size_t)n * n * 4) : 0;
+  o.total = L.total;
+  return o;
+}
+}  // namespace
+
+size_t lift_scratch_bytes(int64_t n, int64_t c, int E, bool a32) { return lift_layout(n, c, E, a32).total; }
+
+es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
+                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                   void* stream, KernelTiming* kt) {
+  cudaStream_t st = (cudaStream_t)stream;
+  LiftConst hK;
+  build_lift_const(good_host, &hK);
+  if (hK.E == 0) return ES_ERR_ARG;
+  const int E = hK.E;
+  const int64_t ld = padded_ld(n), nc = n * c;
+  LiftLayout L = lift_layout(n, c, E, a32);
+  LiftConst* K = reinterpret_cast<LiftConst*>(scratch + L.K);
+  int8_t* R = reinterpret_cast<int8_t*>(scratch + L.R);
+  int8_t* V = reinterpret_cast<int8_t*>(scratch + L.V);
+  int64_t* r[2] = {reinterpret_cast<int64_t*>(scratch + L.r), reinterpret_cast<int64_t*>(scratch + L.r) + nc};
+  uint64_t* xl = reinterpret_cast<uint64_t*>(scratch + L.xl);
+  int32_t* A32 = a32 ? reinterpret_cast<int32_t*>(scratch + L.A32) : nullptr;
+
+  // LiftConst lives in pageable host memory on this thread's stack: copy it
+  // synchronously with respect to the host before returning.
+  ES_CHECK(cuda_status(cudaMemcpyAsync(K, &hK, sizeof(hK), cudaMemcpyHostToDevice, st), "lift const H2D"));
+  ES_CHECK(cuda_status(cudaMemsetAsync(R, 0, (size_t)E * c * ld, st), "memset R"));
+  if (a32) {
+    k_narrow_a<<<(unsigned)((n * n + 255) / 256), 256, 0, st>>>(A_dev, n * n, A32);
+    ES_CHECK(cuda_status(cudaGetLastError(), "k_narrow_a"));
+  }
+  k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R);
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_init"));
+  count_launch(a32 ? 2 : 1);
+  std::vector<cudaEvent_t> ev;
+  if (kt && kt->events) {
+    ev.resize(2 * (size_t)m);
+    for (auto& e : ev) ES_CHECK(cuda_status(cudaEventCreate(&e), "event create"));
+  }
+  for (int32_t i = 0; i < m; ++i) {
+    if (!ev.empty()) cudaEventRecord(ev[2 * i], st);
+    if (c == 1)
+      k_lift_gemv<<<dim3((unsigned)((n + 31) / 32), E), 256, 0, st>>>(B_dev, R, n, ld, K, V);
+    else
+      k_lift_gemm<<<dim3((unsigned)((c + 63) / 64), (unsigned)((n + 63) / 64), E), 256, 0, st>>>(B_dev, R, n, c,
+                                                                                                ld, K, V);
+    if (!ev.empty()) cudaEventRecord(ev[2 * i + 1], st);
+    count_launch(2);
+    k_lift_crt<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
+                                                              xl);
+    if (i + 1 < m) {
+      count_launch(1);
+      const int64_t* rc = r[i & 1];
+      int64_t* rn = r[(i + 1) & 1];
+      if (c == 1) {
+        if (a32)
+          k_lift_resid_gemv<int32_t><<<(unsigned)((n + 7) / 8), 256, 0, st>>>(A32, xl, rc, n, ld, K, rn, R);
+        else
+          k_lift_resid_gemv<int64_t><<<(unsigned)((n + 7) / 8), 256, 0, st>>>(A_dev, xl, rc, n, ld, K, rn, R);
+      } else {
+        dim3 g((unsigned)((c + 31) / 32), (unsigned)((n + 31) / 32));
+        if (a32)
+          k_lift_resid_gemm<int32_t><<<g, 256, 0, st>>>(A32, xl, rc, n, c, ld, K, rn, R);
+        else
+          k_lift_resid_gemm<int64_t><<<g, 256, 0, st>>>(A_dev, xl, rc, n, c, ld, K, rn, R);
+      }
+    }
+  }
+  ES_CHECK(cuda_status(cudaGetLastError(), "lift steps"));
+  es_status sst = cuda_status(cudaStreamSynchronize(st), "lift sync");
+  if (kt) {
+    kt->launches += m;
+    kt->bytes_per_launch = (double)E * ((double)n * (double)n + 2.0 * (double)n * (double)c);
+    for (int32_t i = 0; i < (int32_t)ev.size() / 2; ++i) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]) == cudaSuccess) kt->ms += ms;
+    }
+  }
+  for (auto& e : ev) cudaEventDestroy(e);
+  return sst;
+}
+
+}  // namespace es

@@ -1,0 +1,268 @@
+// Final rational reconstruction on the host.
+//
+// exact-solve card, §Method: "the final rational reconstruction (common
+// denominator from a small sample of components, then one modular multiply
+// per numerator; this CPU stage uses gmpy2 and a process pool when
+// available)".  Here: the library's own limb arithmetic (bigint.h) and a
+// pool of host threads.
+//
+// From the digits x_0 .. x_{m-1} (balanced, base P') of every component:
+//   u_k = sum_i x_{i,k} P'^i mod M,  M = P'^m > 2 Nb Db  (Nb = 2^num_bits, Db = 2^den_bits)
+//   d   = lcm of the denominators of a few sampled components, each found by
+//         Wang's rational reconstruction (extended Euclid on (M, u_k) stopped
+//         at the first remainder <= Nb);
+//   N_k = bal(d u_k mod M), accepted when |N_k| <= Nb.
+// Acceptance certifies d x_k integral: N_k v = d u (mod M) with both sides
+// below M/2 in absolute value forces v | d u, i.e. v = 1.  A component that
+// fails has a denominator not dividing d: it is reconstructed, d grows to the
+// lcm, and the pass repeats.  The final d is the least common denominator
+// (it divides the true one and makes every d x_k integral), so the result is
+// the canonical (N, d) whatever the sample.
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <climits>
+#include <new>
+#include <cstring>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+#include "bigint.h"
+#include "es_common.cuh"
+#include "es_internal.h"
+
+namespace es {
+
+using big::Nat;
+
+namespace {
+
+struct Ctx {
+  const uint64_t* digits;
+  int64_t nc;
+  int32_t m;
+  Nat P, half, M, Mhalf, Mhalf1;  // Mhalf = (M-1)/2, Mhalf1 = (M+1)/2
+  uint64_t P6[kDigitLimbs];       // P' in 6 limbs
+  uint64_t half6[kDigitLimbs];    // (P'-1)/2 in 6 limbs
+  int plen;
+};
+
+// u_k = (sum_i x_i P'^i) mod M in [0, M), by Horner on the shifted digits
+// x_i + (P'-1)/2 in [0, P'-1] and one final offset by (M-1)/2.
+Nat assemble(const Ctx& c, int64_t k) {
+  Nat X;
+  for (int32_t i = c.m - 1; i >= 0; --i) {
+    const uint64_t* dg = c.digits + ((size_t)i * (size_t)c.nc + (size_t)k) * kDigitLimbs;
+    uint64_t xp[kDigitLimbs];
+    unsigned __int128 carry = 0;
+    for (int l = 0; l < kDigitLimbs; ++l) {
+      unsigned __int128 s = (unsigned __int128)dg[l] + c.half6[l] + carry;
+      xp[l] = (uint64_t)s;
+      carry = s >> 64;
+    }
+    int alen = kDigitLimbs;
+    while (alen && xp[alen - 1] == 0) --alen;
+    big::mul_small_add_in(X, c.P6, c.plen, xp, alen);
+  }
+  if (big::cmp(X, c.Mhalf) >= 0)
+    big::sub_in(X, c.Mhalf);
+  else
+    big::add_in(X, c.Mhalf1);
+  return X;
+}
+
+template <typename F>
+void parallel_for(int64_t count, int threads, F&& fn) {
+  if (count <= 0) return;
+  int T = threads > 0 ? threads : (int)std::thread::hardware_concurrency();
+  if (T < 1) T = 1;
+  if ((int64_t)T > count) T = (int)count;
+  std::atomic<int64_t> next(0);
+  auto worker = [&]() {
+    for (;;) {
+      int64_t k = next.fetch_add(1);
+      if (k >= count) break;
+      fn(k);
+    }
+  };
+  if (T == 1) {
+    worker();
+    return;
+  }
+  std::vector<std::thread> pool;
+  for (int t = 0; t < T; ++t) pool.emplace_back(worker);
+  for (auto& th : pool) th.join();
+}
+
+void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
+  for (int64_t l = 0; l < W; ++l) out[l] = l < (int64_t)mag.size() ? mag[(size_t)l] : 0;
+  if (neg) {
+    unsigned __int128 carry = 1;
+    for (int64_t l = 0; l < W; ++l) {
+      unsigned __int128 s = (unsigned __int128)(~out[l]) + carry;
+      out[l] = (uint64_t)s;
+      carry = s >> 64;
+    }
+  }
+}
+
+}  // namespace
+
+es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,
+                      int64_t num_bits, int64_t den_bits, int threads, bool inject_fault, Solution* out) {
+  if (inject_fault) return ES_ERR_INTERNAL;
+  if (!digits || n < 1 || c < 1 || m < 1 || !good || num_bits < 0 || den_bits < 0) return ES_ERR_ARG;
+  Ctx ctx;
+  ctx.digits = digits;
+  ctx.nc = n * c;
+  ctx.m = m;
+  ctx.P = big::from_u64(1);
+  int E = 0;
+  for (int j = 0; j < kNumPrimes; ++j)
+    if (good[j]) {
+      ctx.P = big::mul_small(ctx.P, kPrimes[j]);
+      ++E;
+    }
+  if (E == 0) return ES_ERR_ARG;
+  ctx.half = big::shr(big::sub(ctx.P, big::from_u64(1)), 1);
+  std::memset(ctx.P6, 0, sizeof(ctx.P6));
+  std::memset(ctx.half6, 0, sizeof(ctx.half6));
+  for (size_t l = 0; l < ctx.P.size(); ++l) ctx.P6[l] = ctx.P[l];
+  for (size_t l = 0; l < ctx.half.size(); ++l) ctx.half6[l] = ctx.half[l];
+  ctx.plen = (int)ctx.P.size();
+  // M = P'^m by binary powering
+  Nat M = big::from_u64(1), base = ctx.P;
+  for (int32_t e = m; e; e >>= 1) {
+    if (e & 1) M = big::mul(M, base);
+    if (e > 1) base = big::mul(base, base);
+  }
+  ctx.M = M;
+  // Wang's uniqueness condition M > 2 Nb Db = 2^(num_bits + den_bits + 1)
+  if (big::le_pow2(M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
+  ctx.Mhalf = big::shr(big::sub(M, big::from_u64(1)), 1);
+  ctx.Mhalf1 = big::add(ctx.Mhalf, big::from_u64(1));
+  const int64_t nc = ctx.nc;
+
+  // common denominator from a sample of components
+  const int64_t ns = nc < 4 ? nc : 4;
+  std::vector<Nat> sden((size_t)ns);
+  std::atomic<int> fail(0);
+  parallel_for(ns, threads, [&](int64_t t) {
+    Nat u = assemble(ctx, (t * nc) / ns), num, den;
+    bool neg;
+    if (!big::rational_reconstruct(ctx.M, u, (size_t)num_bits, &num, &neg, &den) ||
+        !big::le_pow2(den, (size_t)den_bits))
+      fail = 1;
+    sden[(size_t)t] = den;
+  });
+  if (fail) return ES_ERR_INTERNAL;
+  Nat d = big::from_u64(1);
+  auto lcm_in = [&](const Nat& v) {
+    if (big::cmp(d, v) == 0 || v.size() == 0) return;
+    Nat g = big::gcd(d, v), q;
+    big::divmod(v, g, &q, nullptr);
+    d = big::mul(d, q);
+  };
+  for (auto& v : sden) lcm_in(v);
+
+  const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
+  const int64_t W = W0 > W1 ? W0 : W1;
+  out->n = n;
+  out->c = c;
+  out->limbs = W;
+  out->num.assign((size_t)(nc * W), 0);
+  for (int round = 0;; ++round) {
+    if (round > 64) return ES_ERR_INTERNAL;
+    std::mutex mu;
+    std::vector<int64_t> failed;
+    parallel_for(nc, threads, [&](int64_t k) {
+      Nat u = assemble(ctx, k);
+      Nat prod = big::mul(d, u), rem;
+      big::divmod(prod, ctx.M, nullptr, &rem);
+      bool neg = big::cmp(rem, ctx.Mhalf) > 0;
+      Nat mag = neg ? big::sub(ctx.M, rem) : rem;
+      if (!big::le_pow2(mag, (size_t)num_bits)) {
+        std::lock_guard<std::mutex> lk(mu);
+        failed.push_back(k);
+        return;
+      }
+      to_limbs(mag, neg, W, out->num.data() + (size_t)k * (size_t)W);
+    });
+    if (failed.empty()) break;
+    std::sort(failed.begin(), failed.end());
+    if (failed.size() > 4) failed.resize(4);
+    for (int64_t k : failed) {
+      Nat u = assemble(ctx, k), num, den;
+      bool neg;
+      if (!big::rational_reconstruct(ctx.M, u, (size_t)num_bits, &num, &neg, &den) ||
+          !big::le_pow2(den, (size_t)den_bits))
+        return ES_ERR_INTERNAL;
+      Nat before = d;
+      lcm_in(den);
+      if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;  // no progress: digits inconsistent
+    }
+  }
+  if (!big::le_pow2(d, (size_t)den_bits)) return ES_ERR_INTERNAL;
+  out->den.assign((size_t)W, 0);
+  to_limbs(d, false, W, out->den.data());
+  out->primes_used = E;
+  out->m = m;
+  return ES_OK;
+}
+
+}  // namespace es
+
+extern "C" es_status es_reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,
+                                    int64_t num_bits, int64_t den_bits, const es_options* opt, es_solution** out) {
+  if (!out) return ES_ERR_ARG;
+  *out = nullptr;
+  es_solution* s = new (std::nothrow) es_solution;
+  if (!s) return ES_ERR_NOMEM;
+  auto t0 = std::chrono::steady_clock::now();
+  es_status st = es::reconstruct(digits, n, c, m, good, num_bits, den_bits, opt ? opt->threads : 0,
+                                 opt && opt->fault_stage == ES_FAULT_RECON, &s->s);
+  if (st != ES_OK) {
+    delete s;
+    return st;
+  }
+  s->s.ms[4] = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  s->s.ms[5] = s->s.ms[4];
+  *out = s;
+  return ES_OK;
+}
+
+extern "C" int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples) {
+  if (lo > hi || lo < INT32_MIN || hi > (int64_t)INT32_MAX - 255 || samples < 0) return -1;
+  int64_t bad = 0;
+  for (int j = 0; j < es::kNumPrimes; ++j) {
+    const es::ModQ mq = es::make_modq(es::kPrimes[j]);
+    const int64_t q = es::kPrimes[j], h = (q - 1) / 2;
+    for (int64_t x = lo; x < hi; ++x) {
+      int64_t r = x % q;
+      if (r > h) r -= q;
+      if (r < -h) r += q;
+      if (es::reduce_bal((int32_t)x, mq) != r) ++bad;
+    }
+    uint64_t s = 0x9E3779B97F4A7C15ull ^ (uint64_t)j;
+    for (int64_t t = 0; t < samples; ++t) {
+      s ^= s << 13;
+      s ^= s >> 7;
+      s ^= s << 17;
+      int64_t a = (int64_t)s;
+      if (t < 8) {  // edge values
+        const int64_t edges[8] = {INT64_MIN, INT64_MIN + 1, -1, 0, 1, INT64_MAX, INT64_MAX - 1, -q};
+        a = edges[t];
+      }
+      __int128 r = (__int128)a % q;
+      if (r > h) r -= q;
+      if (r < -h) r += q;
+      if (es::reduce_i64_bal(a, mq) != (int32_t)r) ++bad;
+      if (a % q != 0) {
+        uint32_t au = es::mod_i64(a, mq);
+        if (es::barrett(au * es::inv_mod(au, mq), mq) != 1) ++bad;
+      }
+    }
+  }
+  return bad;
+}
