@@ -192,16 +192,18 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     if (failed.empty()) break;
     std::sort(failed.begin(), failed.end());
     if (failed.size() > 4) failed.resize(4);
+    // Every failing component's denominator does not divide d, so the round's
+    // lcm must grow d (a later one may already be covered by an earlier one).
+    const Nat before = d;
     for (int64_t k : failed) {
       Nat u = assemble(ctx, k), num, den;
       bool neg;
       if (!big::rational_reconstruct(ctx.M, u, (size_t)num_bits, &num, &neg, &den) ||
           !big::le_pow2(den, (size_t)den_bits))
         return ES_ERR_INTERNAL;
-      Nat before = d;
       lcm_in(den);
-      if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;  // no progress: digits inconsistent
     }
+    if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;  // no progress: digits inconsistent
   }
   if (!big::le_pow2(d, (size_t)den_bits)) return ES_ERR_INTERNAL;
   out->den.assign((size_t)W, 0);

@@ -58,8 +58,8 @@ int current_device() {
 
 es_status grow_device(void** p, size_t* have, size_t need, size_t cap_left, bool inject) {
   if (inject) return ES_ERR_NOMEM;
+  if (cap_left && need > cap_left) return ES_ERR_NOMEM;  // the cap applies to what this call needs
   if (need <= *have) return ES_OK;
-  if (cap_left && need > cap_left) return ES_ERR_NOMEM;
   if (*p) cudaFree(*p);
   *p = nullptr;
   *have = 0;

@@ -51,7 +51,7 @@ def model_digits(A, b, m=None):
     return digits, good, nb, db, m
 
 
-@pytest.mark.parametrize("case", ["n5c2", "pascal30", "n24_24bit", "hilbert6", "planted"])
+@pytest.mark.parametrize("case", ["n5c2", "pascal30", "n24_24bit", "hilbert6", "hilbert12", "n33c5", "planted"])
 def test_host_reconstruction_matches_oracle(lib, case):
     if case == "n5c2":
         A, b = inputs.uniform(5, 2, -50, 51, seed=1)
@@ -59,9 +59,13 @@ def test_host_reconstruction_matches_oracle(lib, case):
         A, b = inputs.pascal_system(30, 1, seed=0)
     elif case == "n24_24bit":
         A, b = inputs.uniform(24, 1, -(1 << 23), 1 << 23, seed=2)
-    elif case == "hilbert6":
-        A = inputs.scaled_hilbert(6)
-        b = np.arange(-3, 3, dtype=np.int64).reshape(6, 1)
+    elif case.startswith("hilbert"):
+        # sampled denominators miss factors that two failing components share
+        k = int(case[7:])
+        A = inputs.scaled_hilbert(k)
+        b = np.arange(1, k + 1, dtype=np.int64).reshape(k, 1)
+    elif case == "n33c5":
+        A, b = inputs.uniform(33, 5, -(1 << 23), 1 << 23, seed=33)
     else:
         A, b, _ = inputs.planted(10, 3, seed=4)
     A, b = A.tolist(), b.tolist()
