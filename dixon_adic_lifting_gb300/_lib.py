@@ -49,6 +49,7 @@ _SIGS = {
     "es_version": (c_i32, []),
     "es_residues_device": (c_i32, [c_vp, c_i64, c_vp, c_vp]),
     "es_inverse_mod_device": (c_i32, [c_vp, c_i64, c_vp, c_vp, c_vp]),
+    "es_inverse_mod_device_noalloc": (c_i32, [c_vp, c_i64, c_vp, c_vp, c_vp]),
     "es_plan_device": (c_i32, [c_vp, c_vp, c_i64, c_i64, c_vp, P_i64, P_i64, P_i32, c_vp]),
     "es_lift_device": (c_i32, [c_vp, c_vp, c_i64, c_i64, c_vp, c_vp, c_i32, c_vp, c_vp]),
     "es_reconstruct": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i64, c_i64, ctypes.POINTER(es_options),

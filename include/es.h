@@ -153,6 +153,27 @@ es_status es_residues_device(const int64_t* A_dev, int64_t count, int8_t* out_de
 es_status es_inverse_mod_device(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev,
                                 void* stream);
 
+/* Batched modular inverse that allocates nothing (the card has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- code inside a framework whose caching allocator already
+ * holds nearly all of it, or latency-bound loops that must not pay the
+ * device-wide synchronisation of cudaFree).  Same arguments, layout and
+ * result as es_inverse_mod_device for n <= 256; its working memory is a
+ * fixed 4.25 MiB array in device memory that every GPU loading the library
+ * holds until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine and creates no stream (NULL = the legacy default
+ * stream).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and should come before
+ * any stream capture.  All calls share the array, which keeps the previous
+ * call's contents (everything that must start at zero is cleared); calls
+ * are serialised on the host and synchronous, and device work that
+ * overlapped them on another stream through this array would race.
+ * Unlike es_inverse_mod_device it accepts any int64 entries (residues are
+ * exact for all of them).  n > 256 -> ES_ERR_RANGE with the reason in
+ * es_last_error(). */
+es_status es_inverse_mod_device_noalloc(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev,
+                                        void* stream);
+
 /* Lift plan (card §Method stop rule): bit bounds and step count that the
  * solve uses.  num_bits / den_bits: Nb = 2^num_bits >= N_H and
  * Db = 2^den_bits >= D_H with D_H = prod_i ||a_i||_2 and
