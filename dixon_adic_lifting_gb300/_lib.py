@@ -28,11 +28,12 @@ NUM_PRIMES = 53
 DIGIT_LIMBS = 6
 NUM_PHASES = 6
 FAULT = {"residues": 1, "inverse": 2, "lift": 3, "recon": 4, "nomem": 5}
+FLAG_HOST_RECON = 1
 
 
 class es_options(ctypes.Structure):
     _fields_ = [("stream", c_vp), ("max_device_bytes", ctypes.c_size_t), ("fault_stage", c_i32),
-                ("threads", c_i32), ("timing", c_i32), ("reserved", c_i32)]
+                ("threads", c_i32), ("timing", c_i32), ("flags", c_i32)]
 
 
 _SIGS = {

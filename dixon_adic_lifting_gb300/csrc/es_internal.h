@@ -50,6 +50,7 @@ inline int64_t padded_ld(int64_t n) { return (n + 15) / 16 * 16; }
 // Device statistics of A and b used by the range check and the bounds.
 struct Stats {
   uint64_t max_abs_a;   // max |A_ij| (|-2^63| = 2^63 as uint64)
+  uint64_t max_abs_b;   // max |b_ij|
   int zero_row;         // some row of A is zero
   double log2_d;        // sum_i 0.5 log2 ||a_i||^2
   double log2_n;        // sum_i 0.5 log2 (||a_i||^2 + max_k b_ik^2)
@@ -102,6 +103,15 @@ struct Solution {
   int64_t launches = 0;
   KernelTiming top;
 };
+
+// Reconstruction with the numerator pass on the GPU (k_recon.cu): applicable
+// when the low-digit certificate needs m' <= m digits.  digits on the device.
+bool recon_device_applicable(int64_t n, int32_t m, const uint8_t* good, int64_t num_bits, int64_t den_bits,
+                             const Stats& stats, int32_t* mp_out);
+size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t num_bits, int64_t den_bits);
+es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_t m, int32_t mp,
+                             const uint8_t* good, int64_t num_bits, int64_t den_bits, const Stats& stats,
+                             int threads, char* scratch, size_t scratch_bytes, void* stream, struct Solution* out);
 
 // Host reconstruction (recon.cpp).  digits [m][n*c][6].
 es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,

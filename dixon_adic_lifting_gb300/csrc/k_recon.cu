@@ -1,0 +1,407 @@
+// Rational reconstruction with the numerator pass on the GPU.
+//
+// exact-solve card, §Method: the final reconstruction takes a common
+// denominator from a small sample of components, then one modular multiply
+// per numerator.  The sample's rational reconstruction (extended Euclid,
+// inherently sequential) stays on the host; the per-numerator pass, which is
+// the bulk of the work and independent per component, runs here.
+//
+// Low-digit certificate.  With Q = P'^m' and X_lo = sum_{i<m'} x_i P'^i the
+// lift guarantees A X_lo = b (mod Q) exactly (b = A sum_{i<m'} x_i P'^i +
+// P'^m' r_m').  For a candidate d (lcm of sampled denominators, so d | the
+// least common denominator and d <= Db) let N_k = bal_Q(d X_lo,k).  If every
+// |N_k| <= Nb then A N = d b (mod Q) and |A N - d b| <= n max|A| Nb +
+// Db max|b| < Q/2, hence A N = d b exactly: N / d is the solution and d is the
+// least common denominator.  So only m' digits are read, with
+// Q > 2 (n max|A| 2^num_bits + 2^den_bits max|b|) -- about half of m.
+//
+// Per component k (one CTA): with G_i = d P'^i mod Q (host-precomputed) and
+// the shifted digits x'_i = x_i + (P'-1)/2 in [0, P'-1],
+//   Z = sum_i x'_i G_i + (Q - H),  H = ((P'-1)/2) sum_i G_i mod Q,
+// so Z = d X_lo (mod Q) with 0 <= Z < (m' P' + 1) Q.  Z is formed as 32-bit
+// word column sums (64-bit accumulators plus carry counts), normalised, and
+// reduced mod Q by Barrett's method with a 13-word reciprocal; then the sign
+// is balanced and |N| <= 2^num_bits is tested.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "bigint.h"
+#include "es_common.cuh"
+#include "es_internal.h"
+#include "recon_common.h"
+
+namespace es {
+
+using big::Nat;
+
+namespace {
+constexpr int kMuWords = 13;  // Barrett reciprocal floor(b^(LG-1+13) / Q), b = 2^32
+constexpr int kZExtra = 12;   // Z < b^(LG + 11)
+constexpr int kDigitWords = 2 * kDigitLimbs;
+
+struct RParams {
+  const uint32_t* D;      // digits as 32-bit words: [m][nc][12]
+  int64_t nc;
+  int mp;                 // digits used (m')
+  int LG;                 // 32-bit words of Q
+  const uint32_t* G;      // [mp][LG]  G_i = d P'^i mod Q
+  const uint32_t* OFF;    // [LG]      Q - H
+  const uint32_t* Q;      // [LG]
+  const uint32_t* Qhalf;  // [LG]      (Q - 1) / 2
+  const uint32_t* MU;     // [13]
+  const uint32_t* H12;    // [12]      (P' - 1) / 2
+  int64_t nb;             // accept |N| <= 2^nb
+  int W;                  // output 64-bit limbs per numerator
+  uint64_t* N;            // [nc][W] two's complement
+  uint8_t* ok;            // [nc]
+};
+
+__device__ __forceinline__ void mac(uint64_t& lo, uint32_t& hi, uint32_t a, uint32_t b) {
+  uint64_t p = (uint64_t)a * b;
+  lo += p;
+  hi += (lo < p) ? 1u : 0u;
+}
+
+__global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
+  const int64_t k = blockIdx.x;
+  const int mp = p.mp, LG = p.LG, LZ = LG + kZExtra;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  extern __shared__ __align__(16) unsigned char sm[];
+  uint64_t* Zlo = reinterpret_cast<uint64_t*>(sm);          // LZ + 1
+  uint32_t* Zhi = reinterpret_cast<uint32_t*>(Zlo + LZ + 1);  // LZ + 1
+  uint32_t* Zn = Zhi + LZ + 1;                              // LZ + 1
+  uint32_t* xs = Zn + LZ + 1;                               // mp * 12
+  __shared__ uint32_t qh[kMuWords];
+  __shared__ int s_ok, s_neg, s_z;
+
+  // shifted digits x'_i = x_i + (P'-1)/2  (384-bit two's complement add)
+  for (int i = tid; i < mp; i += nt) {
+    const uint32_t* src = p.D + ((size_t)i * (size_t)p.nc + (size_t)k) * kDigitWords;
+    uint64_t carry = 0;
+#pragma unroll
+    for (int l = 0; l < kDigitWords; ++l) {
+      uint64_t s = (uint64_t)src[l] + p.H12[l] + carry;
+      xs[i * kDigitWords + l] = (uint32_t)s;
+      carry = s >> 32;
+    }
+  }
+  __syncthreads();
+  // Z word columns: Z[w] = OFF[w] + sum_i sum_l x'_i[l] G_i[w - l]
+  for (int w = tid; w < LZ; w += nt) {
+    uint64_t lo = w < LG ? p.OFF[w] : 0;
+    uint32_t hi = 0;
+    const int lmin = w - LG + 1 > 0 ? w - LG + 1 : 0;
+    const int lmax = w < kDigitWords - 1 ? w : kDigitWords - 1;
+    for (int i = 0; i < mp; ++i) {
+      const uint32_t* Gi = p.G + (size_t)i * LG + w;
+      const uint32_t* xi = xs + i * kDigitWords;
+      if (lmin == 0 && lmax == kDigitWords - 1) {
+#pragma unroll
+        for (int l = 0; l < kDigitWords; ++l) mac(lo, hi, xi[l], __ldg(Gi - l));
+      } else {
+        for (int l = lmin; l <= lmax; ++l) mac(lo, hi, xi[l], __ldg(Gi - l));
+      }
+    }
+    Zlo[w] = lo;
+    Zhi[w] = hi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // normalise the columns into 32-bit words
+    uint64_t carry = 0;
+    for (int w = 0; w < LZ; ++w) {
+      unsigned __int128 s = (unsigned __int128)Zlo[w] + ((unsigned __int128)Zhi[w] << 64) + carry;
+      Zn[w] = (uint32_t)s;
+      carry = (uint64_t)(s >> 32);
+    }
+    // q^ = floor(Z1 MU / b^13) with Z1 = floor(Z / b^(LG-1)) (13 words)
+    uint32_t prod[2 * kMuWords];
+    for (int t = 0; t < 2 * kMuWords; ++t) prod[t] = 0;
+    for (int a = 0; a < kMuWords; ++a) {
+      uint64_t c = 0;
+      const uint64_t za = Zn[LG - 1 + a];
+      for (int b = 0; b < kMuWords; ++b) {
+        uint64_t t = za * p.MU[b] + prod[a + b] + c;
+        prod[a + b] = (uint32_t)t;
+        c = t >> 32;
+      }
+      prod[a + kMuWords] = (uint32_t)c;
+    }
+    for (int t = 0; t < kMuWords; ++t) qh[t] = prod[kMuWords + t];
+  }
+  __syncthreads();
+  // q^ Q, words 0 .. LG (enough: the remainder is below 3Q < b^(LG+1))
+  for (int w = tid; w <= LG; w += nt) {
+    uint64_t lo = 0;
+    uint32_t hi = 0;
+    for (int j = 0; j < kMuWords; ++j) {
+      const int t = w - j;
+      if (t >= 0 && t < LG) mac(lo, hi, qh[j], p.Q[t]);
+    }
+    Zlo[w] = lo;
+    Zhi[w] = hi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // r = Z - q^ Q  (mod b^(LG+1))
+    uint64_t carry = 0;
+    int64_t borrow = 0;
+    for (int w = 0; w <= LG; ++w) {
+      unsigned __int128 s = (unsigned __int128)Zlo[w] + ((unsigned __int128)Zhi[w] << 64) + carry;
+      const uint32_t qq = (uint32_t)s;
+      carry = (uint64_t)(s >> 32);
+      const int64_t d = (int64_t)Zn[w] - (int64_t)qq + borrow;
+      Zn[w] = (uint32_t)d;
+      borrow = d >> 32;
+    }
+    // at most two subtractions of Q
+    for (int rep = 0; rep < 3; ++rep) {
+      bool ge = Zn[LG] != 0;
+      if (!ge) {
+        ge = true;
+        for (int w = LG - 1; w >= 0; --w)
+          if (Zn[w] != p.Q[w]) {
+            ge = Zn[w] > p.Q[w];
+            break;
+          }
+      }
+      if (!ge) break;
+      borrow = 0;
+      for (int w = 0; w <= LG; ++w) {
+        const int64_t d = (int64_t)Zn[w] - (int64_t)(w < LG ? p.Q[w] : 0u) + borrow;
+        Zn[w] = (uint32_t)d;
+        borrow = d >> 32;
+      }
+    }
+    // balanced: r > (Q-1)/2 -> N = r - Q, magnitude Q - r
+    bool neg = false;
+    for (int w = LG - 1; w >= 0; --w)
+      if (Zn[w] != p.Qhalf[w]) {
+        neg = Zn[w] > p.Qhalf[w];
+        break;
+      }
+    if (neg) {
+      borrow = 0;
+      for (int w = 0; w < LG; ++w) {
+        const int64_t d = (int64_t)p.Q[w] - (int64_t)Zn[w] + borrow;
+        Zn[w] = (uint32_t)d;
+        borrow = d >> 32;
+      }
+    }
+    Zn[LG] = 0;
+    // |N| <= 2^nb ?
+    int top = LG - 1;
+    while (top >= 0 && Zn[top] == 0) --top;
+    bool ok = true;
+    if (top >= 0) {
+      const int64_t bl = 32 * (int64_t)top + (32 - __clz(Zn[top]));
+      if (bl > p.nb + 1) {
+        ok = false;
+      } else if (bl == p.nb + 1) {  // equal to 2^nb only
+        ok = Zn[top] == (1u << (p.nb % 32));
+        for (int w = 0; ok && w < top; ++w) ok = Zn[w] == 0;
+      }
+    }
+    int z = 0;
+    while (z < LG && Zn[z] == 0) ++z;
+    s_ok = ok ? 1 : 0;
+    s_neg = neg ? 1 : 0;
+    s_z = z;
+  }
+  __syncthreads();
+  // two's complement output: -mag = ~mag + 1 (words below the lowest nonzero stay 0)
+  const int neg = s_neg, z = s_z;
+  uint64_t* out = p.N + (size_t)k * p.W;
+  for (int t = tid; t < p.W; t += nt) {
+    uint32_t wv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int w = 2 * t + h;
+      const uint32_t m = w < LG ? Zn[w] : 0u;
+      wv[h] = !neg ? m : (w < z ? 0u : (w == z ? (uint32_t)(0u - m) : ~m));
+    }
+    out[t] = (uint64_t)wv[0] | ((uint64_t)wv[1] << 32);
+  }
+  if (tid == 0) p.ok[k] = (uint8_t)s_ok;
+}
+
+// little-endian 32-bit words of a natural, zero-extended to `words`
+void to_words(const Nat& a, int64_t words, uint32_t* out) {
+  for (int64_t w = 0; w < words; ++w) {
+    const size_t limb = (size_t)(w / 2);
+    const uint64_t v = limb < a.size() ? a[limb] : 0;
+    out[w] = (uint32_t)(w % 2 ? v >> 32 : v);
+  }
+}
+
+int64_t u64_bitlen(uint64_t v) { return v ? 64 - __builtin_clzll(v) : 0; }
+
+}  // namespace
+
+bool recon_device_applicable(int64_t n, int32_t m, const uint8_t* good, int64_t num_bits, int64_t den_bits,
+                             const Stats& stats, int32_t* mp_out) {
+  // Q = P'^m' > 2 (n max|A| 2^num_bits + 2^den_bits max|b|): it suffices that
+  // Q > 2^(max(num_bits + bitlen(n max|A|), den_bits + bitlen(max|b|)) + 2)
+  const int64_t na = u64_bitlen((uint64_t)n * stats.max_abs_a);  // n max|A| < 2^63
+  const int64_t need = std::max(num_bits + na, den_bits + u64_bitlen(stats.max_abs_b)) + 2;
+  double log2P = 0.0;
+  for (int j = 0; j < kNumPrimes; ++j)
+    if (good[j]) log2P += std::log2((double)kPrimes[j]);
+  int32_t mp = (int32_t)((double)need / log2P) + 2;  // checked exactly on the host later
+  if (mp > m) return false;
+  *mp_out = mp;
+  return true;
+}
+
+size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t num_bits, int64_t den_bits) {
+  double log2P = 0.0;
+  for (int j = 0; j < kNumPrimes; ++j)
+    if (good[j]) log2P += std::log2((double)kPrimes[j]);
+  const int64_t LG = (int64_t)(mp * log2P / 32.0) + 2;
+  const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
+  const int64_t W = W0 > W1 ? W0 : W1;
+  Layout L;
+  L.add((size_t)mp * LG * 4);
+  L.add((size_t)LG * 4 * 3);
+  L.add(kMuWords * 4 + kDigitWords * 4);
+  L.add((size_t)nc * W * 8);
+  L.add((size_t)nc);
+  return L.total;
+}
+
+es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_t m, int32_t mp,
+                             const uint8_t* good, int64_t num_bits, int64_t den_bits, const Stats& stats,
+                             int threads, char* scratch, size_t scratch_bytes, void* stream, Solution* out) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t nc = n * c;
+  const PrimeSet ps = make_prime_set(good);
+  if (ps.E == 0) return ES_ERR_ARG;
+  const Nat M = pow_nat(ps.P, m);
+  if (big::le_pow2(M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
+  const Nat Mhalf = big::shr(big::sub(M, big::from_u64(1)), 1);
+  const Nat Mhalf1 = big::add(Mhalf, big::from_u64(1));
+  // exact check of the low-digit certificate's modulus
+  const Nat Q = pow_nat(ps.P, mp);
+  {
+    const int64_t na = u64_bitlen((uint64_t)n * stats.max_abs_a);
+    const int64_t need = std::max(num_bits + na, den_bits + u64_bitlen(stats.max_abs_b)) + 2;
+    if (big::le_pow2(Q, (size_t)need)) return ES_ERR_INTERNAL;
+  }
+  // one component's full digits -> its residue mod M (for the denominators)
+  std::vector<uint64_t> hd((size_t)m * kDigitLimbs);
+  auto residue = [&](int64_t k, Nat* u) -> es_status {
+    ES_CHECK(cuda_status(cudaMemcpy2DAsync(hd.data(), kDigitLimbs * 8, D_dev + (size_t)k * kDigitLimbs,
+                                           (size_t)nc * kDigitLimbs * 8, kDigitLimbs * 8, (size_t)m,
+                                           cudaMemcpyDeviceToHost, st),
+                         "sample digits D2H"));
+    ES_CHECK(cuda_status(cudaStreamSynchronize(st), "sample digits sync"));
+    *u = shifted_to_residue(assemble_shifted(ps, hd.data(), kDigitLimbs, m), Mhalf, Mhalf1);
+    return ES_OK;
+  };
+  const int64_t ns = nc < 4 ? nc : 4;
+  std::vector<Nat> su((size_t)ns), sden((size_t)ns);
+  for (int64_t t = 0; t < ns; ++t) ES_CHECK(residue((t * nc) / ns, &su[(size_t)t]));
+  std::atomic<int> fail(0);
+  parallel_for(ns, threads, [&](int64_t t) {
+    if (!component_denominator(M, su[(size_t)t], num_bits, den_bits, &sden[(size_t)t])) fail = 1;
+  });
+  if (fail) return ES_ERR_INTERNAL;
+  Nat d = big::from_u64(1);
+  for (auto& v : sden) lcm_in(d, v);
+
+  // device constants that do not depend on d
+  const int64_t LG = (int64_t)((big::bitlen(Q) + 31) / 32);
+  const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
+  const int64_t W = W0 > W1 ? W0 : W1;
+  Layout L;
+  const size_t oG = L.add((size_t)mp * LG * 4), oC = L.add((size_t)LG * 4 * 3),
+               oM = L.add(kMuWords * 4 + kDigitWords * 4), oN = L.add((size_t)nc * W * 8), oK = L.add((size_t)nc);
+  if (L.total > scratch_bytes) return ES_ERR_INTERNAL;
+  std::vector<uint32_t> hC((size_t)LG * 3), hM(kMuWords + kDigitWords);
+  const Nat Qhalf = big::shr(big::sub(Q, big::from_u64(1)), 1);
+  to_words(Q, LG, hC.data() + LG);
+  to_words(Qhalf, LG, hC.data() + 2 * LG);
+  Nat mu;
+  big::divmod(big::shl(big::from_u64(1), (size_t)(32 * (LG - 1 + kMuWords))), Q, &mu, nullptr);
+  if ((int64_t)((big::bitlen(mu) + 31) / 32) > kMuWords) return ES_ERR_INTERNAL;
+  to_words(mu, kMuWords, hM.data());
+  to_words(ps.half, kDigitWords, hM.data() + kMuWords);
+  ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oM, hM.data(), hM.size() * 4, cudaMemcpyHostToDevice, st),
+                       "recon constants H2D"));
+  const int dyn = (int)((3 * (LG + kZExtra + 1)) * 4 + (LG + kZExtra + 1) * 4 + (size_t)mp * kDigitWords * 4);
+  if (dyn > 48 * 1024)
+    ES_CHECK(cuda_status(cudaFuncSetAttribute(k_recon_numerators, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
+                         "recon smem attribute"));
+  out->n = n;
+  out->c = c;
+  out->limbs = W;
+  out->num.assign((size_t)(nc * W), 0);
+  std::vector<uint8_t> okh((size_t)nc);
+  std::vector<uint32_t> hG((size_t)mp * LG);
+  for (int round = 0;; ++round) {
+    if (round > 64) return ES_ERR_INTERNAL;
+    // G_i = d P'^i mod Q, OFF = Q - ((P'-1)/2 sum_i G_i mod Q)
+    Nat g, sum, rem;
+    big::divmod(d, Q, nullptr, &g);
+    for (int32_t i = 0; i < mp; ++i) {
+      to_words(g, LG, hG.data() + (size_t)i * LG);
+      big::add_in(sum, g);
+      if (i + 1 < mp) {
+        Nat t = big::mul(g, ps.P);
+        big::divmod(t, Q, nullptr, &g);
+      }
+    }
+    big::divmod(big::mul(sum, ps.half), Q, nullptr, &rem);
+    const Nat off = rem.empty() ? Nat{} : big::sub(Q, rem);
+    to_words(off, LG, hC.data());
+    ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oG, hG.data(), hG.size() * 4, cudaMemcpyHostToDevice, st),
+                         "recon G H2D"));
+    ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oC, hC.data(), hC.size() * 4, cudaMemcpyHostToDevice, st),
+                         "recon Q H2D"));
+    RParams rp;
+    rp.D = reinterpret_cast<const uint32_t*>(D_dev);
+    rp.nc = nc;
+    rp.mp = mp;
+    rp.LG = (int)LG;
+    rp.G = reinterpret_cast<const uint32_t*>(scratch + oG);
+    rp.OFF = reinterpret_cast<const uint32_t*>(scratch + oC);
+    rp.Q = rp.OFF + LG;
+    rp.Qhalf = rp.OFF + 2 * LG;
+    rp.MU = reinterpret_cast<const uint32_t*>(scratch + oM);
+    rp.H12 = rp.MU + kMuWords;
+    rp.nb = num_bits;
+    rp.W = (int)W;
+    rp.N = reinterpret_cast<uint64_t*>(scratch + oN);
+    rp.ok = reinterpret_cast<uint8_t*>(scratch + oK);
+    k_recon_numerators<<<(unsigned)nc, 256, dyn, st>>>(rp);
+    count_launch();
+    ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_numerators"));
+    ES_CHECK(cuda_status(cudaMemcpyAsync(okh.data(), rp.ok, (size_t)nc, cudaMemcpyDeviceToHost, st), "ok D2H"));
+    ES_CHECK(cuda_status(cudaMemcpyAsync(out->num.data(), rp.N, (size_t)nc * W * 8, cudaMemcpyDeviceToHost, st),
+                         "numerators D2H"));
+    ES_CHECK(cuda_status(cudaStreamSynchronize(st), "recon sync"));
+    std::vector<int64_t> failed;
+    for (int64_t k = 0; k < nc && failed.size() < 4; ++k)
+      if (!okh[(size_t)k]) failed.push_back(k);
+    if (failed.empty()) break;
+    const Nat before = d;
+    for (int64_t k : failed) {
+      Nat u, den;
+      ES_CHECK(residue(k, &u));
+      if (!component_denominator(M, u, num_bits, den_bits, &den)) return ES_ERR_INTERNAL;
+      lcm_in(d, den);
+    }
+    if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;
+  }
+  if (!big::le_pow2(d, (size_t)den_bits)) return ES_ERR_INTERNAL;
+  out->den.assign((size_t)W, 0);
+  to_limbs(d, false, W, out->den.data());
+  out->primes_used = ps.E;
+  out->m = m;
+  return ES_OK;
+}
+
+}  // namespace es

@@ -71,6 +71,7 @@ struct RowStat {
   double sumsq;     // ||a_i||^2 (rounded; relative error <= n 2^-53)
   double bmax2;     // max_k b_ik^2
   uint64_t maxabs;  // max_k |A_ik|
+  uint64_t bmaxabs; // max_k |b_ik|
 };
 
 __device__ __forceinline__ uint64_t uabs64(int64_t v) {
@@ -84,7 +85,7 @@ __global__ void k_row_stats(const int64_t* __restrict__ A, const int64_t* __rest
   int lane = threadIdx.x % 32;
   if (row >= n) return;
   double s = 0.0, bm = 0.0;
-  uint64_t mx = 0;
+  uint64_t mx = 0, bmx = 0;
   for (int64_t k = lane; k < n; k += 32) {
     int64_t v = A[row * n + k];
     double d = (double)v;
@@ -93,16 +94,21 @@ __global__ void k_row_stats(const int64_t* __restrict__ A, const int64_t* __rest
     mx = u > mx ? u : mx;
   }
   for (int64_t k = lane; k < c; k += 32) {
-    double d = (double)b[row * c + k];
+    int64_t v = b[row * c + k];
+    double d = (double)v;
     bm = fmax(bm, d * d);
+    uint64_t u = uabs64(v);
+    bmx = u > bmx ? u : bmx;
   }
   for (int o = 16; o; o >>= 1) {
     s += __shfl_xor_sync(0xffffffffu, s, o);
     bm = fmax(bm, __shfl_xor_sync(0xffffffffu, bm, o));
     uint64_t om = __shfl_xor_sync(0xffffffffu, mx, o);
     mx = om > mx ? om : mx;
+    uint64_t ob = __shfl_xor_sync(0xffffffffu, bmx, o);
+    bmx = ob > bmx ? ob : bmx;
   }
-  if (lane == 0) out[row] = RowStat{s, bm, mx};
+  if (lane == 0) out[row] = RowStat{s, bm, mx, bmx};
 }
 
 size_t stats_scratch_bytes(int64_t n) { return (size_t)n * sizeof(RowStat); }
@@ -126,10 +132,11 @@ es_status compute_stats(const int64_t* A_dev, const int64_t* b_dev, int64_t n, i
                                        (cudaStream_t)stream),
                        "stats D2H"));
   ES_CHECK(cuda_status(cudaStreamSynchronize((cudaStream_t)stream), "stats sync"));
-  Stats s{0, 0, 0.0, 0.0};
+  Stats s{0, 0, 0, 0.0, 0.0};
   for (int64_t i = 0; i < n; ++i) {
     const RowStat& r = h[(size_t)i];
     s.max_abs_a = r.maxabs > s.max_abs_a ? r.maxabs : s.max_abs_a;
+    s.max_abs_b = r.bmaxabs > s.max_abs_b ? r.bmaxabs : s.max_abs_b;
     if (r.sumsq == 0.0) {
       s.zero_row = 1;
       continue;

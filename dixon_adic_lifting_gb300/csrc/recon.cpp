@@ -31,68 +31,75 @@
 #include "bigint.h"
 #include "es_common.cuh"
 #include "es_internal.h"
+#include "recon_common.h"
 
 namespace es {
 
 using big::Nat;
 
-namespace {
+PrimeSet make_prime_set(const uint8_t* good) {
+  PrimeSet ps;
+  ps.P = big::from_u64(1);
+  for (int j = 0; j < kNumPrimes; ++j)
+    if (good[j]) {
+      ps.P = big::mul_small(ps.P, kPrimes[j]);
+      ++ps.E;
+    }
+  ps.half = big::shr(big::sub(ps.P, big::from_u64(1)), 1);
+  std::memset(ps.P6, 0, sizeof(ps.P6));
+  std::memset(ps.half6, 0, sizeof(ps.half6));
+  for (size_t l = 0; l < ps.P.size() && l < (size_t)kDigitLimbs; ++l) ps.P6[l] = ps.P[l];
+  for (size_t l = 0; l < ps.half.size() && l < (size_t)kDigitLimbs; ++l) ps.half6[l] = ps.half[l];
+  ps.plen = (int)ps.P.size();
+  return ps;
+}
 
-struct Ctx {
-  const uint64_t* digits;
-  int64_t nc;
-  int32_t m;
-  Nat P, half, M, Mhalf, Mhalf1;  // Mhalf = (M-1)/2, Mhalf1 = (M+1)/2
-  uint64_t P6[kDigitLimbs];       // P' in 6 limbs
-  uint64_t half6[kDigitLimbs];    // (P'-1)/2 in 6 limbs
-  int plen;
-};
+Nat pow_nat(const Nat& b, int64_t e) {
+  Nat r = big::from_u64(1), base = b;
+  for (; e; e >>= 1) {
+    if (e & 1) r = big::mul(r, base);
+    if (e > 1) base = big::mul(base, base);
+  }
+  return r;
+}
 
-// u_k = (sum_i x_i P'^i) mod M in [0, M), by Horner on the shifted digits
-// x_i + (P'-1)/2 in [0, P'-1] and one final offset by (M-1)/2.
-Nat assemble(const Ctx& c, int64_t k) {
+Nat assemble_shifted(const PrimeSet& ps, const uint64_t* base, size_t stride, int32_t m) {
   Nat X;
-  for (int32_t i = c.m - 1; i >= 0; --i) {
-    const uint64_t* dg = c.digits + ((size_t)i * (size_t)c.nc + (size_t)k) * kDigitLimbs;
+  for (int32_t i = m - 1; i >= 0; --i) {
+    const uint64_t* dg = base + (size_t)i * stride;
     uint64_t xp[kDigitLimbs];
     unsigned __int128 carry = 0;
     for (int l = 0; l < kDigitLimbs; ++l) {
-      unsigned __int128 s = (unsigned __int128)dg[l] + c.half6[l] + carry;
+      unsigned __int128 s = (unsigned __int128)dg[l] + ps.half6[l] + carry;
       xp[l] = (uint64_t)s;
       carry = s >> 64;
     }
     int alen = kDigitLimbs;
     while (alen && xp[alen - 1] == 0) --alen;
-    big::mul_small_add_in(X, c.P6, c.plen, xp, alen);
+    big::mul_small_add_in(X, ps.P6, ps.plen, xp, alen);
   }
-  if (big::cmp(X, c.Mhalf) >= 0)
-    big::sub_in(X, c.Mhalf);
-  else
-    big::add_in(X, c.Mhalf1);
   return X;
 }
 
-template <typename F>
-void parallel_for(int64_t count, int threads, F&& fn) {
-  if (count <= 0) return;
-  int T = threads > 0 ? threads : (int)std::thread::hardware_concurrency();
-  if (T < 1) T = 1;
-  if ((int64_t)T > count) T = (int)count;
-  std::atomic<int64_t> next(0);
-  auto worker = [&]() {
-    for (;;) {
-      int64_t k = next.fetch_add(1);
-      if (k >= count) break;
-      fn(k);
-    }
-  };
-  if (T == 1) {
-    worker();
-    return;
-  }
-  std::vector<std::thread> pool;
-  for (int t = 0; t < T; ++t) pool.emplace_back(worker);
-  for (auto& th : pool) th.join();
+Nat shifted_to_residue(Nat X, const Nat& Mhalf, const Nat& Mhalf1) {
+  if (big::cmp(X, Mhalf) >= 0)
+    big::sub_in(X, Mhalf);
+  else
+    big::add_in(X, Mhalf1);
+  return X;
+}
+
+void lcm_in(Nat& d, const Nat& v) {
+  if (big::cmp(d, v) == 0 || v.empty()) return;
+  Nat g = big::gcd(d, v), q;
+  big::divmod(v, g, &q, nullptr);
+  d = big::mul(d, q);
+}
+
+bool component_denominator(const Nat& M, const Nat& u, int64_t num_bits, int64_t den_bits, Nat* den) {
+  Nat num;
+  bool neg;
+  return big::rational_reconstruct(M, u, (size_t)num_bits, &num, &neg, den) && big::le_pow2(*den, (size_t)den_bits);
 }
 
 void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
@@ -107,64 +114,33 @@ void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
   }
 }
 
-}  // namespace
-
 es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,
                       int64_t num_bits, int64_t den_bits, int threads, bool inject_fault, Solution* out) {
   if (inject_fault) return ES_ERR_INTERNAL;
   if (!digits || n < 1 || c < 1 || m < 1 || !good || num_bits < 0 || den_bits < 0) return ES_ERR_ARG;
-  Ctx ctx;
-  ctx.digits = digits;
-  ctx.nc = n * c;
-  ctx.m = m;
-  ctx.P = big::from_u64(1);
-  int E = 0;
-  for (int j = 0; j < kNumPrimes; ++j)
-    if (good[j]) {
-      ctx.P = big::mul_small(ctx.P, kPrimes[j]);
-      ++E;
-    }
-  if (E == 0) return ES_ERR_ARG;
-  ctx.half = big::shr(big::sub(ctx.P, big::from_u64(1)), 1);
-  std::memset(ctx.P6, 0, sizeof(ctx.P6));
-  std::memset(ctx.half6, 0, sizeof(ctx.half6));
-  for (size_t l = 0; l < ctx.P.size(); ++l) ctx.P6[l] = ctx.P[l];
-  for (size_t l = 0; l < ctx.half.size(); ++l) ctx.half6[l] = ctx.half[l];
-  ctx.plen = (int)ctx.P.size();
-  // M = P'^m by binary powering
-  Nat M = big::from_u64(1), base = ctx.P;
-  for (int32_t e = m; e; e >>= 1) {
-    if (e & 1) M = big::mul(M, base);
-    if (e > 1) base = big::mul(base, base);
-  }
-  ctx.M = M;
+  const PrimeSet ps = make_prime_set(good);
+  if (ps.E == 0) return ES_ERR_ARG;
+  const int64_t nc = n * c;
+  const Nat M = pow_nat(ps.P, m);
   // Wang's uniqueness condition M > 2 Nb Db = 2^(num_bits + den_bits + 1)
   if (big::le_pow2(M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
-  ctx.Mhalf = big::shr(big::sub(M, big::from_u64(1)), 1);
-  ctx.Mhalf1 = big::add(ctx.Mhalf, big::from_u64(1));
-  const int64_t nc = ctx.nc;
+  const Nat Mhalf = big::shr(big::sub(M, big::from_u64(1)), 1);
+  const Nat Mhalf1 = big::add(Mhalf, big::from_u64(1));
+  auto residue = [&](int64_t k) {
+    return shifted_to_residue(assemble_shifted(ps, digits + (size_t)k * kDigitLimbs, (size_t)nc * kDigitLimbs, m),
+                              Mhalf, Mhalf1);
+  };
 
   // common denominator from a sample of components
   const int64_t ns = nc < 4 ? nc : 4;
   std::vector<Nat> sden((size_t)ns);
   std::atomic<int> fail(0);
   parallel_for(ns, threads, [&](int64_t t) {
-    Nat u = assemble(ctx, (t * nc) / ns), num, den;
-    bool neg;
-    if (!big::rational_reconstruct(ctx.M, u, (size_t)num_bits, &num, &neg, &den) ||
-        !big::le_pow2(den, (size_t)den_bits))
-      fail = 1;
-    sden[(size_t)t] = den;
+    if (!component_denominator(M, residue((t * nc) / ns), num_bits, den_bits, &sden[(size_t)t])) fail = 1;
   });
   if (fail) return ES_ERR_INTERNAL;
   Nat d = big::from_u64(1);
-  auto lcm_in = [&](const Nat& v) {
-    if (big::cmp(d, v) == 0 || v.size() == 0) return;
-    Nat g = big::gcd(d, v), q;
-    big::divmod(v, g, &q, nullptr);
-    d = big::mul(d, q);
-  };
-  for (auto& v : sden) lcm_in(v);
+  for (auto& v : sden) lcm_in(d, v);
 
   const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
   const int64_t W = W0 > W1 ? W0 : W1;
@@ -177,11 +153,10 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     std::mutex mu;
     std::vector<int64_t> failed;
     parallel_for(nc, threads, [&](int64_t k) {
-      Nat u = assemble(ctx, k);
-      Nat prod = big::mul(d, u), rem;
-      big::divmod(prod, ctx.M, nullptr, &rem);
-      bool neg = big::cmp(rem, ctx.Mhalf) > 0;
-      Nat mag = neg ? big::sub(ctx.M, rem) : rem;
+      Nat prod = big::mul(d, residue(k)), rem;
+      big::divmod(prod, M, nullptr, &rem);
+      bool neg = big::cmp(rem, Mhalf) > 0;
+      Nat mag = neg ? big::sub(M, rem) : rem;
       if (!big::le_pow2(mag, (size_t)num_bits)) {
         std::lock_guard<std::mutex> lk(mu);
         failed.push_back(k);
@@ -196,19 +171,16 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     // lcm must grow d (a later one may already be covered by an earlier one).
     const Nat before = d;
     for (int64_t k : failed) {
-      Nat u = assemble(ctx, k), num, den;
-      bool neg;
-      if (!big::rational_reconstruct(ctx.M, u, (size_t)num_bits, &num, &neg, &den) ||
-          !big::le_pow2(den, (size_t)den_bits))
-        return ES_ERR_INTERNAL;
-      lcm_in(den);
+      Nat den;
+      if (!component_denominator(M, residue(k), num_bits, den_bits, &den)) return ES_ERR_INTERNAL;
+      lcm_in(d, den);
     }
     if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;  // no progress: digits inconsistent
   }
   if (!big::le_pow2(d, (size_t)den_bits)) return ES_ERR_INTERNAL;
   out->den.assign((size_t)W, 0);
   to_limbs(d, false, W, out->den.data());
-  out->primes_used = E;
+  out->primes_used = ps.E;
   out->m = m;
   return ES_OK;
 }

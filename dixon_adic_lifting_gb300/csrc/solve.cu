@@ -45,6 +45,8 @@ struct DeviceState {
   size_t digits_size = 0;
   uint64_t* hdigits = nullptr;  // pinned host copy (grow-only)
   size_t hdigits_size = 0;
+  char* recon = nullptr;  // device reconstruction buffers (grow-only)
+  size_t recon_size = 0;
   cudaStream_t stream = nullptr;
   int sms = 0;
 };
@@ -110,6 +112,7 @@ struct Options {
   int threads = 0;
   bool timing = false;
   bool kernel_events = false;
+  bool host_recon = false;
 };
 Options read_options(const es_options* o) {
   Options r;
@@ -120,6 +123,7 @@ Options read_options(const es_options* o) {
     r.threads = o->threads;
     r.timing = o->timing != 0;
     r.kernel_events = o->timing >= 2;
+    r.host_recon = (o->flags & ES_FLAG_HOST_RECON) != 0;
   }
   return r;
 }
@@ -248,27 +252,47 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   kt.events = o.kernel_events;
   ES_CHECK(run_lift(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt));
   tm.mark(3);
-  // digits to host
-  if (dbytes > dev.hdigits_size) {
-    if (dev.hdigits) cudaFreeHost(dev.hdigits);
-    dev.hdigits = nullptr;
-    dev.hdigits_size = 0;
-    if (cudaMallocHost((void**)&dev.hdigits, dbytes) != cudaSuccess) {
-      cudaGetLastError();
-      dev.hdigits = nullptr;
-      return ES_ERR_NOMEM;
-    }
-    dev.hdigits_size = dbytes;
+  if (o.fault == ES_FAULT_RECON) {
+    set_last_error("injected fault: reconstruction");
+    return ES_ERR_INTERNAL;
   }
-  ES_CHECK(cuda_status(cudaMemcpyAsync(dev.hdigits, dev.digits, dbytes, cudaMemcpyDeviceToHost, st), "digits D2H"));
-  tm.mark(4);
-  ES_CHECK(cuda_status(cudaStreamSynchronize(st), "digits sync"));
-  // reconstruction
   es_solution* sol = new (std::nothrow) es_solution;
   if (!sol) return ES_ERR_NOMEM;
+  int32_t mp = 0;
+  const bool on_device = !o.host_recon && recon_device_applicable(n, m, good, num_bits, den_bits, stats, &mp);
+  es_status rs = ES_OK;
   auto t_rec = std::chrono::steady_clock::now();
-  es_status rs = reconstruct(dev.hdigits, n, c, m, good, num_bits, den_bits, o.threads,
-                             o.fault == ES_FAULT_RECON, &sol->s);
+  if (on_device) {
+    // numerators on the GPU from the low m' digits; sampled denominators on the host
+    tm.mark(4);
+    const size_t rbytes = recon_device_bytes(nc, mp, good, num_bits, den_bits);
+    void* p = dev.recon;
+    rs = grow_device(&p, &dev.recon_size, rbytes, 0, false);
+    dev.recon = (char*)p;
+    t_rec = std::chrono::steady_clock::now();
+    if (rs == ES_OK)
+      rs = reconstruct_device(dev.digits, n, c, m, mp, good, num_bits, den_bits, stats, o.threads, dev.recon,
+                              dev.recon_size, st, &sol->s);
+  } else {
+    // all digits to the host, reconstruction on the host
+    if (dbytes > dev.hdigits_size) {
+      if (dev.hdigits) cudaFreeHost(dev.hdigits);
+      dev.hdigits = nullptr;
+      dev.hdigits_size = 0;
+      if (cudaMallocHost((void**)&dev.hdigits, dbytes) != cudaSuccess) {
+        cudaGetLastError();
+        dev.hdigits = nullptr;
+        delete sol;
+        return ES_ERR_NOMEM;
+      }
+      dev.hdigits_size = dbytes;
+    }
+    rs = cuda_status(cudaMemcpyAsync(dev.hdigits, dev.digits, dbytes, cudaMemcpyDeviceToHost, st), "digits D2H");
+    tm.mark(4);
+    if (rs == ES_OK) rs = cuda_status(cudaStreamSynchronize(st), "digits sync");
+    t_rec = std::chrono::steady_clock::now();
+    if (rs == ES_OK) rs = reconstruct(dev.hdigits, n, c, m, good, num_bits, den_bits, o.threads, false, &sol->s);
+  }
   if (rs != ES_OK) {
     delete sol;
     return rs;
@@ -369,6 +393,9 @@ es_status es_release_workspace(void) {
   if (d.ws) cudaFree(d.ws);
   if (d.digits) cudaFree(d.digits);
   if (d.hdigits) cudaFreeHost(d.hdigits);
+  if (d.recon) cudaFree(d.recon);
+  d.recon = nullptr;
+  d.recon_size = 0;
   d.ws = nullptr;
   d.digits = nullptr;
   d.hdigits = nullptr;

@@ -63,8 +63,11 @@ typedef struct es_options {
   int32_t threads;         /* host threads for reconstruction; 0 = all hardware threads */
   int32_t timing;          /* 1: time each phase with CUDA events; 2: also time every launch
                               of the lift's per-prime product kernel (es_solution_kernels) */
-  int32_t reserved;
+  int32_t flags;           /* bit set of ES_FLAG_* */
 } es_options;
+
+/* es_options.flags */
+#define ES_FLAG_HOST_RECON 1 /* reconstruct on the host even when the GPU numerator pass applies */
 
 /* Fault injection points (es_options.fault_stage): the named stage returns
  * the given status without running; used to test error propagation. */
@@ -106,7 +109,9 @@ es_status es_solution_export(const es_solution* s, uint64_t* num, uint64_t* den)
 
 /* Phase times in ms (ms[ES_NUM_PHASES], any may be NULL):
  *   0 range check + bounds + residues, 1 modular inverse, 2 lift,
- *   3 digits device->host, 4 rational reconstruction (host), 5 total.
+ *   3 digits device->host (host reconstruction only), 4 rational
+ *   reconstruction (sampled denominators on the host + numerator pass on the
+ *   GPU, or all on the host), 5 total.
  * Phases 0-3 are filled only when es_options.timing was set; 4 and 5
  * always.  m = lift steps, primes_used = primes not dividing det A. */
 es_status es_solution_phase_ms(const es_solution* s, double* ms, int32_t* m, int32_t* primes_used);

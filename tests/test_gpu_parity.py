@@ -347,3 +347,27 @@ def test_device_memory_cap(torch_cuda):
     with pytest.raises(api.ExactSolveError) as e:
         api.solve_canonical(A, b, max_device_bytes=1 << 16)
     assert e.value.status == -4
+
+
+@pytest.mark.parametrize("case", ["n32", "hilbert12", "n33c5", "n64c3_int8", "diag7", "n256"])
+def test_device_reconstruction_matches_host_path(torch_cuda, case):
+    if case == "n32":
+        A, b = n32_case(1)
+    elif case == "hilbert12":  # sampled denominators incomplete: a second round is needed
+        A = inputs.scaled_hilbert(12)
+        b = np.arange(1, 13, dtype=np.int64).reshape(12, 1)
+    elif case == "n33c5":
+        A, b = inputs.uniform(33, 5, -(1 << 23), 1 << 23, seed=33)
+    elif case == "n64c3_int8":
+        A, b = inputs.uniform(64, 3, -127, 128, seed=65)
+    elif case == "diag7":  # component 7 alone carries the denominator 7
+        A = np.diag([1] * 7 + [7] + [1] * 8).astype(np.int64)
+        A[0, 1:] = 3
+        b = np.ones((16, 1), dtype=np.int64)
+    else:
+        A, b = inputs.workload("n256_c1_24bit", seed=0)
+    dev_s = api.solve_canonical(A, b)
+    host_s = api.solve_canonical(A, b, host_recon=True)
+    assert (dev_s.N, dev_s.d) == (host_s.N, host_s.d)
+    if A.shape[0] <= 64:
+        assert (dev_s.N, dev_s.d) == exact.solve(A.tolist(), b.tolist())
