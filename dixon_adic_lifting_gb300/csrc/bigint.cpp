@@ -310,36 +310,60 @@ static uint64_t bits_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^64
   return b ? (lo >> b) | (hi << (64 - b)) : lo;
 }
 
-// A x + B y for cofactors of opposite signs (or a zero one); the result is
-// known to be non-negative.
-static Nat comb(int64_t A, const Nat& x, int64_t B, const Nat& y) {
-  if (A >= 0 && B >= 0) {
-    Nat t = mul_small(x, (limb)A);
-    add_in(t, mul_small(y, (limb)B));
-    return t;
-  }
-  if (A >= 0) {
-    Nat t = mul_small(x, (limb)A);
-    sub_in(t, mul_small(y, (limb)(-B)));
-    return t;
-  }
-  Nat t = mul_small(y, (limb)B);
-  sub_in(t, mul_small(x, (limb)(-A)));
-  return t;
-}
-
 static inline limb uabs(int64_t v) { return v < 0 ? (limb)(-v) : (limb)v; }
 
+// out = pm P + qm Q (sub = false) or pm P - qm Q (sub = true, known >= 0),
+// one fused pass; out is resized to fit and trimmed.
+static void lin2(Nat& out, limb pm, const Nat& P, limb qm, const Nat& Q, bool sub) {
+  const size_t len = std::max(P.size(), Q.size());
+  out.resize(len + 1);
+  limb cp = 0, cq = 0, borrow = 0;
+  for (size_t i = 0; i < len; ++i) {
+    const u128 p = (u128)pm * (i < P.size() ? P[i] : 0) + cp;
+    const u128 q = (u128)qm * (i < Q.size() ? Q[i] : 0) + cq;
+    cp = (limb)(p >> 64);
+    cq = (limb)(q >> 64);
+    const limb pl = (limb)p, ql = (limb)q;
+    if (sub) {
+      const limb t1 = pl - ql, b1 = pl < ql;
+      const limb t2 = t1 - borrow, b2 = t1 < borrow;
+      out[i] = t2;
+      borrow = b1 | b2;
+    } else {
+      const u128 s = (u128)pl + ql + borrow;  // borrow doubles as the carry
+      out[i] = (limb)s;
+      borrow = (limb)(s >> 64);
+    }
+  }
+  out[len] = sub ? cp - cq - borrow : cp + cq + borrow;
+  trim(out);
+}
+
+// A x + B y for a Lehmer cofactor pair (never both negative when the result
+// is a remainder, i.e. non-negative).
+static void comb(Nat& out, int64_t A, const Nat& x, int64_t B, const Nat& y) {
+  if (A >= 0 && B >= 0)
+    lin2(out, (limb)A, x, (limb)B, y, false);
+  else if (A >= 0)
+    lin2(out, (limb)A, x, uabs(B), y, true);
+  else
+    lin2(out, (limb)B, y, uabs(A), x, true);
+}
+
 // Shared loop: r0 >= r1; stops when r1 <= 2^nbits (or r1 == 0 when nbits < 0).
+// Lehmer batches: up to ~60 quotient steps simulated on the leading 62 bits
+// (Knuth's Algorithm L test with two cofactor bounds), then applied to the
+// full numbers in fused passes.  Close to the stopping point a batch that
+// overshoots is undone and the rest runs one division step at a time.
 static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits) {
   auto done = [&](const Nat& x) { return nbits < 0 ? x.empty() : le_pow2(x, (size_t)nbits); };
   bool single_only = false;
   const size_t nb = nbits < 0 ? 0 : (size_t)nbits;
+  Nat n0, n1, m0, m1, s0, s1, sT0, sT1;
   while (!done(r1)) {
     size_t bl1 = bitlen(r1);
     if (!single_only && r1.size() >= 3 && bl1 > nb + 200) {
       const bool guard = bl1 < nb + 400;
-      Nat s0, s1, sT0, sT1;
       size_t ssteps = *steps;
       if (guard) {
         s0 = r0;
@@ -369,13 +393,13 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
         ++k;
       }
       if (B != 0) {
-        Nat n0 = comb(A, r0, B, r1), n1 = comb(C, r0, D, r1);
+        comb(n0, A, r0, B, r1);
+        comb(n1, C, r0, D, r1);
         r0.swap(n0);
         r1.swap(n1);
         if (T0) {
-          Nat m0 = mul_small(*T0, uabs(A)), m1 = mul_small(*T0, uabs(C));
-          add_in(m0, mul_small(*T1, uabs(B)));
-          add_in(m1, mul_small(*T1, uabs(D)));
+          lin2(m0, uabs(A), *T0, uabs(B), *T1, false);
+          lin2(m1, uabs(C), *T0, uabs(D), *T1, false);
           T0->swap(m0);
           T1->swap(m1);
         }

@@ -176,6 +176,148 @@ __global__ void __launch_bounds__(1024) k_gj_panel(GJParams p, int64_t k0, int k
   }
 }
 
+// Panel in registers (n <= blockDim = 1024): thread i holds row i's NBP panel
+// entries as int32 and applies each exchange step with one multiply-add per
+// entry, without reducing: the pivot column is reduced when it becomes the
+// pivot column (to find the pivot and the multipliers f, |f| <= 125) and the
+// pivot row when it is scaled, so every other entry grows by at most
+// |f p_t| <= 125^2 per step: below 125 + NBP 125^2 < 2^31.  Entries are
+// reduced once, when the panel is written back.  The step loop is not
+// unrolled (the register row is read and written through selects on the
+// step index) so its code stays resident in the instruction cache; the pivot
+// row is scaled by warp 0, one entry per lane, with inverses from a per-prime
+// table in shared memory.  Same result as k_gj_panel.
+template <int NBP>
+__device__ __forceinline__ int32_t sel(const int32_t (&v)[NBP], int a) {
+  int32_t r = 0;
+#pragma unroll
+  for (int t = 0; t < NBP; ++t) r = (t == a) ? v[t] : r;
+  return r;
+}
+
+template <int NBP>
+__global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0, int kb) {
+  const int j = blockIdx.x;
+  if (p.bad[j]) return;
+  const ModQ m = c_modq.v[j];
+  const int n = (int)p.n, ld = (int)p.ld;
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  __shared__ uint8_t s_inv[256];
+  __shared__ __align__(16) int s_wmin[32];
+  __shared__ __align__(16) int32_t s_raw[NBP];
+  __shared__ __align__(16) int32_t s_prow[NBP];
+  __shared__ int s_piv[NBP];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int row = tid;
+  const bool active = row < n;
+  for (int v = tid; v < (int)m.q; v += blockDim.x) s_inv[v] = v ? (uint8_t)inv_mod((uint32_t)v, m) : 0;
+  if (tid < 32) s_wmin[tid] = INT_MAX;
+  int32_t v[NBP];
+#pragma unroll
+  for (int c4 = 0; c4 < NBP / 16; ++c4) {
+    int4 w = make_int4(0, 0, 0, 0);
+    if (active && k0 + 16 * c4 < ld) w = *reinterpret_cast<const int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4);
+    const uint32_t ww[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[c4 * 16 + q4 * 4 + u] = sbyte(ww[q4], u);
+  }
+  bool used = active ? p.used[(int64_t)j * n + row] != 0 : true;
+  __syncthreads();
+#pragma unroll 1
+  for (int a = 0; a < kb; ++a) {
+    const int32_t f = reduce_bal(sel<NBP>(v, a), m);
+    int cand = (!used && f != 0) ? row : INT_MAX;
+    cand = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == 0) s_wmin[warp] = cand;
+    __syncthreads();  // (1) candidates of every warp
+    int pr = INT_MAX;
+#pragma unroll
+    for (int w4 = 0; w4 < 8; ++w4) {
+      const int4 c = *reinterpret_cast<const int4*>(s_wmin + 4 * w4);
+      pr = min(pr, min(min(c.x, c.y), min(c.z, c.w)));
+    }
+    if (pr == INT_MAX) {  // no pivot: q_j | det A
+      if (tid == 0) p.bad[j] = 1;
+      return;
+    }
+    if (row == pr) {
+#pragma unroll
+      for (int t = 0; t < NBP; ++t) s_raw[t] = (t == a) ? f : v[t];
+      used = true;
+      s_piv[a] = pr;
+      p.piv[(int64_t)j * n + k0 + a] = pr;
+    }
+    __syncthreads();  // (2) raw pivot row
+    if (warp == 0) {
+      const int32_t pf = s_raw[a];
+      const uint32_t inv = s_inv[pf < 0 ? pf + (int32_t)m.q : pf];
+      for (int t = lane; t < NBP; t += 32)
+        s_prow[t] = (t == a) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(s_raw[t], m) * (int32_t)inv, m);
+    }
+    __syncthreads();  // (3) scaled pivot row
+    if (row == pr) {
+#pragma unroll
+      for (int t4 = 0; t4 < NBP / 4; ++t4) {
+        const int4 pv = *reinterpret_cast<const int4*>(s_prow + 4 * t4);
+        v[4 * t4] = pv.x;
+        v[4 * t4 + 1] = pv.y;
+        v[4 * t4 + 2] = pv.z;
+        v[4 * t4 + 3] = pv.w;
+      }
+    } else if (f != 0) {
+      const int32_t fa = reduce_bal(-f * s_prow[a], m);
+#pragma unroll
+      for (int t4 = 0; t4 < NBP / 4; ++t4) {
+        const int4 pv = *reinterpret_cast<const int4*>(s_prow + 4 * t4);
+        const int32_t pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int t = 4 * t4 + u;
+          v[t] = (t == a) ? fa : v[t] - f * pp[u];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < NBP; ++t) v[t] = (t == a) ? 0 : v[t];
+    }
+  }
+  // reduce and write the panel back (padding columns stay zero: their pivot-row entries are zero)
+  if (active) {
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4) {
+      if (k0 + 16 * c4 >= ld) continue;
+      uint32_t ww[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          x |= ((uint32_t)(uint8_t)(int8_t)reduce_bal(v[c4 * 16 + q4 * 4 + u], m)) << (8 * u);
+        ww[q4] = x;
+      }
+      *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) = make_int4(ww[0], ww[1], ww[2], ww[3]);
+    }
+    p.used[(int64_t)j * n + row] = used ? 1 : 0;
+  }
+  __syncthreads();
+  // stage U^T (pivot rows outside the panel) and zero those entries in place
+  int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
+  for (int a = 0; a < NBP; ++a) {
+    const int pr = a < kb ? s_piv[a] : 0;
+    for (int col = tid; col < ld; col += blockDim.x) {
+      int8_t val = 0;
+      if (a < kb && (col < k0 || col >= k0 + kb)) {
+        const int64_t off = (int64_t)pr * ld + col;
+        val = Wj[off];
+        Wj[off] = 0;
+      }
+      UTj[(int64_t)col * NBP + a] = val;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ update
 // W[i][t] = bal(W[i][t] + sum_a F[i][a] U[a][t]) for all rows i and all
 // columns t outside the panel; CTA tile 64 rows x 128 columns, one prime.
@@ -243,6 +385,88 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
       *w = (int8_t)reduce_bal((int32_t)*w + acc[r][u], m);
     }
   }
+}
+
+// Update on the int8 tensor-core path (NB = 32): the depth-32 contraction
+// F U is exactly one mma.sync.m16n8k32 (s8 x s8 -> s32) per 16 x 8 output
+// tile.  F rows are contiguous in W and U is staged transposed, so both
+// fragments are 32-bit loads straight from memory: A (row-major 16 x 32) reg r
+// holds row g + 8 (r & 1), columns 4 t + 16 (r >> 1) + 0..3; B (column-major
+// 32 x 8) reg r holds column g, rows 4 t + 16 r + 0..3; C reg r holds row
+// g + 8 (r >> 1), column 2 t + (r & 1)  (g = lane / 4, t = lane % 4).
+// CTA tile 64 rows x 128 columns, 8 warps of 32 x 32.
+__device__ __forceinline__ void mma_s8_16x8x32(int32_t (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, int64_t k0, int kb) {
+  const int j = blockIdx.z;
+  if (p.bad[j]) return;
+  const ModQ m = c_modq.v[j];
+  const int64_t n = p.n, ld = p.ld;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+  const int64_t row0 = (int64_t)blockIdx.y * 64 + (warp >> 2) * 32;
+  const int64_t col0 = (int64_t)blockIdx.x * 128 + (warp & 3) * 32;
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  const int8_t* UTj = p.UT + (int64_t)j * ld * 32;
+  __shared__ int32_t Cs[8][32][33];  // per warp: its 32 x 32 tile of F U
+  // this thread's output row segment (row0 + lane, 32 columns), fetched early
+  const int64_t orow = row0 + lane;
+  // segments are 32-column aligned like the panel: one either is the panel or misses it
+  const bool rowok = orow < n && col0 < ld && col0 != k0;
+  int4 old0 = make_int4(0, 0, 0, 0), old1 = old0;
+  if (rowok) {
+    old0 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0);
+    if (col0 + 16 < ld) old1 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0 + 16);
+  }
+  uint32_t a[2][4], b[4][2];
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t row = row0 + 16 * mi + g + 8 * (r & 1);
+      const int64_t col = k0 + 4 * t + 16 * (r >> 1);
+      a[mi][r] = (row < n && col < ld) ? *reinterpret_cast<const uint32_t*>(Wj + row * ld + col) : 0u;
+    }
+#pragma unroll
+  for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int64_t col = col0 + 8 * ni + g;
+      b[ni][r] = col < ld ? *reinterpret_cast<const uint32_t*>(UTj + col * 32 + 4 * t + 16 * r) : 0u;
+    }
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni) {
+      int32_t c[4] = {0, 0, 0, 0};
+      mma_s8_16x8x32(c, a[mi], b[ni]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) Cs[warp][16 * mi + g + 8 * (r >> 1)][8 * ni + 2 * t + (r & 1)] = c[r];
+    }
+  __syncwarp();
+  if (!rowok) return;
+  uint32_t w[8] = {(uint32_t)old0.x, (uint32_t)old0.y, (uint32_t)old0.z, (uint32_t)old0.w,
+                   (uint32_t)old1.x, (uint32_t)old1.y, (uint32_t)old1.z, (uint32_t)old1.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int cc = 4 * q + u;
+      const int64_t col = col0 + cc;
+      int32_t val = sbyte(w[q], u);
+      if (col < n && (col < k0 || col >= k0 + kb)) val = reduce_bal(val + Cs[warp][lane][cc], m);
+      x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
+    }
+    w[q] = x;
+  }
+  *reinterpret_cast<int4*>(Wj + orow * ld + col0) = make_int4(w[0], w[1], w[2], w[3]);
+  if (col0 + 16 < ld) *reinterpret_cast<int4*>(Wj + orow * ld + col0 + 16) = make_int4(w[4], w[5], w[6], w[7]);
 }
 
 // ------------------------------------------------------------------ permute
@@ -313,10 +537,18 @@ es_status run_blocks(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) {
                                             (int)kPanelSmemLimit + 1024),
                        "panel smem attribute"));
   dim3 ugrid((unsigned)((gp.ld + 127) / 128), (unsigned)((n + 63) / 64), kNumPrimes);
+  const bool reg_panel = NBP == 32 && n <= 1024;  // one row per thread, panel in registers
+  const int reg_threads = (int)((n + 31) / 32 * 32);
   for (int64_t k0 = 0; k0 < n; k0 += NBP) {
     int kb = (int)((n - k0) < NBP ? (n - k0) : NBP);
-    k_gj_panel<NBP><<<kNumPrimes, 1024, smem, st>>>(gp, k0, kb, use_smem ? 1 : 0);
-    k_gj_update<NBP><<<ugrid, 256, 0, st>>>(gp, k0, kb);
+    if (reg_panel)
+      k_gj_panel_reg<NBP><<<kNumPrimes, reg_threads, 0, st>>>(gp, k0, kb);
+    else
+      k_gj_panel<NBP><<<kNumPrimes, 1024, smem, st>>>(gp, k0, kb, use_smem ? 1 : 0);
+    if (NBP == 32)
+      k_gj_update_mma<<<ugrid, 256, 0, st>>>(gp, k0, kb);
+    else
+      k_gj_update<NBP><<<ugrid, 256, 0, st>>>(gp, k0, kb);
     count_launch(2);
   }
   return cuda_status(cudaGetLastError(), "gauss-jordan blocks");

@@ -113,7 +113,11 @@ __global__ void k_lift_init(const int64_t* __restrict__ b, int64_t n, int64_t c,
   for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
 
-// c == 1: V[e][i] = bal(sum_k B_j[i][k] R_e[k]).  Grid (n/32, E'), 8 warps x 4 rows.
+// c == 1: V[e][i] = bal(sum_k B_j[i][k] R_e[k]).  Grid (n / (8 RPW), E'): each
+// of the 8 warps takes RPW rows and walks them in rounds of 64 16-byte chunks
+// (two per lane), issuing all of a round's loads before any dp4a so that
+// 2 (RPW + 1) 16-byte loads per lane are in flight.
+template <int RPW>
 __global__ void __launch_bounds__(256) k_lift_gemv(const int8_t* __restrict__ B, const int8_t* __restrict__ R,
                                                    int64_t n, int64_t ld, const LiftConst* __restrict__ K,
                                                    int8_t* __restrict__ V) {
@@ -121,38 +125,50 @@ __global__ void __launch_bounds__(256) k_lift_gemv(const int8_t* __restrict__ B,
   const int j = K->pidx[e];
   const ModQ m = K->mq[e];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t row0 = (int64_t)blockIdx.x * 32 + warp * 4;
-  const int8_t* Bj = B + (int64_t)j * n * ld;
+  const int64_t row0 = (int64_t)blockIdx.x * (8 * RPW) + warp * RPW;
+  const int4* Bj = reinterpret_cast<const int4*>(B + (int64_t)j * n * ld);
   const int4* Re = reinterpret_cast<const int4*>(R + (int64_t)e * ld);
   const int64_t chunks = ld / 16;
-  int32_t acc[4] = {0, 0, 0, 0};
-  const int4* rows[4];
+  int64_t roff[RPW];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    int64_t i = row0 + u < n ? row0 + u : n - 1;  // clamp; result discarded
-    rows[u] = reinterpret_cast<const int4*>(Bj + i * ld);
-  }
-  for (int64_t k = lane; k < chunks; k += 32) {
-    int4 rv = __ldg(Re + k);
-    int4 bv[4];
+  for (int u = 0; u < RPW; ++u) roff[u] = (row0 + u < n ? row0 + u : n - 1) * chunks;  // clamp; discarded
+  int32_t acc[RPW];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) bv[u] = __ldg(rows[u] + k);
+  for (int u = 0; u < RPW; ++u) acc[u] = 0;
+  for (int64_t k0 = 0; k0 < chunks; k0 += 64) {
+    const int64_t ka = k0 + lane, kb = k0 + 32 + lane;
+    const bool va = ka < chunks, vb = kb < chunks;
+    const int4 z = make_int4(0, 0, 0, 0);
+    const int4 ra = va ? __ldg(Re + ka) : z, rb = vb ? __ldg(Re + kb) : z;
+    int4 ba[RPW], bb[RPW];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc[u] = __dp4a(bv[u].x, rv.x, acc[u]);
-      acc[u] = __dp4a(bv[u].y, rv.y, acc[u]);
-      acc[u] = __dp4a(bv[u].z, rv.z, acc[u]);
-      acc[u] = __dp4a(bv[u].w, rv.w, acc[u]);
+    for (int u = 0; u < RPW; ++u) {
+      ba[u] = va ? __ldg(Bj + roff[u] + ka) : z;
+      bb[u] = vb ? __ldg(Bj + roff[u] + kb) : z;
+    }
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) {
+      acc[u] = __dp4a(ba[u].x, ra.x, acc[u]);
+      acc[u] = __dp4a(ba[u].y, ra.y, acc[u]);
+      acc[u] = __dp4a(ba[u].z, ra.z, acc[u]);
+      acc[u] = __dp4a(ba[u].w, ra.w, acc[u]);
+      acc[u] = __dp4a(bb[u].x, rb.x, acc[u]);
+      acc[u] = __dp4a(bb[u].y, rb.y, acc[u]);
+      acc[u] = __dp4a(bb[u].z, rb.z, acc[u]);
+      acc[u] = __dp4a(bb[u].w, rb.w, acc[u]);
     }
   }
+  int32_t mine = 0;
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < RPW; ++u) {
+    int32_t a = acc[u];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
-  if (lane < 4) {
-    int64_t i = row0 + lane;
-    int32_t a = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
-    if (i < n) V[(int64_t)e * n + i] = (int8_t)reduce_bal(a, m);
+    for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane == u) mine = a;
+  }
+  if (lane < RPW) {
+    const int64_t i = row0 + lane;
+    if (i < n) V[(int64_t)e * n + i] = (int8_t)reduce_bal(mine, m);
   }
 }
 
@@ -219,24 +235,38 @@ __global__ void __launch_bounds__(256) k_lift_gemm(const int8_t* __restrict__ B,
 // Balanced CRT of one entry: x = sum_e c_e (P'/q_e) - t P', c_e = v_e w_e mod q_e,
 // t = floor(sum_e c_e / q_e) estimated in 2^-50 fixed point (exact or one too
 // small), one conditional subtraction of P', then the balanced shift.
-__global__ void __launch_bounds__(128) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
+// One warp per entry: lane l takes primes l and l + 32, the 12 word sums and
+// the fixed-point sum are reduced across the warp, and every lane finishes the
+// (identical) digit; lanes 0..5 store its six limbs.
+__global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
                                                   const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
                                                   uint64_t* __restrict__ xl) {
-  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= nc) return;
   const int E = K->E;
   uint64_t acc[kCrtWords];
 #pragma unroll
   for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
   uint64_t tf = 0;
-  for (int e = 0; e < E; ++e) {
-    const ModQ m = K->mq[e];
-    int32_t v = V[(int64_t)e * nc + t];
-    uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
-    uint32_t ce = barrett(vu * K->w[e], m);
-    tf += (uint64_t)ce * K->tfix[e];
 #pragma unroll
-    for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+  for (int h = 0; h < 2; ++h) {
+    const int e = lane + 32 * h;
+    if (e < E) {
+      const ModQ m = K->mq[e];
+      int32_t v = V[(int64_t)e * nc + t];
+      uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
+      uint32_t ce = barrett(vu * K->w[e], m);
+      tf += (uint64_t)ce * K->tfix[e];
+#pragma unroll
+      for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    tf += __shfl_xor_sync(0xffffffffu, tf, o);
+#pragma unroll
+    for (int l = 0; l < kCrtWords; ++l) acc[l] += __shfl_xor_sync(0xffffffffu, acc[l], o);
   }
   uint32_t S[kCrtWords];
   uint64_t carry = 0;
@@ -262,7 +292,6 @@ __global__ void __launch_bounds__(128) k_lift_crt(const int8_t* __restrict__ V, 
   bool ge = true;
 #pragma unroll
   for (int l = kCrtWords - 1; l >= 0; --l) {
-    // lexicographic compare from the top, branch-free
     if (S[l] != K->P[l]) {
       ge = S[l] > K->P[l];
       break;
@@ -295,10 +324,12 @@ __global__ void __launch_bounds__(128) k_lift_crt(const int8_t* __restrict__ V, 
       borrow = d >> 32;
     }
   }
-  uint64_t* out = D + t * kDigitLimbs;
+  uint64_t limb = 0;
 #pragma unroll
-  for (int l = 0; l < kDigitLimbs; ++l) out[l] = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
-  xl[t] = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+  for (int l = 0; l < kDigitLimbs; ++l)
+    if (lane == l) limb = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
+  if (lane < kDigitLimbs) D[t * kDigitLimbs + lane] = limb;
+  if (lane == 0) xl[t] = limb;
 }
 
 template <typename AT>
@@ -306,18 +337,56 @@ __device__ __forceinline__ uint64_t mac64(uint64_t acc, AT a, uint64_t x) {
   return acc + (uint64_t)(int64_t)a * x;
 }
 
-// c == 1: r'[i] = (r[i] - sum_k A[i][k] xl[k]) Pinv mod 2^64 and its residues.  Warp per row.
+// c == 1: r'[i] = (r[i] - sum_k A[i][k] xl[k]) Pinv mod 2^64 and its residues.
+// Warp per row, 4 warps per CTA.  A is read through rows of stride lda
+// (lda = 4-aligned with zero padding for the int32 copy, so 16-byte loads),
+// xl is zero beyond n.
 template <typename AT>
-__global__ void __launch_bounds__(256) k_lift_resid_gemv(const AT* __restrict__ A, const uint64_t* __restrict__ xl,
+__device__ __forceinline__ uint64_t row_dot(const AT* __restrict__ Ai, const uint64_t* __restrict__ xl, int64_t n,
+                                            int lane);
+template <>
+__device__ __forceinline__ uint64_t row_dot<int32_t>(const int32_t* __restrict__ Ai,
+                                                     const uint64_t* __restrict__ xl, int64_t n, int lane) {
+  const int4* A4 = reinterpret_cast<const int4*>(Ai);
+  const ulonglong2* X2 = reinterpret_cast<const ulonglong2*>(xl);
+  const int64_t q = (n + 3) / 4;
+  uint64_t s0 = 0, s1 = 0;
+  int64_t k = lane;
+  for (; k + 32 < q; k += 64) {
+    const int4 a0 = __ldg(A4 + k), a1 = __ldg(A4 + k + 32);
+    const ulonglong2 x0 = __ldg(X2 + 2 * k), x1 = __ldg(X2 + 2 * k + 1);
+    const ulonglong2 y0 = __ldg(X2 + 2 * (k + 32)), y1 = __ldg(X2 + 2 * (k + 32) + 1);
+    s0 += (uint64_t)(int64_t)a0.x * x0.x + (uint64_t)(int64_t)a0.y * x0.y + (uint64_t)(int64_t)a0.z * x1.x +
+          (uint64_t)(int64_t)a0.w * x1.y;
+    s1 += (uint64_t)(int64_t)a1.x * y0.x + (uint64_t)(int64_t)a1.y * y0.y + (uint64_t)(int64_t)a1.z * y1.x +
+          (uint64_t)(int64_t)a1.w * y1.y;
+  }
+  for (; k < q; k += 32) {
+    const int4 a0 = __ldg(A4 + k);
+    const ulonglong2 x0 = __ldg(X2 + 2 * k), x1 = __ldg(X2 + 2 * k + 1);
+    s0 += (uint64_t)(int64_t)a0.x * x0.x + (uint64_t)(int64_t)a0.y * x0.y + (uint64_t)(int64_t)a0.z * x1.x +
+          (uint64_t)(int64_t)a0.w * x1.y;
+  }
+  return s0 + s1;
+}
+template <>
+__device__ __forceinline__ uint64_t row_dot<int64_t>(const int64_t* __restrict__ Ai,
+                                                     const uint64_t* __restrict__ xl, int64_t n, int lane) {
+  uint64_t s = 0;
+  for (int64_t k = lane; k < n; k += 32) s += (uint64_t)__ldg(Ai + k) * __ldg(xl + k);
+  return s;
+}
+
+template <typename AT>
+__global__ void __launch_bounds__(128) k_lift_resid_gemv(const AT* __restrict__ A, int64_t lda,
+                                                         const uint64_t* __restrict__ xl,
                                                          const int64_t* __restrict__ r, int64_t n, int64_t ld,
                                                          const LiftConst* __restrict__ K,
                                                          int64_t* __restrict__ rn, int8_t* __restrict__ R) {
   const int lane = threadIdx.x & 31;
   const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= n) return;
-  const AT* Ai = A + i * n;
-  uint64_t s = 0;
-  for (int64_t k = lane; k < n; k += 32) s = mac64(s, Ai[k], __ldg(xl + k));
+  uint64_t s = row_dot<AT>(A + i * lda, xl, n, lane);
 #pragma unroll
   for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const int64_t v = (int64_t)(((uint64_t)r[i] - s) * K->Pinv64);
@@ -328,7 +397,8 @@ __global__ void __launch_bounds__(256) k_lift_resid_gemv(const AT* __restrict__ 
 
 // general c: tile 32 rows x 32 columns; thread (tx = row, ty = 4 columns).
 template <typename AT>
-__global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ A, const uint64_t* __restrict__ xl,
+__global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ A, int64_t lda,
+                                                         const uint64_t* __restrict__ xl,
                                                          const int64_t* __restrict__ r, int64_t n, int64_t c,
                                                          int64_t ld, const LiftConst* __restrict__ K,
                                                          int64_t* __restrict__ rn, int8_t* __restrict__ R) {
@@ -341,7 +411,7 @@ __global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ 
     for (int idx = tid; idx < 32 * 32; idx += 256) {
       int rr = idx >> 5, kk = idx & 31;
       int64_t i = row0 + rr, k = k0 + kk;
-      As[rr][kk] = (i < n && k < n) ? (int64_t)A[i * n + k] : 0;
+      As[rr][kk] = (i < n && k < n) ? (int64_t)A[i * lda + k] : 0;
       int64_t col = col0 + kk;  // reuse: Xs[k][col]
       int64_t kr = k0 + rr;
       Xs[rr][kk] = (kr < n && col < c) ? xl[kr * c + col] : 0;
@@ -368,9 +438,12 @@ __global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ 
   }
 }
 
-__global__ void k_narrow_a(const int64_t* __restrict__ A, int64_t count, int32_t* __restrict__ A32) {
+// A32[i][k] = A[i][k] for k < n, 0 for n <= k < lda.
+__global__ void k_narrow_a(const int64_t* __restrict__ A, int64_t n, int64_t lda, int32_t* __restrict__ A32) {
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t < count) A32[t] = (int32_t)A[t];
+  if (t >= n * lda) return;
+  int64_t i = t / lda, k = t - i * lda;
+  A32[t] = k < n ? (int32_t)A[i * n + k] : 0;
 }
 
 // ------------------------------------------------------------ driver
@@ -386,8 +459,8 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   o.R = L.add((size_t)E * c * ld);
   o.V = L.add((size_t)E * n * c);
   o.r = L.add((size_t)2 * n * c * 8);
-  o.xl = L.add((size_t)n * c * 8);
-  o.A32 = a32 ? L.add((size_t)n * n * 4) : 0;
+  o.xl = L.add((size_t)padded_ld(n) * c * 8);
+  o.A32 = a32 ? L.add((size_t)n * padded_ld(n) * 4) : 0;
   o.total = L.total;
   return o;
 }
@@ -416,8 +489,9 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   // synchronously with respect to the host before returning.
   ES_CHECK(cuda_status(cudaMemcpyAsync(K, &hK, sizeof(hK), cudaMemcpyHostToDevice, st), "lift const H2D"));
   ES_CHECK(cuda_status(cudaMemsetAsync(R, 0, (size_t)E * c * ld, st), "memset R"));
+  ES_CHECK(cuda_status(cudaMemsetAsync(xl, 0, (size_t)padded_ld(n) * c * 8, st), "memset xl"));
   if (a32) {
-    k_narrow_a<<<(unsigned)((n * n + 255) / 256), 256, 0, st>>>(A_dev, n * n, A32);
+    k_narrow_a<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, A32);
     ES_CHECK(cuda_status(cudaGetLastError(), "k_narrow_a"));
   }
   k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R);
@@ -431,29 +505,28 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   for (int32_t i = 0; i < m; ++i) {
     if (!ev.empty()) cudaEventRecord(ev[2 * i], st);
     if (c == 1)
-      k_lift_gemv<<<dim3((unsigned)((n + 31) / 32), E), 256, 0, st>>>(B_dev, R, n, ld, K, V);
+      k_lift_gemv<4><<<dim3((unsigned)((n + 31) / 32), E), 256, 0, st>>>(B_dev, R, n, ld, K, V);
     else
       k_lift_gemm<<<dim3((unsigned)((c + 63) / 64), (unsigned)((n + 63) / 64), E), 256, 0, st>>>(B_dev, R, n, c,
                                                                                                 ld, K, V);
     if (!ev.empty()) cudaEventRecord(ev[2 * i + 1], st);
     count_launch(2);
-    k_lift_crt<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
-                                                              xl);
+    k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl);
     if (i + 1 < m) {
       count_launch(1);
       const int64_t* rc = r[i & 1];
       int64_t* rn = r[(i + 1) & 1];
       if (c == 1) {
         if (a32)
-          k_lift_resid_gemv<int32_t><<<(unsigned)((n + 7) / 8), 256, 0, st>>>(A32, xl, rc, n, ld, K, rn, R);
+          k_lift_resid_gemv<int32_t><<<(unsigned)((n + 3) / 4), 128, 0, st>>>(A32, ld, xl, rc, n, ld, K, rn, R);
         else
-          k_lift_resid_gemv<int64_t><<<(unsigned)((n + 7) / 8), 256, 0, st>>>(A_dev, xl, rc, n, ld, K, rn, R);
+          k_lift_resid_gemv<int64_t><<<(unsigned)((n + 3) / 4), 128, 0, st>>>(A_dev, n, xl, rc, n, ld, K, rn, R);
       } else {
         dim3 g((unsigned)((c + 31) / 32), (unsigned)((n + 31) / 32));
         if (a32)
-          k_lift_resid_gemm<int32_t><<<g, 256, 0, st>>>(A32, xl, rc, n, c, ld, K, rn, R);
+          k_lift_resid_gemm<int32_t><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
         else
-          k_lift_resid_gemm<int64_t><<<g, 256, 0, st>>>(A_dev, xl, rc, n, c, ld, K, rn, R);
+          k_lift_resid_gemm<int64_t><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
       }
     }
   }
