@@ -272,8 +272,10 @@ def run_gb300(args, rank, local_rank, world):
             t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
+        # device->host: sampled components' digits (4 x m x 48 B), the numerators
+        # (n c limbs x 8 B), the acceptance flags (n c B) and the good-prime flags
         e2e = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(8 * (n * n + n * c)),
-               "d2h_bytes_per_step": int(s.m * n * c * 48)}
+               "d2h_bytes_per_step": int(min(4, n * c) * s.m * 48 + n * c * s.limbs * 8 + n * c + 53)}
 
     if rank != 0:
         return

@@ -11,7 +11,6 @@ no CPU fallback: a missing library or GPU raises).
 from __future__ import annotations
 
 import ctypes
-from dataclasses import dataclass, field
 from fractions import Fraction
 from typing import List, Optional, Tuple
 
@@ -34,18 +33,41 @@ def _check(st: int, where: str):
         raise ExactSolveError(st, where)
 
 
-@dataclass
 class Solution:
-    """Canonical exact solution: x = N / d with d > 0 least."""
-    N: List[List[int]]
-    d: int
-    m: int = 0
-    primes_used: int = 0
-    phase_ms: List[float] = field(default_factory=list)
-    launches: int = 0              # device kernels launched by the solve
-    top_launches: int = 0          # launches of the lift's per-prime product kernel
-    top_ms: float = 0.0            # their summed CUDA-event time (timing=2 only)
-    top_bytes_per_launch: float = 0.0
+    """Canonical exact solution x = N / d (d > 0 least, gcd(d, N) = 1).
+
+    Holds the exported little-endian two's complement limbs ([n*c, limbs]
+    numerators, [limbs] denominator); Python ints are built on first access
+    of ``N`` or ``d``."""
+
+    def __init__(self, num, den, n, c, m=0, primes_used=0, phase_ms=None, launches=0, top_launches=0, top_ms=0.0,
+                 top_bytes_per_launch=0.0):
+        self.num_limbs = num
+        self.den_limbs = den
+        self.n, self.c = n, c
+        self.limbs = int(den.shape[0])
+        self.m = m
+        self.primes_used = primes_used
+        self.phase_ms = list(phase_ms or [])
+        self.launches = launches              # device kernels launched by the solve
+        self.top_launches = top_launches      # launches of the lift's per-prime product kernel
+        self.top_ms = top_ms                  # their summed CUDA-event time (timing=2 only)
+        self.top_bytes_per_launch = top_bytes_per_launch
+        self._N = None
+        self._d = None
+
+    @property
+    def N(self) -> List[List[int]]:
+        if self._N is None:
+            flat = _limbs_to_ints(self.num_limbs, self.n * self.c, self.limbs, True)
+            self._N = [flat[i * self.c:(i + 1) * self.c] for i in range(self.n)]
+        return self._N
+
+    @property
+    def d(self) -> int:
+        if self._d is None:
+            self._d = _limbs_to_ints(self.den_limbs, 1, self.limbs, False)[0]
+        return self._d
 
     def fractions(self) -> List[List[Fraction]]:
         return [[Fraction(v, self.d) for v in row] for row in self.N]
@@ -83,10 +105,7 @@ def _take_solution(ptr: ctypes.c_void_p) -> Solution:
     _check(lib.es_solution_kernels(ptr, ctypes.byref(la), ctypes.byref(tl), ctypes.byref(tms), ctypes.byref(tb)),
            "es_solution_kernels")
     lib.es_solution_free(ptr)
-    flat = _limbs_to_ints(num, n * c, W, True)
-    d = _limbs_to_ints(den, 1, W, False)[0]
-    N = [flat[i * c:(i + 1) * c] for i in range(n)]
-    return Solution(N, d, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value)
+    return Solution(num, den, n, c, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value)
 
 
 def _as_host_i64(x) -> np.ndarray:

@@ -309,6 +309,9 @@ static uint64_t bits_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^64
   uint64_t lo = w < x.size() ? x[w] : 0, hi = w + 1 < x.size() ? x[w + 1] : 0;
   return b ? (lo >> b) | (hi << (64 - b)) : lo;
 }
+static u128 bits128_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^128
+  return (u128)bits_at(x, sh) | ((u128)bits_at(x, sh + 64) << 64);
+}
 
 static inline limb uabs(int64_t v) { return v < 0 ? (limb)(-v) : (limb)v; }
 
@@ -373,21 +376,37 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
           sT1 = *T1;
         }
       }
-      const size_t sh = bitlen(r0) - 62;
-      int64_t a = (int64_t)bits_at(r0, sh), b = (int64_t)bits_at(r1, sh);
+      // Simulate on the leading 126 bits (Knuth, Algorithm L, with two
+      // quotient checks), cofactors kept below 2^62 in magnitude.
+      const size_t bl0 = bitlen(r0);
+      const size_t sh = bl0 > 126 ? bl0 - 126 : 0;
+      const __int128 kCap = (__int128)1 << 62;
+      __int128 a = (__int128)bits128_at(r0, sh), b = (__int128)bits128_at(r1, sh);
       int64_t A = 1, B = 0, C = 0, D = 1;
       size_t k = 0;
       for (;;) {
-        if (b + C <= 0 || b + D <= 0) break;
-        int64_t q1 = (a + A) / (b + C), q2 = (a + B) / (b + D);
-        if (q1 != q2) break;
-        int64_t t = A - q1 * C;
+        const __int128 bc = b + C, bd = b + D;
+        if (bc <= 0 || bd <= 0) break;
+        const __int128 ac = a + A, ad = a + B;
+        if (ac < bc) break;
+        // q = floor(ac / bc), small quotients by subtraction
+        __int128 q = 1, rem = ac - bc;
+        while (rem >= bc && q < 4) {
+          rem -= bc;
+          ++q;
+        }
+        if (rem >= bc) q = (__int128)((unsigned __int128)ac / (unsigned __int128)bc);
+        // second check: floor(ad / bd) == q
+        if (q >= kCap) break;
+        const __int128 lo = q * bd;
+        if (ad < lo || ad - lo >= bd) break;
+        const __int128 nC = (__int128)A - q * C, nD = (__int128)B - q * D;
+        if (nC >= kCap || -nC >= kCap || nD >= kCap || -nD >= kCap) break;
         A = C;
-        C = t;
-        t = B - q1 * D;
+        C = (int64_t)nC;
         B = D;
-        D = t;
-        t = a - q1 * b;
+        D = (int64_t)nD;
+        const __int128 t = a - q * b;
         a = b;
         b = t;
         ++k;

@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
   __shared__ __align__(16) int s_wmin[32];
   __shared__ __align__(16) int32_t s_raw[NBP];
   __shared__ __align__(16) int32_t s_prow[NBP];
+  __shared__ __align__(16) int32_t s_pupd[NBP];
   __shared__ int s_piv[NBP];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int row = tid;
@@ -253,8 +254,12 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
     if (warp == 0) {
       const int32_t pf = s_raw[a];
       const uint32_t inv = s_inv[pf < 0 ? pf + (int32_t)m.q : pf];
-      for (int t = lane; t < NBP; t += 32)
-        s_prow[t] = (t == a) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(s_raw[t], m) * (int32_t)inv, m);
+      for (int t = lane; t < NBP; t += 32) {
+        const int32_t pt =
+            (t == a) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(s_raw[t], m) * (int32_t)inv, m);
+        s_prow[t] = pt;
+        s_pupd[t] = (t == a) ? pt + 1 : pt;
+      }
     }
     __syncthreads();  // (3) scaled pivot row
     if (row == pr) {
@@ -267,20 +272,16 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
         v[4 * t4 + 3] = pv.w;
       }
     } else if (f != 0) {
-      const int32_t fa = reduce_bal(-f * s_prow[a], m);
+      // v[t] -= f p_t for every t, with p_a taken as inv + 1: the pivot column
+      // then becomes v[a] - f inv - f = -f inv (mod q), since v[a] = f (mod q).
 #pragma unroll
       for (int t4 = 0; t4 < NBP / 4; ++t4) {
-        const int4 pv = *reinterpret_cast<const int4*>(s_prow + 4 * t4);
-        const int32_t pp[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int t = 4 * t4 + u;
-          v[t] = (t == a) ? fa : v[t] - f * pp[u];
-        }
+        const int4 pv = *reinterpret_cast<const int4*>(s_pupd + 4 * t4);
+        v[4 * t4] -= f * pv.x;
+        v[4 * t4 + 1] -= f * pv.y;
+        v[4 * t4 + 2] -= f * pv.z;
+        v[4 * t4 + 3] -= f * pv.w;
       }
-    } else {
-#pragma unroll
-      for (int t = 0; t < NBP; ++t) v[t] = (t == a) ? 0 : v[t];
     }
   }
   // reduce and write the panel back (padding columns stay zero: their pivot-row entries are zero)
@@ -302,19 +303,29 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
     p.used[(int64_t)j * n + row] = used ? 1 : 0;
   }
   __syncthreads();
-  // stage U^T (pivot rows outside the panel) and zero those entries in place
+  // stage U^T (pivot rows outside the panel) and zero those entries in place:
+  // thread = column; all kb loads are issued before any store
   int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
-  for (int a = 0; a < NBP; ++a) {
-    const int pr = a < kb ? s_piv[a] : 0;
-    for (int col = tid; col < ld; col += blockDim.x) {
-      int8_t val = 0;
-      if (a < kb && (col < k0 || col >= k0 + kb)) {
-        const int64_t off = (int64_t)pr * ld + col;
-        val = Wj[off];
-        Wj[off] = 0;
+  for (int col = tid; col < ld; col += blockDim.x) {
+    const bool outside = col < k0 || col >= k0 + kb;
+    uint32_t w[NBP / 4];
+#pragma unroll
+    for (int q = 0; q < NBP / 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int a = 4 * q + u;
+        const uint8_t b = (a < kb && outside) ? (uint8_t)Wj[(int64_t)s_piv[a] * ld + col] : (uint8_t)0;
+        x |= (uint32_t)b << (8 * u);
       }
-      UTj[(int64_t)col * NBP + a] = val;
+      w[q] = x;
     }
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4)
+      *reinterpret_cast<int4*>(UTj + (int64_t)col * NBP + 16 * c4) =
+          make_int4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+    if (outside)
+      for (int a = 0; a < kb; ++a) Wj[(int64_t)s_piv[a] * ld + col] = 0;
   }
 }
 
@@ -403,6 +414,8 @@ __device__ __forceinline__ void mma_s8_16x8x32(int32_t (&c)[4], const uint32_t (
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+__device__ __forceinline__ int rot3(int r) { return ((r << 1) | ((r >> 2) & 1)) & 7; }
+
 __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, int64_t k0, int kb) {
   const int j = blockIdx.z;
   if (p.bad[j]) return;
@@ -413,7 +426,11 @@ __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, int64_t k0, i
   const int64_t col0 = (int64_t)blockIdx.x * 128 + (warp & 3) * 32;
   int8_t* Wj = p.W + (int64_t)j * n * ld;
   const int8_t* UTj = p.UT + (int64_t)j * ld * 32;
-  __shared__ int32_t Cs[8][32][33];  // per warp: its 32 x 32 tile of F U
+  // per warp: its 32 x 32 tile of F U.  Within a row the 16-byte chunk c is
+  // stored at chunk c ^ rot(row) (rot = 3-bit left rotation of row & 7), which
+  // makes both the 8-byte fragment stores (per half-warp) and the 16-byte row
+  // reads (per quarter-warp) hit 32 distinct banks.
+  __shared__ __align__(16) int32_t Cs[8][32][32];
   // this thread's output row segment (row0 + lane, 32 columns), fetched early
   const int64_t orow = row0 + lane;
   // segments are 32-column aligned like the panel: one either is the panel or misses it
@@ -445,13 +462,24 @@ __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, int64_t k0, i
     for (int ni = 0; ni < 4; ++ni) {
       int32_t c[4] = {0, 0, 0, 0};
       mma_s8_16x8x32(c, a[mi], b[ni]);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) Cs[warp][16 * mi + g + 8 * (r >> 1)][8 * ni + 2 * t + (r & 1)] = c[r];
+      const int cw = 8 * ni + 2 * t, sw = (4 * ((cw >> 2) ^ rot3(g))) | (cw & 3);  // rows g, g + 8: same rot
+      *reinterpret_cast<int2*>(&Cs[warp][16 * mi + g][sw]) = make_int2(c[0], c[1]);
+      *reinterpret_cast<int2*>(&Cs[warp][16 * mi + g + 8][sw]) = make_int2(c[2], c[3]);
     }
   __syncwarp();
   if (!rowok) return;
   uint32_t w[8] = {(uint32_t)old0.x, (uint32_t)old0.y, (uint32_t)old0.z, (uint32_t)old0.w,
                    (uint32_t)old1.x, (uint32_t)old1.y, (uint32_t)old1.z, (uint32_t)old1.w};
+  int32_t cv[32];
+  const int rl = rot3(lane);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int4 c4 = *reinterpret_cast<const int4*>(&Cs[warp][lane][4 * (q ^ rl)]);
+    cv[4 * q] = c4.x;
+    cv[4 * q + 1] = c4.y;
+    cv[4 * q + 2] = c4.z;
+    cv[4 * q + 3] = c4.w;
+  }
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     uint32_t x = 0;
@@ -460,7 +488,7 @@ __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, int64_t k0, i
       const int cc = 4 * q + u;
       const int64_t col = col0 + cc;
       int32_t val = sbyte(w[q], u);
-      if (col < n && (col < k0 || col >= k0 + kb)) val = reduce_bal(val + Cs[warp][lane][cc], m);
+      if (col < n) val = reduce_bal(val + cv[cc], m);
       x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
     }
     w[q] = x;

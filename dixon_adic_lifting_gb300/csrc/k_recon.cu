@@ -290,25 +290,29 @@ es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_
     const int64_t need = std::max(num_bits + na, den_bits + u64_bitlen(stats.max_abs_b)) + 2;
     if (big::le_pow2(Q, (size_t)need)) return ES_ERR_INTERNAL;
   }
-  // one component's full digits -> its residue mod M (for the denominators)
-  std::vector<uint64_t> hd((size_t)m * kDigitLimbs);
-  auto residue = [&](int64_t k, Nat* u) -> es_status {
-    ES_CHECK(cuda_status(cudaMemcpy2DAsync(hd.data(), kDigitLimbs * 8, D_dev + (size_t)k * kDigitLimbs,
-                                           (size_t)nc * kDigitLimbs * 8, kDigitLimbs * 8, (size_t)m,
-                                           cudaMemcpyDeviceToHost, st),
-                         "sample digits D2H"));
+  // components' full digits -> residues mod M -> denominators (host threads)
+  auto denominators = [&](const std::vector<int64_t>& ks, std::vector<Nat>* dens) -> es_status {
+    std::vector<uint64_t> hd(ks.size() * (size_t)m * kDigitLimbs);
+    for (size_t t = 0; t < ks.size(); ++t)
+      ES_CHECK(cuda_status(cudaMemcpy2DAsync(hd.data() + t * (size_t)m * kDigitLimbs, kDigitLimbs * 8,
+                                             D_dev + (size_t)ks[t] * kDigitLimbs, (size_t)nc * kDigitLimbs * 8,
+                                             kDigitLimbs * 8, (size_t)m, cudaMemcpyDeviceToHost, st),
+                           "sample digits D2H"));
     ES_CHECK(cuda_status(cudaStreamSynchronize(st), "sample digits sync"));
-    *u = shifted_to_residue(assemble_shifted(ps, hd.data(), kDigitLimbs, m), Mhalf, Mhalf1);
-    return ES_OK;
+    dens->assign(ks.size(), Nat{});
+    std::atomic<int> fail(0);
+    parallel_for((int64_t)ks.size(), threads, [&](int64_t t) {
+      const Nat u = shifted_to_residue(assemble_shifted(ps, hd.data() + (size_t)t * m * kDigitLimbs, kDigitLimbs, m),
+                                       Mhalf, Mhalf1);
+      if (!component_denominator(M, u, num_bits, den_bits, &(*dens)[(size_t)t])) fail = 1;
+    });
+    return fail ? ES_ERR_INTERNAL : ES_OK;
   };
   const int64_t ns = nc < 4 ? nc : 4;
-  std::vector<Nat> su((size_t)ns), sden((size_t)ns);
-  for (int64_t t = 0; t < ns; ++t) ES_CHECK(residue((t * nc) / ns, &su[(size_t)t]));
-  std::atomic<int> fail(0);
-  parallel_for(ns, threads, [&](int64_t t) {
-    if (!component_denominator(M, su[(size_t)t], num_bits, den_bits, &sden[(size_t)t])) fail = 1;
-  });
-  if (fail) return ES_ERR_INTERNAL;
+  std::vector<int64_t> sk;
+  for (int64_t t = 0; t < ns; ++t) sk.push_back((t * nc) / ns);
+  std::vector<Nat> sden;
+  ES_CHECK(denominators(sk, &sden));
   Nat d = big::from_u64(1);
   for (auto& v : sden) lcm_in(d, v);
 
@@ -388,12 +392,9 @@ es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_
       if (!okh[(size_t)k]) failed.push_back(k);
     if (failed.empty()) break;
     const Nat before = d;
-    for (int64_t k : failed) {
-      Nat u, den;
-      ES_CHECK(residue(k, &u));
-      if (!component_denominator(M, u, num_bits, den_bits, &den)) return ES_ERR_INTERNAL;
-      lcm_in(d, den);
-    }
+    std::vector<Nat> fden;
+    ES_CHECK(denominators(failed, &fden));
+    for (auto& v : fden) lcm_in(d, v);
     if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;
   }
   if (!big::le_pow2(d, (size_t)den_bits)) return ES_ERR_INTERNAL;
