@@ -329,6 +329,181 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
   }
 }
 
+// Register panel with R rows per thread and T threads (n <= T R).  Same
+// exchange steps as k_gj_panel_reg, in a rotating frame: after each step a
+// thread's row is rotated by one entry, so that at step a the entry of panel
+// column c sits in v[(c - a) mod NBP] and the pivot column is always v[0] --
+// no runtime-indexed register access.  The update writes v[t] - f u_{t} into
+// v[t - 1] (the rotation costs one move per row), with the pivot row scaled
+// and stored already rotated by warp 0; the row is rotated back once, by kb,
+// when the panel is written.  Rows of thread t: t, t + T, ..., t + T (R - 1).
+template <int NBP, int R, int T>
+__global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, int kb) {
+  const int j = blockIdx.x;
+  if (p.bad[j]) return;
+  const ModQ m = c_modq.v[j];
+  const int n = (int)p.n, ld = (int)p.ld;
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  __shared__ uint8_t s_inv[256];
+  __shared__ __align__(16) int s_wmin[T / 32];
+  __shared__ __align__(16) int32_t s_raw[NBP];   // pivot row, natural column order
+  __shared__ __align__(16) int32_t s_prow[NBP];  // scaled pivot row, rotated: entry t = column (a + t) mod NBP
+  __shared__ __align__(16) int32_t s_pupd[NBP];  // same with the pivot entry + 1
+  __shared__ int s_piv[NBP];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int x = tid; x < (int)m.q; x += T) s_inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
+  int32_t v[R][NBP];
+  bool used[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int row = tid + T * i;
+    const bool active = row < n;
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4) {
+      int4 w = make_int4(0, 0, 0, 0);
+      if (active && k0 + 16 * c4 < ld) w = *reinterpret_cast<const int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4);
+      const uint32_t ww[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[i][c4 * 16 + q4 * 4 + u] = sbyte(ww[q4], u);
+    }
+    used[i] = active ? p.used[(int64_t)j * n + row] != 0 : true;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int a = 0; a < kb; ++a) {
+    int32_t f[R];
+    int cand = INT_MAX;
+#pragma unroll
+    for (int i = R - 1; i >= 0; --i) {  // rows grow with i: the smallest i wins
+      f[i] = reduce_bal(v[i][0], m);
+      if (!used[i] && f[i] != 0) cand = tid + T * i;
+    }
+    cand = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == 0) s_wmin[warp] = cand;
+    __syncthreads();  // (1) candidates of every warp
+    int pr = INT_MAX;
+#pragma unroll
+    for (int w4 = 0; w4 < T / 128; ++w4) {
+      const int4 c = *reinterpret_cast<const int4*>(s_wmin + 4 * w4);
+      pr = min(pr, min(min(c.x, c.y), min(c.z, c.w)));
+    }
+    if (pr == INT_MAX) {  // no pivot: q_j | det A
+      if (tid == 0) p.bad[j] = 1;
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (tid + T * i == pr) {
+#pragma unroll
+        for (int t = 0; t < NBP; ++t) s_raw[(a + t) & (NBP - 1)] = t == 0 ? f[i] : v[i][t];
+        used[i] = true;
+        s_piv[a] = pr;
+        p.piv[(int64_t)j * n + k0 + a] = pr;
+      }
+    __syncthreads();  // (2) raw pivot row
+    if (warp == 0) {
+      const int32_t pf = s_raw[a];
+      const uint32_t inv = s_inv[pf < 0 ? pf + (int32_t)m.q : pf];
+      for (int t = lane; t < NBP; t += 32) {
+        const int c = (a + t) & (NBP - 1);
+        const int32_t pt =
+            (t == 0) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(s_raw[c], m) * (int32_t)inv, m);
+        s_prow[t] = pt;
+        s_pupd[t] = (t == 0) ? pt + 1 : pt;
+      }
+    }
+    __syncthreads();  // (3) scaled pivot row
+    // v[t] <- (v[t + 1] - f u_{t + 1}), v[NBP - 1] <- (v[0] - f u_0); the pivot row takes p instead.
+    // u_0 = p_a + 1 turns the pivot column into -f inv (mod q), as v[0] = f (mod q).
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (tid + T * i == pr) {
+#pragma unroll
+        for (int t4 = 0; t4 < NBP / 4; ++t4) {
+          const int4 pp = *reinterpret_cast<const int4*>(s_prow + 4 * t4);
+          const int32_t ps[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[i][(4 * t4 + u + NBP - 1) & (NBP - 1)] = ps[u];
+        }
+      } else {
+        const int32_t fi = f[i], first = v[i][0] - fi * s_pupd[0];
+#pragma unroll
+        for (int t4 = 0; t4 < NBP / 4; ++t4) {
+          const int4 uu = *reinterpret_cast<const int4*>(s_pupd + 4 * t4);
+          const int32_t us[4] = {uu.x, uu.y, uu.z, uu.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int t = 4 * t4 + u;
+            if (t > 0) v[i][t - 1] = v[i][t] - fi * us[u];
+          }
+        }
+        v[i][NBP - 1] = first;
+      }
+    }
+  }
+  // rotate back by kb (entry t holds column (kb + t) mod NBP), log shifter
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+#pragma unroll
+    for (int sh = 1; sh < NBP; sh <<= 1) {
+      if (kb & sh) {
+        int32_t tmp[NBP];
+#pragma unroll
+        for (int t = 0; t < NBP; ++t) tmp[(t + sh) & (NBP - 1)] = v[i][t];
+#pragma unroll
+        for (int t = 0; t < NBP; ++t) v[i][t] = tmp[t];
+      }
+    }
+  }
+  // reduce and write the panel back (padding columns stay zero: their pivot-row entries are zero)
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int row = tid + T * i;
+    if (row >= n) continue;
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4) {
+      if (k0 + 16 * c4 >= ld) continue;
+      uint32_t ww[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          x |= ((uint32_t)(uint8_t)(int8_t)reduce_bal(v[i][c4 * 16 + q4 * 4 + u], m)) << (8 * u);
+        ww[q4] = x;
+      }
+      *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) = make_int4(ww[0], ww[1], ww[2], ww[3]);
+    }
+    p.used[(int64_t)j * n + row] = used[i] ? 1 : 0;
+  }
+  __syncthreads();
+  // stage U^T (pivot rows outside the panel) and zero those entries in place
+  int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
+  for (int col = tid; col < ld; col += T) {
+    const bool outside = col < k0 || col >= k0 + kb;
+    uint32_t w[NBP / 4];
+#pragma unroll
+    for (int q = 0; q < NBP / 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int aa = 4 * q + u;
+        const uint8_t b = (aa < kb && outside) ? (uint8_t)Wj[(int64_t)s_piv[aa] * ld + col] : (uint8_t)0;
+        x |= (uint32_t)b << (8 * u);
+      }
+      w[q] = x;
+    }
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4)
+      *reinterpret_cast<int4*>(UTj + (int64_t)col * NBP + 16 * c4) =
+          make_int4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+    if (outside)
+      for (int aa = 0; aa < kb; ++aa) Wj[(int64_t)s_piv[aa] * ld + col] = 0;
+  }
+}
+
 // ------------------------------------------------------------------ update
 // W[i][t] = bal(W[i][t] + sum_a F[i][a] U[a][t]) for all rows i and all
 // columns t outside the panel; CTA tile 64 rows x 128 columns, one prime.
@@ -566,11 +741,14 @@ es_status run_blocks(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) {
                        "panel smem attribute"));
   dim3 ugrid((unsigned)((gp.ld + 127) / 128), (unsigned)((n + 63) / 64), kNumPrimes);
   const bool reg_panel = NBP == 32 && n <= 1024;  // one row per thread, panel in registers
-  const int reg_threads = (int)((n + 31) / 32 * 32);
   for (int64_t k0 = 0; k0 < n; k0 += NBP) {
     int kb = (int)((n - k0) < NBP ? (n - k0) : NBP);
-    if (reg_panel)
-      k_gj_panel_reg<NBP><<<kNumPrimes, reg_threads, 0, st>>>(gp, k0, kb);
+    if (reg_panel && n <= 256)
+      k_gj_panel_rows<NBP, 1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
+    else if (reg_panel && n <= 512)
+      k_gj_panel_rows<NBP, 2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
+    else if (reg_panel)
+      k_gj_panel_rows<NBP, 2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb);
     else
       k_gj_panel<NBP><<<kNumPrimes, 1024, smem, st>>>(gp, k0, kb, use_smem ? 1 : 0);
     if (NBP == 32)

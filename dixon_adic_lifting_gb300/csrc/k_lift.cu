@@ -113,10 +113,26 @@ __global__ void k_lift_init(const int64_t* __restrict__ b, int64_t n, int64_t c,
   for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
 
+// 16-byte read-only load with an L2 cache-hint policy (createpolicy).
+__device__ __forceinline__ int4 ld_hint(const int4* ptr, uint64_t pol) {
+  int4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.s32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(ptr), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // c == 1: V[e][i] = bal(sum_k B_j[i][k] R_e[k]).  Grid (n / (8 RPW), E'): each
 // of the 8 warps takes RPW rows and walks them in rounds of 64 16-byte chunks
 // (two per lane), issuing all of a round's loads before any dp4a so that
-// 2 (RPW + 1) 16-byte loads per lane are in flight.
+// 2 (RPW + 1) 16-byte loads per lane are in flight.  B is read every step:
+// its loads carry an L2 evict-last hint so that, when it fits, it stays in L2
+// across the steps instead of being streamed from HBM each time.
 template <int RPW>
 __global__ void __launch_bounds__(256) k_lift_gemv(const int8_t* __restrict__ B, const int8_t* __restrict__ R,
                                                    int64_t n, int64_t ld, const LiftConst* __restrict__ K,
@@ -135,6 +151,7 @@ __global__ void __launch_bounds__(256) k_lift_gemv(const int8_t* __restrict__ B,
   int32_t acc[RPW];
 #pragma unroll
   for (int u = 0; u < RPW; ++u) acc[u] = 0;
+  const uint64_t keep = l2_evict_last_policy();
   for (int64_t k0 = 0; k0 < chunks; k0 += 64) {
     const int64_t ka = k0 + lane, kb = k0 + 32 + lane;
     const bool va = ka < chunks, vb = kb < chunks;
@@ -143,8 +160,8 @@ __global__ void __launch_bounds__(256) k_lift_gemv(const int8_t* __restrict__ B,
     int4 ba[RPW], bb[RPW];
 #pragma unroll
     for (int u = 0; u < RPW; ++u) {
-      ba[u] = va ? __ldg(Bj + roff[u] + ka) : z;
-      bb[u] = vb ? __ldg(Bj + roff[u] + kb) : z;
+      ba[u] = va ? ld_hint(Bj + roff[u] + ka, keep) : z;
+      bb[u] = vb ? ld_hint(Bj + roff[u] + kb, keep) : z;
     }
 #pragma unroll
     for (int u = 0; u < RPW; ++u) {
