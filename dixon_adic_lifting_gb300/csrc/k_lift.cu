@@ -113,10 +113,10 @@ __global__ void k_lift_init(const int64_t* __restrict__ b, int64_t n, int64_t c,
   for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
 
-// 16-byte read-only load with an L2 cache-hint policy (createpolicy).
+// 16-byte load with an L2 cache-hint policy (createpolicy).
 __device__ __forceinline__ int4 ld_hint(const int4* ptr, uint64_t pol) {
   int4 r;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.s32 {%0,%1,%2,%3}, [%4], %5;"
+  asm volatile("ld.global.L2::cache_hint.v4.s32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(ptr), "l"(pol));
   return r;
