@@ -20,24 +20,16 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <string>
 #include <vector>
 
 #include "es_common.cuh"
 #include "es_internal.h"
+#include "lift_internal.h"
 
 namespace es {
 
-struct LiftConst {
-  int32_t E;                      // number of good primes
-  int32_t pidx[kNumPrimes];       // their indices in the prime table, ascending
-  ModQ mq[kNumPrimes];            // reduction constants, compact order
-  uint32_t w[kNumPrimes];         // (P'/q)^{-1} mod q
-  uint64_t tfix[kNumPrimes];      // floor(2^50 / q)
-  uint32_t Mq[kNumPrimes][kCrtWords];  // P'/q, 32-bit little-endian words
-  uint32_t P[kCrtWords];          // P'
-  uint32_t Phalf[kCrtWords];      // (P' - 1) / 2
-  uint64_t Pinv64;                // P'^{-1} mod 2^64
-};
+
 
 // ------------------------------------------------------------ host constants
 namespace {
@@ -465,11 +457,13 @@ __global__ void k_narrow_a(const int64_t* __restrict__ A, int64_t n, int64_t lda
 
 // ------------------------------------------------------------ driver
 namespace {
+constexpr int64_t kTcMinCols = 16;  // c >= 16: product on tcgen05 (k_lift_tc.cu)
 struct LiftLayout {
-  size_t K, R, V, r, xl, A32, total;
+  size_t K, R, V, r, xl, A32, B16, R16, err, total;
 };
 LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   int64_t ld = padded_ld(n);
+  const bool tc = c >= kTcMinCols;
   Layout L;
   LiftLayout o;
   o.K = L.add(sizeof(LiftConst));
@@ -478,6 +472,9 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   o.r = L.add((size_t)2 * n * c * 8);
   o.xl = L.add((size_t)padded_ld(n) * c * 8);
   o.A32 = a32 ? L.add((size_t)n * padded_ld(n) * 4) : 0;
+  o.B16 = tc ? L.add((size_t)kNumPrimes * n * ld * 2) : 0;
+  o.R16 = tc ? L.add((size_t)E * c * ld * 2) : 0;
+  o.err = L.add(sizeof(int));
   o.total = L.total;
   return o;
 }
@@ -501,12 +498,22 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   int64_t* r[2] = {reinterpret_cast<int64_t*>(scratch + L.r), reinterpret_cast<int64_t*>(scratch + L.r) + nc};
   uint64_t* xl = reinterpret_cast<uint64_t*>(scratch + L.xl);
   int32_t* A32 = a32 ? reinterpret_cast<int32_t*>(scratch + L.A32) : nullptr;
+  const bool tc = c >= kTcMinCols;
+  void* B16 = tc ? (void*)(scratch + L.B16) : nullptr;
+  void* R16 = tc ? (void*)(scratch + L.R16) : nullptr;
+  int* err = reinterpret_cast<int*>(scratch + L.err);
+  TcLift tcl;
 
   // LiftConst lives in pageable host memory on this thread's stack: copy it
   // synchronously with respect to the host before returning.
   ES_CHECK(cuda_status(cudaMemcpyAsync(K, &hK, sizeof(hK), cudaMemcpyHostToDevice, st), "lift const H2D"));
   ES_CHECK(cuda_status(cudaMemsetAsync(R, 0, (size_t)E * c * ld, st), "memset R"));
   ES_CHECK(cuda_status(cudaMemsetAsync(xl, 0, (size_t)padded_ld(n) * c * 8, st), "memset xl"));
+  ES_CHECK(cuda_status(cudaMemsetAsync(err, 0, sizeof(int), st), "memset err"));
+  if (tc) {
+    ES_CHECK(tc_convert_f16(B_dev, B16, (int64_t)kNumPrimes * n * ld, st));
+    ES_CHECK(tc_prepare(&tcl, B16, R16, n, c, ld, E));
+  }
   if (a32) {
     k_narrow_a<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, A32);
     ES_CHECK(cuda_status(cudaGetLastError(), "k_narrow_a"));
@@ -520,14 +527,20 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
     for (auto& e : ev) ES_CHECK(cuda_status(cudaEventCreate(&e), "event create"));
   }
   for (int32_t i = 0; i < m; ++i) {
+    if (tc) ES_CHECK(tc_convert_f16(R, R16, (int64_t)E * c * ld, st));
     if (!ev.empty()) cudaEventRecord(ev[2 * i], st);
-    if (c == 1)
+    if (c == 1) {
       k_lift_gemv<4><<<dim3((unsigned)((n + 31) / 32), E), 256, 0, st>>>(B_dev, R, n, ld, K, V);
-    else
+      count_launch();
+    } else if (tc) {
+      ES_CHECK(tc_launch(tcl, K, V, n, c, ld, E, err, st));
+    } else {
       k_lift_gemm<<<dim3((unsigned)((c + 63) / 64), (unsigned)((n + 63) / 64), E), 256, 0, st>>>(B_dev, R, n, c,
                                                                                                 ld, K, V);
+      count_launch();
+    }
     if (!ev.empty()) cudaEventRecord(ev[2 * i + 1], st);
-    count_launch(2);
+    count_launch();
     k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl);
     if (i + 1 < m) {
       count_launch(1);
@@ -548,7 +561,13 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
     }
   }
   ES_CHECK(cuda_status(cudaGetLastError(), "lift steps"));
+  int herr = 0;
+  ES_CHECK(cuda_status(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st), "lift err D2H"));
   es_status sst = cuda_status(cudaStreamSynchronize(st), "lift sync");
+  if (sst == ES_OK && herr) {
+    set_last_error("lift product kernel: bounded wait expired (code " + std::to_string(herr) + ")");
+    sst = ES_ERR_TIMEOUT;
+  }
   if (kt) {
     kt->launches += m;
     kt->bytes_per_launch = (double)E * ((double)n * (double)n + 2.0 * (double)n * (double)c);
