@@ -241,43 +241,11 @@ __global__ void __launch_bounds__(256) k_lift_gemm(const int8_t* __restrict__ B,
   }
 }
 
-// Balanced CRT of one entry: x = sum_e c_e (P'/q_e) - t P', c_e = v_e w_e mod q_e,
-// t = floor(sum_e c_e / q_e) estimated in 2^-50 fixed point (exact or one too
-// small), one conditional subtraction of P', then the balanced shift.
-// One warp per entry: lane l takes primes l and l + 32, the 12 word sums and
-// the fixed-point sum are reduced across the warp, and every lane finishes the
-// (identical) digit; lanes 0..5 store its six limbs.
-__global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
-                                                  const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
-                                                  uint64_t* __restrict__ xl) {
-  const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= nc) return;
-  const int E = K->E;
-  uint64_t acc[kCrtWords];
-#pragma unroll
-  for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
-  uint64_t tf = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int e = lane + 32 * h;
-    if (e < E) {
-      const ModQ m = K->mq[e];
-      int32_t v = V[(int64_t)e * nc + t];
-      uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
-      uint32_t ce = barrett(vu * K->w[e], m);
-      tf += (uint64_t)ce * K->tfix[e];
-#pragma unroll
-      for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    tf += __shfl_xor_sync(0xffffffffu, tf, o);
-#pragma unroll
-    for (int l = 0; l < kCrtWords; ++l) acc[l] += __shfl_xor_sync(0xffffffffu, acc[l], o);
-  }
-  uint32_t S[kCrtWords];
+// The digit from the word sums acc (S = sum_e c_e P'/q_e as 12 base-2^32
+// columns) and the fixed-point estimate tf of floor(S / P'): normalise,
+// subtract t P', one conditional subtraction of P', then the balanced shift.
+__device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uint64_t tf,
+                                           const LiftConst* __restrict__ K, uint32_t (&S)[kCrtWords]) {
   uint64_t carry = 0;
 #pragma unroll
   for (int l = 0; l < kCrtWords; ++l) {
@@ -333,6 +301,73 @@ __global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, 
       borrow = d >> 32;
     }
   }
+}
+
+// Same digit, one thread per entry (for many entries: no cross-lane work).
+__global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restrict__ V, int64_t nc,
+                                                         const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
+                                                         uint64_t* __restrict__ xl) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= nc) return;
+  const int E = K->E;
+  uint64_t acc[kCrtWords];
+#pragma unroll
+  for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
+  uint64_t tf = 0;
+  for (int e = 0; e < E; ++e) {
+    const ModQ m = K->mq[e];
+    const int32_t v = V[(int64_t)e * nc + t];
+    const uint32_t ce = barrett((uint32_t)(v < 0 ? v + (int32_t)m.q : v) * K->w[e], m);
+    tf += (uint64_t)ce * K->tfix[e];
+#pragma unroll
+    for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+  }
+  uint32_t S[kCrtWords];
+  crt_finish(acc, tf, K, S);
+  uint64_t* out = D + t * kDigitLimbs;
+#pragma unroll
+  for (int l = 0; l < kDigitLimbs; ++l) out[l] = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
+  xl[t] = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+}
+
+// Balanced CRT of one entry: x = sum_e c_e (P'/q_e) - t P', c_e = v_e w_e mod q_e,
+// t = floor(sum_e c_e / q_e) estimated in 2^-50 fixed point (exact or one too
+// small), one conditional subtraction of P', then the balanced shift.
+// One warp per entry: lane l takes primes l and l + 32, the 12 word sums and
+// the fixed-point sum are reduced across the warp, and every lane finishes the
+// (identical) digit; lanes 0..5 store its six limbs.
+__global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
+                                                  const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
+                                                  uint64_t* __restrict__ xl) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= nc) return;
+  const int E = K->E;
+  uint64_t acc[kCrtWords];
+#pragma unroll
+  for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
+  uint64_t tf = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = lane + 32 * h;
+    if (e < E) {
+      const ModQ m = K->mq[e];
+      int32_t v = V[(int64_t)e * nc + t];
+      uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
+      uint32_t ce = barrett(vu * K->w[e], m);
+      tf += (uint64_t)ce * K->tfix[e];
+#pragma unroll
+      for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    tf += __shfl_xor_sync(0xffffffffu, tf, o);
+#pragma unroll
+    for (int l = 0; l < kCrtWords; ++l) acc[l] += __shfl_xor_sync(0xffffffffu, acc[l], o);
+  }
+  uint32_t S[kCrtWords];
+  crt_finish(acc, tf, K, S);
   uint64_t limb = 0;
 #pragma unroll
   for (int l = 0; l < kDigitLimbs; ++l)
@@ -404,7 +439,78 @@ __global__ void __launch_bounds__(128) k_lift_resid_gemv(const AT* __restrict__ 
   for (int e = lane; e < E; e += 32) R[(int64_t)e * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
 
-// general c: tile 32 rows x 32 columns; thread (tx = row, ty = 4 columns).
+// general c, int32 A: r'[i][col] = (r - sum_k A[i][k] x[k][col]) Pinv mod 2^64
+// and its residues.  With x = x_lo + 2^32 x_hi, x_lo read as a signed int32
+// and the borrow folded into the high word (x_hi' = x_hi + (x_lo >> 31)):
+//   A x mod 2^64 = sum_k A x_lo_s (exact int64 product) + 2^32 (sum_k A x_hi' mod 2^32)
+// i.e. one 32 x 32 -> 64 multiply-add and one 32-bit multiply-add per term.
+// CTA tile 64 rows x 64 columns, thread tile 4 x 4, K in slices of 32.
+__global__ void __launch_bounds__(256) k_lift_resid_gemm32(const int32_t* __restrict__ A, int64_t lda,
+                                                           const uint64_t* __restrict__ xl,
+                                                           const int64_t* __restrict__ r, int64_t n, int64_t c,
+                                                           int64_t ld, const LiftConst* __restrict__ K,
+                                                           int64_t* __restrict__ rn, int8_t* __restrict__ R) {
+  __shared__ int32_t As[64][33];
+  __shared__ int2 Xs[32][65];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int64_t row0 = (int64_t)blockIdx.y * 64, col0 = (int64_t)blockIdx.x * 64;
+  int64_t lo[4][4];
+  uint32_t hi[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      lo[a][u] = 0;
+      hi[a][u] = 0;
+    }
+  for (int64_t k0 = 0; k0 < n; k0 += 32) {
+    for (int idx = tid; idx < 64 * 32; idx += 256) {
+      const int rr = idx >> 5, kk = idx & 31;
+      const int64_t i = row0 + rr, k = k0 + kk;
+      As[rr][kk] = (i < n && k < n) ? A[i * lda + k] : 0;
+      const int kr = idx >> 6, cc = idx & 63;
+      const int64_t krow = k0 + kr, col = col0 + cc;
+      const uint64_t x = (krow < n && col < c) ? xl[krow * c + col] : 0;
+      const uint32_t xlo = (uint32_t)x;
+      Xs[kr][cc] = make_int2((int32_t)xlo, (int32_t)((uint32_t)(x >> 32) + (xlo >> 31)));
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < 32; ++kk) {
+      int32_t a[4];
+      int2 x[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) a[q] = As[4 * tx + q][kk];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = Xs[kk][4 * ty + u];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          lo[q][u] += (int64_t)a[q] * (int64_t)x[u].x;
+          hi[q][u] += (uint32_t)a[q] * (uint32_t)x[u].y;
+        }
+    }
+    __syncthreads();
+  }
+  const int E = K->E;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int64_t i = row0 + 4 * tx + q;
+    if (i >= n) continue;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t col = col0 + 4 * ty + u;
+      if (col >= c) continue;
+      const uint64_t s = (uint64_t)lo[q][u] + ((uint64_t)hi[q][u] << 32);
+      const int64_t v = (int64_t)(((uint64_t)r[i * c + col] - s) * K->Pinv64);
+      rn[i * c + col] = v;
+      for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+    }
+  }
+}
+
+// general c, int64 A (entries of 2^31 or more): tile 32 rows x 32 columns.
 template <typename AT>
 __global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ A, int64_t lda,
                                                          const uint64_t* __restrict__ xl,
@@ -457,7 +563,8 @@ __global__ void k_narrow_a(const int64_t* __restrict__ A, int64_t n, int64_t lda
 
 // ------------------------------------------------------------ driver
 namespace {
-constexpr int64_t kTcMinCols = 16;  // c >= 16: product on tcgen05 (k_lift_tc.cu)
+constexpr int64_t kTcMinCols = 16;       // c >= 16: product on tcgen05 (k_lift_tc.cu)
+constexpr int64_t kCrtThreadMin = 32768;  // from this many entries: one thread per entry
 struct LiftLayout {
   size_t K, R, V, r, xl, A32, B16, R16, err, total;
 };
@@ -541,7 +648,11 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
     }
     if (!ev.empty()) cudaEventRecord(ev[2 * i + 1], st);
     count_launch();
-    k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl);
+    if (nc >= kCrtThreadMin)
+      k_lift_crt_thread<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
+                                                                      xl);
+    else
+      k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl);
     if (i + 1 < m) {
       count_launch(1);
       const int64_t* rc = r[i & 1];
@@ -552,11 +663,13 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
         else
           k_lift_resid_gemv<int64_t><<<(unsigned)((n + 3) / 4), 128, 0, st>>>(A_dev, n, xl, rc, n, ld, K, rn, R);
       } else {
-        dim3 g((unsigned)((c + 31) / 32), (unsigned)((n + 31) / 32));
-        if (a32)
-          k_lift_resid_gemm<int32_t><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
-        else
+        if (a32) {
+          dim3 g((unsigned)((c + 63) / 64), (unsigned)((n + 63) / 64));
+          k_lift_resid_gemm32<<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+        } else {
+          dim3 g((unsigned)((c + 31) / 32), (unsigned)((n + 31) / 32));
           k_lift_resid_gemm<int64_t><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
+        }
       }
     }
   }
