@@ -149,6 +149,10 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCE = {"k_lift_fused": "k_lift_fused.cu", "k_lift_gemv": "k_lift.cu", "k_lift_gemm": "k_lift.cu",
+                 "k_lift_gemm_tc": "k_lift_tc.cu"}
+
+
 def traffic_for(kernel_file, kernel):
     """dram bytes per launch from the committed ncu summary, if the kernel's
     source has not changed since it was captured (else None)."""
@@ -293,11 +297,11 @@ def run_gb300(args, rank, local_rank, world):
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single"},
         "phases_ms": phases,
-        "roofline": {"kernel": "k_lift_gemv" if c == 1 else "k_lift_gemm", "bound": "hbm",
+        "roofline": {"kernel": s0.top_kernel, "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "launch_us": round(launch_ms * 1e3, 3),
-                     "bytes_per_launch": bytes_launch,
-                     "traffic": traffic_for("k_lift.cu", "k_lift_gemv" if c == 1 else "k_lift_gemm")},
+                     "launches_per_step": s0.top_launches, "bytes_per_launch": bytes_launch,
+                     "traffic": traffic_for(KERNEL_SOURCE.get(s0.top_kernel, ""), s0.top_kernel)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(sum(s.launches for s in sols)),

@@ -29,6 +29,7 @@ DIGIT_LIMBS = 6
 NUM_PHASES = 6
 FAULT = {"residues": 1, "inverse": 2, "lift": 3, "recon": 4, "nomem": 5}
 FLAG_HOST_RECON = 1
+FLAG_STEP_LIFT = 2
 
 
 class es_options(ctypes.Structure):
@@ -43,6 +44,7 @@ _SIGS = {
     "es_solution_export": (c_i32, [c_vp, c_vp, c_vp]),
     "es_solution_phase_ms": (c_i32, [c_vp, P_dbl, P_i32, P_i32]),
     "es_solution_kernels": (c_i32, [c_vp, P_i64, P_i64, P_dbl, P_dbl]),
+    "es_solution_top_kernel": (ctypes.c_char_p, [c_vp]),
     "es_solution_free": (None, [c_vp]),
     "es_status_string": (ctypes.c_char_p, [c_i32]),
     "es_last_error": (ctypes.c_char_p, []),

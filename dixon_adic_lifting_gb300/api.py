@@ -41,7 +41,7 @@ class Solution:
     of ``N`` or ``d``."""
 
     def __init__(self, num, den, n, c, m=0, primes_used=0, phase_ms=None, launches=0, top_launches=0, top_ms=0.0,
-                 top_bytes_per_launch=0.0):
+                 top_bytes_per_launch=0.0, top_kernel=""):
         self.num_limbs = num
         self.den_limbs = den
         self.n, self.c = n, c
@@ -50,7 +50,8 @@ class Solution:
         self.primes_used = primes_used
         self.phase_ms = list(phase_ms or [])
         self.launches = launches              # device kernels launched by the solve
-        self.top_launches = top_launches      # launches of the lift's per-prime product kernel
+        self.top_kernel = top_kernel          # the lift's dominant kernel (fused lift or per-step product)
+        self.top_launches = top_launches      # its launches
         self.top_ms = top_ms                  # their summed CUDA-event time (timing=2 only)
         self.top_bytes_per_launch = top_bytes_per_launch
         self._N = None
@@ -73,9 +74,10 @@ class Solution:
         return [[Fraction(v, self.d) for v in row] for row in self.N]
 
 
-def _opts(stream=None, threads=0, timing=False, fault=None, max_device_bytes=0, host_recon=False):
+def _opts(stream=None, threads=0, timing=False, fault=None, max_device_bytes=0, host_recon=False,
+          step_lift=False):
     o = L.es_options()
-    o.flags = L.FLAG_HOST_RECON if host_recon else 0
+    o.flags = (L.FLAG_HOST_RECON if host_recon else 0) | (L.FLAG_STEP_LIFT if step_lift else 0)
     o.stream = ctypes.c_void_p(stream) if stream else None
     o.max_device_bytes = max_device_bytes
     o.fault_stage = L.FAULT[fault] if isinstance(fault, str) else int(fault or 0)
@@ -104,8 +106,9 @@ def _take_solution(ptr: ctypes.c_void_p) -> Solution:
     la, tl, tms, tb = L.c_i64(), L.c_i64(), ctypes.c_double(), ctypes.c_double()
     _check(lib.es_solution_kernels(ptr, ctypes.byref(la), ctypes.byref(tl), ctypes.byref(tms), ctypes.byref(tb)),
            "es_solution_kernels")
+    top = (lib.es_solution_top_kernel(ptr) or b"").decode()
     lib.es_solution_free(ptr)
-    return Solution(num, den, n, c, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value)
+    return Solution(num, den, n, c, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value, top)
 
 
 def _as_host_i64(x) -> np.ndarray:
@@ -120,7 +123,7 @@ def _as_host_i64(x) -> np.ndarray:
 
 
 def solve_canonical(A, b, *, threads: int = 0, timing: bool = False, fault=None,
-                    max_device_bytes: int = 0, host_recon: bool = False) -> Optional[Solution]:
+                    max_device_bytes: int = 0, host_recon: bool = False, step_lift: bool = False) -> Optional[Solution]:
     """Exact solution of A x = b from host arrays (es_solve), or None if singular."""
     lib = L.load()
     A = _as_host_i64(A)
@@ -130,7 +133,7 @@ def solve_canonical(A, b, *, threads: int = 0, timing: bool = False, fault=None,
     if A.ndim != 2 or A.shape[0] != A.shape[1] or b.shape[0] != A.shape[0]:
         raise ValueError("A must be [n, n] and b [n, c]")
     out = ctypes.c_void_p()
-    o = _opts(None, threads, timing, fault, max_device_bytes, host_recon)
+    o = _opts(None, threads, timing, fault, max_device_bytes, host_recon, step_lift)
     st = lib.es_solve(A.ctypes.data, b.ctypes.data, A.shape[0], b.shape[1], ctypes.byref(o), ctypes.byref(out))
     if st == L.ES_SINGULAR:
         return None
@@ -152,7 +155,7 @@ def _stream_handle(stream):
 
 
 def solve_device(A_t, b_t, *, stream=None, threads: int = 0, timing: bool = False, fault=None,
-                 max_device_bytes: int = 0, host_recon: bool = False) -> Optional[Solution]:
+                 max_device_bytes: int = 0, host_recon: bool = False, step_lift: bool = False) -> Optional[Solution]:
     """Exact solution with A, b already on the GPU (int64 CUDA tensors), es_solve_device."""
     lib = L.load()
     if b_t.dim() == 1:
@@ -160,7 +163,7 @@ def solve_device(A_t, b_t, *, stream=None, threads: int = 0, timing: bool = Fals
     A_t = A_t.contiguous()
     b_t = b_t.contiguous()
     out = ctypes.c_void_p()
-    o = _opts(_stream_handle(stream), threads, timing, fault, max_device_bytes, host_recon)
+    o = _opts(_stream_handle(stream), threads, timing, fault, max_device_bytes, host_recon, step_lift)
     st = lib.es_solve_device(A_t.data_ptr(), b_t.data_ptr(), A_t.shape[0], b_t.shape[1], ctypes.byref(o),
                              ctypes.byref(out))
     if st == L.ES_SINGULAR:

@@ -80,8 +80,10 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
 void count_launch(int64_t k = 1);
 int64_t launch_count();
 struct KernelTiming {
-  bool events = false;       // bracket each product-kernel launch with events
-  int64_t launches = 0;      // product-kernel launches
+  bool events = false;       // bracket each launch of the dominant lift kernel with events
+  bool fused = false;        // the lift ran as one fused launch (k_lift_fused)
+  const char* name = "";     // that kernel's name
+  int64_t launches = 0;      // its launches
   double ms = 0.0;           // their summed event time
   double bytes_per_launch = 0.0;
 };
@@ -90,7 +92,7 @@ struct KernelTiming {
 size_t lift_scratch_bytes(int64_t n, int64_t c, int E, bool a32);
 es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                    const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
-                   void* stream, KernelTiming* kt = nullptr);
+                   void* stream, KernelTiming* kt = nullptr, bool allow_fused = true);
 
 // ---------------------------------------------------------------- solution
 struct Solution {

@@ -26,6 +26,7 @@
 #include "es_common.cuh"
 #include "es_internal.h"
 #include "lift_internal.h"
+#include "lift_device.cuh"
 
 namespace es {
 
@@ -85,6 +86,7 @@ void build_lift_const(const uint8_t* good, LiftConst* K) {
     std::memcpy(K->Mq[e], Mq, sizeof(Mq));
     K->w[e] = inv_small(w_mod_small(Mq, q), q);
     K->tfix[e] = (1ull << 50) / q;
+    K->t56[e] = (1ull << 56) / q;
   }
   // P^{-1} mod 2^64 by Newton's iteration x <- x (2 - P x) (P x = 1 mod 8 for x = P)
   uint64_t p64 = (uint64_t)P[0] | ((uint64_t)P[1] << 32), x = p64;
@@ -241,68 +243,6 @@ __global__ void __launch_bounds__(256) k_lift_gemm(const int8_t* __restrict__ B,
   }
 }
 
-// The digit from the word sums acc (S = sum_e c_e P'/q_e as 12 base-2^32
-// columns) and the fixed-point estimate tf of floor(S / P'): normalise,
-// subtract t P', one conditional subtraction of P', then the balanced shift.
-__device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uint64_t tf,
-                                           const LiftConst* __restrict__ K, uint32_t (&S)[kCrtWords]) {
-  uint64_t carry = 0;
-#pragma unroll
-  for (int l = 0; l < kCrtWords; ++l) {
-    uint64_t s = acc[l] + carry;
-    S[l] = (uint32_t)s;
-    carry = s >> 32;
-  }
-  // x = S - tq P'
-  const uint32_t tq = (uint32_t)(tf >> 50);
-  uint64_t mc = 0;
-  int64_t borrow = 0;
-#pragma unroll
-  for (int l = 0; l < kCrtWords; ++l) {
-    uint64_t prod = (uint64_t)tq * K->P[l] + mc;
-    mc = prod >> 32;
-    int64_t d = (int64_t)S[l] - (int64_t)(uint32_t)prod + borrow;
-    S[l] = (uint32_t)d;
-    borrow = d >> 32;  // 0 or -1
-  }
-  // if S >= P' subtract once
-  bool ge = true;
-#pragma unroll
-  for (int l = kCrtWords - 1; l >= 0; --l) {
-    if (S[l] != K->P[l]) {
-      ge = S[l] > K->P[l];
-      break;
-    }
-  }
-  if (ge) {
-    borrow = 0;
-#pragma unroll
-    for (int l = 0; l < kCrtWords; ++l) {
-      int64_t d = (int64_t)S[l] - (int64_t)K->P[l] + borrow;
-      S[l] = (uint32_t)d;
-      borrow = d >> 32;
-    }
-  }
-  // balanced: if S > (P'-1)/2 then S -= P' (mod 2^384)
-  bool gt = false;
-#pragma unroll
-  for (int l = kCrtWords - 1; l >= 0; --l) {
-    if (S[l] != K->Phalf[l]) {
-      gt = S[l] > K->Phalf[l];
-      break;
-    }
-  }
-  if (gt) {
-    borrow = 0;
-#pragma unroll
-    for (int l = 0; l < kCrtWords; ++l) {
-      int64_t d = (int64_t)S[l] - (int64_t)K->P[l] + borrow;
-      S[l] = (uint32_t)d;
-      borrow = d >> 32;
-    }
-  }
-}
-
 // Same digit, one thread per entry (for many entries: no cross-lane work).
 __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restrict__ V, int64_t nc,
                                                          const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
@@ -343,31 +283,10 @@ __global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, 
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= nc) return;
   const int E = K->E;
-  uint64_t acc[kCrtWords];
-#pragma unroll
-  for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
-  uint64_t tf = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int e = lane + 32 * h;
-    if (e < E) {
-      const ModQ m = K->mq[e];
-      int32_t v = V[(int64_t)e * nc + t];
-      uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
-      uint32_t ce = barrett(vu * K->w[e], m);
-      tf += (uint64_t)ce * K->tfix[e];
-#pragma unroll
-      for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    tf += __shfl_xor_sync(0xffffffffu, tf, o);
-#pragma unroll
-    for (int l = 0; l < kCrtWords; ++l) acc[l] += __shfl_xor_sync(0xffffffffu, acc[l], o);
-  }
+  const int32_t v0 = lane < E ? V[(int64_t)lane * nc + t] : 0;
+  const int32_t v1 = lane + 32 < E ? V[(int64_t)(lane + 32) * nc + t] : 0;
   uint32_t S[kCrtWords];
-  crt_finish(acc, tf, K, S);
+  crt_warp(v0, v1, lane, K, S);
   uint64_t limb = 0;
 #pragma unroll
   for (int l = 0; l < kDigitLimbs; ++l)
@@ -566,7 +485,7 @@ namespace {
 constexpr int64_t kTcMinCols = 16;       // c >= 16: product on tcgen05 (k_lift_tc.cu)
 constexpr int64_t kCrtThreadMin = 32768;  // from this many entries: one thread per entry
 struct LiftLayout {
-  size_t K, R, V, r, xl, A32, B16, R16, err, total;
+  size_t K, R, V, r, xl, A32, B16, R16, Bf, err, bar, total;
 };
 LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   int64_t ld = padded_ld(n);
@@ -581,7 +500,9 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   o.A32 = a32 ? L.add((size_t)n * padded_ld(n) * 4) : 0;
   o.B16 = tc ? L.add((size_t)kNumPrimes * n * ld * 2) : 0;
   o.R16 = tc ? L.add((size_t)E * c * ld * 2) : 0;
+  o.Bf = (c == 1 && ld <= kFusedMaxLd) ? L.add((size_t)E * n * ld) : 0;
   o.err = L.add(sizeof(int));
+  o.bar = L.add(sizeof(unsigned));
   o.total = L.total;
   return o;
 }
@@ -591,7 +512,7 @@ size_t lift_scratch_bytes(int64_t n, int64_t c, int E, bool a32) { return lift_l
 
 es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                    const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
-                   void* stream, KernelTiming* kt) {
+                   void* stream, KernelTiming* kt, bool allow_fused) {
   cudaStream_t st = (cudaStream_t)stream;
   LiftConst hK;
   build_lift_const(good_host, &hK);
@@ -609,7 +530,13 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   void* B16 = tc ? (void*)(scratch + L.B16) : nullptr;
   void* R16 = tc ? (void*)(scratch + L.R16) : nullptr;
   int* err = reinterpret_cast<int*>(scratch + L.err);
+  unsigned* bar = reinterpret_cast<unsigned*>(scratch + L.bar);
   TcLift tcl;
+  int device = 0;
+  ES_CHECK(cuda_status(cudaGetDevice(&device), "get device"));
+  FusedPlan fp;
+  bool fused = allow_fused && L.Bf && fused_lift_plan(n, c, E, device, &fp);
+  int8_t* Bf = fused ? reinterpret_cast<int8_t*>(scratch + L.Bf) : nullptr;
 
   // LiftConst lives in pageable host memory on this thread's stack: copy it
   // synchronously with respect to the host before returning.
@@ -617,6 +544,7 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   ES_CHECK(cuda_status(cudaMemsetAsync(R, 0, (size_t)E * c * ld, st), "memset R"));
   ES_CHECK(cuda_status(cudaMemsetAsync(xl, 0, (size_t)padded_ld(n) * c * 8, st), "memset xl"));
   ES_CHECK(cuda_status(cudaMemsetAsync(err, 0, sizeof(int), st), "memset err"));
+  ES_CHECK(cuda_status(cudaMemsetAsync(bar, 0, sizeof(unsigned), st), "memset barrier"));
   if (tc) {
     ES_CHECK(tc_convert_f16(B_dev, B16, (int64_t)kNumPrimes * n * ld, st));
     ES_CHECK(tc_prepare(&tcl, B16, R16, n, c, ld, E));
@@ -630,10 +558,32 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   count_launch(a32 ? 2 : 1);
   std::vector<cudaEvent_t> ev;
   if (kt && kt->events) {
-    ev.resize(2 * (size_t)m);
+    ev.resize(fused ? 2 : 2 * (size_t)m);
     for (auto& e : ev) ES_CHECK(cuda_status(cudaEventCreate(&e), "event create"));
   }
-  for (int32_t i = 0; i < m; ++i) {
+  if (fused) {
+    ES_CHECK(fused_lift_relayout(fp, B_dev, K, Bf, n, st));
+    count_launch();
+    if (!ev.empty()) cudaEventRecord(ev[0], st);
+    es_status fs = fused_lift_launch(fp, Bf, A32, a32 ? nullptr : A_dev, b_dev, K, R, xl, digits_dev, bar, err,
+                                     n, E, m, st);
+    if (fs == ES_OK) {
+      if (!ev.empty()) cudaEventRecord(ev[1], st);
+      count_launch();
+    } else if (fs == ES_ERR_RANGE) {
+      fused = false;  // co-residency refused: per-step kernels below
+      for (auto& e : ev) cudaEventDestroy(e);
+      ev.clear();
+      if (kt && kt->events) {
+        ev.resize(2 * (size_t)m);
+        for (auto& e : ev) ES_CHECK(cuda_status(cudaEventCreate(&e), "event create"));
+      }
+    } else {
+      for (auto& e : ev) cudaEventDestroy(e);
+      return fs;
+    }
+  }
+  for (int32_t i = 0; i < m && !fused; ++i) {
     if (tc) ES_CHECK(tc_convert_f16(R, R16, (int64_t)E * c * ld, st));
     if (!ev.empty()) cudaEventRecord(ev[2 * i], st);
     if (c == 1) {
@@ -677,13 +627,24 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   int herr = 0;
   ES_CHECK(cuda_status(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st), "lift err D2H"));
   es_status sst = cuda_status(cudaStreamSynchronize(st), "lift sync");
-  if (sst == ES_OK && herr) {
-    set_last_error("lift product kernel: bounded wait expired (code " + std::to_string(herr) + ")");
+  if (sst == ES_OK && herr == kFusedErrDigit) {
+    set_last_error("fused lift kernel: the short-path digit disagreed with the full digit");
+    sst = ES_ERR_INTERNAL;
+  } else if (sst == ES_OK && herr) {
+    set_last_error(std::string(fused ? "fused lift kernel" : "lift product kernel") +
+                   ": bounded wait expired (code " + std::to_string(herr) + ")");
     sst = ES_ERR_TIMEOUT;
   }
   if (kt) {
-    kt->launches += m;
-    kt->bytes_per_launch = (double)E * ((double)n * (double)n + 2.0 * (double)n * (double)c);
+    kt->launches += fused ? 1 : m;
+    // algorithmic bytes: per step E' n^2 of B, w_A n^2 of A and n (8 + E' + 48)
+    // for the residual, its residues and the digit (fused: all m steps);
+    // per-step product kernels: E' (n^2 + 2 n c)
+    const double nn = (double)n * (double)n;
+    kt->bytes_per_launch = fused ? (double)m * (E * nn + (a32 ? 4.0 : 8.0) * nn + (double)n * (8.0 + E + 48.0))
+                                 : (double)E * (nn + 2.0 * (double)n * (double)c);
+    kt->fused = fused;
+    kt->name = fused ? "k_lift_fused" : c == 1 ? "k_lift_gemv" : tc ? "k_lift_gemm_tc" : "k_lift_gemm";
     for (int32_t i = 0; i < (int32_t)ev.size() / 2; ++i) {
       float ms = 0.f;
       if (cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]) == cudaSuccess) kt->ms += ms;

@@ -16,6 +16,7 @@ struct LiftConst {
   ModQ mq[kNumPrimes];            // reduction constants, compact order
   uint32_t w[kNumPrimes];         // (P'/q)^{-1} mod q
   uint64_t tfix[kNumPrimes];      // floor(2^50 / q)
+  uint64_t t56[kNumPrimes];       // floor(2^56 / q)
   uint32_t Mq[kNumPrimes][kCrtWords];  // P'/q, 32-bit little-endian words
   uint32_t P[kCrtWords];          // P'
   uint32_t Phalf[kCrtWords];      // (P' - 1) / 2
@@ -32,5 +33,26 @@ es_status tc_convert_f16(const int8_t* src, void* dst, int64_t count, void* stre
 es_status tc_prepare(TcLift* t, const void* B16, const void* R16, int64_t n, int64_t c, int64_t ld, int E);
 es_status tc_launch(const TcLift& t, const LiftConst* K, int8_t* V, int64_t n, int64_t c, int64_t ld, int E,
                     int* err, void* stream);
+
+constexpr int kFusedErrDigit = 15;  // error code: the fused lift's two digit paths disagreed
+
+// Fused single-launch lift for c == 1 (k_lift_fused.cu), for n <= kFusedMaxLd:
+// each consumer warp keeps its row of A (int32) in registers.
+constexpr int64_t kFusedMaxLd = 1024;
+struct FusedPlan {
+  int G = 0;         // CTAs (one per SM, at most n)
+  int slots = 0;     // ring slots per CTA
+  int slot_bytes = 0;  // bytes per ring slot (two primes x the most owned rows)
+  size_t smem = 0;   // dynamic shared memory per CTA
+  size_t relayout_bytes = 0;  // B in the order of ownership (E' n ld bytes)
+};
+bool fused_lift_plan(int64_t n, int64_t c, int E, int device, FusedPlan* p);
+// B [53][n][ld] -> Bf [n][E'][ld] in the order of row ownership.
+es_status fused_lift_relayout(const FusedPlan& p, const int8_t* B, const LiftConst* K, int8_t* Bf, int64_t n,
+                              void* stream);
+// ES_ERR_RANGE when the cooperative launch is refused (then nothing ran).
+es_status fused_lift_launch(const FusedPlan& p, const int8_t* Bf, const int32_t* A32, const int64_t* A64,
+                            const int64_t* b, const LiftConst* K, int8_t* R, uint64_t* xl, uint64_t* D,
+                            unsigned* bar, int* err, int64_t n, int E, int32_t m, void* stream);
 
 }  // namespace es

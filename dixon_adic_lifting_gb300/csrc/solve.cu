@@ -113,6 +113,7 @@ struct Options {
   bool timing = false;
   bool kernel_events = false;
   bool host_recon = false;
+  bool step_lift = false;
 };
 Options read_options(const es_options* o) {
   Options r;
@@ -124,6 +125,7 @@ Options read_options(const es_options* o) {
     r.timing = o->timing != 0;
     r.kernel_events = o->timing >= 2;
     r.host_recon = (o->flags & ES_FLAG_HOST_RECON) != 0;
+    r.step_lift = (o->flags & ES_FLAG_STEP_LIFT) != 0;
   }
   return r;
 }
@@ -250,7 +252,7 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   const bool a32 = stats.max_abs_a < (uint64_t(1) << 31);
   KernelTiming kt;
   kt.events = o.kernel_events;
-  ES_CHECK(run_lift(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt));
+  ES_CHECK(run_lift(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt, !o.step_lift));
   tm.mark(3);
   if (o.fault == ES_FAULT_RECON) {
     set_last_error("injected fault: reconstruction");
@@ -362,6 +364,8 @@ es_status es_solution_kernels(const es_solution* s, int64_t* launches, int64_t* 
   if (top_bytes_per_launch) *top_bytes_per_launch = s->s.top.bytes_per_launch;
   return ES_OK;
 }
+
+const char* es_solution_top_kernel(const es_solution* s) { return s && s->s.top.name ? s->s.top.name : ""; }
 
 void es_solution_free(es_solution* s) { delete s; }
 

@@ -51,7 +51,7 @@ typedef enum {
   ES_ERR_RANGE = -2,    /* outside n <= 2^17, n * max|A_ij| < 2^63 */
   ES_ERR_CUDA = -3,     /* a CUDA runtime call failed (es_last_error has the text) */
   ES_ERR_NOMEM = -4,    /* device or host allocation failed, or max_device_bytes exceeded */
-  ES_ERR_TIMEOUT = -5,  /* a bounded wait ran out (produced only by fault injection: no kernel waits) */
+  ES_ERR_TIMEOUT = -5,  /* a kernel's bounded wait ran out (its error flag was set), or fault injection */
   ES_ERR_INTERNAL = -6, /* a self-check failed (e.g. a reconstruction bound) */
   ES_ERR_NODEVICE = -7  /* no CUDA device visible */
 } es_status;
@@ -68,6 +68,7 @@ typedef struct es_options {
 
 /* es_options.flags */
 #define ES_FLAG_HOST_RECON 1 /* reconstruct on the host even when the GPU numerator pass applies */
+#define ES_FLAG_STEP_LIFT 2  /* c == 1: run the lift as per-step kernels instead of the fused launch */
 
 /* Fault injection points (es_options.fault_stage): the named stage returns
  * the given status without running; used to test error propagation. */
@@ -117,14 +118,21 @@ es_status es_solution_export(const es_solution* s, uint64_t* num, uint64_t* den)
 es_status es_solution_phase_ms(const es_solution* s, double* ms, int32_t* m, int32_t* primes_used);
 
 /* Kernel accounting of the solve: launches = device kernels the library
- * launched for it; for the lift's per-prime product kernel (the B_j R_j
- * contraction, the dominant kernel of the lift): its launch count, the
- * summed CUDA-event duration of those launches in ms (only with
- * es_options.timing == 2, else 0), and its algorithmic bytes per launch
- * (B_j bytes of every good prime + residues read + residues written).
+ * launched for it; for the dominant kernel of the lift (named by
+ * es_solution_top_kernel): its launch count, the summed CUDA-event duration
+ * of those launches in ms (only with es_options.timing == 2, else 0), and
+ * its algorithmic bytes per launch:
+ *   k_lift_fused (c == 1, n <= 1024: all m steps in one launch):
+ *     m (E' n^2 + w_A n^2 + n (8 + E' + 48)), w_A = 4 or 8 bytes per entry of A
+ *   per-step product kernels (B_j R_j of every good prime):
+ *     E' (n^2 + 2 n c)
  * Any pointer may be NULL. */
 es_status es_solution_kernels(const es_solution* s, int64_t* launches, int64_t* top_launches, double* top_ms,
                               double* top_bytes_per_launch);
+
+/* Name of that dominant lift kernel ("k_lift_fused", "k_lift_gemv",
+ * "k_lift_gemm" or "k_lift_gemm_tc"); a static string, "" for NULL. */
+const char* es_solution_top_kernel(const es_solution* s);
 
 void es_solution_free(es_solution* s);
 

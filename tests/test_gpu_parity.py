@@ -201,6 +201,23 @@ def test_lift_full_size_by_residuals(torch_cuda, name, steps):
     check_lift_by_residuals(A, b, digits, good.cpu().numpy(), steps or m)
 
 
+@pytest.mark.parametrize("n,bits", [(1, 23), (2, 7), (152, 23), (153, 23), (300, 40), (1000, 23), (1024, 23)])
+def test_fused_lift_matches_step_kernels(torch_cuda, n, bits):
+    """c = 1 and n <= 1024 run the whole lift as one cooperative launch; the
+    per-step kernels (ES_FLAG_STEP_LIFT) are an independent route to the same
+    unique digits, so the canonical solutions agree bit for bit."""
+    A, b = inputs.uniform(n, 1, -(1 << bits), 1 << bits, seed=1000 + n)
+    At, bt = dev(torch_cuda, A), dev(torch_cuda, b)
+    fused = api.solve_device(At, bt, timing=2)
+    step = api.solve_device(At, bt, timing=2, step_lift=True)
+    assert fused.top_kernel == "k_lift_fused" and fused.top_launches == 1
+    assert step.top_kernel == "k_lift_gemv" and step.top_launches == step.m
+    assert fused.m == step.m and fused.top_ms > 0
+    assert (fused.N, fused.d) == (step.N, step.d)
+    if n <= 300:
+        check_identity(A, b, fused.N, fused.d)
+
+
 # ------------------------------------------------------------------ solve
 def n32_case(seed):
     with open(os.path.join(GOLDEN, "n32_attempts.json")) as f:
