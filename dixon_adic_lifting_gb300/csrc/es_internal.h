@@ -10,6 +10,8 @@
 
 namespace es {
 
+constexpr int kMaxDevices = 64;
+
 // ---------------------------------------------------------------- errors
 void set_last_error(const std::string& s);
 // Records the CUDA error (if any) and returns ES_ERR_CUDA / ES_OK.
@@ -90,6 +92,27 @@ struct KernelTiming {
 
 // Lift: m steps -> digits [m][n*c][6].
 size_t lift_scratch_bytes(int64_t n, int64_t c, int E, bool a32);
+// A lift in flight: run_lift_start enqueues every launch on the stream and
+// returns without waiting; run_lift_finish waits for it, reads the kernels'
+// error flag and fills the timing (the host is free in between).
+struct LiftRun {
+  void* stream = nullptr;
+  std::vector<void*> ev;  // cudaEvent_t pairs around each launch of the dominant kernel
+  int* err = nullptr;     // device error flag of the lift kernels
+  bool fused = false, tc = false, a32 = false;
+  int E = 0;
+  int64_t n = 0, c = 0;
+  int32_t m = 0;
+  KernelTiming* kt = nullptr;
+  LiftRun() = default;
+  LiftRun(const LiftRun&) = delete;
+  LiftRun& operator=(const LiftRun&) = delete;
+  ~LiftRun();  // destroys the events
+};
+es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
+                         const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                         void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run);
+es_status run_lift_finish(LiftRun* run);
 es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                    const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
                    void* stream, KernelTiming* kt = nullptr, bool allow_fused = true);
@@ -111,9 +134,14 @@ struct Solution {
 bool recon_device_applicable(int64_t n, int32_t m, const uint8_t* good, int64_t num_bits, int64_t den_bits,
                              const Stats& stats, int32_t* mp_out);
 size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t num_bits, int64_t den_bits);
-es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_t m, int32_t mp,
-                             const uint8_t* good, int64_t num_bits, int64_t den_bits, const Stats& stats,
-                             int threads, char* scratch, size_t scratch_bytes, void* stream, struct Solution* out);
+// Its digit-independent constants (P'^m, Q = P'^m', Q's reciprocal) are
+// built first, on the host, while the lift runs.
+struct ReconPlan;
+void recon_plan_free(ReconPlan* p);
+es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, const uint8_t* good, int64_t num_bits,
+                               int64_t den_bits, const Stats& stats, ReconPlan** out);
+es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads, char* scratch,
+                             size_t scratch_bytes, void* stream, struct Solution* out);
 
 // Host reconstruction (recon.cpp).  digits [m][n*c][6].
 es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,

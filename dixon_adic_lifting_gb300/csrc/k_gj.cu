@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <string>
 
 #include "es_common.cuh"
 #include "es_internal.h"
@@ -43,11 +44,13 @@ struct GJParams {
   int32_t* pinv;   // [53][n] inverse permutation
   uint8_t* used;   // [53][n] row already a pivot
   int32_t* bad;    // [53] prime divides det A
-  int8_t* UT;      // [53][ld][NBP] pivot rows' values, transposed, zero for a >= kb
+  int8_t* UT;      // [53][ld][utw] pivot rows' values, transposed, zero for a >= kb
+  int utw;         // bytes per U^T row (NB = 16: 16; NB = 32: 64, two panels side by side)
   int8_t* gpanel;  // [53][n][NBP] panel in global memory when shared memory is too small
 };
 
 __device__ __forceinline__ int32_t sbyte(uint32_t w, int u) { return (int32_t)(w << (24 - 8 * u)) >> 24; }
+
 
 // ------------------------------------------------------------------ panel
 template <int NBP>
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(1024) k_gj_panel(GJParams p, int64_t k0, int k
   if (use_smem)
     for (int64_t i = tid; i < n; i += blockDim.x) p.used[(int64_t)j * n + i] = usedS[i];
   // stage U^T (pivot rows outside the panel) and zero those entries in place
-  int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
+  int8_t* UTj = p.UT + (int64_t)j * ld * p.utw;
   for (int64_t idx = tid; idx < (int64_t)NBP * ld; idx += blockDim.x) {
     int a = (int)(idx / ld);
     int64_t col = idx - (int64_t)a * ld;
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(1024) k_gj_panel(GJParams p, int64_t k0, int k
       v = Wj[off];
       Wj[off] = 0;
     }
-    UTj[col * NBP + a] = v;
+    UTj[col * p.utw + a] = v;
   }
 }
 
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
   __syncthreads();
   // stage U^T (pivot rows outside the panel) and zero those entries in place:
   // thread = column; all kb loads are issued before any store
-  int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
+  int8_t* UTj = p.UT + (int64_t)j * ld * p.utw;
   for (int col = tid; col < ld; col += blockDim.x) {
     const bool outside = col < k0 || col >= k0 + kb;
     uint32_t w[NBP / 4];
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
     }
 #pragma unroll
     for (int c4 = 0; c4 < NBP / 16; ++c4)
-      *reinterpret_cast<int4*>(UTj + (int64_t)col * NBP + 16 * c4) =
+      *reinterpret_cast<int4*>(UTj + (int64_t)col * p.utw + 16 * c4) =
           make_int4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
     if (outside)
       for (int a = 0; a < kb; ++a) Wj[(int64_t)s_piv[a] * ld + col] = 0;
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, 
   }
   __syncthreads();
   // stage U^T (pivot rows outside the panel) and zero those entries in place
-  int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
+  int8_t* UTj = p.UT + (int64_t)j * ld * p.utw;
   for (int col = tid; col < ld; col += T) {
     const bool outside = col < k0 || col >= k0 + kb;
     uint32_t w[NBP / 4];
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, 
     }
 #pragma unroll
     for (int c4 = 0; c4 < NBP / 16; ++c4)
-      *reinterpret_cast<int4*>(UTj + (int64_t)col * NBP + 16 * c4) =
+      *reinterpret_cast<int4*>(UTj + (int64_t)col * p.utw + 16 * c4) =
           make_int4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
     if (outside)
       for (int aa = 0; aa < kb; ++aa) Wj[(int64_t)s_piv[aa] * ld + col] = 0;
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
   const int64_t n = p.n, ld = p.ld;
   const int64_t row0 = (int64_t)blockIdx.y * 64, col0 = (int64_t)blockIdx.x * 128;
   int8_t* Wj = p.W + (int64_t)j * n * ld;
-  const int8_t* UTj = p.UT + (int64_t)j * ld * NBP;
+  const int8_t* UTj = p.UT + (int64_t)j * ld * p.utw;
   constexpr int KW = NBP / 4;  // 32-bit words along the panel
   __shared__ int32_t Fs[64][KW + 1];
   __shared__ int32_t Us[128][KW + 1];
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
     int cc = idx / (NBP / 16), cch = idx % (NBP / 16);
     int64_t col = col0 + cc;
     int4 v = make_int4(0, 0, 0, 0);
-    if (col < ld) v = *reinterpret_cast<const int4*>(UTj + col * NBP + 16 * cch);
+    if (col < ld) v = *reinterpret_cast<const int4*>(UTj + col * p.utw + 16 * cch);
     Us[cc][cch * 4 + 0] = v.x;
     Us[cc][cch * 4 + 1] = v.y;
     Us[cc][cch * 4 + 2] = v.z;
@@ -573,14 +576,17 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
   }
 }
 
-// Update on the int8 tensor-core path (NB = 32): the depth-32 contraction
-// F U is exactly one mma.sync.m16n8k32 (s8 x s8 -> s32) per 16 x 8 output
-// tile.  F rows are contiguous in W and U is staged transposed, so both
-// fragments are 32-bit loads straight from memory: A (row-major 16 x 32) reg r
-// holds row g + 8 (r & 1), columns 4 t + 16 (r >> 1) + 0..3; B (column-major
-// 32 x 8) reg r holds column g, rows 4 t + 16 r + 0..3; C reg r holds row
+// Update on the int8 tensor-core path: the depth-KW contraction F U (KW = 32
+// or 64) is KW / 32 mma.sync.m16n8k32 (s8 x s8 -> s32) per 16 x 8 output
+// tile.  F = W[:, k0 .. k0 + KW) is read straight from W and U^T (row width
+// utw bytes, U^T[col][a] = pivot row a's entry of column col) from the staging
+// buffer, both as 32-bit fragment loads: A (row-major 16 x 32) reg r holds row
+// g + 8 (r & 1), columns 4 t + 16 (r >> 1) + 0..3; B (column-major 32 x 8)
+// reg r holds column g, rows 4 t + 16 r + 0..3; C reg r holds row
 // g + 8 (r >> 1), column 2 t + (r & 1)  (g = lane / 4, t = lane % 4).
-// CTA tile 64 rows x 128 columns, 8 warps of 32 x 32.
+// KW = 64 is exact too: 64 * 125^2 + 125 < 2^31.  CTA tile 64 rows x 128
+// columns, 8 warps of 32 x 32.  Columns updated: 32-column segments col0 with
+// cbase <= col0 < cend outside [k0, k0 + KW).
 __device__ __forceinline__ void mma_s8_16x8x32(int32_t (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(
       "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -591,52 +597,59 @@ __device__ __forceinline__ void mma_s8_16x8x32(int32_t (&c)[4], const uint32_t (
 
 __device__ __forceinline__ int rot3(int r) { return ((r << 1) | ((r >> 2) & 1)) & 7; }
 
-__global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, int64_t k0, int kb) {
+template <int KW>
+__global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, const int8_t* __restrict__ UT, int utw,
+                                                       int64_t k0, int64_t cbase, int64_t cend) {
   const int j = blockIdx.z;
   if (p.bad[j]) return;
   const ModQ m = c_modq.v[j];
   const int64_t n = p.n, ld = p.ld;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
   const int64_t row0 = (int64_t)blockIdx.y * 64 + (warp >> 2) * 32;
-  const int64_t col0 = (int64_t)blockIdx.x * 128 + (warp & 3) * 32;
+  const int64_t col0 = cbase + (int64_t)blockIdx.x * 128 + (warp & 3) * 32;
   int8_t* Wj = p.W + (int64_t)j * n * ld;
-  const int8_t* UTj = p.UT + (int64_t)j * ld * 32;
+  const int8_t* UTj = UT + (int64_t)j * ld * utw;
   // per warp: its 32 x 32 tile of F U.  Within a row the 16-byte chunk c is
   // stored at chunk c ^ rot(row) (rot = 3-bit left rotation of row & 7), which
   // makes both the 8-byte fragment stores (per half-warp) and the 16-byte row
   // reads (per quarter-warp) hit 32 distinct banks.
   __shared__ __align__(16) int32_t Cs[8][32][32];
-  // this thread's output row segment (row0 + lane, 32 columns), fetched early
+  // this thread's output row segment (row0 + lane, 32 columns), fetched early;
+  // segments are 32-column aligned like the panel: one either lies in it or misses it
   const int64_t orow = row0 + lane;
-  // segments are 32-column aligned like the panel: one either is the panel or misses it
-  const bool rowok = orow < n && col0 < ld && col0 != k0;
+  const bool rowok = orow < n && col0 < ld && col0 < cend && (col0 < k0 || col0 >= k0 + KW);
   int4 old0 = make_int4(0, 0, 0, 0), old1 = old0;
   if (rowok) {
     old0 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0);
     if (col0 + 16 < ld) old1 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0 + 16);
   }
-  uint32_t a[2][4], b[4][2];
+  uint32_t a[KW / 32][2][4], b[KW / 32][4][2];
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
+  for (int kk = 0; kk < KW / 32; ++kk) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int64_t row = row0 + 16 * mi + g + 8 * (r & 1);
-      const int64_t col = k0 + 4 * t + 16 * (r >> 1);
-      a[mi][r] = (row < n && col < ld) ? *reinterpret_cast<const uint32_t*>(Wj + row * ld + col) : 0u;
-    }
+    for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-  for (int ni = 0; ni < 4; ++ni)
+      for (int r = 0; r < 4; ++r) {
+        const int64_t row = row0 + 16 * mi + g + 8 * (r & 1);
+        const int64_t col = k0 + 32 * kk + 4 * t + 16 * (r >> 1);
+        a[kk][mi][r] = (row < n && col < ld) ? *reinterpret_cast<const uint32_t*>(Wj + row * ld + col) : 0u;
+      }
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int64_t col = col0 + 8 * ni + g;
-      b[ni][r] = col < ld ? *reinterpret_cast<const uint32_t*>(UTj + col * 32 + 4 * t + 16 * r) : 0u;
-    }
+    for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int64_t col = col0 + 8 * ni + g;
+        b[kk][ni][r] =
+            col < ld ? *reinterpret_cast<const uint32_t*>(UTj + col * utw + 32 * kk + 4 * t + 16 * r) : 0u;
+      }
+  }
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
     for (int ni = 0; ni < 4; ++ni) {
       int32_t c[4] = {0, 0, 0, 0};
-      mma_s8_16x8x32(c, a[mi], b[ni]);
+#pragma unroll
+      for (int kk = 0; kk < KW / 32; ++kk) mma_s8_16x8x32(c, a[kk][mi], b[kk][ni]);
       const int cw = 8 * ni + 2 * t, sw = (4 * ((cw >> 2) ^ rot3(g))) | (cw & 3);  // rows g, g + 8: same rot
       *reinterpret_cast<int2*>(&Cs[warp][16 * mi + g][sw]) = make_int2(c[0], c[1]);
       *reinterpret_cast<int2*>(&Cs[warp][16 * mi + g + 8][sw]) = make_int2(c[2], c[3]);
@@ -723,7 +736,7 @@ InvLayout inverse_layout(int64_t n) {
   Layout L;
   InvLayout r;
   r.W = L.add((size_t)kNumPrimes * n * ld);
-  r.UT = L.add((size_t)kNumPrimes * ld * nbp);
+  r.UT = L.add((size_t)kNumPrimes * ld * (nbp == 32 ? 64 : nbp));  // NB = 32: two panels' U^T side by side
   r.piv = L.add((size_t)kNumPrimes * n * 4);
   r.pinv = L.add((size_t)kNumPrimes * n * 4);
   r.used = L.add((size_t)kNumPrimes * n);
@@ -733,30 +746,81 @@ InvLayout inverse_layout(int64_t n) {
   return r;
 }
 
+// One NB-column panel: pivots, multipliers, and the pivot rows of every other
+// column staged into U^T (at gp.UT, rows of gp.utw bytes) and zeroed in W.
 template <int NBP>
-es_status run_blocks(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) {
-  size_t smem = use_smem ? (size_t)n * NBP + (size_t)n : 0;
-  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_gj_panel<NBP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+void panel(GJParams& gp, int64_t n, int64_t k0, int kb, bool use_smem, cudaStream_t st) {
+  const bool reg_panel = NBP == 32 && n <= 1024;  // one row per thread, panel in registers
+  if (reg_panel && n <= 256)
+    k_gj_panel_rows<NBP, 1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
+  else if (reg_panel && n <= 512)
+    k_gj_panel_rows<NBP, 2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
+  else if (reg_panel)
+    k_gj_panel_rows<NBP, 2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb);
+  else
+    k_gj_panel<NBP><<<kNumPrimes, 1024, use_smem ? (size_t)n * NBP + (size_t)n : 0, st>>>(gp, k0, kb,
+                                                                                       use_smem ? 1 : 0);
+  count_launch();
+}
+
+// NB = 16: panel, then the dp4a update of every other column.
+es_status run_blocks16(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) {
+  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_gj_panel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)kPanelSmemLimit + 1024),
                        "panel smem attribute"));
-  dim3 ugrid((unsigned)((gp.ld + 127) / 128), (unsigned)((n + 63) / 64), kNumPrimes);
-  const bool reg_panel = NBP == 32 && n <= 1024;  // one row per thread, panel in registers
-  for (int64_t k0 = 0; k0 < n; k0 += NBP) {
-    int kb = (int)((n - k0) < NBP ? (n - k0) : NBP);
-    if (reg_panel && n <= 256)
-      k_gj_panel_rows<NBP, 1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
-    else if (reg_panel && n <= 512)
-      k_gj_panel_rows<NBP, 2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
-    else if (reg_panel)
-      k_gj_panel_rows<NBP, 2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb);
-    else
-      k_gj_panel<NBP><<<kNumPrimes, 1024, smem, st>>>(gp, k0, kb, use_smem ? 1 : 0);
-    if (NBP == 32)
-      k_gj_update_mma<<<ugrid, 256, 0, st>>>(gp, k0, kb);
-    else
-      k_gj_update<NBP><<<ugrid, 256, 0, st>>>(gp, k0, kb);
-    count_launch(2);
+  gp.utw = 16;
+  const dim3 ugrid((unsigned)((gp.ld + 127) / 128), (unsigned)((n + 63) / 64), kNumPrimes);
+  for (int64_t k0 = 0; k0 < n; k0 += 16) {
+    const int kb = (int)((n - k0) < 16 ? (n - k0) : 16);
+    panel<16>(gp, n, k0, kb, use_smem, st);
+    k_gj_update<16><<<ugrid, 256, 0, st>>>(gp, k0, kb);
+    count_launch();
   }
+  return cuda_status(cudaGetLastError(), "gauss-jordan blocks");
+}
+
+// NB = 32 panels in blocks of 64 columns.  The exchange steps of a block act
+// on every column t outside it as W_t <- W_t[R -> 0] + F W_t[R] (R = the
+// block's 64 pivot rows in order, F = the block's 64 columns after all its
+// steps; by induction over the steps, since each step is
+// I - e_p e_p^T + f e_p^T), so inside the block the two panels update each
+// other's 32 columns, and every other column gets ONE depth-64 update:
+//   panel k0        -> U^T[:, 0..32)   (pivot rows R1, all columns, zeroed)
+//   update [k0+32, k0+64) by F1 U1
+//   panel k0 + 32   -> U^T[:, 32..64)  (pivot rows R2, all columns, zeroed)
+//   update [k0, k0+32) by F2 U2
+//   update every column outside [k0, k0+64) by W[:, k0..k0+64) U^T
+// R2's entries outside the block are staged before any update reached them,
+// as the formula needs.  The number of full passes over W halves.
+es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) {
+  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_gj_panel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kPanelSmemLimit + 1024),
+                       "panel smem attribute"));
+  int8_t* const UT = gp.UT;
+  const int64_t ld = gp.ld;
+  const unsigned rtiles = (unsigned)((n + 63) / 64);
+  const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
+  gp.utw = 64;
+  for (int64_t k0 = 0; k0 < n; k0 += 64) {
+    const int kb1 = (int)((n - k0) < 32 ? (n - k0) : 32);
+    const int64_t k1 = k0 + 32;
+    const bool two = k1 < n;
+    gp.UT = UT;
+    panel<32>(gp, n, k0, kb1, use_smem, st);
+    if (two) {
+      const int kb2 = (int)((n - k1) < 32 ? (n - k1) : 32);
+      k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT, 64, k0, k1, k1 + 32);
+      gp.UT = UT + 32;
+      panel<32>(gp, n, k1, kb2, use_smem, st);
+      k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT + 32, 64, k1, k0, k0 + 32);
+      k_gj_update_mma<64><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+      count_launch(3);
+    } else {
+      k_gj_update_mma<32><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+      count_launch();
+    }
+  }
+  gp.UT = UT;
   return cuda_status(cudaGetLastError(), "gauss-jordan blocks");
 }
 }  // namespace
@@ -774,6 +838,7 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
   gp.ld = padded_ld(n);
   gp.W = reinterpret_cast<int8_t*>(scratch + L.W);
   gp.UT = reinterpret_cast<int8_t*>(scratch + L.UT);
+  gp.utw = nbp;
   gp.piv = reinterpret_cast<int32_t*>(scratch + L.piv);
   gp.pinv = reinterpret_cast<int32_t*>(scratch + L.pinv);
   gp.used = reinterpret_cast<uint8_t*>(scratch + L.used);
@@ -783,9 +848,9 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
   ES_CHECK(cuda_status(cudaMemsetAsync(gp.bad, 0, (size_t)kNumPrimes * 4, st), "memset bad"));
   ES_CHECK(launch_residues_matrix(A_dev, n, gp.ld, gp.W, st));
   if (nbp == 32)
-    ES_CHECK(run_blocks<32>(gp, n, use_smem, st));
+    ES_CHECK(run_blocks64(gp, n, use_smem, st));
   else
-    ES_CHECK(run_blocks<16>(gp, n, use_smem, st));
+    ES_CHECK(run_blocks16(gp, n, use_smem, st));
   k_gj_pinv<<<dim3((unsigned)((n + 255) / 256), kNumPrimes), 256, 0, st>>>(gp);
   count_launch(2);  // pinv + permute
   ES_CHECK(cuda_status(cudaGetLastError(), "k_gj_pinv"));

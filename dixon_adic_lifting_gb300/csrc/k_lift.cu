@@ -510,9 +510,28 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
 
 size_t lift_scratch_bytes(int64_t n, int64_t c, int E, bool a32) { return lift_layout(n, c, E, a32).total; }
 
-es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
-                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
-                   void* stream, KernelTiming* kt, bool allow_fused) {
+LiftRun::~LiftRun() {
+  for (void* e : ev)
+    if (e) cudaEventDestroy((cudaEvent_t)e);
+}
+
+namespace {
+es_status create_events(LiftRun* run, size_t count) {
+  for (void* e : run->ev)
+    if (e) cudaEventDestroy((cudaEvent_t)e);
+  run->ev.assign(count, nullptr);
+  for (auto& e : run->ev) {
+    cudaEvent_t x = nullptr;
+    ES_CHECK(cuda_status(cudaEventCreate(&x), "event create"));
+    e = x;
+  }
+  return ES_OK;
+}
+}  // namespace
+
+es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
+                         const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                         void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run) {
   cudaStream_t st = (cudaStream_t)stream;
   LiftConst hK;
   build_lift_const(good_host, &hK);
@@ -556,36 +575,29 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
   k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R);
   ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_init"));
   count_launch(a32 ? 2 : 1);
-  std::vector<cudaEvent_t> ev;
-  if (kt && kt->events) {
-    ev.resize(fused ? 2 : 2 * (size_t)m);
-    for (auto& e : ev) ES_CHECK(cuda_status(cudaEventCreate(&e), "event create"));
-  }
+  run->stream = stream;
+  run->kt = kt;
+  if (kt && kt->events) ES_CHECK(create_events(run, fused ? 2 : 2 * (size_t)m));
+  auto ev = [&](size_t i) { return (cudaEvent_t)run->ev[i]; };
   if (fused) {
     ES_CHECK(fused_lift_relayout(fp, B_dev, K, Bf, n, st));
     count_launch();
-    if (!ev.empty()) cudaEventRecord(ev[0], st);
+    if (!run->ev.empty()) cudaEventRecord(ev(0), st);
     es_status fs = fused_lift_launch(fp, Bf, A32, a32 ? nullptr : A_dev, b_dev, K, R, xl, digits_dev, bar, err,
                                      n, E, m, st);
     if (fs == ES_OK) {
-      if (!ev.empty()) cudaEventRecord(ev[1], st);
+      if (!run->ev.empty()) cudaEventRecord(ev(1), st);
       count_launch();
     } else if (fs == ES_ERR_RANGE) {
       fused = false;  // co-residency refused: per-step kernels below
-      for (auto& e : ev) cudaEventDestroy(e);
-      ev.clear();
-      if (kt && kt->events) {
-        ev.resize(2 * (size_t)m);
-        for (auto& e : ev) ES_CHECK(cuda_status(cudaEventCreate(&e), "event create"));
-      }
+      if (kt && kt->events) ES_CHECK(create_events(run, 2 * (size_t)m));
     } else {
-      for (auto& e : ev) cudaEventDestroy(e);
       return fs;
     }
   }
   for (int32_t i = 0; i < m && !fused; ++i) {
     if (tc) ES_CHECK(tc_convert_f16(R, R16, (int64_t)E * c * ld, st));
-    if (!ev.empty()) cudaEventRecord(ev[2 * i], st);
+    if (!run->ev.empty()) cudaEventRecord(ev(2 * i), st);
     if (c == 1) {
       k_lift_gemv<4><<<dim3((unsigned)((n + 31) / 32), E), 256, 0, st>>>(B_dev, R, n, ld, K, V);
       count_launch();
@@ -596,7 +608,7 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
                                                                                                 ld, K, V);
       count_launch();
     }
-    if (!ev.empty()) cudaEventRecord(ev[2 * i + 1], st);
+    if (!run->ev.empty()) cudaEventRecord(ev(2 * i + 1), st);
     count_launch();
     if (nc >= kCrtThreadMin)
       k_lift_crt_thread<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
@@ -624,9 +636,23 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
     }
   }
   ES_CHECK(cuda_status(cudaGetLastError(), "lift steps"));
+  run->err = err;
+  run->fused = fused;
+  run->tc = tc;
+  run->a32 = a32;
+  run->E = E;
+  run->n = n;
+  run->c = c;
+  run->m = m;
+  return ES_OK;
+}
+
+es_status run_lift_finish(LiftRun* run) {
+  cudaStream_t st = (cudaStream_t)run->stream;
   int herr = 0;
-  ES_CHECK(cuda_status(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st), "lift err D2H"));
+  ES_CHECK(cuda_status(cudaMemcpyAsync(&herr, run->err, sizeof(int), cudaMemcpyDeviceToHost, st), "lift err D2H"));
   es_status sst = cuda_status(cudaStreamSynchronize(st), "lift sync");
+  const bool fused = run->fused;
   if (sst == ES_OK && herr == kFusedErrDigit) {
     set_last_error("fused lift kernel: the short-path digit disagreed with the full digit");
     sst = ES_ERR_INTERNAL;
@@ -635,23 +661,33 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
                    ": bounded wait expired (code " + std::to_string(herr) + ")");
     sst = ES_ERR_TIMEOUT;
   }
-  if (kt) {
-    kt->launches += fused ? 1 : m;
+  if (KernelTiming* kt = run->kt) {
+    const int64_t n = run->n, c = run->c;
+    const int E = run->E;
+    kt->launches += fused ? 1 : run->m;
     // algorithmic bytes: per step E' n^2 of B, w_A n^2 of A and n (8 + E' + 48)
     // for the residual, its residues and the digit (fused: all m steps);
     // per-step product kernels: E' (n^2 + 2 n c)
     const double nn = (double)n * (double)n;
-    kt->bytes_per_launch = fused ? (double)m * (E * nn + (a32 ? 4.0 : 8.0) * nn + (double)n * (8.0 + E + 48.0))
+    kt->bytes_per_launch = fused ? (double)run->m * (E * nn + (run->a32 ? 4.0 : 8.0) * nn + (double)n * (8.0 + E + 48.0))
                                  : (double)E * (nn + 2.0 * (double)n * (double)c);
     kt->fused = fused;
-    kt->name = fused ? "k_lift_fused" : c == 1 ? "k_lift_gemv" : tc ? "k_lift_gemm_tc" : "k_lift_gemm";
-    for (int32_t i = 0; i < (int32_t)ev.size() / 2; ++i) {
+    kt->name = fused ? "k_lift_fused" : c == 1 ? "k_lift_gemv" : run->tc ? "k_lift_gemm_tc" : "k_lift_gemm";
+    for (size_t i = 0; i + 1 < run->ev.size(); i += 2) {
       float ms = 0.f;
-      if (cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]) == cudaSuccess) kt->ms += ms;
+      if (cudaEventElapsedTime(&ms, (cudaEvent_t)run->ev[i], (cudaEvent_t)run->ev[i + 1]) == cudaSuccess) kt->ms += ms;
     }
   }
-  for (auto& e : ev) cudaEventDestroy(e);
   return sst;
+}
+
+es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
+                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                   void* stream, KernelTiming* kt, bool allow_fused) {
+  LiftRun run;
+  ES_CHECK(run_lift_start(A_dev, b_dev, n, c, B_dev, good_host, m, digits_dev, a32, scratch, stream, kt,
+                          allow_fused, &run));
+  return run_lift_finish(&run);
 }
 
 }  // namespace es

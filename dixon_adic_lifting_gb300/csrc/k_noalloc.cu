@@ -25,9 +25,10 @@
 namespace es {
 
 // Working memory for n <= kNoAllocMaxN: inverse_scratch_bytes(256) is
-// 4,029,952 bytes (W 3.47 MB, U^T 0.43 MB, pivots 0.11 MB, flags).
+// 4,464,128 bytes (W 3.47 MB, U^T of two panels 0.87 MB, pivots 0.11 MB,
+// flags).
 constexpr int64_t kNoAllocMaxN = 256;
-constexpr size_t kNoAllocScratchBytes = size_t(4352) << 10;  // 4.25 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(4608) << 10;  // 4.5 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -24,6 +24,9 @@
 // is balanced and |N| <= 2^num_bits is tested.
 #include <cuda_runtime.h>
 
+#include <memory>
+#include <new>
+
 #include <algorithm>
 #include <cstring>
 #include <vector>
@@ -272,24 +275,164 @@ size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t n
   return L.total;
 }
 
-es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_t m, int32_t mp,
-                             const uint8_t* good, int64_t num_bits, int64_t den_bits, const Stats& stats,
-                             int threads, char* scratch, size_t scratch_bytes, void* stream, Solution* out) {
-  cudaStream_t st = (cudaStream_t)stream;
-  const int64_t nc = n * c;
-  const PrimeSet ps = make_prime_set(good);
-  if (ps.E == 0) return ES_ERR_ARG;
-  const Nat M = pow_nat(ps.P, m);
-  if (big::le_pow2(M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
-  const Nat Mhalf = big::shr(big::sub(M, big::from_u64(1)), 1);
-  const Nat Mhalf1 = big::add(Mhalf, big::from_u64(1));
+// G_{i+1} = G_i P' mod Q for i < mp, written as LG 32-bit words each, and
+// their sum.  Knuth's division with the divisor normalised once: G is kept
+// shifted left by the normalising shift s, so each step is one multiply by
+// the 6-limb P' and a division whose quotient has at most 6 limbs, in place.
+static void g_chain(const Nat& Q, const Nat& P, const Nat& g0, int32_t mp, int64_t LG, uint32_t* out, Nat* sum) {
+  using limb = big::limb;
+  using u128 = unsigned __int128;
+  const size_t n = Q.size(), pn = P.size();
+  const int s = __builtin_clzll(Q.back());
+  std::vector<limb> qn(n), g(n + 1, 0), t(n + pn + 1, 0), plain(n);
+  for (size_t i = n - 1; i > 0; --i) qn[i] = (Q[i] << s) | (s ? Q[i - 1] >> (64 - s) : 0);
+  qn[0] = Q[0] << s;
+  // g = g0 << s (g0 < Q, so it fits in n limbs)
+  for (size_t i = 0; i < n; ++i) {
+    const limb lo = i < g0.size() ? g0[i] : 0, below = (i > 0 && i - 1 < g0.size()) ? g0[i - 1] : 0;
+    g[i] = (lo << s) | (s && i > 0 ? below >> (64 - s) : 0);
+  }
+  const limb vtop = qn[n - 1], vsec = n > 1 ? qn[n - 2] : 0;
+  sum->clear();
+  for (int32_t i = 0; i < mp; ++i) {
+    // output G_i = g >> s
+    for (size_t l = 0; l < n; ++l) plain[l] = (g[l] >> s) | (s && l + 1 < n ? g[l + 1] << (64 - s) : 0);
+    Nat gi(plain.begin(), plain.end());
+    big::trim(gi);
+    for (int64_t w = 0; w < LG; ++w) {
+      const size_t l = (size_t)w / 2;
+      out[(size_t)i * LG + w] = l < n ? (uint32_t)(plain[l] >> (32 * (w & 1))) : 0u;
+    }
+    big::add_in(*sum, gi);
+    if (i + 1 == mp) break;
+    // t = g P (n + pn limbs), then t mod qn -> g
+    std::fill(t.begin(), t.end(), 0);
+    for (size_t a = 0; a < pn; ++a) {
+      limb carry = 0;
+      for (size_t b = 0; b < n; ++b) {
+        const u128 pr = (u128)P[a] * g[b] + t[a + b] + carry;
+        t[a + b] = (limb)pr;
+        carry = (limb)(pr >> 64);
+      }
+      t[a + n] = carry;
+    }
+    for (ptrdiff_t j = (ptrdiff_t)pn; j >= 0; --j) {
+      if (j + n >= t.size()) continue;
+      const u128 num = ((u128)t[j + n] << 64) | t[j + n - 1];
+      u128 qhat = num / vtop, rhat = num % vtop;
+      while ((qhat >> 64) != 0 || (n > 1 && qhat * vsec > ((rhat << 64) | t[j + n - 2]))) {
+        qhat -= 1;
+        rhat += vtop;
+        if ((rhat >> 64) != 0) break;
+      }
+      if (qhat == 0) continue;
+      limb borrow = 0, carry = 0;
+      const limb qh = (limb)qhat;
+      for (size_t b = 0; b < n; ++b) {
+        const u128 pr = (u128)qh * qn[b] + carry;
+        carry = (limb)(pr >> 64);
+        const limb pl = (limb)pr, x = t[b + j];
+        const limb t1 = x - pl, b1 = x < pl;
+        const limb t2 = t1 - borrow, b2 = t1 < borrow;
+        t[b + j] = t2;
+        borrow = b1 | b2;
+      }
+      const limb x = t[j + n];
+      const limb t1 = x - carry, b1 = x < carry;
+      const limb t2 = t1 - borrow, b2 = t1 < borrow;
+      t[j + n] = t2;
+      if (b1 | b2) {  // went negative: add back once
+        limb c = 0;
+        for (size_t b = 0; b < n; ++b) {
+          const u128 sm = (u128)t[b + j] + qn[b] + c;
+          t[b + j] = (limb)sm;
+          c = (limb)(sm >> 64);
+        }
+        t[j + n] += c;
+      }
+    }
+    for (size_t l = 0; l < n; ++l) g[l] = t[l];
+    g[n] = 0;
+  }
+}
+
+// The digit-independent part of the device reconstruction: P'^m, Q = P'^m',
+// the reciprocal and word images of Q, sizes and offsets.  Built on the host
+// while the lift runs.
+struct ReconPlan {
+  int64_t n = 0, c = 0, nc = 0, num_bits = 0, den_bits = 0;
+  int32_t m = 0, mp = 0;
+  PrimeSet ps;
+  Nat M, Mhalf, Mhalf1, Q;
+  int64_t LG = 0, W = 0;
+  size_t oG = 0, oC = 0, oM = 0, oN = 0, oK = 0, total = 0;
+  std::vector<uint32_t> hC, hM;
+  int dyn = 0;
+};
+
+void recon_plan_free(ReconPlan* p) { delete p; }
+
+es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, const uint8_t* good, int64_t num_bits,
+                               int64_t den_bits, const Stats& stats, ReconPlan** out) {
+  *out = nullptr;
+  std::unique_ptr<ReconPlan> rp(new (std::nothrow) ReconPlan);
+  if (!rp) return ES_ERR_NOMEM;
+  ReconPlan& R = *rp;
+  R.n = n;
+  R.c = c;
+  R.nc = n * c;
+  R.m = m;
+  R.mp = mp;
+  R.num_bits = num_bits;
+  R.den_bits = den_bits;
+  R.ps = make_prime_set(good);
+  if (R.ps.E == 0) return ES_ERR_ARG;
+  R.M = pow_nat(R.ps.P, m);
+  if (big::le_pow2(R.M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
+  R.Mhalf = big::shr(big::sub(R.M, big::from_u64(1)), 1);
+  R.Mhalf1 = big::add(R.Mhalf, big::from_u64(1));
   // exact check of the low-digit certificate's modulus
-  const Nat Q = pow_nat(ps.P, mp);
+  R.Q = pow_nat(R.ps.P, mp);
   {
     const int64_t na = u64_bitlen((uint64_t)n * stats.max_abs_a);
     const int64_t need = std::max(num_bits + na, den_bits + u64_bitlen(stats.max_abs_b)) + 2;
-    if (big::le_pow2(Q, (size_t)need)) return ES_ERR_INTERNAL;
+    if (big::le_pow2(R.Q, (size_t)need)) return ES_ERR_INTERNAL;
   }
+  const Nat& Q = R.Q;
+  const int64_t LG = (int64_t)((big::bitlen(Q) + 31) / 32);
+  const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
+  R.LG = LG;
+  R.W = W0 > W1 ? W0 : W1;
+  Layout L;
+  R.oG = L.add((size_t)mp * LG * 4);
+  R.oC = L.add((size_t)LG * 4 * 3);
+  R.oM = L.add(kMuWords * 4 + kDigitWords * 4);
+  R.oN = L.add((size_t)R.nc * R.W * 8);
+  R.oK = L.add((size_t)R.nc);
+  R.total = L.total;
+  R.hC.assign((size_t)LG * 3, 0);
+  R.hM.assign(kMuWords + kDigitWords, 0);
+  const Nat Qhalf = big::shr(big::sub(Q, big::from_u64(1)), 1);
+  to_words(Q, LG, R.hC.data() + LG);
+  to_words(Qhalf, LG, R.hC.data() + 2 * LG);
+  Nat mu;
+  big::divmod(big::shl(big::from_u64(1), (size_t)(32 * (LG - 1 + kMuWords))), Q, &mu, nullptr);
+  if ((int64_t)((big::bitlen(mu) + 31) / 32) > kMuWords) return ES_ERR_INTERNAL;
+  to_words(mu, kMuWords, R.hM.data());
+  to_words(R.ps.half, kDigitWords, R.hM.data() + kMuWords);
+  R.dyn = (int)((3 * (LG + kZExtra + 1)) * 4 + (LG + kZExtra + 1) * 4 + (size_t)mp * kDigitWords * 4);
+  *out = rp.release();
+  return ES_OK;
+}
+
+es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads, char* scratch,
+                             size_t scratch_bytes, void* stream, Solution* out) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const ReconPlan& R = *plan;
+  const int64_t n = R.n, c = R.c, nc = R.nc, num_bits = R.num_bits, den_bits = R.den_bits;
+  const int32_t m = R.m, mp = R.mp;
+  const PrimeSet& ps = R.ps;
+  const Nat &M = R.M, &Mhalf = R.Mhalf, &Mhalf1 = R.Mhalf1, &Q = R.Q;
   // components' full digits -> residues mod M -> denominators (host threads)
   auto denominators = [&](const std::vector<int64_t>& ks, std::vector<Nat>* dens) -> es_status {
     std::vector<uint64_t> hd(ks.size() * (size_t)m * kDigitLimbs);
@@ -317,25 +460,13 @@ es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_
   for (auto& v : sden) lcm_in(d, v);
 
   // device constants that do not depend on d
-  const int64_t LG = (int64_t)((big::bitlen(Q) + 31) / 32);
-  const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
-  const int64_t W = W0 > W1 ? W0 : W1;
-  Layout L;
-  const size_t oG = L.add((size_t)mp * LG * 4), oC = L.add((size_t)LG * 4 * 3),
-               oM = L.add(kMuWords * 4 + kDigitWords * 4), oN = L.add((size_t)nc * W * 8), oK = L.add((size_t)nc);
-  if (L.total > scratch_bytes) return ES_ERR_INTERNAL;
-  std::vector<uint32_t> hC((size_t)LG * 3), hM(kMuWords + kDigitWords);
-  const Nat Qhalf = big::shr(big::sub(Q, big::from_u64(1)), 1);
-  to_words(Q, LG, hC.data() + LG);
-  to_words(Qhalf, LG, hC.data() + 2 * LG);
-  Nat mu;
-  big::divmod(big::shl(big::from_u64(1), (size_t)(32 * (LG - 1 + kMuWords))), Q, &mu, nullptr);
-  if ((int64_t)((big::bitlen(mu) + 31) / 32) > kMuWords) return ES_ERR_INTERNAL;
-  to_words(mu, kMuWords, hM.data());
-  to_words(ps.half, kDigitWords, hM.data() + kMuWords);
-  ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oM, hM.data(), hM.size() * 4, cudaMemcpyHostToDevice, st),
+  const int64_t LG = R.LG, W = R.W;
+  const size_t oG = R.oG, oC = R.oC, oM = R.oM, oN = R.oN, oK = R.oK;
+  if (R.total > scratch_bytes) return ES_ERR_INTERNAL;
+  std::vector<uint32_t> hC = R.hC;
+  ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oM, R.hM.data(), R.hM.size() * 4, cudaMemcpyHostToDevice, st),
                        "recon constants H2D"));
-  const int dyn = (int)((3 * (LG + kZExtra + 1)) * 4 + (LG + kZExtra + 1) * 4 + (size_t)mp * kDigitWords * 4);
+  const int dyn = R.dyn;
   if (dyn > 48 * 1024)
     ES_CHECK(cuda_status(cudaFuncSetAttribute(k_recon_numerators, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn),
                          "recon smem attribute"));
@@ -350,14 +481,7 @@ es_status reconstruct_device(const uint64_t* D_dev, int64_t n, int64_t c, int32_
     // G_i = d P'^i mod Q, OFF = Q - ((P'-1)/2 sum_i G_i mod Q)
     Nat g, sum, rem;
     big::divmod(d, Q, nullptr, &g);
-    for (int32_t i = 0; i < mp; ++i) {
-      to_words(g, LG, hG.data() + (size_t)i * LG);
-      big::add_in(sum, g);
-      if (i + 1 < mp) {
-        Nat t = big::mul(g, ps.P);
-        big::divmod(t, Q, nullptr, &g);
-      }
-    }
+    g_chain(Q, ps.P, g, mp, LG, hG.data(), &sum);
     big::divmod(big::mul(sum, ps.half), Q, nullptr, &rem);
     const Nat off = rem.empty() ? Nat{} : big::sub(Q, rem);
     to_words(off, LG, hC.data());

@@ -10,6 +10,7 @@
 #include <atomic>
 #include <chrono>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <new>
 #include <string>
@@ -36,7 +37,6 @@ int64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 // ------------------------------------------------------------ per-device state
 namespace {
-constexpr int kMaxDevices = 64;
 struct DeviceState {
   std::mutex mu;
   char* ws = nullptr;
@@ -252,7 +252,22 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   const bool a32 = stats.max_abs_a < (uint64_t(1) << 31);
   KernelTiming kt;
   kt.events = o.kernel_events;
-  ES_CHECK(run_lift(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt, !o.step_lift));
+  int32_t mp = 0;
+  const bool on_device = !o.host_recon && recon_device_applicable(n, m, good, num_bits, den_bits, stats, &mp);
+  std::unique_ptr<ReconPlan, void (*)(ReconPlan*)> rplan(nullptr, recon_plan_free);
+  {
+    LiftRun lr;
+    ES_CHECK(run_lift_start(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt, !o.step_lift, &lr));
+    // while the GPU lifts: the reconstruction's digit-independent constants
+    es_status ps = ES_OK;
+    if (on_device) {
+      ReconPlan* rp = nullptr;
+      ps = recon_device_prepare(n, c, m, mp, good, num_bits, den_bits, stats, &rp);
+      rplan.reset(rp);
+    }
+    ES_CHECK(run_lift_finish(&lr));
+    ES_CHECK(ps);
+  }
   tm.mark(3);
   if (o.fault == ES_FAULT_RECON) {
     set_last_error("injected fault: reconstruction");
@@ -260,8 +275,6 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   }
   es_solution* sol = new (std::nothrow) es_solution;
   if (!sol) return ES_ERR_NOMEM;
-  int32_t mp = 0;
-  const bool on_device = !o.host_recon && recon_device_applicable(n, m, good, num_bits, den_bits, stats, &mp);
   es_status rs = ES_OK;
   auto t_rec = std::chrono::steady_clock::now();
   if (on_device) {
@@ -272,9 +285,7 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
     rs = grow_device(&p, &dev.recon_size, rbytes, 0, false);
     dev.recon = (char*)p;
     t_rec = std::chrono::steady_clock::now();
-    if (rs == ES_OK)
-      rs = reconstruct_device(dev.digits, n, c, m, mp, good, num_bits, den_bits, stats, o.threads, dev.recon,
-                              dev.recon_size, st, &sol->s);
+    if (rs == ES_OK) rs = reconstruct_device(rplan.get(), dev.digits, o.threads, dev.recon, dev.recon_size, st, &sol->s);
   } else {
     // all digits to the host, reconstruction on the host
     if (dbytes > dev.hdigits_size) {

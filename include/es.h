@@ -172,7 +172,7 @@ es_status es_inverse_mod_device(const int64_t* A_dev, int64_t n, int8_t* B_dev, 
  * holds nearly all of it, or latency-bound loops that must not pay the
  * device-wide synchronisation of cudaFree).  Same arguments, layout and
  * result as es_inverse_mod_device for n <= 256; its working memory is a
- * fixed 4.25 MiB array in device memory that every GPU loading the library
+ * fixed 4.5 MiB array in device memory that every GPU loading the library
  * holds until the process exits.  It calls no cudaMalloc, cudaFree or other
  * allocating routine and creates no stream (NULL = the legacy default
  * stream).  The first call on a device looks up the array's device address
