@@ -27,7 +27,7 @@ STATUS = {0: "ES_OK", 1: "ES_SINGULAR", -1: "ES_ERR_ARG", -2: "ES_ERR_RANGE", -3
 NUM_PRIMES = 53
 DIGIT_LIMBS = 6
 NUM_PHASES = 6
-FAULT = {"residues": 1, "inverse": 2, "lift": 3, "recon": 4, "nomem": 5}
+FAULT = {"residues": 1, "inverse": 2, "lift": 3, "recon": 4, "nomem": 5, "lift_wait": 6}
 FLAG_HOST_RECON = 1
 FLAG_STEP_LIFT = 2
 

@@ -531,7 +531,7 @@ es_status create_events(LiftRun* run, size_t count) {
 
 es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                          const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
-                         void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run) {
+                         void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run, bool stall_barrier) {
   cudaStream_t st = (cudaStream_t)stream;
   LiftConst hK;
   build_lift_const(good_host, &hK);
@@ -563,7 +563,14 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
   ES_CHECK(cuda_status(cudaMemsetAsync(R, 0, (size_t)E * c * ld, st), "memset R"));
   ES_CHECK(cuda_status(cudaMemsetAsync(xl, 0, (size_t)padded_ld(n) * c * 8, st), "memset xl"));
   ES_CHECK(cuda_status(cudaMemsetAsync(err, 0, sizeof(int), st), "memset err"));
-  ES_CHECK(cuda_status(cudaMemsetAsync(bar, 0, sizeof(unsigned), st), "memset barrier"));
+  if (stall_barrier) {
+    // arrivals wrap the counter to G - 11 < G: the first barrier never completes
+    static const unsigned kStalled = 0u - 11u;
+    ES_CHECK(cuda_status(cudaMemcpyAsync(bar, &kStalled, sizeof(unsigned), cudaMemcpyHostToDevice, st),
+                         "barrier init"));
+  } else {
+    ES_CHECK(cuda_status(cudaMemsetAsync(bar, 0, sizeof(unsigned), st), "memset barrier"));
+  }
   if (tc) {
     ES_CHECK(tc_convert_f16(B_dev, B16, (int64_t)kNumPrimes * n * ld, st));
     ES_CHECK(tc_prepare(&tcl, B16, R16, n, c, ld, E));

@@ -257,7 +257,8 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   std::unique_ptr<ReconPlan, void (*)(ReconPlan*)> rplan(nullptr, recon_plan_free);
   {
     LiftRun lr;
-    ES_CHECK(run_lift_start(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt, !o.step_lift, &lr));
+    ES_CHECK(run_lift_start(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt, !o.step_lift, &lr,
+                            o.fault == ES_FAULT_LIFT_WAIT));
     // while the GPU lifts: the reconstruction's digit-independent constants
     es_status ps = ES_OK;
     if (on_device) {

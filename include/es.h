@@ -59,7 +59,7 @@ typedef enum {
 typedef struct es_options {
   void* stream;            /* cudaStream_t to order device work on; NULL = library stream */
   size_t max_device_bytes; /* 0 = no cap; else ES_ERR_NOMEM when the workspace would exceed it */
-  int32_t fault_stage;     /* host-side fault injection: 0 = none, else see ES_FAULT_* */
+  int32_t fault_stage;     /* fault injection: 0 = none, else see ES_FAULT_* */
   int32_t threads;         /* host threads for reconstruction; 0 = all hardware threads */
   int32_t timing;          /* 1: time each phase with CUDA events; 2: also time every launch
                               of the lift's per-prime product kernel (es_solution_kernels) */
@@ -77,6 +77,9 @@ typedef struct es_options {
 #define ES_FAULT_LIFT 3      /* -> ES_ERR_TIMEOUT */
 #define ES_FAULT_RECON 4     /* -> ES_ERR_INTERNAL */
 #define ES_FAULT_NOMEM 5     /* -> ES_ERR_NOMEM at workspace allocation */
+#define ES_FAULT_LIFT_WAIT 6 /* device side: the fused lift (c == 1, n <= 1024) starts its grid-barrier
+                                counter where the first barrier can never complete; every CTA's
+                                bounded wait (2 s) expires, the kernel returns -> ES_ERR_TIMEOUT */
 
 typedef struct es_solution es_solution; /* opaque, owned by the library */
 

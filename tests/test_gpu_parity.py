@@ -359,6 +359,23 @@ def test_fault_injection_leaves_context_usable(torch_cuda, fault, status):
     assert (api.solve_canonical(A, b).N, ) == (exact.solve(A.tolist(), b.tolist())[0], )
 
 
+def test_fused_lift_expired_wait_returns_timeout(torch_cuda):
+    """Device side: the fused lift's first grid barrier can never complete (its
+    counter starts where arrivals wrap below the target).  Every CTA's bounded
+    wait (2 s) expires, the producer lets its copies land, the kernel returns,
+    the host reports ES_ERR_TIMEOUT, and the next solve on the same context
+    is exact."""
+    A, b = inputs.uniform(64, 1, -(1 << 20), 1 << 20, seed=64)
+    s = api.solve_canonical(A, b, timing=2)
+    assert s.top_kernel == "k_lift_fused" and s.m >= 2
+    with pytest.raises(api.ExactSolveError) as e:
+        api.solve_canonical(A, b, fault="lift_wait")
+    assert e.value.status == -5
+    again = api.solve_canonical(A, b)
+    assert (again.N, again.d) == (s.N, s.d)
+    check_identity(A, b, again.N, again.d)
+
+
 def test_device_memory_cap(torch_cuda):
     A, b = inputs.uniform(64, 1, -99, 100, seed=4)
     with pytest.raises(api.ExactSolveError) as e:
