@@ -315,42 +315,48 @@ static u128 bits128_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^128
 
 static inline limb uabs(int64_t v) { return v < 0 ? (limb)(-v) : (limb)v; }
 
-// out = pm P + qm Q (sub = false) or pm P - qm Q (sub = true, known >= 0),
-// one fused pass; out is resized to fit and trimmed.
-static void lin2(Nat& out, limb pm, const Nat& P, limb qm, const Nat& Q, bool sub) {
-  const size_t len = std::max(P.size(), Q.size());
-  out.resize(len + 1);
-  limb cp = 0, cq = 0, borrow = 0;
+// Both rows of a Lehmer cofactor matrix in one pass:
+//   o0 = A x + B y,  o1 = C x + D y   (|A|, |B|, |C|, |D| < 2^62, results >= 0)
+// Each product |coef| * limb is below 2^126, so one signed 128-bit accumulator
+// per output holds the limb sum and a signed carry; the signs are template
+// parameters so the loop has no branches.
+template <bool NA, bool NB, bool NC, bool ND>
+static void lin2x2_pass(limb* o0, limb* o1, const limb* x, size_t xn, const limb* y, size_t yn, size_t len, limb a,
+                        limb b, limb c, limb d) {
+  __int128 c0 = 0, c1 = 0;
   for (size_t i = 0; i < len; ++i) {
-    const u128 p = (u128)pm * (i < P.size() ? P[i] : 0) + cp;
-    const u128 q = (u128)qm * (i < Q.size() ? Q[i] : 0) + cq;
-    cp = (limb)(p >> 64);
-    cq = (limb)(q >> 64);
-    const limb pl = (limb)p, ql = (limb)q;
-    if (sub) {
-      const limb t1 = pl - ql, b1 = pl < ql;
-      const limb t2 = t1 - borrow, b2 = t1 < borrow;
-      out[i] = t2;
-      borrow = b1 | b2;
-    } else {
-      const u128 s = (u128)pl + ql + borrow;  // borrow doubles as the carry
-      out[i] = (limb)s;
-      borrow = (limb)(s >> 64);
-    }
+    const limb xi = i < xn ? x[i] : 0, yi = i < yn ? y[i] : 0;
+    const __int128 pa = (__int128)((u128)a * xi), pb = (__int128)((u128)b * yi);
+    const __int128 pc = (__int128)((u128)c * xi), pd = (__int128)((u128)d * yi);
+    const __int128 t0 = c0 + (NA ? -pa : pa) + (NB ? -pb : pb);
+    const __int128 t1 = c1 + (NC ? -pc : pc) + (ND ? -pd : pd);
+    o0[i] = (limb)t0;
+    o1[i] = (limb)t1;
+    c0 = t0 >> 64;
+    c1 = t1 >> 64;
   }
-  out[len] = sub ? cp - cq - borrow : cp + cq + borrow;
-  trim(out);
+  o0[len] = (limb)c0;
+  o1[len] = (limb)c1;
 }
 
-// A x + B y for a Lehmer cofactor pair (never both negative when the result
-// is a remainder, i.e. non-negative).
-static void comb(Nat& out, int64_t A, const Nat& x, int64_t B, const Nat& y) {
-  if (A >= 0 && B >= 0)
-    lin2(out, (limb)A, x, (limb)B, y, false);
-  else if (A >= 0)
-    lin2(out, (limb)A, x, uabs(B), y, true);
-  else
-    lin2(out, (limb)B, y, uabs(A), x, true);
+static void comb2(Nat& o0, Nat& o1, int64_t A, int64_t B, int64_t C, int64_t D, const Nat& x, const Nat& y) {
+  const size_t len = std::max(x.size(), y.size());
+  o0.resize(len + 1);
+  o1.resize(len + 1);
+  const int code = (A < 0) << 3 | (B < 0) << 2 | (C < 0) << 1 | (D < 0);
+  const limb a = uabs(A), b = uabs(B), c = uabs(C), d = uabs(D);
+#define ES_LIN2X2(k)                                                                                              \
+  case k:                                                                                                         \
+    lin2x2_pass<(k >> 3) & 1, (k >> 2) & 1, (k >> 1) & 1, k & 1>(o0.data(), o1.data(), x.data(), x.size(),       \
+                                                                  y.data(), y.size(), len, a, b, c, d);           \
+    break;
+  switch (code) {
+    ES_LIN2X2(0) ES_LIN2X2(1) ES_LIN2X2(2) ES_LIN2X2(3) ES_LIN2X2(4) ES_LIN2X2(5) ES_LIN2X2(6) ES_LIN2X2(7)
+    ES_LIN2X2(8) ES_LIN2X2(9) ES_LIN2X2(10) ES_LIN2X2(11) ES_LIN2X2(12) ES_LIN2X2(13) ES_LIN2X2(14) ES_LIN2X2(15)
+  }
+#undef ES_LIN2X2
+  trim(o0);
+  trim(o1);
 }
 
 // Shared loop: r0 >= r1; stops when r1 <= 2^nbits (or r1 == 0 when nbits < 0).
@@ -412,13 +418,11 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
         ++k;
       }
       if (B != 0) {
-        comb(n0, A, r0, B, r1);
-        comb(n1, C, r0, D, r1);
+        comb2(n0, n1, A, B, C, D, r0, r1);
         r0.swap(n0);
         r1.swap(n1);
-        if (T0) {
-          lin2(m0, uabs(A), *T0, uabs(B), *T1, false);
-          lin2(m1, uabs(C), *T0, uabs(D), *T1, false);
+        if (T0) {  // consecutive cofactors alternate in sign: the magnitudes add
+          comb2(m0, m1, (int64_t)uabs(A), (int64_t)uabs(B), (int64_t)uabs(C), (int64_t)uabs(D), *T0, *T1);
           T0->swap(m0);
           T1->swap(m1);
         }
