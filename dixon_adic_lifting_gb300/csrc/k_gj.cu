@@ -332,29 +332,32 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
   }
 }
 
-// Register panel with R rows per thread and T threads (n <= T R).  Same
-// exchange steps as k_gj_panel_reg, in a rotating frame: after each step a
-// thread's row is rotated by one entry, so that at step a the entry of panel
-// column c sits in v[(c - a) mod NBP] and the pivot column is always v[0] --
-// no runtime-indexed register access.  The update writes v[t] - f u_{t} into
+// Register panel with R rows per thread and T threads (n <= T R), one CTA
+// per prime.  Exchange steps in a rotating frame: after each step a thread's
+// row is rotated by one entry, so that at step a the entry of panel column c
+// sits in v[(c - a) mod NBP] and the pivot column is always v[0] -- no
+// runtime-indexed register access.  The update writes v[t] - f u_{t} into
 // v[t - 1] (the rotation costs one move per row), with the pivot row scaled
 // and stored already rotated by warp 0; the row is rotated back once, by kb,
 // when the panel is written.  Rows of thread t: t, t + T, ..., t + T (R - 1).
+struct PanelSmem {
+  uint8_t inv[256];                  // inverses mod q
+  __align__(16) int wmin[32];        // per-warp pivot candidates
+  __align__(16) int32_t raw[32];     // pivot row, natural column order
+  __align__(16) int32_t prow[32];    // scaled pivot row, rotated: entry t = column (a + t) mod NBP
+  __align__(16) int32_t pupd[32];    // same with the pivot entry + 1
+  int piv[32];                       // the panel's pivot rows
+  __align__(16) uint32_t u[32][8];   // a narrow update's U: column c, pivot rows 4w .. 4w + 3 in word w
+};
+
+// The kb exchange steps of the panel at k0; writes the reduced panel back to
+// W and the used flags, and leaves each of the thread's rows as 8 packed
+// words in Fp.  False when the prime has no pivot (it is flagged bad).
 template <int NBP, int R, int T>
-__global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, int kb) {
-  const int j = blockIdx.x;
-  if (p.bad[j]) return;
-  const ModQ m = c_modq.v[j];
+__device__ __forceinline__ bool panel_factor(const GJParams& p, int j, const ModQ& m, int8_t* Wj, int64_t k0, int kb,
+                                             PanelSmem& S, uint32_t (&Fp)[R][NBP / 4]) {
   const int n = (int)p.n, ld = (int)p.ld;
-  int8_t* Wj = p.W + (int64_t)j * n * ld;
-  __shared__ uint8_t s_inv[256];
-  __shared__ __align__(16) int s_wmin[T / 32];
-  __shared__ __align__(16) int32_t s_raw[NBP];   // pivot row, natural column order
-  __shared__ __align__(16) int32_t s_prow[NBP];  // scaled pivot row, rotated: entry t = column (a + t) mod NBP
-  __shared__ __align__(16) int32_t s_pupd[NBP];  // same with the pivot entry + 1
-  __shared__ int s_piv[NBP];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int x = tid; x < (int)m.q; x += T) s_inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
   int32_t v[R][NBP];
   bool used[R];
 #pragma unroll
@@ -384,37 +387,37 @@ __global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, 
       if (!used[i] && f[i] != 0) cand = tid + T * i;
     }
     cand = __reduce_min_sync(0xffffffffu, cand);
-    if (lane == 0) s_wmin[warp] = cand;
+    if (lane == 0) S.wmin[warp] = cand;
     __syncthreads();  // (1) candidates of every warp
     int pr = INT_MAX;
 #pragma unroll
     for (int w4 = 0; w4 < T / 128; ++w4) {
-      const int4 c = *reinterpret_cast<const int4*>(s_wmin + 4 * w4);
+      const int4 c = *reinterpret_cast<const int4*>(S.wmin + 4 * w4);
       pr = min(pr, min(min(c.x, c.y), min(c.z, c.w)));
     }
     if (pr == INT_MAX) {  // no pivot: q_j | det A
       if (tid == 0) p.bad[j] = 1;
-      return;
+      return false;
     }
 #pragma unroll
     for (int i = 0; i < R; ++i)
       if (tid + T * i == pr) {
 #pragma unroll
-        for (int t = 0; t < NBP; ++t) s_raw[(a + t) & (NBP - 1)] = t == 0 ? f[i] : v[i][t];
+        for (int t = 0; t < NBP; ++t) S.raw[(a + t) & (NBP - 1)] = t == 0 ? f[i] : v[i][t];
         used[i] = true;
-        s_piv[a] = pr;
+        S.piv[a] = pr;
         p.piv[(int64_t)j * n + k0 + a] = pr;
       }
     __syncthreads();  // (2) raw pivot row
     if (warp == 0) {
-      const int32_t pf = s_raw[a];
-      const uint32_t inv = s_inv[pf < 0 ? pf + (int32_t)m.q : pf];
+      const int32_t pf = S.raw[a];
+      const uint32_t inv = S.inv[pf < 0 ? pf + (int32_t)m.q : pf];
       for (int t = lane; t < NBP; t += 32) {
         const int c = (a + t) & (NBP - 1);
         const int32_t pt =
-            (t == 0) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(s_raw[c], m) * (int32_t)inv, m);
-        s_prow[t] = pt;
-        s_pupd[t] = (t == 0) ? pt + 1 : pt;
+            (t == 0) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(S.raw[c], m) * (int32_t)inv, m);
+        S.prow[t] = pt;
+        S.pupd[t] = (t == 0) ? pt + 1 : pt;
       }
     }
     __syncthreads();  // (3) scaled pivot row
@@ -425,16 +428,16 @@ __global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, 
       if (tid + T * i == pr) {
 #pragma unroll
         for (int t4 = 0; t4 < NBP / 4; ++t4) {
-          const int4 pp = *reinterpret_cast<const int4*>(s_prow + 4 * t4);
+          const int4 pp = *reinterpret_cast<const int4*>(S.prow + 4 * t4);
           const int32_t ps[4] = {pp.x, pp.y, pp.z, pp.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) v[i][(4 * t4 + u + NBP - 1) & (NBP - 1)] = ps[u];
         }
       } else {
-        const int32_t fi = f[i], first = v[i][0] - fi * s_pupd[0];
+        const int32_t fi = f[i], first = v[i][0] - fi * S.pupd[0];
 #pragma unroll
         for (int t4 = 0; t4 < NBP / 4; ++t4) {
-          const int4 uu = *reinterpret_cast<const int4*>(s_pupd + 4 * t4);
+          const int4 uu = *reinterpret_cast<const int4*>(S.pupd + 4 * t4);
           const int32_t us[4] = {uu.x, uu.y, uu.z, uu.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -464,27 +467,31 @@ __global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, 
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int row = tid + T * i;
+#pragma unroll
+    for (int q = 0; q < NBP / 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x |= ((uint32_t)(uint8_t)(int8_t)reduce_bal(v[i][4 * q + u], m)) << (8 * u);
+      Fp[i][q] = x;
+    }
     if (row >= n) continue;
 #pragma unroll
-    for (int c4 = 0; c4 < NBP / 16; ++c4) {
-      if (k0 + 16 * c4 >= ld) continue;
-      uint32_t ww[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t x = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          x |= ((uint32_t)(uint8_t)(int8_t)reduce_bal(v[i][c4 * 16 + q4 * 4 + u], m)) << (8 * u);
-        ww[q4] = x;
-      }
-      *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) = make_int4(ww[0], ww[1], ww[2], ww[3]);
-    }
+    for (int c4 = 0; c4 < NBP / 16; ++c4)
+      if (k0 + 16 * c4 < ld)
+        *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) =
+            make_int4(Fp[i][4 * c4], Fp[i][4 * c4 + 1], Fp[i][4 * c4 + 2], Fp[i][4 * c4 + 3]);
     p.used[(int64_t)j * n + row] = used[i] ? 1 : 0;
   }
-  __syncthreads();
-  // stage U^T (pivot rows outside the panel) and zero those entries in place
-  int8_t* UTj = p.UT + (int64_t)j * ld * p.utw;
-  for (int col = tid; col < ld; col += T) {
+  return true;
+}
+
+// Stage U^T of the panel at k0 (pivot rows S.piv, kb of them) for every
+// column outside the panel into UT[col][0 .. NBP) (row width utw) and zero
+// those entries in W.
+template <int NBP, int T>
+__device__ __forceinline__ void panel_stage(int64_t ld, int8_t* Wj, int64_t k0, int kb, const PanelSmem& S,
+                                            int8_t* UTj, int utw) {
+  for (int64_t col = threadIdx.x; col < ld; col += T) {
     const bool outside = col < k0 || col >= k0 + kb;
     uint32_t w[NBP / 4];
 #pragma unroll
@@ -493,18 +500,102 @@ __global__ void __launch_bounds__(T, 1) k_gj_panel_rows(GJParams p, int64_t k0, 
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int aa = 4 * q + u;
-        const uint8_t b = (aa < kb && outside) ? (uint8_t)Wj[(int64_t)s_piv[aa] * ld + col] : (uint8_t)0;
+        const uint8_t b = (aa < kb && outside) ? (uint8_t)Wj[(int64_t)S.piv[aa] * ld + col] : (uint8_t)0;
         x |= (uint32_t)b << (8 * u);
       }
       w[q] = x;
     }
 #pragma unroll
     for (int c4 = 0; c4 < NBP / 16; ++c4)
-      *reinterpret_cast<int4*>(UTj + (int64_t)col * p.utw + 16 * c4) =
+      *reinterpret_cast<int4*>(UTj + col * utw + 16 * c4) =
           make_int4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
     if (outside)
-      for (int aa = 0; aa < kb; ++aa) Wj[(int64_t)s_piv[aa] * ld + col] = 0;
+      for (int aa = 0; aa < kb; ++aa) Wj[(int64_t)S.piv[aa] * ld + col] = 0;
   }
+}
+
+// W[r][c0 + c] += sum_a F[r][a] U[a][c] (mod q) for the 32 columns c0 .. c0+31
+// and every row r of this thread (F = its packed panel rows, U = the staged
+// pivot rows of those columns, UT[col][0..32) at row width utw): 8 dp4a per
+// entry, exact (32 * 125^2 + 125 < 2^31).
+template <int R, int T>
+__device__ __forceinline__ void narrow_update(const GJParams& p, int8_t* Wj, const ModQ& m,
+                                              const uint32_t (&Fp)[R][8], const int8_t* UTj, int utw, int64_t c0,
+                                              PanelSmem& S) {
+  const int n = (int)p.n;
+  const int64_t ld = p.ld;
+  const int tid = threadIdx.x;
+  if (tid < 64) {
+    const int c = tid >> 1, h = tid & 1;
+    const int64_t col = c0 + c;
+    const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + col * utw + 16 * h) : make_int4(0, 0, 0, 0);
+    *reinterpret_cast<int4*>(&S.u[c][4 * h]) = x;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int row = tid + T * i;
+    if (row >= n) continue;
+    int8_t* wr = Wj + (int64_t)row * ld + c0;
+    const bool two = c0 + 16 < ld;
+    const int4 o0 = *reinterpret_cast<const int4*>(wr), o1 = two ? *reinterpret_cast<const int4*>(wr + 16)
+                                                                 : make_int4(0, 0, 0, 0);
+    uint32_t w[8] = {(uint32_t)o0.x, (uint32_t)o0.y, (uint32_t)o0.z, (uint32_t)o0.w,
+                     (uint32_t)o1.x, (uint32_t)o1.y, (uint32_t)o1.z, (uint32_t)o1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = 4 * q + u;
+        const int4 ua = *reinterpret_cast<const int4*>(&S.u[c][0]), ub = *reinterpret_cast<const int4*>(&S.u[c][4]);
+        int32_t acc = 0;
+        acc = __dp4a((int)Fp[i][0], ua.x, acc);
+        acc = __dp4a((int)Fp[i][1], ua.y, acc);
+        acc = __dp4a((int)Fp[i][2], ua.z, acc);
+        acc = __dp4a((int)Fp[i][3], ua.w, acc);
+        acc = __dp4a((int)Fp[i][4], ub.x, acc);
+        acc = __dp4a((int)Fp[i][5], ub.y, acc);
+        acc = __dp4a((int)Fp[i][6], ub.z, acc);
+        acc = __dp4a((int)Fp[i][7], ub.w, acc);
+        int32_t val = sbyte(w[q], u);
+        if (c0 + c < n) val = reduce_bal(val + acc, m);
+        x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
+      }
+      w[q] = x;
+    }
+    *reinterpret_cast<int4*>(wr) = make_int4(w[0], w[1], w[2], w[3]);
+    if (two) *reinterpret_cast<int4*>(wr + 16) = make_int4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// One 64-column block (n <= 1024): panel k0 (kb1 columns), its U^T into
+// UT[:, 0..32) with the pivot rows zeroed, the update of the block's other
+// 32 columns, panel k0 + 32 (kb2 columns, 0 = none), its U^T into
+// UT[:, 32..64), the update of the first 32 columns.  One CTA per prime.
+template <int R, int T>
+__global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int kb1, int kb2) {
+  const int j = blockIdx.x;
+  if (p.bad[j]) return;
+  const ModQ m = c_modq.v[j];
+  int8_t* Wj = p.W + (int64_t)j * p.n * p.ld;
+  int8_t* UTj = p.UT + (int64_t)j * p.ld * 64;
+  __shared__ PanelSmem S;
+  for (int x = threadIdx.x; x < (int)m.q; x += T) S.inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
+  uint32_t Fp[R][8];
+  if (!panel_factor<32, R, T>(p, j, m, Wj, k0, kb1, S, Fp)) return;
+  __syncthreads();
+  panel_stage<32, T>(p.ld, Wj, k0, kb1, S, UTj, 64);
+  if (kb2 == 0) return;
+  const int64_t k1 = k0 + 32;
+  __syncthreads();
+  narrow_update<R, T>(p, Wj, m, Fp, UTj, 64, k1, S);
+  __syncthreads();
+  if (!panel_factor<32, R, T>(p, j, m, Wj, k1, kb2, S, Fp)) return;
+  __syncthreads();
+  panel_stage<32, T>(p.ld, Wj, k1, kb2, S, UTj + 32, 64);
+  __syncthreads();
+  narrow_update<R, T>(p, Wj, m, Fp, UTj + 32, 64, k0, S);
 }
 
 // ------------------------------------------------------------------ update
@@ -750,16 +841,8 @@ InvLayout inverse_layout(int64_t n) {
 // column staged into U^T (at gp.UT, rows of gp.utw bytes) and zeroed in W.
 template <int NBP>
 void panel(GJParams& gp, int64_t n, int64_t k0, int kb, bool use_smem, cudaStream_t st) {
-  const bool reg_panel = NBP == 32 && n <= 1024;  // one row per thread, panel in registers
-  if (reg_panel && n <= 256)
-    k_gj_panel_rows<NBP, 1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
-  else if (reg_panel && n <= 512)
-    k_gj_panel_rows<NBP, 2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb);
-  else if (reg_panel)
-    k_gj_panel_rows<NBP, 2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb);
-  else
-    k_gj_panel<NBP><<<kNumPrimes, 1024, use_smem ? (size_t)n * NBP + (size_t)n : 0, st>>>(gp, k0, kb,
-                                                                                       use_smem ? 1 : 0);
+  k_gj_panel<NBP><<<kNumPrimes, 1024, use_smem ? (size_t)n * NBP + (size_t)n : 0, st>>>(gp, k0, kb,
+                                                                                     use_smem ? 1 : 0);
   count_launch();
 }
 
@@ -800,25 +883,38 @@ es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) 
   const int64_t ld = gp.ld;
   const unsigned rtiles = (unsigned)((n + 63) / 64);
   const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
+  const bool reg_block = n <= 1024;  // the whole block in one launch, panel in registers
   gp.utw = 64;
   for (int64_t k0 = 0; k0 < n; k0 += 64) {
     const int kb1 = (int)((n - k0) < 32 ? (n - k0) : 32);
     const int64_t k1 = k0 + 32;
     const bool two = k1 < n;
-    gp.UT = UT;
-    panel<32>(gp, n, k0, kb1, use_smem, st);
-    if (two) {
-      const int kb2 = (int)((n - k1) < 32 ? (n - k1) : 32);
-      k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT, 64, k0, k1, k1 + 32);
-      gp.UT = UT + 32;
-      panel<32>(gp, n, k1, kb2, use_smem, st);
-      k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT + 32, 64, k1, k0, k0 + 32);
-      k_gj_update_mma<64><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
-      count_launch(3);
-    } else {
-      k_gj_update_mma<32><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+    const int kb2 = two ? (int)((n - k1) < 32 ? (n - k1) : 32) : 0;
+    if (reg_block) {
+      if (n <= 256)
+        k_gj_block64<1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2);
+      else if (n <= 512)
+        k_gj_block64<2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2);
+      else
+        k_gj_block64<2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb1, kb2);
       count_launch();
+    } else {
+      gp.UT = UT;
+      panel<32>(gp, n, k0, kb1, use_smem, st);
+      if (two) {
+        k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT, 64, k0, k1, k1 + 32);
+        gp.UT = UT + 32;
+        panel<32>(gp, n, k1, kb2, use_smem, st);
+        k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT + 32, 64, k1, k0, k0 + 32);
+        count_launch(2);
+      }
+      gp.UT = UT;
     }
+    if (two)
+      k_gj_update_mma<64><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+    else
+      k_gj_update_mma<32><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+    count_launch();
   }
   gp.UT = UT;
   return cuda_status(cudaGetLastError(), "gauss-jordan blocks");
