@@ -74,8 +74,12 @@ es_status launch_residues_matrix(const int64_t* A, int64_t n, int64_t ld, int8_t
 
 // Batched modular inverse: A_dev -> B [53][n][ld], good [53] (device).
 size_t inverse_scratch_bytes(int64_t n);
+// split: run the blocks on two SM partitions (green contexts) when the
+// device supports them (no extra streams otherwise).
 es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev, char* scratch,
-                      void* stream);
+                      void* stream, bool split = true);
+// Destroys the SM partitions of device `dev` (es_release_workspace).
+void release_inverse_partitions(int dev);
 
 // Kernel accounting: every launch site adds to the launch counter; the lift
 // optionally brackets each launch of its product kernel with CUDA events.

@@ -27,9 +27,11 @@
 //                   (A^{-1})[k][t] = W[p_k][pinv[t]].
 // A prime with no pivot in some column divides det A; it is flagged bad and
 // its CTAs exit early in every later launch.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <mutex>
 #include <string>
 
 #include "es_common.cuh"
@@ -485,13 +487,13 @@ __device__ __forceinline__ bool panel_factor(const GJParams& p, int j, const Mod
   return true;
 }
 
-// Stage U^T of the panel at k0 (pivot rows S.piv, kb of them) for every
-// column outside the panel into UT[col][0 .. NBP) (row width utw) and zero
-// those entries in W.
+// Stage U^T of the panel at k0 (pivot rows S.piv, kb of them) for the
+// columns cb <= col < ce outside the panel into UT[col][0 .. NBP) (row width
+// utw) and zero those entries in W.
 template <int NBP, int T>
-__device__ __forceinline__ void panel_stage(int64_t ld, int8_t* Wj, int64_t k0, int kb, const PanelSmem& S,
-                                            int8_t* UTj, int utw) {
-  for (int64_t col = threadIdx.x; col < ld; col += T) {
+__device__ __forceinline__ void panel_stage(int64_t cb, int64_t ce, int8_t* Wj, int64_t ld, int64_t k0, int kb,
+                                            const PanelSmem& S, int8_t* UTj, int utw) {
+  for (int64_t col = cb + threadIdx.x; col < ce; col += T) {
     const bool outside = col < k0 || col >= k0 + kb;
     uint32_t w[NBP / 4];
 #pragma unroll
@@ -573,19 +575,87 @@ __device__ __forceinline__ void narrow_update(const GJParams& p, int8_t* Wj, con
 // UT[:, 0..32) with the pivot rows zeroed, the update of the block's other
 // 32 columns, panel k0 + 32 (kb2 columns, 0 = none), its U^T into
 // UT[:, 32..64), the update of the first 32 columns.  One CTA per prime.
+// W[r][k0 + c] += sum_a F[r][a] U[a][c] (mod q) for the 64 columns of the
+// block at k0 and every row r of this thread: the previous block's update of
+// these columns, F = W[:, prev .. prev + 64) (its final columns), U = its
+// staged pivot rows, UT[k0 + c][0 .. 64).  16 dp4a per entry, exact
+// (64 * 125^2 + 125 < 2^31); U is broadcast from shared memory.
 template <int R, int T>
-__global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int kb1, int kb2) {
+__device__ __forceinline__ void catch_up(const GJParams& p, int8_t* Wj, const int8_t* UTj, const ModQ& m, int64_t prev,
+                                         int64_t k0, uint32_t (*Us)[16]) {
+  const int n = (int)p.n;
+  const int64_t ld = p.ld;
+  const int tid = threadIdx.x;
+  for (int idx = tid; idx < 64 * 4; idx += T) {
+    const int c = idx >> 2, h = idx & 3;
+    const int64_t col = k0 + c;
+    const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + col * 64 + 16 * h) : make_int4(0, 0, 0, 0);
+    *reinterpret_cast<int4*>(&Us[c][4 * h]) = x;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int row = tid + T * i;
+    if (row >= n) continue;
+    uint32_t f[16], w[16];
+    const int4* fr = reinterpret_cast<const int4*>(Wj + (int64_t)row * ld + prev);
+    int4* wr = reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int4 a = fr[h];
+      const int4 b = (k0 + 16 * h < ld) ? wr[h] : make_int4(0, 0, 0, 0);
+      f[4 * h] = a.x, f[4 * h + 1] = a.y, f[4 * h + 2] = a.z, f[4 * h + 3] = a.w;
+      w[4 * h] = b.x, w[4 * h + 1] = b.y, w[4 * h + 2] = b.z, w[4 * h + 3] = b.w;
+    }
+#pragma unroll 4
+    for (int q = 0; q < 16; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = 4 * q + u;
+        int32_t acc = 0;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint4 uu = *reinterpret_cast<const uint4*>(&Us[c][4 * h]);
+          acc = __dp4a((int)f[4 * h], (int)uu.x, acc);
+          acc = __dp4a((int)f[4 * h + 1], (int)uu.y, acc);
+          acc = __dp4a((int)f[4 * h + 2], (int)uu.z, acc);
+          acc = __dp4a((int)f[4 * h + 3], (int)uu.w, acc);
+        }
+        int32_t val = sbyte(w[q], u);
+        if (k0 + c < n) val = reduce_bal(val + acc, m);
+        x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
+      }
+      w[q] = x;
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (k0 + 16 * h < ld) wr[h] = make_int4(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
+  }
+  __syncthreads();
+}
+
+// own_only: stage only the block's own columns; the other columns' pivot
+// rows are staged later by k_gj_stage64 (the schedule that overlaps this
+// kernel with the previous block's update of those columns).  prev >= 0:
+// first bring the block's columns up to date with the block at prev.
+template <int R, int T>
+__global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int kb1, int kb2, int own_only,
+                                                     int64_t prev) {
   const int j = blockIdx.x;
   if (p.bad[j]) return;
   const ModQ m = c_modq.v[j];
   int8_t* Wj = p.W + (int64_t)j * p.n * p.ld;
   int8_t* UTj = p.UT + (int64_t)j * p.ld * 64;
   __shared__ PanelSmem S;
+  __shared__ __align__(16) uint32_t Us[64][16];
   for (int x = threadIdx.x; x < (int)m.q; x += T) S.inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
+  if (prev >= 0) catch_up<R, T>(p, Wj, UTj, m, prev, k0, Us);
   uint32_t Fp[R][8];
+  const int64_t cb = own_only ? k0 : 0, ce = own_only ? (k0 + 64 < p.ld ? k0 + 64 : p.ld) : p.ld;
   if (!panel_factor<32, R, T>(p, j, m, Wj, k0, kb1, S, Fp)) return;
   __syncthreads();
-  panel_stage<32, T>(p.ld, Wj, k0, kb1, S, UTj, 64);
+  panel_stage<32, T>(cb, ce, Wj, p.ld, k0, kb1, S, UTj, 64);
   if (kb2 == 0) return;
   const int64_t k1 = k0 + 32;
   __syncthreads();
@@ -593,9 +663,54 @@ __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int
   __syncthreads();
   if (!panel_factor<32, R, T>(p, j, m, Wj, k1, kb2, S, Fp)) return;
   __syncthreads();
-  panel_stage<32, T>(p.ld, Wj, k1, kb2, S, UTj + 32, 64);
+  panel_stage<32, T>(cb, ce, Wj, p.ld, k1, kb2, S, UTj + 32, 64);
   __syncthreads();
   narrow_update<R, T>(p, Wj, m, Fp, UTj + 32, 64, k0, S);
+}
+
+// The block's U^T for every column outside it: the pivot rows
+// piv[k0 .. k0 + 64) (the first kb1 of the first panel, the second panel's at
+// 32 .. 32 + kb2) go to UT[col][0 .. 64) (zero where there is no pivot) and
+// are zeroed in W.  Thread per 4 consecutive columns and prime: one 4-byte
+// load per pivot row (a warp reads whole 128-byte lines), all loads before
+// any zeroing store, bytes transposed in registers.
+__global__ void __launch_bounds__(128) k_gj_stage64(GJParams p, int64_t k0, int kb1, int kb2) {
+  const int j = blockIdx.y;
+  if (p.bad[j]) return;
+  const int64_t n = p.n, ld = p.ld;
+  const int64_t col = 4 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+  if (col >= ld || (col >= k0 && col < k0 + 64)) return;  // ld and k0 are multiples of 4
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  const int32_t* pv = p.piv + (int64_t)j * n + k0;
+  uint32_t x[64];
+#pragma unroll
+  for (int a = 0; a < 64; ++a) {
+    const bool have = a < 32 ? a < kb1 : a - 32 < kb2;
+    x[a] = have ? *reinterpret_cast<const uint32_t*>(Wj + (int64_t)pv[a] * ld + col) : 0u;
+  }
+#pragma unroll
+  for (int a = 0; a < 64; ++a) {
+    const bool have = a < 32 ? a < kb1 : a - 32 < kb2;
+    if (have) *reinterpret_cast<uint32_t*>(Wj + (int64_t)pv[a] * ld + col) = 0u;
+  }
+  // column c of the four: bytes c of x[0 .. 64), packed four at a time
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    int4* dst = reinterpret_cast<int4*>(p.UT + ((int64_t)j * ld + col + c) * 64);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int a0 = 16 * c4 + 4 * q;
+        // gather byte c of x[a0 .. a0 + 4) into one word
+        const uint32_t lo = __byte_perm(x[a0], x[a0 + 1], c | (c + 4) << 4);
+        const uint32_t hi = __byte_perm(x[a0 + 2], x[a0 + 3], c | (c + 4) << 4);
+        w[q] = __byte_perm(lo, hi, 0x5410);
+      }
+      dst[c4] = make_int4(w[0], w[1], w[2], w[3]);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ update
@@ -677,7 +792,7 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
 // g + 8 (r >> 1), column 2 t + (r & 1)  (g = lane / 4, t = lane % 4).
 // KW = 64 is exact too: 64 * 125^2 + 125 < 2^31.  CTA tile 64 rows x 128
 // columns, 8 warps of 32 x 32.  Columns updated: 32-column segments col0 with
-// cbase <= col0 < cend outside [k0, k0 + KW).
+// cbase <= col0 < cend outside [xb, xe) (which holds at least the panel).
 __device__ __forceinline__ void mma_s8_16x8x32(int32_t (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(
       "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -690,7 +805,8 @@ __device__ __forceinline__ int rot3(int r) { return ((r << 1) | ((r >> 2) & 1)) 
 
 template <int KW>
 __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, const int8_t* __restrict__ UT, int utw,
-                                                       int64_t k0, int64_t cbase, int64_t cend) {
+                                                       int64_t k0, int64_t cbase, int64_t cend, int64_t xb,
+                                                       int64_t xe) {
   const int j = blockIdx.z;
   if (p.bad[j]) return;
   const ModQ m = c_modq.v[j];
@@ -708,7 +824,7 @@ __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, const int8_t*
   // this thread's output row segment (row0 + lane, 32 columns), fetched early;
   // segments are 32-column aligned like the panel: one either lies in it or misses it
   const int64_t orow = row0 + lane;
-  const bool rowok = orow < n && col0 < ld && col0 < cend && (col0 < k0 || col0 >= k0 + KW);
+  const bool rowok = orow < n && col0 < ld && col0 < cend && (col0 < xb || col0 >= xe);
   int4 old0 = make_int4(0, 0, 0, 0), old1 = old0;
   if (rowok) {
     old0 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0);
@@ -892,39 +1008,184 @@ es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) 
     const int kb2 = two ? (int)((n - k1) < 32 ? (n - k1) : 32) : 0;
     if (reg_block) {
       if (n <= 256)
-        k_gj_block64<1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2);
+        k_gj_block64<1, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2, 0, -1);
       else if (n <= 512)
-        k_gj_block64<2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2);
+        k_gj_block64<2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2, 0, -1);
       else
-        k_gj_block64<2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb1, kb2);
+        k_gj_block64<2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb1, kb2, 0, -1);
       count_launch();
     } else {
       gp.UT = UT;
       panel<32>(gp, n, k0, kb1, use_smem, st);
       if (two) {
-        k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT, 64, k0, k1, k1 + 32);
+        k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT, 64, k0, k1, k1 + 32, k0, k1);
         gp.UT = UT + 32;
         panel<32>(gp, n, k1, kb2, use_smem, st);
-        k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT + 32, 64, k1, k0, k0 + 32);
+        k_gj_update_mma<32><<<dim3(1, rtiles, kNumPrimes), 256, 0, st>>>(gp, UT + 32, 64, k1, k0, k0 + 32, k1,
+                                                                          k1 + 32);
         count_launch(2);
       }
       gp.UT = UT;
     }
     if (two)
-      k_gj_update_mma<64><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+      k_gj_update_mma<64><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld, k0, k0 + 64);
     else
-      k_gj_update_mma<32><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld);
+      k_gj_update_mma<32><<<wide, 256, 0, st>>>(gp, UT, 64, k0, 0, ld, k0, k0 + 32);
     count_launch();
   }
   gp.UT = UT;
   return cuda_status(cudaGetLastError(), "gauss-jordan blocks");
 }
+
+// ------------------------------------------------------------------ overlap
+// Two SM partitions per device (green contexts, driver API looked up at run
+// time): one of at least 53 SMs for the block kernels (one CTA per prime, a
+// whole SM's registers each) and the rest for the updates, each with a
+// stream.  While the panel partition brings block b + 1 up to date and
+// factors it, the update of block b reaches every other column on the other:
+//   update stream: [wait pb] stage b's pivot rows of the other columns -> (wn)
+//                  -> update every column outside blocks b and b + 1
+//   panel stream:  [wait wn] block b+1, which first applies block b's update
+//                  to its own 64 columns -> (pb)
+// The two kernels that run at the same time touch disjoint columns of W and
+// disjoint rows of U^T.  Created once per device; es_release_workspace
+// destroys them.
+struct Partitions {
+  bool tried = false, ok = false;
+  CUgreenCtx gp = nullptr, gu = nullptr;
+  cudaStream_t sp = nullptr, su = nullptr;
+  cudaEvent_t fork = nullptr, pb = nullptr, wn = nullptr, join = nullptr;
+};
+std::mutex g_part_mu;
+Partitions g_part[kMaxDevices];
+
+template <class F>
+bool driver_entry(const char* name, F* fn) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, CUDA_VERSION, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !ptr) {
+    cudaGetLastError();
+    return false;
+  }
+  *fn = reinterpret_cast<F>(ptr);
+  return true;
+}
+
+using GreenDestroyFn = CUresult (*)(CUgreenCtx);
+
+void drop_partitions(Partitions& P) {
+  GreenDestroyFn destroy = nullptr;
+  driver_entry("cuGreenCtxDestroy", &destroy);
+  for (cudaStream_t* s : {&P.sp, &P.su})
+    if (*s) cudaStreamDestroy(*s);
+  for (cudaEvent_t* e : {&P.fork, &P.pb, &P.wn, &P.join})
+    if (*e) cudaEventDestroy(*e);
+  if (destroy) {
+    if (P.gp) destroy(P.gp);
+    if (P.gu) destroy(P.gu);
+  }
+  cudaGetLastError();
+  P = Partitions{};
+}
+
+bool make_partitions(int dev, Partitions& P) {
+  CUresult (*get_dev)(CUdevice*, int) = nullptr;
+  CUresult (*get_res)(CUdevice, CUdevResource*, CUdevResourceType) = nullptr;
+  CUresult (*split)(CUdevResource*, unsigned*, const CUdevResource*, CUdevResource*, unsigned, unsigned) = nullptr;
+  CUresult (*gen_desc)(CUdevResourceDesc*, CUdevResource*, unsigned) = nullptr;
+  CUresult (*create)(CUgreenCtx*, CUdevResourceDesc, CUdevice, unsigned) = nullptr;
+  CUresult (*stream_create)(CUstream*, CUgreenCtx, unsigned, int) = nullptr;
+  if (!driver_entry("cuDeviceGet", &get_dev) || !driver_entry("cuDeviceGetDevResource", &get_res) ||
+      !driver_entry("cuDevSmResourceSplitByCount", &split) || !driver_entry("cuDevResourceGenerateDesc", &gen_desc) ||
+      !driver_entry("cuGreenCtxCreate", &create) || !driver_entry("cuGreenCtxStreamCreate", &stream_create))
+    return false;
+  CUdevice d;
+  CUdevResource all, grp[1], rest;
+  unsigned ngroups = 1;
+  if (get_dev(&d, dev) != CUDA_SUCCESS || get_res(d, &all, CU_DEV_RESOURCE_TYPE_SM) != CUDA_SUCCESS ||
+      split(grp, &ngroups, &all, &rest, 0, kNumPrimes) != CUDA_SUCCESS || ngroups != 1 ||
+      grp[0].sm.smCount < (unsigned)kNumPrimes || rest.sm.smCount < 32)
+    return false;
+  CUdevResourceDesc dp, du;
+  CUstream sp = nullptr, su = nullptr;
+  if (gen_desc(&dp, grp, 1) != CUDA_SUCCESS || gen_desc(&du, &rest, 1) != CUDA_SUCCESS ||
+      create(&P.gp, dp, d, CU_GREEN_CTX_DEFAULT_STREAM) != CUDA_SUCCESS ||
+      create(&P.gu, du, d, CU_GREEN_CTX_DEFAULT_STREAM) != CUDA_SUCCESS ||
+      stream_create(&sp, P.gp, CU_STREAM_NON_BLOCKING, 0) != CUDA_SUCCESS ||
+      stream_create(&su, P.gu, CU_STREAM_NON_BLOCKING, 0) != CUDA_SUCCESS) {
+    P.sp = (cudaStream_t)sp;
+    P.su = (cudaStream_t)su;
+    drop_partitions(P);
+    return false;
+  }
+  P.sp = (cudaStream_t)sp;
+  P.su = (cudaStream_t)su;
+  for (cudaEvent_t* e : {&P.fork, &P.pb, &P.wn, &P.join})
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+      drop_partitions(P);
+      return false;
+    }
+  return true;
+}
+
+template <int R, int T>
+void block64(GJParams& gp, int64_t k0, int kb1, int kb2, int own_only, int64_t prev, cudaStream_t st) {
+  k_gj_block64<R, T><<<kNumPrimes, T, 0, st>>>(gp, k0, kb1, kb2, own_only, prev);
+}
+
+es_status run_blocks64_split(GJParams& gp, int64_t n, cudaStream_t st, Partitions& P) {
+  int8_t* const UT = gp.UT;
+  const int64_t ld = gp.ld;
+  const unsigned rtiles = (unsigned)((n + 63) / 64);
+  const dim3 sgrid((unsigned)((ld / 4 + 127) / 128), kNumPrimes);
+  const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
+  gp.utw = 64;
+  ES_CHECK(cuda_status(cudaEventRecord(P.fork, st), "fork"));
+  ES_CHECK(cuda_status(cudaStreamWaitEvent(P.sp, P.fork, 0), "fork panel"));
+  ES_CHECK(cuda_status(cudaStreamWaitEvent(P.su, P.fork, 0), "fork update"));
+  int64_t prev = -1;  // the previous block's first column
+  for (int64_t k0 = 0; k0 < n; k0 += 64) {
+    const int kb1 = (int)((n - k0) < 32 ? (n - k0) : 32);
+    const int64_t k1 = k0 + 32, n0 = k0 + 64;
+    const int kb2 = k1 < n ? (int)((n - k1) < 32 ? (n - k1) : 32) : 0;
+    if (prev >= 0) ES_CHECK(cuda_status(cudaStreamWaitEvent(P.sp, P.wn, 0), "wait stage"));
+    if (n <= 256)
+      block64<1, 256>(gp, k0, kb1, kb2, 1, prev, P.sp);
+    else if (n <= 512)
+      block64<2, 256>(gp, k0, kb1, kb2, 1, prev, P.sp);
+    else
+      block64<2, 512>(gp, k0, kb1, kb2, 1, prev, P.sp);
+    ES_CHECK(cuda_status(cudaEventRecord(P.pb, P.sp), "record block"));
+    // stage this block's pivot rows of every other column (after the
+    // previous block's update reached them), then update all but the next block
+    ES_CHECK(cuda_status(cudaStreamWaitEvent(P.su, P.pb, 0), "wait block"));
+    k_gj_stage64<<<sgrid, 128, 0, P.su>>>(gp, k0, kb1, kb2);
+    ES_CHECK(cuda_status(cudaEventRecord(P.wn, P.su), "record stage"));
+    const int64_t xe = n0 < n ? n0 + 64 : n0;  // keep off the next block (done on the panel side)
+    if (kb2)
+      k_gj_update_mma<64><<<wide, 256, 0, P.su>>>(gp, UT, 64, k0, 0, ld, k0, xe);
+    else
+      k_gj_update_mma<32><<<wide, 256, 0, P.su>>>(gp, UT, 64, k0, 0, ld, k0, xe);
+    count_launch(3);
+    prev = k0;
+  }
+  ES_CHECK(cuda_status(cudaEventRecord(P.join, P.su), "join"));
+  ES_CHECK(cuda_status(cudaStreamWaitEvent(st, P.join, 0), "join wait"));
+  return cuda_status(cudaGetLastError(), "gauss-jordan blocks (split)");
+}
 }  // namespace
 
 size_t inverse_scratch_bytes(int64_t n) { return inverse_layout(n).total; }
 
+void release_inverse_partitions(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return;
+  std::lock_guard<std::mutex> lock(g_part_mu);
+  drop_partitions(g_part[dev]);
+}
+
 es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev, char* scratch,
-                      void* stream) {
+                      void* stream, bool split) {
   cudaStream_t st = (cudaStream_t)stream;
   InvLayout L = inverse_layout(n);
   bool use_smem;
@@ -943,10 +1204,29 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
   ES_CHECK(cuda_status(cudaMemsetAsync(gp.used, 0, (size_t)kNumPrimes * n, st), "memset used"));
   ES_CHECK(cuda_status(cudaMemsetAsync(gp.bad, 0, (size_t)kNumPrimes * 4, st), "memset bad"));
   ES_CHECK(launch_residues_matrix(A_dev, n, gp.ld, gp.W, st));
-  if (nbp == 32)
+  bool done = false;
+  if (nbp == 32 && n <= 1024 && split) {
+    int dev = 0;
+    ES_CHECK(cuda_status(cudaGetDevice(&dev), "get device"));
+    if (dev >= 0 && dev < kMaxDevices) {
+      std::lock_guard<std::mutex> lock(g_part_mu);
+      Partitions& P = g_part[dev];
+      if (!P.tried) {
+        P.tried = true;
+        P.ok = make_partitions(dev, P);
+      }
+      if (P.ok) {
+        ES_CHECK(run_blocks64_split(gp, n, st, P));
+        done = true;
+      }
+    }
+  }
+  if (done) {
+  } else if (nbp == 32) {
     ES_CHECK(run_blocks64(gp, n, use_smem, st));
-  else
+  } else {
     ES_CHECK(run_blocks16(gp, n, use_smem, st));
+  }
   k_gj_pinv<<<dim3((unsigned)((n + 255) / 256), kNumPrimes), 256, 0, st>>>(gp);
   count_launch(2);  // pinv + permute
   ES_CHECK(cuda_status(cudaGetLastError(), "k_gj_pinv"));

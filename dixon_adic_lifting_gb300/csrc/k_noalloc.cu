@@ -59,6 +59,7 @@ extern "C" es_status es_inverse_mod_device_noalloc(const int64_t* A_dev, int64_t
     es::g_noalloc_ptr[dev] = p;
   }
   cudaStream_t st = (cudaStream_t)stream;  // NULL: the legacy default stream (no stream is created)
-  ES_CHECK(es::run_inverse(A_dev, n, B_dev, good_dev, static_cast<char*>(es::g_noalloc_ptr[dev]), st));
+  // one stream, no SM partitions: this entry point creates nothing
+  ES_CHECK(es::run_inverse(A_dev, n, B_dev, good_dev, static_cast<char*>(es::g_noalloc_ptr[dev]), st, false));
   return es::cuda_status(cudaStreamSynchronize(st), "es_inverse_mod_device_noalloc");
 }

@@ -416,6 +416,7 @@ es_status es_release_workspace(void) {
   d.digits = nullptr;
   d.hdigits = nullptr;
   d.ws_size = d.digits_size = d.hdigits_size = 0;
+  es::release_inverse_partitions(es::current_device());
   return ES_OK;
 }
 
