@@ -44,13 +44,18 @@ namespace {
 constexpr int kMuWords = 13;  // Barrett reciprocal floor(b^(LG-1+13) / Q), b = 2^32
 constexpr int kZExtra = 12;   // Z < b^(LG + 11)
 constexpr int kDigitWords = 2 * kDigitLimbs;
+// G rows: word w of G_i at [i * g_stride(LG) + kGPad + w], zeros around it,
+// so a thread can load the 16 words ending at its 4 output columns aligned.
+constexpr int kGPad = 16;
+inline int64_t g_stride(int64_t LG) { return (LG + 3) / 4 * 4 + 2 * kGPad; }
 
 struct RParams {
   const uint32_t* D;      // digits as 32-bit words: [m][nc][12]
   int64_t nc;
   int mp;                 // digits used (m')
   int LG;                 // 32-bit words of Q
-  const uint32_t* G;      // [mp][LG]  G_i = d P'^i mod Q
+  const uint32_t* G;      // [mp][GS]  G_i = d P'^i mod Q (see g_stride)
+  int64_t GS;
   const uint32_t* OFF;    // [LG]      Q - H
   const uint32_t* Q;      // [LG]
   const uint32_t* Qhalf;  // [LG]      (Q - 1) / 2
@@ -66,6 +71,13 @@ __device__ __forceinline__ void mac(uint64_t& lo, uint32_t& hi, uint32_t a, uint
   uint64_t p = (uint64_t)a * b;
   lo += p;
   hi += (lo < p) ? 1u : 0u;
+}
+
+// acc (96 bits, little-endian words) += x y, one carry chain
+__device__ __forceinline__ void mac96(uint32_t (&acc)[3], uint32_t x, uint32_t y) {
+  asm("mad.lo.cc.u32 %0, %3, %4, %0;\n\tmadc.hi.cc.u32 %1, %3, %4, %1;\n\taddc.u32 %2, %2, 0;"
+      : "+r"(acc[0]), "+r"(acc[1]), "+r"(acc[2])
+      : "r"(x), "r"(y));
 }
 
 __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
@@ -92,24 +104,42 @@ __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
     }
   }
   __syncthreads();
-  // Z word columns: Z[w] = OFF[w] + sum_i sum_l x'_i[l] G_i[w - l]
-  for (int w = tid; w < LZ; w += nt) {
-    uint64_t lo = w < LG ? p.OFF[w] : 0;
-    uint32_t hi = 0;
-    const int lmin = w - LG + 1 > 0 ? w - LG + 1 : 0;
-    const int lmax = w < kDigitWords - 1 ? w : kDigitWords - 1;
-    for (int i = 0; i < mp; ++i) {
-      const uint32_t* Gi = p.G + (size_t)i * LG + w;
-      const uint32_t* xi = xs + i * kDigitWords;
-      if (lmin == 0 && lmax == kDigitWords - 1) {
+  // Z word columns: Z[w] = OFF[w] + sum_i sum_l x'_i[l] G_i[w - l].  A thread
+  // owns 4 consecutive columns: per digit it loads the 16 words of G_i they
+  // need (4 aligned 16-byte loads) and the digit's 12 words, then 48 96-bit MACs.
+  for (int w0 = 4 * tid; w0 < LZ; w0 += 4 * nt) {
+    uint32_t acc[4][3];
 #pragma unroll
-        for (int l = 0; l < kDigitWords; ++l) mac(lo, hi, xi[l], __ldg(Gi - l));
-      } else {
-        for (int l = lmin; l <= lmax; ++l) mac(lo, hi, xi[l], __ldg(Gi - l));
-      }
+    for (int o = 0; o < 4; ++o) {
+      acc[o][0] = w0 + o < LG ? p.OFF[w0 + o] : 0u;
+      acc[o][1] = 0u;
+      acc[o][2] = 0u;
     }
-    Zlo[w] = lo;
-    Zhi[w] = hi;
+    for (int i = 0; i < mp; ++i) {
+      const uint4* gr = reinterpret_cast<const uint4*>(p.G + (size_t)i * p.GS + kGPad + w0 - 12);
+      const uint4* xr = reinterpret_cast<const uint4*>(xs + i * kDigitWords);
+      uint32_t g[16], x[kDigitWords];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint4 v = __ldg(gr + h);
+        g[4 * h] = v.x, g[4 * h + 1] = v.y, g[4 * h + 2] = v.z, g[4 * h + 3] = v.w;
+      }
+#pragma unroll
+      for (int h = 0; h < kDigitWords / 4; ++h) {
+        const uint4 v = xr[h];
+        x[4 * h] = v.x, x[4 * h + 1] = v.y, x[4 * h + 2] = v.z, x[4 * h + 3] = v.w;
+      }
+#pragma unroll
+      for (int o = 0; o < 4; ++o)
+#pragma unroll
+        for (int l = 0; l < kDigitWords; ++l) mac96(acc[o], x[l], g[o + 12 - l]);
+    }
+#pragma unroll
+    for (int o = 0; o < 4; ++o)
+      if (w0 + o < LZ) {
+        Zlo[w0 + o] = (uint64_t)acc[o][0] | ((uint64_t)acc[o][1] << 32);
+        Zhi[w0 + o] = acc[o][2];
+      }
   }
   __syncthreads();
   if (tid == 0) {
@@ -267,7 +297,7 @@ size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t n
   const int64_t W0 = (num_bits + 2 + 63) / 64, W1 = (den_bits + 1 + 63) / 64;
   const int64_t W = W0 > W1 ? W0 : W1;
   Layout L;
-  L.add((size_t)mp * LG * 4);
+  L.add((size_t)mp * g_stride(LG) * 4);
   L.add((size_t)LG * 4 * 3);
   L.add(kMuWords * 4 + kDigitWords * 4);
   L.add((size_t)nc * W * 8);
@@ -275,11 +305,13 @@ size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t n
   return L.total;
 }
 
-// G_{i+1} = G_i P' mod Q for i < mp, written as LG 32-bit words each, and
+// G_{i+1} = G_i P' mod Q for i < mp, written as LG 32-bit words each (row i
+// at out + i GS + kGPad), and
 // their sum.  Knuth's division with the divisor normalised once: G is kept
 // shifted left by the normalising shift s, so each step is one multiply by
 // the 6-limb P' and a division whose quotient has at most 6 limbs, in place.
-static void g_chain(const Nat& Q, const Nat& P, const Nat& g0, int32_t mp, int64_t LG, uint32_t* out, Nat* sum) {
+static void g_chain(const Nat& Q, const Nat& P, const Nat& g0, int32_t mp, int64_t LG, int64_t GS, uint32_t* out,
+                    Nat* sum) {
   using limb = big::limb;
   using u128 = unsigned __int128;
   const size_t n = Q.size(), pn = P.size();
@@ -301,7 +333,7 @@ static void g_chain(const Nat& Q, const Nat& P, const Nat& g0, int32_t mp, int64
     big::trim(gi);
     for (int64_t w = 0; w < LG; ++w) {
       const size_t l = (size_t)w / 2;
-      out[(size_t)i * LG + w] = l < n ? (uint32_t)(plain[l] >> (32 * (w & 1))) : 0u;
+      out[(size_t)i * GS + kGPad + w] = l < n ? (uint32_t)(plain[l] >> (32 * (w & 1))) : 0u;
     }
     big::add_in(*sum, gi);
     if (i + 1 == mp) break;
@@ -404,7 +436,7 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
   R.LG = LG;
   R.W = W0 > W1 ? W0 : W1;
   Layout L;
-  R.oG = L.add((size_t)mp * LG * 4);
+  R.oG = L.add((size_t)mp * g_stride(LG) * 4);
   R.oC = L.add((size_t)LG * 4 * 3);
   R.oM = L.add(kMuWords * 4 + kDigitWords * 4);
   R.oN = L.add((size_t)R.nc * R.W * 8);
@@ -475,13 +507,14 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   out->limbs = W;
   out->num.assign((size_t)(nc * W), 0);
   std::vector<uint8_t> okh((size_t)nc);
-  std::vector<uint32_t> hG((size_t)mp * LG);
+  const int64_t GS = g_stride(LG);
+  std::vector<uint32_t> hG((size_t)mp * GS, 0u);
   for (int round = 0;; ++round) {
     if (round > 64) return ES_ERR_INTERNAL;
     // G_i = d P'^i mod Q, OFF = Q - ((P'-1)/2 sum_i G_i mod Q)
     Nat g, sum, rem;
     big::divmod(d, Q, nullptr, &g);
-    g_chain(Q, ps.P, g, mp, LG, hG.data(), &sum);
+    g_chain(Q, ps.P, g, mp, LG, GS, hG.data(), &sum);
     big::divmod(big::mul(sum, ps.half), Q, nullptr, &rem);
     const Nat off = rem.empty() ? Nat{} : big::sub(Q, rem);
     to_words(off, LG, hC.data());
@@ -495,6 +528,7 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     rp.mp = mp;
     rp.LG = (int)LG;
     rp.G = reinterpret_cast<const uint32_t*>(scratch + oG);
+    rp.GS = GS;
     rp.OFF = reinterpret_cast<const uint32_t*>(scratch + oC);
     rp.Q = rp.OFF + LG;
     rp.Qhalf = rp.OFF + 2 * LG;
