@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--one-stream", action="store_true",
+                   help="inverse on the solve's stream alone (for profilers that do not see the SM partitions)")
     return p.parse_args()
 
 
@@ -223,7 +225,7 @@ def run_gb300(args, rank, local_rank, world):
     bt = torch.as_tensor(b, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
-        s = api.solve_device(At, bt)
+        s = api.solve_device(At, bt, one_stream=args.one_stream)
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = Clocks(local_rank)
@@ -233,7 +235,7 @@ def run_gb300(args, rank, local_rank, world):
     for k in range(args.steps):
         flush.zero_()
         ev[k][0].record(stream)
-        s = api.solve_device(At, bt, stream=stream, timing=2)
+        s = api.solve_device(At, bt, stream=stream, timing=2, one_stream=args.one_stream)
         ev[k][1].record(stream)
         sols.append(s)
     barrier()

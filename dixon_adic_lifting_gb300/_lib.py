@@ -30,6 +30,7 @@ NUM_PHASES = 6
 FAULT = {"residues": 1, "inverse": 2, "lift": 3, "recon": 4, "nomem": 5, "lift_wait": 6}
 FLAG_HOST_RECON = 1
 FLAG_STEP_LIFT = 2
+FLAG_ONE_STREAM = 4
 
 
 class es_options(ctypes.Structure):

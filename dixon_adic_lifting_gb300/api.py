@@ -75,9 +75,10 @@ class Solution:
 
 
 def _opts(stream=None, threads=0, timing=False, fault=None, max_device_bytes=0, host_recon=False,
-          step_lift=False):
+          step_lift=False, one_stream=False):
     o = L.es_options()
-    o.flags = (L.FLAG_HOST_RECON if host_recon else 0) | (L.FLAG_STEP_LIFT if step_lift else 0)
+    o.flags = ((L.FLAG_HOST_RECON if host_recon else 0) | (L.FLAG_STEP_LIFT if step_lift else 0)
+               | (L.FLAG_ONE_STREAM if one_stream else 0))
     o.stream = ctypes.c_void_p(stream) if stream else None
     o.max_device_bytes = max_device_bytes
     o.fault_stage = L.FAULT[fault] if isinstance(fault, str) else int(fault or 0)
@@ -123,7 +124,8 @@ def _as_host_i64(x) -> np.ndarray:
 
 
 def solve_canonical(A, b, *, threads: int = 0, timing: bool = False, fault=None,
-                    max_device_bytes: int = 0, host_recon: bool = False, step_lift: bool = False) -> Optional[Solution]:
+                    max_device_bytes: int = 0, host_recon: bool = False, step_lift: bool = False,
+                    one_stream: bool = False) -> Optional[Solution]:
     """Exact solution of A x = b from host arrays (es_solve), or None if singular."""
     lib = L.load()
     A = _as_host_i64(A)
@@ -133,7 +135,7 @@ def solve_canonical(A, b, *, threads: int = 0, timing: bool = False, fault=None,
     if A.ndim != 2 or A.shape[0] != A.shape[1] or b.shape[0] != A.shape[0]:
         raise ValueError("A must be [n, n] and b [n, c]")
     out = ctypes.c_void_p()
-    o = _opts(None, threads, timing, fault, max_device_bytes, host_recon, step_lift)
+    o = _opts(None, threads, timing, fault, max_device_bytes, host_recon, step_lift, one_stream)
     st = lib.es_solve(A.ctypes.data, b.ctypes.data, A.shape[0], b.shape[1], ctypes.byref(o), ctypes.byref(out))
     if st == L.ES_SINGULAR:
         return None
@@ -155,7 +157,8 @@ def _stream_handle(stream):
 
 
 def solve_device(A_t, b_t, *, stream=None, threads: int = 0, timing: bool = False, fault=None,
-                 max_device_bytes: int = 0, host_recon: bool = False, step_lift: bool = False) -> Optional[Solution]:
+                 max_device_bytes: int = 0, host_recon: bool = False, step_lift: bool = False,
+                 one_stream: bool = False) -> Optional[Solution]:
     """Exact solution with A, b already on the GPU (int64 CUDA tensors), es_solve_device."""
     lib = L.load()
     if b_t.dim() == 1:
@@ -163,7 +166,7 @@ def solve_device(A_t, b_t, *, stream=None, threads: int = 0, timing: bool = Fals
     A_t = A_t.contiguous()
     b_t = b_t.contiguous()
     out = ctypes.c_void_p()
-    o = _opts(_stream_handle(stream), threads, timing, fault, max_device_bytes, host_recon, step_lift)
+    o = _opts(_stream_handle(stream), threads, timing, fault, max_device_bytes, host_recon, step_lift, one_stream)
     st = lib.es_solve_device(A_t.data_ptr(), b_t.data_ptr(), A_t.shape[0], b_t.shape[1], ctypes.byref(o),
                              ctypes.byref(out))
     if st == L.ES_SINGULAR:

@@ -511,10 +511,25 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   std::vector<uint32_t> hG((size_t)mp * GS, 0u);
   for (int round = 0;; ++round) {
     if (round > 64) return ES_ERR_INTERNAL;
-    // G_i = d P'^i mod Q, OFF = Q - ((P'-1)/2 sum_i G_i mod Q)
-    Nat g, sum, rem;
-    big::divmod(d, Q, nullptr, &g);
-    g_chain(Q, ps.P, g, mp, LG, GS, hG.data(), &sum);
+    // G_i = d P'^i mod Q, OFF = Q - ((P'-1)/2 sum_i G_i mod Q).  The chain is
+    // cut into segments run on host threads: since Q = P'^mp, a segment's
+    // first term is G_i0 = (d mod P'^(mp - i0)) P'^i0, below Q already.
+    Nat sum, rem;
+    const int nseg = mp >= 32 ? 4 : 1;
+    std::vector<Nat> ssum((size_t)nseg);
+    parallel_for(nseg, threads > 0 && threads < nseg ? threads : nseg, [&](int64_t t) {
+      const int32_t i0 = (int32_t)(t * mp / nseg), i1 = (int32_t)((t + 1) * mp / nseg);
+      Nat g;
+      if (i0 == 0) {
+        big::divmod(d, Q, nullptr, &g);
+      } else {
+        Nat low;
+        big::divmod(d, pow_nat(ps.P, mp - i0), nullptr, &low);
+        g = big::mul(low, pow_nat(ps.P, i0));
+      }
+      g_chain(Q, ps.P, g, i1 - i0, LG, GS, hG.data() + (size_t)i0 * GS, &ssum[(size_t)t]);
+    });
+    for (auto& v : ssum) big::add_in(sum, v);
     big::divmod(big::mul(sum, ps.half), Q, nullptr, &rem);
     const Nat off = rem.empty() ? Nat{} : big::sub(Q, rem);
     to_words(off, LG, hC.data());

@@ -114,6 +114,7 @@ struct Options {
   bool kernel_events = false;
   bool host_recon = false;
   bool step_lift = false;
+  bool one_stream = false;
 };
 Options read_options(const es_options* o) {
   Options r;
@@ -126,6 +127,7 @@ Options read_options(const es_options* o) {
     r.kernel_events = o->timing >= 2;
     r.host_recon = (o->flags & ES_FLAG_HOST_RECON) != 0;
     r.step_lift = (o->flags & ES_FLAG_STEP_LIFT) != 0;
+    r.one_stream = (o->flags & ES_FLAG_ONE_STREAM) != 0;
   }
   return r;
 }
@@ -222,7 +224,7 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   // batched modular inverse
   int8_t* B = reinterpret_cast<int8_t*>(ws + SL.B);
   uint8_t* good_dev = reinterpret_cast<uint8_t*>(ws + SL.good);
-  ES_CHECK(run_inverse(A, n, B, good_dev, ws + SL.work, st));
+  ES_CHECK(run_inverse(A, n, B, good_dev, ws + SL.work, st, !o.one_stream));
   uint8_t good[kNumPrimes];
   ES_CHECK(cuda_status(cudaMemcpyAsync(good, good_dev, kNumPrimes, cudaMemcpyDeviceToHost, st), "good D2H"));
   ES_CHECK(cuda_status(cudaStreamSynchronize(st), "inverse sync"));

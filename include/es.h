@@ -69,6 +69,7 @@ typedef struct es_options {
 /* es_options.flags */
 #define ES_FLAG_HOST_RECON 1 /* reconstruct on the host even when the GPU numerator pass applies */
 #define ES_FLAG_STEP_LIFT 2  /* c == 1: run the lift as per-step kernels instead of the fused launch */
+#define ES_FLAG_ONE_STREAM 4 /* run the inverse on the caller's stream alone, without the two SM partitions */
 
 /* Fault injection points (es_options.fault_stage): the named stage returns
  * the given status without running; used to test error propagation. */

@@ -218,6 +218,21 @@ def test_fused_lift_matches_step_kernels(torch_cuda, n, bits):
         check_identity(A, b, fused.N, fused.d)
 
 
+@pytest.mark.parametrize("n", [97, 300, 640, 1000])
+def test_split_inverse_matches_one_stream(torch_cuda, n):
+    """The inverse's default schedule (next 64-column block factorized on one SM
+    partition while the previous block's update runs on the other) and the
+    single-stream schedule are independent routes to the same unique B_j;
+    the solves agree bit for bit and are exact."""
+    A, b = inputs.uniform(n, 1, -(1 << 23), 1 << 23, seed=2000 + n)
+    split = api.solve_canonical(A, b)
+    one = api.solve_canonical(A, b, one_stream=True)
+    assert (split.N, split.d) == (one.N, one.d)
+    assert split.launches > one.launches  # the split schedule stages and updates in separate launches
+    if n <= 300:
+        check_identity(A, b, split.N, split.d)
+
+
 # ------------------------------------------------------------------ solve
 def n32_case(seed):
     with open(os.path.join(GOLDEN, "n32_attempts.json")) as f:
