@@ -782,45 +782,84 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
   }
 }
 
-// Update on the int8 tensor-core path: the depth-KW contraction F U (KW = 32
-// or 64) is KW / 32 mma.sync.m16n8k32 (s8 x s8 -> s32) per 16 x 8 output
-// tile.  F = W[:, k0 .. k0 + KW) is read straight from W and U^T (row width
-// utw bytes, U^T[col][a] = pivot row a's entry of column col) from the staging
-// buffer, both as 32-bit fragment loads: A (row-major 16 x 32) reg r holds row
-// g + 8 (r & 1), columns 4 t + 16 (r >> 1) + 0..3; B (column-major 32 x 8)
-// reg r holds column g, rows 4 t + 16 r + 0..3; C reg r holds row
-// g + 8 (r >> 1), column 2 t + (r & 1)  (g = lane / 4, t = lane % 4).
-// KW = 64 is exact too: 64 * 125^2 + 125 < 2^31.  CTA tile 64 rows x 128
-// columns, 8 warps of 32 x 32.  Columns updated: 32-column segments col0 with
-// cbase <= col0 < cend outside [xb, xe) (which holds at least the panel).
-__device__ __forceinline__ void mma_s8_16x8x32(int32_t (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+// Update on the tensor cores, f16 x f16 -> f32 (mma.sync.m16n8k16): a
+// balanced residue (|x| <= 125) is exact in f16, and every depth-KW sum of
+// products plus the old entry (|s| <= 64 * 125^2 + 125 < 2^20) is exact in
+// the f32 accumulator, so the contraction F U (KW = 32 or 64) is exact.  On
+// this part the f16 path has four times the rate of the s8 one.
+//
+// F = W[:, k0 .. k0 + KW) and U^T (row width utw bytes, U^T[col][a] = pivot
+// row a's entry of column col) are staged as int8 in shared memory with
+// 16-byte loads (rows of 64 bytes, chunk c of row r at chunk c ^ ((r >> 1) & 3):
+// conflict-free for the stores and for ldmatrix), read with ldmatrix as s8
+// fragments of m16n8k32 shape and widened to f16 in registers.  A 32-bit s8
+// fragment word holds four consecutive k; its low pair goes to the f16
+// fragment register for k-slots 2t, 2t + 1 and its high pair to 2t + 8, 2t + 9,
+// on both operands, so the products pair up the same k.
+//
+// The residue of v = old + (F U)[i][t] is taken in f32 as v - q rint(v / q~),
+// q~ = fl(1/q): the quotient estimate errs by at most |v| / q * 2^-24 <
+// 1/(16 q), while v / q is at least 1/(2 q) away from a half-integer (q odd),
+// so the rounding is always the exact one and the result is the balanced
+// residue.  CTA tile 64 rows x 128 columns, 8 warps of 32 x 32.  Columns
+// updated: 32-column segments col0 with cbase <= col0 < cend outside
+// [xb, xe) (which holds at least the panel).
+__device__ __forceinline__ void mma_f16_16x8x16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
-      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+
+// Four signed bytes -> f16x2 of bytes 0, 1 (lo) and of bytes 2, 3 (hi): with
+// u = x + 128 (the top bit flipped), 0x64uu is the f16 1024 + u, and
+// 1024 + u - 1152 = x exactly.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+struct QInvTable {
+  float v[kNumPrimes];
+};
+constexpr QInvTable make_qinv_table() {
+  QInvTable t{};
+  for (int i = 0; i < kNumPrimes; ++i) t.v[i] = 1.0f / (float)kPrimes[i];
+  return t;
+}
+__constant__ QInvTable c_qinv = make_qinv_table();
+
 __device__ __forceinline__ int rot3(int r) { return ((r << 1) | ((r >> 2) & 1)) & 7; }
+__device__ __forceinline__ int swz64(int r, int c) { return r * 64 + 16 * (c ^ ((r >> 1) & 3)); }
 
 template <int KW>
 __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, const int8_t* __restrict__ UT, int utw,
                                                        int64_t k0, int64_t cbase, int64_t cend, int64_t xb,
                                                        int64_t xe) {
+  constexpr int KC = KW / 16;  // 16-byte chunks per operand row
   const int j = blockIdx.z;
   if (p.bad[j]) return;
-  const ModQ m = c_modq.v[j];
   const int64_t n = p.n, ld = p.ld;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-  const int64_t row0 = (int64_t)blockIdx.y * 64 + (warp >> 2) * 32;
-  const int64_t col0 = cbase + (int64_t)blockIdx.x * 128 + (warp & 3) * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t rowc = (int64_t)blockIdx.y * 64, colc = cbase + (int64_t)blockIdx.x * 128;
+  const int64_t row0 = rowc + (warp >> 2) * 32;
+  const int64_t col0 = colc + (warp & 3) * 32;
   int8_t* Wj = p.W + (int64_t)j * n * ld;
   const int8_t* UTj = UT + (int64_t)j * ld * utw;
-  // per warp: its 32 x 32 tile of F U.  Within a row the 16-byte chunk c is
-  // stored at chunk c ^ rot(row) (rot = 3-bit left rotation of row & 7), which
-  // makes both the 8-byte fragment stores (per half-warp) and the 16-byte row
-  // reads (per quarter-warp) hit 32 distinct banks.
-  __shared__ __align__(16) int32_t Cs[8][32][32];
+  __shared__ __align__(16) float Cs[8][32][32];
+  __shared__ __align__(16) uint8_t As[64 * 64];
+  __shared__ __align__(16) uint8_t Bs[128 * 64];
   // this thread's output row segment (row0 + lane, 32 columns), fetched early;
   // segments are 32-column aligned like the panel: one either lies in it or misses it
   const int64_t orow = row0 + lane;
@@ -830,66 +869,104 @@ __global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, const int8_t*
     old0 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0);
     if (col0 + 16 < ld) old1 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0 + 16);
   }
-  uint32_t a[KW / 32][2][4], b[KW / 32][4][2];
-#pragma unroll
-  for (int kk = 0; kk < KW / 32; ++kk) {
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int64_t row = row0 + 16 * mi + g + 8 * (r & 1);
-        const int64_t col = k0 + 32 * kk + 4 * t + 16 * (r >> 1);
-        a[kk][mi][r] = (row < n && col < ld) ? *reinterpret_cast<const uint32_t*>(Wj + row * ld + col) : 0u;
-      }
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int64_t col = col0 + 8 * ni + g;
-        b[kk][ni][r] =
-            col < ld ? *reinterpret_cast<const uint32_t*>(UTj + col * utw + 32 * kk + 4 * t + 16 * r) : 0u;
-      }
+  for (int i = tid; i < 64 * KC; i += 256) {
+    const int r = i / KC, c = i % KC;
+    const int64_t row = rowc + r, col = k0 + 16 * c;
+    int4 v = make_int4(0, 0, 0, 0);
+    if (row < n && col < ld) v = *reinterpret_cast<const int4*>(Wj + row * ld + col);
+    *reinterpret_cast<int4*>(As + swz64(r, c)) = v;
   }
+  for (int i = tid; i < 128 * KC; i += 256) {
+    const int r = i / KC, c = i % KC;
+    const int64_t col = colc + r;
+    int4 v = make_int4(0, 0, 0, 0);
+    if (col < ld) v = *reinterpret_cast<const int4*>(UTj + col * utw + 16 * c);
+    *reinterpret_cast<int4*>(Bs + swz64(r, c)) = v;
+  }
+  __syncthreads();
+  const int mi8 = lane >> 3, rr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+  float acc[2][4][4];
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-    for (int ni = 0; ni < 4; ++ni) {
-      int32_t c[4] = {0, 0, 0, 0};
+    for (int ni = 0; ni < 4; ++ni)
 #pragma unroll
-      for (int kk = 0; kk < KW / 32; ++kk) mma_s8_16x8x32(c, a[kk][mi], b[kk][ni]);
-      const int cw = 8 * ni + 2 * t, sw = (4 * ((cw >> 2) ^ rot3(g))) | (cw & 3);  // rows g, g + 8: same rot
-      *reinterpret_cast<int2*>(&Cs[warp][16 * mi + g][sw]) = make_int2(c[0], c[1]);
-      *reinterpret_cast<int2*>(&Cs[warp][16 * mi + g + 8][sw]) = make_int2(c[2], c[3]);
+      for (int r = 0; r < 4; ++r) acc[mi][ni][r] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KW / 32; ++kk) {
+    // s8 fragments: A reg r = rows g + 8 (r & 1), k 4 t + 16 (r >> 1) + 0..3;
+    // B reg r of column tile 2 np + (i >> 1) (i = 2 (ni & 1) + r) = column g, k 4 t + 16 r + 0..3
+    uint32_t a8[2][4], b8[2][4];
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+      ldsm_x4(a8[mi], As + swz64((warp >> 2) * 32 + 16 * mi + rr + 8 * (mi8 & 1), 2 * kk + (mi8 >> 1)));
+#pragma unroll
+    for (int np = 0; np < 2; ++np)
+      ldsm_x4(b8[np], Bs + swz64((warp & 3) * 32 + 8 * (2 * np + (mi8 >> 1)) + rr, 2 * kk + (mi8 & 1)));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t af[2][4], bf[4][2];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        s8x4_to_f16(a8[mi][2 * h], af[mi][0], af[mi][2]);
+        s8x4_to_f16(a8[mi][2 * h + 1], af[mi][1], af[mi][3]);
+      }
+#pragma unroll
+      for (int ni = 0; ni < 4; ++ni) s8x4_to_f16(b8[ni >> 1][2 * (ni & 1) + h], bf[ni][0], bf[ni][1]);
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bf[ni]);
     }
+  }
+  // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1); within a row the
+  // 16-byte chunk c sits at chunk c ^ rot(row) (rot = 3-bit left rotation of
+  // row & 7): conflict-free for the 8-byte stores (per half-warp) and the
+  // 16-byte row reads (per quarter-warp)
+  {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int ni = 0; ni < 4; ++ni) {
+        const int cw = 8 * ni + 2 * t, sw = (4 * ((cw >> 2) ^ rot3(g))) | (cw & 3);  // rows g, g + 8: same rot
+        *reinterpret_cast<float2*>(&Cs[warp][16 * mi + g][sw]) = make_float2(acc[mi][ni][0], acc[mi][ni][1]);
+        *reinterpret_cast<float2*>(&Cs[warp][16 * mi + g + 8][sw]) = make_float2(acc[mi][ni][2], acc[mi][ni][3]);
+      }
+  }
   __syncwarp();
   if (!rowok) return;
-  uint32_t w[8] = {(uint32_t)old0.x, (uint32_t)old0.y, (uint32_t)old0.z, (uint32_t)old0.w,
-                   (uint32_t)old1.x, (uint32_t)old1.y, (uint32_t)old1.z, (uint32_t)old1.w};
-  int32_t cv[32];
+  const float qf = (float)c_modq.v[j].q, qinv = c_qinv.v[j];
+  const float kM = 12582912.0f;  // 1.5 * 2^23: x + kM has ulp 1 for |x| < 2^22
+  const uint32_t w[8] = {(uint32_t)old0.x, (uint32_t)old0.y, (uint32_t)old0.z, (uint32_t)old0.w,
+                         (uint32_t)old1.x, (uint32_t)old1.y, (uint32_t)old1.z, (uint32_t)old1.w};
+  uint32_t o[8];
   const int rl = rot3(lane);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const int4 c4 = *reinterpret_cast<const int4*>(&Cs[warp][lane][4 * (q ^ rl)]);
-    cv[4 * q] = c4.x;
-    cv[4 * q + 1] = c4.y;
-    cv[4 * q + 2] = c4.z;
-    cv[4 * q + 3] = c4.w;
-  }
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint32_t x = 0;
+    const float4 c4 = *reinterpret_cast<const float4*>(&Cs[warp][lane][4 * (q ^ rl)]);
+    const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+    const uint32_t wu = w[q] ^ 0x80808080u;  // bytes x + 128
+    uint32_t rb[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int cc = 4 * q + u;
-      const int64_t col = col0 + cc;
-      int32_t val = sbyte(w[q], u);
-      if (col < n) val = reduce_bal(val + cv[cc], m);
-      x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
+      // 2^23 + x + 128 from the bits 0x4B0000uu
+      const float fb = __int_as_float((int)__byte_perm(wu, 0x4B000000u, 0x7540 + u));
+      const float v = __fadd_rn(__fadd_rn(cv[u], fb), -8388736.0f);
+      const float k = __fadd_rn(__fmaf_rn(v, qinv, kM), -kM);
+      rb[u] = (uint32_t)__float_as_int(__fadd_rn(__fmaf_rn(-k, qf, v), kM));  // low byte = residue
     }
-    w[q] = x;
+    o[q] = __byte_perm(__byte_perm(rb[0], rb[1], 0x0040), __byte_perm(rb[2], rb[3], 0x0040), 0x5410);
   }
-  *reinterpret_cast<int4*>(Wj + orow * ld + col0) = make_int4(w[0], w[1], w[2], w[3]);
-  if (col0 + 16 < ld) *reinterpret_cast<int4*>(Wj + orow * ld + col0 + 16) = make_int4(w[4], w[5], w[6], w[7]);
+  if (col0 + 32 > n) {  // columns n .. ld - 1 keep their zero padding
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (col0 + 4 * q + u >= n) o[q] = (o[q] & ~(0xFFu << (8 * u))) | (w[q] & (0xFFu << (8 * u)));
+  }
+  *reinterpret_cast<int4*>(Wj + orow * ld + col0) = make_int4(o[0], o[1], o[2], o[3]);
+  if (col0 + 16 < ld) *reinterpret_cast<int4*>(Wj + orow * ld + col0 + 16) = make_int4(o[4], o[5], o[6], o[7]);
 }
 
 // ------------------------------------------------------------------ permute
