@@ -53,6 +53,66 @@ struct GJParams {
 
 __device__ __forceinline__ int32_t sbyte(uint32_t w, int u) { return (int32_t)(w << (24 - 8 * u)) >> 24; }
 
+// fl(1/q) per prime (correctly rounded)
+struct QInvTable {
+  float v[kNumPrimes];
+};
+constexpr QInvTable make_qinv_table() {
+  QInvTable t{};
+  for (int i = 0; i < kNumPrimes; ++i) t.v[i] = 1.0f / (float)kPrimes[i];
+  return t;
+}
+__constant__ QInvTable c_qinv = make_qinv_table();
+
+// Exact residue arithmetic in f32 for |x| < 2^20: bal(x) = x - q rint(x fl(1/q))
+// (the quotient estimate errs by less than 1/(16 q), and x / q is never
+// within 1/(2 q) of a half-integer since q is odd).
+struct ModF {
+  float q, qinv;
+};
+__device__ __forceinline__ float fred(float x, const ModF& mf) {
+  const float kM = 12582912.0f;  // 1.5 * 2^23
+  const float k = __fadd_rn(__fmaf_rn(x, mf.qinv, kM), -kM);
+  return __fmaf_rn(-k, mf.q, x);
+}
+// 2^23 + 128 + x for the signed byte x = byte u of w: the f32 with bits 0x4B0000uu, uu = x + 128
+__device__ __forceinline__ float sbyte_fb(uint32_t w, int u) {
+  return __int_as_float((int)__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540 + u));
+}
+// signed byte u of w as f32
+__device__ __forceinline__ float sbyte_f(uint32_t w, int u) { return __fadd_rn(sbyte_fb(w, u), -8388736.0f); }
+// low byte of an exact integer-valued f32 in (-2^22, 2^22), two's complement
+__device__ __forceinline__ uint32_t fbyte(float x) { return (uint32_t)__float_as_int(__fadd_rn(x, 12582912.0f)) & 0xFFu; }
+
+__device__ __forceinline__ void mma_f16_16x8x16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+
+// Four signed bytes -> f16x2 of bytes 0, 1 (lo) and of bytes 2, 3 (hi): with
+// u = x + 128 (the top bit flipped), 0x64uu is the f16 1024 + u, and
+// 1024 + u - 1152 = x exactly.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x4140);
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+
+
+
 
 // ------------------------------------------------------------------ panel
 template <int NBP>
@@ -343,25 +403,37 @@ __global__ void __launch_bounds__(1024, 1) k_gj_panel_reg(GJParams p, int64_t k0
 // and stored already rotated by warp 0; the row is rotated back once, by kb,
 // when the panel is written.  Rows of thread t: t, t + T, ..., t + T (R - 1).
 struct PanelSmem {
-  uint8_t inv[256];                  // inverses mod q
-  __align__(16) int wmin[32];        // per-warp pivot candidates
-  __align__(16) int32_t raw[32];     // pivot row, natural column order
-  __align__(16) int32_t prow[32];    // scaled pivot row, rotated: entry t = column (a + t) mod NBP
-  __align__(16) int32_t pupd[32];    // same with the pivot entry + 1
-  int piv[32];                       // the panel's pivot rows
-  __align__(16) uint32_t u[32][8];   // a narrow update's U: column c, pivot rows 4w .. 4w + 3 in word w
+  uint8_t inv[256];                   // inverses mod q
+  __align__(16) int wmin[2][32];      // per-warp pivot candidate (row), by step parity
+  __align__(16) float cand[2][32][32];  // per-warp candidate row's entries, reduced, rotated frame
+  int piv[32];                        // the panel's pivot rows
+  __align__(16) uint32_t u[32][8];    // a narrow update's U: column c, pivot rows 4w .. 4w + 3 in word w
 };
 
 // The kb exchange steps of the panel at k0; writes the reduced panel back to
-// W and the used flags, and leaves each of the thread's rows as 8 packed
-// words in Fp.  False when the prime has no pivot (it is flagged bad).
+// W and the used flags.  False when the prime has no pivot (it is flagged bad).
+//
+// Rows live in registers as exact f32 in a rotated frame (entry t of step a
+// = column (a + t) mod NBP, so the pivot column is always entry 0).  One
+// barrier per step: every warp publishes its own lowest unused row with a
+// nonzero pivot-column entry, reduced by the warp's lanes, and after the
+// barrier every thread takes the lowest of them, p = its pivot entry, and
+// updates its rows with the multiplier f' = f p^-1:  v[t] <- v[t] - f' raw[t],
+// pivot column <- -f'.  The pivot row itself is not scaled: it keeps raw with
+// the pivot entry set to 1 and a scale p^-1 that multiplies the whole row on
+// write-back (the multiplier of a scaled row's stored form is again its
+// stored pivot entry times p^-1, so later steps treat it like any other row).
+// Entries stay below 32 * 125^2 + 125 < 2^20 in magnitude.
 template <int NBP, int R, int T>
 __device__ __forceinline__ bool panel_factor(const GJParams& p, int j, const ModQ& m, int8_t* Wj, int64_t k0, int kb,
-                                             PanelSmem& S, uint32_t (&Fp)[R][NBP / 4]) {
+                                             PanelSmem& S) {
+  static_assert(NBP == 32, "one reduced entry per lane");
   const int n = (int)p.n, ld = (int)p.ld;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int32_t v[R][NBP];
-  bool used[R];
+  const ModF mf{(float)m.q, c_qinv.v[j]};
+  float v[R][NBP];
+  int32_t sc[R];  // 0: row not yet a pivot (used rows of earlier panels stay 0 too), else its scale
+  uint32_t usedm = 0;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int row = tid + T * i;
@@ -374,81 +446,76 @@ __device__ __forceinline__ bool panel_factor(const GJParams& p, int j, const Mod
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[i][c4 * 16 + q4 * 4 + u] = sbyte(ww[q4], u);
+        for (int u = 0; u < 4; ++u) v[i][c4 * 16 + q4 * 4 + u] = sbyte_f(ww[q4], u);
     }
-    used[i] = active ? p.used[(int64_t)j * n + row] != 0 : true;
+    if (!active || p.used[(int64_t)j * n + row] != 0) usedm |= 1u << i;
+    sc[i] = 0;
   }
   __syncthreads();
 #pragma unroll 1
   for (int a = 0; a < kb; ++a) {
-    int32_t f[R];
+    const int par = a & 1;
+    float f[R];
     int cand = INT_MAX;
 #pragma unroll
     for (int i = R - 1; i >= 0; --i) {  // rows grow with i: the smallest i wins
-      f[i] = reduce_bal(v[i][0], m);
-      if (!used[i] && f[i] != 0) cand = tid + T * i;
+      f[i] = fred(v[i][0], mf);
+      if (!((usedm >> i) & 1) && f[i] != 0.0f) cand = tid + T * i;
     }
-    cand = __reduce_min_sync(0xffffffffu, cand);
-    if (lane == 0) S.wmin[warp] = cand;
-    __syncthreads();  // (1) candidates of every warp
+    const int wc = __reduce_min_sync(0xffffffffu, cand);
+    if (wc != INT_MAX) {
+      float* slot = S.cand[par][warp];
+      if (cand == wc) {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+          if (tid + T * i == wc) {
+#pragma unroll
+            for (int t4 = 0; t4 < NBP / 4; ++t4)
+              *reinterpret_cast<float4*>(slot + 4 * t4) =
+                  make_float4(v[i][4 * t4], v[i][4 * t4 + 1], v[i][4 * t4 + 2], v[i][4 * t4 + 3]);
+          }
+      }
+      __syncwarp();
+      slot[lane] = fred(slot[lane], mf);
+    }
+    if (lane == 0) S.wmin[par][warp] = wc;
+    __syncthreads();  // the candidates of every warp
     int pr = INT_MAX;
 #pragma unroll
     for (int w4 = 0; w4 < T / 128; ++w4) {
-      const int4 c = *reinterpret_cast<const int4*>(S.wmin + 4 * w4);
+      const int4 c = *reinterpret_cast<const int4*>(&S.wmin[par][4 * w4]);
       pr = min(pr, min(min(c.x, c.y), min(c.z, c.w)));
     }
     if (pr == INT_MAX) {  // no pivot: q_j | det A
       if (tid == 0) p.bad[j] = 1;
       return false;
     }
+    const float* raw = S.cand[par][(pr % T) >> 5];
+    const int p0 = (int)raw[0];
+    const int32_t inv = (int32_t)S.inv[p0 < 0 ? p0 + (int)m.q : p0];
+    const float finv = (float)inv;
 #pragma unroll
-    for (int i = 0; i < R; ++i)
-      if (tid + T * i == pr) {
-#pragma unroll
-        for (int t = 0; t < NBP; ++t) S.raw[(a + t) & (NBP - 1)] = t == 0 ? f[i] : v[i][t];
-        used[i] = true;
+    for (int i = 0; i < R; ++i) {
+      // the pivot row takes multiplier 0 and pivot entry 1 (its scale records p^-1)
+      const bool is_piv = tid + T * i == pr;
+      if (is_piv) {
+        usedm |= 1u << i;
+        sc[i] = inv;
         S.piv[a] = pr;
         p.piv[(int64_t)j * n + k0 + a] = pr;
       }
-    __syncthreads();  // (2) raw pivot row
-    if (warp == 0) {
-      const int32_t pf = S.raw[a];
-      const uint32_t inv = S.inv[pf < 0 ? pf + (int32_t)m.q : pf];
-      for (int t = lane; t < NBP; t += 32) {
-        const int c = (a + t) & (NBP - 1);
-        const int32_t pt =
-            (t == 0) ? bal_from_unsigned(inv, m) : reduce_bal(reduce_bal(S.raw[c], m) * (int32_t)inv, m);
-        S.prow[t] = pt;
-        S.pupd[t] = (t == 0) ? pt + 1 : pt;
-      }
-    }
-    __syncthreads();  // (3) scaled pivot row
-    // v[t] <- (v[t + 1] - f u_{t + 1}), v[NBP - 1] <- (v[0] - f u_0); the pivot row takes p instead.
-    // u_0 = p_a + 1 turns the pivot column into -f inv (mod q), as v[0] = f (mod q).
+      const float fp = is_piv ? 0.0f : fred(f[i] * finv, mf);
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      if (tid + T * i == pr) {
+      for (int t4 = 0; t4 < NBP / 4; ++t4) {
+        const float4 r4 = *reinterpret_cast<const float4*>(raw + 4 * t4);
+        const float rs[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-        for (int t4 = 0; t4 < NBP / 4; ++t4) {
-          const int4 pp = *reinterpret_cast<const int4*>(S.prow + 4 * t4);
-          const int32_t ps[4] = {pp.x, pp.y, pp.z, pp.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[i][(4 * t4 + u + NBP - 1) & (NBP - 1)] = ps[u];
+        for (int u = 0; u < 4; ++u) {
+          const int t = 4 * t4 + u;
+          if (t > 0) v[i][t - 1] = __fmaf_rn(-fp, rs[u], v[i][t]);
         }
-      } else {
-        const int32_t fi = f[i], first = v[i][0] - fi * S.pupd[0];
-#pragma unroll
-        for (int t4 = 0; t4 < NBP / 4; ++t4) {
-          const int4 uu = *reinterpret_cast<const int4*>(S.pupd + 4 * t4);
-          const int32_t us[4] = {uu.x, uu.y, uu.z, uu.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int t = 4 * t4 + u;
-            if (t > 0) v[i][t - 1] = v[i][t] - fi * us[u];
-          }
-        }
-        v[i][NBP - 1] = first;
       }
+      v[i][NBP - 1] = is_piv ? 1.0f : -fp;
     }
   }
   // rotate back by kb (entry t holds column (kb + t) mod NBP), log shifter
@@ -457,7 +524,7 @@ __device__ __forceinline__ bool panel_factor(const GJParams& p, int j, const Mod
 #pragma unroll
     for (int sh = 1; sh < NBP; sh <<= 1) {
       if (kb & sh) {
-        int32_t tmp[NBP];
+        float tmp[NBP];
 #pragma unroll
         for (int t = 0; t < NBP; ++t) tmp[(t + sh) & (NBP - 1)] = v[i][t];
 #pragma unroll
@@ -465,24 +532,26 @@ __device__ __forceinline__ bool panel_factor(const GJParams& p, int j, const Mod
       }
     }
   }
-  // reduce and write the panel back (padding columns stay zero: their pivot-row entries are zero)
+  // reduce (times the row's scale, if it became a pivot here) and write the
+  // panel back (padding columns stay zero: their pivot-row entries are zero)
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int row = tid + T * i;
-#pragma unroll
-    for (int q = 0; q < NBP / 4; ++q) {
-      uint32_t x = 0;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) x |= ((uint32_t)(uint8_t)(int8_t)reduce_bal(v[i][4 * q + u], m)) << (8 * u);
-      Fp[i][q] = x;
-    }
     if (row >= n) continue;
+    const float s = sc[i] ? (float)sc[i] : 1.0f;
 #pragma unroll
-    for (int c4 = 0; c4 < NBP / 16; ++c4)
+    for (int c4 = 0; c4 < NBP / 16; ++c4) {
+      uint32_t x[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        x[q] = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[q] |= fbyte(fred(fred(v[i][16 * c4 + 4 * q + u], mf) * s, mf)) << (8 * u);
+      }
       if (k0 + 16 * c4 < ld)
-        *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) =
-            make_int4(Fp[i][4 * c4], Fp[i][4 * c4 + 1], Fp[i][4 * c4 + 2], Fp[i][4 * c4 + 3]);
-    p.used[(int64_t)j * n + row] = used[i] ? 1 : 0;
+        *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) = make_int4(x[0], x[1], x[2], x[3]);
+    }
+    p.used[(int64_t)j * n + row] = ((usedm >> i) & 1) ? 1 : 0;
   }
   return true;
 }
@@ -516,200 +585,181 @@ __device__ __forceinline__ void panel_stage(int64_t cb, int64_t ce, int8_t* Wj, 
   }
 }
 
-// W[r][c0 + c] += sum_a F[r][a] U[a][c] (mod q) for the 32 columns c0 .. c0+31
-// and every row r of this thread (F = its packed panel rows, U = the staged
-// pivot rows of those columns, UT[col][0..32) at row width utw): 8 dp4a per
-// entry, exact (32 * 125^2 + 125 < 2^31).
-template <int R, int T>
-__device__ __forceinline__ void narrow_update(const GJParams& p, int8_t* Wj, const ModQ& m,
-                                              const uint32_t (&Fp)[R][8], const int8_t* UTj, int utw, int64_t c0,
-                                              PanelSmem& S) {
-  const int n = (int)p.n;
-  const int64_t ld = p.ld;
-  const int tid = threadIdx.x;
-  if (tid < 64) {
-    const int c = tid >> 1, h = tid & 1;
-    const int64_t col = c0 + c;
-    const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + col * utw + 16 * h) : make_int4(0, 0, 0, 0);
-    *reinterpret_cast<int4*>(&S.u[c][4 * h]) = x;
-  }
-  __syncthreads();
+// W[r][tc + c] = bal(W[r][tc + c] + sum_{a < K} W[r][fc + a] U[c][a]) for
+// every row r < n and c < NC (columns at or past n keep their zero padding),
+// with U staged in shared memory as Us[c][0 .. K) (row pitch K bytes).  f16
+// tensor-core tiles, exact as in k_gj_update_mma (|sum| < 2^20): each warp
+// takes 16-row tiles in turn with U's fragments held in registers, reading F
+// as 32-bit words of m16n8k32 s8 layout and widening them to f16.
+template <int K, int NC, int T>
+__device__ __forceinline__ void block_mma_update(int8_t* Wj, int64_t ld, int n, int64_t fc, int64_t tc,
+                                                 const uint8_t* Us, const ModF& mf) {
+  constexpr int NT = NC / 8, KK = K / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+  uint32_t bf[NT][KK][2][2];
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int row = tid + T * i;
-    if (row >= n) continue;
-    int8_t* wr = Wj + (int64_t)row * ld + c0;
-    const bool two = c0 + 16 < ld;
-    const int4 o0 = *reinterpret_cast<const int4*>(wr), o1 = two ? *reinterpret_cast<const int4*>(wr + 16)
-                                                                 : make_int4(0, 0, 0, 0);
-    uint32_t w[8] = {(uint32_t)o0.x, (uint32_t)o0.y, (uint32_t)o0.z, (uint32_t)o0.w,
-                     (uint32_t)o1.x, (uint32_t)o1.y, (uint32_t)o1.z, (uint32_t)o1.w};
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      uint32_t x = 0;
+    for (int kk = 0; kk < KK; ++kk)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = 4 * q + u;
-        const int4 ua = *reinterpret_cast<const int4*>(&S.u[c][0]), ub = *reinterpret_cast<const int4*>(&S.u[c][4]);
-        int32_t acc = 0;
-        acc = __dp4a((int)Fp[i][0], ua.x, acc);
-        acc = __dp4a((int)Fp[i][1], ua.y, acc);
-        acc = __dp4a((int)Fp[i][2], ua.z, acc);
-        acc = __dp4a((int)Fp[i][3], ua.w, acc);
-        acc = __dp4a((int)Fp[i][4], ub.x, acc);
-        acc = __dp4a((int)Fp[i][5], ub.y, acc);
-        acc = __dp4a((int)Fp[i][6], ub.z, acc);
-        acc = __dp4a((int)Fp[i][7], ub.w, acc);
-        int32_t val = sbyte(w[q], u);
-        if (c0 + c < n) val = reduce_bal(val + acc, m);
-        x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(Us + (8 * nt + g) * K + 32 * kk + 16 * h + 4 * t);
+        s8x4_to_f16(w, bf[nt][kk][h][0], bf[nt][kk][h][1]);
       }
-      w[q] = x;
+  // a tile's F words and old target entries (two columns per C register pair)
+  auto load_tile = [&](int mt, uint32_t (&a8)[KK][4], uint32_t (&old)[NT][2]) {
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int row = 16 * mt + g + 8 * (r & 1);
+        const int64_t col = fc + 32 * kk + 16 * (r >> 1) + 4 * t;
+        a8[kk][r] = (row < n && col < ld) ? *reinterpret_cast<const uint32_t*>(Wj + (int64_t)row * ld + col) : 0u;
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int row = 16 * mt + g + 8 * rr;
+        const int64_t col = tc + 8 * nt + 2 * t;
+        old[nt][rr] = (row < n && col < ld) ? *reinterpret_cast<const uint16_t*>(Wj + (int64_t)row * ld + col) : 0u;
+      }
+  };
+  const int ntiles = (n + 15) / 16;
+  uint32_t a8[KK][4], old[NT][2];
+  if (warp < ntiles) load_tile(warp, a8, old);
+#pragma unroll 1
+  for (int mt = warp; mt < ntiles; mt += T / 32) {
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t af[4];
+        s8x4_to_f16(a8[kk][2 * h], af[0], af[2]);
+        s8x4_to_f16(a8[kk][2 * h + 1], af[1], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16_16x8x16(acc[nt], af, bf[nt][kk][h]);
+      }
+    uint32_t cur[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) cur[nt][0] = old[nt][0], cur[nt][1] = old[nt][1];
+    // the next tile's loads go out before this tile's stores (which the
+    // compiler cannot move loads across)
+    if (mt + T / 32 < ntiles) load_tile(mt + T / 32, a8, old);
+    // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int64_t col = tc + 8 * nt + 2 * t;
+      if (col >= ld) continue;  // ld is even: col + 1 < ld as well
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int row = 16 * mt + g + 8 * rr;
+        if (row >= n) continue;
+        const uint32_t ov = cur[nt][rr];
+        uint32_t nb = fbyte(fred(__fadd_rn(acc[nt][2 * rr], sbyte_f(ov, 0)), mf)) |
+                      fbyte(fred(__fadd_rn(acc[nt][2 * rr + 1], sbyte_f(ov, 1)), mf)) << 8;
+        if (col + 1 >= n) nb = col >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+        *reinterpret_cast<uint16_t*>(Wj + (int64_t)row * ld + col) = (uint16_t)nb;
+      }
     }
-    *reinterpret_cast<int4*>(wr) = make_int4(w[0], w[1], w[2], w[3]);
-    if (two) *reinterpret_cast<int4*>(wr + 16) = make_int4(w[4], w[5], w[6], w[7]);
   }
 }
 
-// One 64-column block (n <= 1024): panel k0 (kb1 columns), its U^T into
-// UT[:, 0..32) with the pivot rows zeroed, the update of the block's other
-// 32 columns, panel k0 + 32 (kb2 columns, 0 = none), its U^T into
-// UT[:, 32..64), the update of the first 32 columns.  One CTA per prime.
-// W[r][k0 + c] += sum_a F[r][a] U[a][c] (mod q) for the 64 columns of the
-// block at k0 and every row r of this thread: the previous block's update of
-// these columns, F = W[:, prev .. prev + 64) (its final columns), U = its
-// staged pivot rows, UT[k0 + c][0 .. 64).  16 dp4a per entry, exact
-// (64 * 125^2 + 125 < 2^31); U is broadcast from shared memory.
-template <int R, int T>
-__device__ __forceinline__ void catch_up(const GJParams& p, int8_t* Wj, const int8_t* UTj, const ModQ& m, int64_t prev,
-                                         int64_t k0, uint32_t (*Us)[16]) {
-  const int n = (int)p.n;
-  const int64_t ld = p.ld;
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < 64 * 4; idx += T) {
-    const int c = idx >> 2, h = idx & 3;
-    const int64_t col = k0 + c;
-    const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + col * 64 + 16 * h) : make_int4(0, 0, 0, 0);
-    *reinterpret_cast<int4*>(&Us[c][4 * h]) = x;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int row = tid + T * i;
-    if (row >= n) continue;
-    uint32_t f[16], w[16];
-    const int4* fr = reinterpret_cast<const int4*>(Wj + (int64_t)row * ld + prev);
-    int4* wr = reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0);
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int4 a = fr[h];
-      const int4 b = (k0 + 16 * h < ld) ? wr[h] : make_int4(0, 0, 0, 0);
-      f[4 * h] = a.x, f[4 * h + 1] = a.y, f[4 * h + 2] = a.z, f[4 * h + 3] = a.w;
-      w[4 * h] = b.x, w[4 * h + 1] = b.y, w[4 * h + 2] = b.z, w[4 * h + 3] = b.w;
-    }
-#pragma unroll 4
-    for (int q = 0; q < 16; ++q) {
-      uint32_t x = 0;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = 4 * q + u;
-        int32_t acc = 0;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint4 uu = *reinterpret_cast<const uint4*>(&Us[c][4 * h]);
-          acc = __dp4a((int)f[4 * h], (int)uu.x, acc);
-          acc = __dp4a((int)f[4 * h + 1], (int)uu.y, acc);
-          acc = __dp4a((int)f[4 * h + 2], (int)uu.z, acc);
-          acc = __dp4a((int)f[4 * h + 3], (int)uu.w, acc);
-        }
-        int32_t val = sbyte(w[q], u);
-        if (k0 + c < n) val = reduce_bal(val + acc, m);
-        x |= ((uint32_t)(uint8_t)(int8_t)val) << (8 * u);
-      }
-      w[q] = x;
-    }
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-      if (k0 + 16 * h < ld) wr[h] = make_int4(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
-  }
-  __syncthreads();
-}
-
+// One 64-column block (n <= 1024), one CTA per prime.  prev >= 0: first the
+// previous block's update of this block's columns, F = W[:, prev .. prev + 64)
+// (its final columns), U = its staged pivot rows UT[k0 + c][0 .. 64).  Then
+// for each 32-column half h: panel k0 + 32 h (kb1 or kb2 columns, kb2 = 0 =
+// none), its U^T into UT[:, 32 h .. 32 h + 32) with the pivot rows zeroed,
+// and the update of the block's other half by it (before the second panel
+// is factored, after the first).
 // own_only: stage only the block's own columns; the other columns' pivot
 // rows are staged later by k_gj_stage64 (the schedule that overlaps this
-// kernel with the previous block's update of those columns).  prev >= 0:
-// first bring the block's columns up to date with the block at prev.
+// kernel with the previous block's update of those columns).
 template <int R, int T>
 __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int kb1, int kb2, int own_only,
                                                      int64_t prev) {
   const int j = blockIdx.x;
   if (p.bad[j]) return;
   const ModQ m = c_modq.v[j];
-  int8_t* Wj = p.W + (int64_t)j * p.n * p.ld;
-  int8_t* UTj = p.UT + (int64_t)j * p.ld * 64;
+  const ModF mf{(float)m.q, c_qinv.v[j]};
+  const int n = (int)p.n;
+  const int64_t ld = p.ld;
+  int8_t* Wj = p.W + (int64_t)j * p.n * ld;
+  int8_t* UTj = p.UT + (int64_t)j * ld * 64;
   __shared__ PanelSmem S;
-  __shared__ __align__(16) uint32_t Us[64][16];
+  __shared__ __align__(16) uint8_t Us[64 * 64];
   for (int x = threadIdx.x; x < (int)m.q; x += T) S.inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
-  if (prev >= 0) catch_up<R, T>(p, Wj, UTj, m, prev, k0, Us);
-  uint32_t Fp[R][8];
-  const int64_t cb = own_only ? k0 : 0, ce = own_only ? (k0 + 64 < p.ld ? k0 + 64 : p.ld) : p.ld;
-  if (!panel_factor<32, R, T>(p, j, m, Wj, k0, kb1, S, Fp)) return;
+  if (prev >= 0) {
+    for (int idx = threadIdx.x; idx < 64 * 4; idx += T) {
+      const int c = idx >> 2, h = idx & 3;
+      const int64_t col = k0 + c;
+      const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + col * 64 + 16 * h) : make_int4(0, 0, 0, 0);
+      *reinterpret_cast<int4*>(Us + 64 * c + 16 * h) = x;
+    }
+    __syncthreads();
+    block_mma_update<64, 64, T>(Wj, ld, n, prev, k0, Us, mf);
+  }
   __syncthreads();
-  panel_stage<32, T>(cb, ce, Wj, p.ld, k0, kb1, S, UTj, 64);
-  if (kb2 == 0) return;
-  const int64_t k1 = k0 + 32;
-  __syncthreads();
-  narrow_update<R, T>(p, Wj, m, Fp, UTj, 64, k1, S);
-  __syncthreads();
-  if (!panel_factor<32, R, T>(p, j, m, Wj, k1, kb2, S, Fp)) return;
-  __syncthreads();
-  panel_stage<32, T>(cb, ce, Wj, p.ld, k1, kb2, S, UTj + 32, 64);
-  __syncthreads();
-  narrow_update<R, T>(p, Wj, m, Fp, UTj + 32, 64, k0, S);
+  const int64_t cb = own_only ? k0 : 0, ce = own_only ? (k0 + 64 < ld ? k0 + 64 : ld) : ld;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    const int64_t kp = k0 + 32 * h, other = k0 + 32 * (1 - h);
+    const int kb = h ? kb2 : kb1;
+    if (!panel_factor<32, R, T>(p, j, m, Wj, kp, kb, S)) return;
+    __syncthreads();
+    panel_stage<32, T>(cb, ce, Wj, ld, kp, kb, S, UTj + 32 * h, 64);
+    if (kb2 == 0) return;
+    __syncthreads();
+    if (threadIdx.x < 64) {
+      const int c = threadIdx.x >> 1, hh = threadIdx.x & 1;
+      const int64_t col = other + c;
+      const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + 32 * h + col * 64 + 16 * hh) : make_int4(0, 0, 0, 0);
+      *reinterpret_cast<int4*>(&S.u[c][4 * hh]) = x;
+    }
+    __syncthreads();
+    block_mma_update<32, 32, T>(Wj, ld, n, kp, other, reinterpret_cast<const uint8_t*>(S.u), mf);
+    __syncthreads();
+  }
 }
 
 // The block's U^T for every column outside it: the pivot rows
 // piv[k0 .. k0 + 64) (the first kb1 of the first panel, the second panel's at
 // 32 .. 32 + kb2) go to UT[col][0 .. 64) (zero where there is no pivot) and
-// are zeroed in W.  Thread per 4 consecutive columns and prime: one 4-byte
-// load per pivot row (a warp reads whole 128-byte lines), all loads before
-// any zeroing store, bytes transposed in registers.
+// are zeroed in W.  Thread per 4 consecutive columns, 16 pivot rows
+// (blockIdx.z = which 16) and prime: one 4-byte load per pivot row (a warp
+// reads whole 128-byte lines), all loads before any zeroing store, bytes
+// transposed in registers into one 16-byte store per column.
 __global__ void __launch_bounds__(128) k_gj_stage64(GJParams p, int64_t k0, int kb1, int kb2) {
-  const int j = blockIdx.y;
+  const int j = blockIdx.y, a0 = 16 * (int)blockIdx.z;
   if (p.bad[j]) return;
   const int64_t n = p.n, ld = p.ld;
   const int64_t col = 4 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
   if (col >= ld || (col >= k0 && col < k0 + 64)) return;  // ld and k0 are multiples of 4
   int8_t* Wj = p.W + (int64_t)j * n * ld;
   const int32_t* pv = p.piv + (int64_t)j * n + k0;
-  uint32_t x[64];
+  auto have = [&](int a) { return a < 32 ? a < kb1 : a - 32 < kb2; };
+  uint32_t x[16];
 #pragma unroll
-  for (int a = 0; a < 64; ++a) {
-    const bool have = a < 32 ? a < kb1 : a - 32 < kb2;
-    x[a] = have ? *reinterpret_cast<const uint32_t*>(Wj + (int64_t)pv[a] * ld + col) : 0u;
-  }
+  for (int a = 0; a < 16; ++a)
+    x[a] = have(a0 + a) ? *reinterpret_cast<const uint32_t*>(Wj + (int64_t)pv[a0 + a] * ld + col) : 0u;
 #pragma unroll
-  for (int a = 0; a < 64; ++a) {
-    const bool have = a < 32 ? a < kb1 : a - 32 < kb2;
-    if (have) *reinterpret_cast<uint32_t*>(Wj + (int64_t)pv[a] * ld + col) = 0u;
-  }
-  // column c of the four: bytes c of x[0 .. 64), packed four at a time
+  for (int a = 0; a < 16; ++a)
+    if (have(a0 + a)) *reinterpret_cast<uint32_t*>(Wj + (int64_t)pv[a0 + a] * ld + col) = 0u;
+  // column c of the four: bytes c of x[0 .. 16), packed four at a time
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    int4* dst = reinterpret_cast<int4*>(p.UT + ((int64_t)j * ld + col + c) * 64);
+    uint32_t w[4];
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      uint32_t w[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int a0 = 16 * c4 + 4 * q;
-        // gather byte c of x[a0 .. a0 + 4) into one word
-        const uint32_t lo = __byte_perm(x[a0], x[a0 + 1], c | (c + 4) << 4);
-        const uint32_t hi = __byte_perm(x[a0 + 2], x[a0 + 3], c | (c + 4) << 4);
-        w[q] = __byte_perm(lo, hi, 0x5410);
-      }
-      dst[c4] = make_int4(w[0], w[1], w[2], w[3]);
+    for (int q = 0; q < 4; ++q) {
+      // gather byte c of x[4 q .. 4 q + 4) into one word
+      const uint32_t lo = __byte_perm(x[4 * q], x[4 * q + 1], c | (c + 4) << 4);
+      const uint32_t hi = __byte_perm(x[4 * q + 2], x[4 * q + 3], c | (c + 4) << 4);
+      w[q] = __byte_perm(lo, hi, 0x5410);
     }
+    *reinterpret_cast<int4*>(p.UT + ((int64_t)j * ld + col + c) * 64 + a0) = make_int4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -788,185 +838,176 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
 // the f32 accumulator, so the contraction F U (KW = 32 or 64) is exact.  On
 // this part the f16 path has four times the rate of the s8 one.
 //
-// F = W[:, k0 .. k0 + KW) and U^T (row width utw bytes, U^T[col][a] = pivot
-// row a's entry of column col) are staged as int8 in shared memory with
-// 16-byte loads (rows of 64 bytes, chunk c of row r at chunk c ^ ((r >> 1) & 3):
-// conflict-free for the stores and for ldmatrix), read with ldmatrix as s8
-// fragments of m16n8k32 shape and widened to f16 in registers.  A 32-bit s8
-// fragment word holds four consecutive k; its low pair goes to the f16
-// fragment register for k-slots 2t, 2t + 1 and its high pair to 2t + 8, 2t + 9,
-// on both operands, so the products pair up the same k.
+// A CTA takes 128 columns of one prime and kUpdRowTiles tiles of 64 rows
+// below each other; 8 warps, each 32 rows x 32 columns of a tile.  U^T (row
+// width utw bytes, U^T[col][a] = pivot row a's entry of column col) is
+// staged once and its fragments stay in registers; each tile's F =
+// W[:, k0 .. k0 + KW) and old entries are brought in by cp.async, double
+// buffered (the next tile loads while this one computes).  Shared-memory
+// rows of F and U^T are 64 bytes with chunk c of row r at c ^ ((r >> 1) & 3),
+// read with ldmatrix as s8 fragments of m16n8k32 shape and widened to f16 in
+// registers: a 32-bit s8 fragment word holds four consecutive k; its low pair
+// goes to the f16 register for k-slots 2t, 2t + 1 and its high pair to 2t + 8,
+// 2t + 9 on both operands, so the products pair up the same k.  The old tile
+// (rows of 128 bytes, chunk c of row r at c ^ (r & 7)) is updated in place
+// from the C fragments and written back with 16-byte stores.
 //
-// The residue of v = old + (F U)[i][t] is taken in f32 as v - q rint(v / q~),
-// q~ = fl(1/q): the quotient estimate errs by at most |v| / q * 2^-24 <
-// 1/(16 q), while v / q is at least 1/(2 q) away from a half-integer (q odd),
-// so the rounding is always the exact one and the result is the balanced
-// residue.  CTA tile 64 rows x 128 columns, 8 warps of 32 x 32.  Columns
-// updated: 32-column segments col0 with cbase <= col0 < cend outside
-// [xb, xe) (which holds at least the panel).
-__device__ __forceinline__ void mma_f16_16x8x16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
+// The residue is taken in f32 as in fred (exact for |v| < 2^20).  The
+// accumulators start at -(2^23 + 128), so adding an old byte's float
+// 2^23 + (x + 128) gives v = x + (F U) exactly.  Columns updated: 32-column
+// segments col0 with cbase <= col0 < cend outside [xb, xe) (which holds at
+// least the panel); other segments are neither read nor written.
+constexpr int kUpdRowTiles = 4;
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
 }
-
-// Four signed bytes -> f16x2 of bytes 0, 1 (lo) and of bytes 2, 3 (hi): with
-// u = x + 128 (the top bit flipped), 0x64uu is the f16 1024 + u, and
-// 1024 + u - 1152 = x exactly.
-__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  lo = __byte_perm(u, 0x64646464u, 0x4140);
-  hi = __byte_perm(u, 0x64646464u, 0x4342);
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-
-struct QInvTable {
-  float v[kNumPrimes];
-};
-constexpr QInvTable make_qinv_table() {
-  QInvTable t{};
-  for (int i = 0; i < kNumPrimes; ++i) t.v[i] = 1.0f / (float)kPrimes[i];
-  return t;
-}
-__constant__ QInvTable c_qinv = make_qinv_table();
 
 __device__ __forceinline__ int rot3(int r) { return ((r << 1) | ((r >> 2) & 1)) & 7; }
 __device__ __forceinline__ int swz64(int r, int c) { return r * 64 + 16 * (c ^ ((r >> 1) & 3)); }
+__device__ __forceinline__ int swz128(int r, int c) { return r * 128 + 16 * (c ^ (r & 7)); }
 
 template <int KW>
-__global__ void __launch_bounds__(256) k_gj_update_mma(GJParams p, const int8_t* __restrict__ UT, int utw,
-                                                       int64_t k0, int64_t cbase, int64_t cend, int64_t xb,
-                                                       int64_t xe) {
+__global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8_t* __restrict__ UT, int utw,
+                                                          int64_t k0, int64_t cbase, int64_t cend, int64_t xb,
+                                                          int64_t xe) {
   constexpr int KC = KW / 16;  // 16-byte chunks per operand row
   const int j = blockIdx.z;
   if (p.bad[j]) return;
   const int64_t n = p.n, ld = p.ld;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t rowc = (int64_t)blockIdx.y * 64, colc = cbase + (int64_t)blockIdx.x * 128;
-  const int64_t row0 = rowc + (warp >> 2) * 32;
-  const int64_t col0 = colc + (warp & 3) * 32;
+  const int64_t colc = cbase + (int64_t)blockIdx.x * 128;
+  const int64_t rowc0 = (int64_t)blockIdx.y * (64 * kUpdRowTiles);
+  const int ntile = (int)min((int64_t)kUpdRowTiles, (n - rowc0 + 63) / 64);
   int8_t* Wj = p.W + (int64_t)j * n * ld;
   const int8_t* UTj = UT + (int64_t)j * ld * utw;
-  __shared__ __align__(16) float Cs[8][32][32];
-  __shared__ __align__(16) uint8_t As[64 * 64];
-  __shared__ __align__(16) uint8_t Bs[128 * 64];
-  // this thread's output row segment (row0 + lane, 32 columns), fetched early;
-  // segments are 32-column aligned like the panel: one either lies in it or misses it
-  const int64_t orow = row0 + lane;
-  const bool rowok = orow < n && col0 < ld && col0 < cend && (col0 < xb || col0 >= xe);
-  int4 old0 = make_int4(0, 0, 0, 0), old1 = old0;
-  if (rowok) {
-    old0 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0);
-    if (col0 + 16 < ld) old1 = *reinterpret_cast<const int4*>(Wj + orow * ld + col0 + 16);
-  }
-  for (int i = tid; i < 64 * KC; i += 256) {
-    const int r = i / KC, c = i % KC;
-    const int64_t row = rowc + r, col = k0 + 16 * c;
-    int4 v = make_int4(0, 0, 0, 0);
-    if (row < n && col < ld) v = *reinterpret_cast<const int4*>(Wj + row * ld + col);
-    *reinterpret_cast<int4*>(As + swz64(r, c)) = v;
-  }
+  __shared__ __align__(128) uint8_t Bs[128 * 64];
+  __shared__ __align__(128) uint8_t As[2][64 * 64];
+  __shared__ __align__(128) uint8_t Os[2][64 * 128];
+  auto seg_ok = [&](int s) {  // 32-column segment s of this CTA is updated
+    const int64_t c0 = colc + 32 * s;
+    return c0 < ld && c0 < cend && (c0 < xb || c0 >= xe);
+  };
+  auto issue_tile = [&](int k) {
+    const int buf = k & 1;
+    const int64_t rowc = rowc0 + 64 * k;
+    for (int i = tid; i < 64 * KC; i += 256) {
+      const int r = i / KC, c = i % KC;
+      const int64_t row = rowc + r, col = k0 + 16 * c;
+      const bool ok = row < n && col < ld;
+      cp_async16(As[buf] + swz64(r, c), ok ? Wj + row * ld + col : Wj, ok);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + 256 * i, r = idx >> 3, c = idx & 7;
+      const int64_t row = rowc + r, col = colc + 16 * c;
+      const bool ok = row < n && col < ld && seg_ok(c >> 1);
+      cp_async16(Os[buf] + swz128(r, c), ok ? Wj + row * ld + col : Wj, ok);
+    }
+    cp_async_commit();
+  };
   for (int i = tid; i < 128 * KC; i += 256) {
     const int r = i / KC, c = i % KC;
     const int64_t col = colc + r;
-    int4 v = make_int4(0, 0, 0, 0);
-    if (col < ld) v = *reinterpret_cast<const int4*>(UTj + col * utw + 16 * c);
-    *reinterpret_cast<int4*>(Bs + swz64(r, c)) = v;
+    cp_async16(Bs + swz64(r, c), col < ld ? UTj + col * utw + 16 * c : UTj, col < ld);
   }
-  __syncthreads();
-  const int mi8 = lane >> 3, rr = lane & 7;  // ldmatrix: matrix and row this lane addresses
-  float acc[2][4][4];
+  issue_tile(0);
+  if (ntile > 1) issue_tile(1);
+  const int mi8 = lane >> 3, rr8 = lane & 7;  // ldmatrix: matrix and row this lane addresses
+  const int g = lane >> 2, t = lane & 3;
+  const int wr = (warp >> 2) * 32, wc = (warp & 3) * 32;  // the warp's rows in a tile, columns in the CTA
+  const bool wok = seg_ok(warp & 3);
+  const float qf = (float)c_modq.v[j].q, qinv = c_qinv.v[j];
+  const ModF mf{qf, qinv};
+  uint32_t bf[KW / 32][2][4][2];  // U's f16 fragments: [kk][h][ni][reg]
+#pragma unroll 1
+  for (int k = 0; k < ntile; ++k) {
+    const int buf = k & 1;
+    if (k + 1 < ntile)
+      cp_async_wait<1>();
+    else
+      cp_async_wait<0>();
+    __syncthreads();
+    if (k == 0) {
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
+      for (int kk = 0; kk < KW / 32; ++kk)
 #pragma unroll
-    for (int ni = 0; ni < 4; ++ni)
+        for (int np = 0; np < 2; ++np) {
+          uint32_t b8[4];  // reg i: column tile 2 np + (i >> 1), k half i & 1
+          ldsm_x4(b8, Bs + swz64(wc + 8 * (2 * np + (mi8 >> 1)) + rr8, 2 * kk + (mi8 & 1)));
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc[mi][ni][r] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < KW / 32; ++kk) {
-    // s8 fragments: A reg r = rows g + 8 (r & 1), k 4 t + 16 (r >> 1) + 0..3;
-    // B reg r of column tile 2 np + (i >> 1) (i = 2 (ni & 1) + r) = column g, k 4 t + 16 r + 0..3
-    uint32_t a8[2][4], b8[2][4];
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-      ldsm_x4(a8[mi], As + swz64((warp >> 2) * 32 + 16 * mi + rr + 8 * (mi8 & 1), 2 * kk + (mi8 >> 1)));
-#pragma unroll
-    for (int np = 0; np < 2; ++np)
-      ldsm_x4(b8[np], Bs + swz64((warp & 3) * 32 + 8 * (2 * np + (mi8 >> 1)) + rr, 2 * kk + (mi8 & 1)));
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t af[2][4], bf[4][2];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        s8x4_to_f16(a8[mi][2 * h], af[mi][0], af[mi][2]);
-        s8x4_to_f16(a8[mi][2 * h + 1], af[mi][1], af[mi][3]);
-      }
-#pragma unroll
-      for (int ni = 0; ni < 4; ++ni) s8x4_to_f16(b8[ni >> 1][2 * (ni & 1) + h], bf[ni][0], bf[ni][1]);
+          for (int i = 0; i < 4; ++i)
+            s8x4_to_f16(b8[i], bf[kk][i & 1][2 * np + (i >> 1)][0], bf[kk][i & 1][2 * np + (i >> 1)][1]);
+        }
+    }
+    if (wok) {
+      float acc[2][4][4];
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bf[ni]);
-    }
-  }
-  // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1); within a row the
-  // 16-byte chunk c sits at chunk c ^ rot(row) (rot = 3-bit left rotation of
-  // row & 7): conflict-free for the 8-byte stores (per half-warp) and the
-  // 16-byte row reads (per quarter-warp)
-  {
-    const int g = lane >> 2, t = lane & 3;
+        for (int ni = 0; ni < 4; ++ni)
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
+          for (int r = 0; r < 4; ++r) acc[mi][ni][r] = -8388736.0f;
 #pragma unroll
-      for (int ni = 0; ni < 4; ++ni) {
-        const int cw = 8 * ni + 2 * t, sw = (4 * ((cw >> 2) ^ rot3(g))) | (cw & 3);  // rows g, g + 8: same rot
-        *reinterpret_cast<float2*>(&Cs[warp][16 * mi + g][sw]) = make_float2(acc[mi][ni][0], acc[mi][ni][1]);
-        *reinterpret_cast<float2*>(&Cs[warp][16 * mi + g + 8][sw]) = make_float2(acc[mi][ni][2], acc[mi][ni][3]);
+      for (int kk = 0; kk < KW / 32; ++kk) {
+        // s8 fragment reg r = rows g + 8 (r & 1), k 4 t + 16 (r >> 1) + 0..3
+        uint32_t a8[2][4];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+          ldsm_x4(a8[mi], As[buf] + swz64(wr + 16 * mi + rr8 + 8 * (mi8 & 1), 2 * kk + (mi8 >> 1)));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t af[2][4];
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            s8x4_to_f16(a8[mi][2 * h], af[mi][0], af[mi][2]);
+            s8x4_to_f16(a8[mi][2 * h + 1], af[mi][1], af[mi][3]);
+          }
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bf[kk][h][ni]);
+        }
       }
-  }
-  __syncwarp();
-  if (!rowok) return;
-  const float qf = (float)c_modq.v[j].q, qinv = c_qinv.v[j];
-  const float kM = 12582912.0f;  // 1.5 * 2^23: x + kM has ulp 1 for |x| < 2^22
-  const uint32_t w[8] = {(uint32_t)old0.x, (uint32_t)old0.y, (uint32_t)old0.z, (uint32_t)old0.w,
-                         (uint32_t)old1.x, (uint32_t)old1.y, (uint32_t)old1.z, (uint32_t)old1.w};
-  uint32_t o[8];
-  const int rl = rot3(lane);
+      // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1); two bytes of the old tile per pair
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float4 c4 = *reinterpret_cast<const float4*>(&Cs[warp][lane][4 * (q ^ rl)]);
-    const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
-    const uint32_t wu = w[q] ^ 0x80808080u;  // bytes x + 128
-    uint32_t rb[4];
+      for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      // 2^23 + x + 128 from the bits 0x4B0000uu
-      const float fb = __int_as_float((int)__byte_perm(wu, 0x4B000000u, 0x7540 + u));
-      const float v = __fadd_rn(__fadd_rn(cv[u], fb), -8388736.0f);
-      const float k = __fadd_rn(__fmaf_rn(v, qinv, kM), -kM);
-      rb[u] = (uint32_t)__float_as_int(__fadd_rn(__fmaf_rn(-k, qf, v), kM));  // low byte = residue
+        for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int r = wr + 16 * mi + g + 8 * rr, c = wc + 8 * ni + 2 * t;
+            uint16_t* o = reinterpret_cast<uint16_t*>(Os[buf] + swz128(r, c >> 4) + (c & 15));
+            const uint32_t ov = *o;
+            const float v0 = __fadd_rn(acc[mi][ni][2 * rr], sbyte_fb(ov, 0));
+            const float v1 = __fadd_rn(acc[mi][ni][2 * rr + 1], sbyte_fb(ov, 1));
+            uint32_t nb = fbyte(fred(v0, mf)) | fbyte(fred(v1, mf)) << 8;
+            const int64_t gc = colc + c;
+            if (gc + 1 >= n) nb = gc >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+            *o = (uint16_t)nb;
+          }
     }
-    o[q] = __byte_perm(__byte_perm(rb[0], rb[1], 0x0040), __byte_perm(rb[2], rb[3], 0x0040), 0x5410);
-  }
-  if (col0 + 32 > n) {  // columns n .. ld - 1 keep their zero padding
+    __syncthreads();
+    const int64_t rowc = rowc0 + 64 * k;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (col0 + 4 * q + u >= n) o[q] = (o[q] & ~(0xFFu << (8 * u))) | (w[q] & (0xFFu << (8 * u)));
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + 256 * i, r = idx >> 3, c = idx & 7;
+      const int64_t row = rowc + r, col = colc + 16 * c;
+      if (row < n && col < ld && seg_ok(c >> 1))
+        *reinterpret_cast<int4*>(Wj + row * ld + col) = *reinterpret_cast<const int4*>(Os[buf] + swz128(r, c));
+    }
+    if (k + 2 < ntile) {
+      __syncthreads();  // every thread has read this buffer
+      issue_tile(k + 2);
+    }
   }
-  *reinterpret_cast<int4*>(Wj + orow * ld + col0) = make_int4(o[0], o[1], o[2], o[3]);
-  if (col0 + 16 < ld) *reinterpret_cast<int4*>(Wj + orow * ld + col0 + 16) = make_int4(o[4], o[5], o[6], o[7]);
 }
 
 // ------------------------------------------------------------------ permute
@@ -978,7 +1019,8 @@ __global__ void k_gj_pinv(GJParams p) {
   p.pinv[(int64_t)j * p.n + p.piv[(int64_t)j * p.n + k]] = (int32_t)k;
 }
 
-// B[j][k][t] = W[j][piv[k]][pinv[t]] (t < n), zero for n <= t < ld.
+// B[j][k][t] = W[j][piv[k]][pinv[t]] (t < n), zero for n <= t < ld.  One CTA
+// per row (any n).
 __global__ void k_gj_permute(GJParams p, int8_t* __restrict__ B, uint8_t* __restrict__ good) {
   const int j = blockIdx.y;
   const int64_t n = p.n, ld = p.ld, k = blockIdx.x;
@@ -992,6 +1034,56 @@ __global__ void k_gj_permute(GJParams p, int8_t* __restrict__ B, uint8_t* __rest
   const int32_t* pinv = p.pinv + (int64_t)j * n;
   int8_t* dst = B + (int64_t)j * n * ld + k * ld;
   for (int64_t t = threadIdx.x; t < ld; t += blockDim.x) dst[t] = t < n ? (int8_t)rowS[pinv[t]] : (int8_t)0;
+}
+
+// The same for n <= kPermuteMaxN, CTA per kPermuteRows rows and prime: the
+// inverse permutation sits in shared memory as 16-bit indices, each warp
+// takes rows in turn with its own shared row buffer (the next row's 16-byte
+// loads in flight while this one is gathered) and writes 4 bytes per lane.
+constexpr int kPermuteMaxN = 8192, kPermuteRows = 64;
+template <int kMaxCh>  // 16-byte chunks per lane and row: ld <= 512 kMaxCh
+__global__ void __launch_bounds__(256) k_gj_permute_rows(GJParams p, int8_t* __restrict__ B,
+                                                         uint8_t* __restrict__ good) {
+  const int j = blockIdx.y;
+  const int64_t n = p.n, ld = p.ld;
+  if (blockIdx.x == 0 && threadIdx.x == 0) good[j] = p.bad[j] ? 0 : 1;
+  if (p.bad[j]) return;
+  extern __shared__ __align__(16) unsigned char psm[];
+  uint16_t* pinv = reinterpret_cast<uint16_t*>(psm);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* rowS = psm + ((2 * n + 15) / 16) * 16 + (int64_t)warp * ld;
+  const int32_t* pj = p.pinv + (int64_t)j * n;
+  for (int64_t t = threadIdx.x; t < n; t += blockDim.x) pinv[t] = (uint16_t)pj[t];
+  __syncthreads();
+  const int8_t* Wj = p.W + (int64_t)j * n * ld;
+  const int32_t* piv = p.piv + (int64_t)j * n;
+  const int64_t k0 = (int64_t)blockIdx.x * kPermuteRows, k1 = min(n, k0 + kPermuteRows);
+  const int nch = (int)(ld / 16);  // 16-byte chunks per row
+  int4 buf[kMaxCh];
+  auto fetch = [&](int64_t k) {
+    const int4* src = reinterpret_cast<const int4*>(Wj + (int64_t)piv[k] * ld);
+#pragma unroll
+    for (int i = 0; i < kMaxCh; ++i)
+      if (lane + 32 * i < nch) buf[i] = src[lane + 32 * i];
+  };
+  int64_t k = k0 + warp;
+  if (k < k1) fetch(k);
+  for (; k < k1; k += 8) {
+#pragma unroll
+    for (int i = 0; i < kMaxCh; ++i)
+      if (lane + 32 * i < nch) reinterpret_cast<int4*>(rowS)[lane + 32 * i] = buf[i];
+    __syncwarp();
+    if (k + 8 < k1) fetch(k + 8);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(B + (int64_t)j * n * ld + k * ld);
+    for (int64_t t = 4 * lane; t < ld; t += 128) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (t + u < n) w |= (uint32_t)rowS[pinv[t + u]] << (8 * u);
+      dst[t / 4] = w;
+    }
+    __syncwarp();
+  }
 }
 
 // ------------------------------------------------------------------ driver
@@ -1074,7 +1166,7 @@ es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) 
                        "panel smem attribute"));
   int8_t* const UT = gp.UT;
   const int64_t ld = gp.ld;
-  const unsigned rtiles = (unsigned)((n + 63) / 64);
+  const unsigned rtiles = (unsigned)((n + 64 * kUpdRowTiles - 1) / (64 * kUpdRowTiles));
   const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
   const bool reg_block = n <= 1024;  // the whole block in one launch, panel in registers
   gp.utw = 64;
@@ -1089,7 +1181,7 @@ es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) 
       else if (n <= 512)
         k_gj_block64<2, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2, 0, -1);
       else
-        k_gj_block64<2, 512><<<kNumPrimes, 512, 0, st>>>(gp, k0, kb1, kb2, 0, -1);
+        k_gj_block64<4, 256><<<kNumPrimes, 256, 0, st>>>(gp, k0, kb1, kb2, 0, -1);
       count_launch();
     } else {
       gp.UT = UT;
@@ -1214,8 +1306,8 @@ void block64(GJParams& gp, int64_t k0, int kb1, int kb2, int own_only, int64_t p
 es_status run_blocks64_split(GJParams& gp, int64_t n, cudaStream_t st, Partitions& P) {
   int8_t* const UT = gp.UT;
   const int64_t ld = gp.ld;
-  const unsigned rtiles = (unsigned)((n + 63) / 64);
-  const dim3 sgrid((unsigned)((ld / 4 + 127) / 128), kNumPrimes);
+  const unsigned rtiles = (unsigned)((n + 64 * kUpdRowTiles - 1) / (64 * kUpdRowTiles));
+  const dim3 sgrid((unsigned)((ld / 4 + 127) / 128), kNumPrimes, 4);
   const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
   gp.utw = 64;
   ES_CHECK(cuda_status(cudaEventRecord(P.fork, st), "fork"));
@@ -1232,7 +1324,7 @@ es_status run_blocks64_split(GJParams& gp, int64_t n, cudaStream_t st, Partition
     else if (n <= 512)
       block64<2, 256>(gp, k0, kb1, kb2, 1, prev, P.sp);
     else
-      block64<2, 512>(gp, k0, kb1, kb2, 1, prev, P.sp);
+      block64<4, 256>(gp, k0, kb1, kb2, 1, prev, P.sp);
     ES_CHECK(cuda_status(cudaEventRecord(P.pb, P.sp), "record block"));
     // stage this block's pivot rows of every other column (after the
     // previous block's update reached them), then update all but the next block
@@ -1307,6 +1399,20 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
   k_gj_pinv<<<dim3((unsigned)((n + 255) / 256), kNumPrimes), 256, 0, st>>>(gp);
   count_launch(2);  // pinv + permute
   ES_CHECK(cuda_status(cudaGetLastError(), "k_gj_pinv"));
+  if (n <= kPermuteMaxN) {
+    const size_t psm = (size_t)(2 * n + 15) / 16 * 16 + 8 * (size_t)gp.ld;
+    const dim3 grid((unsigned)((n + kPermuteRows - 1) / kPermuteRows), kNumPrimes);
+    auto launch = [&](auto kern) -> es_status {
+      if (psm > 48 * 1024)
+        ES_CHECK(cuda_status(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm),
+                             "permute smem attribute"));
+      kern<<<grid, 256, psm, st>>>(gp, B_dev, good_dev);
+      return cuda_status(cudaGetLastError(), "k_gj_permute_rows");
+    };
+    if (gp.ld <= 1024) return launch(k_gj_permute_rows<2>);
+    if (gp.ld <= 4096) return launch(k_gj_permute_rows<8>);
+    return launch(k_gj_permute_rows<kPermuteMaxN / 512>);
+  }
   size_t rsm = (size_t)gp.ld;
   if (rsm > 48 * 1024)
     ES_CHECK(cuda_status(cudaFuncSetAttribute(k_gj_permute, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm),
