@@ -359,10 +359,52 @@ static void comb2(Nat& o0, Nat& o1, int64_t A, int64_t B, int64_t C, int64_t D, 
   trim(o1);
 }
 
+// One Lehmer batch: the quotient steps simulated on the leading bits a >= b
+// of (r0, r1) (at most 126 bits, same shift), Knuth's Algorithm L with two
+// quotient checks, cofactors kept below 2^62 in magnitude.  The batch maps
+// (r0, r1) to (A r0 + B r1, C r0 + D r1); B == 0 means no step was certain.
+struct LMat {
+  int64_t A = 1, B = 0, C = 0, D = 1;
+  size_t k = 0;  // quotient steps
+};
+static LMat lehmer_sim(__int128 a, __int128 b) {
+  const __int128 kCap = (__int128)1 << 62;
+  LMat M;
+  int64_t A = 1, B = 0, C = 0, D = 1;
+  size_t k = 0;
+  for (;;) {
+    const __int128 bc = b + C, bd = b + D;
+    if (bc <= 0 || bd <= 0) break;
+    const __int128 ac = a + A, ad = a + B;
+    if (ac < bc) break;
+    // q = floor(ac / bc), small quotients by subtraction
+    __int128 q = 1, rem = ac - bc;
+    while (rem >= bc && q < 4) {
+      rem -= bc;
+      ++q;
+    }
+    if (rem >= bc) q = (__int128)((unsigned __int128)ac / (unsigned __int128)bc);
+    // second check: floor(ad / bd) == q
+    if (q >= kCap) break;
+    const __int128 lo = q * bd;
+    if (ad < lo || ad - lo >= bd) break;
+    const __int128 nC = (__int128)A - q * C, nD = (__int128)B - q * D;
+    if (nC >= kCap || -nC >= kCap || nD >= kCap || -nD >= kCap) break;
+    A = C;
+    C = (int64_t)nC;
+    B = D;
+    D = (int64_t)nD;
+    const __int128 t = a - q * b;
+    a = b;
+    b = t;
+    ++k;
+  }
+  M.A = A, M.B = B, M.C = C, M.D = D, M.k = k;
+  return M;
+}
+
 // Shared loop: r0 >= r1; stops when r1 <= 2^nbits (or r1 == 0 when nbits < 0).
-// Lehmer batches: up to ~60 quotient steps simulated on the leading 62 bits
-// (Knuth's Algorithm L test with two cofactor bounds), then applied to the
-// full numbers in fused passes.  Close to the stopping point a batch that
+// Lehmer batches (lehmer_sim), applied to the full numbers in fused passes.  Close to the stopping point a batch that
 // overshoots is undone and the rest runs one division step at a time.
 static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits) {
   auto done = [&](const Nat& x) { return nbits < 0 ? x.empty() : le_pow2(x, (size_t)nbits); };
@@ -382,41 +424,11 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
           sT1 = *T1;
         }
       }
-      // Simulate on the leading 126 bits (Knuth, Algorithm L, with two
-      // quotient checks), cofactors kept below 2^62 in magnitude.
       const size_t bl0 = bitlen(r0);
       const size_t sh = bl0 > 126 ? bl0 - 126 : 0;
-      const __int128 kCap = (__int128)1 << 62;
-      __int128 a = (__int128)bits128_at(r0, sh), b = (__int128)bits128_at(r1, sh);
-      int64_t A = 1, B = 0, C = 0, D = 1;
-      size_t k = 0;
-      for (;;) {
-        const __int128 bc = b + C, bd = b + D;
-        if (bc <= 0 || bd <= 0) break;
-        const __int128 ac = a + A, ad = a + B;
-        if (ac < bc) break;
-        // q = floor(ac / bc), small quotients by subtraction
-        __int128 q = 1, rem = ac - bc;
-        while (rem >= bc && q < 4) {
-          rem -= bc;
-          ++q;
-        }
-        if (rem >= bc) q = (__int128)((unsigned __int128)ac / (unsigned __int128)bc);
-        // second check: floor(ad / bd) == q
-        if (q >= kCap) break;
-        const __int128 lo = q * bd;
-        if (ad < lo || ad - lo >= bd) break;
-        const __int128 nC = (__int128)A - q * C, nD = (__int128)B - q * D;
-        if (nC >= kCap || -nC >= kCap || nD >= kCap || -nD >= kCap) break;
-        A = C;
-        C = (int64_t)nC;
-        B = D;
-        D = (int64_t)nD;
-        const __int128 t = a - q * b;
-        a = b;
-        b = t;
-        ++k;
-      }
+      const LMat L = lehmer_sim((__int128)bits128_at(r0, sh), (__int128)bits128_at(r1, sh));
+      const int64_t A = L.A, B = L.B, C = L.C, D = L.D;
+      const size_t k = L.k;
       if (B != 0) {
         comb2(n0, n1, A, B, C, D, r0, r1);
         r0.swap(n0);
@@ -454,6 +466,7 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
     ++*steps;
   }
 }
+
 
 bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den) {
   Nat r0 = M, r1 = u, T0, T1 = from_u64(1);

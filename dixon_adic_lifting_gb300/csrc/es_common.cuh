@@ -5,7 +5,7 @@
 // of primes q_j < 256; it must be odd (the residual update divides by P
 // modulo 2^64), so the set is the 53 odd primes 3..251.
 //
-// Reduction (card §Method: "Barrett reduction in place of hardware modulo"):
+// Reduction (card §Method: Barrett's method instead of the hardware remainder):
 // Barrett's method with a 32-bit reciprocal.  For an odd q < 256 let
 // mu = floor(2^32 / q).  For any u < 2^32, t = floor(u * mu / 2^32)
 // satisfies floor(u/q) - 1 <= t <= floor(u/q) because

@@ -1,10 +1,9 @@
 // Batched modular inverse B_j = A^{-1} mod q_j for all 53 primes at once.
 //
-// exact-solve card, §Method: "a batched modular inverse (A^{-1} mod q_j for
-// every prime by Gauss-Jordan over the augmented matrix, one grid per
-// elimination step spanning all primes, Barrett reduction in place of
-// hardware modulo)"; §Requirements: working memory scales with the prime
-// count and n.
+// exact-solve card, §Method: A^{-1} mod q_j is formed for every prime at
+// once by Gauss-Jordan elimination, each elimination step one launch over
+// all primes, with Barrett reduction instead of the hardware remainder;
+// §Requirements: working memory grows with the prime count and n.
 //
 // GB300 design.  Gauss-Jordan is run in place (no augmented half: the
 // exchange form of Gauss-Jordan stores the inverse's columns where the

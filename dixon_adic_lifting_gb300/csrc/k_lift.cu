@@ -2,11 +2,12 @@
 //     x_i = B r_i mod P      (per prime: Y_j = B_j R_j, exact int32, then mod q_j)
 //     balanced CRT of the E' residues into one base-P digit x_i
 //     r_{i+1} = (r_i - A x_i) P^{-1} mod 2^64   (one signed 64-bit limb)
-// exact-solve card, §Method: "the lift (per-step per-prime products as one
-// batched INT8 GEMM, CRT reconstruction of the wide digit, and the residual
-// update in one limb as (r_i - A x_i) P^{-1} mod 2^64, P odd)", with the
-// range n * max|A_ij| < 2^63 keeping the residual in one limb and K = n <=
-// 2^17 keeping the int32 accumulator exact (2^17 * 125^2 < 2^31).
+// exact-solve card, §Method: each lift step forms the products of every
+// prime's inverse with the residual's residues as one batched int8 matrix
+// product, combines the residues into the wide digit by CRT, and updates the
+// residual in a single 64-bit limb as (r_i - A x_i) P^{-1} mod 2^64 (P odd).
+// The range n * max|A_ij| < 2^63 keeps the residual in one limb and K = n <=
+// 2^17 keeps the int32 accumulator exact (2^17 * 125^2 < 2^31).
 //
 // Device buffers of one lift:
 //   B     int8   [53][n][ld]       inverses (ld = n rounded up to 16), only good primes read

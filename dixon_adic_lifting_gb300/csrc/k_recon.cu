@@ -396,6 +396,8 @@ struct ReconPlan {
   int32_t m = 0, mp = 0;
   PrimeSet ps;
   Nat M, Mhalf, Mhalf1, Q;
+  std::vector<Nat> ppow;  // P'^k, k = 0 .. max(mp, m / 2)
+  AssemblePlan ap;
   int64_t LG = 0, W = 0;
   size_t oG = 0, oC = 0, oM = 0, oN = 0, oK = 0, total = 0;
   std::vector<uint32_t> hC, hM;
@@ -420,6 +422,8 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
   R.ps = make_prime_set(good);
   if (R.ps.E == 0) return ES_ERR_ARG;
   R.M = pow_nat(R.ps.P, m);
+  power_table(R.ps, std::max(mp, m / 2 + 1), &R.ppow);
+  assemble_plan_init(R.ps, m, &R.ap, &R.ppow);
   if (big::le_pow2(R.M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
   R.Mhalf = big::shr(big::sub(R.M, big::from_u64(1)), 1);
   R.Mhalf1 = big::add(R.Mhalf, big::from_u64(1));
@@ -465,6 +469,7 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   const int32_t m = R.m, mp = R.mp;
   const PrimeSet& ps = R.ps;
   const Nat &M = R.M, &Mhalf = R.Mhalf, &Mhalf1 = R.Mhalf1, &Q = R.Q;
+  const int hw_threads = threads > 0 ? threads : std::max(1, (int)std::thread::hardware_concurrency());
   // components' full digits -> residues mod M -> denominators (host threads)
   auto denominators = [&](const std::vector<int64_t>& ks, std::vector<Nat>* dens) -> es_status {
     std::vector<uint64_t> hd(ks.size() * (size_t)m * kDigitLimbs);
@@ -476,9 +481,9 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     ES_CHECK(cuda_status(cudaStreamSynchronize(st), "sample digits sync"));
     dens->assign(ks.size(), Nat{});
     std::atomic<int> fail(0);
-    parallel_for((int64_t)ks.size(), threads, [&](int64_t t) {
-      const Nat u = shifted_to_residue(assemble_shifted(ps, hd.data() + (size_t)t * m * kDigitLimbs, kDigitLimbs, m),
-                                       Mhalf, Mhalf1);
+    parallel_for((int64_t)ks.size(), hw_threads, [&](int64_t t) {
+      const Nat u = shifted_to_residue(
+          assemble_shifted_dc(ps, R.ap, hd.data() + (size_t)t * m * kDigitLimbs, kDigitLimbs), Mhalf, Mhalf1);
       if (!component_denominator(M, u, num_bits, den_bits, &(*dens)[(size_t)t])) fail = 1;
     });
     return fail ? ES_ERR_INTERNAL : ES_OK;
@@ -515,17 +520,17 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     // cut into segments run on host threads: since Q = P'^mp, a segment's
     // first term is G_i0 = (d mod P'^(mp - i0)) P'^i0, below Q already.
     Nat sum, rem;
-    const int nseg = mp >= 32 ? 4 : 1;
+    const int nseg = std::max(1, std::min(mp / 4, hw_threads));
     std::vector<Nat> ssum((size_t)nseg);
-    parallel_for(nseg, threads > 0 && threads < nseg ? threads : nseg, [&](int64_t t) {
+    parallel_for(nseg, nseg, [&](int64_t t) {
       const int32_t i0 = (int32_t)(t * mp / nseg), i1 = (int32_t)((t + 1) * mp / nseg);
       Nat g;
       if (i0 == 0) {
         big::divmod(d, Q, nullptr, &g);
       } else {
         Nat low;
-        big::divmod(d, pow_nat(ps.P, mp - i0), nullptr, &low);
-        g = big::mul(low, pow_nat(ps.P, i0));
+        big::divmod(d, R.ppow[(size_t)(mp - i0)], nullptr, &low);
+        g = big::mul(low, R.ppow[(size_t)i0]);
       }
       g_chain(Q, ps.P, g, i1 - i0, LG, GS, hG.data() + (size_t)i0 * GS, &ssum[(size_t)t]);
     });

@@ -1,10 +1,10 @@
 // Final rational reconstruction on the host.
 //
-// exact-solve card, §Method: "the final rational reconstruction (common
-// denominator from a small sample of components, then one modular multiply
-// per numerator; this CPU stage uses gmpy2 and a process pool when
-// available)".  Here: the library's own limb arithmetic (bigint.h) and a
-// pool of host threads.
+// exact-solve card, §Method: the last stage reconstructs the rationals on
+// the CPU -- a common denominator taken from a few sampled components, then a
+// single modular multiplication for each numerator (the card runs it with a
+// multiprecision package and worker processes).  Here: the library's own
+// limb arithmetic (bigint.h) and a pool of host threads.
 //
 // From the digits x_0 .. x_{m-1} (balanced, base P') of every component:
 //   u_k = sum_i x_{i,k} P'^i mod M,  M = P'^m > 2 Nb Db  (Nb = 2^num_bits, Db = 2^den_bits)
@@ -81,6 +81,54 @@ Nat assemble_shifted(const PrimeSet& ps, const uint64_t* base, size_t stride, in
   return X;
 }
 
+namespace {
+constexpr int32_t kAssembleLeaf = 24;
+void split_lengths(int32_t len, std::vector<int32_t>& out) {
+  if (len <= kAssembleLeaf) return;
+  const int32_t h = len / 2;
+  out.push_back(h);
+  split_lengths(h, out);
+  split_lengths(len - h, out);
+}
+Nat assemble_range(const PrimeSet& ps, const AssemblePlan& ap, const uint64_t* base, size_t stride, int32_t lo,
+                   int32_t len) {
+  if (len <= kAssembleLeaf) return assemble_shifted(ps, base + (size_t)lo * stride, stride, len);
+  const int32_t h = len / 2;
+  const Nat* ph = nullptr;
+  for (const auto& e : ap.pw)
+    if (e.first == h) ph = &e.second;
+  if (!ph) return assemble_shifted(ps, base + (size_t)lo * stride, stride, len);
+  Nat r = big::mul(assemble_range(ps, ap, base, stride, lo + h, len - h), *ph);
+  big::add_in(r, assemble_range(ps, ap, base, stride, lo, h));
+  return r;
+}
+}  // namespace
+
+void power_table(const PrimeSet& ps, int32_t kmax, std::vector<Nat>* pw) {
+  pw->assign((size_t)kmax + 1, Nat{});
+  (*pw)[0] = big::from_u64(1);
+  for (int32_t k = 1; k <= kmax; ++k) {
+    Nat v = (*pw)[(size_t)k - 1];
+    big::mul_small_add_in(v, ps.P6, ps.plen, nullptr, 0);
+    (*pw)[(size_t)k] = std::move(v);
+  }
+}
+
+void assemble_plan_init(const PrimeSet& ps, int32_t m, AssemblePlan* ap, const std::vector<Nat>* table) {
+  ap->m = m;
+  ap->pw.clear();
+  std::vector<int32_t> hs;
+  split_lengths(m, hs);
+  std::sort(hs.begin(), hs.end());
+  hs.erase(std::unique(hs.begin(), hs.end()), hs.end());
+  for (int32_t h : hs)
+    ap->pw.emplace_back(h, table && (size_t)h < table->size() ? (*table)[(size_t)h] : pow_nat(ps.P, h));
+}
+
+Nat assemble_shifted_dc(const PrimeSet& ps, const AssemblePlan& ap, const uint64_t* base, size_t stride) {
+  return assemble_range(ps, ap, base, stride, 0, ap.m);
+}
+
 Nat shifted_to_residue(Nat X, const Nat& Mhalf, const Nat& Mhalf1) {
   if (big::cmp(X, Mhalf) >= 0)
     big::sub_in(X, Mhalf);
@@ -126,8 +174,10 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
   if (big::le_pow2(M, (size_t)(num_bits + den_bits + 1))) return ES_ERR_INTERNAL;
   const Nat Mhalf = big::shr(big::sub(M, big::from_u64(1)), 1);
   const Nat Mhalf1 = big::add(Mhalf, big::from_u64(1));
+  AssemblePlan ap;
+  assemble_plan_init(ps, m, &ap);
   auto residue = [&](int64_t k) {
-    return shifted_to_residue(assemble_shifted(ps, digits + (size_t)k * kDigitLimbs, (size_t)nc * kDigitLimbs, m),
+    return shifted_to_residue(assemble_shifted_dc(ps, ap, digits + (size_t)k * kDigitLimbs, (size_t)nc * kDigitLimbs),
                               Mhalf, Mhalf1);
   };
 
@@ -170,11 +220,12 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     // Every failing component's denominator does not divide d, so the round's
     // lcm must grow d (a later one may already be covered by an earlier one).
     const Nat before = d;
-    for (int64_t k : failed) {
-      Nat den;
-      if (!component_denominator(M, residue(k), num_bits, den_bits, &den)) return ES_ERR_INTERNAL;
-      lcm_in(d, den);
-    }
+    std::vector<Nat> fden(failed.size());
+    parallel_for((int64_t)failed.size(), threads, [&](int64_t t) {
+      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t])) fail = 1;
+    });
+    if (fail) return ES_ERR_INTERNAL;
+    for (auto& v : fden) lcm_in(d, v);
     if (big::cmp(before, d) == 0) return ES_ERR_INTERNAL;  // no progress: digits inconsistent
   }
   if (!big::le_pow2(d, (size_t)den_bits)) return ES_ERR_INTERNAL;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <atomic>
+#include <functional>
 #include <thread>
 #include <vector>
 
@@ -26,6 +27,18 @@ big::Nat pow_nat(const big::Nat& b, int64_t e);
 // little-endian two's complement limbs at base + i * stride (in limbs):
 // Horner on the shifted digits x_i + (P'-1)/2 in [0, P'-1].
 big::Nat assemble_shifted(const PrimeSet& ps, const uint64_t* base, size_t stride, int32_t m);
+// The same sum split in halves down to short runs of digits (Horner on the
+// runs), X = X_lo + P'^h X_hi.  The powers P'^h of every split length depend
+// on m only and are built beforehand (from `table` when it reaches h).
+struct AssemblePlan {
+  int32_t m = 0;
+  std::vector<std::pair<int32_t, big::Nat>> pw;  // (h, P'^h)
+};
+void assemble_plan_init(const PrimeSet& ps, int32_t m, AssemblePlan* ap,
+                        const std::vector<big::Nat>* table = nullptr);
+big::Nat assemble_shifted_dc(const PrimeSet& ps, const AssemblePlan& ap, const uint64_t* base, size_t stride);
+// P'^k for k = 0 .. kmax, one multiplication by P' each
+void power_table(const PrimeSet& ps, int32_t kmax, std::vector<big::Nat>* pw);
 // u = X mod M in [0, M) from the shifted sum X' (M = P'^m, Mhalf = (M-1)/2).
 big::Nat shifted_to_residue(big::Nat X, const big::Nat& Mhalf, const big::Nat& Mhalf1);
 
@@ -40,27 +53,12 @@ bool component_denominator(const big::Nat& M, const big::Nat& u, int64_t num_bit
 // Two's complement little-endian limbs of +-mag into out[0..W).
 void to_limbs(const big::Nat& mag, bool neg, int64_t W, uint64_t* out);
 
+// fn(i) for i in [0, count) on up to `threads` host threads (<= 0: all
+// cores) of the process-wide pool (host_pool.cpp); returns when all are done.
+void host_parallel_for(int64_t count, int threads, const std::function<void(int64_t)>& fn);
 template <typename F>
 void parallel_for(int64_t count, int threads, F&& fn) {
-  if (count <= 0) return;
-  int T = threads > 0 ? threads : (int)std::thread::hardware_concurrency();
-  if (T < 1) T = 1;
-  if ((int64_t)T > count) T = (int)count;
-  std::atomic<int64_t> next(0);
-  auto worker = [&]() {
-    for (;;) {
-      int64_t k = next.fetch_add(1);
-      if (k >= count) break;
-      fn(k);
-    }
-  };
-  if (T == 1) {
-    worker();
-    return;
-  }
-  std::vector<std::thread> pool;
-  for (int t = 0; t < T; ++t) pool.emplace_back(worker);
-  for (auto& th : pool) th.join();
+  host_parallel_for(count, threads, std::function<void(int64_t)>(std::forward<F>(fn)));
 }
 
 }  // namespace es
