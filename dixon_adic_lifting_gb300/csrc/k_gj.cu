@@ -98,6 +98,18 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
                : "r"(a));
 }
 
+// 16-byte global -> shared copy (zero fill when !valid), its group commit and wait
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // Four signed bytes -> f16x2 of bytes 0, 1 (lo) and of bytes 2, 3 (hi): with
 // u = x + 128 (the top bit flipped), 0x64uu is the f16 1024 + u, and
 // 1024 + u - 1152 = x exactly.
@@ -589,12 +601,19 @@ __device__ __forceinline__ void panel_stage(int64_t cb, int64_t ce, int8_t* Wj, 
 // with U staged in shared memory as Us[c][0 .. K) (row pitch K bytes).  f16
 // tensor-core tiles, exact as in k_gj_update_mma (|sum| < 2^20): each warp
 // takes 16-row tiles in turn with U's fragments held in registers, reading F
-// as 32-bit words of m16n8k32 s8 layout and widening them to f16.
+// as 32-bit words of m16n8k32 s8 layout and widening them to f16.  A tile's
+// old entries come into the warp's own shared buffer by cp.async (double
+// buffered, 16-byte copies), are updated there and leave with 16-byte stores.
+// Buffer rows are NC bytes with chunk c of row r at c ^ f(r) (f = (r >> 1) & 3
+// for 64-byte rows, (r >> 2) & 1 for 32-byte rows), conflict-free for the
+// two-byte accesses of the C fragments.
+constexpr int kBlkBuf = 2 * 16 * 64;  // bytes of a warp's two tile buffers
 template <int K, int NC, int T>
 __device__ __forceinline__ void block_mma_update(int8_t* Wj, int64_t ld, int n, int64_t fc, int64_t tc,
-                                                 const uint8_t* Us, const ModF& mf) {
-  constexpr int NT = NC / 8, KK = K / 32;
+                                                 const uint8_t* Us, const ModF& mf, uint8_t* wbuf) {
+  constexpr int NT = NC / 8, KK = K / 32, CPR = NC / 16;  // n-tiles, k chunks, 16-byte chunks per row
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+  auto swzo = [](int r, int c) { return r * NC + 16 * (c ^ (NC == 64 ? (r >> 1) & 3 : (r >> 2) & 1)); };
   uint32_t bf[NT][KK][2][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -605,8 +624,7 @@ __device__ __forceinline__ void block_mma_update(int8_t* Wj, int64_t ld, int n, 
         const uint32_t w = *reinterpret_cast<const uint32_t*>(Us + (8 * nt + g) * K + 32 * kk + 16 * h + 4 * t);
         s8x4_to_f16(w, bf[nt][kk][h][0], bf[nt][kk][h][1]);
       }
-  // a tile's F words and old target entries (two columns per C register pair)
-  auto load_tile = [&](int mt, uint32_t (&a8)[KK][4], uint32_t (&old)[NT][2]) {
+  auto load_a = [&](int mt, uint32_t (&a8)[KK][4]) {
 #pragma unroll
     for (int kk = 0; kk < KK; ++kk)
 #pragma unroll
@@ -615,23 +633,44 @@ __device__ __forceinline__ void block_mma_update(int8_t* Wj, int64_t ld, int n, 
         const int64_t col = fc + 32 * kk + 16 * (r >> 1) + 4 * t;
         a8[kk][r] = (row < n && col < ld) ? *reinterpret_cast<const uint32_t*>(Wj + (int64_t)row * ld + col) : 0u;
       }
+  };
+  auto issue_old = [&](int mt, uint8_t* buf) {  // 16 rows x NC bytes, 16 * CPR chunks
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int row = 16 * mt + g + 8 * rr;
-        const int64_t col = tc + 8 * nt + 2 * t;
-        old[nt][rr] = (row < n && col < ld) ? *reinterpret_cast<const uint16_t*>(Wj + (int64_t)row * ld + col) : 0u;
+    for (int i = 0; i < (16 * CPR + 31) / 32; ++i) {
+      const int idx = lane + 32 * i;
+      if (idx < 16 * CPR) {
+        const int r = idx / CPR, c = idx % CPR;
+        const int row = 16 * mt + r;
+        const int64_t col = tc + 16 * c;
+        const bool ok = row < n && col < ld;
+        cp_async16(buf + swzo(r, c), ok ? Wj + (int64_t)row * ld + col : Wj, ok);
       }
+    }
+    cp_async_commit();
   };
   const int ntiles = (n + 15) / 16;
-  uint32_t a8[KK][4], old[NT][2];
-  if (warp < ntiles) load_tile(warp, a8, old);
+  uint8_t* const obuf = wbuf + (size_t)warp * kBlkBuf;  // buffer i at obuf + 1024 i
+  uint32_t a8[KK][4];
+  if (warp < ntiles) {
+    load_a(warp, a8);
+    issue_old(warp, obuf);
+  }
+  const bool full = tc + NC <= n;  // no padding column among the NC
+  int it = 0;
 #pragma unroll 1
-  for (int mt = warp; mt < ntiles; mt += T / 32) {
+  for (int mt = warp; mt < ntiles; mt += T / 32, ++it) {
+    uint8_t* buf = obuf + 1024 * (it & 1);
+    const int mn = mt + T / 32;
+    if (mn < ntiles) {
+      issue_old(mn, obuf + 1024 * ((it + 1) & 1));
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
     float acc[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = -8388736.0f;
 #pragma unroll
     for (int kk = 0; kk < KK; ++kk)
 #pragma unroll
@@ -642,28 +681,40 @@ __device__ __forceinline__ void block_mma_update(int8_t* Wj, int64_t ld, int n, 
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_f16_16x8x16(acc[nt], af, bf[nt][kk][h]);
       }
-    uint32_t cur[NT][2];
+    if (mn < ntiles) load_a(mn, a8);  // the next tile's F in flight during the epilogue
+    // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1); the accumulators
+    // start at -(2^23 + 128) so that adding the old byte's 2^23 + (x + 128)
+    // gives v = x + (F U) exactly
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) cur[nt][0] = old[nt][0], cur[nt][1] = old[nt][1];
-    // the next tile's loads go out before this tile's stores (which the
-    // compiler cannot move loads across)
-    if (mt + T / 32 < ntiles) load_tile(mt + T / 32, a8, old);
-    // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int64_t col = tc + 8 * nt + 2 * t;
-      if (col >= ld) continue;  // ld is even: col + 1 < ld as well
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const int row = 16 * mt + g + 8 * rr;
-        if (row >= n) continue;
-        const uint32_t ov = cur[nt][rr];
-        uint32_t nb = fbyte(fred(__fadd_rn(acc[nt][2 * rr], sbyte_f(ov, 0)), mf)) |
-                      fbyte(fred(__fadd_rn(acc[nt][2 * rr + 1], sbyte_f(ov, 1)), mf)) << 8;
-        if (col + 1 >= n) nb = col >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
-        *reinterpret_cast<uint16_t*>(Wj + (int64_t)row * ld + col) = (uint16_t)nb;
+        const int r = g + 8 * rr, c = 8 * nt + 2 * t;
+        uint16_t* o = reinterpret_cast<uint16_t*>(buf + swzo(r, c >> 4) + (c & 15));
+        const uint32_t ov = *o;
+        const float v0 = __fadd_rn(acc[nt][2 * rr], sbyte_fb(ov, 0));
+        const float v1 = __fadd_rn(acc[nt][2 * rr + 1], sbyte_fb(ov, 1));
+        uint32_t nb = __byte_perm((uint32_t)__float_as_int(__fadd_rn(fred(v0, mf), 12582912.0f)),
+                                  (uint32_t)__float_as_int(__fadd_rn(fred(v1, mf), 12582912.0f)), 0x0040);
+        if (!full) {
+          const int64_t gc = tc + c;
+          if (gc + 1 >= n) nb = gc >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+        }
+        *o = (uint16_t)nb;
+      }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < (16 * CPR + 31) / 32; ++i) {
+      const int idx = lane + 32 * i;
+      if (idx < 16 * CPR) {
+        const int r = idx / CPR, c = idx % CPR;
+        const int row = 16 * mt + r;
+        const int64_t col = tc + 16 * c;
+        if (row < n && col < ld)
+          *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + col) = *reinterpret_cast<const int4*>(buf + swzo(r, c));
       }
     }
+    __syncwarp();  // the buffer is refilled two tiles on
   }
 }
 
@@ -690,6 +741,7 @@ __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int
   int8_t* UTj = p.UT + (int64_t)j * ld * 64;
   __shared__ PanelSmem S;
   __shared__ __align__(16) uint8_t Us[64 * 64];
+  __shared__ __align__(128) uint8_t wbuf[(T / 32) * kBlkBuf];
   for (int x = threadIdx.x; x < (int)m.q; x += T) S.inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
   if (prev >= 0) {
     for (int idx = threadIdx.x; idx < 64 * 4; idx += T) {
@@ -699,7 +751,7 @@ __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int
       *reinterpret_cast<int4*>(Us + 64 * c + 16 * h) = x;
     }
     __syncthreads();
-    block_mma_update<64, 64, T>(Wj, ld, n, prev, k0, Us, mf);
+    block_mma_update<64, 64, T>(Wj, ld, n, prev, k0, Us, mf, wbuf);
   }
   __syncthreads();
   const int64_t cb = own_only ? k0 : 0, ce = own_only ? (k0 + 64 < ld ? k0 + 64 : ld) : ld;
@@ -719,7 +771,7 @@ __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int
       *reinterpret_cast<int4*>(&S.u[c][4 * hh]) = x;
     }
     __syncthreads();
-    block_mma_update<32, 32, T>(Wj, ld, n, kp, other, reinterpret_cast<const uint8_t*>(S.u), mf);
+    block_mma_update<32, 32, T>(Wj, ld, n, kp, other, reinterpret_cast<const uint8_t*>(S.u), mf, wbuf);
     __syncthreads();
   }
 }
@@ -843,11 +895,13 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
 // staged once and its fragments stay in registers; each tile's F =
 // W[:, k0 .. k0 + KW) and old entries are brought in by cp.async, double
 // buffered (the next tile loads while this one computes).  Shared-memory
-// rows of F and U^T are 64 bytes with chunk c of row r at c ^ ((r >> 1) & 3),
-// read with ldmatrix as s8 fragments of m16n8k32 shape and widened to f16 in
-// registers: a 32-bit s8 fragment word holds four consecutive k; its low pair
-// goes to the f16 register for k-slots 2t, 2t + 1 and its high pair to 2t + 8,
-// 2t + 9 on both operands, so the products pair up the same k.  The old tile
+// rows of the s8 F and U^T are 64 bytes with chunk c of row r at
+// c ^ ((r >> 1) & 3).  U^T is read with ldmatrix as s8 fragments of m16n8k32
+// shape and widened to f16 in registers: a 32-bit s8 fragment word holds four
+// consecutive k; its low pair goes to the f16 register for k-slots 2t, 2t + 1
+// and its high pair to 2t + 8, 2t + 9.  F is widened once per tile by all
+// threads into an f16 tile laid out so that ldmatrix yields the same k-slot
+// mapping, so the products pair up the same k.  The old tile
 // (rows of 128 bytes, chunk c of row r at c ^ (r & 7)) is updated in place
 // from the C fragments and written back with 16-byte stores.
 //
@@ -858,16 +912,6 @@ __global__ void __launch_bounds__(256) k_gj_update(GJParams p, int64_t k0, int k
 // least the panel); other segments are neither read nor written.
 constexpr int kUpdRowTiles = 4;
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ int rot3(int r) { return ((r << 1) | ((r >> 2) & 1)) & 7; }
 __device__ __forceinline__ int swz64(int r, int c) { return r * 64 + 16 * (c ^ ((r >> 1) & 3)); }
@@ -890,6 +934,9 @@ __global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8
   __shared__ __align__(128) uint8_t Bs[128 * 64];
   __shared__ __align__(128) uint8_t As[2][64 * 64];
   __shared__ __align__(128) uint8_t Os[2][64 * 128];
+  __shared__ __align__(128) uint8_t Af[64 * 2 * KW];  // the tile's F widened to f16, rows of 2 KW bytes
+  // chunk c of an Af row r: 128-byte rows c ^ (r & 7), 64-byte rows c ^ ((r >> 1) & 3)
+  auto swzA = [](int r, int c) { return KW == 64 ? swz128(r, c) : swz64(r, c); };
   auto seg_ok = [&](int s) {  // 32-column segment s of this CTA is updated
     const int64_t c0 = colc + 32 * s;
     return c0 < ld && c0 < cend && (c0 < xb || c0 >= xe);
@@ -934,6 +981,22 @@ __global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8
     else
       cp_async_wait<0>();
     __syncthreads();
+    // widen F once for all warps: an s8 chunk (16 consecutive k, four words)
+    // becomes the f16 chunk pair 2 c (the words' low halves, k-slots 2t, 2t+1)
+    // and 2 c + 1 (their high halves, k-slots 2t + 8, 2t + 9), so ldmatrix
+    // gives the fragments the s8 path would widen in registers
+    for (int i = tid; i < 64 * KC; i += 256) {
+      const int r = i / KC, c = i % KC;
+      const int4 w = *reinterpret_cast<const int4*>(As[buf] + swz64(r, c));
+      uint32_t lo[4], hi[4];
+      s8x4_to_f16((uint32_t)w.x, lo[0], hi[0]);
+      s8x4_to_f16((uint32_t)w.y, lo[1], hi[1]);
+      s8x4_to_f16((uint32_t)w.z, lo[2], hi[2]);
+      s8x4_to_f16((uint32_t)w.w, lo[3], hi[3]);
+      *reinterpret_cast<int4*>(Af + swzA(r, 2 * c)) = make_int4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<int4*>(Af + swzA(r, 2 * c + 1)) = make_int4(hi[0], hi[1], hi[2], hi[3]);
+    }
+    __syncthreads();
     if (k == 0) {
 #pragma unroll
       for (int kk = 0; kk < KW / 32; ++kk)
@@ -955,27 +1018,20 @@ __global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8
 #pragma unroll
           for (int r = 0; r < 4; ++r) acc[mi][ni][r] = -8388736.0f;
 #pragma unroll
-      for (int kk = 0; kk < KW / 32; ++kk) {
-        // s8 fragment reg r = rows g + 8 (r & 1), k 4 t + 16 (r >> 1) + 0..3
-        uint32_t a8[2][4];
+      for (int G = 0; G < KW / 16; ++G) {  // 16-k group: k half G & 1 of s8 chunk pair G >> 1
+        // f16 fragment reg r = rows g + 8 (r & 1), k-slots 2 t + 8 (r >> 1) + 0..1
+        uint32_t af[2][4];
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi)
-          ldsm_x4(a8[mi], As[buf] + swz64(wr + 16 * mi + rr8 + 8 * (mi8 & 1), 2 * kk + (mi8 >> 1)));
+          ldsm_x4(af[mi], Af + swzA(wr + 16 * mi + rr8 + 8 * (mi8 & 1), 2 * G + (mi8 >> 1)));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t af[2][4];
+        for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-          for (int mi = 0; mi < 2; ++mi) {
-            s8x4_to_f16(a8[mi][2 * h], af[mi][0], af[mi][2]);
-            s8x4_to_f16(a8[mi][2 * h + 1], af[mi][1], af[mi][3]);
-          }
-#pragma unroll
-          for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bf[kk][h][ni]);
-        }
+          for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bf[G >> 1][G & 1][ni]);
       }
-      // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1); two bytes of the old tile per pair
+      // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1); two bytes of the old tile per pair.
+      // The low bytes of x + 1.5 2^23 (x the balanced residue) are x's two's complement byte.
+      const bool full = colc + wc + 32 <= n;  // no padding column in the warp's 32
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
@@ -987,9 +1043,12 @@ __global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8
             const uint32_t ov = *o;
             const float v0 = __fadd_rn(acc[mi][ni][2 * rr], sbyte_fb(ov, 0));
             const float v1 = __fadd_rn(acc[mi][ni][2 * rr + 1], sbyte_fb(ov, 1));
-            uint32_t nb = fbyte(fred(v0, mf)) | fbyte(fred(v1, mf)) << 8;
-            const int64_t gc = colc + c;
-            if (gc + 1 >= n) nb = gc >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+            uint32_t nb = __byte_perm((uint32_t)__float_as_int(__fadd_rn(fred(v0, mf), 12582912.0f)),
+                                      (uint32_t)__float_as_int(__fadd_rn(fred(v1, mf), 12582912.0f)), 0x0040);
+            if (!full) {
+              const int64_t gc = colc + c;
+              if (gc + 1 >= n) nb = gc >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+            }
             *o = (uint16_t)nb;
           }
     }
