@@ -54,6 +54,7 @@ class Solution:
         self.top_launches = top_launches      # its launches
         self.top_ms = top_ms                  # their summed CUDA-event time (timing=2 only)
         self.top_bytes_per_launch = top_bytes_per_launch
+        self.inverse_split = False            # the inverse ran on two SM partitions (green contexts)
         self._N = None
         self._d = None
 
@@ -108,8 +109,11 @@ def _take_solution(ptr: ctypes.c_void_p) -> Solution:
     _check(lib.es_solution_kernels(ptr, ctypes.byref(la), ctypes.byref(tl), ctypes.byref(tms), ctypes.byref(tb)),
            "es_solution_kernels")
     top = (lib.es_solution_top_kernel(ptr) or b"").decode()
+    split = bool(lib.es_solution_inverse_split(ptr))
     lib.es_solution_free(ptr)
-    return Solution(num, den, n, c, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value, top)
+    sol = Solution(num, den, n, c, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value, top)
+    sol.inverse_split = split
+    return sol
 
 
 def _as_host_i64(x) -> np.ndarray:

@@ -75,9 +75,10 @@ es_status launch_residues_matrix(const int64_t* A, int64_t n, int64_t ld, int8_t
 // Batched modular inverse: A_dev -> B [53][n][ld], good [53] (device).
 size_t inverse_scratch_bytes(int64_t n);
 // split: run the blocks on two SM partitions (green contexts) when the
-// device supports them (no extra streams otherwise).
+// device supports them (no extra streams otherwise); *used_split (if given)
+// tells whether they ran that way.
 es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev, char* scratch,
-                      void* stream, bool split = true);
+                      void* stream, bool split = true, bool* used_split = nullptr);
 // Destroys the SM partitions of device `dev` (es_release_workspace).
 void release_inverse_partitions(int dev);
 
@@ -134,6 +135,7 @@ struct Solution {
   int32_t m = 0;
   int32_t primes_used = 0;
   int64_t launches = 0;
+  bool inverse_split = false;  // the inverse ran on the two SM partitions
   KernelTiming top;
 };
 

@@ -720,14 +720,15 @@ __device__ __forceinline__ void block_mma_update(int8_t* Wj, int64_t ld, int n, 
 
 // One 64-column block (n <= 1024), one CTA per prime.  prev >= 0: first the
 // previous block's update of this block's columns, F = W[:, prev .. prev + 64)
-// (its final columns), U = its staged pivot rows UT[k0 + c][0 .. 64).  Then
+// (its final columns), U = its pivot rows in these columns (gathered and
+// zeroed here; they must be current through the block before it).  Then
 // for each 32-column half h: panel k0 + 32 h (kb1 or kb2 columns, kb2 = 0 =
 // none), its U^T into UT[:, 32 h .. 32 h + 32) with the pivot rows zeroed,
 // and the update of the block's other half by it (before the second panel
 // is factored, after the first).
-// own_only: stage only the block's own columns; the other columns' pivot
-// rows are staged later by k_gj_stage64 (the schedule that overlaps this
-// kernel with the previous block's update of those columns).
+// own_only: stage only the block's own columns; the other columns read the
+// pivot rows themselves (k_gj_update_strip, and the next block's catch-up),
+// in the schedule that overlaps this kernel with the previous block's update.
 template <int R, int T>
 __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int kb1, int kb2, int own_only,
                                                      int64_t prev) {
@@ -744,11 +745,33 @@ __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int
   __shared__ __align__(128) uint8_t wbuf[(T / 32) * kBlkBuf];
   for (int x = threadIdx.x; x < (int)m.q; x += T) S.inv[x] = x ? (uint8_t)inv_mod((uint32_t)x, m) : 0;
   if (prev >= 0) {
+    // U of the previous block for this block's columns, gathered here from
+    // its 64 pivot rows (a full block: every one is a pivot), which are
+    // then zeroed in these columns: Us[c][a] = W[piv[prev + a]][k0 + c]
+    uint8_t* Pr = wbuf;  // [64][64] staging, free until the block updates
     for (int idx = threadIdx.x; idx < 64 * 4; idx += T) {
-      const int c = idx >> 2, h = idx & 3;
-      const int64_t col = k0 + c;
-      const int4 x = col < ld ? *reinterpret_cast<const int4*>(UTj + col * 64 + 16 * h) : make_int4(0, 0, 0, 0);
-      *reinterpret_cast<int4*>(Us + 64 * c + 16 * h) = x;
+      const int a = idx >> 2, h = idx & 3;
+      const int64_t col = k0 + 16 * h;
+      int4 x = make_int4(0, 0, 0, 0);
+      if (col < ld) {
+        int4* src = reinterpret_cast<int4*>(Wj + (int64_t)p.piv[(int64_t)j * p.n + prev + a] * ld + col);
+        x = *src;
+        *src = make_int4(0, 0, 0, 0);
+      }
+      *reinterpret_cast<int4*>(Pr + 64 * a + 16 * h) = x;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < 64 * 4; idx += T) {
+      const int c = idx >> 2, a0 = 16 * (idx & 3);
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x |= (uint32_t)Pr[64 * (a0 + 4 * q + u) + c] << (8 * u);
+        w[q] = x;
+      }
+      *reinterpret_cast<int4*>(Us + 64 * c + a0) = make_int4(w[0], w[1], w[2], w[3]);
     }
     __syncthreads();
     block_mma_update<64, 64, T>(Wj, ld, n, prev, k0, Us, mf, wbuf);
@@ -773,44 +796,6 @@ __global__ void __launch_bounds__(T, 1) k_gj_block64(GJParams p, int64_t k0, int
     __syncthreads();
     block_mma_update<32, 32, T>(Wj, ld, n, kp, other, reinterpret_cast<const uint8_t*>(S.u), mf, wbuf);
     __syncthreads();
-  }
-}
-
-// The block's U^T for every column outside it: the pivot rows
-// piv[k0 .. k0 + 64) (the first kb1 of the first panel, the second panel's at
-// 32 .. 32 + kb2) go to UT[col][0 .. 64) (zero where there is no pivot) and
-// are zeroed in W.  Thread per 4 consecutive columns, 16 pivot rows
-// (blockIdx.z = which 16) and prime: one 4-byte load per pivot row (a warp
-// reads whole 128-byte lines), all loads before any zeroing store, bytes
-// transposed in registers into one 16-byte store per column.
-__global__ void __launch_bounds__(128) k_gj_stage64(GJParams p, int64_t k0, int kb1, int kb2) {
-  const int j = blockIdx.y, a0 = 16 * (int)blockIdx.z;
-  if (p.bad[j]) return;
-  const int64_t n = p.n, ld = p.ld;
-  const int64_t col = 4 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
-  if (col >= ld || (col >= k0 && col < k0 + 64)) return;  // ld and k0 are multiples of 4
-  int8_t* Wj = p.W + (int64_t)j * n * ld;
-  const int32_t* pv = p.piv + (int64_t)j * n + k0;
-  auto have = [&](int a) { return a < 32 ? a < kb1 : a - 32 < kb2; };
-  uint32_t x[16];
-#pragma unroll
-  for (int a = 0; a < 16; ++a)
-    x[a] = have(a0 + a) ? *reinterpret_cast<const uint32_t*>(Wj + (int64_t)pv[a0 + a] * ld + col) : 0u;
-#pragma unroll
-  for (int a = 0; a < 16; ++a)
-    if (have(a0 + a)) *reinterpret_cast<uint32_t*>(Wj + (int64_t)pv[a0 + a] * ld + col) = 0u;
-  // column c of the four: bytes c of x[0 .. 16), packed four at a time
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      // gather byte c of x[4 q .. 4 q + 4) into one word
-      const uint32_t lo = __byte_perm(x[4 * q], x[4 * q + 1], c | (c + 4) << 4);
-      const uint32_t hi = __byte_perm(x[4 * q + 2], x[4 * q + 3], c | (c + 4) << 4);
-      w[q] = __byte_perm(lo, hi, 0x5410);
-    }
-    *reinterpret_cast<int4*>(p.UT + ((int64_t)j * ld + col + c) * 64 + a0) = make_int4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -1068,6 +1053,185 @@ __global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8
   }
 }
 
+// The wide update of the two-partition schedule, with the staging of U folded
+// in.  A CTA owns one 64-column strip of one prime for every row, so it can
+// read U straight from the block's pivot rows before anything writes them:
+// no other CTA touches the strip.  The pivot rows' old entries count as zero
+// (exactly what staging leaves in W), so W[pr][t] becomes F[pr] U[:, t].
+// Per iteration a tile of 128 rows x 64 columns: 8 warps of 32 x 32, F and
+// the old tile brought in by cp.async (double buffered), F widened to f16
+// once per tile, U's f16 fragments held in registers, the old tile updated
+// in shared memory and written back with 16-byte stores; arithmetic as in
+// k_gj_update_mma (f16 mma.sync, exact f32 epilogue).  Strips inside
+// [k0, xe) (the block and the next one, left to the panel side) are skipped.
+// The block's pivots are piv[k0 + a] for a < kb1 and 32 <= a < 32 + kb2.
+constexpr int kStripRows = 128;
+constexpr size_t kStripSmem = 64 * 64 + 64 * 64 + 2 * kStripRows * 64 + kStripRows * 128 + 2 * kStripRows * 64 + 64 * 4;
+__global__ void __launch_bounds__(256, 2) k_gj_update_strip(GJParams p, int64_t k0, int kb1, int kb2, int64_t xe) {
+  const int j = blockIdx.y;
+  if (p.bad[j]) return;
+  const int64_t n = p.n, ld = p.ld;
+  const int64_t colc = (int64_t)blockIdx.x * 64;
+  if (colc >= ld || (colc >= k0 && colc < xe)) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  extern __shared__ __align__(128) uint8_t usm[];
+  uint8_t* Bs = usm;                      // U^T [64 columns][64 pivots], swz64
+  uint8_t* Pr = Bs + 64 * 64;             // the pivot rows' strip [64][64], swz64
+  uint8_t* As = Pr + 64 * 64;             // [2][128][64] s8 F, swz64
+  uint8_t* Af = As + 2 * kStripRows * 64; // [128][128] f16 F, swz128
+  uint8_t* Os = Af + kStripRows * 128;    // [2][128][64] old tile, swz64
+  int32_t* pv = reinterpret_cast<int32_t*>(Os + 2 * kStripRows * 64);  // the block's pivot rows, -1 = none
+  if (tid < 64) pv[tid] = (tid < 32 ? tid < kb1 : tid - 32 < kb2) ? p.piv[(int64_t)j * n + k0 + tid] : -1;
+  __syncthreads();
+  const int ntile = (int)((n + kStripRows - 1) / kStripRows);
+  // this thread's two rows of a tile (r0, r0 + 64) and 16-byte chunk c of F
+  // and of the strip; offsets within the prime fit 32 bits (n <= 1024 here)
+  const int r0 = tid >> 2, c16 = 16 * (tid & 3);
+  const int ni32 = (int)n, ld32 = (int)ld;
+  const bool cf = k0 + c16 < ld, co = colc + c16 < ld;
+  const int offA = (int)k0 + c16, offO = (int)colc + c16;
+  const int sA0 = swz64(r0, tid & 3), sA1 = swz64(r0 + 64, tid & 3);
+  auto issue_tile = [&](int k) {
+    const int row0 = k * kStripRows + r0, row1 = row0 + 64;
+    uint8_t* A = As + (k & 1) * kStripRows * 64;
+    uint8_t* O = Os + (k & 1) * kStripRows * 64;
+    const bool ok0 = row0 < ni32, ok1 = row1 < ni32;
+    cp_async16(A + sA0, Wj + (ok0 && cf ? row0 * ld32 + offA : 0), ok0 && cf);
+    cp_async16(O + sA0, Wj + (ok0 && co ? row0 * ld32 + offO : 0), ok0 && co);
+    cp_async16(A + sA1, Wj + (ok1 && cf ? row1 * ld32 + offA : 0), ok1 && cf);
+    cp_async16(O + sA1, Wj + (ok1 && co ? row1 * ld32 + offO : 0), ok1 && co);
+    cp_async_commit();
+  };
+  {  // the pivot rows' strip (before this CTA writes any of them)
+    const int r = tid >> 2, c = tid & 3;
+    const int pr = pv[r];
+    const bool ok = pr >= 0 && colc + 16 * c < ld;
+    cp_async16(Pr + swz64(r, c), ok ? Wj + (int64_t)pr * ld + colc + 16 * c : Wj, ok);
+    cp_async_commit();
+  }
+  issue_tile(0);
+  if (ntile > 1) {
+    issue_tile(1);
+    cp_async_wait<2>();  // the pivot strip (the two tiles may still be in flight)
+  } else {
+    cp_async_wait<1>();
+  }
+  __syncthreads();
+  {  // transpose: U^T[col][a] = Pr[a][col]; thread: column tid >> 2, pivots 16 (tid & 3) .. + 16
+    const int col = tid >> 2, a0 = 16 * (tid & 3);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int a = a0 + 4 * q + u;
+        x |= (uint32_t)Pr[swz64(a, col >> 4) + (col & 15)] << (8 * u);
+      }
+      w[q] = x;
+    }
+    *reinterpret_cast<int4*>(Bs + swz64(col, a0 >> 4)) = make_int4(w[0], w[1], w[2], w[3]);
+  }
+  __syncthreads();
+  const int mi8 = lane >> 3, rr8 = lane & 7;
+  const int g = lane >> 2, t = lane & 3;
+  const int wr = (warp >> 1) * 32, wc = (warp & 1) * 32;  // warp's rows in a tile, columns in the strip
+  const ModF mf{(float)c_modq.v[j].q, c_qinv.v[j]};
+  uint32_t bf[2][2][4][2];  // U's f16 fragments: [kk][h][ni][reg]
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t b8[4];  // reg i: column tile 2 np + (i >> 1), k half i & 1
+      ldsm_x4(b8, Bs + swz64(wc + 8 * (2 * np + (mi8 >> 1)) + rr8, 2 * kk + (mi8 & 1)));
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        s8x4_to_f16(b8[i], bf[kk][i & 1][2 * np + (i >> 1)][0], bf[kk][i & 1][2 * np + (i >> 1)][1]);
+    }
+  const bool full = colc + wc + 32 <= n;  // no padding column in the warp's 32
+#pragma unroll 1
+  for (int k = 0; k < ntile; ++k) {
+    const int64_t rowc = (int64_t)k * kStripRows;
+    uint8_t* A = As + (k & 1) * kStripRows * 64;
+    uint8_t* O = Os + (k & 1) * kStripRows * 64;
+    if (k + 1 < ntile)
+      cp_async_wait<1>();
+    else
+      cp_async_wait<0>();
+    __syncthreads();
+    // widen F (see k_gj_update_mma) and clear the tile's pivot rows in the old tile
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = r0 + 64 * i, c = tid & 3;
+      const int4 w = *reinterpret_cast<const int4*>(A + (i ? sA1 : sA0));
+      uint32_t lo[4], hi[4];
+      s8x4_to_f16((uint32_t)w.x, lo[0], hi[0]);
+      s8x4_to_f16((uint32_t)w.y, lo[1], hi[1]);
+      s8x4_to_f16((uint32_t)w.z, lo[2], hi[2]);
+      s8x4_to_f16((uint32_t)w.w, lo[3], hi[3]);
+      *reinterpret_cast<int4*>(Af + swz128(r, 2 * c)) = make_int4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<int4*>(Af + swz128(r, 2 * c + 1)) = make_int4(hi[0], hi[1], hi[2], hi[3]);
+    }
+    if (tid < 64) {
+      const int pr = pv[tid];
+      if (pr >= rowc && pr < rowc + kStripRows) {
+        const int r = (int)(pr - rowc);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) *reinterpret_cast<int4*>(O + swz64(r, c)) = make_int4(0, 0, 0, 0);
+      }
+    }
+    __syncthreads();
+    float acc[2][4][4];
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[mi][ni][r] = -8388736.0f;
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      uint32_t af[2][4];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) ldsm_x4(af[mi], Af + swz128(wr + 16 * mi + rr8 + 8 * (mi8 & 1), 2 * G + (mi8 >> 1)));
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bf[G >> 1][G & 1][ni]);
+    }
+    // C reg r = row g + 8 (r >> 1), column 2 t + (r & 1)
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = wr + 16 * mi + g + 8 * rr, c = wc + 8 * ni + 2 * t;
+          uint16_t* o = reinterpret_cast<uint16_t*>(O + swz64(r, c >> 4) + (c & 15));
+          const uint32_t ov = *o;
+          const float v0 = __fadd_rn(acc[mi][ni][2 * rr], sbyte_fb(ov, 0));
+          const float v1 = __fadd_rn(acc[mi][ni][2 * rr + 1], sbyte_fb(ov, 1));
+          uint32_t nb = __byte_perm((uint32_t)__float_as_int(__fadd_rn(fred(v0, mf), 12582912.0f)),
+                                    (uint32_t)__float_as_int(__fadd_rn(fred(v1, mf), 12582912.0f)), 0x0040);
+          if (!full) {
+            const int64_t gc = colc + c;
+            if (gc + 1 >= n) nb = gc >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+          }
+          *o = (uint16_t)nb;
+        }
+    __syncthreads();
+    {
+      const int row0 = (int)rowc + r0, row1 = row0 + 64;
+      if (co && row0 < ni32) *reinterpret_cast<int4*>(Wj + row0 * ld32 + offO) = *reinterpret_cast<const int4*>(O + sA0);
+      if (co && row1 < ni32) *reinterpret_cast<int4*>(Wj + row1 * ld32 + offO) = *reinterpret_cast<const int4*>(O + sA1);
+    }
+    if (k + 2 < ntile) {
+      __syncthreads();  // every thread has read this buffer
+      issue_tile(k + 2);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ permute
 __global__ void k_gj_pinv(GJParams p) {
   const int j = blockIdx.y;
@@ -1281,7 +1445,7 @@ struct Partitions {
   bool tried = false, ok = false;
   CUgreenCtx gp = nullptr, gu = nullptr;
   cudaStream_t sp = nullptr, su = nullptr;
-  cudaEvent_t fork = nullptr, pb = nullptr, wn = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, pb = nullptr, wn[2] = {nullptr, nullptr}, join = nullptr;
 };
 std::mutex g_part_mu;
 Partitions g_part[kMaxDevices];
@@ -1306,7 +1470,7 @@ void drop_partitions(Partitions& P) {
   driver_entry("cuGreenCtxDestroy", &destroy);
   for (cudaStream_t* s : {&P.sp, &P.su})
     if (*s) cudaStreamDestroy(*s);
-  for (cudaEvent_t* e : {&P.fork, &P.pb, &P.wn, &P.join})
+  for (cudaEvent_t* e : {&P.fork, &P.pb, &P.wn[0], &P.wn[1], &P.join})
     if (*e) cudaEventDestroy(*e);
   if (destroy) {
     if (P.gp) destroy(P.gp);
@@ -1348,7 +1512,7 @@ bool make_partitions(int dev, Partitions& P) {
   }
   P.sp = (cudaStream_t)sp;
   P.su = (cudaStream_t)su;
-  for (cudaEvent_t* e : {&P.fork, &P.pb, &P.wn, &P.join})
+  for (cudaEvent_t* e : {&P.fork, &P.pb, &P.wn[0], &P.wn[1], &P.join})
     if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
       drop_partitions(P);
       return false;
@@ -1362,21 +1526,27 @@ void block64(GJParams& gp, int64_t k0, int kb1, int kb2, int own_only, int64_t p
 }
 
 es_status run_blocks64_split(GJParams& gp, int64_t n, cudaStream_t st, Partitions& P) {
-  int8_t* const UT = gp.UT;
   const int64_t ld = gp.ld;
-  const unsigned rtiles = (unsigned)((n + 64 * kUpdRowTiles - 1) / (64 * kUpdRowTiles));
-  const dim3 sgrid((unsigned)((ld / 4 + 127) / 128), kNumPrimes, 4);
-  const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
+  const dim3 strips((unsigned)((ld + 63) / 64), kNumPrimes);
   gp.utw = 64;
+  ES_CHECK(cuda_status(
+      cudaFuncSetAttribute(k_gj_update_strip, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStripSmem),
+      "update strip smem attribute"));
   ES_CHECK(cuda_status(cudaEventRecord(P.fork, st), "fork"));
   ES_CHECK(cuda_status(cudaStreamWaitEvent(P.sp, P.fork, 0), "fork panel"));
   ES_CHECK(cuda_status(cudaStreamWaitEvent(P.su, P.fork, 0), "fork update"));
+  // Panel side: block k (after update k-2, which brings block k's columns
+  // up to date through block k-2) first applies block k-1 to its own columns
+  // with block k-1's pivot rows there, then factors.  Update side: block k's
+  // update of all columns but blocks k and k+1, U read from its pivot rows.
+  // The updates' completions alternate between two events.
   int64_t prev = -1;  // the previous block's first column
-  for (int64_t k0 = 0; k0 < n; k0 += 64) {
+  int blk = 0;
+  for (int64_t k0 = 0; k0 < n; k0 += 64, ++blk) {
     const int kb1 = (int)((n - k0) < 32 ? (n - k0) : 32);
     const int64_t k1 = k0 + 32, n0 = k0 + 64;
     const int kb2 = k1 < n ? (int)((n - k1) < 32 ? (n - k1) : 32) : 0;
-    if (prev >= 0) ES_CHECK(cuda_status(cudaStreamWaitEvent(P.sp, P.wn, 0), "wait stage"));
+    if (blk >= 2) ES_CHECK(cuda_status(cudaStreamWaitEvent(P.sp, P.wn[blk & 1], 0), "wait update"));
     if (n <= 256)
       block64<1, 256>(gp, k0, kb1, kb2, 1, prev, P.sp);
     else if (n <= 512)
@@ -1384,17 +1554,11 @@ es_status run_blocks64_split(GJParams& gp, int64_t n, cudaStream_t st, Partition
     else
       block64<4, 256>(gp, k0, kb1, kb2, 1, prev, P.sp);
     ES_CHECK(cuda_status(cudaEventRecord(P.pb, P.sp), "record block"));
-    // stage this block's pivot rows of every other column (after the
-    // previous block's update reached them), then update all but the next block
     ES_CHECK(cuda_status(cudaStreamWaitEvent(P.su, P.pb, 0), "wait block"));
-    k_gj_stage64<<<sgrid, 128, 0, P.su>>>(gp, k0, kb1, kb2);
-    ES_CHECK(cuda_status(cudaEventRecord(P.wn, P.su), "record stage"));
-    const int64_t xe = n0 < n ? n0 + 64 : n0;  // keep off the next block (done on the panel side)
-    if (kb2)
-      k_gj_update_mma<64><<<wide, 256, 0, P.su>>>(gp, UT, 64, k0, 0, ld, k0, xe);
-    else
-      k_gj_update_mma<32><<<wide, 256, 0, P.su>>>(gp, UT, 64, k0, 0, ld, k0, xe);
-    count_launch(3);
+    const int64_t xe = n0 < n ? n0 + 64 : n0;  // blocks k and k+1 stay with the panel side
+    k_gj_update_strip<<<strips, 256, kStripSmem, P.su>>>(gp, k0, kb1, kb2, xe);
+    ES_CHECK(cuda_status(cudaEventRecord(P.wn[blk & 1], P.su), "record update"));
+    count_launch(2);
     prev = k0;
   }
   ES_CHECK(cuda_status(cudaEventRecord(P.join, P.su), "join"));
@@ -1412,7 +1576,7 @@ void release_inverse_partitions(int dev) {
 }
 
 es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* good_dev, char* scratch,
-                      void* stream, bool split) {
+                      void* stream, bool split, bool* used_split) {
   cudaStream_t st = (cudaStream_t)stream;
   InvLayout L = inverse_layout(n);
   bool use_smem;
@@ -1432,6 +1596,7 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
   ES_CHECK(cuda_status(cudaMemsetAsync(gp.bad, 0, (size_t)kNumPrimes * 4, st), "memset bad"));
   ES_CHECK(launch_residues_matrix(A_dev, n, gp.ld, gp.W, st));
   bool done = false;
+  if (used_split) *used_split = false;
   if (nbp == 32 && n <= 1024 && split) {
     int dev = 0;
     ES_CHECK(cuda_status(cudaGetDevice(&dev), "get device"));
@@ -1445,6 +1610,7 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
       if (P.ok) {
         ES_CHECK(run_blocks64_split(gp, n, st, P));
         done = true;
+        if (used_split) *used_split = true;
       }
     }
   }

@@ -224,7 +224,8 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   // batched modular inverse
   int8_t* B = reinterpret_cast<int8_t*>(ws + SL.B);
   uint8_t* good_dev = reinterpret_cast<uint8_t*>(ws + SL.good);
-  ES_CHECK(run_inverse(A, n, B, good_dev, ws + SL.work, st, !o.one_stream));
+  bool inverse_split = false;
+  ES_CHECK(run_inverse(A, n, B, good_dev, ws + SL.work, st, !o.one_stream, &inverse_split));
   uint8_t good[kNumPrimes];
   ES_CHECK(cuda_status(cudaMemcpyAsync(good, good_dev, kNumPrimes, cudaMemcpyDeviceToHost, st), "good D2H"));
   ES_CHECK(cuda_status(cudaStreamSynchronize(st), "inverse sync"));
@@ -324,6 +325,7 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   S.m = m;
   S.primes_used = E;
   S.launches = launch_count() - launches0;
+  S.inverse_split = inverse_split;
   S.top = kt;
   *out = sol;
   return ES_OK;
@@ -380,6 +382,8 @@ es_status es_solution_kernels(const es_solution* s, int64_t* launches, int64_t* 
 }
 
 const char* es_solution_top_kernel(const es_solution* s) { return s && s->s.top.name ? s->s.top.name : ""; }
+
+int32_t es_solution_inverse_split(const es_solution* s) { return s && s->s.inverse_split ? 1 : 0; }
 
 void es_solution_free(es_solution* s) { delete s; }
 

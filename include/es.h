@@ -137,6 +137,11 @@ es_status es_solution_kernels(const es_solution* s, int64_t* launches, int64_t* 
 /* Name of that dominant lift kernel ("k_lift_fused", "k_lift_gemv",
  * "k_lift_gemm" or "k_lift_gemm_tc"); a static string, "" for NULL. */
 const char* es_solution_top_kernel(const es_solution* s);
+/* 1 when the solve's modular inverse ran on two SM partitions (green
+ * contexts: the next column block's panels on 56 SMs while the previous
+ * block's update uses the rest), 0 when it ran on the solve's stream alone
+ * (ES_FLAG_ONE_STREAM, n > 1024, or no green-context support); 0 for NULL. */
+int32_t es_solution_inverse_split(const es_solution* s);
 
 void es_solution_free(es_solution* s);
 
