@@ -47,6 +47,7 @@ _SIGS = {
     "es_solution_kernels": (c_i32, [c_vp, P_i64, P_i64, P_dbl, P_dbl]),
     "es_solution_top_kernel": (ctypes.c_char_p, [c_vp]),
     "es_solution_inverse_split": (c_i32, [c_vp]),
+    "es_solution_data": (c_i32, [c_vp, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)]),
     "es_solution_free": (None, [c_vp]),
     "es_status_string": (ctypes.c_char_p, [c_i32]),
     "es_last_error": (ctypes.c_char_p, []),

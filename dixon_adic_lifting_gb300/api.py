@@ -94,14 +94,36 @@ def _limbs_to_ints(buf: np.ndarray, count: int, W: int, signed: bool) -> List[in
     return [int.from_bytes(raw[i * step:(i + 1) * step], "little", signed=signed) for i in range(count)]
 
 
+class _Owner:
+    """Holds an es_solution until the last array viewing its limbs is gone."""
+
+    def __init__(self, lib, ptr):
+        self._lib, self._ptr = lib, ptr
+
+    def __del__(self):
+        if self._ptr:
+            self._lib.es_solution_free(self._ptr)
+            self._ptr = None
+
+
+class _View:
+    """Array interface over limbs owned by an es_solution (no copy)."""
+
+    def __init__(self, owner: _Owner, addr: int, count: int):
+        self._owner = owner
+        self.__array_interface__ = {"shape": (count,), "typestr": "<u8", "data": (addr, True), "version": 3}
+
+
 def _take_solution(ptr: ctypes.c_void_p) -> Solution:
     lib = L.load()
     n, c, W = L.c_i64(), L.c_i64(), L.c_i64()
     _check(lib.es_solution_shape(ptr, ctypes.byref(n), ctypes.byref(c), ctypes.byref(W)), "es_solution_shape")
     n, c, W = n.value, c.value, W.value
-    num = np.zeros(n * c * W, dtype=np.uint64)
-    den = np.zeros(W, dtype=np.uint64)
-    _check(lib.es_solution_export(ptr, num.ctypes.data, den.ctypes.data), "es_solution_export")
+    pn, pd = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(lib.es_solution_data(ptr, ctypes.byref(pn), ctypes.byref(pd)), "es_solution_data")
+    owner = _Owner(lib, ptr)  # frees the solution with the last view (read-only arrays)
+    num = np.asarray(_View(owner, pn.value or 0, n * c * W)) if n * c * W else np.zeros(0, np.uint64)
+    den = np.asarray(_View(owner, pd.value or 0, W)) if W else np.zeros(0, np.uint64)
     ms = (ctypes.c_double * L.NUM_PHASES)()
     m, pu = L.c_i32(), L.c_i32()
     _check(lib.es_solution_phase_ms(ptr, ms, ctypes.byref(m), ctypes.byref(pu)), "es_solution_phase_ms")
@@ -110,7 +132,6 @@ def _take_solution(ptr: ctypes.c_void_p) -> Solution:
            "es_solution_kernels")
     top = (lib.es_solution_top_kernel(ptr) or b"").decode()
     split = bool(lib.es_solution_inverse_split(ptr))
-    lib.es_solution_free(ptr)
     sol = Solution(num, den, n, c, m.value, pu.value, list(ms), la.value, tl.value, tms.value, tb.value, top)
     sol.inverse_split = split
     return sol

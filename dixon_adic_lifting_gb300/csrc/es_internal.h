@@ -3,7 +3,10 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <memory>
+#include <new>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/es.h"
@@ -127,9 +130,31 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
                    void* stream, KernelTiming* kt = nullptr, bool allow_fused = true);
 
 // ---------------------------------------------------------------- solution
+// Allocator whose element construction leaves trivial values uninitialised:
+// the numerator buffer is written in full right after it is sized (by a
+// device copy or per component), so zero-filling it first is wasted time.
+template <class T>
+struct NoInitAlloc : std::allocator<T> {
+  template <class U>
+  struct rebind {
+    using other = NoInitAlloc<U>;
+  };
+  NoInitAlloc() = default;
+  template <class U>
+  NoInitAlloc(const NoInitAlloc<U>&) {}
+  template <class U>
+  void construct(U* p) {
+    ::new (static_cast<void*>(p)) U;
+  }
+  template <class U, class... A>
+  void construct(U* p, A&&... a) {
+    ::new (static_cast<void*>(p)) U(std::forward<A>(a)...);
+  }
+};
+
 struct Solution {
   int64_t n = 0, c = 0, limbs = 0;
-  std::vector<uint64_t> num;  // [n*c*limbs]
+  std::vector<uint64_t, NoInitAlloc<uint64_t>> num;  // [n*c*limbs]
   std::vector<uint64_t> den;  // [limbs]
   double ms[ES_NUM_PHASES] = {0, 0, 0, 0, 0, 0};
   int32_t m = 0;

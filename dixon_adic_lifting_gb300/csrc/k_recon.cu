@@ -510,6 +510,8 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   out->n = n;
   out->c = c;
   out->limbs = W;
+  // zero-filled before the device copy: the fill touches the fresh pages far
+  // faster than a copy into untouched pageable memory would
   out->num.assign((size_t)(nc * W), 0);
   std::vector<uint8_t> okh((size_t)nc);
   const int64_t GS = g_stride(LG);

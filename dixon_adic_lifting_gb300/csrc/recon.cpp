@@ -197,7 +197,7 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
   out->n = n;
   out->c = c;
   out->limbs = W;
-  out->num.assign((size_t)(nc * W), 0);
+  out->num.resize((size_t)(nc * W));  // every component writes its W limbs before the round ends
   for (int round = 0;; ++round) {
     if (round > 64) return ES_ERR_INTERNAL;
     std::mutex mu;

@@ -362,6 +362,13 @@ es_status es_solution_export(const es_solution* s, uint64_t* num, uint64_t* den)
   return ES_OK;
 }
 
+es_status es_solution_data(const es_solution* s, const uint64_t** num, const uint64_t** den) {
+  if (!s) return ES_ERR_ARG;
+  if (num) *num = s->s.num.data();
+  if (den) *den = s->s.den.data();
+  return ES_OK;
+}
+
 es_status es_solution_phase_ms(const es_solution* s, double* ms, int32_t* m, int32_t* primes_used) {
   if (!s) return ES_ERR_ARG;
   if (ms)

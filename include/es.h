@@ -111,6 +111,10 @@ es_status es_solution_shape(const es_solution* s, int64_t* n, int64_t* c, int64_
  * two's complement limbs), den [limbs] (little-endian, > 0).  Host buffers
  * owned by the caller. */
 es_status es_solution_export(const es_solution* s, uint64_t* num, uint64_t* den);
+/* The same limbs in place: *num ([n*c][limbs]) and *den ([limbs]) point into
+ * the solution and stay valid until es_solution_free (no copy).  Any
+ * pointer may be NULL; ES_ERR_ARG for a NULL solution. */
+es_status es_solution_data(const es_solution* s, const uint64_t** num, const uint64_t** den);
 
 /* Phase times in ms (ms[ES_NUM_PHASES], any may be NULL):
  *   0 range check + bounds + residues, 1 modular inverse, 2 lift,
