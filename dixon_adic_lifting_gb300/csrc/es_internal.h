@@ -130,31 +130,32 @@ es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_
                    void* stream, KernelTiming* kt = nullptr, bool allow_fused = true);
 
 // ---------------------------------------------------------------- solution
-// Allocator whose element construction leaves trivial values uninitialised:
-// the numerator buffer is written in full right after it is sized (by a
-// device copy or per component), so zero-filling it first is wasted time.
-template <class T>
-struct NoInitAlloc : std::allocator<T> {
-  template <class U>
-  struct rebind {
-    using other = NoInitAlloc<U>;
-  };
-  NoInitAlloc() = default;
-  template <class U>
-  NoInitAlloc(const NoInitAlloc<U>&) {}
-  template <class U>
-  void construct(U* p) {
-    ::new (static_cast<void*>(p)) U;
-  }
-  template <class U, class... A>
-  void construct(U* p, A&&... a) {
-    ::new (static_cast<void*>(p)) U(std::forward<A>(a)...);
-  }
+// Host buffer of result limbs.  Blocks come from a small process-wide pool
+// (host_pool.cpp): page-locked when a CUDA device is present (a device copy
+// into them runs at full speed, with no page faults once warm), returned to
+// the pool when the buffer dies.  resize() keeps no contents.
+class LimbBuffer {
+ public:
+  LimbBuffer() = default;
+  LimbBuffer(const LimbBuffer&) = delete;
+  LimbBuffer& operator=(const LimbBuffer&) = delete;
+  ~LimbBuffer() { release(); }
+  void resize(size_t count);  // contents unspecified afterwards
+  uint64_t* data() { return p_; }
+  const uint64_t* data() const { return p_; }
+  size_t size() const { return n_; }
+  bool pinned() const { return pinned_; }
+
+ private:
+  void release();
+  uint64_t* p_ = nullptr;
+  size_t n_ = 0, cap_ = 0;
+  bool pinned_ = false;
 };
 
 struct Solution {
   int64_t n = 0, c = 0, limbs = 0;
-  std::vector<uint64_t, NoInitAlloc<uint64_t>> num;  // [n*c*limbs]
+  LimbBuffer num;              // [n*c*limbs]
   std::vector<uint64_t> den;  // [limbs]
   double ms[ES_NUM_PHASES] = {0, 0, 0, 0, 0, 0};
   int32_t m = 0;

@@ -510,9 +510,10 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   out->n = n;
   out->c = c;
   out->limbs = W;
-  // zero-filled before the device copy: the fill touches the fresh pages far
-  // faster than a copy into untouched pageable memory would
-  out->num.assign((size_t)(nc * W), 0);
+  out->num.resize((size_t)(nc * W));
+  // a pageable buffer is filled before the device copy: the fill touches its
+  // fresh pages far faster than a copy into untouched pageable memory would
+  if (!out->num.pinned()) std::memset(out->num.data(), 0, out->num.size() * 8);
   std::vector<uint8_t> okh((size_t)nc);
   const int64_t GS = g_stride(LG);
   std::vector<uint32_t> hG((size_t)mp * GS, 0u);

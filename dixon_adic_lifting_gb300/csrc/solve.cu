@@ -332,6 +332,86 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
 }
 
 }  // namespace
+// ------------------------------------------------------------ limb blocks
+// Result limbs leave the device once per solve into a buffer the caller may
+// keep.  A fresh pageable buffer costs page faults (and a staged copy); the
+// blocks here are page-locked when a device is present and recycled: a
+// freed buffer's block waits in a short list for the next solve.  Blocks
+// above kPinMax bytes are plain allocations and are not kept.
+namespace {
+constexpr size_t kPinMax = size_t(256) << 20;
+constexpr size_t kKeep = 4;  // blocks kept for reuse
+struct Block {
+  uint64_t* p;
+  size_t cap;
+  bool pinned;
+};
+std::mutex g_blk_mu;
+std::vector<Block> g_blocks;
+
+Block block_new(size_t count) {
+  Block b{nullptr, count, false};
+  if (count * 8 <= kPinMax) {
+    void* p = nullptr;
+    if (cudaMallocHost(&p, count * 8) == cudaSuccess) {
+      b.p = static_cast<uint64_t*>(p);
+      b.pinned = true;
+      return b;
+    }
+    cudaGetLastError();  // no device: fall back to a plain allocation
+  }
+  b.p = new (std::nothrow) uint64_t[count];
+  return b;
+}
+void block_delete(const Block& b) {
+  if (b.pinned)
+    cudaFreeHost(b.p);
+  else
+    delete[] b.p;
+}
+}  // namespace
+
+void LimbBuffer::resize(size_t count) {
+  if (count <= cap_) {
+    n_ = count;
+    return;
+  }
+  release();
+  Block b{nullptr, 0, false};
+  {
+    std::lock_guard<std::mutex> lk(g_blk_mu);
+    size_t best = g_blocks.size();
+    for (size_t i = 0; i < g_blocks.size(); ++i)
+      if (g_blocks[i].cap >= count && (best == g_blocks.size() || g_blocks[i].cap < g_blocks[best].cap)) best = i;
+    if (best < g_blocks.size()) {
+      b = g_blocks[best];
+      g_blocks.erase(g_blocks.begin() + (std::ptrdiff_t)best);
+    }
+  }
+  if (!b.p) b = block_new(count);
+  if (!b.p) throw std::bad_alloc();
+  p_ = b.p;
+  cap_ = b.cap;
+  n_ = count;
+  pinned_ = b.pinned;
+}
+
+void LimbBuffer::release() {
+  if (!p_) return;
+  Block b{p_, cap_, pinned_};
+  p_ = nullptr;
+  n_ = cap_ = 0;
+  pinned_ = false;
+  if (b.cap * 8 <= kPinMax) {
+    std::lock_guard<std::mutex> lk(g_blk_mu);
+    if (g_blocks.size() < kKeep) {
+      g_blocks.push_back(b);
+      return;
+    }
+  }
+  block_delete(b);
+}
+
 }  // namespace es
 
 // ------------------------------------------------------------ C ABI
