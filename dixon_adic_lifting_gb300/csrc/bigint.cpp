@@ -361,13 +361,14 @@ static void comb2(Nat& o0, Nat& o1, int64_t A, int64_t B, int64_t C, int64_t D, 
 
 // One Lehmer batch: the quotient steps simulated on the leading bits a >= b
 // of (r0, r1) (at most 126 bits, same shift), Knuth's Algorithm L with two
-// quotient checks, cofactors kept below 2^62 in magnitude.  The batch maps
-// (r0, r1) to (A r0 + B r1, C r0 + D r1); B == 0 means no step was certain.
+// quotient checks, cofactors kept below 2^62 in magnitude, and no step whose
+// simulated remainder falls below `stop`.  The batch maps (r0, r1) to
+// (A r0 + B r1, C r0 + D r1); B == 0 means no step was certain.
 struct LMat {
   int64_t A = 1, B = 0, C = 0, D = 1;
   size_t k = 0;  // quotient steps
 };
-static LMat lehmer_sim(__int128 a, __int128 b) {
+static LMat lehmer_sim(__int128 a, __int128 b, __int128 stop) {
   const __int128 kCap = (__int128)1 << 62;
   LMat M;
   int64_t A = 1, B = 0, C = 0, D = 1;
@@ -390,11 +391,12 @@ static LMat lehmer_sim(__int128 a, __int128 b) {
     if (ad < lo || ad - lo >= bd) break;
     const __int128 nC = (__int128)A - q * C, nD = (__int128)B - q * D;
     if (nC >= kCap || -nC >= kCap || nD >= kCap || -nD >= kCap) break;
+    const __int128 t = a - q * b;
+    if (t < stop) break;
     A = C;
     C = (int64_t)nC;
     B = D;
     D = (int64_t)nD;
-    const __int128 t = a - q * b;
     a = b;
     b = t;
     ++k;
@@ -404,31 +406,28 @@ static LMat lehmer_sim(__int128 a, __int128 b) {
 }
 
 // Shared loop: r0 >= r1; stops when r1 <= 2^nbits (or r1 == 0 when nbits < 0).
-// Lehmer batches (lehmer_sim), applied to the full numbers in fused passes.  Close to the stopping point a batch that
-// overshoots is undone and the rest runs one division step at a time.
+// Lehmer batches (lehmer_sim), applied to the full numbers in fused passes.
+// A batch never crosses the stopping point: with r = 2^sh a0 + alpha,
+// 2^sh b0 + beta (0 <= alpha, beta < 2^sh) and cofactors |A|, |B| < 2^62 of
+// opposite signs, the true remainder A r0 + B r1 differs from 2^sh times the
+// simulated one, A a0 + B b0, by less than 2^(sh + 62); so a simulated
+// remainder of at least 2^(nbits - sh) + 2^63 keeps the true one above
+// 2^nbits.  Batches run until no certain step is left, then single
+// division steps finish (a few near the stopping point).
 static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits) {
   auto done = [&](const Nat& x) { return nbits < 0 ? x.empty() : le_pow2(x, (size_t)nbits); };
-  bool single_only = false;
-  const size_t nb = nbits < 0 ? 0 : (size_t)nbits;
-  Nat n0, n1, m0, m1, s0, s1, sT0, sT1;
+  Nat n0, n1, m0, m1;
   while (!done(r1)) {
-    size_t bl1 = bitlen(r1);
-    if (!single_only && r1.size() >= 3 && bl1 > nb + 200) {
-      const bool guard = bl1 < nb + 400;
-      size_t ssteps = *steps;
-      if (guard) {
-        s0 = r0;
-        s1 = r1;
-        if (T0) {
-          sT0 = *T0;
-          sT1 = *T1;
-        }
-      }
+    if (r1.size() >= 3) {
       const size_t bl0 = bitlen(r0);
       const size_t sh = bl0 > 126 ? bl0 - 126 : 0;
-      const LMat L = lehmer_sim((__int128)bits128_at(r0, sh), (__int128)bits128_at(r1, sh));
+      __int128 stop = (__int128)1 << 63;
+      if (nbits >= 0 && (size_t)nbits >= sh) {
+        const size_t e = (size_t)nbits - sh;
+        stop = e >= 126 ? ((__int128)1 << 126) : stop + ((__int128)1 << e);
+      }
+      const LMat L = lehmer_sim((__int128)bits128_at(r0, sh), (__int128)bits128_at(r1, sh), stop);
       const int64_t A = L.A, B = L.B, C = L.C, D = L.D;
-      const size_t k = L.k;
       if (B != 0) {
         comb2(n0, n1, A, B, C, D, r0, r1);
         r0.swap(n0);
@@ -438,17 +437,7 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
           T0->swap(m0);
           T1->swap(m1);
         }
-        *steps += k;
-        if (guard && done(r1)) {  // overshot the stopping point: redo singly
-          r0.swap(s0);
-          r1.swap(s1);
-          if (T0) {
-            T0->swap(sT0);
-            T1->swap(sT1);
-          }
-          *steps = ssteps;
-          single_only = true;
-        }
+        *steps += L.k;
         continue;
       }
     }
@@ -466,7 +455,6 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
     ++*steps;
   }
 }
-
 
 bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den) {
   Nat r0 = M, r1 = u, T0, T1 = from_u64(1);
