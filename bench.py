@@ -5,7 +5,9 @@ One step = one full exact solve (range check + Hadamard terms, batched
 modular inverse over all 53 primes, the m-step lift, digits to host, host
 rational reconstruction) of the n=1024, c=1 system with 24-bit entries
 (uniform in [-2^23, 2^23), seed 0): the workload the exact-solve card's
-§Measured table quotes (24-bit entries, n = 1024, c = 1).
+§Measured table quotes (24-bit entries, n = 1024, c = 1).  --workload names
+another system of inputs.WORKLOADS (the rest of that table's grid, the
+planted and scaled-Hilbert systems, the test configurations).
 
 Prints ONE JSON line (rank 0).  `value` = ms per solve with A and b already
 in HBM (CUDA events on the solve's stream; the host reconstruction is inside
@@ -38,10 +40,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "full exact-solve ms at n=1024,c=1"
 WORKLOAD = "n1024_c1_24bit"
-# exact-solve card §Measured: n=1024, c=1 median full solve, 2411 ms (RTX PRO 6000
-# Blackwell) / 2235 ms (H200); the faster of the two is the comparison point.
-PAGES_MS = 2235.0
+# exact-solve card §Measured: median full solves with 24-bit entries on H200 (the
+# faster of its two GPUs at n = 1024: 2411 ms RTX PRO 6000 Blackwell / 2235 ms H200).
+# Another machine's numbers: context for --workload runs of the same grid point.
+PAGES_H200_MS = {"n128_c1_24bit": 33.0, "n256_c1_24bit": 97.0, "n512_c1_24bit": 437.0,
+                 "n1024_c1_24bit": 2235.0, "n256_c16_24bit": 448.0, "n512_c16_24bit": 2624.0}
 L2_FLUSH_BYTES = 256 << 20
+
+
+def metric_for(workload):
+    return METRIC if workload == WORKLOAD else "full exact-solve ms (%s)" % workload
 
 
 def parse():
@@ -121,7 +129,10 @@ def oracle_sample(A, b, budget_s, sizes=None):
     n = A.shape[0]
     pts = []
     spent = 0.0
-    for k in sizes or (32, 48, 64, 80, 96, 112, 128, 160, 192, 224, 256):
+    sizes = sizes or (32, 48, 64, 80, 96, 112, 128, 160, 192, 224, 256)
+    if n <= sizes[0]:
+        sizes = (n,)  # small systems: the whole solve
+    for k in sizes:
         if k > n:
             break
         t0 = time.perf_counter()
@@ -188,9 +199,11 @@ def run_reference(args, rank, world):
         vals.append(v)
     wall = time.perf_counter() - t0
     v = statistics.median(vals)
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_for(args.workload), "value": v, "unit": "ms", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": v / PAGES_MS, "dtype": "int (Python big integers)",
+            "scaling": "weak",
+            "vs_baseline": (v / PAGES_H200_MS[args.workload]) if args.workload in PAGES_H200_MS else None,
+            "dtype": "int (Python big integers)",
             "data": "synthetic", "config": {"workload": args.workload, "seed": args.seed},
             "cpu_baseline": {"value": v, "unit": "ms", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -289,12 +302,15 @@ def run_gb300(args, rank, local_rank, world):
     if not args.no_cpu_baseline and world == 1:
         v, desc, _ = oracle_sample(A, b, args.cpu_budget)
         cpu = {"value": round(v, 1), "unit": "ms", "cores": 1, "kind": "oracle", "sample": desc}
+    base_ms = PAGES_H200_MS.get(args.workload)
     line = {
-        "metric": METRIC, "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(args.workload),
+        "value": round(ms, 4), "unit": "ms", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": round(ms / PAGES_MS, 6) if args.workload == WORKLOAD else None,
+        "vs_baseline": round(ms / base_ms, 6) if base_ms else None,
         "dtype": "int8", "data": "synthetic",
-        "config": {"workload": args.workload, "n": n, "c": c, "entries": "uniform [-2^23, 2^23)",
+        "config": {"workload": args.workload, "n": n, "c": c,
+                   "entries": inputs.WORKLOADS[args.workload].description,
                    "seed": args.seed, "m": s0.m, "primes_used": s0.primes_used,
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single"},

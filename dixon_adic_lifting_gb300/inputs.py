@@ -89,15 +89,26 @@ class Workload:
     description: str
 
 
-# The five systems the solver is measured and checked on.
+# The systems the solver is measured and checked on: the five test
+# configurations, the rest of the card's §Measured grid (24-bit entries),
+# and one each of its planted and scaled-Hilbert systems (§Correctness).
+_U24 = "A, b uniform in [-2^23, 2^23)"
 WORKLOADS = {
     "n32_c1_int8": Workload("n32_c1_int8", 32, 1,
                             "A, b uniform in [-127, 127]; A redrawn until invertible modulo every odd prime < 256"),
     "pascal30": Workload("pascal30", 30, 1,
                          "order-30 Pascal A_ij = C(i+j, i); b uniform in [-2^23, 2^23)"),
-    "n256_c1_24bit": Workload("n256_c1_24bit", 256, 1, "A, b uniform in [-2^23, 2^23)"),
-    "n1024_c1_24bit": Workload("n1024_c1_24bit", 1024, 1, "A, b uniform in [-2^23, 2^23)"),
+    "n128_c1_24bit": Workload("n128_c1_24bit", 128, 1, _U24),
+    "n256_c1_24bit": Workload("n256_c1_24bit", 256, 1, _U24),
+    "n512_c1_24bit": Workload("n512_c1_24bit", 512, 1, _U24),
+    "n1024_c1_24bit": Workload("n1024_c1_24bit", 1024, 1, _U24),
+    "n256_c16_24bit": Workload("n256_c16_24bit", 256, 16, _U24),
+    "n512_c16_24bit": Workload("n512_c16_24bit", 512, 16, _U24),
     "n4096_c64_16bit": Workload("n4096_c64_16bit", 4096, 64, "A, b uniform in [-2^15, 2^15)"),
+    "hilbert21": Workload("hilbert21", 21, 1,
+                          "scaled Hilbert A_ij = lcm(1..41) / (i + j + 1); b uniform in [-2^23, 2^23)"),
+    "planted256": Workload("planted256", 256, 1,
+                           "A uniform in [-2^23, 2^23), b = A x* for integer x* uniform in [-2^20, 2^20)"),
 }
 
 
@@ -108,10 +119,15 @@ def workload(name: str, seed: int = 0, attempt: int = 0):
         return uniform(32, 1, -127, 128, seed, attempt)
     if name == "pascal30":
         return pascal_system(30, 1, seed)
-    if name == "n256_c1_24bit":
-        return uniform(256, 1, -(1 << 23), 1 << 23, seed)
-    if name == "n1024_c1_24bit":
-        return uniform(1024, 1, -(1 << 23), 1 << 23, seed)
     if name == "n4096_c64_16bit":
         return uniform(4096, 64, -(1 << 15), 1 << 15, seed)
+    if name == "hilbert21":
+        g = _rng(seed, 21)
+        return scaled_hilbert(21), g.integers(-(1 << 23), 1 << 23, size=(21, 1), dtype=np.int64)
+    if name == "planted256":
+        A, b, _ = planted(256, 1, seed)
+        return A, b
+    if name in WORKLOADS and name.endswith("_24bit"):
+        w = WORKLOADS[name]
+        return uniform(w.n, w.c, -(1 << 23), 1 << 23, seed)
     raise KeyError(name)
