@@ -121,12 +121,12 @@ struct LiftRun {
 // wrapping around, so that its first barrier never completes (fault injection
 // of an expiring bounded wait).
 es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
-                         const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
-                         void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run,
+                         const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a,
+                         char* scratch, void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run,
                          bool stall_barrier = false);
 es_status run_lift_finish(LiftRun* run);
 es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
-                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a, char* scratch,
                    void* stream, KernelTiming* kt = nullptr, bool allow_fused = true);
 
 // ---------------------------------------------------------------- solution

@@ -110,16 +110,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Four signed bytes -> f16x2 of bytes 0, 1 (lo) and of bytes 2, 3 (hi): with
-// u = x + 128 (the top bit flipped), 0x64uu is the f16 1024 + u, and
-// 1024 + u - 1152 = x exactly.
-__device__ __forceinline__ void s8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  lo = __byte_perm(u, 0x64646464u, 0x4140);
-  hi = __byte_perm(u, 0x64646464u, 0x4342);
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
-}
 
 
 

@@ -18,6 +18,7 @@
 //   D     uint64 [m][n*c][6]       the digits
 //   A32   int32  [n][n]            A narrowed when max|A| < 2^31 (else A int64 is read)
 //   K     LiftConst                CRT / residual constants of the good prime set
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -244,10 +245,25 @@ __global__ void __launch_bounds__(256) k_lift_gemm(const int8_t* __restrict__ B,
   }
 }
 
+// Limb s of x mod 2^64 in balanced base 256: x = sum_s d_s 256^s (mod 2^64)
+// with d_s in [-128, 127] is byte s of x + 0x80...80, less 128.
+__device__ __forceinline__ __half x_limb(uint64_t x, int s) {
+  const uint64_t u = x + 0x8080808080808080ull;
+  return __int2half_rn((int)((u >> (8 * s)) & 255u) - 128);
+}
+
+// Where the tcgen05 residual update runs, the CRT also writes the limbs of
+// x_i mod 2^64 as f16 planes XL[na - 1 + s][col][i] (limb s, entry t = i c + col).
+struct XLimbs {
+  __half* XL;  // null: not written
+  int64_t c, ld;
+  int na;
+};
+
 // Same digit, one thread per entry (for many entries: no cross-lane work).
 __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restrict__ V, int64_t nc,
                                                          const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
-                                                         uint64_t* __restrict__ xl) {
+                                                         uint64_t* __restrict__ xl, XLimbs xo) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= nc) return;
   const int E = K->E;
@@ -255,20 +271,37 @@ __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restric
 #pragma unroll
   for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
   uint64_t tf = 0;
-  for (int e = 0; e < E; ++e) {
-    const ModQ m = K->mq[e];
-    const int32_t v = V[(int64_t)e * nc + t];
-    const uint32_t ce = barrett((uint32_t)(v < 0 ? v + (int32_t)m.q : v) * K->w[e], m);
-    tf += (uint64_t)ce * K->tfix[e];
+  // eight primes' residues are loaded before any is used, so that their
+  // latencies overlap
+#pragma unroll 1
+  for (int e0 = 0; e0 < E; e0 += 8) {
+    int32_t vv[8];
 #pragma unroll
-    for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+    for (int u = 0; u < 8; ++u) vv[u] = e0 + u < E ? V[(int64_t)(e0 + u) * nc + t] : 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u;
+      if (e >= E) break;
+      const ModQ m = K->mq[e];
+      const int32_t v = vv[u];
+      const uint32_t ce = barrett((uint32_t)(v < 0 ? v + (int32_t)m.q : v) * K->w[e], m);
+      tf += (uint64_t)ce * K->tfix[e];
+#pragma unroll
+      for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+    }
   }
   uint32_t S[kCrtWords];
   crt_finish(acc, tf, K, S);
   uint64_t* out = D + t * kDigitLimbs;
 #pragma unroll
   for (int l = 0; l < kDigitLimbs; ++l) out[l] = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
-  xl[t] = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+  const uint64_t x = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+  xl[t] = x;
+  if (xo.XL) {
+    const int64_t i = t / xo.c, col = t - i * xo.c;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) xo.XL[((int64_t)(xo.na - 1 + s) * xo.c + col) * xo.ld + i] = x_limb(x, s);
+  }
 }
 
 // Balanced CRT of one entry: x = sum_e c_e (P'/q_e) - t P', c_e = v_e w_e mod q_e,
@@ -279,7 +312,7 @@ __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restric
 // (identical) digit; lanes 0..5 store its six limbs.
 __global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
                                                   const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
-                                                  uint64_t* __restrict__ xl) {
+                                                  uint64_t* __restrict__ xl, XLimbs xo) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= nc) return;
@@ -294,6 +327,11 @@ __global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, 
     if (lane == l) limb = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
   if (lane < kDigitLimbs) D[t * kDigitLimbs + lane] = limb;
   if (lane == 0) xl[t] = limb;
+  if (xo.XL && lane < 8) {
+    const int64_t i = t / xo.c, col = t - i * xo.c;
+    const uint64_t x = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+    xo.XL[((int64_t)(xo.na - 1 + lane) * xo.c + col) * xo.ld + i] = x_limb(x, lane);
+  }
 }
 
 template <typename AT>
@@ -359,117 +397,178 @@ __global__ void __launch_bounds__(128) k_lift_resid_gemv(const AT* __restrict__ 
   for (int e = lane; e < E; e += 32) R[(int64_t)e * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
 
-// general c, int32 A: r'[i][col] = (r - sum_k A[i][k] x[k][col]) Pinv mod 2^64
-// and its residues.  With x = x_lo + 2^32 x_hi, x_lo read as a signed int32
-// and the borrow folded into the high word (x_hi' = x_hi + (x_lo >> 31)):
-//   A x mod 2^64 = sum_k A x_lo_s (exact int64 product) + 2^32 (sum_k A x_hi' mod 2^32)
-// i.e. one 32 x 32 -> 64 multiply-add and one 32-bit multiply-add per term.
-// CTA tile 64 rows x 64 columns, thread tile 4 x 4, K in slices of 32.
-__global__ void __launch_bounds__(256) k_lift_resid_gemm32(const int32_t* __restrict__ A, int64_t lda,
-                                                           const uint64_t* __restrict__ xl,
-                                                           const int64_t* __restrict__ r, int64_t n, int64_t c,
-                                                           int64_t ld, const LiftConst* __restrict__ K,
-                                                           int64_t* __restrict__ rn, int8_t* __restrict__ R) {
-  __shared__ int32_t As[64][33];
-  __shared__ int2 Xs[32][65];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int64_t row0 = (int64_t)blockIdx.y * 64, col0 = (int64_t)blockIdx.x * 64;
-  int64_t lo[4][4];
-  uint32_t hi[4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      lo[a][u] = 0;
-      hi[a][u] = 0;
-    }
-  for (int64_t k0 = 0; k0 < n; k0 += 32) {
-    for (int idx = tid; idx < 64 * 32; idx += 256) {
-      const int rr = idx >> 5, kk = idx & 31;
-      const int64_t i = row0 + rr, k = k0 + kk;
-      As[rr][kk] = (i < n && k < n) ? A[i * lda + k] : 0;
-      const int kr = idx >> 6, cc = idx & 63;
-      const int64_t krow = k0 + kr, col = col0 + cc;
-      const uint64_t x = (krow < n && col < c) ? xl[krow * c + col] : 0;
-      const uint32_t xlo = (uint32_t)x;
-      Xs[kr][cc] = make_int2((int32_t)xlo, (int32_t)((uint32_t)(x >> 32) + (xlo >> 31)));
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int kk = 0; kk < 32; ++kk) {
-      int32_t a[4];
-      int2 x[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) a[q] = As[4 * tx + q][kk];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) x[u] = Xs[kk][4 * ty + u];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          lo[q][u] += (int64_t)a[q] * (int64_t)x[u].x;
-          hi[q][u] += (uint32_t)a[q] * (uint32_t)x[u].y;
-        }
-    }
-    __syncthreads();
-  }
-  const int E = K->E;
+// general c: r'[i][col] = (r[i][col] - sum_k A[i][k] x[k][col]) Pinv mod 2^64
+// and its residues.  CTA tile 16 rows x 16 columns.  Its 256 threads are 16
+// thread tiles of 4 x 4 outputs times 16 slices of K (slice s takes the
+// groups k = 4s + 64t .. 4s + 64t + 3); the slices' partial sums meet in
+// shared memory, one thread per output adds them, and all threads then share
+// the E residues of the tile's 256 new residual entries (four rows, one
+// 32-bit store, per task).
+// For int32 A the product uses x = x_lo + 2^32 x_hi with x_lo read as a
+// signed int32 and its borrow folded into the high word (x_hi' = x_hi +
+// (x_lo >> 31)):
+//   A x mod 2^64 = sum_k A x_lo_s (exact int64) + 2^32 (sum_k A x_hi' mod 2^32),
+// one 32 x 32 -> 64 multiply-add and one 32-bit multiply-add per term; A is
+// the zero-padded int32 copy (lda = padded row length, a multiple of 16) and
+// x is zero for k >= n, so whole groups of four run to lda.  For int64 A
+// (entries of 2^31 or more, lda = n) the terms are full 64-bit products and
+// the groups stop at n.
+constexpr int kResidTile = 16;
+
+template <typename AT, bool VecX>
+__device__ __forceinline__ void resid_group(const AT* __restrict__ A, int64_t lda, const uint64_t* __restrict__ xl,
+                                            int64_t n, int64_t c, const int64_t (&arow)[4], int64_t col,
+                                            int64_t k, uint64_t (&acc)[4][4], uint32_t (&hi)[4][4]);
+
+// int32 A: four k at once (int4 of each row), x for four columns per k
+template <>
+__device__ __forceinline__ void resid_group<int32_t, true>(const int32_t* __restrict__ A, int64_t lda,
+                                                           const uint64_t* __restrict__ xl, int64_t n, int64_t c,
+                                                           const int64_t (&arow)[4], int64_t col, int64_t k,
+                                                           uint64_t (&acc)[4][4], uint32_t (&hi)[4][4]) {
+  int32_t a[4][4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int64_t i = row0 + 4 * tx + q;
-    if (i >= n) continue;
+    const int4 v = __ldg(reinterpret_cast<const int4*>(A + arow[q] * lda + k));
+    a[q][0] = v.x;
+    a[q][1] = v.y;
+    a[q][2] = v.z;
+    a[q][3] = v.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // c is a multiple of four: a column group lies wholly inside or outside [0, c)
+    const ulonglong2* X2 = reinterpret_cast<const ulonglong2*>(xl + (k + j) * c + col);
+    const ulonglong2 z = make_ulonglong2(0, 0);
+    const ulonglong2 x01 = col < c ? __ldg(X2) : z, x23 = col < c ? __ldg(X2 + 1) : z;
+    const uint64_t x[4] = {x01.x, x01.y, x23.x, x23.y};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int64_t col = col0 + 4 * ty + u;
-      if (col >= c) continue;
-      const uint64_t s = (uint64_t)lo[q][u] + ((uint64_t)hi[q][u] << 32);
-      const int64_t v = (int64_t)(((uint64_t)r[i * c + col] - s) * K->Pinv64);
-      rn[i * c + col] = v;
-      for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+      const uint32_t lo = (uint32_t)x[u];
+      const int64_t los = (int64_t)(int32_t)lo;
+      const uint32_t hw = (uint32_t)(x[u] >> 32) + (lo >> 31);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[q][u] += (uint64_t)((int64_t)a[q][j] * los);
+        hi[q][u] += (uint32_t)a[q][j] * hw;
+      }
     }
   }
 }
 
-// general c, int64 A (entries of 2^31 or more): tile 32 rows x 32 columns.
-template <typename AT>
-__global__ void __launch_bounds__(256) k_lift_resid_gemm(const AT* __restrict__ A, int64_t lda,
+// int32 A, c not a multiple of four: x read one column at a time
+template <>
+__device__ __forceinline__ void resid_group<int32_t, false>(const int32_t* __restrict__ A, int64_t lda,
+                                                            const uint64_t* __restrict__ xl, int64_t n, int64_t c,
+                                                            const int64_t (&arow)[4], int64_t col, int64_t k,
+                                                            uint64_t (&acc)[4][4], uint32_t (&hi)[4][4]) {
+  int32_t a[4][4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int4 v = __ldg(reinterpret_cast<const int4*>(A + arow[q] * lda + k));
+    a[q][0] = v.x;
+    a[q][1] = v.y;
+    a[q][2] = v.z;
+    a[q][3] = v.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint64_t x = col + u < c ? __ldg(xl + (k + j) * c + col + u) : 0;
+      const uint32_t lo = (uint32_t)x;
+      const int64_t los = (int64_t)(int32_t)lo;
+      const uint32_t hw = (uint32_t)(x >> 32) + (lo >> 31);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[q][u] += (uint64_t)((int64_t)a[q][j] * los);
+        hi[q][u] += (uint32_t)a[q][j] * hw;
+      }
+    }
+  }
+}
+
+// int64 A: plain 64-bit products, k < n
+template <>
+__device__ __forceinline__ void resid_group<int64_t, false>(const int64_t* __restrict__ A, int64_t lda,
+                                                            const uint64_t* __restrict__ xl, int64_t n, int64_t c,
+                                                            const int64_t (&arow)[4], int64_t col, int64_t k,
+                                                            uint64_t (&acc)[4][4], uint32_t (&)[4][4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (k + j >= n) break;
+    uint64_t x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = col + u < c ? __ldg(xl + (k + j) * c + col + u) : 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t a = (uint64_t)__ldg(A + arow[q] * lda + k + j);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[q][u] += a * x[u];
+    }
+  }
+}
+
+template <typename AT, bool VecX>
+__global__ void __launch_bounds__(256) k_lift_resid_tile(const AT* __restrict__ A, int64_t lda,
                                                          const uint64_t* __restrict__ xl,
                                                          const int64_t* __restrict__ r, int64_t n, int64_t c,
                                                          int64_t ld, const LiftConst* __restrict__ K,
                                                          int64_t* __restrict__ rn, int8_t* __restrict__ R) {
-  __shared__ int64_t As[32][33];
-  __shared__ uint64_t Xs[32][33];
-  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
-  const int64_t row0 = (int64_t)blockIdx.y * 32, col0 = (int64_t)blockIdx.x * 32;
-  uint64_t acc[4] = {0, 0, 0, 0};
-  for (int64_t k0 = 0; k0 < n; k0 += 32) {
-    for (int idx = tid; idx < 32 * 32; idx += 256) {
-      int rr = idx >> 5, kk = idx & 31;
-      int64_t i = row0 + rr, k = k0 + kk;
-      As[rr][kk] = (i < n && k < n) ? (int64_t)A[i * lda + k] : 0;
-      int64_t col = col0 + kk;  // reuse: Xs[k][col]
-      int64_t kr = k0 + rr;
-      Xs[rr][kk] = (kr < n && col < c) ? xl[kr * c + col] : 0;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < 32; ++kk) {
-      int64_t a = As[tx][kk];
+  constexpr int T = kResidTile;
+  __shared__ uint64_t part[16][T * T];
+  __shared__ int64_t vs[T][T + 1];  // [column][row]
+  const int tid = threadIdx.x, sub = tid & 15, s = tid >> 4;
+  const int rg = sub >> 2, cg = sub & 3;
+  const int64_t row0 = (int64_t)blockIdx.x * T, col0 = (int64_t)blockIdx.y * T;
+  const int64_t col = col0 + 4 * cg;
+  int64_t arow[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc[u] += (uint64_t)a * Xs[kk][ty * 4 + u];
-    }
-    __syncthreads();
+  for (int q = 0; q < 4; ++q) {
+    const int64_t i = row0 + 4 * rg + q;
+    arow[q] = i < n ? i : n - 1;  // clamped; its result is discarded
   }
-  const int64_t i = row0 + tx;
-  if (i >= n) return;
-  const int E = K->E;
+  uint64_t acc[4][4];
+  uint32_t hi[4][4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    int64_t col = col0 + ty * 4 + u;
-    if (col >= c) continue;
-    int64_t v = (int64_t)(((uint64_t)r[i * c + col] - acc[u]) * K->Pinv64);
-    rn[i * c + col] = v;
-    for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + i] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc[q][u] = 0;
+      hi[q][u] = 0;
+    }
+  const int64_t kend = sizeof(AT) == 4 ? lda : n;
+  for (int64_t k = 4 * s; k < kend; k += 64) resid_group<AT, VecX>(A, lda, xl, n, c, arow, col, k, acc, hi);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      part[s][(4 * rg + q) * T + 4 * cg + u] = acc[q][u] + ((uint64_t)hi[q][u] << 32);
+  __syncthreads();
+  {
+    const int rl = tid >> 4, cl = tid & 15;
+    const int64_t i = row0 + rl, cc = col0 + cl;
+    uint64_t sum = 0;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) sum += part[t][tid];
+    int64_t v = 0;
+    if (i < n && cc < c) {
+      v = (int64_t)(((uint64_t)r[i * c + cc] - sum) * K->Pinv64);
+      rn[i * c + cc] = v;
+    }
+    vs[cl][rl] = v;
+  }
+  __syncthreads();
+  const int E = K->E;
+  for (int t = tid; t < E * T * 4; t += 256) {
+    const int e = t / (T * 4), cl = (t >> 2) & (T - 1), g = t & 3;
+    const int64_t cc = col0 + cl;
+    if (cc >= c) continue;
+    const ModQ m = K->mq[e];
+    uint32_t w = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) w |= (uint32_t)(uint8_t)(int8_t)reduce_i64_bal(vs[cl][4 * g + b], m) << (8 * b);
+    *reinterpret_cast<uint32_t*>(R + ((int64_t)e * c + cc) * ld + row0 + 4 * g) = w;
   }
 }
 
@@ -484,9 +583,10 @@ __global__ void k_narrow_a(const int64_t* __restrict__ A, int64_t n, int64_t lda
 // ------------------------------------------------------------ driver
 namespace {
 constexpr int64_t kTcMinCols = 16;       // c >= 16: product on tcgen05 (k_lift_tc.cu)
+constexpr int64_t kResidTcMinN = 1024;   // from this n: the residual update on tcgen05 (k_lift_tc.cu)
 constexpr int64_t kCrtThreadMin = 32768;  // from this many entries: one thread per entry
 struct LiftLayout {
-  size_t K, R, V, r, xl, A32, B16, R16, Bf, err, bar, total;
+  size_t K, R, V, r, xl, A32, R16, A16, X16, Bf, err, bar, total;
 };
 LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   int64_t ld = padded_ld(n);
@@ -499,8 +599,9 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   o.r = L.add((size_t)2 * n * c * 8);
   o.xl = L.add((size_t)padded_ld(n) * c * 8);
   o.A32 = a32 ? L.add((size_t)n * padded_ld(n) * 4) : 0;
-  o.B16 = tc ? L.add((size_t)kNumPrimes * n * ld * 2) : 0;
   o.R16 = tc ? L.add((size_t)E * c * ld * 2) : 0;
+  o.A16 = tc && a32 ? L.add((size_t)kResidLimbsMax * n * ld * 2) : 0;
+  o.X16 = tc && a32 ? L.add((size_t)(kResidLimbsMax + 7) * c * ld * 2) : 0;
   o.Bf = (c == 1 && ld <= kFusedMaxLd) ? L.add((size_t)E * n * ld) : 0;
   o.err = L.add(sizeof(int));
   o.bar = L.add(sizeof(unsigned));
@@ -531,9 +632,11 @@ es_status create_events(LiftRun* run, size_t count) {
 }  // namespace
 
 es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
-                         const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
-                         void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run, bool stall_barrier) {
+                         const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a,
+                         char* scratch, void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run,
+                         bool stall_barrier) {
   cudaStream_t st = (cudaStream_t)stream;
+  const bool a32 = max_abs_a < (uint64_t(1) << 31);
   LiftConst hK;
   build_lift_const(good_host, &hK);
   if (hK.E == 0) return ES_ERR_ARG;
@@ -547,8 +650,15 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
   uint64_t* xl = reinterpret_cast<uint64_t*>(scratch + L.xl);
   int32_t* A32 = a32 ? reinterpret_cast<int32_t*>(scratch + L.A32) : nullptr;
   const bool tc = c >= kTcMinCols;
-  void* B16 = tc ? (void*)(scratch + L.B16) : nullptr;
   void* R16 = tc ? (void*)(scratch + L.R16) : nullptr;
+  // tcgen05 residual update with the tcgen05 product (entries below 2^31,
+  // n >= kResidTcMinN: below that its few CTAs, each forming the residues of
+  // 128 x 8 entries, lose to the CUDA-core update)
+  int na = tc && a32 && n >= kResidTcMinN ? resid_limbs(max_abs_a) : 0;
+  if ((int64_t)na * n > kResidTcMaxK) na = 0;
+  TcResid tcr;
+  XLimbs xo{nullptr, c, ld, na};
+  if (na) xo.XL = reinterpret_cast<__half*>(scratch + L.X16);
   int* err = reinterpret_cast<int*>(scratch + L.err);
   unsigned* bar = reinterpret_cast<unsigned*>(scratch + L.bar);
   TcLift tcl;
@@ -572,17 +682,15 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
   } else {
     ES_CHECK(cuda_status(cudaMemsetAsync(bar, 0, sizeof(unsigned), st), "memset barrier"));
   }
-  if (tc) {
-    ES_CHECK(tc_convert_f16(B_dev, B16, (int64_t)kNumPrimes * n * ld, st));
-    ES_CHECK(tc_prepare(&tcl, B16, R16, n, c, ld, E));
-  }
-  if (a32) {
+  if (tc) ES_CHECK(tc_prepare(&tcl, B_dev, R16, n, c, ld, E));
+  if (na) ES_CHECK(tc_resid_prepare(&tcr, A_dev, scratch + L.A16, xo.XL, n, c, ld, na, st));
+  if (a32 && !na) {
     k_narrow_a<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, A32);
     ES_CHECK(cuda_status(cudaGetLastError(), "k_narrow_a"));
   }
   k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R);
   ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_init"));
-  count_launch(a32 ? 2 : 1);
+  count_launch(a32 && !na ? 2 : 1);
   run->stream = stream;
   run->kt = kt;
   if (kt && kt->events) ES_CHECK(create_events(run, fused ? 2 : 2 * (size_t)m));
@@ -604,7 +712,8 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     }
   }
   for (int32_t i = 0; i < m && !fused; ++i) {
-    if (tc) ES_CHECK(tc_convert_f16(R, R16, (int64_t)E * c * ld, st));
+    // the tcgen05 residual update writes R16 itself; step 0 converts the residues of b
+    if (tc && (i == 0 || !na)) ES_CHECK(tc_convert_f16(R, R16, (int64_t)E * c * ld, st));
     if (!run->ev.empty()) cudaEventRecord(ev(2 * i), st);
     if (c == 1) {
       k_lift_gemv<4><<<dim3((unsigned)((n + 31) / 32), E), 256, 0, st>>>(B_dev, R, n, ld, K, V);
@@ -620,26 +729,31 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     count_launch();
     if (nc >= kCrtThreadMin)
       k_lift_crt_thread<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
-                                                                      xl);
+                                                                      xl, xo);
     else
-      k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl);
+      k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl,
+                                                          xo);
     if (i + 1 < m) {
-      count_launch(1);
       const int64_t* rc = r[i & 1];
       int64_t* rn = r[(i + 1) & 1];
+      if (na) {
+        ES_CHECK(tc_resid_launch(tcr, K, rc, rn, R16, n, c, ld, err, st));
+        continue;
+      }
+      count_launch(1);
       if (c == 1) {
         if (a32)
           k_lift_resid_gemv<int32_t><<<(unsigned)((n + 3) / 4), 128, 0, st>>>(A32, ld, xl, rc, n, ld, K, rn, R);
         else
           k_lift_resid_gemv<int64_t><<<(unsigned)((n + 3) / 4), 128, 0, st>>>(A_dev, n, xl, rc, n, ld, K, rn, R);
       } else {
-        if (a32) {
-          dim3 g((unsigned)((c + 63) / 64), (unsigned)((n + 63) / 64));
-          k_lift_resid_gemm32<<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
-        } else {
-          dim3 g((unsigned)((c + 31) / 32), (unsigned)((n + 31) / 32));
-          k_lift_resid_gemm<int64_t><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
-        }
+        const dim3 g((unsigned)((n + kResidTile - 1) / kResidTile), (unsigned)((c + kResidTile - 1) / kResidTile));
+        if (a32 && c % 4 == 0)
+          k_lift_resid_tile<int32_t, true><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+        else if (a32)
+          k_lift_resid_tile<int32_t, false><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+        else
+          k_lift_resid_tile<int64_t, false><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
       }
     }
   }
@@ -665,7 +779,7 @@ es_status run_lift_finish(LiftRun* run) {
     set_last_error("fused lift kernel: the short-path digit disagreed with the full digit");
     sst = ES_ERR_INTERNAL;
   } else if (sst == ES_OK && herr) {
-    set_last_error(std::string(fused ? "fused lift kernel" : "lift product kernel") +
+    set_last_error(std::string(fused ? "fused lift kernel" : "lift step kernels") +
                    ": bounded wait expired (code " + std::to_string(herr) + ")");
     sst = ES_ERR_TIMEOUT;
   }
@@ -690,10 +804,10 @@ es_status run_lift_finish(LiftRun* run) {
 }
 
 es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
-                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, bool a32, char* scratch,
+                   const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a, char* scratch,
                    void* stream, KernelTiming* kt, bool allow_fused) {
   LiftRun run;
-  ES_CHECK(run_lift_start(A_dev, b_dev, n, c, B_dev, good_host, m, digits_dev, a32, scratch, stream, kt,
+  ES_CHECK(run_lift_start(A_dev, b_dev, n, c, B_dev, good_host, m, digits_dev, max_abs_a, scratch, stream, kt,
                           allow_fused, &run));
   return run_lift_finish(&run);
 }

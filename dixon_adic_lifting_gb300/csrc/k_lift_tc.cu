@@ -3,23 +3,30 @@
 // (exact-solve card, §Method: the per-step per-prime products as one batched
 // GEMM on balanced residues, exact in the integer accumulator).
 //
-// sm_103a has no integer tcgen05 MMA kind, so residues are kept as f16
-// (every |v| <= 125 is exact in f16) and multiplied with tcgen05.mma
-// .kind::f16 into an FP32 accumulator in tensor memory.  FP32 is exact for
-// integers below 2^24; the accumulator is folded into int32 registers every
-// kFoldBlocks K-blocks (K = 512: |partial| <= 512 * 125^2 < 2^23) and then
-// restarted, so the product is exact for any n <= 2^17.
+// sm_103a has no integer tcgen05 MMA kind, so residues are multiplied as f16
+// (every |v| <= 125 is exact in f16) with tcgen05.mma .kind::f16 into an FP32
+// accumulator in tensor memory.  FP32 is exact for integers below 2^24; the
+// accumulator is folded into int32 registers every 512 K (|partial| <= 512 *
+// 125^2 < 2^23) and then restarted, so the product is exact for any n <= 2^17.
+// B_j stays int8 in HBM (the product is bound by reading it once per step):
+// TMA brings 128 x 128 int8 tiles into shared memory and four converter warps
+// widen them into the f16 operand tiles the MMA reads.
 //
 // CTA = one prime e, 128 rows of B_j (MMA M = 128) and NT columns (N = NT):
-//   warp 0      one thread: TMA producer, 4-stage ring of 128B-swizzled
-//               K-major tiles (A: 128 x 64 f16 of B_j, B: NT x 64 f16 of R_e)
-//   warp 1      one thread: issues 4 MMAs (K = 16 each) per stage; commits
-//               free the stage and, at chunk ends, publish the accumulator
+//   warp 0      one thread: TMA producer, 3-stage ring; a stage is K = 128:
+//               the int8 tile of B_j and two NT x 64 f16 tiles of R_e
+//               (128-byte swizzled, K-major)
+//   warps 6..9  converters: thread r widens row r of the int8 tile into the
+//               stage's two 128 x 64 f16 tiles (same swizzle), then a
+//               proxy fence and an arrive on the stage's `conv` barrier
+//   warp 1      one thread: 8 MMAs (K = 16 each) per stage; a commit frees
+//               the stage and, at 512-K chunk ends, publishes the accumulator
 //   warps 2..5  epilogue: fold each finished chunk from TMEM (tcgen05.ld,
 //               lane quarter = warp % 4) into int32, Barrett at the end.
 // The TMEM accumulator is double-buffered (2 NT columns) so MMAs of the next
 // chunk overlap the fold of the previous one.  Every mbarrier wait is bounded:
-// on expiry the kernel records an error code, stops issuing work and returns.
+// on expiry the kernel records an error code, stops issuing work, lets the
+// copies and MMAs in flight land and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -35,42 +42,64 @@ namespace es {
 namespace {
 using namespace tc;
 
-constexpr int kBM = 128;           // MMA M (rows of B_j per CTA)
-constexpr int kBK = 64;            // K per stage: one 128-byte row of f16
-constexpr int kStages = 4;
-constexpr int kFoldBlocks = 8;     // fold every 8 stages (K = 512)
-constexpr int kThreads = 192;
+constexpr int kBM = 128;           // MMA M (rows per CTA)
+constexpr int kBK = 64;            // f16 tile K: one 128-byte row
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 
+// product kernel
+constexpr int kPStages = 3;
+constexpr int kPK = 128;                    // K per stage: one 128-byte int8 row
+constexpr int kPTileI8 = kBM * kPK;         // 16 KB
+constexpr int kPFoldStages = 4;             // fold every 4 stages (K = 512)
+constexpr int kPThreads = 320;
+
+// residual kernel
+constexpr int kStages = 4;
+constexpr int kFoldBlocks = 8;     // fold every 8 K-blocks (K = 512)
+constexpr int kThreads = 192;
+
+// The producer's exit: wait (bounded, whatever the error flag) for the copies
+// of the last `depth` stages it issued, so that none is still writing shared
+// memory when the CTA ends.
+__device__ __forceinline__ void drain_loads(uint64_t* full, int issued, int depth) {
+  for (int kb = issued > depth ? issued - depth : 0; kb < issued; ++kb)
+    mbar_wait_drain(full + kb % depth, (kb / depth) & 1);
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 1)
     k_lift_gemm_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmR,
-                   const LiftConst* __restrict__ K, int8_t* __restrict__ V, int n, int c, int kblocks,
+                   const LiftConst* __restrict__ K, int8_t* __restrict__ V, int n, int c, int kstages,
                    int* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kATileBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * NT * 128);
-  uint64_t* empty = full + kStages;
-  uint64_t* accfull = empty + kStages;
+  uint8_t* sI = smem;                               // [S] 128 x 128 int8
+  uint8_t* sF = sI + kPStages * kPTileI8;           // [S][2] 128 x 64 f16
+  uint8_t* sR = sF + kPStages * 2 * kATileBytes;    // [S][2] NT x 64 f16
+  uint64_t* full = reinterpret_cast<uint64_t*>(sR + kPStages * 2 * NT * 128);
+  uint64_t* conv = full + kPStages;
+  uint64_t* empty = conv + kPStages;
+  uint64_t* accfull = empty + kPStages;
   uint64_t* accempty = accfull + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(accempty + 2);
+  uint64_t* drained = accempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.z, j = K->pidx[e];
   const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * NT;
-  const int nchunks = (kblocks + kFoldBlocks - 1) / kFoldBlocks;
+  const int nchunks = (kstages + kPFoldStages - 1) / kPFoldStages;
   constexpr uint32_t kCols = 2 * NT < 32 ? 32 : 2 * NT;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kPStages; ++s) {
       mbar_init(full + s, 1);
+      mbar_init(conv + s, 128);
       mbar_init(empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accfull + b, 1);
       mbar_init(accempty + b, 128);
     }
+    mbar_init(drained, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -85,32 +114,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages && !mbar_wait(empty + s, ((kb / kStages) & 1) ^ 1, err, 1)) break;
-        mbar_expect_tx(full + s, kATileBytes + NT * 128);
-        tma_load_3d(sA + s * kATileBytes, &tmB, full + s, kb * kBK, m0, j);
-        tma_load_3d(sB + s * NT * 128, &tmR, full + s, kb * kBK, n0, e);
+      int issued = 0;
+      for (int st = 0; st < kstages; ++st) {
+        const int s = st % kPStages;
+        if (st >= kPStages && !mbar_wait(empty + s, ((st / kPStages) & 1) ^ 1, err, 1)) break;
+        mbar_expect_tx(full + s, kPTileI8 + 2 * NT * 128);
+        tma_load_3d(sI + s * kPTileI8, &tmB, full + s, st * kPK, m0, j);
+        tma_load_3d(sR + (2 * s) * NT * 128, &tmR, full + s, st * kPK, n0, e);
+        tma_load_3d(sR + (2 * s + 1) * NT * 128, &tmR, full + s, st * kPK + kBK, n0, e);
+        issued = st + 1;
       }
+      drain_loads(full, issued, kPStages);
+    }
+  } else if (warp >= 6) {  // converters: thread r owns row r
+    const int r = threadIdx.x - 192, sw = r & 7;
+    for (int st = 0; st < kstages; ++st) {
+      const int s = st % kPStages;
+      if (!mbar_wait(full + s, (st / kPStages) & 1, err, 5)) break;
+      const uint8_t* src = sI + s * kPTileI8 + r * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {  // 16-byte chunk q of the int8 row: k = 16 q .. 16 q + 15
+        const uint4 w = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
+        uint4 a, b;
+        s8x4_to_f16(w.x, a.x, a.y);
+        s8x4_to_f16(w.y, a.z, a.w);
+        s8x4_to_f16(w.z, b.x, b.y);
+        s8x4_to_f16(w.w, b.z, b.w);
+        // f16 tile q / 4, its chunks 2 (q % 4) and 2 (q % 4) + 1
+        uint8_t* dst = sF + (2 * s + (q >> 2)) * kATileBytes + r * 128;
+        const int c0 = 2 * (q & 3);
+        *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) = a;
+        *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ sw) << 4)) = b;
+      }
+      fence_proxy_async_smem();  // the generic-proxy writes, before the tensor core reads them
+      mbar_arrive(conv + s);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages, ch = kb / kFoldBlocks, buf = ch & 1;
-        const bool first = (kb % kFoldBlocks) == 0;
+      for (int st = 0; st < kstages; ++st) {
+        const int s = st % kPStages, ch = st / kPFoldStages, buf = ch & 1;
+        const bool first = (st % kPFoldStages) == 0;
         if (first && ch >= 2 && !mbar_wait(accempty + buf, ((ch - 2) >> 1) & 1, err, 2)) break;
-        if (!mbar_wait(full + s, (kb / kStages) & 1, err, 3)) break;
+        if (!mbar_wait(conv + s, (st / kPStages) & 1, err, 3)) break;
         tc_fence_after();
-        const uint64_t ad = desc_sw128(sA + s * kATileBytes), bd = desc_sw128(sB + s * NT * 128);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          mma_f16(tmem + buf * NT, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t ad = desc_sw128(sF + (2 * s + h) * kATileBytes), bd = desc_sw128(sR + (2 * s + h) * NT * 128);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_f16(tmem + buf * NT, ad + 2 * k, bd + 2 * k, idesc, (first && h == 0 && k == 0) ? 0u : 1u);
+        }
         mma_commit(empty + s);
-        if ((kb % kFoldBlocks) == kFoldBlocks - 1 || kb == kblocks - 1) mma_commit(accfull + buf);
+        if ((st % kPFoldStages) == kPFoldStages - 1 || st == kstages - 1) mma_commit(accfull + buf);
       }
+      // every MMA issued has completed before tensor memory is released
+      mma_commit(drained);
+      mbar_wait_drain(drained, 0);
     }
-  } else {  // epilogue warpgroup
+  } else {  // epilogue warpgroup (warps 2..5)
     const int quarter = warp & 3;
     const int row = m0 + 32 * quarter + lane;
     const ModQ m = K->mq[e];
@@ -150,6 +212,175 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- residual
+// r_{i+1} = (r_i - A x_i) P'^{-1} mod 2^64 on the tensor cores (exact-solve
+// card, §Method: the residual kept in one 64-bit limb).  With A = sum_a A_a
+// 256^a and x_i = sum_s X_s 256^s (mod 2^64) in balanced 8-bit limbs (|A_a|,
+// |X_s| <= 128, exact in f16),
+//     A x_i = sum_{s < 8} 256^s Y_s  (mod 2^64),   Y_s = sum_a A_a X_{s-a},
+// which is one GEMM with K' = na ld: the A operand is A's limb planes side by
+// side; on the K range of plane a, row (s, col) of the B operand is
+// X_{s-a}[col], read by one 3-D TMA box of 8 limb planes x 8 columns from the
+// X planes (stored after na - 1 zero planes, so X_{s-a} is plane s - a + na - 1).
+// Products are at most 2^14, so 512-term FP32 partial sums are exact; the
+// accumulator is folded into int32 registers every kFoldBlocks K-blocks as in
+// the product kernel (|Y_s| <= na n 2^14 <= 2^30 for na n <= kResidTcMaxK).
+// The epilogue combines each column's eight Y_s and writes r_{i+1};
+// k_lift_r16 then forms its balanced residues as f16, straight into the
+// product's B operand (R16 [E'][c][ld]).
+// CTA = 128 rows x 8 columns (MMA N = 64: limb-major, column-minor); warp
+// roles as in k_lift_gemm_tc; two CTAs per SM, so that one's epilogue
+// overlaps the other's main loop.
+constexpr int kRNT = 64;
+constexpr int kRCols = 8;
+
+__global__ void __launch_bounds__(kThreads, 2)
+    k_lift_resid_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX,
+                    const LiftConst* __restrict__ K, const int64_t* __restrict__ r, int64_t* __restrict__ rn,
+                    int n, int c, int na, int kbp, int* __restrict__ err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kRNT * 128);
+  uint64_t* empty = full + kStages;
+  uint64_t* accfull = empty + kStages;
+  uint64_t* accempty = accfull + 2;
+  uint64_t* drained = accempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM, col0 = blockIdx.y * kRCols;
+  const int kblocks = na * kbp;
+  const int nchunks = (kblocks + kFoldBlocks - 1) / kFoldBlocks;
+  constexpr uint32_t kCols = 2 * kRNT;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accfull + b, 1);
+      mbar_init(accempty + b, 128);
+    }
+    mbar_init(drained, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(kCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      int issued = 0;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int s = kb % kStages, a = kb / kbp, k0 = (kb - a * kbp) * kBK;
+        if (kb >= kStages && !mbar_wait(empty + s, ((kb / kStages) & 1) ^ 1, err, 1)) break;
+        mbar_expect_tx(full + s, kATileBytes + kRNT * 128);
+        tma_load_3d(sA + s * kATileBytes, &tmA, full + s, k0, m0, a);
+        tma_load_3d(sB + s * kRNT * 128, &tmX, full + s, k0, col0, na - 1 - a);
+        issued = kb + 1;
+      }
+      drain_loads(full, issued, kStages);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(kRNT >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int s = kb % kStages, ch = kb / kFoldBlocks, buf = ch & 1;
+        const bool first = (kb % kFoldBlocks) == 0;
+        if (first && ch >= 2 && !mbar_wait(accempty + buf, ((ch - 2) >> 1) & 1, err, 2)) break;
+        if (!mbar_wait(full + s, (kb / kStages) & 1, err, 3)) break;
+        tc_fence_after();
+        const uint64_t ad = desc_sw128(sA + s * kATileBytes), bd = desc_sw128(sB + s * kRNT * 128);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          mma_f16(tmem + buf * kRNT, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
+        mma_commit(empty + s);
+        if ((kb % kFoldBlocks) == kFoldBlocks - 1 || kb == kblocks - 1) mma_commit(accfull + buf);
+      }
+      // every MMA issued has completed before tensor memory is released
+      mma_commit(drained);
+      mbar_wait_drain(drained, 0);
+    }
+  } else {  // epilogue warpgroup
+    const int quarter = warp & 3;
+    const int row = m0 + 32 * quarter + lane;
+    int32_t acc[kRNT];
+#pragma unroll
+    for (int t = 0; t < kRNT; ++t) acc[t] = 0;
+    bool ok = true;
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int buf = ch & 1;
+      if (!mbar_wait(accfull + buf, (ch >> 1) & 1, err, 4)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int c16 = 0; c16 < kRNT / 16; ++c16) {
+        float f[16];
+        tmem_ld<16>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kRNT + 16 * c16), f);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) acc[16 * c16 + t] += __float2int_rn(f[t]);
+      }
+      tc_fence_before();
+      mbar_arrive(accempty + buf);
+    }
+    if (ok && row < n) {
+      const uint64_t pinv = K->Pinv64;
+#pragma unroll
+      for (int cl = 0; cl < kRCols; ++cl) {
+        const int col = col0 + cl;
+        if (col >= c) break;
+        uint64_t S = 0;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) S += (uint64_t)(int64_t)acc[s * kRCols + cl] << (8 * s);
+        rn[(int64_t)row * c + col] = (int64_t)(((uint64_t)r[(int64_t)row * c + col] - S) * pinv);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+  }
+}
+
+// R16[e][col][i] = balanced residue of r_{i+1}[i][col] mod q_e, as f16; one
+// thread per entry, rows fastest so that the stores of a prime are coalesced.
+__global__ void __launch_bounds__(256) k_lift_r16(const int64_t* __restrict__ rn, int64_t n, int64_t c, int64_t ld,
+                                                  const LiftConst* __restrict__ K, __half* __restrict__ R16) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n * c) return;
+  const int64_t col = t / n, i = t - col * n;
+  const int64_t v = rn[i * c + col];
+  const int E = K->E;
+  __half* out = R16 + col * ld + i;
+  for (int e = 0; e < E; ++e) out[(int64_t)e * c * ld] = __int2half_rn(reduce_i64_bal(v, K->mq[e]));
+}
+
+// A16[a][i][k] = limb a of A[i][k] in balanced base 256 (k < n), 0 for n <= k < ld.
+__global__ void k_a_limbs(const int64_t* __restrict__ A, int64_t n, int64_t ld, int na, __half* __restrict__ A16) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n * ld) return;
+  const int64_t i = t / ld, k = t - i * ld;
+  int64_t v = k < n ? A[i * n + k] : 0;
+  for (int a = 0; a < na - 1; ++a) {
+    const int64_t d = ((v + 128) & 255) - 128;
+    A16[((int64_t)a * n + i) * ld + k] = __int2half_rn((int)d);
+    v = (v - d) >> 8;
+  }
+  A16[((int64_t)(na - 1) * n + i) * ld + k] = __int2half_rn((int)v);
+}
+
 __global__ void k_to_f16(const int8_t* __restrict__ src, __half* __restrict__ dst, int64_t count) {
   int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (t + 4 <= count) {
@@ -165,14 +396,14 @@ __global__ void k_to_f16(const int8_t* __restrict__ src, __half* __restrict__ ds
 template <int NT>
 es_status launch_nt(const CUtensorMap& mB, const CUtensorMap& mR, const LiftConst* K, int8_t* V, int64_t n,
                     int64_t c, int64_t ld, int E, int* err, cudaStream_t st) {
-  const size_t smem = 1024 + (size_t)kStages * (kATileBytes + NT * 128) + 256;
+  const size_t smem = 1024 + (size_t)kPStages * (kPTileI8 + 2 * kATileBytes + 2 * NT * 128) + 256;
   static_assert(NT % 16 == 0 && NT <= 64, "N tile");
   ES_CHECK(cuda_status(cudaFuncSetAttribute(k_lift_gemm_tc<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)smem),
                        "tc smem attribute"));
   dim3 grid((unsigned)((n + kBM - 1) / kBM), (unsigned)((c + NT - 1) / NT), (unsigned)E);
-  const int kblocks = (int)((ld + kBK - 1) / kBK);
-  k_lift_gemm_tc<NT><<<grid, kThreads, smem, st>>>(mB, mR, K, V, (int)n, (int)c, kblocks, err);
+  const int kstages = (int)((ld + kPK - 1) / kPK);
+  k_lift_gemm_tc<NT><<<grid, kPThreads, smem, st>>>(mB, mR, K, V, (int)n, (int)c, kstages, err);
   return cuda_status(cudaGetLastError(), "k_lift_gemm_tc");
 }
 
@@ -185,11 +416,50 @@ es_status tc_convert_f16(const int8_t* src, void* dst, int64_t count, void* stre
   return cuda_status(cudaGetLastError(), "k_to_f16");
 }
 
-es_status tc_prepare(TcLift* t, const void* B16, const void* R16, int64_t n, int64_t c, int64_t ld, int E) {
+es_status tc_prepare(TcLift* t, const int8_t* B, const void* R16, int64_t n, int64_t c, int64_t ld, int E) {
   t->nt = c <= 16 ? 16 : c <= 32 ? 32 : 64;
-  ES_CHECK(make_map(&t->mapB, B16, ld, n, kNumPrimes, kBM));
+  ES_CHECK(make_map_u8(&t->mapB, B, ld, n, kNumPrimes, kBM));
   ES_CHECK(make_map(&t->mapR, R16, ld, c, E, t->nt));
   return ES_OK;
+}
+
+int resid_limbs(uint64_t max_abs_a) {
+  // After na - 1 balanced peels |top| <= (|A| + 128 (256^(na-1) - 1) / 255) / 256^(na-1),
+  // which stays within 128 when |A| + 128 (256^(na-1) - 1) / 255 < 129 256^(na-1).
+  for (int na = 1; na <= kResidLimbsMax; ++na) {
+    const uint64_t w = uint64_t(1) << (8 * (na - 1));
+    if (max_abs_a + 128 * ((w - 1) / 255) < 129 * w) return na;
+  }
+  return 0;
+}
+
+es_status tc_resid_prepare(TcResid* t, const int64_t* A_dev, void* A16, void* X16, int64_t n, int64_t c, int64_t ld,
+                           int na, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (na < 1 || na > kResidLimbsMax) return ES_ERR_INTERNAL;
+  t->na = na;
+  t->kbp = (int)((ld + kBK - 1) / kBK);
+  k_a_limbs<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, na, (__half*)A16);
+  count_launch();
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_a_limbs"));
+  ES_CHECK(cuda_status(cudaMemsetAsync(X16, 0, (size_t)(na + 7) * c * ld * 2, st), "memset x limbs"));
+  ES_CHECK(make_map(&t->mapA, A16, ld, n, na, kBM));
+  ES_CHECK(make_map(&t->mapX, X16, ld, c, na + 7, kRCols, 8));
+  return ES_OK;
+}
+
+es_status tc_resid_launch(const TcResid& t, const LiftConst* K, const int64_t* r, int64_t* rn, void* R16, int64_t n,
+                          int64_t c, int64_t ld, int* err, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t smem = 1024 + (size_t)kStages * (kATileBytes + kRNT * 128) + 256;
+  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_lift_resid_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                       "tc resid smem attribute"));
+  dim3 grid((unsigned)((n + kBM - 1) / kBM), (unsigned)((c + kRCols - 1) / kRCols));
+  k_lift_resid_tc<<<grid, kThreads, smem, st>>>(t.mapA, t.mapX, K, r, rn, (int)n, (int)c, t.na, t.kbp, err);
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_resid_tc"));
+  k_lift_r16<<<(unsigned)((n * c + 255) / 256), 256, 0, st>>>(rn, n, c, ld, K, (__half*)R16);
+  count_launch(2);
+  return cuda_status(cudaGetLastError(), "k_lift_r16");
 }
 
 es_status tc_launch(const TcLift& t, const LiftConst* K, int8_t* V, int64_t n, int64_t c, int64_t ld, int E,

@@ -488,9 +488,8 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     });
     return fail ? ES_ERR_INTERNAL : ES_OK;
   };
-  const int64_t ns = nc < 4 ? nc : 4;
-  std::vector<int64_t> sk;
-  for (int64_t t = 0; t < ns; ++t) sk.push_back((t * nc) / ns);
+  const int64_t per_round = sample_count(c, hw_threads);
+  const std::vector<int64_t> sk = sample_components(n, c, per_round);
   std::vector<Nat> sden;
   ES_CHECK(denominators(sk, &sden));
   Nat d = big::from_u64(1);
@@ -511,9 +510,21 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   out->c = c;
   out->limbs = W;
   out->num.resize((size_t)(nc * W));
-  // a pageable buffer is filled before the device copy: the fill touches its
-  // fresh pages far faster than a copy into untouched pageable memory would
-  if (!out->num.pinned()) std::memset(out->num.data(), 0, out->num.size() * 8);
+  // A page-locked result buffer is written by the kernel directly.  A
+  // pageable one is filled before the device copy: the fill touches its fresh
+  // pages far faster than a copy into untouched pageable memory would.
+  uint64_t* Nout = reinterpret_cast<uint64_t*>(scratch + oN);
+  bool direct = false;
+  if (out->num.pinned()) {
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, out->num.data(), 0) == cudaSuccess) {
+      Nout = static_cast<uint64_t*>(dp);
+      direct = true;
+    } else {
+      cudaGetLastError();
+    }
+  }
+  if (!direct) std::memset(out->num.data(), 0, out->num.size() * 8);
   std::vector<uint8_t> okh((size_t)nc);
   const int64_t GS = g_stride(LG);
   std::vector<uint32_t> hG((size_t)mp * GS, 0u);
@@ -559,18 +570,20 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     rp.H12 = rp.MU + kMuWords;
     rp.nb = num_bits;
     rp.W = (int)W;
-    rp.N = reinterpret_cast<uint64_t*>(scratch + oN);
+    rp.N = Nout;
     rp.ok = reinterpret_cast<uint8_t*>(scratch + oK);
     k_recon_numerators<<<(unsigned)nc, 256, dyn, st>>>(rp);
     count_launch();
     ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_numerators"));
     ES_CHECK(cuda_status(cudaMemcpyAsync(okh.data(), rp.ok, (size_t)nc, cudaMemcpyDeviceToHost, st), "ok D2H"));
-    ES_CHECK(cuda_status(cudaMemcpyAsync(out->num.data(), rp.N, (size_t)nc * W * 8, cudaMemcpyDeviceToHost, st),
-                         "numerators D2H"));
+    if (!direct)
+      ES_CHECK(cuda_status(cudaMemcpyAsync(out->num.data(), rp.N, (size_t)nc * W * 8, cudaMemcpyDeviceToHost, st),
+                           "numerators D2H"));
     ES_CHECK(cuda_status(cudaStreamSynchronize(st), "recon sync"));
     std::vector<int64_t> failed;
-    for (int64_t k = 0; k < nc && failed.size() < 4; ++k)
+    for (int64_t k = 0; k < nc; ++k)
       if (!okh[(size_t)k]) failed.push_back(k);
+    failed = first_failure_per_column(failed, c, per_round);
     if (failed.empty()) break;
     const Nat before = d;
     std::vector<Nat> fden;

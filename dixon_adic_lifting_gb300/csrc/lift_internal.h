@@ -25,14 +25,31 @@ struct LiftConst {
 
 // tcgen05 lift product (k_lift_tc.cu), used for c >= 16.
 struct TcLift {
-  CUtensorMap mapB;  // f16 [53][n][ld] inverses
+  CUtensorMap mapB;  // int8 [53][n][ld] inverses
   CUtensorMap mapR;  // f16 [E'][c][ld] residues of r_i
   int nt = 64;       // MMA N tile
 };
 es_status tc_convert_f16(const int8_t* src, void* dst, int64_t count, void* stream);
-es_status tc_prepare(TcLift* t, const void* B16, const void* R16, int64_t n, int64_t c, int64_t ld, int E);
+es_status tc_prepare(TcLift* t, const int8_t* B, const void* R16, int64_t n, int64_t c, int64_t ld, int E);
 es_status tc_launch(const TcLift& t, const LiftConst* K, int8_t* V, int64_t n, int64_t c, int64_t ld, int E,
                     int* err, void* stream);
+
+// tcgen05 residual update (k_lift_tc.cu), used with the tcgen05 product when
+// max|A| < 2^31: A and x_i mod 2^64 in balanced 8-bit limbs, A x_i mod 2^64
+// as one f16 GEMM.
+constexpr int kResidLimbsMax = 4;      // limbs of A (|A| < 2^31)
+constexpr int64_t kResidTcMaxK = 65536;  // na n at most this: int32 sums stay exact
+struct TcResid {
+  CUtensorMap mapA;  // f16 [na][n][ld]      limbs of A, zero for k >= n
+  CUtensorMap mapX;  // f16 [na + 7][c][ld]  limbs of x_i mod 2^64 on planes na - 1 .. na + 6, the rest zero
+  int na = 0;        // limbs of A
+  int kbp = 0;       // 64-wide K blocks per limb plane
+};
+int resid_limbs(uint64_t max_abs_a);  // na for entries up to max_abs_a (0: not representable)
+es_status tc_resid_prepare(TcResid* t, const int64_t* A_dev, void* A16, void* X16, int64_t n, int64_t c, int64_t ld,
+                           int na, void* stream);
+es_status tc_resid_launch(const TcResid& t, const LiftConst* K, const int64_t* r, int64_t* rn, void* R16, int64_t n,
+                          int64_t c, int64_t ld, int* err, void* stream);
 
 constexpr int kFusedErrDigit = 15;  // error code: the fused lift's two digit paths disagreed
 

@@ -162,6 +162,27 @@ void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
   }
 }
 
+int64_t sample_count(int64_t c, int width) { return std::max<int64_t>(4, std::min<int64_t>(c, width)); }
+
+std::vector<int64_t> sample_components(int64_t n, int64_t c, int64_t count) {
+  const int64_t ns = std::min(n * c, count);
+  std::vector<int64_t> k((size_t)ns);
+  for (int64_t t = 0; t < ns; ++t) k[(size_t)t] = ((t * n) / ns) * c + (t * c) / ns;
+  return k;
+}
+
+std::vector<int64_t> first_failure_per_column(const std::vector<int64_t>& failed, int64_t c, int64_t count) {
+  std::vector<int64_t> out;
+  std::vector<uint8_t> taken((size_t)c, 0);
+  for (int64_t k : failed) {
+    if ((int64_t)out.size() >= count) break;
+    if (taken[(size_t)(k % c)]) continue;
+    taken[(size_t)(k % c)] = 1;
+    out.push_back(k);
+  }
+  return out;
+}
+
 es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,
                       int64_t num_bits, int64_t den_bits, int threads, bool inject_fault, Solution* out) {
   if (inject_fault) return ES_ERR_INTERNAL;
@@ -182,11 +203,14 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
   };
 
   // common denominator from a sample of components
-  const int64_t ns = nc < 4 ? nc : 4;
+  const int width = threads > 0 ? threads : std::max(1, (int)std::thread::hardware_concurrency());
+  const int64_t per_round = sample_count(c, width);
+  const std::vector<int64_t> sk = sample_components(n, c, per_round);
+  const int64_t ns = (int64_t)sk.size();
   std::vector<Nat> sden((size_t)ns);
   std::atomic<int> fail(0);
   parallel_for(ns, threads, [&](int64_t t) {
-    if (!component_denominator(M, residue((t * nc) / ns), num_bits, den_bits, &sden[(size_t)t])) fail = 1;
+    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t])) fail = 1;
   });
   if (fail) return ES_ERR_INTERNAL;
   Nat d = big::from_u64(1);
@@ -216,7 +240,7 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     });
     if (failed.empty()) break;
     std::sort(failed.begin(), failed.end());
-    if (failed.size() > 4) failed.resize(4);
+    failed = first_failure_per_column(failed, c, per_round);
     // Every failing component's denominator does not divide d, so the round's
     // lcm must grow d (a later one may already be covered by an earlier one).
     const Nat before = d;

@@ -53,6 +53,16 @@ bool component_denominator(const big::Nat& M, const big::Nat& u, int64_t num_bit
 // Two's complement little-endian limbs of +-mag into out[0..W).
 void to_limbs(const big::Nat& mag, bool neg, int64_t W, uint64_t* out);
 
+// Components whose denominators seed the common denominator.  Components of
+// one column usually share its least denominator while columns differ, so the
+// sample takes one component per column (rows spread out): `count` of them,
+// where count = max(4, min(c, width)) for `width` host threads.
+int64_t sample_count(int64_t c, int width);
+std::vector<int64_t> sample_components(int64_t n, int64_t c, int64_t count);
+// From the failed components in ascending order, the first of each column, at
+// most `count` of them.
+std::vector<int64_t> first_failure_per_column(const std::vector<int64_t>& failed, int64_t c, int64_t count);
+
 // fn(i) for i in [0, count) on up to `threads` host threads (<= 0: all
 // cores) of the process-wide pool (host_pool.cpp); returns when all are done.
 void host_parallel_for(int64_t count, int threads, const std::function<void(int64_t)>& fn);

@@ -252,7 +252,6 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
     set_last_error("injected fault: lift wait timed out");
     return ES_ERR_TIMEOUT;
   }
-  const bool a32 = stats.max_abs_a < (uint64_t(1) << 31);
   KernelTiming kt;
   kt.events = o.kernel_events;
   int32_t mp = 0;
@@ -260,7 +259,8 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   std::unique_ptr<ReconPlan, void (*)(ReconPlan*)> rplan(nullptr, recon_plan_free);
   {
     LiftRun lr;
-    ES_CHECK(run_lift_start(A, b, n, c, B, good, m, dev.digits, a32, ws + SL.work, st, &kt, !o.step_lift, &lr,
+    ES_CHECK(run_lift_start(A, b, n, c, B, good, m, dev.digits, stats.max_abs_a, ws + SL.work, st, &kt,
+                            !o.step_lift, &lr,
                             o.fault == ES_FAULT_LIFT_WAIT));
     // while the GPU lifts: the reconstruction's digit-independent constants
     es_status ps = ES_OK;
@@ -335,12 +335,14 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
 // ------------------------------------------------------------ limb blocks
 // Result limbs leave the device once per solve into a buffer the caller may
 // keep.  A fresh pageable buffer costs page faults (and a staged copy); the
-// blocks here are page-locked when a device is present and recycled: a
-// freed buffer's block waits in a short list for the next solve.  Blocks
-// above kPinMax bytes are plain allocations and are not kept.
+// blocks here are page-locked when a device is present, so the numerator
+// kernel can write them directly, and recycled: a freed buffer's block waits
+// in a short list for the next solve.  Blocks above kPinMax bytes are plain
+// allocations, and the list holds at most kKeep blocks and kKeepBytes bytes.
 namespace {
-constexpr size_t kPinMax = size_t(256) << 20;
-constexpr size_t kKeep = 4;  // blocks kept for reuse
+constexpr size_t kPinMax = size_t(8) << 30;
+constexpr size_t kKeep = 4;
+constexpr size_t kKeepBytes = size_t(8) << 30;
 struct Block {
   uint64_t* p;
   size_t cap;
@@ -348,6 +350,7 @@ struct Block {
 };
 std::mutex g_blk_mu;
 std::vector<Block> g_blocks;
+size_t g_kept_bytes = 0;
 
 Block block_new(size_t count) {
   Block b{nullptr, count, false};
@@ -385,6 +388,7 @@ void LimbBuffer::resize(size_t count) {
       if (g_blocks[i].cap >= count && (best == g_blocks.size() || g_blocks[i].cap < g_blocks[best].cap)) best = i;
     if (best < g_blocks.size()) {
       b = g_blocks[best];
+      g_kept_bytes -= b.cap * 8;
       g_blocks.erase(g_blocks.begin() + (std::ptrdiff_t)best);
     }
   }
@@ -404,8 +408,9 @@ void LimbBuffer::release() {
   pinned_ = false;
   if (b.cap * 8 <= kPinMax) {
     std::lock_guard<std::mutex> lk(g_blk_mu);
-    if (g_blocks.size() < kKeep) {
+    if (g_blocks.size() < kKeep && g_kept_bytes + b.cap * 8 <= kKeepBytes) {
       g_blocks.push_back(b);
+      g_kept_bytes += b.cap * 8;
       return;
     }
   }
@@ -569,8 +574,7 @@ es_status es_lift_device(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
   es::Stats stats;
   ES_CHECK(es::compute_stats(A_dev, b_dev, n, c, ws, st, &stats));
   if (!es::in_range(n, stats.max_abs_a)) return ES_ERR_RANGE;
-  const bool a32 = stats.max_abs_a < (uint64_t(1) << 31);
-  return es::run_lift(A_dev, b_dev, n, c, B_dev, good, m, digits_dev, a32, ws + soff, st);
+  return es::run_lift(A_dev, b_dev, n, c, B_dev, good, m, digits_dev, stats.max_abs_a, ws + soff, st);
 }
 
 }  // extern "C"

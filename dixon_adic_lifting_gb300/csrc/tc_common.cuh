@@ -140,8 +140,9 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D f16 tensor [planes][rows][ld] with boxes of 64 x box_rows x 1.
-inline es_status make_map(CUtensorMap* map, const void* base, int64_t ld, int64_t rows, int64_t planes, int box_rows) {
+// 3-D f16 tensor [planes][rows][ld] with boxes of 64 x box_rows x box_planes.
+inline es_status make_map(CUtensorMap* map, const void* base, int64_t ld, int64_t rows, int64_t planes, int box_rows,
+                          int box_planes = 1) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     set_last_error("cuTensorMapEncodeTiled unavailable");
@@ -149,7 +150,7 @@ inline es_status make_map(CUtensorMap* map, const void* base, int64_t ld, int64_
   }
   const cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)rows, (cuuint64_t)planes};
   const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(ld * rows * 2)};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -161,6 +162,31 @@ inline es_status make_map(CUtensorMap* map, const void* base, int64_t ld, int64_
   return ES_OK;
 }
 
+// 3-D uint8 tensor [planes][rows][ld] with boxes of 128 x box_rows x 1
+// (one 128-byte swizzled row per box row).
+inline es_status make_map_u8(CUtensorMap* map, const void* base, int64_t ld, int64_t rows, int64_t planes,
+                             int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    set_last_error("cuTensorMapEncodeTiled unavailable");
+    return ES_ERR_CUDA;
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)(ld * rows)};
+  const cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_last_error("cuTensorMapEncodeTiled (u8) failed: " + std::to_string((int)r));
+    return ES_ERR_CUDA;
+  }
+  return ES_OK;
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 }  // namespace tc
 }  // namespace es

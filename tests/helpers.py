@@ -61,8 +61,14 @@ def exact_matmul_cols(A, X):
     amax = int(np.abs(A).max()) if n else 0
     w = 16
     if amax.bit_length() + w + n.bit_length() > 52:
-        Ai = A.tolist()
-        return [[sum(int(a) * x for a, x in zip(row, col)) for row in Ai] for col in X]
+        if 17 + w + n.bit_length() > 52:
+            Ai = A.tolist()
+            return [[sum(int(a) * x for a, x in zip(row, col)) for row in Ai] for col in X]
+        # A = A0 + 2^16 A1 with 0 <= A0 < 2^16 (both exact in int64)
+        A0 = A & 0xFFFF
+        A1 = (A - A0) >> 16
+        P0, P1 = exact_matmul_cols(A0, X), exact_matmul_cols(A1, X)
+        return [[u + (v << 16) for u, v in zip(c0, c1)] for c0, c1 in zip(P0, P1)]
     Af = A.astype(np.float64)
     rows = [int(v) for v in A.sum(axis=1)]
     out = []

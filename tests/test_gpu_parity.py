@@ -190,6 +190,22 @@ def check_lift_by_residuals(A, b, digits, good, steps):
         r = nxt
 
 
+@pytest.mark.parametrize("n,c,bits", [(1024, 16, 7), (1030, 20, 15), (1024, 16, 23), (1100, 24, 31),
+                                      (130, 16, 23), (20, 16, 40)])
+def test_lift_many_columns_by_residuals(torch_cuda, n, c, bits):
+    """c >= 16: the tcgen05 product; from n = 1024 with the tcgen05 residual
+    update for one to four 8-bit limbs of A (bits 7, 15, 23, 31; c = 20 and
+    24 leave a partial 8-column tile, n = 1030 and 1100 a partial row tile and
+    K block), below it and for entries of 2^31 and more the CUDA-core update."""
+    A, b = inputs.uniform(n, c, -(1 << bits) + 1, 1 << bits, seed=n + c)
+    At, bt = dev(torch_cuda, A), dev(torch_cuda, b)
+    B, good = api.inverse_mod_device(At)
+    nb, db, m = api.plan_device(At, bt, good)
+    steps = min(m, 6)
+    D = api.lift_device(At, bt, B, good, steps)
+    check_lift_by_residuals(A, b, api.digits_to_ints(D), good, steps)
+
+
 @pytest.mark.parametrize("name,steps", [("n256_c1_24bit", None), ("n1024_c1_24bit", 6)])
 def test_lift_full_size_by_residuals(torch_cuda, name, steps):
     A, b = inputs.workload(name, seed=0)

@@ -85,6 +85,18 @@ def test_host_reconstruction_needs_a_second_round(lib):
     assert (s.N, s.d) == exact.solve(A, b) == ([[7]] * 7 + [[1]], 7)
 
 
+@pytest.mark.parametrize("threads", [1, 3])
+def test_host_reconstruction_failures_in_several_columns(lib, threads):
+    # the sample (one component per column, rows 0, 2, 4, 6) holds integers
+    # only; row 7 is 1/7 in columns 0 and 1 and an integer in column 2
+    A = [[7 if (i == j == 7) else (1 if i == j else 0) for j in range(8)] for i in range(8)]
+    b = [[1, 2, 7] for _ in range(8)]
+    digits, good, nb, db, m = model_digits(A, b)
+    s = api.reconstruct(digits_to_limbs(digits), 8, 3, m, good, nb, db, threads=threads)
+    assert (s.N, s.d) == exact.solve(A, b)
+    assert s.d == 7 and s.N[7] == [1, 2, 7]
+
+
 def test_host_reconstruction_large_numbers(lib):
     # numerators of ~1300 bits: exercises the Lehmer and Karatsuba paths
     A, b = inputs.uniform(44, 1, -(1 << 23), 1 << 23, seed=5)
