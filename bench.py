@@ -179,6 +179,15 @@ def traffic_for(kernel_file, kernel):
         return None
 
 
+class SolveFigures:
+    """The per-solve figures the bench line reports, without the result."""
+
+    def __init__(self, s):
+        for k in ("m", "primes_used", "launches", "phase_ms", "top_kernel", "top_launches", "top_ms",
+                  "top_bytes_per_launch"):
+            setattr(self, k, getattr(s, k))
+
+
 # ------------------------------------------------------------------ arms
 def run_reference(args, rank, world):
     """The oracle as the reference arm: each step a bounded sample of the same
@@ -245,12 +254,16 @@ def run_gb300(args, rank, local_rank, world):
     barrier()
     clocks.start()
     sols = []
+    s = None  # the warm-up's result goes before the first timed solve
     for k in range(args.steps):
         flush.zero_()
         ev[k][0].record(stream)
         s = api.solve_device(At, bt, stream=stream, timing=2, one_stream=args.one_stream)
         ev[k][1].record(stream)
-        sols.append(s)
+        # keep the step's figures, not its result: a caller that drops each
+        # result lets the next solve reuse its page-locked block
+        sols.append(SolveFigures(s))
+        s = None
     barrier()
     clk = clocks.stop()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]

@@ -66,11 +66,23 @@ __device__ __forceinline__ void drain_loads(uint64_t* full, int issued, int dept
     mbar_wait_drain(full + kb % depth, (kb / depth) & 1);
 }
 
+// Persistent: one CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ...
+// (tile t = (row tile, column tile, prime), row tile fastest); the copy ring,
+// the f16 slots and the two TMEM buffers run on across tiles, so a CTA's set-up
+// and its pipeline fill are paid once rather than per tile.
+struct ProdTile {
+  int m0, n0, e;
+};
+__device__ __forceinline__ ProdTile prod_tile(int t, int tiles_m, int tiles_n, int nt) {
+  const int mt = t % tiles_m, rest = t / tiles_m;
+  return ProdTile{mt * kBM, (rest % tiles_n) * nt, rest / tiles_n};
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kPThreads, 1)
     k_lift_gemm_tc(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmR,
-                   const LiftConst* __restrict__ K, int8_t* __restrict__ V, int n, int c, int kstages,
-                   int* __restrict__ err) {
+                   const LiftConst* __restrict__ K, int8_t* __restrict__ V, int n, int c, int kstages, int tiles_m,
+                   int tiles_n, int ntiles, int* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sI = smem;                               // [S] 128 x 128 int8
@@ -84,8 +96,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* drained = accempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.z, j = K->pidx[e];
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * NT;
   const int nchunks = (kstages + kPFoldStages - 1) / kPFoldStages;
   constexpr uint32_t kCols = 2 * NT < 32 ? 32 : 2 * NT;
 
@@ -114,59 +124,84 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
-      int issued = 0;
-      for (int st = 0; st < kstages; ++st) {
-        const int s = st % kPStages;
-        if (st >= kPStages && !mbar_wait(empty + s, ((st / kPStages) & 1) ^ 1, err, 1)) break;
-        mbar_expect_tx(full + s, kPTileI8 + 2 * NT * 128);
-        tma_load_3d(sI + s * kPTileI8, &tmB, full + s, st * kPK, m0, j);
-        tma_load_3d(sR + (2 * s) * NT * 128, &tmR, full + s, st * kPK, n0, e);
-        tma_load_3d(sR + (2 * s + 1) * NT * 128, &tmR, full + s, st * kPK + kBK, n0, e);
-        issued = st + 1;
+      int g = 0;      // stages issued by this CTA
+      bool stop = false;
+      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+        const ProdTile T = prod_tile(t, tiles_m, tiles_n, NT);
+        const int j = K->pidx[T.e];
+        for (int st = 0; st < kstages; ++st, ++g) {
+          const int s = g % kPStages;
+          if (g >= kPStages && !mbar_wait(empty + s, ((g / kPStages) & 1) ^ 1, err, 1)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(full + s, kPTileI8 + 2 * NT * 128);
+          tma_load_3d(sI + s * kPTileI8, &tmB, full + s, st * kPK, T.m0, j);
+          tma_load_3d(sR + (2 * s) * NT * 128, &tmR, full + s, st * kPK, T.n0, T.e);
+          tma_load_3d(sR + (2 * s + 1) * NT * 128, &tmR, full + s, st * kPK + kBK, T.n0, T.e);
+        }
       }
-      drain_loads(full, issued, kPStages);
+      drain_loads(full, g, kPStages);
     }
   } else if (warp >= 6) {  // converters: thread r owns row r
     const int r = threadIdx.x - 192, sw = r & 7;
-    for (int st = 0; st < kstages; ++st) {
-      const int s = st % kPStages;
-      if (!mbar_wait(full + s, (st / kPStages) & 1, err, 5)) break;
-      const uint8_t* src = sI + s * kPTileI8 + r * 128;
+    int g = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+      for (int st = 0; st < kstages; ++st, ++g) {
+        const int s = g % kPStages;
+        if (!mbar_wait(full + s, (g / kPStages) & 1, err, 5)) {
+          stop = true;
+          break;
+        }
+        const uint8_t* src = sI + s * kPTileI8 + r * 128;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {  // 16-byte chunk q of the int8 row: k = 16 q .. 16 q + 15
-        const uint4 w = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
-        uint4 a, b;
-        s8x4_to_f16(w.x, a.x, a.y);
-        s8x4_to_f16(w.y, a.z, a.w);
-        s8x4_to_f16(w.z, b.x, b.y);
-        s8x4_to_f16(w.w, b.z, b.w);
-        // f16 tile q / 4, its chunks 2 (q % 4) and 2 (q % 4) + 1
-        uint8_t* dst = sF + (2 * s + (q >> 2)) * kATileBytes + r * 128;
-        const int c0 = 2 * (q & 3);
-        *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) = a;
-        *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ sw) << 4)) = b;
+        for (int q = 0; q < 8; ++q) {  // 16-byte chunk q of the int8 row: k = 16 q .. 16 q + 15
+          const uint4 w = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
+          uint4 a, b;
+          s8x4_to_f16(w.x, a.x, a.y);
+          s8x4_to_f16(w.y, a.z, a.w);
+          s8x4_to_f16(w.z, b.x, b.y);
+          s8x4_to_f16(w.w, b.z, b.w);
+          // f16 tile q / 4, its chunks 2 (q % 4) and 2 (q % 4) + 1
+          uint8_t* dst = sF + (2 * s + (q >> 2)) * kATileBytes + r * 128;
+          const int c0 = 2 * (q & 3);
+          *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) = a;
+          *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ sw) << 4)) = b;
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes, before the tensor core reads them
+        mbar_arrive(conv + s);
       }
-      fence_proxy_async_smem();  // the generic-proxy writes, before the tensor core reads them
-      mbar_arrive(conv + s);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-      for (int st = 0; st < kstages; ++st) {
-        const int s = st % kPStages, ch = st / kPFoldStages, buf = ch & 1;
-        const bool first = (st % kPFoldStages) == 0;
-        if (first && ch >= 2 && !mbar_wait(accempty + buf, ((ch - 2) >> 1) & 1, err, 2)) break;
-        if (!mbar_wait(conv + s, (st / kPStages) & 1, err, 3)) break;
-        tc_fence_after();
+      int g = 0, gc0 = 0;  // stages and accumulator chunks of earlier tiles
+      bool stop = false;
+      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x, gc0 += nchunks) {
+        for (int st = 0; st < kstages; ++st, ++g) {
+          const int s = g % kPStages, gc = gc0 + st / kPFoldStages, buf = gc & 1;
+          const bool first = (st % kPFoldStages) == 0;
+          if (first && gc >= 2 && !mbar_wait(accempty + buf, ((gc - 2) >> 1) & 1, err, 2)) {
+            stop = true;
+            break;
+          }
+          if (!mbar_wait(conv + s, (g / kPStages) & 1, err, 3)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint64_t ad = desc_sw128(sF + (2 * s + h) * kATileBytes), bd = desc_sw128(sR + (2 * s + h) * NT * 128);
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t ad = desc_sw128(sF + (2 * s + h) * kATileBytes),
+                           bd = desc_sw128(sR + (2 * s + h) * NT * 128);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_f16(tmem + buf * NT, ad + 2 * k, bd + 2 * k, idesc, (first && h == 0 && k == 0) ? 0u : 1u);
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_f16(tmem + buf * NT, ad + 2 * k, bd + 2 * k, idesc, (first && h == 0 && k == 0) ? 0u : 1u);
+          }
+          mma_commit(empty + s);
+          if ((st % kPFoldStages) == kPFoldStages - 1 || st == kstages - 1) mma_commit(accfull + buf);
         }
-        mma_commit(empty + s);
-        if ((st % kPFoldStages) == kPFoldStages - 1 || st == kstages - 1) mma_commit(accfull + buf);
       }
       // every MMA issued has completed before tensor memory is released
       mma_commit(drained);
@@ -174,34 +209,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   } else {  // epilogue warpgroup (warps 2..5)
     const int quarter = warp & 3;
-    const int row = m0 + 32 * quarter + lane;
-    const ModQ m = K->mq[e];
-    int32_t acc[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0;
+    int gc0 = 0;
     bool ok = true;
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const int buf = ch & 1;
-      if (!mbar_wait(accfull + buf, (ch >> 1) & 1, err, 4)) {
-        ok = false;
-        break;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, gc0 += nchunks) {
+      const ProdTile T = prod_tile(t, tiles_m, tiles_n, NT);
+      const int row = T.m0 + 32 * quarter + lane;
+      int32_t acc[NT];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) acc[i] = 0;
+      for (int ch = 0; ch < nchunks; ++ch) {
+        const int gc = gc0 + ch, buf = gc & 1;
+        if (!mbar_wait(accfull + buf, (gc >> 1) & 1, err, 4)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c16 = 0; c16 < NT / 16; ++c16) {
+          float f[16];
+          tmem_ld<16>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * NT + 16 * c16), f);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[16 * c16 + i] += __float2int_rn(f[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(accempty + buf);
       }
-      tc_fence_after();
+      if (ok && row < n) {
+        const ModQ m = K->mq[T.e];
+        int8_t* out = V + ((int64_t)T.e * n + row) * c;
 #pragma unroll
-      for (int c16 = 0; c16 < NT / 16; ++c16) {
-        float f[16];
-        tmem_ld<16>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * NT + 16 * c16), f);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) acc[16 * c16 + t] += __float2int_rn(f[t]);
+        for (int i = 0; i < NT; ++i)
+          if (T.n0 + i < c) out[T.n0 + i] = (int8_t)reduce_bal(acc[i], m);
       }
-      tc_fence_before();
-      mbar_arrive(accempty + buf);
-    }
-    if (ok && row < n) {
-      int8_t* out = V + ((int64_t)e * n + row) * c;
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        if (n0 + t < c) out[n0 + t] = (int8_t)reduce_bal(acc[t], m);
     }
   }
   tc_fence_before();
@@ -393,6 +432,19 @@ __global__ void k_to_f16(const int8_t* __restrict__ src, __half* __restrict__ ds
   }
 }
 
+int sm_count() {
+  static int count = 0;
+  if (!count) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      count = v;
+    else
+      return 1;
+  }
+  return count;
+}
+
 template <int NT>
 es_status launch_nt(const CUtensorMap& mB, const CUtensorMap& mR, const LiftConst* K, int8_t* V, int64_t n,
                     int64_t c, int64_t ld, int E, int* err, cudaStream_t st) {
@@ -401,9 +453,12 @@ es_status launch_nt(const CUtensorMap& mB, const CUtensorMap& mR, const LiftCons
   ES_CHECK(cuda_status(cudaFuncSetAttribute(k_lift_gemm_tc<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)smem),
                        "tc smem attribute"));
-  dim3 grid((unsigned)((n + kBM - 1) / kBM), (unsigned)((c + NT - 1) / NT), (unsigned)E);
+  const int tiles_m = (int)((n + kBM - 1) / kBM), tiles_n = (int)((c + NT - 1) / NT);
+  const int ntiles = tiles_m * tiles_n * E;
   const int kstages = (int)((ld + kPK - 1) / kPK);
-  k_lift_gemm_tc<NT><<<grid, kPThreads, smem, st>>>(mB, mR, K, V, (int)n, (int)c, kstages, err);
+  const int grid = ntiles < sm_count() ? ntiles : sm_count();
+  k_lift_gemm_tc<NT><<<grid, kPThreads, smem, st>>>(mB, mR, K, V, (int)n, (int)c, kstages, tiles_m, tiles_n, ntiles,
+                                                    err);
   return cuda_status(cudaGetLastError(), "k_lift_gemm_tc");
 }
 

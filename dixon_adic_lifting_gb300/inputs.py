@@ -91,7 +91,8 @@ class Workload:
 
 # The systems the solver is measured and checked on: the five test
 # configurations, the rest of the card's §Measured grid (24-bit entries),
-# and one each of its planted and scaled-Hilbert systems (§Correctness).
+# one each of its planted and scaled-Hilbert systems (§Correctness), and a
+# half-size n = 4096, c = 64 system (a profiling case of a few GB).
 _U24 = "A, b uniform in [-2^23, 2^23)"
 WORKLOADS = {
     "n32_c1_int8": Workload("n32_c1_int8", 32, 1,
@@ -104,6 +105,7 @@ WORKLOADS = {
     "n1024_c1_24bit": Workload("n1024_c1_24bit", 1024, 1, _U24),
     "n256_c16_24bit": Workload("n256_c16_24bit", 256, 16, _U24),
     "n512_c16_24bit": Workload("n512_c16_24bit", 512, 16, _U24),
+    "n2048_c64_16bit": Workload("n2048_c64_16bit", 2048, 64, "A, b uniform in [-2^15, 2^15)"),
     "n4096_c64_16bit": Workload("n4096_c64_16bit", 4096, 64, "A, b uniform in [-2^15, 2^15)"),
     "hilbert21": Workload("hilbert21", 21, 1,
                           "scaled Hilbert A_ij = lcm(1..41) / (i + j + 1); b uniform in [-2^23, 2^23)"),
@@ -119,8 +121,9 @@ def workload(name: str, seed: int = 0, attempt: int = 0):
         return uniform(32, 1, -127, 128, seed, attempt)
     if name == "pascal30":
         return pascal_system(30, 1, seed)
-    if name == "n4096_c64_16bit":
-        return uniform(4096, 64, -(1 << 15), 1 << 15, seed)
+    if name in ("n2048_c64_16bit", "n4096_c64_16bit"):
+        w = WORKLOADS[name]
+        return uniform(w.n, w.c, -(1 << 15), 1 << 15, seed)
     if name == "hilbert21":
         g = _rng(seed, 21)
         return scaled_hilbert(21), g.integers(-(1 << 23), 1 << 23, size=(21, 1), dtype=np.int64)
