@@ -9,16 +9,17 @@
 // accumulator is folded into int32 registers every 512 K (|partial| <= 512 *
 // 125^2 < 2^23) and then restarted, so the product is exact for any n <= 2^17.
 // B_j stays int8 in HBM (the product is bound by reading it once per step):
-// TMA brings 128 x 128 int8 tiles into shared memory and four converter warps
+// TMA brings 128 x 128 int8 tiles into shared memory and eight converter warps
 // widen them into the f16 operand tiles the MMA reads.
 //
 // CTA = one prime e, 128 rows of B_j (MMA M = 128) and NT columns (N = NT):
 //   warp 0      one thread: TMA producer, 3-stage ring; a stage is K = 128:
 //               the int8 tile of B_j and two NT x 64 f16 tiles of R_e
 //               (128-byte swizzled, K-major)
-//   warps 6..9  converters: thread r widens row r of the int8 tile into the
-//               stage's two 128 x 64 f16 tiles (same swizzle), then a
-//               proxy fence and an arrive on the stage's `conv` barrier
+//   warps 6..13 converters: thread u widens half u / 128 of row u % 128 of
+//               the int8 tile into one of the stage's two 128 x 64 f16 tiles
+//               (same swizzle), then a proxy fence and an arrive on the
+//               stage's `conv` barrier
 //   warp 1      one thread: 8 MMAs (K = 16 each) per stage; a commit frees
 //               the stage and, at 512-K chunk ends, publishes the accumulator
 //   warps 2..5  epilogue: fold each finished chunk from TMEM (tcgen05.ld,
@@ -51,7 +52,7 @@ constexpr int kPStages = 3;
 constexpr int kPK = 128;                    // K per stage: one 128-byte int8 row
 constexpr int kPTileI8 = kBM * kPK;         // 16 KB
 constexpr int kPFoldStages = 4;             // fold every 4 stages (K = 512)
-constexpr int kPThreads = 320;
+constexpr int kPThreads = 448;             // producer, MMA, 4 epilogue and 8 converter warps
 
 // residual kernel
 constexpr int kStages = 4;
@@ -102,7 +103,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPStages; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(conv + s, 128);
+      mbar_init(conv + s, 256);
       mbar_init(empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -143,8 +144,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       drain_loads(full, g, kPStages);
     }
-  } else if (warp >= 6) {  // converters: thread r owns row r
-    const int r = threadIdx.x - 192, sw = r & 7;
+  } else if (warp >= 6) {  // converters: thread u widens half u / 128 (one f16 tile) of row u % 128
+    const int u = threadIdx.x - 192, r = u & 127, hq = 4 * (u >> 7), sw = r & 7;
     int g = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         const uint8_t* src = sI + s * kPTileI8 + r * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // 16-byte chunk q of the int8 row: k = 16 q .. 16 q + 15
+        for (int q = hq; q < hq + 4; ++q) {  // 16-byte chunk q of the int8 row: k = 16 q .. 16 q + 15
           const uint4 w = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
           uint4 a, b;
           s8x4_to_f16(w.x, a.x, a.y);
@@ -236,10 +237,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (ok && row < n) {
         const ModQ m = K->mq[T.e];
-        int8_t* out = V + ((int64_t)T.e * n + row) * c;
+        int8_t* out = V + ((int64_t)T.e * n + row) * c + T.n0;
+        if (c % 16 == 0 && T.n0 + NT <= c) {
+          // the row's NT bytes are contiguous and 16-byte aligned: 16-byte stores
+          // (byte stores here would hold up the converter warps' shared-memory traffic)
 #pragma unroll
-        for (int i = 0; i < NT; ++i)
-          if (T.n0 + i < c) out[T.n0 + i] = (int8_t)reduce_bal(acc[i], m);
+          for (int i = 0; i < NT; i += 16) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              w[q] = (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q], m) |
+                     (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q + 1], m) << 8 |
+                     (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q + 2], m) << 16 |
+                     (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q + 3], m) << 24;
+            *reinterpret_cast<uint4*>(out + i) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < NT; ++i)
+            if (T.n0 + i < c) out[i] = (int8_t)reduce_bal(acc[i], m);
+        }
       }
     }
   }
