@@ -261,12 +261,26 @@ struct XLimbs {
 };
 
 // Same digit, one thread per entry (for many entries: no cross-lane work).
+// The per-prime constants are staged in shared memory once per CTA, so the
+// inner loop reads P'/q_e as three 16-byte broadcasts instead of twelve
+// global loads.
 __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restrict__ V, int64_t nc,
                                                          const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
                                                          uint64_t* __restrict__ xl, XLimbs xo) {
+  __shared__ __align__(16) uint32_t sMq[kNumPrimes * kCrtWords];
+  __shared__ uint64_t sTf[kNumPrimes];
+  __shared__ uint32_t sW[kNumPrimes], sQ[kNumPrimes], sMu[kNumPrimes];
+  const int E = K->E;
+  for (int i = threadIdx.x; i < E * kCrtWords; i += blockDim.x) sMq[i] = K->Mq[i / kCrtWords][i % kCrtWords];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    sTf[e] = K->tfix[e];
+    sW[e] = K->w[e];
+    sQ[e] = K->mq[e].q;
+    sMu[e] = K->mq[e].mu;
+  }
+  __syncthreads();
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= nc) return;
-  const int E = K->E;
   uint64_t acc[kCrtWords];
 #pragma unroll
   for (int l = 0; l < kCrtWords; ++l) acc[l] = 0;
@@ -282,12 +296,21 @@ __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restric
     for (int u = 0; u < 8; ++u) {
       const int e = e0 + u;
       if (e >= E) break;
-      const ModQ m = K->mq[e];
+      ModQ m{};
+      m.q = sQ[e];
+      m.mu = sMu[e];
       const int32_t v = vv[u];
-      const uint32_t ce = barrett((uint32_t)(v < 0 ? v + (int32_t)m.q : v) * K->w[e], m);
-      tf += (uint64_t)ce * K->tfix[e];
+      const uint32_t ce = barrett((uint32_t)(v < 0 ? v + (int32_t)m.q : v) * sW[e], m);
+      tf += (uint64_t)ce * sTf[e];
+      const uint4* mq4 = reinterpret_cast<const uint4*>(sMq + e * kCrtWords);
 #pragma unroll
-      for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];
+      for (int h = 0; h < kCrtWords / 4; ++h) {
+        const uint4 w = mq4[h];
+        acc[4 * h] += (uint64_t)ce * w.x;
+        acc[4 * h + 1] += (uint64_t)ce * w.y;
+        acc[4 * h + 2] += (uint64_t)ce * w.z;
+        acc[4 * h + 3] += (uint64_t)ce * w.w;
+      }
     }
   }
   uint32_t S[kCrtWords];
