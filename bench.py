@@ -72,6 +72,17 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x (each replica's time; the job ends with the slowest)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ clocks
 class Clocks:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -267,11 +278,7 @@ def run_gb300(args, rank, local_rank, world):
     barrier()
     clk = clocks.stop()
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dist, "cuda")
     s0 = sols[-1]
     top_launches = sum(s.top_launches for s in sols)
     top_ms = sum(s.top_ms for s in sols)
@@ -299,11 +306,7 @@ def run_gb300(args, rank, local_rank, world):
             t0 = time.perf_counter()
             s = api.solve_canonical(An, bn)
             times.append((time.perf_counter() - t0) * 1e3)
-        e2e_ms = sum(times) / len(times)
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(sum(times) / len(times), dist, "cuda")
         # device->host: sampled components' digits (4 x m x 48 B), the numerators
         # (n c limbs x 8 B), the acceptance flags (n c B) and the good-prime flags
         e2e = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(8 * (n * n + n * c)),
