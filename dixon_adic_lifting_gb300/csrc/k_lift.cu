@@ -421,12 +421,12 @@ __global__ void __launch_bounds__(128) k_lift_resid_gemv(const AT* __restrict__ 
 }
 
 // general c: r'[i][col] = (r[i][col] - sum_k A[i][k] x[k][col]) Pinv mod 2^64
-// and its residues.  CTA tile 16 rows x 16 columns.  Its 256 threads are 16
-// thread tiles of 4 x 4 outputs times 16 slices of K (slice s takes the
-// groups k = 4s + 64t .. 4s + 64t + 3); the slices' partial sums meet in
-// shared memory, one thread per output adds them, and all threads then share
-// the E residues of the tile's 256 new residual entries (four rows, one
-// 32-bit store, per task).
+// and its residues.  CTA tile TR rows (16, or 8 for small grids) x 16
+// columns.  Its 256 threads are TR thread tiles of 4 x 4 outputs times
+// 256 / TR slices of K (slice s takes the groups k = 4s + 4 S t .. 4s + 4 S t + 3
+// for S slices); the slices' partial sums meet in shared memory, one thread per
+// output adds them, and all threads then share the E residues of the tile's
+// 16 TR new residual entries (four rows, one 32-bit store, per task).
 // For int32 A the product uses x = x_lo + 2^32 x_hi with x_lo read as a
 // signed int32 and its borrow folded into the high word (x_hi' = x_hi +
 // (x_lo >> 31)):
@@ -436,7 +436,8 @@ __global__ void __launch_bounds__(128) k_lift_resid_gemv(const AT* __restrict__ 
 // x is zero for k >= n, so whole groups of four run to lda.  For int64 A
 // (entries of 2^31 or more, lda = n) the terms are full 64-bit products and
 // the groups stop at n.
-constexpr int kResidTile = 16;
+constexpr int kResidTile = 16;           // columns per CTA of the tiled residual update
+constexpr int64_t kResidSmallGrid = 152;  // below 2 x this many 16-row CTAs: 8-row tiles
 
 template <typename AT, bool VecX>
 __device__ __forceinline__ void resid_group(const AT* __restrict__ A, int64_t lda, const uint64_t* __restrict__ xl,
@@ -532,18 +533,22 @@ __device__ __forceinline__ void resid_group<int64_t, false>(const int64_t* __res
   }
 }
 
-template <typename AT, bool VecX>
+template <typename AT, bool VecX, int TR>
 __global__ void __launch_bounds__(256) k_lift_resid_tile(const AT* __restrict__ A, int64_t lda,
                                                          const uint64_t* __restrict__ xl,
                                                          const int64_t* __restrict__ r, int64_t n, int64_t c,
                                                          int64_t ld, const LiftConst* __restrict__ K,
                                                          int64_t* __restrict__ rn, int8_t* __restrict__ R) {
-  constexpr int T = kResidTile;
-  __shared__ uint64_t part[16][T * T];
-  __shared__ int64_t vs[T][T + 1];  // [column][row]
-  const int tid = threadIdx.x, sub = tid & 15, s = tid >> 4;
+  constexpr int T = kResidTile;      // columns per CTA
+  constexpr int G4 = TR / 4;         // groups of four rows
+  constexpr int SUBS = G4 * 4;       // 4 x 4 thread tiles
+  constexpr int SL = 256 / SUBS;     // K slices
+  static_assert(TR == 8 || TR == 16, "row tile");
+  __shared__ uint64_t part[SL][TR * T];
+  __shared__ int64_t vs[T][TR + 1];  // [column][row]
+  const int tid = threadIdx.x, sub = tid % SUBS, s = tid / SUBS;
   const int rg = sub >> 2, cg = sub & 3;
-  const int64_t row0 = (int64_t)blockIdx.x * T, col0 = (int64_t)blockIdx.y * T;
+  const int64_t row0 = (int64_t)blockIdx.x * TR, col0 = (int64_t)blockIdx.y * T;
   const int64_t col = col0 + 4 * cg;
   int64_t arow[4];
 #pragma unroll
@@ -561,19 +566,19 @@ __global__ void __launch_bounds__(256) k_lift_resid_tile(const AT* __restrict__ 
       hi[q][u] = 0;
     }
   const int64_t kend = sizeof(AT) == 4 ? lda : n;
-  for (int64_t k = 4 * s; k < kend; k += 64) resid_group<AT, VecX>(A, lda, xl, n, c, arow, col, k, acc, hi);
+  for (int64_t k = 4 * s; k < kend; k += 4 * SL) resid_group<AT, VecX>(A, lda, xl, n, c, arow, col, k, acc, hi);
 #pragma unroll
   for (int q = 0; q < 4; ++q)
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       part[s][(4 * rg + q) * T + 4 * cg + u] = acc[q][u] + ((uint64_t)hi[q][u] << 32);
   __syncthreads();
-  {
-    const int rl = tid >> 4, cl = tid & 15;
+  if (tid < TR * T) {
+    const int rl = tid / T, cl = tid % T;
     const int64_t i = row0 + rl, cc = col0 + cl;
     uint64_t sum = 0;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) sum += part[t][tid];
+    for (int t = 0; t < SL; ++t) sum += part[t][tid];
     int64_t v = 0;
     if (i < n && cc < c) {
       v = (int64_t)(((uint64_t)r[i * c + cc] - sum) * K->Pinv64);
@@ -583,8 +588,8 @@ __global__ void __launch_bounds__(256) k_lift_resid_tile(const AT* __restrict__ 
   }
   __syncthreads();
   const int E = K->E;
-  for (int t = tid; t < E * T * 4; t += 256) {
-    const int e = t / (T * 4), cl = (t >> 2) & (T - 1), g = t & 3;
+  for (int t = tid; t < E * T * G4; t += 256) {
+    const int e = t / (T * G4), cl = (t / G4) % T, g = t % G4;
     const int64_t cc = col0 + cl;
     if (cc >= c) continue;
     const ModQ m = K->mq[e];
@@ -770,13 +775,27 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
         else
           k_lift_resid_gemv<int64_t><<<(unsigned)((n + 3) / 4), 128, 0, st>>>(A_dev, n, xl, rc, n, ld, K, rn, R);
       } else {
-        const dim3 g((unsigned)((n + kResidTile - 1) / kResidTile), (unsigned)((c + kResidTile - 1) / kResidTile));
-        if (a32 && c % 4 == 0)
-          k_lift_resid_tile<int32_t, true><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
-        else if (a32)
-          k_lift_resid_tile<int32_t, false><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
-        else
-          k_lift_resid_tile<int64_t, false><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
+        // 16-row tiles, or 8-row ones (twice the CTAs, K in 32 slices) while
+        // there would be fewer than two per SM
+        const unsigned gy = (unsigned)((c + kResidTile - 1) / kResidTile);
+        const bool small = ((n + 15) / 16) * (int64_t)gy < 2 * kResidSmallGrid;
+        const dim3 g((unsigned)((n + (small ? 7 : 15)) / (small ? 8 : 16)), gy);
+        if (a32 && c % 4 == 0) {
+          if (small)
+            k_lift_resid_tile<int32_t, true, 8><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+          else
+            k_lift_resid_tile<int32_t, true, 16><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+        } else if (a32) {
+          if (small)
+            k_lift_resid_tile<int32_t, false, 8><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+          else
+            k_lift_resid_tile<int32_t, false, 16><<<g, 256, 0, st>>>(A32, ld, xl, rc, n, c, ld, K, rn, R);
+        } else {
+          if (small)
+            k_lift_resid_tile<int64_t, false, 8><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
+          else
+            k_lift_resid_tile<int64_t, false, 16><<<g, 256, 0, st>>>(A_dev, n, xl, rc, n, c, ld, K, rn, R);
+        }
       }
     }
   }
