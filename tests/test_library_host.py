@@ -165,3 +165,23 @@ def test_named_workloads_match_their_descriptions():
     _, _, X = inputs.planted(256, 1, seed=0)
     assert [[int(v)] for v in (A.astype(object) @ X.astype(object)).ravel()] == b.tolist()
     assert inputs.workload("hilbert21")[0].tolist() == inputs.scaled_hilbert(21).tolist()
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_host_reconstruction_random_many_columns(lib, seed):
+    """Small random systems with more columns than rows or samples: the
+    column-spread sample and the per-column retry rounds still give the
+    oracle's canonical (N, d)."""
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.integers(2, 7))
+    c = int(rng.integers(n + 1, 3 * n + 3))
+    A = rng.integers(-9, 10, size=(n, n))
+    while exact.solve(A.tolist(), [[1]] * n) is None:
+        A = rng.integers(-9, 10, size=(n, n))
+    b = rng.integers(-20, 21, size=(n, c))
+    b[:, 0] = 0  # an all-zero column: numerators 0
+    A, b = A.tolist(), b.tolist()
+    digits, good, nb, db, m = model_digits(A, b)
+    for threads in (1, 4):
+        s = api.reconstruct(digits_to_limbs(digits), n, c, m, good, nb, db, threads=threads)
+        assert (s.N, s.d) == exact.solve(A, b)
