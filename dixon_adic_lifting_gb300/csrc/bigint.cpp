@@ -122,32 +122,42 @@ static void sub_into(limb* r, size_t rn, const limb* a, size_t an) {  // r -= a 
 
 constexpr size_t kKaraThreshold = 40;
 
-// r[0 .. 2n) = a[0..n) * b[0..n)
-static void kara(limb* r, const limb* a, const limb* b, size_t n) {
+// scratch limbs kara() needs for size n
+static size_t kara_scratch(size_t n) {
+  size_t total = 0;
+  while (n >= kKaraThreshold) {
+    const size_t hh = n - n / 2;
+    total += 4 * (hh + 1);
+    n = hh + 1;
+  }
+  return total;
+}
+
+// r[0 .. 2n) = a[0..n) * b[0..n); ws holds kara_scratch(n) limbs.  The two
+// half products go straight into r; the middle one and the half sums use ws.
+static void kara(limb* r, const limb* a, const limb* b, size_t n, limb* ws) {
   if (n < kKaraThreshold) {
     std::fill(r, r + 2 * n, 0);
     mul_school(r, a, n, b, n);
     return;
   }
-  size_t h = n / 2, hh = n - h;
-  std::fill(r, r + 2 * n, 0);
-  std::vector<limb> z0(2 * h), z2(2 * hh);
-  kara(z0.data(), a, b, h);
-  kara(z2.data(), a + h, b + h, hh);
-  std::vector<limb> sa(hh + 1, 0), sb(hh + 1, 0);
-  std::copy(a + h, a + n, sa.begin());
-  std::copy(b + h, b + n, sb.begin());
-  sa[hh] = add_into(sa.data(), hh, a, h);
-  sb[hh] = add_into(sb.data(), hh, b, h);
-  std::vector<limb> z1(2 * (hh + 1));
-  kara(z1.data(), sa.data(), sb.data(), hh + 1);
-  sub_into(z1.data(), z1.size(), z0.data(), z0.size());
-  sub_into(z1.data(), z1.size(), z2.data(), z2.size());
-  std::copy(z0.begin(), z0.end(), r);
-  std::copy(z2.begin(), z2.end(), r + 2 * h);
-  size_t z1n = z1.size();
+  const size_t h = n / 2, hh = n - h;
+  kara(r, a, b, h, ws);
+  kara(r + 2 * h, a + h, b + h, hh, ws);
+  limb* sa = ws;
+  limb* sb = sa + (hh + 1);
+  limb* z1 = sb + (hh + 1);
+  limb* next = z1 + 2 * (hh + 1);
+  std::copy(a + h, a + n, sa);
+  std::copy(b + h, b + n, sb);
+  sa[hh] = add_into(sa, hh, a, h);
+  sb[hh] = add_into(sb, hh, b, h);
+  kara(z1, sa, sb, hh + 1, next);
+  sub_into(z1, 2 * (hh + 1), r, 2 * h);
+  sub_into(z1, 2 * (hh + 1), r + 2 * h, 2 * hh);
+  size_t z1n = 2 * (hh + 1);
   while (z1n && z1[z1n - 1] == 0) --z1n;
-  add_into(r + h, 2 * n - h, z1.data(), z1n);
+  add_into(r + h, 2 * n - h, z1, z1n);
 }
 
 Nat mul(const Nat& a, const Nat& b) {
@@ -159,11 +169,11 @@ Nat mul(const Nat& a, const Nat& b) {
   if (n < kKaraThreshold) {
     mul_school(r.data(), x.data(), n, y.data(), m);
   } else {
-    std::vector<limb> t(2 * n);
+    std::vector<limb> t(2 * n), ws(kara_scratch(n));
     for (size_t off = 0; off < m; off += n) {
       size_t len = std::min(n, m - off);
       if (len == n) {
-        kara(t.data(), x.data(), y.data() + off, n);
+        kara(t.data(), x.data(), y.data() + off, n, ws.data());
         add_into(r.data() + off, n + m - off, t.data(), 2 * n);
       } else {
         Nat part(y.begin() + off, y.begin() + off + len), xx = x;
