@@ -61,6 +61,7 @@ _SIGS = {
     "es_reconstruct": (c_i32, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i64, c_i64, ctypes.POINTER(es_options),
                                ctypes.POINTER(c_vp)]),
     "es_selftest_modular": (c_i64, [c_i64, c_i64, c_i64]),
+    "es_selftest_bigint": (c_i64, [ctypes.c_uint64, c_i64]),
 }
 
 _lib = None

@@ -281,6 +281,11 @@ def reconstruct(digits, n: int, c: int, m: int, good, num_bits: int, den_bits: i
     return _take_solution(out)
 
 
+def selftest_bigint(seed: int, rounds: int) -> int:
+    """Failed checks of the host big-integer arithmetic (es_selftest_bigint; 0 = pass)."""
+    return L.load().es_selftest_bigint(seed, rounds)
+
+
 def selftest_modular(lo: int, hi: int, samples: int) -> int:
     """Mismatches of the library's Barrett reductions against % (host, no GPU)."""
     return L.load().es_selftest_modular(lo, hi, samples)

@@ -315,3 +315,82 @@ extern "C" int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples) 
   }
   return bad;
 }
+
+extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
+  using es::big::Nat;
+  namespace big = es::big;
+  if (rounds < 0) return -1;
+  uint64_t st = seed * 0x9E3779B97F4A7C15ull + 1;
+  auto rnd = [&]() {
+    st ^= st << 13;
+    st ^= st >> 7;
+    st ^= st << 17;
+    return st;
+  };
+  auto number = [&](size_t limbs) {
+    Nat x(limbs);
+    const uint64_t kind = rnd() % 4;
+    for (auto& v : x) v = kind == 1 ? ~0ull : kind == 2 ? (rnd() % 8 == 0 ? rnd() : 0) : rnd();
+    if (!x.empty() && x.back() == 0) x.back() = 1;
+    big::trim(x);
+    return x;
+  };
+  // plain O(n m) product, independent of the library's multiplication
+  auto school = [](const Nat& a, const Nat& b) {
+    Nat r(a.size() + b.size(), 0);
+    for (size_t i = 0; i < a.size(); ++i) {
+      unsigned __int128 carry = 0;
+      for (size_t j = 0; j < b.size(); ++j) {
+        const unsigned __int128 t = (unsigned __int128)a[i] * b[j] + r[i + j] + carry;
+        r[i + j] = (uint64_t)t;
+        carry = t >> 64;
+      }
+      for (size_t k = i + b.size(); carry; ++k) {
+        const unsigned __int128 t = (unsigned __int128)r[k] + carry;
+        r[k] = (uint64_t)t;
+        carry = t >> 64;
+      }
+    }
+    big::trim(r);
+    return r;
+  };
+  int64_t bad = 0;
+  for (int64_t t = 0; t < rounds; ++t) {
+    const size_t an = 1 + rnd() % 1200, bn = (t % 3 == 0) ? an : 1 + rnd() % 1200;
+    const Nat a = number(an), b = number(bn);
+    // products
+    if (big::mul(a, b) != school(a, b)) ++bad;
+    // division: a = q b + r, 0 <= r < b
+    if (!b.empty()) {
+      Nat q, r;
+      big::divmod(a, b, &q, &r);
+      Nat back = big::mul(q, b);
+      big::add_in(back, r);
+      if (back != a || big::cmp(r, b) >= 0) ++bad;
+    }
+    // shifts
+    const size_t sh = rnd() % 200;
+    if (big::shr(big::shl(a, sh), sh) != a) ++bad;
+    // rational reconstruction: num = +-den u (mod M), |num| <= 2^nbits, den > 0
+    if (t % 4 == 0) {
+      const size_t ml = 2 + rnd() % 120;
+      Nat M = number(ml);
+      if (M.empty()) continue;
+      M[0] |= 1;
+      Nat u;
+      big::divmod(number(ml), M, nullptr, &u);
+      const size_t nbits = big::bitlen(M) / 2;
+      Nat num, den;
+      bool neg = false;
+      if (big::rational_reconstruct(M, u, nbits, &num, &neg, &den)) {
+        Nat du, rem, nm;
+        big::divmod(big::mul(den, u), M, nullptr, &du);
+        big::divmod(num, M, nullptr, &nm);
+        // den u = num (mod M) for num >= 0, or = M - num for a negative one
+        if (neg && !nm.empty()) nm = big::sub(M, nm);
+        if (den.empty() || !big::le_pow2(num, nbits) || du != nm) ++bad;
+      }
+    }
+  }
+  return bad;
+}

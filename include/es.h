@@ -236,6 +236,15 @@ es_status es_reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m
  * (0 = pass), or -1 on bad arguments. */
 int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples);
 
+/* Host self-check of the reconstruction's big-integer arithmetic (no GPU):
+ * `rounds` pseudo-random cases from `seed` (sizes 1..1200 limbs, dense,
+ * all-ones and sparse patterns) checking Karatsuba products against a plain
+ * schoolbook product, division (q v + r == u, r < v), shifts, and the
+ * rational reconstruction's output (num == +-den u mod M, |num| <= 2^nbits,
+ * den > 0).  Returns the number of failed checks (0 = pass), or -1 on bad
+ * arguments. */
+int64_t es_selftest_bigint(uint64_t seed, int64_t rounds);
+
 #ifdef __cplusplus
 }
 #endif

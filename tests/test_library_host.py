@@ -51,6 +51,14 @@ def model_digits(A, b, m=None):
     return digits, good, nb, db, m
 
 
+def test_bigint_selftest(lib):
+    """Karatsuba products against a plain product, division and shift
+    identities and the rational reconstruction's defining congruence, on
+    random operands up to 1200 limbs (the reconstruction's big integers)."""
+    assert api.selftest_bigint(1, 300) == 0
+    assert api.selftest_bigint(2024, 300) == 0
+
+
 @pytest.mark.parametrize("case", ["n5c2", "pascal30", "n24_24bit", "hilbert6", "hilbert12", "n33c5", "planted"])
 def test_host_reconstruction_matches_oracle(lib, case):
     if case == "n5c2":
