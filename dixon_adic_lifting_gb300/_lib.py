@@ -62,6 +62,7 @@ _SIGS = {
                                ctypes.POINTER(c_vp)]),
     "es_selftest_modular": (c_i64, [c_i64, c_i64, c_i64]),
     "es_selftest_bigint": (c_i64, [ctypes.c_uint64, c_i64]),
+    "es_selftest_gj_reduction": (c_i64, []),
 }
 
 _lib = None

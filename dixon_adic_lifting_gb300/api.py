@@ -289,3 +289,9 @@ def selftest_bigint(seed: int, rounds: int) -> int:
 def selftest_modular(lo: int, hi: int, samples: int) -> int:
     """Mismatches of the library's Barrett reductions against % (host, no GPU)."""
     return L.load().es_selftest_modular(lo, hi, samples)
+
+
+def selftest_gj_reduction() -> int:
+    """Mismatches of the Gauss-Jordan kernels' f32 residue arithmetic against %
+    over every |x| < 2^20 and every prime (host, no GPU; 0 = pass)."""
+    return L.load().es_selftest_gj_reduction()

@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cmath>
+#include <cstring>
 #include <mutex>
 #include <string>
 
@@ -69,10 +71,18 @@ __constant__ QInvTable c_qinv = make_qinv_table();
 struct ModF {
   float q, qinv;
 };
-__device__ __forceinline__ float fred(float x, const ModF& mf) {
+// The host branch performs the same three IEEE operations (fused multiply-add,
+// add, fused multiply-add, round to nearest) so that es_selftest_gj_reduction
+// can check this function exhaustively on the CPU.
+ES_HD float fred(float x, const ModF& mf) {
   const float kM = 12582912.0f;  // 1.5 * 2^23
+#if defined(__CUDA_ARCH__)
   const float k = __fadd_rn(__fmaf_rn(x, mf.qinv, kM), -kM);
   return __fmaf_rn(-k, mf.q, x);
+#else
+  const float k = std::fmaf(x, mf.qinv, kM) + (-kM);
+  return std::fmaf(-k, mf.q, x);
+#endif
 }
 // 2^23 + 128 + x for the signed byte x = byte u of w: the f32 with bits 0x4B0000uu, uu = x + 128
 __device__ __forceinline__ float sbyte_fb(uint32_t w, int u) {
@@ -81,7 +91,16 @@ __device__ __forceinline__ float sbyte_fb(uint32_t w, int u) {
 // signed byte u of w as f32
 __device__ __forceinline__ float sbyte_f(uint32_t w, int u) { return __fadd_rn(sbyte_fb(w, u), -8388736.0f); }
 // low byte of an exact integer-valued f32 in (-2^22, 2^22), two's complement
-__device__ __forceinline__ uint32_t fbyte(float x) { return (uint32_t)__float_as_int(__fadd_rn(x, 12582912.0f)) & 0xFFu; }
+ES_HD uint32_t fbyte(float x) {
+#if defined(__CUDA_ARCH__)
+  return (uint32_t)__float_as_int(__fadd_rn(x, 12582912.0f)) & 0xFFu;
+#else
+  const float t = x + 12582912.0f;
+  uint32_t u;
+  std::memcpy(&u, &t, 4);
+  return u & 0xFFu;
+#endif
+}
 
 __device__ __forceinline__ void mma_f16_16x8x16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(
@@ -1636,3 +1655,26 @@ es_status run_inverse(const int64_t* A_dev, int64_t n, int8_t* B_dev, uint8_t* g
 }
 
 }  // namespace es
+
+// Host self-check of the f32 residue arithmetic of the Gauss-Jordan kernels:
+// for every odd prime q < 256 and every integer |x| < 2^20 (the domain the
+// kernels use it on), fred(x) must be the balanced residue of x and fbyte of
+// it that residue's two's complement low byte.  Returns the number of
+// mismatches.
+extern "C" int64_t es_selftest_gj_reduction(void) {
+  using namespace es;
+  const QInvTable qi = make_qinv_table();
+  int64_t bad = 0;
+  for (int j = 0; j < kNumPrimes; ++j) {
+    const int32_t q = (int32_t)kPrimes[j], h = (q - 1) / 2;
+    const ModF mf{(float)q, qi.v[j]};
+    for (int32_t x = -(1 << 20) + 1; x < (1 << 20); ++x) {
+      int32_t r = x % q;
+      if (r > h) r -= q;
+      if (r < -h) r += q;
+      const float f = fred((float)x, mf);
+      if (f != (float)r || fbyte(f) != ((uint32_t)r & 0xFFu)) ++bad;
+    }
+  }
+  return bad;
+}

@@ -391,6 +391,32 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
         if (den.empty() || !big::le_pow2(num, nbits) || du != nm) ++bad;
       }
     }
+    // planted fraction num / den: with M = den k + 1, den^{-1} = M - k (mod M),
+    // so u = -num k (mod M) represents it; with 2^(nbits+1) den < M the stopped
+    // Euclid must return exactly (num, den), sign included
+    if (t % 4 == 1) {
+      Nat den = number(1 + rnd() % 40), k = number(1 + rnd() % 40);
+      if (den.empty() || k.empty()) continue;
+      Nat M = big::mul(den, k);
+      big::add_in(M, big::from_u64(1));
+      const size_t dbits = big::bitlen(den), mbits = big::bitlen(M);
+      if (mbits < dbits + 4) continue;
+      const size_t nbits = mbits - dbits - 2;
+      Nat num = big::shr(number((nbits + 63) / 64 + 1), 64 * ((nbits + 63) / 64 + 1) - nbits);  // < 2^nbits
+      if (num.empty()) num = big::from_u64(1);
+      const bool neg = (rnd() & 1) != 0;
+      Nat u;
+      big::divmod(big::mul(num, k), M, nullptr, &u);  // num k mod M
+      if (!neg && !u.empty()) u = big::sub(M, u);    // -num k mod M
+      const Nat g = big::gcd(num, den);
+      if (!(g.size() == 1 && g[0] == 1)) {  // the expected result is the reduced fraction
+        big::divmod(Nat(num), g, &num, nullptr);
+        big::divmod(Nat(den), g, &den, nullptr);
+      }
+      Nat rn, rd;
+      bool rneg = false;
+      if (!big::rational_reconstruct(M, u, nbits, &rn, &rneg, &rd) || rn != num || rd != den || rneg != neg) ++bad;
+    }
   }
   return bad;
 }

@@ -192,8 +192,12 @@ es_status es_inverse_mod_device(const int64_t* A_dev, int64_t n, int8_t* B_dev, 
  * (cudaGetSymbolAddress, with that device current) and should come before
  * any stream capture.  All calls share the array, which keeps the previous
  * call's contents (everything that must start at zero is cleared); calls
- * are serialised on the host and synchronous, and device work that
- * overlapped them on another stream through this array would race.
+ * are serialised on the host, and each returns only after its device work
+ * has finished (it synchronises the stream it was given), so device work
+ * that overlapped a call on another stream through this array would race.
+ * The array's address is looked up once per device and kept for the life of
+ * the process: a caller that resets a device (cudaDeviceReset) must not
+ * call this entry point on that device again in the same process.
  * Unlike es_inverse_mod_device it accepts any int64 entries (residues are
  * exact for all of them).  n > 256 -> ES_ERR_RANGE with the reason in
  * es_last_error(). */
@@ -241,9 +245,20 @@ int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples);
  * all-ones and sparse patterns) checking Karatsuba products against a plain
  * schoolbook product, division (q v + r == u, r < v), shifts, and the
  * rational reconstruction's output (num == +-den u mod M, |num| <= 2^nbits,
- * den > 0).  Returns the number of failed checks (0 = pass), or -1 on bad
+ * den > 0), and its exact recovery of planted fractions num / den with
+ * 2^(nbits+1) den < M (sign included).  Returns the number of failed checks (0 = pass), or -1 on bad
  * arguments. */
 int64_t es_selftest_bigint(uint64_t seed, int64_t rounds);
+
+/* Host self-check of the Gauss-Jordan kernels' f32 residue arithmetic (no
+ * GPU; card §Method: the inverse's modular reduction).  The kernels keep row
+ * entries as exact f32 integers below 2^20 in magnitude and reduce them as
+ * x - q rint(x fl(1/q)) (one fused multiply-add against 1.5 * 2^23, one add,
+ * one fused multiply-add); the same source function is run here for every
+ * odd prime q < 256 and every integer |x| < 2^20 and compared with the
+ * balanced residue by the % operator, together with the byte extraction
+ * that stores the result.  Returns the number of mismatches (0 = pass). */
+int64_t es_selftest_gj_reduction(void);
 
 #ifdef __cplusplus
 }

@@ -39,6 +39,12 @@ def test_barrett_reduction_matches_mod(lib):
     assert api.selftest_modular((1 << 31) - 256 - (1 << 20), (1 << 31) - 256, 0) == 0
 
 
+def test_gauss_jordan_f32_reduction_is_exact(lib):
+    """The inverse kernels reduce exact f32 integers |x| < 2^20 as
+    x - q rint(x fl(1/q)); every such x and every prime, against %."""
+    assert api.selftest_gj_reduction() == 0
+
+
 def model_digits(A, b, m=None):
     gp, Bs = dm.good_primes(A)
     P = math.prod(gp)

@@ -258,6 +258,35 @@ def test_hadamard_bounds_hold():
                 assert y * y <= N2
 
 
+def test_hadamard_numerator_bound_carries_the_b_term():
+    """N_H = prod_i sqrt(||a_i||^2 + max_k b_ik^2) must include b: with A = I_4
+    the Cramer numerators are b itself while prod_i ||a_i|| = 1; and for a dense
+    4 x 4 system with 40-bit entries and 62-bit b, the bound without b asks for
+    one step although P' <= 2 |N| d (one step cannot determine the fraction),
+    so only the bound with b gives enough steps for the model to match the
+    oracle."""
+    A = [[int(i == j) for j in range(4)] for i in range(4)]
+    b = [[(1 << 40) - 3], [-(1 << 40) + 5], [(1 << 39) + 1], [-(1 << 40) + 7]]
+    N2, D2 = dm.hadamard_squares(A, b)
+    assert D2 == 1
+    dp, Y = exact.solve_numerators(A, b)
+    assert dp == 1 and [row[0] for row in Y] == [row[0] for row in b]
+    assert all(y * y <= N2 for row in Y for y in row)
+
+    rng = random.Random(41)
+    A = [[rng.randrange(-(1 << 40), 1 << 40) for _ in range(4)] for _ in range(4)]
+    b = [[rng.randrange(-(1 << 62), 1 << 62)] for _ in range(4)]
+    N, d = exact.solve(A, b)
+    gp, _ = dm.good_primes(A)
+    P = math.prod(gp)
+    N2, D2 = dm.hadamard_squares(A, b)
+    assert all(v * v <= N2 for row in N for v in row)
+    assert dm.steps_needed(P, D2, D2) == 1          # what a bound without b would ask for
+    assert P <= 2 * max(abs(v) for row in N for v in row) * d
+    res = dm.solve(A, b)
+    assert res is not None and (res[0], res[1]) == (N, d) and res[2]["m"] >= 2
+
+
 def test_steps_needed_is_minimal():
     P = math.prod(dm.PRIMES)
     for N2, D2 in ((1, 1), (10 ** 50, 10 ** 80), (2 ** 600, 2 ** 700), (2 ** 5000, 3 ** 4000)):
