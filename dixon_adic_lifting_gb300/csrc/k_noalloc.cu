@@ -15,6 +15,10 @@
 // shadow variable), so the address is fetched with cudaGetSymbolAddress once
 // per device, with that device current, the first time the entry point runs
 // on it.  That first call should therefore come before any stream capture.
+// Every call synchronises the stream it was given before returning.  The
+// address is kept for the life of the process, so a caller that resets a
+// device (cudaDeviceReset, which may reload the module elsewhere) must not
+// call the entry point on that device again.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -49,6 +49,32 @@ def test_noalloc_inverse_matches_allocating_entry_point(lib):
     assert g[0] == 0 and g[1] == 0
 
 
+def test_noalloc_accepts_any_int64_entries(lib):
+    """Residues of any int64 are exact, so this entry point takes entries far
+    beyond the solver's range (n max|A_ij| < 2^63), which the allocating entry
+    point rejects; its inverses match the oracle's Gauss-Jordan mod q_j."""
+    import torch
+
+    from oracle import dixon_model as dm
+
+    rng = np.random.default_rng(73)
+    n = 24
+    A = rng.integers(-(1 << 62), 1 << 62, size=(n, n), dtype=np.int64)
+    A[0, 0], A[1, 1], A[2, 3] = np.iinfo(np.int64).min, np.iinfo(np.int64).max, -(1 << 62)
+    st_ref, _, _ = _inverse(lib, torch, lib.es_inverse_mod_device, A)
+    assert st_ref == -2  # ES_ERR_RANGE: outside the solver's range
+    for call in range(2):  # two calls in a row through the shared array
+        st, B, g = _inverse(lib, torch, lib.es_inverse_mod_device_noalloc, A)
+        assert st == 0
+        Al = A.tolist()
+        for j, q in enumerate(dm.PRIMES):
+            Bq = dm.inverse_mod(Al, q)
+            assert g[j] == (0 if Bq is None else 1), (call, q)
+            if Bq is not None:
+                exp = np.array([[dm.bal(v, q) for v in row] for row in Bq], dtype=np.int8)
+                assert np.array_equal(B[j][:, :n], exp), (call, q)
+
+
 def test_noalloc_rejects_sizes_beyond_its_maximum(lib):
     import torch
 
