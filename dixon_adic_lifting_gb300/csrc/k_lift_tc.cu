@@ -10,24 +10,31 @@
 // 125^2 < 2^23) and then restarted, so the product is exact for any n <= 2^17.
 // B_j stays int8 in HBM (the product is bound by reading it once per step):
 // TMA brings 128 x 128 int8 tiles into shared memory and eight converter warps
-// widen them into the f16 operand tiles the MMA reads.
+// widen them to f16 straight into tensor memory, where the MMA reads its A
+// operand.  Shared memory then carries only the int8 tile (written by TMA,
+// read once by the converters) and the f16 residue tile of R_e (the B
+// operand), a third of the traffic of widening into shared memory, so that
+// reading B_j from HBM is the bound rather than shared-memory bandwidth.
 //
 // CTA = one prime e, 128 rows of B_j (MMA M = 128) and NT columns (N = NT):
-//   warp 0      one thread: TMA producer, 3-stage ring; a stage is K = 128:
+//   warp 0      one thread: TMA producer, 6-stage ring; a stage is K = 128:
 //               the int8 tile of B_j and two NT x 64 f16 tiles of R_e
 //               (128-byte swizzled, K-major)
-//   warps 6..13 converters: thread u widens half u / 128 of row u % 128 of
-//               the int8 tile into one of the stage's two 128 x 64 f16 tiles
-//               (same swizzle), then a proxy fence and an arrive on the
-//               stage's `conv` barrier
-//   warp 1      one thread: 8 MMAs (K = 16 each) per stage; a commit frees
-//               the stage and, at 512-K chunk ends, publishes the accumulator
+//   warps 6..13 converters: warp w may touch tensor-memory lanes 32 (w % 4)
+//               .. + 31, so thread (w, lane) widens half (w - 6) / 4 of row
+//               32 (w % 4) + lane of the int8 tile into 32 columns of the
+//               stage's A slot (tcgen05.st), waits for its stores and
+//               arrives on the stage's `conv` barrier
+//   warp 1      one thread: 8 MMAs (K = 16 each, A from tensor memory) per
+//               stage; a commit frees the stage's shared memory and A slot
+//               and, at 512-K chunk ends, publishes the accumulator
 //   warps 2..5  epilogue: fold each finished chunk from TMEM (tcgen05.ld,
 //               lane quarter = warp % 4) into int32, Barrett at the end.
-// The TMEM accumulator is double-buffered (2 NT columns) so MMAs of the next
-// chunk overlap the fold of the previous one.  Every mbarrier wait is bounded:
-// on expiry the kernel records an error code, stops issuing work, lets the
-// copies and MMAs in flight land and returns.
+// Tensor memory (512 columns, one CTA per SM): the accumulator double-buffered
+// in columns 0 .. 2 NT (MMAs of the next chunk overlap the fold of the
+// previous one) and six 64-column A slots from column 128.  Every mbarrier
+// wait is bounded: on expiry the kernel records an error code, stops issuing
+// work, lets the copies and MMAs in flight land and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -48,11 +55,16 @@ constexpr int kBK = 64;            // f16 tile K: one 128-byte row
 constexpr int kATileBytes = kBM * kBK * 2;  // 16 KB
 
 // product kernel
-constexpr int kPStages = 3;
+constexpr int kPStages = 6;
 constexpr int kPK = 128;                    // K per stage: one 128-byte int8 row
 constexpr int kPTileI8 = kBM * kPK;         // 16 KB
 constexpr int kPFoldStages = 4;             // fold every 4 stages (K = 512)
 constexpr int kPThreads = 448;             // producer, MMA, 4 epilogue and 8 converter warps
+// tensor memory: two accumulator buffers (2 NT <= 128 columns) from column 0,
+// then one f16 A slot of 64 columns (128 rows x 128 K) per stage
+constexpr uint32_t kPColA = 128;
+constexpr uint32_t kPTmemCols = 512;
+static_assert(kPColA + 64 * kPStages <= kPTmemCols, "tensor memory A slots");
 
 // residual kernel
 constexpr int kStages = 4;
@@ -87,8 +99,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sI = smem;                               // [S] 128 x 128 int8
-  uint8_t* sF = sI + kPStages * kPTileI8;           // [S][2] 128 x 64 f16
-  uint8_t* sR = sF + kPStages * 2 * kATileBytes;    // [S][2] NT x 64 f16
+  uint8_t* sR = sI + kPStages * kPTileI8;           // [S][2] NT x 64 f16
   uint64_t* full = reinterpret_cast<uint64_t*>(sR + kPStages * 2 * NT * 128);
   uint64_t* conv = full + kPStages;
   uint64_t* empty = conv + kPStages;
@@ -98,7 +109,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (kstages + kPFoldStages - 1) / kPFoldStages;
-  constexpr uint32_t kCols = 2 * NT < 32 ? 32 : 2 * NT;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPStages; ++s) {
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
-                 "r"(kCols));
+                 "r"(kPTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -144,33 +154,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       drain_loads(full, g, kPStages);
     }
-  } else if (warp >= 6) {  // converters: thread u widens half u / 128 (one f16 tile) of row u % 128
-    const int u = threadIdx.x - 192, r = u & 127, hq = 4 * (u >> 7), sw = r & 7;
+  } else if (warp >= 6) {
+    // converters: warp w may touch tensor-memory lanes 32 (w % 4) .. + 31, so
+    // thread u of the eight warps widens half h of row r of the int8 tile
+    // (64 K) into 32 columns of the stage's A slot in tensor memory
+    const int quarter = warp & 3, h = (warp - 6) >> 2, r = 32 * quarter + lane, sw = r & 7;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
     int g = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
       for (int st = 0; st < kstages; ++st, ++g) {
         const int s = g % kPStages;
+        // the slot's previous MMAs completed before its copy was issued (empty -> full)
         if (!mbar_wait(full + s, (g / kPStages) & 1, err, 5)) {
           stop = true;
           break;
         }
+        tc_fence_after();
         const uint8_t* src = sI + s * kPTileI8 + r * 128;
+        uint32_t wv[32];
 #pragma unroll
-        for (int q = hq; q < hq + 4; ++q) {  // 16-byte chunk q of the int8 row: k = 16 q .. 16 q + 15
-          const uint4 w = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
-          uint4 a, b;
-          s8x4_to_f16(w.x, a.x, a.y);
-          s8x4_to_f16(w.y, a.z, a.w);
-          s8x4_to_f16(w.z, b.x, b.y);
-          s8x4_to_f16(w.w, b.z, b.w);
-          // f16 tile q / 4, its chunks 2 (q % 4) and 2 (q % 4) + 1
-          uint8_t* dst = sF + (2 * s + (q >> 2)) * kATileBytes + r * 128;
-          const int c0 = 2 * (q & 3);
-          *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) = a;
-          *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ sw) << 4)) = b;
+        for (int q = 0; q < 4; ++q) {  // 16-byte chunk 4 h + q of the row: k = 64 h + 16 q .. + 15
+          const uint4 w = *reinterpret_cast<const uint4*>(src + (((4 * h + q) ^ sw) << 4));
+          s8x4_to_f16(w.x, wv[8 * q + 0], wv[8 * q + 1]);
+          s8x4_to_f16(w.y, wv[8 * q + 2], wv[8 * q + 3]);
+          s8x4_to_f16(w.z, wv[8 * q + 4], wv[8 * q + 5]);
+          s8x4_to_f16(w.w, wv[8 * q + 6], wv[8 * q + 7]);
         }
-        fence_proxy_async_smem();  // the generic-proxy writes, before the tensor core reads them
+        tmem_st32(trow + (uint32_t)(kPColA + s * 64 + 32 * h), wv);
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(conv + s);
       }
     }
@@ -193,12 +206,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint64_t ad = desc_sw128(sF + (2 * s + h) * kATileBytes),
-                           bd = desc_sw128(sR + (2 * s + h) * NT * 128);
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t bd = desc_sw128(sR + (2 * s + hh) * NT * 128);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              mma_f16(tmem + buf * NT, ad + 2 * k, bd + 2 * k, idesc, (first && h == 0 && k == 0) ? 0u : 1u);
+              mma_f16_ta(tmem + buf * NT, tmem + (uint32_t)(kPColA + s * 64 + 32 * hh + 8 * k), bd + 2 * k, idesc,
+                         (first && hh == 0 && k == 0) ? 0u : 1u);
           }
           mma_commit(empty + s);
           if ((st % kPFoldStages) == kPFoldStages - 1 || st == kstages - 1) mma_commit(accfull + buf);
@@ -240,7 +253,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         int8_t* out = V + ((int64_t)T.e * n + row) * c + T.n0;
         if (c % 16 == 0 && T.n0 + NT <= c) {
           // the row's NT bytes are contiguous and 16-byte aligned: 16-byte stores
-          // (byte stores here would hold up the converter warps' shared-memory traffic)
 #pragma unroll
           for (int i = 0; i < NT; i += 16) {
             uint32_t w[4];
@@ -264,7 +276,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPTmemCols));
   }
 }
 
@@ -465,7 +477,7 @@ int sm_count() {
 template <int NT>
 es_status launch_nt(const CUtensorMap& mB, const CUtensorMap& mR, const LiftConst* K, int8_t* V, int64_t n,
                     int64_t c, int64_t ld, int E, int* err, cudaStream_t st) {
-  const size_t smem = 1024 + (size_t)kPStages * (kPTileI8 + 2 * kATileBytes + 2 * NT * 128) + 256;
+  const size_t smem = 1024 + (size_t)kPStages * (kPTileI8 + 2 * NT * 128) + 256;
   static_assert(NT % 16 == 0 && NT <= 64, "N tile");
   ES_CHECK(cuda_status(cudaFuncSetAttribute(k_lift_gemm_tc<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)smem),
