@@ -614,7 +614,7 @@ constexpr int64_t kTcMinCols = 16;       // c >= 16: product on tcgen05 (k_lift_
 constexpr int64_t kResidTcMinN = 1024;   // from this n: the residual update on tcgen05 (k_lift_tc.cu)
 constexpr int64_t kCrtThreadMin = 32768;  // from this many entries: one thread per entry
 struct LiftLayout {
-  size_t K, R, V, r, xl, A32, R16, A16, X16, Bf, err, bar, total;
+  size_t K, R, V, r, xl, A32, R16, A16, X16, Bf, Bt, err, bar, total;
 };
 LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   int64_t ld = padded_ld(n);
@@ -631,6 +631,7 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   o.A16 = tc && a32 ? L.add((size_t)kResidLimbsMax * n * ld * 2) : 0;
   o.X16 = tc && a32 ? L.add((size_t)(kResidLimbsMax + 7) * c * ld * 2) : 0;
   o.Bf = (c == 1 && ld <= kFusedMaxLd) ? L.add((size_t)E * n * ld) : 0;
+  o.Bt = tc ? L.add(tc_tiled_b_bytes(n, E)) : 0;
   o.err = L.add(sizeof(int));
   o.bar = L.add(sizeof(unsigned));
   o.total = L.total;
@@ -710,7 +711,11 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
   } else {
     ES_CHECK(cuda_status(cudaMemsetAsync(bar, 0, sizeof(unsigned), st), "memset barrier"));
   }
-  if (tc) ES_CHECK(tc_prepare(&tcl, B_dev, R16, n, c, ld, E));
+  if (tc) {
+    int8_t* Bt = reinterpret_cast<int8_t*>(scratch + L.Bt);
+    ES_CHECK(tc_prepare(&tcl, Bt, R16, n, c, ld, E));
+    ES_CHECK(tc_tile_b(B_dev, K, Bt, n, ld, E, st));
+  }
   if (na) ES_CHECK(tc_resid_prepare(&tcr, A_dev, scratch + L.A16, xo.XL, n, c, ld, na, st));
   if (a32 && !na) {
     k_narrow_a<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, A32);

@@ -131,29 +131,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *s_tmem;
+  // broadcast: the compiler then knows the base is the same in every lane
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *s_tmem, 0);
 
-  if (warp == 0) {
-    if (lane == 0) {  // TMA producer
-      int g = 0;      // stages issued by this CTA
-      bool stop = false;
-      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
-        const ProdTile T = prod_tile(t, tiles_m, tiles_n, NT);
-        const int j = K->pidx[T.e];
-        for (int st = 0; st < kstages; ++st, ++g) {
-          const int s = g % kPStages;
-          if (g >= kPStages && !mbar_wait(empty + s, ((g / kPStages) & 1) ^ 1, err, 1)) {
-            stop = true;
-            break;
-          }
+  if (warp == 0) {  // TMA producer: the warp runs the loop, one elected lane issues
+    int g = 0;      // stages issued by this CTA
+    bool stop = false;
+    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+      const ProdTile T = prod_tile(t, tiles_m, tiles_n, NT);
+      for (int st = 0; st < kstages; ++st, ++g) {
+        const int s = g % kPStages;
+        if (g >= kPStages && !mbar_wait_warp(empty + s, ((g / kPStages) & 1) ^ 1, err, 1)) {
+          stop = true;
+          break;
+        }
+        if (elect_one()) {
           mbar_expect_tx(full + s, kPTileI8 + 2 * NT * 128);
-          tma_load_3d(sI + s * kPTileI8, &tmB, full + s, st * kPK, T.m0, j);
+          tma_load_3d(sI + s * kPTileI8, &tmB, full + s, 0, 0, (T.e * tiles_m + T.m0 / kBM) * kstages + st);
           tma_load_3d(sR + (2 * s) * NT * 128, &tmR, full + s, st * kPK, T.n0, T.e);
           tma_load_3d(sR + (2 * s + 1) * NT * 128, &tmR, full + s, st * kPK + kBK, T.n0, T.e);
         }
+        __syncwarp();
       }
-      drain_loads(full, g, kPStages);
     }
+    drain_loads(full, g, kPStages);
   } else if (warp >= 6) {
     // converters: warp w may touch tensor-memory lanes 32 (w % 4) .. + 31, so
     // thread u of the eight warps widens half h of row r of the int8 tile
@@ -187,24 +188,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_arrive(conv + s);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-      int g = 0, gc0 = 0;  // stages and accumulator chunks of earlier tiles
-      bool stop = false;
-      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x, gc0 += nchunks) {
-        for (int st = 0; st < kstages; ++st, ++g) {
-          const int s = g % kPStages, gc = gc0 + st / kPFoldStages, buf = gc & 1;
-          const bool first = (st % kPFoldStages) == 0;
-          if (first && gc >= 2 && !mbar_wait(accempty + buf, ((gc - 2) >> 1) & 1, err, 2)) {
-            stop = true;
-            break;
-          }
-          if (!mbar_wait(conv + s, (g / kPStages) & 1, err, 3)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
+  } else if (warp == 1) {  // MMA issuer: the warp runs the loop, one elected lane issues
+    const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+    int g = 0, gc0 = 0;  // stages and accumulator chunks of earlier tiles
+    bool stop = false;
+    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x, gc0 += nchunks) {
+      for (int st = 0; st < kstages; ++st, ++g) {
+        const int s = g % kPStages, gc = gc0 + st / kPFoldStages, buf = gc & 1;
+        const bool first = (st % kPFoldStages) == 0;
+        if (first && gc >= 2 && !mbar_wait_warp(accempty + buf, ((gc - 2) >> 1) & 1, err, 2)) {
+          stop = true;
+          break;
+        }
+        if (!mbar_wait_warp(conv + s, (g / kPStages) & 1, err, 3)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const uint64_t bd = desc_sw128(sR + (2 * s + hh) * NT * 128);
@@ -216,11 +217,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
           mma_commit(empty + s);
           if ((st % kPFoldStages) == kPFoldStages - 1 || st == kstages - 1) mma_commit(accfull + buf);
         }
+        __syncwarp();
       }
-      // every MMA issued has completed before tensor memory is released
-      mma_commit(drained);
-      mbar_wait_drain(drained, 0);
     }
+    // every MMA issued has completed before tensor memory is released
+    if (elect_one()) mma_commit(drained);
+    __syncwarp();
+    mbar_wait_drain(drained, 0);
   } else {  // epilogue warpgroup (warps 2..5)
     const int quarter = warp & 3;
     int gc0 = 0;
@@ -424,15 +427,29 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // R16[e][col][i] = balanced residue of r_{i+1}[i][col] mod q_e, as f16; one
 // thread per entry, rows fastest so that the stores of a prime are coalesced.
+// The residual is usually far inside the int32 range (|r_{i+1}| < n max|A| / 2
+// + 1 once the first step is done), so a CTA whose entries all fit takes the
+// one-Barrett path; the reduction constants come from shared memory.
 __global__ void __launch_bounds__(256) k_lift_r16(const int64_t* __restrict__ rn, int64_t n, int64_t c, int64_t ld,
                                                   const LiftConst* __restrict__ K, __half* __restrict__ R16) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= n * c) return;
-  const int64_t col = t / n, i = t - col * n;
-  const int64_t v = rn[i * c + col];
+  __shared__ ModQ sm[kNumPrimes];
   const int E = K->E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sm[e] = K->mq[e];
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool live = t < n * c;
+  const int64_t col = live ? t / n : 0, i = live ? t - col * n : 0;
+  const int64_t v = live ? rn[i * c + col] : 0;
+  // -2^31 < v < 2^31 - 256: the signed 32-bit reduction applies
+  const bool narrow = __syncthreads_and(v > -(int64_t(1) << 31) && v < (int64_t(1) << 31) - 256);
+  if (!live) return;
   __half* out = R16 + col * ld + i;
-  for (int e = 0; e < E; ++e) out[(int64_t)e * c * ld] = __int2half_rn(reduce_i64_bal(v, K->mq[e]));
+  if (narrow) {
+    const int32_t v32 = (int32_t)v;
+#pragma unroll 4
+    for (int e = 0; e < E; ++e) out[(int64_t)e * c * ld] = __int2half_rn(reduce_bal(v32, sm[e]));
+  } else {
+    for (int e = 0; e < E; ++e) out[(int64_t)e * c * ld] = __int2half_rn(reduce_i64_bal(v, sm[e]));
+  }
 }
 
 // A16[a][i][k] = limb a of A[i][k] in balanced base 256 (k < n), 0 for n <= k < ld.
@@ -447,6 +464,25 @@ __global__ void k_a_limbs(const int64_t* __restrict__ A, int64_t n, int64_t ld, 
     v = (v - d) >> 8;
   }
   A16[((int64_t)(na - 1) * n + i) * ld + k] = __int2half_rn((int)v);
+}
+
+// Bt[e][mt][kb][r][k'] = B_j[128 mt + r][128 kb + k'] (j = K->pidx[e]), zero
+// outside n rows and ld columns; one thread per 16-byte chunk, in Bt order.
+__global__ void k_tile_b(const int8_t* __restrict__ B, const LiftConst* __restrict__ K, int8_t* __restrict__ Bt,
+                         int64_t n, int64_t ld, int64_t tiles_m, int64_t kst, int64_t chunks) {
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= chunks) return;
+  const int q = (int)(u & 7);
+  int64_t rest = u >> 3;
+  const int r = (int)(rest % kBM);
+  rest /= kBM;
+  const int64_t kb = rest % kst;
+  rest /= kst;
+  const int64_t mt = rest % tiles_m, e = rest / tiles_m;
+  const int64_t i = mt * kBM + r, k = kb * kPK + 16 * q;
+  int4 v = make_int4(0, 0, 0, 0);
+  if (i < n && k < ld) v = *reinterpret_cast<const int4*>(B + ((int64_t)K->pidx[e] * n + i) * ld + k);
+  reinterpret_cast<int4*>(Bt)[u] = v;
 }
 
 __global__ void k_to_f16(const int8_t* __restrict__ src, __half* __restrict__ dst, int64_t count) {
@@ -500,11 +536,26 @@ es_status tc_convert_f16(const int8_t* src, void* dst, int64_t count, void* stre
   return cuda_status(cudaGetLastError(), "k_to_f16");
 }
 
-es_status tc_prepare(TcLift* t, const int8_t* B, const void* R16, int64_t n, int64_t c, int64_t ld, int E) {
+size_t tc_tiled_b_bytes(int64_t n, int E) {
+  const int64_t tiles_m = (n + kBM - 1) / kBM, kst = (padded_ld(n) + kPK - 1) / kPK;
+  return (size_t)E * tiles_m * kst * kPTileI8;
+}
+
+es_status tc_prepare(TcLift* t, const int8_t* Bt, const void* R16, int64_t n, int64_t c, int64_t ld, int E) {
   t->nt = c <= 16 ? 16 : c <= 32 ? 32 : 64;
-  ES_CHECK(make_map_u8(&t->mapB, B, ld, n, kNumPrimes, kBM));
+  t->tiles_m = (int)((n + kBM - 1) / kBM);
+  t->kstages = (int)((ld + kPK - 1) / kPK);
+  ES_CHECK(make_map_u8(&t->mapB, Bt, kPK, kBM, (int64_t)E * t->tiles_m * t->kstages, kBM));
   ES_CHECK(make_map(&t->mapR, R16, ld, c, E, t->nt));
   return ES_OK;
+}
+
+es_status tc_tile_b(const int8_t* B, const LiftConst* K, int8_t* Bt, int64_t n, int64_t ld, int E, void* stream) {
+  const int64_t tiles_m = (n + kBM - 1) / kBM, kst = (ld + kPK - 1) / kPK;
+  const int64_t chunks = (int64_t)E * tiles_m * kst * (kPTileI8 / 16);
+  k_tile_b<<<(unsigned)((chunks + 255) / 256), 256, 0, (cudaStream_t)stream>>>(B, K, Bt, n, ld, tiles_m, kst, chunks);
+  count_launch();
+  return cuda_status(cudaGetLastError(), "k_tile_b");
 }
 
 int resid_limbs(uint64_t max_abs_a) {

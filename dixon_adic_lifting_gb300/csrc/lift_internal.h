@@ -23,14 +23,21 @@ struct LiftConst {
   uint64_t Pinv64;                // P'^{-1} mod 2^64
 };
 
-// tcgen05 lift product (k_lift_tc.cu), used for c >= 16.
+// tcgen05 lift product (k_lift_tc.cu), used for c >= 16.  It reads the
+// inverses of the good primes from a tiled copy Bt [E'][n / 128][ld / 128]
+// [128][128] (rounded up, zero padded): each 128 x 128 tile one contiguous
+// 16 KB block, so that every copy streams whole DRAM pages.
 struct TcLift {
-  CUtensorMap mapB;  // int8 [53][n][ld] inverses
+  CUtensorMap mapB;  // int8 Bt, one 128 x 128 tile per plane
   CUtensorMap mapR;  // f16 [E'][c][ld] residues of r_i
   int nt = 64;       // MMA N tile
+  int tiles_m = 0, kstages = 0;
 };
+size_t tc_tiled_b_bytes(int64_t n, int E);
 es_status tc_convert_f16(const int8_t* src, void* dst, int64_t count, void* stream);
-es_status tc_prepare(TcLift* t, const int8_t* B, const void* R16, int64_t n, int64_t c, int64_t ld, int E);
+es_status tc_prepare(TcLift* t, const int8_t* Bt, const void* R16, int64_t n, int64_t c, int64_t ld, int E);
+// B [53][n][ld] (good primes via K->pidx) -> Bt, once per lift.
+es_status tc_tile_b(const int8_t* B, const LiftConst* K, int8_t* Bt, int64_t n, int64_t ld, int E, void* stream);
 es_status tc_launch(const TcLift& t, const LiftConst* K, int8_t* V, int64_t n, int64_t c, int64_t ld, int E,
                     int* err, void* stream);
 
