@@ -94,6 +94,31 @@ void build_lift_const(const uint8_t* good, LiftConst* K) {
   uint64_t p64 = (uint64_t)P[0] | ((uint64_t)P[1] << 32), x = p64;
   for (int it = 0; it < 6; ++it) x *= 2 - p64 * x;
   K->Pinv64 = x;
+  // byte matrix of the CRT product, row e (prime), column b (byte), as the B
+  // fragments of mma.sync m16n8k16: lane = 4 g + t, register 0 holds rows
+  // 16 ks + 2 t, + 1 and register 1 rows 16 ks + 2 t + 8, + 9, column 8 nt + g
+  auto mbyte = [&](int e, int b) -> uint32_t {
+    if (e >= E) return 0;
+    if (b < 42) return (K->Mq[e][b / 4] >> (8 * (b % 4))) & 0xFFu;
+    if (b < 49) return (uint32_t)((K->tfix[e] >> (8 * (b - 42))) & 0xFFu);
+    return 0;
+  };
+  auto f16bits = [](uint32_t v) -> uint32_t {  // exact f16 of an integer 0 <= v <= 255
+    if (v == 0) return 0;
+    int ex = 0;
+    while ((v >> ex) > 1) ++ex;                        // 2^ex <= v < 2^(ex+1)
+    const uint32_t mant = (v << (10 - ex)) & 0x3FFu;  // ex <= 7: exact
+    return ((uint32_t)(ex + 15) << 10) | mant;
+  };
+  for (int nt = 0; nt < kCrtNTiles; ++nt)
+    for (int ks = 0; ks < 4; ++ks)
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3, col = 8 * nt + g;
+        for (int rg = 0; rg < 2; ++rg) {
+          const int e0 = 16 * ks + 2 * t + 8 * rg;
+          K->crt_bfrag[nt][ks][lane][rg] = f16bits(mbyte(e0, col)) | (f16bits(mbyte(e0 + 1, col)) << 16);
+        }
+      }
 }
 
 // ------------------------------------------------------------ kernels
@@ -324,6 +349,149 @@ __global__ void __launch_bounds__(128) k_lift_crt_thread(const int8_t* __restric
     const int64_t i = t / xo.c, col = t - i * xo.c;
 #pragma unroll
     for (int s = 0; s < 8; ++s) xo.XL[((int64_t)(xo.na - 1 + s) * xo.c + col) * xo.ld + i] = x_limb(x, s);
+  }
+}
+
+// The same digit from c_e = v_e w_e mod q_e in [0, q_e) (V holds c_e as bytes,
+// as the tensor-core product writes them), with the word sums on the tensor
+// cores: the byte columns S_b = sum_e c_e byte_b(P'/q_e) (and of floor(2^50/q_e))
+// are one mma.sync m16n8k16 product of the [entries x primes] matrix of c_e by
+// the constant [primes x 56] byte matrix, exact in the FP32 accumulator (each
+// product < 2^16, 53 of them < 2^22).  CTA = 4 warps over four sub-tiles of
+// 128 consecutive entries: per sub-tile the c_e tile is staged in shared
+// memory, each warp forms the column sums of its 32 entries (two 16-row tiles
+// x 7 column tiles x 4 k-steps), parks them in shared memory, and each lane
+// assembles and finishes the digit of one entry.  The limb planes of x_i mod
+// 2^64 (for the tensor-core residual) are written at the end, rows fastest.
+__device__ __forceinline__ uint32_t u8pair_f16(uint32_t lo, uint32_t hi) {
+  // 0x64uu is the f16 1024 + u; subtracting 1024 leaves u exactly
+  uint32_t r = (lo & 0xFFu) | ((hi & 0xFFu) << 16) | 0x64006400u;
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(r) : "r"(0x64006400u));
+  return r;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+constexpr int kCrtDStride = 49;  // words per entry row of the parked sums (odd: no bank conflicts)
+constexpr int kCrtSub = 4;       // 128-entry sub-tiles per CTA
+__global__ void __launch_bounds__(128) k_lift_crt_mma(const uint8_t* __restrict__ V, int64_t nc,
+                                                      const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
+                                                      uint64_t* __restrict__ xl, XLimbs xo) {
+  __shared__ __align__(16) uint8_t sV[64][128];
+  __shared__ uint32_t sD[128 * kCrtDStride];
+  __shared__ __align__(16) uint32_t sB[kCrtNTiles * 4 * 32 * 2];
+  __shared__ uint64_t sX[kCrtSub * 128];
+  __shared__ uint32_t sP[kCrtWords], sPh[kCrtWords];
+  const int E = K->E;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+  const int64_t tcta = (int64_t)blockIdx.x * (128 * kCrtSub);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(&K->crt_bfrag[0][0][0][0]);
+    for (int i = tid; i < kCrtNTiles * 4 * 32 * 2 / 4; i += 128) reinterpret_cast<uint4*>(sB)[i] = src[i];
+    if (tid < kCrtWords) {
+      sP[tid] = K->P[tid];
+      sPh[tid] = K->Phalf[tid];
+    }
+  }
+  for (int sub = 0; sub < kCrtSub; ++sub) {
+    const int64_t t0 = tcta + 128 * sub, tt = t0 + tid;
+    if (t0 >= nc) break;
+    __syncthreads();  // the previous sub-tile's reads of sV are done (and the constants are in place)
+    if ((nc & 15) == 0 && t0 + 128 <= nc) {
+      // 16-byte pieces of the rows: all four of a thread's loads in flight at once
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = tid + 128 * u, e = idx >> 3, q = idx & 7;
+        v[u] = e < E ? *reinterpret_cast<const uint4*>(V + (int64_t)e * nc + t0 + 16 * q) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = tid + 128 * u;
+        *reinterpret_cast<uint4*>(&sV[idx >> 3][16 * (idx & 7)]) = v[u];
+      }
+    } else {
+#pragma unroll 8
+      for (int e = 0; e < 64; ++e) sV[e][tid] = (e < E && tt < nc) ? V[(int64_t)e * nc + tt] : 0;
+    }
+    __syncthreads();
+    // A fragments of this warp's two 16-entry tiles
+    uint32_t a[2][4][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int r0 = 32 * warp + 16 * mt + g;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int e0 = 16 * ks + 2 * t4;
+        a[mt][ks][0] = u8pair_f16(sV[e0][r0], sV[e0 + 1][r0]);
+        a[mt][ks][1] = u8pair_f16(sV[e0][r0 + 8], sV[e0 + 1][r0 + 8]);
+        a[mt][ks][2] = u8pair_f16(sV[e0 + 8][r0], sV[e0 + 9][r0]);
+        a[mt][ks][3] = u8pair_f16(sV[e0 + 8][r0 + 8], sV[e0 + 9][r0 + 8]);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < kCrtNTiles; ++nt) {
+      float d[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint2 bb = *reinterpret_cast<const uint2*>(&sB[((nt * 4 + ks) * 32 + lane) * 2]);
+        mma16816(d[0], a[0][ks], bb.x, bb.y);
+        mma16816(d[1], a[1][ks], bb.x, bb.y);
+      }
+      const int c0 = 8 * nt + 2 * t4;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = 32 * warp + 16 * mt + g;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // columns c0, c0 + 1 (only the first 49 are used)
+          if (c0 + h < kCrtDStride) {
+            sD[r0 * kCrtDStride + c0 + h] = (uint32_t)d[mt][h];
+            sD[(r0 + 8) * kCrtDStride + c0 + h] = (uint32_t)d[mt][2 + h];
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (tt < nc) {
+      const uint32_t* col = sD + tid * kCrtDStride;  // this lane's entry: row 32 warp + lane = tid
+      uint64_t acc[kCrtWords];
+#pragma unroll
+      for (int l = 0; l < kCrtWords; ++l) {
+        uint64_t w = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (4 * l + j < 42) w += (uint64_t)col[4 * l + j] << (8 * j);
+        acc[l] = w;
+      }
+      uint64_t tf = 0;
+#pragma unroll
+      for (int j = 0; j < 7; ++j) tf += (uint64_t)col[42 + j] << (8 * j);
+      uint32_t S[kCrtWords];
+      crt_finish(acc, tf, sP, sPh, S);
+      uint64_t* out = D + tt * kDigitLimbs;
+#pragma unroll
+      for (int l = 0; l < kDigitLimbs; ++l) out[l] = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
+      const uint64_t x = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
+      xl[tt] = x;
+      sX[128 * sub + tid] = x;
+    }
+  }
+  if (!xo.XL) return;
+  __syncthreads();
+  // limb planes XL[na - 1 + s][col][i] of this CTA's entries [tcta, tcta + cnt):
+  // walked with i fastest, so that consecutive threads store consecutive i
+  const int64_t cnt = (nc - tcta) < 128 * kCrtSub ? (nc - tcta) : 128 * kCrtSub;
+  const int64_t c = xo.c, i0 = tcta / c;
+  const int nr = (int)((tcta + cnt - 1) / c - i0 + 1);  // rows touched (at most 512 / c + 2)
+  const int cnr = (int)c * nr, total = 8 * cnr;          // c <= 2^24: fits 32 bits
+  for (int idx = tid; idx < total; idx += 128) {
+    const int s8 = idx / cnr, rem = idx - s8 * cnr, cl = rem / nr;
+    const int64_t i = i0 + (rem - cl * nr), t = i * c + cl;
+    if (t < tcta || t >= tcta + cnt) continue;
+    xo.XL[((int64_t)(xo.na - 1 + s8) * c + cl) * xo.ld + i] = x_limb(sX[t - tcta], s8);
   }
 }
 
@@ -614,7 +782,7 @@ constexpr int64_t kTcMinCols = 16;       // c >= 16: product on tcgen05 (k_lift_
 constexpr int64_t kResidTcMinN = 1024;   // from this n: the residual update on tcgen05 (k_lift_tc.cu)
 constexpr int64_t kCrtThreadMin = 32768;  // from this many entries: one thread per entry
 struct LiftLayout {
-  size_t K, R, V, r, xl, A32, R16, A16, X16, Bf, Bt, err, bar, total;
+  size_t K, R, V, r, xl, A32, R16, A16, X16, Sacc, Bf, Bt, err, bar, total;
 };
 LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   int64_t ld = padded_ld(n);
@@ -630,6 +798,7 @@ LiftLayout lift_layout(int64_t n, int64_t c, int E, bool a32) {
   o.R16 = tc ? L.add((size_t)E * c * ld * 2) : 0;
   o.A16 = tc && a32 ? L.add((size_t)kResidLimbsMax * n * ld * 2) : 0;
   o.X16 = tc && a32 ? L.add((size_t)(kResidLimbsMax + 7) * c * ld * 2) : 0;
+  o.Sacc = tc && a32 ? L.add((size_t)n * c * 8) : 0;
   o.Bf = (c == 1 && ld <= kFusedMaxLd) ? L.add((size_t)E * n * ld) : 0;
   o.Bt = tc ? L.add(tc_tiled_b_bytes(n, E)) : 0;
   o.err = L.add(sizeof(int));
@@ -716,7 +885,11 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     ES_CHECK(tc_prepare(&tcl, Bt, R16, n, c, ld, E));
     ES_CHECK(tc_tile_b(B_dev, K, Bt, n, ld, E, st));
   }
-  if (na) ES_CHECK(tc_resid_prepare(&tcr, A_dev, scratch + L.A16, xo.XL, n, c, ld, na, st));
+  uint64_t* Sacc = na ? reinterpret_cast<uint64_t*>(scratch + L.Sacc) : nullptr;
+  if (na) {
+    ES_CHECK(tc_resid_prepare(&tcr, A_dev, scratch + L.A16, xo.XL, n, c, ld, na, st));
+    ES_CHECK(cuda_status(cudaMemsetAsync(Sacc, 0, (size_t)nc * 8, st), "memset Sacc"));
+  }
   if (a32 && !na) {
     k_narrow_a<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, A32);
     ES_CHECK(cuda_status(cudaGetLastError(), "k_narrow_a"));
@@ -760,7 +933,10 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     }
     if (!run->ev.empty()) cudaEventRecord(ev(2 * i + 1), st);
     count_launch();
-    if (nc >= kCrtThreadMin)
+    if (tc)
+      k_lift_crt_mma<<<(unsigned)((nc + 128 * kCrtSub - 1) / (128 * kCrtSub)), 128, 0, st>>>(reinterpret_cast<const uint8_t*>(V), nc, K,
+                                                                   digits_dev + (size_t)i * nc * kDigitLimbs, xl, xo);
+    else if (nc >= kCrtThreadMin)
       k_lift_crt_thread<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
                                                                       xl, xo);
     else
@@ -770,7 +946,7 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
       const int64_t* rc = r[i & 1];
       int64_t* rn = r[(i + 1) & 1];
       if (na) {
-        ES_CHECK(tc_resid_launch(tcr, K, rc, rn, R16, n, c, ld, err, st));
+        ES_CHECK(tc_resid_launch(tcr, K, rc, rn, Sacc, R16, n, c, ld, err, st));
         continue;
       }
       count_launch(1);

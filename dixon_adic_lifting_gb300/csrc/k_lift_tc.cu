@@ -1,5 +1,7 @@
 // Lift product on the 5th-generation tensor cores, for c >= 16 columns:
-//     V[e][i][col] = bal( sum_k B_j[i][k] R_e[col][k]  mod q_j )
+//     V[e][i][col] = w_e bal( sum_k B_j[i][k] R_e[col][k] ) mod q_j   in [0, q_j)
+// (w_e = (P'/q_e)^{-1} mod q_e: the CRT's weight, so that the digit is
+// sum_e V[e] P'/q_e reduced mod P', formed by k_lift_crt_mma)
 // (exact-solve card, §Method: the per-step per-prime products as one batched
 // GEMM on balanced residues, exact in the integer accumulator).
 //
@@ -66,10 +68,6 @@ constexpr uint32_t kPColA = 128;
 constexpr uint32_t kPTmemCols = 512;
 static_assert(kPColA + 64 * kPStages <= kPTmemCols, "tensor memory A slots");
 
-// residual kernel
-constexpr int kStages = 4;
-constexpr int kFoldBlocks = 8;     // fold every 8 K-blocks (K = 512)
-constexpr int kThreads = 192;
 
 // The producer's exit: wait (bounded, whatever the error flag) for the copies
 // of the last `depth` stages it issued, so that none is still writing shared
@@ -252,8 +250,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_arrive(accempty + buf);
       }
       if (ok && row < n) {
+        // the CRT's weight of this prime applied here: c_e = y w_e mod q_e in [0, q_e)
         const ModQ m = K->mq[T.e];
-        int8_t* out = V + ((int64_t)T.e * n + row) * c + T.n0;
+        const uint32_t we = K->w[T.e];
+        auto ce = [&](int32_t y) -> uint32_t { return barrett(barrett((uint32_t)y + m.off, m) * we, m); };
+        uint8_t* out = reinterpret_cast<uint8_t*>(V) + ((int64_t)T.e * n + row) * c + T.n0;
         if (c % 16 == 0 && T.n0 + NT <= c) {
           // the row's NT bytes are contiguous and 16-byte aligned: 16-byte stores
 #pragma unroll
@@ -261,16 +262,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              w[q] = (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q], m) |
-                     (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q + 1], m) << 8 |
-                     (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q + 2], m) << 16 |
-                     (uint32_t)(uint8_t)reduce_bal(acc[i + 4 * q + 3], m) << 24;
+              w[q] = ce(acc[i + 4 * q]) | ce(acc[i + 4 * q + 1]) << 8 | ce(acc[i + 4 * q + 2]) << 16 |
+                     ce(acc[i + 4 * q + 3]) << 24;
             *reinterpret_cast<uint4*>(out + i) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < NT; ++i)
-            if (T.n0 + i < c) out[i] = (int8_t)reduce_bal(acc[i], m);
+            if (T.n0 + i < c) out[i] = (uint8_t)ce(acc[i]);
         }
       }
     }
@@ -284,49 +283,56 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 // ---------------------------------------------------------------- residual
-// r_{i+1} = (r_i - A x_i) P'^{-1} mod 2^64 on the tensor cores (exact-solve
-// card, §Method: the residual kept in one 64-bit limb).  With A = sum_a A_a
-// 256^a and x_i = sum_s X_s 256^s (mod 2^64) in balanced 8-bit limbs (|A_a|,
-// |X_s| <= 128, exact in f16),
-//     A x_i = sum_{s < 8} 256^s Y_s  (mod 2^64),   Y_s = sum_a A_a X_{s-a},
-// which is one GEMM with K' = na ld: the A operand is A's limb planes side by
-// side; on the K range of plane a, row (s, col) of the B operand is
-// X_{s-a}[col], read by one 3-D TMA box of 8 limb planes x 8 columns from the
-// X planes (stored after na - 1 zero planes, so X_{s-a} is plane s - a + na - 1).
-// Products are at most 2^14, so 512-term FP32 partial sums are exact; the
-// accumulator is folded into int32 registers every kFoldBlocks K-blocks as in
-// the product kernel (|Y_s| <= na n 2^14 <= 2^30 for na n <= kResidTcMaxK).
-// The epilogue combines each column's eight Y_s and writes r_{i+1};
-// k_lift_r16 then forms its balanced residues as f16, straight into the
-// product's B operand (R16 [E'][c][ld]).
-// CTA = 128 rows x 8 columns (MMA N = 64: limb-major, column-minor); warp
-// roles as in k_lift_gemm_tc; two CTAs per SM, so that one's epilogue
-// overlaps the other's main loop.
-constexpr int kRNT = 64;
-constexpr int kRCols = 8;
+// A x_i mod 2^64 on the tensor cores, for r_{i+1} = (r_i - A x_i) P'^{-1} mod
+// 2^64 (exact-solve card, §Method: the residual kept in one 64-bit limb).
+// With A = sum_a A_a 256^a and x_i = sum_t X_t 256^t (mod 2^64) in balanced
+// 8-bit limbs (|A_a|, |X_t| <= 128, exact in f16),
+//     A x_i = sum_a S_a (mod 2^64),   S_a = sum_{s < 8} 256^s A_a X_{s-a},
+// and each plane's S_a is one GEMM whose B operand rows (s, col) are
+// X_{s-a}[col]: one 3-D TMA box of 8 limb planes x NC columns from the X
+// planes, stored after na - 1 zero planes (X_{s-a} is plane s - a + na - 1).
+// CTA = (128 rows, NC columns, plane a): MMA M = 128, N = 8 NC (limb-major),
+// K = one plane (split K: the planes run in parallel).  Products are at most
+// 2^14, so 1024-term FP32 partial sums are exact (at most 2^24); every such
+// chunk the epilogue folds the accumulator into one 64-bit word per column,
+// S += sum_s 256^s y_s (mod 2^64), double-buffered in tensor memory so the
+// MMAs of the next chunk overlap the fold.  At the end each plane's S_a is
+// added into Sacc [n][c] (64-bit atomics: addition mod 2^64), which
+// k_lift_r16 turns into r_{i+1} and its residues and clears.
+constexpr int kR2Fold = 16;  // fold every 16 K-blocks (K = 1024)
+constexpr int kR2Threads = 192;
 
-__global__ void __launch_bounds__(kThreads, 2)
-    k_lift_resid_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX,
-                    const LiftConst* __restrict__ K, const int64_t* __restrict__ r, int64_t* __restrict__ rn,
-                    int n, int c, int na, int kbp, int* __restrict__ err) {
+template <int NC>
+struct R2Cfg {
+  static constexpr int N = 8 * NC;                  // MMA N
+  static constexpr int Stages = NC == 32 ? 4 : 3;   // 48 KB or 32 KB per stage
+  static constexpr int CtasPerSm = NC == 32 ? 1 : 2;
+  static constexpr uint32_t Cols = 2 * N;           // double-buffered accumulator
+  static constexpr size_t Smem = 1024 + (size_t)Stages * (kATileBytes + N * 128) + 256;
+};
+
+template <int NC>
+__global__ void __launch_bounds__(kR2Threads, R2Cfg<NC>::CtasPerSm)
+    k_lift_resid_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmX, int n, int c,
+                    int na, int kbp, uint64_t* __restrict__ Sacc, int* __restrict__ err) {
+  using Cfg = R2Cfg<NC>;
+  constexpr int N = Cfg::N, S_ = Cfg::Stages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kATileBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kRNT * 128);
-  uint64_t* empty = full + kStages;
-  uint64_t* accfull = empty + kStages;
+  uint8_t* sB = smem + S_ * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + S_ * N * 128);
+  uint64_t* empty = full + S_;
+  uint64_t* accfull = empty + S_;
   uint64_t* accempty = accfull + 2;
   uint64_t* drained = accempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM, col0 = blockIdx.y * kRCols;
-  const int kblocks = na * kbp;
-  const int nchunks = (kblocks + kFoldBlocks - 1) / kFoldBlocks;
-  constexpr uint32_t kCols = 2 * kRNT;
+  const int m0 = blockIdx.x * kBM, col0 = blockIdx.y * NC, a = blockIdx.z;
+  const int nchunks = (kbp + kR2Fold - 1) / kR2Fold;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S_; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
@@ -339,53 +345,56 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
-                 "r"(kCols));
+                 "r"(Cfg::Cols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *s_tmem;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *s_tmem, 0);
 
-  if (warp == 0) {
-    if (lane == 0) {  // TMA producer
-      int issued = 0;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages, a = kb / kbp, k0 = (kb - a * kbp) * kBK;
-        if (kb >= kStages && !mbar_wait(empty + s, ((kb / kStages) & 1) ^ 1, err, 1)) break;
-        mbar_expect_tx(full + s, kATileBytes + kRNT * 128);
-        tma_load_3d(sA + s * kATileBytes, &tmA, full + s, k0, m0, a);
-        tma_load_3d(sB + s * kRNT * 128, &tmX, full + s, k0, col0, na - 1 - a);
-        issued = kb + 1;
+  if (warp == 0) {  // TMA producer: the warp runs the loop, one elected lane issues
+    int issued = 0;
+    for (int kb = 0; kb < kbp; ++kb) {
+      const int s = kb % S_;
+      if (kb >= S_ && !mbar_wait_warp(empty + s, ((kb / S_) & 1) ^ 1, err, 1)) break;
+      if (elect_one()) {
+        mbar_expect_tx(full + s, kATileBytes + N * 128);
+        tma_load_3d(sA + s * kATileBytes, &tmA, full + s, kb * kBK, m0, a);
+        tma_load_3d(sB + s * N * 128, &tmX, full + s, kb * kBK, col0, na - 1 - a);
       }
-      drain_loads(full, issued, kStages);
+      __syncwarp();
+      issued = kb + 1;
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer
-      const uint32_t idesc = (1u << 4) | ((uint32_t)(kRNT >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % kStages, ch = kb / kFoldBlocks, buf = ch & 1;
-        const bool first = (kb % kFoldBlocks) == 0;
-        if (first && ch >= 2 && !mbar_wait(accempty + buf, ((ch - 2) >> 1) & 1, err, 2)) break;
-        if (!mbar_wait(full + s, (kb / kStages) & 1, err, 3)) break;
-        tc_fence_after();
-        const uint64_t ad = desc_sw128(sA + s * kATileBytes), bd = desc_sw128(sB + s * kRNT * 128);
+    drain_loads(full, issued, S_);
+  } else if (warp == 1) {  // MMA issuer: the warp runs the loop, one elected lane issues
+    const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+    for (int kb = 0; kb < kbp; ++kb) {
+      const int s = kb % S_, ch = kb / kR2Fold, buf = ch & 1;
+      const bool first = (kb % kR2Fold) == 0;
+      if (first && ch >= 2 && !mbar_wait_warp(accempty + buf, ((ch - 2) >> 1) & 1, err, 2)) break;
+      if (!mbar_wait_warp(full + s, (kb / S_) & 1, err, 3)) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t ad = desc_sw128(sA + s * kATileBytes), bd = desc_sw128(sB + s * N * 128);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k)
-          mma_f16(tmem + buf * kRNT, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
+          mma_f16(tmem + buf * N, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
         mma_commit(empty + s);
-        if ((kb % kFoldBlocks) == kFoldBlocks - 1 || kb == kblocks - 1) mma_commit(accfull + buf);
+        if ((kb % kR2Fold) == kR2Fold - 1 || kb == kbp - 1) mma_commit(accfull + buf);
       }
-      // every MMA issued has completed before tensor memory is released
-      mma_commit(drained);
-      mbar_wait_drain(drained, 0);
+      __syncwarp();
     }
-  } else {  // epilogue warpgroup
+    // every MMA issued has completed before tensor memory is released
+    if (elect_one()) mma_commit(drained);
+    __syncwarp();
+    mbar_wait_drain(drained, 0);
+  } else {  // epilogue warpgroup (warps 2..5)
     const int quarter = warp & 3;
     const int row = m0 + 32 * quarter + lane;
-    int32_t acc[kRNT];
+    uint64_t S[NC];
 #pragma unroll
-    for (int t = 0; t < kRNT; ++t) acc[t] = 0;
+    for (int t = 0; t < NC; ++t) S[t] = 0;
     bool ok = true;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int buf = ch & 1;
@@ -394,26 +403,22 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       tc_fence_after();
+#pragma unroll 1
+      for (int s8 = 0; s8 < 8; ++s8) {
+        float f[NC];
+        tmem_ld<NC>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * N + s8 * NC), f);
 #pragma unroll
-      for (int c16 = 0; c16 < kRNT / 16; ++c16) {
-        float f[16];
-        tmem_ld<16>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kRNT + 16 * c16), f);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) acc[16 * c16 + t] += __float2int_rn(f[t]);
+        for (int t = 0; t < NC; ++t) S[t] += (uint64_t)(int64_t)__float2int_rn(f[t]) << (8 * s8);
       }
       tc_fence_before();
       mbar_arrive(accempty + buf);
     }
     if (ok && row < n) {
-      const uint64_t pinv = K->Pinv64;
 #pragma unroll
-      for (int cl = 0; cl < kRCols; ++cl) {
+      for (int cl = 0; cl < NC; ++cl) {
         const int col = col0 + cl;
         if (col >= c) break;
-        uint64_t S = 0;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) S += (uint64_t)(int64_t)acc[s * kRCols + cl] << (8 * s);
-        rn[(int64_t)row * c + col] = (int64_t)(((uint64_t)r[(int64_t)row * c + col] - S) * pinv);
+        atomicAdd(reinterpret_cast<unsigned long long*>(Sacc + (int64_t)row * c + col), (unsigned long long)S[cl]);
       }
     }
   }
@@ -421,16 +426,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Cfg::Cols));
   }
 }
 
-// R16[e][col][i] = balanced residue of r_{i+1}[i][col] mod q_e, as f16; one
-// thread per entry, rows fastest so that the stores of a prime are coalesced.
-// The residual is usually far inside the int32 range (|r_{i+1}| < n max|A| / 2
-// + 1 once the first step is done), so a CTA whose entries all fit takes the
-// one-Barrett path; the reduction constants come from shared memory.
-__global__ void __launch_bounds__(256) k_lift_r16(const int64_t* __restrict__ rn, int64_t n, int64_t c, int64_t ld,
+// r_{i+1} = (r_i - A x_i) P'^{-1} mod 2^64 from Sacc = A x_i mod 2^64 (which is
+// cleared for the next step), and R16[e][col][i] = its balanced residue mod
+// q_e as f16; one thread per entry, rows fastest so that the stores of a prime
+// are coalesced.  The residual is usually far inside the int32 range
+// (|r_{i+1}| < n max|A| / 2 + 1 once the first step is done), so a CTA whose
+// entries all fit takes the one-Barrett path; the reduction constants come
+// from shared memory.
+__global__ void __launch_bounds__(256) k_lift_r16(const int64_t* __restrict__ r, uint64_t* __restrict__ Sacc,
+                                                  int64_t* __restrict__ rn, int64_t n, int64_t c, int64_t ld,
                                                   const LiftConst* __restrict__ K, __half* __restrict__ R16) {
   __shared__ ModQ sm[kNumPrimes];
   const int E = K->E;
@@ -438,7 +446,13 @@ __global__ void __launch_bounds__(256) k_lift_r16(const int64_t* __restrict__ rn
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const bool live = t < n * c;
   const int64_t col = live ? t / n : 0, i = live ? t - col * n : 0;
-  const int64_t v = live ? rn[i * c + col] : 0;
+  int64_t v = 0;
+  if (live) {
+    const int64_t at = i * c + col;
+    v = (int64_t)(((uint64_t)r[at] - Sacc[at]) * K->Pinv64);
+    rn[at] = v;
+    Sacc[at] = 0;
+  }
   // -2^31 < v < 2^31 - 256: the signed 32-bit reduction applies
   const bool narrow = __syncthreads_and(v > -(int64_t(1) << 31) && v < (int64_t(1) << 31) - 256);
   if (!live) return;
@@ -497,18 +511,6 @@ __global__ void k_to_f16(const int8_t* __restrict__ src, __half* __restrict__ ds
   }
 }
 
-int sm_count() {
-  static int count = 0;
-  if (!count) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      count = v;
-    else
-      return 1;
-  }
-  return count;
-}
 
 template <int NT>
 es_status launch_nt(const CUtensorMap& mB, const CUtensorMap& mR, const LiftConst* K, int8_t* V, int64_t n,
@@ -578,21 +580,36 @@ es_status tc_resid_prepare(TcResid* t, const int64_t* A_dev, void* A16, void* X1
   count_launch();
   ES_CHECK(cuda_status(cudaGetLastError(), "k_a_limbs"));
   ES_CHECK(cuda_status(cudaMemsetAsync(X16, 0, (size_t)(na + 7) * c * ld * 2, st), "memset x limbs"));
+  // 32 columns per CTA (MMA N = 256) while that still gives at least one CTA
+  // per SM, else 16 (N = 128, two CTAs per SM)
+  const int64_t tiles_m = (n + kBM - 1) / kBM;
+  t->nc = tiles_m * ((c + 31) / 32) * na >= sm_count() ? 32 : 16;
   ES_CHECK(make_map(&t->mapA, A16, ld, n, na, kBM));
-  ES_CHECK(make_map(&t->mapX, X16, ld, c, na + 7, kRCols, 8));
+  ES_CHECK(make_map(&t->mapX, X16, ld, c, na + 7, t->nc, 8));
   return ES_OK;
 }
 
-es_status tc_resid_launch(const TcResid& t, const LiftConst* K, const int64_t* r, int64_t* rn, void* R16, int64_t n,
-                          int64_t c, int64_t ld, int* err, void* stream) {
-  cudaStream_t st = (cudaStream_t)stream;
-  const size_t smem = 1024 + (size_t)kStages * (kATileBytes + kRNT * 128) + 256;
-  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_lift_resid_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+namespace {
+template <int NC>
+es_status launch_resid(const TcResid& t, uint64_t* Sacc, int64_t n, int64_t c, int* err, cudaStream_t st) {
+  const size_t smem = R2Cfg<NC>::Smem;
+  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_lift_resid_tc<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)smem),
                        "tc resid smem attribute"));
-  dim3 grid((unsigned)((n + kBM - 1) / kBM), (unsigned)((c + kRCols - 1) / kRCols));
-  k_lift_resid_tc<<<grid, kThreads, smem, st>>>(t.mapA, t.mapX, K, r, rn, (int)n, (int)c, t.na, t.kbp, err);
-  ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_resid_tc"));
-  k_lift_r16<<<(unsigned)((n * c + 255) / 256), 256, 0, st>>>(rn, n, c, ld, K, (__half*)R16);
+  dim3 grid((unsigned)((n + kBM - 1) / kBM), (unsigned)((c + NC - 1) / NC), (unsigned)t.na);
+  k_lift_resid_tc<NC><<<grid, kR2Threads, smem, st>>>(t.mapA, t.mapX, (int)n, (int)c, t.na, t.kbp, Sacc, err);
+  return cuda_status(cudaGetLastError(), "k_lift_resid_tc");
+}
+}  // namespace
+
+es_status tc_resid_launch(const TcResid& t, const LiftConst* K, const int64_t* r, int64_t* rn, uint64_t* Sacc,
+                          void* R16, int64_t n, int64_t c, int64_t ld, int* err, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (t.nc == 32)
+    ES_CHECK(launch_resid<32>(t, Sacc, n, c, err, st));
+  else
+    ES_CHECK(launch_resid<16>(t, Sacc, n, c, err, st));
+  k_lift_r16<<<(unsigned)((n * c + 255) / 256), 256, 0, st>>>(r, Sacc, rn, n, c, ld, K, (__half*)R16);
   count_launch(2);
   return cuda_status(cudaGetLastError(), "k_lift_r16");
 }

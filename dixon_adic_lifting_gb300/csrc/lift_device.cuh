@@ -9,8 +9,15 @@ namespace es {
 // The digit from the word sums acc (S = sum_e c_e P'/q_e as 12 base-2^32
 // columns) and the fixed-point estimate tf of floor(S / P'): normalise,
 // subtract t P', one conditional subtraction of P', then the balanced shift.
+__device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uint64_t tf, const uint32_t* Pw,
+                                           const uint32_t* Phw, uint32_t (&S)[kCrtWords]);
 __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uint64_t tf,
                                            const LiftConst* __restrict__ K, uint32_t (&S)[kCrtWords]) {
+  crt_finish(acc, tf, K->P, K->Phalf, S);
+}
+// P' and (P' - 1) / 2 as 32-bit words, read from Pw and Phw (global or shared).
+__device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uint64_t tf, const uint32_t* Pw,
+                                           const uint32_t* Phw, uint32_t (&S)[kCrtWords]) {
   uint64_t carry = 0;
 #pragma unroll
   for (int l = 0; l < kCrtWords; ++l) {
@@ -24,7 +31,7 @@ __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uin
   int64_t borrow = 0;
 #pragma unroll
   for (int l = 0; l < kCrtWords; ++l) {
-    uint64_t prod = (uint64_t)tq * K->P[l] + mc;
+    uint64_t prod = (uint64_t)tq * Pw[l] + mc;
     mc = prod >> 32;
     int64_t d = (int64_t)S[l] - (int64_t)(uint32_t)prod + borrow;
     S[l] = (uint32_t)d;
@@ -34,8 +41,8 @@ __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uin
   bool ge = true;
 #pragma unroll
   for (int l = kCrtWords - 1; l >= 0; --l) {
-    if (S[l] != K->P[l]) {
-      ge = S[l] > K->P[l];
+    if (S[l] != Pw[l]) {
+      ge = S[l] > Pw[l];
       break;
     }
   }
@@ -43,7 +50,7 @@ __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uin
     borrow = 0;
 #pragma unroll
     for (int l = 0; l < kCrtWords; ++l) {
-      int64_t d = (int64_t)S[l] - (int64_t)K->P[l] + borrow;
+      int64_t d = (int64_t)S[l] - (int64_t)Pw[l] + borrow;
       S[l] = (uint32_t)d;
       borrow = d >> 32;
     }
@@ -52,8 +59,8 @@ __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uin
   bool gt = false;
 #pragma unroll
   for (int l = kCrtWords - 1; l >= 0; --l) {
-    if (S[l] != K->Phalf[l]) {
-      gt = S[l] > K->Phalf[l];
+    if (S[l] != Phw[l]) {
+      gt = S[l] > Phw[l];
       break;
     }
   }
@@ -61,7 +68,7 @@ __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uin
     borrow = 0;
 #pragma unroll
     for (int l = 0; l < kCrtWords; ++l) {
-      int64_t d = (int64_t)S[l] - (int64_t)K->P[l] + borrow;
+      int64_t d = (int64_t)S[l] - (int64_t)Pw[l] + borrow;
       S[l] = (uint32_t)d;
       borrow = d >> 32;
     }

@@ -10,6 +10,8 @@
 
 namespace es {
 
+constexpr int kCrtNTiles = 7;  // 56 byte columns of the CRT product
+
 struct LiftConst {
   int32_t E;                      // number of good primes
   int32_t pidx[kNumPrimes];       // their indices in the prime table, ascending
@@ -21,6 +23,13 @@ struct LiftConst {
   uint32_t P[kCrtWords];          // P'
   uint32_t Phalf[kCrtWords];      // (P' - 1) / 2
   uint64_t Pinv64;                // P'^{-1} mod 2^64
+  // The CRT as one small matrix product (k_lift_crt_mma): with c_e in [0, q_e)
+  // the digit's word sums are sum_e c_e P'/q_e, and the fixed-point quotient
+  // estimate is sum_e c_e floor(2^50/q_e).  Byte columns 0..41 hold the bytes
+  // of P'/q_e, columns 42..48 those of floor(2^50/q_e), 49..55 are zero; rows
+  // are the primes (zero from E').  Stored as the B fragments of mma.sync
+  // m16n8k16 (f16 pairs): [n-tile 7][k-step 4][lane 32][register 2].
+  uint32_t crt_bfrag[kCrtNTiles][4][32][2];
 };
 
 // tcgen05 lift product (k_lift_tc.cu), used for c >= 16.  It reads the
@@ -43,7 +52,8 @@ es_status tc_launch(const TcLift& t, const LiftConst* K, int8_t* V, int64_t n, i
 
 // tcgen05 residual update (k_lift_tc.cu), used with the tcgen05 product when
 // max|A| < 2^31: A and x_i mod 2^64 in balanced 8-bit limbs, A x_i mod 2^64
-// as one f16 GEMM.
+// as f16 GEMMs (one per limb plane of A) summed into Sacc [n][c] (zero on
+// entry, cleared again once r_{i+1} is formed).
 constexpr int kResidLimbsMax = 4;      // limbs of A (|A| < 2^31)
 constexpr int64_t kResidTcMaxK = 65536;  // na n at most this: int32 sums stay exact
 struct TcResid {
@@ -51,12 +61,13 @@ struct TcResid {
   CUtensorMap mapX;  // f16 [na + 7][c][ld]  limbs of x_i mod 2^64 on planes na - 1 .. na + 6, the rest zero
   int na = 0;        // limbs of A
   int kbp = 0;       // 64-wide K blocks per limb plane
+  int nc = 32;       // columns per CTA (MMA N = 8 nc)
 };
 int resid_limbs(uint64_t max_abs_a);  // na for entries up to max_abs_a (0: not representable)
 es_status tc_resid_prepare(TcResid* t, const int64_t* A_dev, void* A16, void* X16, int64_t n, int64_t c, int64_t ld,
                            int na, void* stream);
-es_status tc_resid_launch(const TcResid& t, const LiftConst* K, const int64_t* r, int64_t* rn, void* R16, int64_t n,
-                          int64_t c, int64_t ld, int* err, void* stream);
+es_status tc_resid_launch(const TcResid& t, const LiftConst* K, const int64_t* r, int64_t* rn, uint64_t* Sacc,
+                          void* R16, int64_t n, int64_t c, int64_t ld, int* err, void* stream);
 
 constexpr int kFusedErrDigit = 15;  // error code: the fused lift's two digit paths disagreed
 
