@@ -22,6 +22,7 @@
 // word column sums (64-bit accumulators plus carry counts), normalised, and
 // reduced mod Q by Barrett's method with a 13-word reciprocal; then the sign
 // is balanced and |N| <= 2^num_bits is tested.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <memory>
@@ -29,12 +30,14 @@
 
 #include <algorithm>
 #include <cstring>
+#include <string>
 #include <vector>
 
 #include "bigint.h"
 #include "es_common.cuh"
 #include "es_internal.h"
 #include "recon_common.h"
+#include "tc_common.cuh"
 
 namespace es {
 
@@ -80,76 +83,19 @@ __device__ __forceinline__ void mac96(uint32_t (&acc)[3], uint32_t x, uint32_t y
       : "r"(x), "r"(y));
 }
 
-__global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
-  const int64_t k = blockIdx.x;
-  const int mp = p.mp, LG = p.LG, LZ = LG + kZExtra;
+// From the normalised words Zn[0 .. LG + kZExtra) of Z (in shared memory, Z <
+// b^(LG + 11)): N = bal_Q(Z mod Q) by Barrett's method with the 13-word
+// reciprocal, the acceptance test |N| <= 2^nb, and the two's complement
+// output of component k.  Zlo / Zhi are shared scratch of LG + 1 entries.
+// Called by every thread of the CTA (it synchronises).
+__device__ __forceinline__ void numerator_tail(const RParams& p, int64_t k, uint32_t* Zn, uint64_t* Zlo,
+                                               uint32_t* Zhi) {
+  const int LG = p.LG;
   const int tid = threadIdx.x, nt = blockDim.x;
-  extern __shared__ __align__(16) unsigned char sm[];
-  uint64_t* Zlo = reinterpret_cast<uint64_t*>(sm);          // LZ + 1
-  uint32_t* Zhi = reinterpret_cast<uint32_t*>(Zlo + LZ + 1);  // LZ + 1
-  uint32_t* Zn = Zhi + LZ + 1;                              // LZ + 1
-  uint32_t* xs = Zn + LZ + 1;                               // mp * 12
   __shared__ uint32_t qh[kMuWords];
   __shared__ int s_ok, s_neg, s_z;
-
-  // shifted digits x'_i = x_i + (P'-1)/2  (384-bit two's complement add)
-  for (int i = tid; i < mp; i += nt) {
-    const uint32_t* src = p.D + ((size_t)i * (size_t)p.nc + (size_t)k) * kDigitWords;
-    uint64_t carry = 0;
-#pragma unroll
-    for (int l = 0; l < kDigitWords; ++l) {
-      uint64_t s = (uint64_t)src[l] + p.H12[l] + carry;
-      xs[i * kDigitWords + l] = (uint32_t)s;
-      carry = s >> 32;
-    }
-  }
-  __syncthreads();
-  // Z word columns: Z[w] = OFF[w] + sum_i sum_l x'_i[l] G_i[w - l].  A thread
-  // owns 4 consecutive columns: per digit it loads the 16 words of G_i they
-  // need (4 aligned 16-byte loads) and the digit's 12 words, then 48 96-bit MACs.
-  for (int w0 = 4 * tid; w0 < LZ; w0 += 4 * nt) {
-    uint32_t acc[4][3];
-#pragma unroll
-    for (int o = 0; o < 4; ++o) {
-      acc[o][0] = w0 + o < LG ? p.OFF[w0 + o] : 0u;
-      acc[o][1] = 0u;
-      acc[o][2] = 0u;
-    }
-    for (int i = 0; i < mp; ++i) {
-      const uint4* gr = reinterpret_cast<const uint4*>(p.G + (size_t)i * p.GS + kGPad + w0 - 12);
-      const uint4* xr = reinterpret_cast<const uint4*>(xs + i * kDigitWords);
-      uint32_t g[16], x[kDigitWords];
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint4 v = __ldg(gr + h);
-        g[4 * h] = v.x, g[4 * h + 1] = v.y, g[4 * h + 2] = v.z, g[4 * h + 3] = v.w;
-      }
-#pragma unroll
-      for (int h = 0; h < kDigitWords / 4; ++h) {
-        const uint4 v = xr[h];
-        x[4 * h] = v.x, x[4 * h + 1] = v.y, x[4 * h + 2] = v.z, x[4 * h + 3] = v.w;
-      }
-#pragma unroll
-      for (int o = 0; o < 4; ++o)
-#pragma unroll
-        for (int l = 0; l < kDigitWords; ++l) mac96(acc[o], x[l], g[o + 12 - l]);
-    }
-#pragma unroll
-    for (int o = 0; o < 4; ++o)
-      if (w0 + o < LZ) {
-        Zlo[w0 + o] = (uint64_t)acc[o][0] | ((uint64_t)acc[o][1] << 32);
-        Zhi[w0 + o] = acc[o][2];
-      }
-  }
   __syncthreads();
   if (tid == 0) {
-    // normalise the columns into 32-bit words
-    uint64_t carry = 0;
-    for (int w = 0; w < LZ; ++w) {
-      unsigned __int128 s = (unsigned __int128)Zlo[w] + ((unsigned __int128)Zhi[w] << 64) + carry;
-      Zn[w] = (uint32_t)s;
-      carry = (uint64_t)(s >> 32);
-    }
     // q^ = floor(Z1 MU / b^13) with Z1 = floor(Z / b^(LG-1)) (13 words)
     uint32_t prod[2 * kMuWords];
     for (int t = 0; t < 2 * kMuWords; ++t) prod[t] = 0;
@@ -261,6 +207,443 @@ __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
   if (tid == 0) p.ok[k] = (uint8_t)s_ok;
 }
 
+
+__global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
+  const int64_t k = blockIdx.x;
+  const int mp = p.mp, LG = p.LG, LZ = LG + kZExtra;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  extern __shared__ __align__(16) unsigned char sm[];
+  uint64_t* Zlo = reinterpret_cast<uint64_t*>(sm);          // LZ + 1
+  uint32_t* Zhi = reinterpret_cast<uint32_t*>(Zlo + LZ + 1);  // LZ + 1
+  uint32_t* Zn = Zhi + LZ + 1;                              // LZ + 1
+  uint32_t* xs = Zn + LZ + 1;                               // mp * 12
+
+  // shifted digits x'_i = x_i + (P'-1)/2  (384-bit two's complement add)
+  for (int i = tid; i < mp; i += nt) {
+    const uint32_t* src = p.D + ((size_t)i * (size_t)p.nc + (size_t)k) * kDigitWords;
+    uint64_t carry = 0;
+#pragma unroll
+    for (int l = 0; l < kDigitWords; ++l) {
+      uint64_t s = (uint64_t)src[l] + p.H12[l] + carry;
+      xs[i * kDigitWords + l] = (uint32_t)s;
+      carry = s >> 32;
+    }
+  }
+  __syncthreads();
+  // Z word columns: Z[w] = OFF[w] + sum_i sum_l x'_i[l] G_i[w - l].  A thread
+  // owns 4 consecutive columns: per digit it loads the 16 words of G_i they
+  // need (4 aligned 16-byte loads) and the digit's 12 words, then 48 96-bit MACs.
+  for (int w0 = 4 * tid; w0 < LZ; w0 += 4 * nt) {
+    uint32_t acc[4][3];
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      acc[o][0] = w0 + o < LG ? p.OFF[w0 + o] : 0u;
+      acc[o][1] = 0u;
+      acc[o][2] = 0u;
+    }
+    for (int i = 0; i < mp; ++i) {
+      const uint4* gr = reinterpret_cast<const uint4*>(p.G + (size_t)i * p.GS + kGPad + w0 - 12);
+      const uint4* xr = reinterpret_cast<const uint4*>(xs + i * kDigitWords);
+      uint32_t g[16], x[kDigitWords];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint4 v = __ldg(gr + h);
+        g[4 * h] = v.x, g[4 * h + 1] = v.y, g[4 * h + 2] = v.z, g[4 * h + 3] = v.w;
+      }
+#pragma unroll
+      for (int h = 0; h < kDigitWords / 4; ++h) {
+        const uint4 v = xr[h];
+        x[4 * h] = v.x, x[4 * h + 1] = v.y, x[4 * h + 2] = v.z, x[4 * h + 3] = v.w;
+      }
+#pragma unroll
+      for (int o = 0; o < 4; ++o)
+#pragma unroll
+        for (int l = 0; l < kDigitWords; ++l) mac96(acc[o], x[l], g[o + 12 - l]);
+    }
+#pragma unroll
+    for (int o = 0; o < 4; ++o)
+      if (w0 + o < LZ) {
+        Zlo[w0 + o] = (uint64_t)acc[o][0] | ((uint64_t)acc[o][1] << 32);
+        Zhi[w0 + o] = acc[o][2];
+      }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // normalise the columns into 32-bit words
+    uint64_t carry = 0;
+    for (int w = 0; w < LZ; ++w) {
+      unsigned __int128 s = (unsigned __int128)Zlo[w] + ((unsigned __int128)Zhi[w] << 64) + carry;
+      Zn[w] = (uint32_t)s;
+      carry = (uint64_t)(s >> 32);
+    }
+  }
+  numerator_tail(p, k, Zn, Zlo, Zhi);
+}
+
+// ------------------------------------------------------------------ tensor cores
+// The numerators' products on the 5th-generation tensor cores.  With x_i the
+// balanced digits of component k and G_i = d P'^i mod Q,
+//     Z_k = sum_{i < m'} x_i G_i = sum_p 256^p S_p,
+//     S_p = sum_i sum_{b < 48} X_i[b] G_i[p - b],
+// where X_i[b] are the balanced bytes (in [-128, 127]) of x_i and G_i[u] those
+// of G_i.  Over all components this is one GEMM: M = components, N = byte
+// columns p, K = (digit, byte) = 48 m'; each product is at most 2^14, so the
+// FP32 accumulator is exact over 1008 terms (21 digits) and is folded into
+// int32 (|S_p| <= 48 m' 2^14 < 2^31 for m' < 2730).
+//
+// The B operand is Toeplitz: with b' = 47 - b (A's bytes reversed), row p of
+// B holds G_i[p - 47 + b'].  In the canonical K-major layout without swizzle
+// (core matrices of 8 rows x 16 bytes), the core matrix of rows 8q .. 8q + 7
+// and K elements 8s .. 8s + 7 is, with T[j][r][e] = G_i[8 j + r + 1 + e] as
+// f16, exactly T[j] for j = q + s - 6 (plus the tile's offset): a matrix
+// descriptor whose two core-matrix strides are both 128 bytes reads B
+// straight from one contiguous 128-byte-per-unit copy of T.  T is built once
+// per digit (8 f16 per byte of G_i, all of it resident in L2) and each stage
+// loads the 21 units a 128-column tile needs.
+//
+// CTA tile = 128 components (MMA M, A operand in tensor memory: four
+// converter warps widen each component's 48 digit bytes, balanced and
+// reversed, with tcgen05.st) x 128 byte columns (MMA N); a stage is one digit
+// (three K = 16 MMAs).  Persistent CTAs walk the tiles with the byte-column
+// tile fastest, so the CTAs running together share a component tile and its
+// digits stay in L2.  The epilogue (eight warps) folds each 21-digit chunk
+// into int32 column sums, and at the tile's end normalises each component's
+// 128 columns into 128 bytes plus a signed carry.  k_recon_finish then adds
+// the tiles, reduces mod Q and writes the numerator.
+namespace rg {
+constexpr int kM = 128;                     // components per tile
+constexpr int kN = 128;                     // byte columns per tile
+constexpr int kDig = 48;                    // bytes per digit (K per stage)
+constexpr int kStages = 8;
+constexpr int kXBytes = kM * kDig;          // 6144
+constexpr int kUnits = kN / 8 + kDig / 8 - 1;  // 21 core-matrix units per window
+constexpr int kTBytes = kUnits * 128;       // 2688
+constexpr int kFold = 21;                   // digits per exact FP32 chunk (1008 K)
+constexpr uint32_t kColA = 2 * kN;          // A slots after the two accumulators
+constexpr uint32_t kTmemCols = 512;
+constexpr int kZStride = kN + 1;            // words per row of the epilogue's staging (odd)
+constexpr int kThreads = 448;               // producer, MMA, 4 converter and 8 epilogue warps
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kXBytes + kTBytes) + (size_t)kM * kZStride * 4 + 512;
+static_assert(kColA + 32 * kStages <= kTmemCols, "tensor memory");
+}  // namespace rg
+
+struct GParams {
+  const uint8_t* X;    // digits as bytes: [m][nc][48]
+  const uint8_t* T;    // [mp][NU][128]: f16 T units of every digit
+  int64_t nc;
+  int mp, NP, NU;
+  int tiles;           // comp tiles x NP
+  uint8_t* Zb;         // [nc][NP * 128] normalised bytes
+  int32_t* Zc;         // [nc][NP]       carry out of each tile
+  int* err;
+};
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
+}
+// K-major, no swizzle: core matrices of 8 rows x 16 bytes, `lbo` bytes apart
+// along K and `sbo` bytes apart along M/N.
+__device__ __forceinline__ uint64_t desc_interleave(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (saddr >> 4) & 0x3FFFull;
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version; base offset 0, no swizzle
+  return d;
+}
+// f16 pairs of byte - 128 for the four unsigned bytes of w: 0x64uu is the f16
+// 1024 + uu, and 1024 + uu - 1152 = uu - 128 exactly.
+__device__ __forceinline__ void u8x4_m128_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(w, 0x64646464u, 0x4140);
+  hi = __byte_perm(w, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+// T[i][u][r][e] = G_i[8 (u - 6) + r + 1 + e] as f16 (zero outside the bytes of
+// G_i), from the balanced bytes Gb [mp][LGB1]; one thread per 16-byte row.
+__global__ void k_recon_tbuild(const int8_t* __restrict__ Gb, int64_t LGB1, int NU, int mp,
+                               uint8_t* __restrict__ T) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)mp * NU * 8) return;
+  const int r = (int)(t & 7);
+  const int64_t ui = t >> 3, i = ui / NU, u = ui - i * NU;
+  const int64_t base = 8 * (u - 6) + r + 1;
+  uint32_t w[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    uint32_t pr = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int64_t idx = base + 2 * h + q;
+      const int v = (idx >= 0 && idx < LGB1) ? (int)Gb[i * LGB1 + idx] : 0;
+      pr |= (uint32_t)__half_as_ushort(__int2half_rn(v)) << (16 * q);
+    }
+    w[h] = pr;
+  }
+  reinterpret_cast<uint4*>(T)[t] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
+  using namespace rg;
+  using namespace tc;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sX = smem;                                   // [S][128][48] digit bytes
+  uint8_t* sT = sX + kStages * kXBytes;                 // [S][21][128] T windows
+  int32_t* sZ = reinterpret_cast<int32_t*>(sT + kStages * kTBytes);  // [128][129]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sZ + kM * kZStride);
+  uint64_t* conv = full + kStages;
+  uint64_t* empty = conv + kStages;
+  uint64_t* accfull = empty + kStages;
+  uint64_t* accempty = accfull + 2;
+  uint64_t* drained = accempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mp = p.mp, nch = (mp + kFold - 1) / kFold;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(conv + s, 128);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accfull + b, 1);
+      mbar_init(accempty + b, 256);
+    }
+    mbar_init(drained, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *s_tmem, 0);
+  int* err = p.err;
+
+  if (warp == 0) {  // producer: the digit bytes of the tile's components and the T window, per digit
+    int g = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
+      const int ct = t / p.NP, pt = t - ct * p.NP;
+      const int64_t c0 = (int64_t)ct * kM;
+      const uint32_t cnt = (uint32_t)(p.nc - c0 < kM ? p.nc - c0 : kM);
+      for (int i = 0; i < mp; ++i, ++g) {
+        const int s = g % kStages;
+        if (g >= kStages && !mbar_wait_warp(empty + s, ((g / kStages) & 1) ^ 1, err, 21)) {
+          stop = true;
+          break;
+        }
+        if (elect_one()) {
+          mbar_expect_tx(full + s, cnt * kDig + kTBytes);
+          bulk_g2s(sX + s * kXBytes, p.X + ((int64_t)i * p.nc + c0) * kDig, cnt * kDig, full + s);
+          bulk_g2s(sT + s * kTBytes, p.T + ((int64_t)i * p.NU + 16 * pt) * 128, kTBytes, full + s);
+        }
+        __syncwarp();
+      }
+    }
+    for (int k = g > kStages ? g - kStages : 0; k < g; ++k) mbar_wait_drain(full + k % kStages, (k / kStages) & 1);
+  } else if (warp == 1) {  // MMA issuer
+    const uint32_t idesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+    int g = 0, gc = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
+      for (int i = 0; i < mp; ++i, ++g) {
+        const int s = g % kStages, buf = gc & 1;
+        const bool first = (i % kFold) == 0;
+        if (first && gc >= 2 && !mbar_wait_warp(accempty + buf, ((gc - 2) >> 1) & 1, err, 22)) {
+          stop = true;
+          break;
+        }
+        if (!mbar_wait_warp(full + s, (g / kStages) & 1, err, 23) ||
+            !mbar_wait_warp(conv + s, (g / kStages) & 1, err, 24)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t tb = smem_u32(sT + s * kTBytes);
+#pragma unroll
+          for (int k = 0; k < kDig / 16; ++k)
+            mma_f16_ta(tmem + buf * kN, tmem + kColA + 32 * s + 8 * k, desc_interleave(tb + 256 * k, 128, 128),
+                       idesc, (first && k == 0) ? 0u : 1u);
+          mma_commit(empty + s);
+          if (i % kFold == kFold - 1 || i == mp - 1) mma_commit(accfull + buf);
+        }
+        __syncwarp();
+        if (i % kFold == kFold - 1 || i == mp - 1) ++gc;
+      }
+    }
+    if (elect_one()) mma_commit(drained);
+    __syncwarp();
+    mbar_wait_drain(drained, 0);
+  } else if (warp < 6) {
+    // converters: warp w touches tensor-memory lanes 32 (w % 4) .. + 31; thread =
+    // one component (row): its 48 digit bytes, balanced (bytes of x + 0x80..80,
+    // less 128) and reversed (A's element b' = byte 47 - b'), as 24 columns
+    const int quarter = warp & 3, r = 32 * quarter + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
+    int g = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
+      const int ct = t / p.NP;
+      const bool live = (int64_t)ct * kM + r < p.nc;
+      for (int i = 0; i < mp; ++i, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait_warp(full + s, (g / kStages) & 1, err, 25)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t wv[24];
+        if (live) {
+          const uint4* src = reinterpret_cast<const uint4*>(sX + s * kXBytes + r * kDig);
+          const uint4 v0 = src[0], v1 = src[1], v2 = src[2];
+          // x + 0x8080...80 over 384 bits
+          uint64_t w64[6] = {(uint64_t)v0.x | ((uint64_t)v0.y << 32), (uint64_t)v0.z | ((uint64_t)v0.w << 32),
+                             (uint64_t)v1.x | ((uint64_t)v1.y << 32), (uint64_t)v1.z | ((uint64_t)v1.w << 32),
+                             (uint64_t)v2.x | ((uint64_t)v2.y << 32), (uint64_t)v2.z | ((uint64_t)v2.w << 32)};
+          uint32_t cy = 0;
+#pragma unroll
+          for (int l = 0; l < 6; ++l) {
+            const uint64_t a = w64[l] + 0x8080808080808080ull, b = a + cy;
+            cy = (a < w64[l] || b < a) ? 1u : 0u;
+            w64[l] = b;
+          }
+          // reversed bytes: word k' of the reversal = bytes 47 - 4k' .. 44 - 4k'
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk) {
+            const int src_w = 11 - kk;
+            const uint32_t word = (uint32_t)(w64[src_w >> 1] >> (32 * (src_w & 1)));
+            u8x4_m128_to_f16(__byte_perm(word, 0, 0x0123), wv[2 * kk], wv[2 * kk + 1]);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 24; ++kk) wv[kk] = 0;
+        }
+        uint32_t lo[16], hi[8];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) lo[kk] = wv[kk];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) hi[kk] = wv[16 + kk];
+        tmem_st16(trow + kColA + 32 * s, lo);
+        tmem_st8(trow + kColA + 32 * s + 16, hi);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(conv + s);
+      }
+    }
+  } else {
+    // epilogue: warp w folds columns 64 h .. 64 h + 63 (h = (w - 6) / 4) of the
+    // rows of lane quarter w % 4; at a tile's end the rows are normalised into
+    // bytes and a carry through the staging area
+    const int quarter = warp & 3, h = (warp - 6) >> 2, r = 32 * quarter + lane;
+    int gc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+      const int ct = t / p.NP, pt = t - ct * p.NP;
+      int32_t acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0;
+      for (int ch = 0; ch < nch; ++ch, ++gc) {
+        const int buf = gc & 1;
+        if (!mbar_wait(accfull + buf, (gc >> 1) & 1, err, 26)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c16 = 0; c16 < 4; ++c16) {
+          float f[16];
+          tmem_ld<16>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(buf * kN + 64 * h + 16 * c16), f);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[16 * c16 + j] += __float2int_rn(f[j]);
+        }
+        tc_fence_before();
+        mbar_arrive(accempty + buf);
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) sZ[r * kZStride + 64 * h + j] = acc[j];
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const int64_t comp = (int64_t)ct * kM + r;
+      if (h == 0 && comp < p.nc) {
+        int64_t carry = 0;
+        uint8_t* zb = p.Zb + (comp * p.NP + pt) * kN;
+#pragma unroll 1
+        for (int q = 0; q < kN / 16; ++q) {
+          uint32_t wd[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int64_t v = (int64_t)sZ[r * kZStride + 16 * q + 4 * u + e] + carry;
+              word |= (uint32_t)(v & 255) << (8 * e);
+              carry = v >> 8;
+            }
+            wd[u] = word;
+          }
+          *reinterpret_cast<uint4*>(zb + 16 * q) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+        p.Zc[comp * p.NP + pt] = (int32_t)carry;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(rg::kTmemCols));
+  }
+}
+
+struct FParams {
+  const uint8_t* Zb;
+  const int32_t* Zc;
+  const uint32_t* OFF2;  // [LZ2] words of mp ((P'+1)/2) Q, so that Z + OFF2 >= 0
+  int NP;
+  int LZ2;               // words assembled: max(LG + kZExtra, 32 NP + 1)
+};
+
+// Z' = OFF2 + sum_t (bytes of tile t + carry_t 256^128) 256^(128 t), which is
+// d X_lo (mod Q) in [0, b^LZ2), normalised into words, then numerator_tail.
+__global__ void __launch_bounds__(128) k_recon_finish(RParams p, FParams f) {
+  const int64_t k = blockIdx.x;
+  const int LZ2 = f.LZ2, NW = 32 * f.NP;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  extern __shared__ __align__(16) unsigned char sm[];
+  uint64_t* Zlo = reinterpret_cast<uint64_t*>(sm);            // LZ2 + 1 (int64 columns first)
+  uint32_t* Zhi = reinterpret_cast<uint32_t*>(Zlo + LZ2 + 1);  // LZ2 + 1
+  uint32_t* Zn = Zhi + LZ2 + 1;                               // LZ2 + 1
+  int64_t* col = reinterpret_cast<int64_t*>(Zlo);
+  const uint32_t* zw = reinterpret_cast<const uint32_t*>(f.Zb + k * (int64_t)NW * 4);
+  for (int w = tid; w < LZ2; w += nt) {
+    int64_t v = (int64_t)f.OFF2[w];
+    if (w < NW) v += zw[w];
+    if (w >= 32 && (w & 31) == 0 && (w >> 5) - 1 < f.NP) v += f.Zc[k * f.NP + (w >> 5) - 1];
+    col[w] = v;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int64_t carry = 0;
+    for (int w = 0; w < LZ2; ++w) {
+      const int64_t s = col[w] + carry;
+      Zn[w] = (uint32_t)s;
+      carry = s >> 32;  // arithmetic: the columns may be negative
+    }
+  }
+  numerator_tail(p, k, Zn, Zlo, Zhi);
+}
+
 // little-endian 32-bit words of a natural, zero-extended to `words`
 void to_words(const Nat& a, int64_t words, uint32_t* out) {
   for (int64_t w = 0; w < words; ++w) {
@@ -271,6 +654,32 @@ void to_words(const Nat& a, int64_t words, uint32_t* out) {
 }
 
 int64_t u64_bitlen(uint64_t v) { return v ? 64 - __builtin_clzll(v) : 0; }
+
+// The tensor-core numerator product pays off once there are enough
+// components to fill the GPU with 128-component tiles; its int32 column sums
+// stay exact for m' < 2730 (48 m' 2^14 < 2^31).
+constexpr int64_t kReconTcMinComponents = 4096;
+bool tc_numerators(int64_t nc, int32_t mp) { return nc >= kReconTcMinComponents && mp >= 1 && mp < 2730; }
+struct TcSizes {
+  int64_t LGB1 = 0;
+  int NP = 0, NU = 0, LZ2 = 0;
+};
+TcSizes tc_sizes(int64_t LG) {
+  TcSizes z;
+  z.LGB1 = 4 * LG + 1;  // balanced bytes of G_i < Q < b^LG (one more for the top carry)
+  z.NP = (int)((z.LGB1 + rg::kDig - 1 + rg::kN - 1) / rg::kN);  // byte columns p < LGB1 + 47
+  z.NU = 16 * z.NP + 6;
+  z.LZ2 = (int)std::max<int64_t>(LG + kZExtra, 32 * (int64_t)z.NP + 1);
+  return z;
+}
+void tc_layout_add(Layout& L, int64_t nc, int32_t mp, const TcSizes& z, size_t* o) {
+  o[0] = L.add((size_t)mp * z.NU * 128);             // T
+  o[1] = L.add((size_t)mp * z.LGB1);                 // balanced bytes of G_i
+  o[2] = L.add((size_t)nc * z.NP * rg::kN);          // tile bytes
+  o[3] = L.add((size_t)nc * z.NP * 4);               // tile carries
+  o[4] = L.add((size_t)z.LZ2 * 4);                   // OFF2
+  o[5] = L.add(sizeof(int));                         // error flag
+}
 
 }  // namespace
 
@@ -302,6 +711,10 @@ size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t n
   L.add(kMuWords * 4 + kDigitWords * 4);
   L.add((size_t)nc * W * 8);
   L.add((size_t)nc);
+  if (tc_numerators(nc, mp)) {
+    size_t o[6];
+    tc_layout_add(L, nc, mp, tc_sizes(LG), o);
+  }
   return L.total;
 }
 
@@ -402,6 +815,11 @@ struct ReconPlan {
   size_t oG = 0, oC = 0, oM = 0, oN = 0, oK = 0, total = 0;
   std::vector<uint32_t> hC, hM;
   int dyn = 0;
+  // tensor-core numerator product
+  bool tc = false;
+  TcSizes tz;
+  size_t oTc[6] = {0, 0, 0, 0, 0, 0};  // T, Gb, Zb, Zc, OFF2, err
+  std::vector<uint32_t> hOff2;
 };
 
 void recon_plan_free(ReconPlan* p) { delete p; }
@@ -445,6 +863,16 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
   R.oM = L.add(kMuWords * 4 + kDigitWords * 4);
   R.oN = L.add((size_t)R.nc * R.W * 8);
   R.oK = L.add((size_t)R.nc);
+  R.tc = tc_numerators(R.nc, mp);
+  if (R.tc) {
+    R.tz = tc_sizes(LG);
+    tc_layout_add(L, R.nc, mp, R.tz, R.oTc);
+    // OFF2 = m' ((P' + 1) / 2) Q > |sum_i x_i G_i|, a multiple of Q
+    const Nat off2 = big::mul(big::mul(big::from_u64((uint64_t)mp), big::add(R.ps.half, big::from_u64(1))), Q);
+    if ((int64_t)((big::bitlen(off2) + 32) / 32) > R.tz.LZ2 - 1) return ES_ERR_INTERNAL;
+    R.hOff2.assign((size_t)R.tz.LZ2, 0u);
+    to_words(off2, R.tz.LZ2, R.hOff2.data());
+  }
   R.total = L.total;
   R.hC.assign((size_t)LG * 3, 0);
   R.hM.assign(kMuWords + kDigitWords, 0);
@@ -458,6 +886,75 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
   to_words(R.ps.half, kDigitWords, R.hM.data() + kMuWords);
   R.dyn = (int)((3 * (LG + kZExtra + 1)) * 4 + (LG + kZExtra + 1) * 4 + (size_t)mp * kDigitWords * 4);
   *out = rp.release();
+  return ES_OK;
+}
+
+// One numerator pass on the tensor cores: the balanced bytes of every G_i
+// (host), their T units, the product of all components' digit bytes by them,
+// and the per-component finish.
+static es_status tc_numerator_pass(const ReconPlan& R, const std::vector<uint32_t>& hG, int64_t GS,
+                                   const uint64_t* D_dev, char* scratch, const RParams& rp, std::vector<int8_t>& hGb,
+                                   cudaStream_t st) {
+  const TcSizes& z = R.tz;
+  const int32_t mp = R.mp;
+  const int64_t LG = R.LG, nc = R.nc;
+  // balanced bytes: G = sum_u gb_u 256^u, gb_u in [-128, 127] (carry up)
+  parallel_for(mp, 0, [&](int64_t i) {
+    const uint32_t* gw = hG.data() + (size_t)i * GS + kGPad;
+    int8_t* out = hGb.data() + (size_t)i * z.LGB1;
+    int carry = 0;
+    for (int64_t u = 0; u < z.LGB1; ++u) {
+      const int64_t w = u >> 2;
+      int v = (w < LG ? (int)((gw[w] >> (8 * (u & 3))) & 0xFFu) : 0) + carry;
+      carry = v > 127 ? 1 : 0;
+      out[u] = (int8_t)(v - 256 * carry);
+    }
+  });
+  uint8_t* T = reinterpret_cast<uint8_t*>(scratch + R.oTc[0]);
+  int8_t* Gb = reinterpret_cast<int8_t*>(scratch + R.oTc[1]);
+  int* err = reinterpret_cast<int*>(scratch + R.oTc[5]);
+  ES_CHECK(cuda_status(cudaMemcpyAsync(Gb, hGb.data(), hGb.size(), cudaMemcpyHostToDevice, st), "recon Gb H2D"));
+  ES_CHECK(cuda_status(cudaMemsetAsync(err, 0, sizeof(int), st), "recon err memset"));
+  const int64_t rows = (int64_t)mp * z.NU * 8;
+  k_recon_tbuild<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(Gb, z.LGB1, z.NU, mp, T);
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_tbuild"));
+  GParams gp;
+  gp.X = reinterpret_cast<const uint8_t*>(D_dev);
+  gp.T = T;
+  gp.nc = nc;
+  gp.mp = mp;
+  gp.NP = z.NP;
+  gp.NU = z.NU;
+  gp.tiles = (int)(((nc + rg::kM - 1) / rg::kM) * z.NP);
+  gp.Zb = reinterpret_cast<uint8_t*>(scratch + R.oTc[2]);
+  gp.Zc = reinterpret_cast<int32_t*>(scratch + R.oTc[3]);
+  gp.err = err;
+  ES_CHECK(cuda_status(cudaFuncSetAttribute(k_recon_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)rg::kSmem),
+                       "recon gemm smem attribute"));
+  const int grid = std::min(gp.tiles, sm_count());
+  k_recon_gemm<<<grid, rg::kThreads, rg::kSmem, st>>>(gp);
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_gemm"));
+  FParams fp;
+  fp.Zb = gp.Zb;
+  fp.Zc = gp.Zc;
+  fp.OFF2 = reinterpret_cast<const uint32_t*>(scratch + R.oTc[4]);
+  fp.NP = z.NP;
+  fp.LZ2 = z.LZ2;
+  const int fdyn = 16 * (z.LZ2 + 1);
+  if (fdyn > 48 * 1024)
+    ES_CHECK(cuda_status(cudaFuncSetAttribute(k_recon_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, fdyn),
+                         "recon finish smem attribute"));
+  k_recon_finish<<<(unsigned)nc, 128, fdyn, st>>>(rp, fp);
+  count_launch(3);
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_finish"));
+  int herr = 0;
+  ES_CHECK(cuda_status(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st), "recon err D2H"));
+  ES_CHECK(cuda_status(cudaStreamSynchronize(st), "recon gemm sync"));
+  if (herr) {
+    set_last_error("numerator product: bounded wait expired (code " + std::to_string(herr) + ")");
+    return ES_ERR_TIMEOUT;
+  }
   return ES_OK;
 }
 
@@ -528,6 +1025,11 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   std::vector<uint8_t> okh((size_t)nc);
   const int64_t GS = g_stride(LG);
   std::vector<uint32_t> hG((size_t)mp * GS, 0u);
+  std::vector<int8_t> hGb(R.tc ? (size_t)mp * R.tz.LGB1 : 0);
+  if (R.tc)
+    ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + R.oTc[4], R.hOff2.data(), R.hOff2.size() * 4,
+                                         cudaMemcpyHostToDevice, st),
+                         "recon OFF2 H2D"));
   for (int round = 0;; ++round) {
     if (round > 64) return ES_ERR_INTERNAL;
     // G_i = d P'^i mod Q, OFF = Q - ((P'-1)/2 sum_i G_i mod Q).  The chain is
@@ -552,8 +1054,9 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     big::divmod(big::mul(sum, ps.half), Q, nullptr, &rem);
     const Nat off = rem.empty() ? Nat{} : big::sub(Q, rem);
     to_words(off, LG, hC.data());
-    ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oG, hG.data(), hG.size() * 4, cudaMemcpyHostToDevice, st),
-                         "recon G H2D"));
+    if (!R.tc)
+      ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oG, hG.data(), hG.size() * 4, cudaMemcpyHostToDevice, st),
+                           "recon G H2D"));
     ES_CHECK(cuda_status(cudaMemcpyAsync(scratch + oC, hC.data(), hC.size() * 4, cudaMemcpyHostToDevice, st),
                          "recon Q H2D"));
     RParams rp;
@@ -572,9 +1075,13 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     rp.W = (int)W;
     rp.N = Nout;
     rp.ok = reinterpret_cast<uint8_t*>(scratch + oK);
-    k_recon_numerators<<<(unsigned)nc, 256, dyn, st>>>(rp);
-    count_launch();
-    ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_numerators"));
+    if (R.tc) {
+      ES_CHECK(tc_numerator_pass(R, hG, GS, D_dev, scratch, rp, hGb, st));
+    } else {
+      k_recon_numerators<<<(unsigned)nc, 256, dyn, st>>>(rp);
+      count_launch();
+      ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_numerators"));
+    }
     ES_CHECK(cuda_status(cudaMemcpyAsync(okh.data(), rp.ok, (size_t)nc, cudaMemcpyDeviceToHost, st), "ok D2H"));
     if (!direct)
       ES_CHECK(cuda_status(cudaMemcpyAsync(out->num.data(), rp.N, (size_t)nc * W * 8, cudaMemcpyDeviceToHost, st),
