@@ -301,30 +301,38 @@ __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
 // per digit (8 f16 per byte of G_i, all of it resident in L2) and each stage
 // loads the 21 units a 128-column tile needs.
 //
-// CTA tile = 128 components (MMA M, A operand in tensor memory: four
-// converter warps widen each component's 48 digit bytes, balanced and
-// reversed, with tcgen05.st) x 128 byte columns (MMA N); a stage is one digit
-// (three K = 16 MMAs).  Persistent CTAs walk the tiles with the byte-column
-// tile fastest, so the CTAs running together share a component tile and its
-// digits stay in L2.  The epilogue (eight warps) folds each 21-digit chunk
-// into int32 column sums, and at the tile's end normalises each component's
-// 128 columns into 128 bytes plus a signed carry.  k_recon_finish then adds
-// the tiles, reduces mod Q and writes the numerator.
+// CTA tile = 128 components (MMA M, A operand in tensor memory: eight
+// converter warps, one per lane quarter and digit, widen each component's 48
+// digit bytes, balanced and reversed, with tcgen05.st) x 128 byte columns
+// (MMA N); a pipeline stage is two digits (six K = 16 MMAs), five stages in
+// flight.  Persistent CTAs walk the tiles with the byte-column tile fastest,
+// so the CTAs running together share a component tile and its digits stay in
+// L2.  The epilogue (eight warps) folds each 20-digit chunk into int32 column
+// sums, and at the tile's end normalises each component's 128 columns into 32
+// words plus a signed carry, stored word-major (component fastest).
+// k_recon_finish (one thread per component) adds the tiles, reduces mod Q and
+// writes the numerator limbs, which k_recon_transpose puts in component order.
 namespace rg {
 constexpr int kM = 128;                     // components per tile
 constexpr int kN = 128;                     // byte columns per tile
 constexpr int kDig = 48;                    // bytes per digit (K per stage)
-constexpr int kStages = 8;
-constexpr int kXBytes = kM * kDig;          // 6144
+constexpr int kDPS = 2;                     // digits per pipeline stage
+constexpr int kStages = 5;                  // pipeline stages (shared memory and A slots)
+constexpr int kXBytes = kM * kDig;          // 6144 per digit
 constexpr int kUnits = kN / 8 + kDig / 8 - 1;  // 21 core-matrix units per window
-constexpr int kTBytes = kUnits * 128;       // 2688
-constexpr int kFold = 21;                   // digits per exact FP32 chunk (1008 K)
+constexpr int kTBytes = kUnits * 128;       // 2688 per digit
+constexpr int kFold = 10;                   // stages per exact FP32 chunk (20 digits: 960 K)
 constexpr uint32_t kColA = 2 * kN;          // A slots after the two accumulators
+constexpr uint32_t kSlotCols = 48;          // per stage: 24 columns per digit
 constexpr uint32_t kTmemCols = 512;
 constexpr int kZStride = kN + 1;            // words per row of the epilogue's staging (odd)
-constexpr int kThreads = 448;               // producer, MMA, 4 converter and 8 epilogue warps
-constexpr size_t kSmem = 1024 + (size_t)kStages * (kXBytes + kTBytes) + (size_t)kM * kZStride * 4 + 512;
-static_assert(kColA + 32 * kStages <= kTmemCols, "tensor memory");
+constexpr int kConvWarps = 4 * kDPS;        // one warp per lane quarter and digit of a stage
+constexpr int kEpiWarp0 = 2 + kConvWarps;   // first epilogue warp
+constexpr int kThreads = 32 * (kEpiWarp0 + 8);  // producer, MMA, converter and 8 epilogue warps
+constexpr size_t kSmem =
+    1024 + (size_t)kStages * kDPS * (kXBytes + kTBytes) + (size_t)kM * kZStride * 4 + 512;
+static_assert(kColA + kSlotCols * kStages <= kTmemCols, "tensor memory");
+static_assert(24 * kDPS <= (int)kSlotCols, "A slot");
 }  // namespace rg
 
 struct GParams {
@@ -333,8 +341,8 @@ struct GParams {
   int64_t nc;
   int mp, NP, NU;
   int tiles;           // comp tiles x NP
-  uint8_t* Zb;         // [nc][NP * 128] normalised bytes
-  int32_t* Zc;         // [nc][NP]       carry out of each tile
+  uint32_t* Zw;        // [NP * 32 + 1][nc] normalised words of the tiles, component fastest
+  int32_t* Zc;         // [NP][nc]       carry out of each tile
   int* err;
 };
 
@@ -391,24 +399,24 @@ __global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
   using namespace tc;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sX = smem;                                   // [S][128][48] digit bytes
-  uint8_t* sT = sX + kStages * kXBytes;                 // [S][21][128] T windows
-  int32_t* sZ = reinterpret_cast<int32_t*>(sT + kStages * kTBytes);  // [128][129]
+  uint8_t* sX = smem;                                   // [S][DPS][128][48] digit bytes
+  uint8_t* sT = sX + kStages * kDPS * kXBytes;          // [S][DPS][21][128] T windows
+  int32_t* sZ = reinterpret_cast<int32_t*>(sT + kStages * kDPS * kTBytes);  // [128][129]
   uint64_t* full = reinterpret_cast<uint64_t*>(sZ + kM * kZStride);
-  uint64_t* conv = full + kStages;
-  uint64_t* empty = conv + kStages;
-  uint64_t* accfull = empty + kStages;
+  uint64_t* empty = full + kStages;
+  uint64_t* conv = empty + kStages;
+  uint64_t* accfull = conv + kStages;
   uint64_t* accempty = accfull + 2;
   uint64_t* drained = accempty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drained + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mp = p.mp, nch = (mp + kFold - 1) / kFold;
+  const int mp = p.mp, nst = (mp + kDPS - 1) / kDPS, nch = (nst + kFold - 1) / kFold;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(conv + s, 128);
       mbar_init(empty + s, 1);
+      mbar_init(conv + s, 32 * kConvWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accfull + b, 1);
@@ -435,16 +443,19 @@ __global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
       const int ct = t / p.NP, pt = t - ct * p.NP;
       const int64_t c0 = (int64_t)ct * kM;
       const uint32_t cnt = (uint32_t)(p.nc - c0 < kM ? p.nc - c0 : kM);
-      for (int i = 0; i < mp; ++i, ++g) {
-        const int s = g % kStages;
+      for (int j = 0; j < nst; ++j, ++g) {
+        const int s = g % kStages, nd = mp - kDPS * j < kDPS ? mp - kDPS * j : kDPS;
         if (g >= kStages && !mbar_wait_warp(empty + s, ((g / kStages) & 1) ^ 1, err, 21)) {
           stop = true;
           break;
         }
         if (elect_one()) {
-          mbar_expect_tx(full + s, cnt * kDig + kTBytes);
-          bulk_g2s(sX + s * kXBytes, p.X + ((int64_t)i * p.nc + c0) * kDig, cnt * kDig, full + s);
-          bulk_g2s(sT + s * kTBytes, p.T + ((int64_t)i * p.NU + 16 * pt) * 128, kTBytes, full + s);
+          mbar_expect_tx(full + s, nd * (cnt * kDig + kTBytes));
+          for (int d = 0; d < nd; ++d) {
+            const int i = kDPS * j + d;
+            bulk_g2s(sX + (s * kDPS + d) * kXBytes, p.X + ((int64_t)i * p.nc + c0) * kDig, cnt * kDig, full + s);
+            bulk_g2s(sT + (s * kDPS + d) * kTBytes, p.T + ((int64_t)i * p.NU + 16 * pt) * 128, kTBytes, full + s);
+          }
         }
         __syncwarp();
       }
@@ -455,9 +466,9 @@ __global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
     int g = 0, gc = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
-      for (int i = 0; i < mp; ++i, ++g) {
-        const int s = g % kStages, buf = gc & 1;
-        const bool first = (i % kFold) == 0;
+      for (int j = 0; j < nst; ++j, ++g) {
+        const int s = g % kStages, buf = gc & 1, nd = mp - kDPS * j < kDPS ? mp - kDPS * j : kDPS;
+        const bool first = (j % kFold) == 0;
         if (first && gc >= 2 && !mbar_wait_warp(accempty + buf, ((gc - 2) >> 1) & 1, err, 22)) {
           stop = true;
           break;
@@ -469,82 +480,89 @@ __global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
         }
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t tb = smem_u32(sT + s * kTBytes);
+          for (int d = 0; d < nd; ++d) {
+            // K = 16 steps advance the window by two 128-byte units (16 in the address field)
+            const uint64_t bd = desc_interleave(smem_u32(sT + (s * kDPS + d) * kTBytes), 128, 128);
 #pragma unroll
-          for (int k = 0; k < kDig / 16; ++k)
-            mma_f16_ta(tmem + buf * kN, tmem + kColA + 32 * s + 8 * k, desc_interleave(tb + 256 * k, 128, 128),
-                       idesc, (first && k == 0) ? 0u : 1u);
+            for (int k = 0; k < kDig / 16; ++k)
+              mma_f16_ta(tmem + buf * kN, tmem + kColA + kSlotCols * s + 24 * d + 8 * k, bd + 16 * k, idesc,
+                         (first && d == 0 && k == 0) ? 0u : 1u);
+          }
           mma_commit(empty + s);
-          if (i % kFold == kFold - 1 || i == mp - 1) mma_commit(accfull + buf);
+          if (j % kFold == kFold - 1 || j == nst - 1) mma_commit(accfull + buf);
         }
         __syncwarp();
-        if (i % kFold == kFold - 1 || i == mp - 1) ++gc;
+        if (j % kFold == kFold - 1 || j == nst - 1) ++gc;
       }
     }
     if (elect_one()) mma_commit(drained);
     __syncwarp();
     mbar_wait_drain(drained, 0);
-  } else if (warp < 6) {
-    // converters: warp w touches tensor-memory lanes 32 (w % 4) .. + 31; thread =
-    // one component (row): its 48 digit bytes, balanced (bytes of x + 0x80..80,
-    // less 128) and reversed (A's element b' = byte 47 - b'), as 24 columns
-    const int quarter = warp & 3, r = 32 * quarter + lane;
+  } else if (warp < kEpiWarp0) {
+    // converters: warp w touches tensor-memory lanes 32 (w % 4) .. + 31 and
+    // takes digit d = (w - 2) / 4 of each stage; thread = one component (row):
+    // its 48 digit bytes, balanced (bytes of x + 0x80..80, less 128) and
+    // reversed (A's element b' = byte 47 - b'), as 24 columns
+    const int quarter = warp & 3, d = (warp - 2) >> 2, r = 32 * quarter + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
     int g = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < p.tiles && !stop; t += gridDim.x) {
       const int ct = t / p.NP;
       const bool live = (int64_t)ct * kM + r < p.nc;
-      for (int i = 0; i < mp; ++i, ++g) {
-        const int s = g % kStages;
+      for (int j = 0; j < nst; ++j, ++g) {
+        const int s = g % kStages, nd = mp - kDPS * j < kDPS ? mp - kDPS * j : kDPS;
+        // the slot's previous MMAs completed before its copy was issued (empty -> full)
         if (!mbar_wait_warp(full + s, (g / kStages) & 1, err, 25)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        uint32_t wv[24];
-        if (live) {
-          const uint4* src = reinterpret_cast<const uint4*>(sX + s * kXBytes + r * kDig);
-          const uint4 v0 = src[0], v1 = src[1], v2 = src[2];
-          // x + 0x8080...80 over 384 bits
-          uint64_t w64[6] = {(uint64_t)v0.x | ((uint64_t)v0.y << 32), (uint64_t)v0.z | ((uint64_t)v0.w << 32),
-                             (uint64_t)v1.x | ((uint64_t)v1.y << 32), (uint64_t)v1.z | ((uint64_t)v1.w << 32),
-                             (uint64_t)v2.x | ((uint64_t)v2.y << 32), (uint64_t)v2.z | ((uint64_t)v2.w << 32)};
-          uint32_t cy = 0;
+        if (d < nd) {
+          uint32_t wv[24];
+          if (live) {
+            const uint4* src = reinterpret_cast<const uint4*>(sX + (s * kDPS + d) * kXBytes + r * kDig);
+            const uint4 v0 = src[0], v1 = src[1], v2 = src[2];
+            // x + 0x8080...80 over 384 bits
+            uint64_t w64[6] = {(uint64_t)v0.x | ((uint64_t)v0.y << 32), (uint64_t)v0.z | ((uint64_t)v0.w << 32),
+                               (uint64_t)v1.x | ((uint64_t)v1.y << 32), (uint64_t)v1.z | ((uint64_t)v1.w << 32),
+                               (uint64_t)v2.x | ((uint64_t)v2.y << 32), (uint64_t)v2.z | ((uint64_t)v2.w << 32)};
+            uint32_t cy = 0;
 #pragma unroll
-          for (int l = 0; l < 6; ++l) {
-            const uint64_t a = w64[l] + 0x8080808080808080ull, b = a + cy;
-            cy = (a < w64[l] || b < a) ? 1u : 0u;
-            w64[l] = b;
+            for (int l = 0; l < 6; ++l) {
+              const uint64_t a = w64[l] + 0x8080808080808080ull, b = a + cy;
+              cy = (a < w64[l] || b < a) ? 1u : 0u;
+              w64[l] = b;
+            }
+            // reversed bytes: word k' of the reversal = bytes 47 - 4k' .. 44 - 4k'
+#pragma unroll
+            for (int kk = 0; kk < 12; ++kk) {
+              const int src_w = 11 - kk;
+              const uint32_t word = (uint32_t)(w64[src_w >> 1] >> (32 * (src_w & 1)));
+              u8x4_m128_to_f16(__byte_perm(word, 0, 0x0123), wv[2 * kk], wv[2 * kk + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 24; ++kk) wv[kk] = 0;
           }
-          // reversed bytes: word k' of the reversal = bytes 47 - 4k' .. 44 - 4k'
+          uint32_t lo[16], hi[8];
 #pragma unroll
-          for (int kk = 0; kk < 12; ++kk) {
-            const int src_w = 11 - kk;
-            const uint32_t word = (uint32_t)(w64[src_w >> 1] >> (32 * (src_w & 1)));
-            u8x4_m128_to_f16(__byte_perm(word, 0, 0x0123), wv[2 * kk], wv[2 * kk + 1]);
-          }
-        } else {
+          for (int kk = 0; kk < 16; ++kk) lo[kk] = wv[kk];
 #pragma unroll
-          for (int kk = 0; kk < 24; ++kk) wv[kk] = 0;
+          for (int kk = 0; kk < 8; ++kk) hi[kk] = wv[16 + kk];
+          tmem_st16(trow + kColA + kSlotCols * s + 24 * d, lo);
+          tmem_st8(trow + kColA + kSlotCols * s + 24 * d + 16, hi);
+          tmem_st_wait();
         }
-        uint32_t lo[16], hi[8];
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) lo[kk] = wv[kk];
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) hi[kk] = wv[16 + kk];
-        tmem_st16(trow + kColA + 32 * s, lo);
-        tmem_st8(trow + kColA + 32 * s + 16, hi);
-        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(conv + s);
       }
     }
   } else {
-    // epilogue: warp w folds columns 64 h .. 64 h + 63 (h = (w - 6) / 4) of the
+    // epilogue: warp w folds columns 64 h .. 64 h + 63 (h = (w - kEpiWarp0) / 4) of the
     // rows of lane quarter w % 4; at a tile's end the rows are normalised into
     // bytes and a carry through the staging area
-    const int quarter = warp & 3, h = (warp - 6) >> 2, r = 32 * quarter + lane;
+    const int quarter = warp & 3, h = (warp - kEpiWarp0) >> 2, r = 32 * quarter + lane;
     int gc = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
@@ -575,25 +593,21 @@ __global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
       asm volatile("bar.sync 1, 256;" ::: "memory");
       const int64_t comp = (int64_t)ct * kM + r;
       if (h == 0 && comp < p.nc) {
+        // words of the tile, component fastest: a warp's stores are 128 contiguous bytes
         int64_t carry = 0;
-        uint8_t* zb = p.Zb + (comp * p.NP + pt) * kN;
+        uint32_t* zw = p.Zw + (int64_t)(kN / 4) * pt * p.nc + comp;
 #pragma unroll 1
-        for (int q = 0; q < kN / 16; ++q) {
-          uint32_t wd[4];
+        for (int q = 0; q < kN / 4; ++q) {
+          uint32_t word = 0;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int64_t v = (int64_t)sZ[r * kZStride + 16 * q + 4 * u + e] + carry;
-              word |= (uint32_t)(v & 255) << (8 * e);
-              carry = v >> 8;
-            }
-            wd[u] = word;
+          for (int e = 0; e < 4; ++e) {
+            const int64_t v = (int64_t)sZ[r * kZStride + 4 * q + e] + carry;
+            word |= (uint32_t)(v & 255) << (8 * e);
+            carry = v >> 8;
           }
-          *reinterpret_cast<uint4*>(zb + 16 * q) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          zw[(int64_t)q * p.nc] = word;
         }
-        p.Zc[comp * p.NP + pt] = (int32_t)carry;
+        p.Zc[(int64_t)pt * p.nc + comp] = (int32_t)carry;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
     }
@@ -607,41 +621,174 @@ __global__ void __launch_bounds__(rg::kThreads, 1) k_recon_gemm(GParams p) {
 }
 
 struct FParams {
-  const uint8_t* Zb;
-  const int32_t* Zc;
-  const uint32_t* OFF2;  // [LZ2] words of mp ((P'+1)/2) Q, so that Z + OFF2 >= 0
-  int NP;
-  int LZ2;               // words assembled: max(LG + kZExtra, 32 NP + 1)
+  uint32_t* Zw;          // [LZ2][nc] words, component fastest (in: the tiles' words)
+  const int32_t* Zc;     // [NP][nc]
+  const uint32_t* OFF2;  // [LZ2] words of m' ((P'+1)/2) Q, so that Z + OFF2 >= 0
+  const uint32_t* Q;     // [LG]
+  const uint32_t* Qhalf; // [LG]  (Q - 1) / 2
+  const uint32_t* MU;    // [13]  floor(b^(LG-1+13) / Q)
+  int64_t nc, nb;
+  int LG, NP, LZ2, W;
+  uint64_t* Nw;          // [W][nc] numerator limbs, component fastest
+  uint8_t* ok;           // [nc]
 };
 
-// Z' = OFF2 + sum_t (bytes of tile t + carry_t 256^128) 256^(128 t), which is
-// d X_lo (mod Q) in [0, b^LZ2), normalised into words, then numerator_tail.
-__global__ void __launch_bounds__(128) k_recon_finish(RParams p, FParams f) {
-  const int64_t k = blockIdx.x;
-  const int LZ2 = f.LZ2, NW = 32 * f.NP;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  extern __shared__ __align__(16) unsigned char sm[];
-  uint64_t* Zlo = reinterpret_cast<uint64_t*>(sm);            // LZ2 + 1 (int64 columns first)
-  uint32_t* Zhi = reinterpret_cast<uint32_t*>(Zlo + LZ2 + 1);  // LZ2 + 1
-  uint32_t* Zn = Zhi + LZ2 + 1;                               // LZ2 + 1
-  int64_t* col = reinterpret_cast<int64_t*>(Zlo);
-  const uint32_t* zw = reinterpret_cast<const uint32_t*>(f.Zb + k * (int64_t)NW * 4);
-  for (int w = tid; w < LZ2; w += nt) {
-    int64_t v = (int64_t)f.OFF2[w];
-    if (w < NW) v += zw[w];
-    if (w >= 32 && (w & 31) == 0 && (w >> 5) - 1 < f.NP) v += f.Zc[k * f.NP + (w >> 5) - 1];
-    col[w] = v;
-  }
-  __syncthreads();
-  if (tid == 0) {
+// One thread per component (every step of the finish is a carry chain, so
+// the components, not the words, are spread over the threads; the word-major
+// layout keeps each warp's accesses contiguous):
+//   Z' = OFF2 + sum_t (words of tile t + carry_t b^32) b^(32 t) = d X_lo (mod Q),
+//   r = Z' - q^ Q with q^ = floor(floor(Z' / b^(LG-1)) MU / b^13) (Barrett),
+//   at most two subtractions of Q, the balanced N = r or r - Q, |N| <= 2^nb,
+//   and N's two's complement limbs.
+__global__ void __launch_bounds__(128) k_recon_finish(FParams f) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= f.nc) return;
+  const int64_t nc = f.nc;
+  const int LG = f.LG, LZ2 = f.LZ2, LW = 32 * f.NP;
+  uint32_t* Z = f.Zw + k;  // word w at Z[w * nc]
+  // Z' normalised into words
+  {
     int64_t carry = 0;
     for (int w = 0; w < LZ2; ++w) {
-      const int64_t s = col[w] + carry;
-      Zn[w] = (uint32_t)s;
-      carry = s >> 32;  // arithmetic: the columns may be negative
+      int64_t v = (int64_t)f.OFF2[w] + carry;
+      if (w < LW) v += Z[(int64_t)w * nc];
+      if (w >= 32 && (w & 31) == 0 && (w >> 5) - 1 < f.NP) v += f.Zc[(int64_t)((w >> 5) - 1) * nc + k];
+      Z[(int64_t)w * nc] = (uint32_t)v;
+      carry = v >> 32;  // arithmetic: the columns may be negative
     }
   }
-  numerator_tail(p, k, Zn, Zlo, Zhi);
+  // q^ from the top 13 words
+  uint32_t qh[kMuWords];
+  {
+    uint32_t prod[2 * kMuWords];
+#pragma unroll
+    for (int t = 0; t < 2 * kMuWords; ++t) prod[t] = 0;
+#pragma unroll 1
+    for (int a = 0; a < kMuWords; ++a) {
+      uint64_t c = 0;
+      const uint64_t za = Z[(int64_t)(LG - 1 + a) * nc];
+#pragma unroll
+      for (int b = 0; b < kMuWords; ++b) {
+        const uint64_t t = za * f.MU[b] + prod[a + b] + c;
+        prod[a + b] = (uint32_t)t;
+        c = t >> 32;
+      }
+      prod[a + kMuWords] = (uint32_t)c;
+    }
+#pragma unroll
+    for (int t = 0; t < kMuWords; ++t) qh[t] = prod[kMuWords + t];
+  }
+  // r = Z' - q^ Q over words 0 .. LG (the remainder is below 3Q < b^(LG+1))
+  {
+    uint64_t plo = 0;  // running column sum of q^ Q (96 bits: plo + 2^64 phi)
+    uint32_t phi = 0;
+    int64_t borrow = 0;
+    for (int w = 0; w <= LG; ++w) {
+#pragma unroll
+      for (int j = 0; j < kMuWords; ++j) {
+        const int t = w - j;
+        if (t >= 0 && t < LG) {
+          const uint64_t pr = (uint64_t)qh[j] * f.Q[t];
+          plo += pr;
+          phi += plo < pr ? 1u : 0u;
+        }
+      }
+      const uint32_t qq = (uint32_t)plo;
+      plo = (plo >> 32) | ((uint64_t)phi << 32);
+      phi = 0;
+      const int64_t d = (int64_t)Z[(int64_t)w * nc] - (int64_t)qq + borrow;
+      Z[(int64_t)w * nc] = (uint32_t)d;
+      borrow = d >> 32;
+    }
+  }
+  // at most two subtractions of Q
+  for (int rep = 0; rep < 3; ++rep) {
+    bool ge = Z[(int64_t)LG * nc] != 0;
+    if (!ge) {
+      ge = true;
+      for (int w = LG - 1; w >= 0; --w) {
+        const uint32_t zw = Z[(int64_t)w * nc], qw = f.Q[w];
+        if (zw != qw) {
+          ge = zw > qw;
+          break;
+        }
+      }
+    }
+    if (!ge) break;
+    int64_t borrow = 0;
+    for (int w = 0; w <= LG; ++w) {
+      const int64_t d = (int64_t)Z[(int64_t)w * nc] - (int64_t)(w < LG ? f.Q[w] : 0u) + borrow;
+      Z[(int64_t)w * nc] = (uint32_t)d;
+      borrow = d >> 32;
+    }
+  }
+  // balanced: r > (Q-1)/2 -> N = r - Q, magnitude Q - r
+  bool neg = false;
+  for (int w = LG - 1; w >= 0; --w) {
+    const uint32_t zw = Z[(int64_t)w * nc], hw = f.Qhalf[w];
+    if (zw != hw) {
+      neg = zw > hw;
+      break;
+    }
+  }
+  if (neg) {
+    int64_t borrow = 0;
+    for (int w = 0; w < LG; ++w) {
+      const int64_t d = (int64_t)f.Q[w] - (int64_t)Z[(int64_t)w * nc] + borrow;
+      Z[(int64_t)w * nc] = (uint32_t)d;
+      borrow = d >> 32;
+    }
+  }
+  // |N| <= 2^nb ?
+  int top = LG - 1;
+  while (top >= 0 && Z[(int64_t)top * nc] == 0) --top;
+  bool ok = true;
+  if (top >= 0) {
+    const uint32_t zt = Z[(int64_t)top * nc];
+    const int64_t bl = 32 * (int64_t)top + (32 - __clz(zt));
+    if (bl > f.nb + 1) {
+      ok = false;
+    } else if (bl == f.nb + 1) {  // equal to 2^nb only
+      ok = zt == (1u << (f.nb % 32));
+      for (int w = 0; ok && w < top; ++w) ok = Z[(int64_t)w * nc] == 0;
+    }
+  }
+  f.ok[k] = ok ? 1 : 0;
+  // two's complement limbs: -mag = ~mag + 1
+  uint32_t cy = neg ? 1u : 0u;
+  for (int t = 0; t < f.W; ++t) {
+    uint32_t wv[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int w = 2 * t + hh;
+      const uint32_t m = w < LG ? Z[(int64_t)w * nc] : 0u;
+      if (neg) {
+        const uint64_t v = (uint64_t)(~m) + cy;
+        wv[hh] = (uint32_t)v;
+        cy = (uint32_t)(v >> 32);
+      } else {
+        wv[hh] = m;
+      }
+    }
+    f.Nw[(int64_t)t * nc + k] = (uint64_t)wv[0] | ((uint64_t)wv[1] << 32);
+  }
+}
+
+// out[k][t] = Nw[t][k]: 32 x 32 tiles through shared memory, both sides
+// contiguous (the destination may be page-locked host memory).
+__global__ void k_recon_transpose(const uint64_t* __restrict__ Nw, int64_t nc, int W, uint64_t* __restrict__ out) {
+  __shared__ uint64_t tile[32][33];
+  const int64_t k0 = (int64_t)blockIdx.x * 32, t0 = (int64_t)blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int64_t t = t0 + yy, k = k0 + tx;
+    if (t < W && k < nc) tile[yy][tx] = Nw[t * nc + k];
+  }
+  __syncthreads();
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int64_t k = k0 + yy, t = t0 + tx;
+    if (t < W && k < nc) out[k * W + t] = tile[tx][yy];
+  }
 }
 
 // little-endian 32-bit words of a natural, zero-extended to `words`
@@ -672,13 +819,14 @@ TcSizes tc_sizes(int64_t LG) {
   z.LZ2 = (int)std::max<int64_t>(LG + kZExtra, 32 * (int64_t)z.NP + 1);
   return z;
 }
-void tc_layout_add(Layout& L, int64_t nc, int32_t mp, const TcSizes& z, size_t* o) {
+void tc_layout_add(Layout& L, int64_t nc, int32_t mp, int64_t W, const TcSizes& z, size_t* o) {
   o[0] = L.add((size_t)mp * z.NU * 128);             // T
   o[1] = L.add((size_t)mp * z.LGB1);                 // balanced bytes of G_i
-  o[2] = L.add((size_t)nc * z.NP * rg::kN);          // tile bytes
+  o[2] = L.add((size_t)nc * z.LZ2 * 4);              // Z' words, component fastest
   o[3] = L.add((size_t)nc * z.NP * 4);               // tile carries
   o[4] = L.add((size_t)z.LZ2 * 4);                   // OFF2
   o[5] = L.add(sizeof(int));                         // error flag
+  o[6] = L.add((size_t)nc * W * 8);                  // numerator limbs, component fastest
 }
 
 }  // namespace
@@ -712,8 +860,8 @@ size_t recon_device_bytes(int64_t nc, int32_t mp, const uint8_t* good, int64_t n
   L.add((size_t)nc * W * 8);
   L.add((size_t)nc);
   if (tc_numerators(nc, mp)) {
-    size_t o[6];
-    tc_layout_add(L, nc, mp, tc_sizes(LG), o);
+    size_t o[7];
+    tc_layout_add(L, nc, mp, W, tc_sizes(LG), o);
   }
   return L.total;
 }
@@ -818,7 +966,7 @@ struct ReconPlan {
   // tensor-core numerator product
   bool tc = false;
   TcSizes tz;
-  size_t oTc[6] = {0, 0, 0, 0, 0, 0};  // T, Gb, Zb, Zc, OFF2, err
+  size_t oTc[7] = {0, 0, 0, 0, 0, 0, 0};  // T, Gb, Zw, Zc, OFF2, err, Nw
   std::vector<uint32_t> hOff2;
 };
 
@@ -866,7 +1014,7 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
   R.tc = tc_numerators(R.nc, mp);
   if (R.tc) {
     R.tz = tc_sizes(LG);
-    tc_layout_add(L, R.nc, mp, R.tz, R.oTc);
+    tc_layout_add(L, R.nc, mp, R.W, R.tz, R.oTc);
     // OFF2 = m' ((P' + 1) / 2) Q > |sum_i x_i G_i|, a multiple of Q
     const Nat off2 = big::mul(big::mul(big::from_u64((uint64_t)mp), big::add(R.ps.half, big::from_u64(1))), Q);
     if ((int64_t)((big::bitlen(off2) + 32) / 32) > R.tz.LZ2 - 1) return ES_ERR_INTERNAL;
@@ -894,7 +1042,7 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
 // and the per-component finish.
 static es_status tc_numerator_pass(const ReconPlan& R, const std::vector<uint32_t>& hG, int64_t GS,
                                    const uint64_t* D_dev, char* scratch, const RParams& rp, std::vector<int8_t>& hGb,
-                                   cudaStream_t st) {
+                                   uint64_t* host_out, int host_threads, cudaStream_t st) {
   const TcSizes& z = R.tz;
   const int32_t mp = R.mp;
   const int64_t LG = R.LG, nc = R.nc;
@@ -926,7 +1074,7 @@ static es_status tc_numerator_pass(const ReconPlan& R, const std::vector<uint32_
   gp.NP = z.NP;
   gp.NU = z.NU;
   gp.tiles = (int)(((nc + rg::kM - 1) / rg::kM) * z.NP);
-  gp.Zb = reinterpret_cast<uint8_t*>(scratch + R.oTc[2]);
+  gp.Zw = reinterpret_cast<uint32_t*>(scratch + R.oTc[2]);
   gp.Zc = reinterpret_cast<int32_t*>(scratch + R.oTc[3]);
   gp.err = err;
   ES_CHECK(cuda_status(cudaFuncSetAttribute(k_recon_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -936,20 +1084,39 @@ static es_status tc_numerator_pass(const ReconPlan& R, const std::vector<uint32_
   k_recon_gemm<<<grid, rg::kThreads, rg::kSmem, st>>>(gp);
   ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_gemm"));
   FParams fp;
-  fp.Zb = gp.Zb;
+  fp.Zw = gp.Zw;
   fp.Zc = gp.Zc;
   fp.OFF2 = reinterpret_cast<const uint32_t*>(scratch + R.oTc[4]);
+  fp.Q = rp.Q;
+  fp.Qhalf = rp.Qhalf;
+  fp.MU = rp.MU;
+  fp.nc = nc;
+  fp.nb = rp.nb;
+  fp.LG = (int)LG;
   fp.NP = z.NP;
   fp.LZ2 = z.LZ2;
-  const int fdyn = 16 * (z.LZ2 + 1);
-  if (fdyn > 48 * 1024)
-    ES_CHECK(cuda_status(cudaFuncSetAttribute(k_recon_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, fdyn),
-                         "recon finish smem attribute"));
-  k_recon_finish<<<(unsigned)nc, 128, fdyn, st>>>(rp, fp);
-  count_launch(3);
+  fp.W = rp.W;
+  fp.Nw = reinterpret_cast<uint64_t*>(scratch + R.oTc[6]);
+  fp.ok = rp.ok;
+  k_recon_finish<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(fp);
   ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_finish"));
+  k_recon_transpose<<<dim3((unsigned)((nc + 31) / 32), (unsigned)((rp.W + 31) / 32)), dim3(32, 8), 0, st>>>(
+      fp.Nw, nc, rp.W, rp.N);
+  count_launch(4);
+  ES_CHECK(cuda_status(cudaGetLastError(), "k_recon_transpose"));
   int herr = 0;
   ES_CHECK(cuda_status(cudaMemcpyAsync(&herr, err, sizeof(int), cudaMemcpyDeviceToHost, st), "recon err D2H"));
+  // While the GPU works: the host threads write the result buffer once, which
+  // makes the copy into it that follows several times faster on this host
+  // (measured: a copy into a page-locked buffer the host has not just written
+  // ran at a fraction of the copy engine's rate).
+  {
+    const size_t words = (size_t)nc * (size_t)rp.W, chunk = size_t(1) << 20;
+    parallel_for((int64_t)((words + chunk - 1) / chunk), host_threads, [&](int64_t t) {
+      const size_t a = (size_t)t * chunk, b = std::min(words, a + chunk);
+      std::memset(host_out + a, 0, (b - a) * 8);
+    });
+  }
   ES_CHECK(cuda_status(cudaStreamSynchronize(st), "recon gemm sync"));
   if (herr) {
     set_last_error("numerator product: bounded wait expired (code " + std::to_string(herr) + ")");
@@ -1010,9 +1177,11 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   // A page-locked result buffer is written by the kernel directly.  A
   // pageable one is filled before the device copy: the fill touches its fresh
   // pages far faster than a copy into untouched pageable memory would.
+  // The tensor-core path's transpose writes device memory, and one copy then
+  // moves the limbs (the copy engine outruns kernel stores to host memory).
   uint64_t* Nout = reinterpret_cast<uint64_t*>(scratch + oN);
   bool direct = false;
-  if (out->num.pinned()) {
+  if (out->num.pinned() && !R.tc) {
     void* dp = nullptr;
     if (cudaHostGetDevicePointer(&dp, out->num.data(), 0) == cudaSuccess) {
       Nout = static_cast<uint64_t*>(dp);
@@ -1021,7 +1190,7 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
       cudaGetLastError();
     }
   }
-  if (!direct) std::memset(out->num.data(), 0, out->num.size() * 8);
+  if (!out->num.pinned() && !R.tc) std::memset(out->num.data(), 0, out->num.size() * 8);
   std::vector<uint8_t> okh((size_t)nc);
   const int64_t GS = g_stride(LG);
   std::vector<uint32_t> hG((size_t)mp * GS, 0u);
@@ -1076,7 +1245,7 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     rp.N = Nout;
     rp.ok = reinterpret_cast<uint8_t*>(scratch + oK);
     if (R.tc) {
-      ES_CHECK(tc_numerator_pass(R, hG, GS, D_dev, scratch, rp, hGb, st));
+      ES_CHECK(tc_numerator_pass(R, hG, GS, D_dev, scratch, rp, hGb, out->num.data(), hw_threads, st));
     } else {
       k_recon_numerators<<<(unsigned)nc, 256, dyn, st>>>(rp);
       count_launch();

@@ -407,12 +407,29 @@ void LimbBuffer::release() {
   n_ = cap_ = 0;
   pinned_ = false;
   if (b.cap * 8 <= kPinMax) {
-    std::lock_guard<std::mutex> lk(g_blk_mu);
-    if (g_blocks.size() < kKeep && g_kept_bytes + b.cap * 8 <= kKeepBytes) {
-      g_blocks.push_back(b);
-      g_kept_bytes += b.cap * 8;
-      return;
+    // keep it, evicting smaller kept blocks while the list is full: a large
+    // page-locked block costs far more to make again than a small one
+    std::vector<Block> evict;
+    bool kept = false;
+    {
+      std::lock_guard<std::mutex> lk(g_blk_mu);
+      while (g_blocks.size() >= kKeep || g_kept_bytes + b.cap * 8 > kKeepBytes) {
+        size_t small = 0;
+        for (size_t i = 1; i < g_blocks.size(); ++i)
+          if (g_blocks[i].cap < g_blocks[small].cap) small = i;
+        if (g_blocks.empty() || g_blocks[small].cap >= b.cap) break;
+        evict.push_back(g_blocks[small]);
+        g_kept_bytes -= g_blocks[small].cap * 8;
+        g_blocks.erase(g_blocks.begin() + (std::ptrdiff_t)small);
+      }
+      if (g_blocks.size() < kKeep && g_kept_bytes + b.cap * 8 <= kKeepBytes) {
+        g_blocks.push_back(b);
+        g_kept_bytes += b.cap * 8;
+        kept = true;
+      }
     }
+    for (const Block& e : evict) block_delete(e);
+    if (kept) return;
   }
   block_delete(b);
 }
