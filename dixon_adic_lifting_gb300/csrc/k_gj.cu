@@ -261,6 +261,229 @@ __global__ void __launch_bounds__(1024) k_gj_panel(GJParams p, int64_t k0, int k
   }
 }
 
+// ------------------------------------------------------------------ cluster panel
+// The NB = 32 panel for 1024 < n <= 4096, spread over a thread-block cluster of
+// kClCtas CTAs per prime, so that the rows fit in registers and 424 CTAs share
+// the SMs instead of 53.  CTA c of the cluster owns rows c kClRows + tid +
+// kClThreads i (i < kClR) as exact f32 in a rotating frame: at step a the
+// entry of panel column (a + t) mod 32 sits in v[t], so the pivot column is
+// always v[0] and no register is indexed at run time.  Entries are reduced
+// lazily: each step adds at most |f p_t| <= 125^2, so after 32 steps they
+// stay below 2^19 (exact in f32 and in fred's range).  One cluster barrier
+// per step: every warp broadcasts (distributed shared memory) its lowest
+// unused row with a nonzero reduced pivot entry and that row's reduced
+// entries to all CTAs of the cluster; after the barrier every thread takes
+// the lowest of the cluster's 32 candidates as the pivot row, scales it by
+// the pivot's inverse, and updates its rows (exchange form: the pivot
+// column becomes -f p^-1, as in k_gj_panel).  Every decision is taken from
+// the same broadcast data in every CTA, so the control flow (including a
+// prime without a pivot) is uniform over the cluster.  Then the panel is
+// written back, and the CTAs stage U^T and zero the pivot rows column-wise.
+constexpr int kClCtas = 8, kClThreads = 128, kClR = 4, kClRows = kClThreads * kClR;
+constexpr int64_t kClMaxN = (int64_t)kClCtas * kClRows;  // 4096
+constexpr int kClWarps = kClCtas * kClThreads / 32;      // 32 candidates per step
+
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cl_st_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cl_st_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kClThreads) k_gj_panel_cl(GJParams p, int64_t k0, int kb) {
+  constexpr int NBP = 32;
+  const int j = blockIdx.x / kClCtas;
+  if (p.bad[j]) return;  // the same for every CTA of the cluster
+  const uint32_t crank = cl_rank();
+  const ModQ m = c_modq.v[j];
+  const ModF mf{(float)m.q, c_qinv.v[j]};
+  const int n = (int)p.n, ld = (int)p.ld;
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  __shared__ uint8_t s_inv[256];
+  __shared__ int s_wmin[2][kClWarps];
+  __shared__ __align__(16) float s_cand[2][kClWarps][NBP];
+  __shared__ int s_piv[NBP];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gw = (int)crank * (kClThreads / 32) + warp;
+  for (int v = tid; v < (int)m.q; v += kClThreads) s_inv[v] = v ? (uint8_t)inv_mod((uint32_t)v, m) : 0;
+  float v[kClR][NBP];
+  bool used[kClR];
+  int rowi[kClR];
+#pragma unroll
+  for (int i = 0; i < kClR; ++i) {
+    const int row = (int)crank * kClRows + tid + kClThreads * i;
+    rowi[i] = row;
+    const bool active = row < n;
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4) {
+      int4 w = make_int4(0, 0, 0, 0);
+      if (active && k0 + 16 * c4 < ld) w = *reinterpret_cast<const int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4);
+      const uint32_t ww[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[i][c4 * 16 + q4 * 4 + u] = (float)sbyte(ww[q4], u);
+    }
+    used[i] = active ? p.used[(int64_t)j * n + row] != 0 : true;
+  }
+  cl_sync();  // every CTA of the cluster runs before any broadcast reaches it
+#pragma unroll 1
+  for (int a = 0; a < kb; ++a) {
+    const int par = a & 1;
+    // this thread's lowest candidate row (its rows ascend with i)
+    float f[kClR];
+    int cand = INT_MAX, ci = 0;
+#pragma unroll
+    for (int i = kClR - 1; i >= 0; --i) {
+      f[i] = fred(v[i][0], mf);
+      if (!used[i] && f[i] != 0.0f) {
+        cand = rowi[i];
+        ci = i;
+      }
+    }
+    const int wc = __reduce_min_sync(0xffffffffu, cand);
+    const unsigned own = __ballot_sync(0xffffffffu, cand == wc && wc != INT_MAX);
+    float mine = 0.0f;
+    if (wc != INT_MAX) {
+      const int owner = __ffs(own) - 1;
+#pragma unroll
+      for (int t = 0; t < NBP; ++t) {
+        float x = v[0][t];
+#pragma unroll
+        for (int i = 1; i < kClR; ++i) x = ci == i ? v[i][t] : x;
+        x = __shfl_sync(0xffffffffu, x, owner);
+        if (lane == t) mine = fred(x, mf);
+      }
+    }
+#pragma unroll 1
+    for (uint32_t dst = 0; dst < (uint32_t)kClCtas; ++dst) {
+      if (wc != INT_MAX) cl_st_f32(cl_map(&s_cand[par][gw][lane], dst), mine);
+      if (lane == 0) cl_st_s32(cl_map(&s_wmin[par][gw], dst), wc);
+    }
+    cl_sync();
+    int pr = INT_MAX, pw = 0;
+#pragma unroll 4
+    for (int w = 0; w < kClWarps; ++w) {
+      const int x = s_wmin[par][w];
+      if (x < pr) {
+        pr = x;
+        pw = w;
+      }
+    }
+    if (pr == INT_MAX) {  // no pivot in this column: q_j | det A (every CTA sees it)
+      if (crank == 0 && tid == 0) p.bad[j] = 1;
+      cl_sync();
+      return;
+    }
+    // the pivot row scaled by its inverse (rotated frame; entry 0 = the pivot
+    // entry): lane t holds entry t, handed to the update by shuffles
+    float pl;
+    {
+      const float p0 = s_cand[par][pw][0];
+      const int p0i = (int)p0;
+      const float inv = (float)bal_from_unsigned(s_inv[p0i < 0 ? p0i + (int)m.q : p0i], m);
+      pl = lane == 0 ? inv : fred(s_cand[par][pw][lane] * inv, mf);
+    }
+    if (tid == 0) s_piv[a] = pr;
+    if (crank == 0 && tid == 0) p.piv[(int64_t)j * n + k0 + a] = pr;
+    float fe[kClR];  // multiplier per row: -f, 0 for an untouched row; the pivot row takes the scaled row
+    bool isp[kClR];
+#pragma unroll
+    for (int i = 0; i < kClR; ++i) {
+      isp[i] = rowi[i] == pr;
+      fe[i] = isp[i] ? 0.0f : -f[i];
+      if (isp[i]) used[i] = true;
+    }
+    // update and rotate by one in place (column a + 1 becomes entry 0): entry
+    // t - 1 takes the new value of entry t, the last one the new pivot column
+    // (-f p^-1, the scaled pivot entry for the pivot row, the old entry when f = 0)
+    const float p0s = __shfl_sync(0xffffffffu, pl, 0);
+    float last[kClR];
+#pragma unroll
+    for (int i = 0; i < kClR; ++i) last[i] = isp[i] ? p0s : (fe[i] != 0.0f ? fe[i] * p0s : v[i][0]);
+#pragma unroll
+    for (int t = 1; t < NBP; ++t) {
+      const float pt = __shfl_sync(0xffffffffu, pl, t);
+#pragma unroll
+      for (int i = 0; i < kClR; ++i) v[i][t - 1] = isp[i] ? pt : __fmaf_rn(fe[i], pt, v[i][t]);
+    }
+#pragma unroll
+    for (int i = 0; i < kClR; ++i) v[i][NBP - 1] = last[i];
+  }
+  // rotate the frame back: column c at v[c] (kb < 32 only on the last panel)
+  for (int a = kb; a < NBP; ++a)
+#pragma unroll
+    for (int i = 0; i < kClR; ++i) {
+      const float v0 = v[i][0];
+#pragma unroll
+      for (int t = 1; t < NBP; ++t) v[i][t - 1] = v[i][t];
+      v[i][NBP - 1] = v0;
+    }
+  // write back the panel's kb real columns and the used flags
+#pragma unroll
+  for (int i = 0; i < kClR; ++i) {
+    const int row = rowi[i];
+    if (row >= n) continue;
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4) {
+      if (k0 + 16 * c4 >= ld) continue;
+      uint32_t ww[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c4 * 16 + q4 * 4 + u;
+          const uint32_t b = c < kb ? fbyte(fred(v[i][c], mf)) : (uint32_t)(uint8_t)Wj[(int64_t)row * ld + k0 + c];
+          x |= b << (8 * u);
+        }
+        ww[q4] = x;
+      }
+      *reinterpret_cast<int4*>(Wj + (int64_t)row * ld + k0 + 16 * c4) = make_int4(ww[0], ww[1], ww[2], ww[3]);
+    }
+    p.used[(int64_t)j * n + row] = used[i] ? 1 : 0;
+  }
+  __syncthreads();
+  // stage U^T (pivot rows outside the panel) and zero those entries in place;
+  // the cluster's CTAs take interleaved columns
+  int8_t* UTj = p.UT + (int64_t)j * ld * p.utw;
+  for (int col = (int)crank * kClThreads + tid; col < ld; col += kClCtas * kClThreads) {
+    const bool outside = col < k0 || col >= k0 + kb;
+    uint32_t w[NBP / 4];
+#pragma unroll
+    for (int q = 0; q < NBP / 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int a = 4 * q + u;
+        const uint8_t b = (a < kb && outside) ? (uint8_t)Wj[(int64_t)s_piv[a] * ld + col] : (uint8_t)0;
+        x |= (uint32_t)b << (8 * u);
+      }
+      w[q] = x;
+    }
+#pragma unroll
+    for (int c4 = 0; c4 < NBP / 16; ++c4)
+      *reinterpret_cast<int4*>(UTj + (int64_t)col * p.utw + 16 * c4) =
+          make_int4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+    if (outside)
+      for (int a = 0; a < kb; ++a) Wj[(int64_t)s_piv[a] * ld + col] = 0;
+  }
+  cl_sync();  // no CTA leaves while another could still address its shared memory
+}
+
 // Panel in registers (n <= blockDim = 1024): thread i holds row i's NBP panel
 // entries as int32 and applies each exchange step with one multiply-add per
 // entry, without reducing: the pivot column is reduced when it becomes the
@@ -1357,8 +1580,24 @@ InvLayout inverse_layout(int64_t n) {
 // column staged into U^T (at gp.UT, rows of gp.utw bytes) and zeroed in W.
 template <int NBP>
 void panel(GJParams& gp, int64_t n, int64_t k0, int kb, bool use_smem, cudaStream_t st) {
-  k_gj_panel<NBP><<<kNumPrimes, 1024, use_smem ? (size_t)n * NBP + (size_t)n : 0, st>>>(gp, k0, kb,
-                                                                                     use_smem ? 1 : 0);
+  if (NBP == 32 && n > 1024 && n <= kClMaxN) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(kNumPrimes * kClCtas));
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, k_gj_panel_cl, gp, k0, kb);
+  } else {
+    k_gj_panel<NBP><<<kNumPrimes, 1024, use_smem ? (size_t)n * NBP + (size_t)n : 0, st>>>(gp, k0, kb,
+                                                                                       use_smem ? 1 : 0);
+  }
   count_launch();
 }
 

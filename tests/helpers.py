@@ -212,3 +212,27 @@ def check_identity_mod_primes(A, b, num_limbs, W, d, primes=CHECK_PRIMES):
         bd = (b % p) * (d % p) % p
         bad = np.argwhere(AN != bd)
         assert bad.size == 0, (p, bad[:5].tolist())
+
+
+def det_mod_q_gpu(A, q):
+    """det A mod q by Gaussian elimination over GF(q), the same steps as
+    det_mod_q on int64 CUDA tensors (for large n; test infrastructure)."""
+    import torch
+
+    M = torch.as_tensor(np.asarray(A, dtype=np.int64) % q, device="cuda")
+    n = M.shape[0]
+    det = 1
+    for k in range(n):
+        nz = torch.nonzero(M[k:, k])
+        if nz.numel() == 0:
+            return 0
+        p = k + int(nz[0, 0])
+        if p != k:
+            M[[k, p]] = M[[p, k]]
+            det = -det
+        piv = int(M[k, k])
+        det = det * piv % q
+        inv = pow(piv, q - 2, q)
+        f = (M[k + 1:, k] * inv) % q
+        M[k + 1:] = (M[k + 1:] - torch.outer(f, M[k])) % q
+    return det % q
