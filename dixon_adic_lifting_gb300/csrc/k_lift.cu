@@ -501,6 +501,9 @@ __global__ void __launch_bounds__(128) k_lift_crt_mma(const uint8_t* __restrict_
 // One warp per entry: lane l takes primes l and l + 32, the 12 word sums and
 // the fixed-point sum are reduced across the warp, and every lane finishes the
 // (identical) digit; lanes 0..5 store its six limbs.
+// kWeights: V holds the CRT weights c_e in [0, q_e) (as the tensor-core
+// product writes them) instead of balanced residues.
+template <bool kWeights>
 __global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, int64_t nc,
                                                   const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
                                                   uint64_t* __restrict__ xl, XLimbs xo) {
@@ -508,10 +511,12 @@ __global__ void __launch_bounds__(256) k_lift_crt(const int8_t* __restrict__ V, 
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= nc) return;
   const int E = K->E;
-  const int32_t v0 = lane < E ? V[(int64_t)lane * nc + t] : 0;
-  const int32_t v1 = lane + 32 < E ? V[(int64_t)(lane + 32) * nc + t] : 0;
+  const int32_t v0 = lane < E ? (kWeights ? (int32_t)(uint8_t)V[(int64_t)lane * nc + t] : V[(int64_t)lane * nc + t]) : 0;
+  const int32_t v1 =
+      lane + 32 < E ? (kWeights ? (int32_t)(uint8_t)V[(int64_t)(lane + 32) * nc + t] : V[(int64_t)(lane + 32) * nc + t])
+                    : 0;
   uint32_t S[kCrtWords];
-  crt_warp(v0, v1, lane, K, S);
+  crt_warp<kWeights>(v0, v1, lane, K, S);
   uint64_t limb = 0;
 #pragma unroll
   for (int l = 0; l < kDigitLimbs; ++l)
@@ -781,6 +786,7 @@ namespace {
 constexpr int64_t kTcMinCols = 16;       // c >= 16: product on tcgen05 (k_lift_tc.cu)
 constexpr int64_t kResidTcMinN = 1024;   // from this n: the residual update on tcgen05 (k_lift_tc.cu)
 constexpr int64_t kCrtThreadMin = 32768;  // from this many entries: one thread per entry
+constexpr int64_t kCrtMmaMin = 32768;     // tensor-core product path: from this many entries the CRT on mma.sync
 struct LiftLayout {
   size_t K, R, V, r, xl, A32, R16, A16, X16, Sacc, Bf, Bt, err, bar, total;
 };
@@ -933,15 +939,18 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     }
     if (!run->ev.empty()) cudaEventRecord(ev(2 * i + 1), st);
     count_launch();
-    if (tc)
-      k_lift_crt_mma<<<(unsigned)((nc + 128 * kCrtSub - 1) / (128 * kCrtSub)), 128, 0, st>>>(reinterpret_cast<const uint8_t*>(V), nc, K,
-                                                                   digits_dev + (size_t)i * nc * kDigitLimbs, xl, xo);
+    if (tc && nc >= kCrtMmaMin)
+      k_lift_crt_mma<<<(unsigned)((nc + 128 * kCrtSub - 1) / (128 * kCrtSub)), 128, 0, st>>>(
+          reinterpret_cast<const uint8_t*>(V), nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl, xo);
+    else if (tc)  // few entries: one warp each, from the CRT weights
+      k_lift_crt<true><<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
+                                                                 xl, xo);
     else if (nc >= kCrtThreadMin)
       k_lift_crt_thread<<<(unsigned)((nc + 127) / 128), 128, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
                                                                       xl, xo);
     else
-      k_lift_crt<<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs, xl,
-                                                          xo);
+      k_lift_crt<false><<<(unsigned)((nc + 7) / 8), 256, 0, st>>>(V, nc, K, digits_dev + (size_t)i * nc * kDigitLimbs,
+                                                                  xl, xo);
     if (i + 1 < m) {
       const int64_t* rc = r[i & 1];
       int64_t* rn = r[(i + 1) & 1];

@@ -803,9 +803,10 @@ void to_words(const Nat& a, int64_t words, uint32_t* out) {
 int64_t u64_bitlen(uint64_t v) { return v ? 64 - __builtin_clzll(v) : 0; }
 
 // The tensor-core numerator product pays off once there are enough
-// components to fill the GPU with 128-component tiles; its int32 column sums
+// components to fill the GPU with 128-component tiles (measured: at 4096 and
+// 8192 components the per-component kernel is still faster); its int32 column sums
 // stay exact for m' < 2730 (48 m' 2^14 < 2^31).
-constexpr int64_t kReconTcMinComponents = 4096;
+constexpr int64_t kReconTcMinComponents = 16384;
 bool tc_numerators(int64_t nc, int32_t mp) { return nc >= kReconTcMinComponents && mp >= 1 && mp < 2730; }
 struct TcSizes {
   int64_t LGB1 = 0;

@@ -76,11 +76,13 @@ __device__ __forceinline__ void crt_finish(const uint64_t (&acc)[kCrtWords], uin
 }
 
 // Balanced CRT digit of one entry, one warp: lane l contributes the residues
-// v_e of primes e = l and l + 32 (v0, v1; ignored where e >= E').
+// v_e of primes e = l and l + 32 (v0, v1; ignored where e >= E'), or with
+// kWeights their CRT weights c_e = v_e w_e mod q_e.
 //   c_e = v_e w_e mod q_e,  S = sum_e c_e P'/q_e  (12 word columns),
 //   t estimated as floor(sum_e c_e floor(2^50/q_e) / 2^50)
 // The word sums and the estimate are reduced across the warp; every lane
 // finishes the same digit and returns its 12 words in S.
+template <bool kWeights = false>
 __device__ __forceinline__ void crt_warp(int32_t v0, int32_t v1, int lane, const LiftConst* __restrict__ K,
                                          uint32_t (&S)[kCrtWords]) {
   const int E = K->E;
@@ -95,7 +97,8 @@ __device__ __forceinline__ void crt_warp(int32_t v0, int32_t v1, int lane, const
       const ModQ m = K->mq[e];
       const int32_t v = h ? v1 : v0;
       const uint32_t vu = (uint32_t)(v < 0 ? v + (int32_t)m.q : v);
-      const uint32_t ce = barrett(vu * K->w[e], m);
+      // kWeights: the inputs are the CRT weights c_e in [0, q_e) already
+      const uint32_t ce = kWeights ? (uint32_t)v : barrett(vu * K->w[e], m);
       tf += (uint64_t)ce * K->tfix[e];
 #pragma unroll
       for (int l = 0; l < kCrtWords; ++l) acc[l] += (uint64_t)ce * K->Mq[e][l];

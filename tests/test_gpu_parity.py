@@ -418,11 +418,11 @@ def test_device_memory_cap(torch_cuda):
 
 
 @pytest.mark.parametrize("case", ["n32", "hilbert12", "n33c5", "n64c3_int8", "diag7", "n256", "n256c16",
-                                  "n130c33", "hilbert12c400"])
+                                  "n256c64", "n130c127", "hilbert12c1400"])
 def test_device_reconstruction_matches_host_path(torch_cuda, case):
     """The numerators on the GPU against the all-host reconstruction; from
-    4096 components (n256c16, n130c33: a partial 128-component tile;
-    hilbert12c400: dense denominators) on the tensor-core product."""
+    16384 components (n256c64; n130c127: a partial 128-component tile;
+    hilbert12c1400: dense denominators) on the tensor-core product."""
     if case == "n32":
         A, b = n32_case(1)
     elif case == "hilbert12":  # sampled denominators incomplete: a second round is needed
@@ -434,11 +434,13 @@ def test_device_reconstruction_matches_host_path(torch_cuda, case):
         A, b = inputs.uniform(64, 3, -127, 128, seed=65)
     elif case == "n256c16":
         A, b = inputs.uniform(256, 16, -(1 << 23), 1 << 23, seed=256)
-    elif case == "n130c33":
-        A, b = inputs.uniform(130, 33, -(1 << 15), 1 << 15, seed=130)
-    elif case == "hilbert12c400":  # 4800 components whose denominators differ
+    elif case == "n256c64":
+        A, b = inputs.uniform(256, 64, -(1 << 15), 1 << 15, seed=257)
+    elif case == "n130c127":
+        A, b = inputs.uniform(130, 127, -(1 << 15), 1 << 15, seed=130)
+    elif case == "hilbert12c1400":  # 16800 components whose denominators differ
         A = inputs.scaled_hilbert(12)
-        b = np.random.default_rng(12).integers(-(1 << 20), 1 << 20, size=(12, 400), dtype=np.int64)
+        b = np.random.default_rng(12).integers(-(1 << 20), 1 << 20, size=(12, 1400), dtype=np.int64)
     elif case == "diag7":  # component 7 alone carries the denominator 7
         A = np.diag([1] * 7 + [7] + [1] * 8).astype(np.int64)
         A[0, 1:] = 3
