@@ -13,7 +13,7 @@
 //   B     int8   [53][n][ld]       inverses (ld = n rounded up to 16), only good primes read
 //   R     int8   [E'][c][ld]       balanced residues of r_i, column-major per prime, zero padded
 //   V     int8   [E'][n*c]         balanced residues of x_i
-//   r     int64  [2][n*c]          residual (double buffer)
+//   r     int64  [2][n*c]          residual (double buffer; [c][n] with the tensor-core residual update)
 //   xl    uint64 [n*c]             x_i mod 2^64
 //   D     uint64 [m][n*c][6]       the digits
 //   A32   int32  [n][n]            A narrowed when max|A| < 2^31 (else A int64 is read)
@@ -124,12 +124,13 @@ void build_lift_const(const uint8_t* good, LiftConst* K) {
 // ------------------------------------------------------------ kernels
 // r0 = b, R = residues of b.  Thread per entry, row fastest.
 __global__ void k_lift_init(const int64_t* __restrict__ b, int64_t n, int64_t c, int64_t ld,
-                            const LiftConst* __restrict__ K, int64_t* __restrict__ r, int8_t* __restrict__ R) {
+                            const LiftConst* __restrict__ K, int64_t* __restrict__ r, int8_t* __restrict__ R,
+                            int col_major) {
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= n * c) return;
   int64_t row = t % n, col = t / n;
   int64_t v = b[row * c + col];
-  r[row * c + col] = v;
+  r[col_major ? t : row * c + col] = v;
   const int E = K->E;
   for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
@@ -376,11 +377,11 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 constexpr int kCrtDStride = 49;  // words per entry row of the parked sums (odd: no bank conflicts)
-constexpr int kCrtSub = 4;       // 128-entry sub-tiles per CTA
+constexpr int kCrtSub = 2;       // 128-entry sub-tiles per CTA
 __global__ void __launch_bounds__(128) k_lift_crt_mma(const uint8_t* __restrict__ V, int64_t nc,
                                                       const LiftConst* __restrict__ K, uint64_t* __restrict__ D,
                                                       uint64_t* __restrict__ xl, XLimbs xo) {
-  __shared__ __align__(16) uint8_t sV[64][128];
+  __shared__ __align__(16) uint8_t sV[64][144];  // rows of 144 bytes: the fragment loads hit distinct banks
   __shared__ uint32_t sD[128 * kCrtDStride];
   __shared__ __align__(16) uint32_t sB[kCrtNTiles * 4 * 32 * 2];
   __shared__ uint64_t sX[kCrtSub * 128];
@@ -396,23 +397,29 @@ __global__ void __launch_bounds__(128) k_lift_crt_mma(const uint8_t* __restrict_
       sPh[tid] = K->Phalf[tid];
     }
   }
+  // 16-byte pieces of the rows (all four of a thread's loads in flight at once);
+  // the next sub-tile's pieces are loaded while this one is worked on
+  const bool wide = (nc & 15) == 0;
+  auto load_tile = [&](int64_t t0, uint4 (&v)[4]) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = tid + 128 * u, e = idx >> 3, q = idx & 7;
+      v[u] = e < E ? *reinterpret_cast<const uint4*>(V + (int64_t)e * nc + t0 + 16 * q) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 pre[4];
+  if (wide && tcta + 128 <= nc) load_tile(tcta, pre);
   for (int sub = 0; sub < kCrtSub; ++sub) {
     const int64_t t0 = tcta + 128 * sub, tt = t0 + tid;
     if (t0 >= nc) break;
     __syncthreads();  // the previous sub-tile's reads of sV are done (and the constants are in place)
-    if ((nc & 15) == 0 && t0 + 128 <= nc) {
-      // 16-byte pieces of the rows: all four of a thread's loads in flight at once
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int idx = tid + 128 * u, e = idx >> 3, q = idx & 7;
-        v[u] = e < E ? *reinterpret_cast<const uint4*>(V + (int64_t)e * nc + t0 + 16 * q) : make_uint4(0, 0, 0, 0);
-      }
+    if (wide && t0 + 128 <= nc) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int idx = tid + 128 * u;
-        *reinterpret_cast<uint4*>(&sV[idx >> 3][16 * (idx & 7)]) = v[u];
+        *reinterpret_cast<uint4*>(&sV[idx >> 3][16 * (idx & 7)]) = pre[u];
       }
+      if (sub + 1 < kCrtSub && wide && t0 + 256 <= nc) load_tile(t0 + 128, pre);
     } else {
 #pragma unroll 8
       for (int e = 0; e < 64; ++e) sV[e][tid] = (e < E && tt < nc) ? V[(int64_t)e * nc + tt] : 0;
@@ -471,12 +478,22 @@ __global__ void __launch_bounds__(128) k_lift_crt_mma(const uint8_t* __restrict_
       for (int j = 0; j < 7; ++j) tf += (uint64_t)col[42 + j] << (8 * j);
       uint32_t S[kCrtWords];
       crt_finish(acc, tf, sP, sPh, S);
-      uint64_t* out = D + tt * kDigitLimbs;
+      // the digit's words go back into this entry's own row, for a coalesced store below
 #pragma unroll
-      for (int l = 0; l < kDigitLimbs; ++l) out[l] = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
+      for (int l = 0; l < kCrtWords; ++l) sD[tid * kCrtDStride + l] = S[l];
       const uint64_t x = (uint64_t)S[0] | ((uint64_t)S[1] << 32);
       xl[tt] = x;
       sX[128 * sub + tid] = x;
+    }
+    __syncthreads();
+    {  // the sub-tile's digits are 48 contiguous bytes per entry: 16-byte stores
+      const int cnt = (int)(nc - t0 < 128 ? nc - t0 : 128);
+      uint8_t* dst = reinterpret_cast<uint8_t*>(D + t0 * kDigitLimbs);
+      for (int ch = tid; ch < 3 * cnt; ch += 128) {
+        const int en = ch / 3, part = ch - 3 * en;
+        const uint32_t* w = sD + en * kCrtDStride + 4 * part;
+        *reinterpret_cast<uint4*>(dst + 16 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
   if (!xo.XL) return;
@@ -900,7 +917,9 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     k_narrow_a<<<(unsigned)((n * ld + 255) / 256), 256, 0, st>>>(A_dev, n, ld, A32);
     ES_CHECK(cuda_status(cudaGetLastError(), "k_narrow_a"));
   }
-  k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R);
+  // the tensor-core residual keeps r column by column ([c][n]), so that forming
+  // r_{i+1} and its residues reads and writes whole columns
+  k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R, na ? 1 : 0);
   ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_init"));
   count_launch(a32 && !na ? 2 : 1);
   run->stream = stream;

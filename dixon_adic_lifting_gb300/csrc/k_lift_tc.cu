@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
   if (warp == 0) {  // TMA producer: the warp runs the loop, one elected lane issues
     int g = 0;      // stages issued by this CTA
     bool stop = false;
+    // B_j is streamed once per step: evict-first, so that the residues, the
+    // residual's operands and the CRT weights stay in L2
+    const uint64_t stream_pol = l2_evict_first();
     for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
       const ProdTile T = prod_tile(t, tiles_m, tiles_n, NT);
       for (int st = 0; st < kstages; ++st, ++g) {
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         if (elect_one()) {
           mbar_expect_tx(full + s, kPTileI8 + 2 * NT * 128);
-          tma_load_3d(sI + s * kPTileI8, &tmB, full + s, 0, 0, (T.e * tiles_m + T.m0 / kBM) * kstages + st);
+          tma_load_3d_hint(sI + s * kPTileI8, &tmB, full + s, 0, 0, (T.e * tiles_m + T.m0 / kBM) * kstages + st,
+                           stream_pol);
           tma_load_3d(sR + (2 * s) * NT * 128, &tmR, full + s, st * kPK, T.n0, T.e);
           tma_load_3d(sR + (2 * s + 1) * NT * 128, &tmR, full + s, st * kPK + kBK, T.n0, T.e);
         }
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // chunk the epilogue folds the accumulator into one 64-bit word per column,
 // S += sum_s 256^s y_s (mod 2^64), double-buffered in tensor memory so the
 // MMAs of the next chunk overlap the fold.  At the end each plane's S_a is
-// added into Sacc [n][c] (64-bit atomics: addition mod 2^64), which
+// added into Sacc [c][n] (64-bit atomics: addition mod 2^64), which
 // k_lift_r16 turns into r_{i+1} and its residues and clears.
 constexpr int kR2Fold = 16;  // fold every 16 K-blocks (K = 1024)
 constexpr int kR2Threads = 192;
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(kR2Threads, R2Cfg<NC>::CtasPerSm)
       for (int cl = 0; cl < NC; ++cl) {
         const int col = col0 + cl;
         if (col >= c) break;
-        atomicAdd(reinterpret_cast<unsigned long long*>(Sacc + (int64_t)row * c + col), (unsigned long long)S[cl]);
+        atomicAdd(reinterpret_cast<unsigned long long*>(Sacc + (int64_t)col * n + row), (unsigned long long)S[cl]);
       }
     }
   }
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(kR2Threads, R2Cfg<NC>::CtasPerSm)
 // r_{i+1} = (r_i - A x_i) P'^{-1} mod 2^64 from Sacc = A x_i mod 2^64 (which is
 // cleared for the next step), and R16[e][col][i] = its balanced residue mod
 // q_e as f16; one thread per entry, rows fastest so that the stores of a prime
-// are coalesced.  The residual is usually far inside the int32 range
+// are coalesced (r, r_{i+1} and Sacc are stored [c][n]).  The residual is usually far inside the int32 range
 // (|r_{i+1}| < n max|A| / 2 + 1 once the first step is done), so a CTA whose
 // entries all fit takes the one-Barrett path; the reduction constants come
 // from shared memory.
@@ -447,11 +451,10 @@ __global__ void __launch_bounds__(256) k_lift_r16(const int64_t* __restrict__ r,
   const bool live = t < n * c;
   const int64_t col = live ? t / n : 0, i = live ? t - col * n : 0;
   int64_t v = 0;
-  if (live) {
-    const int64_t at = i * c + col;
-    v = (int64_t)(((uint64_t)r[at] - Sacc[at]) * K->Pinv64);
-    rn[at] = v;
-    Sacc[at] = 0;
+  if (live) {  // r, r_{i+1} and Sacc are [c][n]: entry t
+    v = (int64_t)(((uint64_t)r[t] - Sacc[t]) * K->Pinv64);
+    rn[t] = v;
+    Sacc[t] = 0;
   }
   // -2^31 < v < 2^31 - 256: the signed 32-bit reduction applies
   const bool narrow = __syncthreads_and(v > -(int64_t(1) << 31) && v < (int64_t(1) << 31) - 256);

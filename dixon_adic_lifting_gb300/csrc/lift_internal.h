@@ -52,8 +52,8 @@ es_status tc_launch(const TcLift& t, const LiftConst* K, int8_t* V, int64_t n, i
 
 // tcgen05 residual update (k_lift_tc.cu), used with the tcgen05 product when
 // max|A| < 2^31: A and x_i mod 2^64 in balanced 8-bit limbs, A x_i mod 2^64
-// as f16 GEMMs (one per limb plane of A) summed into Sacc [n][c] (zero on
-// entry, cleared again once r_{i+1} is formed).
+// as f16 GEMMs (one per limb plane of A) summed into Sacc [c][n] (zero on
+// entry, cleared again once r_{i+1} is formed; r and r_{i+1} are [c][n] too).
 constexpr int kResidLimbsMax = 4;      // limbs of A (|A| < 2^31)
 constexpr int64_t kResidTcMaxK = 65536;  // na n at most this: int32 sums stay exact
 struct TcResid {
