@@ -2,7 +2,10 @@
 #include "bigint.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
+#include <memory>
+#include <thread>
 
 namespace es {
 namespace big {
@@ -323,18 +326,17 @@ static u128 bits128_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^128
   return (u128)bits_at(x, sh) | ((u128)bits_at(x, sh + 64) << 64);
 }
 
-static inline limb uabs(int64_t v) { return v < 0 ? (limb)(-v) : (limb)v; }
-
-// Both rows of a Lehmer cofactor matrix in one pass:
-//   o0 = A x + B y,  o1 = C x + D y   (|A|, |B|, |C|, |D| < 2^62, results >= 0)
+// Both rows of a Lehmer cofactor matrix over limbs [lo, hi):
+//   o0 = A x + B y,  o1 = C x + D y   (|A|, |B|, |C|, |D| < 2^62)
+// with no carry coming in at lo; the carries out of limb hi - 1 are returned.
 // Each product |coef| * limb is below 2^126, so one signed 128-bit accumulator
 // per output holds the limb sum and a signed carry; the signs are template
 // parameters so the loop has no branches.
 template <bool NA, bool NB, bool NC, bool ND>
-static void lin2x2_pass(limb* o0, limb* o1, const limb* x, size_t xn, const limb* y, size_t yn, size_t len, limb a,
-                        limb b, limb c, limb d) {
+static void lin2x2_range(limb* o0, limb* o1, const limb* x, size_t xn, const limb* y, size_t yn, size_t lo,
+                         size_t hi, limb a, limb b, limb c, limb d, __int128* cr0, __int128* cr1) {
   __int128 c0 = 0, c1 = 0;
-  for (size_t i = 0; i < len; ++i) {
+  for (size_t i = lo; i < hi; ++i) {
     const limb xi = i < xn ? x[i] : 0, yi = i < yn ? y[i] : 0;
     const __int128 pa = (__int128)((u128)a * xi), pb = (__int128)((u128)b * yi);
     const __int128 pc = (__int128)((u128)c * xi), pd = (__int128)((u128)d * yi);
@@ -345,26 +347,38 @@ static void lin2x2_pass(limb* o0, limb* o1, const limb* x, size_t xn, const limb
     c0 = t0 >> 64;
     c1 = t1 >> 64;
   }
-  o0[len] = (limb)c0;
-  o1[len] = (limb)c1;
+  *cr0 = c0;
+  *cr1 = c1;
 }
 
-static void comb2(Nat& o0, Nat& o1, int64_t A, int64_t B, int64_t C, int64_t D, const Nat& x, const Nat& y) {
-  const size_t len = std::max(x.size(), y.size());
-  o0.resize(len + 1);
-  o1.resize(len + 1);
-  const int code = (A < 0) << 3 | (B < 0) << 2 | (C < 0) << 1 | (D < 0);
-  const limb a = uabs(A), b = uabs(B), c = uabs(C), d = uabs(D);
-#define ES_LIN2X2(k)                                                                                              \
-  case k:                                                                                                         \
-    lin2x2_pass<(k >> 3) & 1, (k >> 2) & 1, (k >> 1) & 1, k & 1>(o0.data(), o1.data(), x.data(), x.size(),       \
-                                                                  y.data(), y.size(), len, a, b, c, d);           \
+static inline limb uabs(int64_t v) { return v < 0 ? (limb)(-v) : (limb)v; }
+static int sign_code(int64_t A, int64_t B, int64_t C, int64_t D) {
+  return (A < 0) << 3 | (B < 0) << 2 | (C < 0) << 1 | (D < 0);
+}
+static void comb2_range(int code, limb* o0, limb* o1, const limb* x, size_t xn, const limb* y, size_t yn, size_t lo,
+                        size_t hi, limb a, limb b, limb c, limb d, __int128* cr0, __int128* cr1) {
+#define ES_LIN2X2(k)                                                                                      \
+  case k:                                                                                                 \
+    lin2x2_range<(k >> 3) & 1, (k >> 2) & 1, (k >> 1) & 1, k & 1>(o0, o1, x, xn, y, yn, lo, hi, a, b, c, d, \
+                                                                  cr0, cr1);                              \
     break;
   switch (code) {
     ES_LIN2X2(0) ES_LIN2X2(1) ES_LIN2X2(2) ES_LIN2X2(3) ES_LIN2X2(4) ES_LIN2X2(5) ES_LIN2X2(6) ES_LIN2X2(7)
     ES_LIN2X2(8) ES_LIN2X2(9) ES_LIN2X2(10) ES_LIN2X2(11) ES_LIN2X2(12) ES_LIN2X2(13) ES_LIN2X2(14) ES_LIN2X2(15)
   }
 #undef ES_LIN2X2
+}
+
+// (o0, o1) = (A x + B y, C x + D y) for results known to be >= 0.
+static void comb2(Nat& o0, Nat& o1, int64_t A, int64_t B, int64_t C, int64_t D, const Nat& x, const Nat& y) {
+  const size_t len = std::max(x.size(), y.size());
+  o0.resize(len + 1);
+  o1.resize(len + 1);
+  __int128 c0, c1;
+  comb2_range(sign_code(A, B, C, D), o0.data(), o1.data(), x.data(), x.size(), y.data(), y.size(), 0, len, uabs(A),
+              uabs(B), uabs(C), uabs(D), &c0, &c1);
+  o0[len] = (limb)c0;
+  o1[len] = (limb)c1;
   trim(o0);
   trim(o1);
 }
@@ -424,7 +438,11 @@ static LMat lehmer_sim(__int128 a, __int128 b, __int128 stop) {
 // remainder of at least 2^(nbits - sh) + 2^63 keeps the true one above
 // 2^nbits.  Batches run until no certain step is left, then single
 // division steps finish (a few near the stopping point).
-static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits) {
+// T0, T1 (optional) follow the magnitudes of the cofactors of the second
+// number (r = s r0_in + t r1_in), S0, S1 (optional) those of the first; both
+// alternate in sign from step to step.
+static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits, Nat* S0 = nullptr,
+                   Nat* S1 = nullptr) {
   auto done = [&](const Nat& x) { return nbits < 0 ? x.empty() : le_pow2(x, (size_t)nbits); };
   Nat n0, n1, m0, m1;
   while (!done(r1)) {
@@ -447,6 +465,11 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
           T0->swap(m0);
           T1->swap(m1);
         }
+        if (S0) {
+          comb2(m0, m1, (int64_t)uabs(A), (int64_t)uabs(B), (int64_t)uabs(C), (int64_t)uabs(D), *S0, *S1);
+          S0->swap(m0);
+          S1->swap(m1);
+        }
         *steps += L.k;
         continue;
       }
@@ -462,14 +485,325 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
       T0->swap(*T1);
       T1->swap(t);
     }
+    if (S0) {
+      Nat t = mul(q, *S1);
+      add_in(t, *S0);
+      S0->swap(*S1);
+      S1->swap(t);
+    }
     ++*steps;
   }
 }
 
-bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den) {
+// ------------------------------------------------------------ threaded Lehmer
+// The Lehmer loop of rational_reconstruct with a helper thread: it applies
+// every batch's matrix to the cofactors (T0, T1), taking the matrices in order
+// from a single-producer ring, so the cofactors never hold up the remainders.
+// A plain division step first waits for the ring to drain and then updates
+// the cofactors itself.  (Splitting the remainder updates between threads as
+// well did not pay: the handoff per batch costs what the split saves.)
+namespace {
+inline void spin_wait(int& spins) {
+  if (++spins > 512) std::this_thread::yield();
+}
+
+struct CofactorThread {
+  struct Item {
+    limb a, b, c, d;
+  };
+  static constexpr uint32_t kRing = 512;
+  Item ring[kRing];
+  std::atomic<uint32_t> head{0}, tail{0};
+  std::atomic<bool> quit{false};
+  Nat* T0 = nullptr;
+  Nat* T1 = nullptr;
+  Nat m0, m1;
+  void run() {
+    uint32_t t = 0;
+    for (;;) {
+      int spins = 0;
+      uint32_t h;
+      while ((h = head.load(std::memory_order_acquire)) == t) {
+        if (quit.load(std::memory_order_acquire) && head.load(std::memory_order_acquire) == t) return;
+        spin_wait(spins);
+      }
+      for (; t != h; ++t) {
+        const Item it = ring[t % kRing];
+        // consecutive cofactors alternate in sign: the magnitudes add
+        comb2(m0, m1, (int64_t)it.a, (int64_t)it.b, (int64_t)it.c, (int64_t)it.d, *T0, *T1);
+        T0->swap(m0);
+        T1->swap(m1);
+        tail.store(t + 1, std::memory_order_release);
+      }
+    }
+  }
+  void push(limb a, limb b, limb c, limb d) {
+    const uint32_t h = head.load(std::memory_order_relaxed);
+    int spins = 0;
+    while (h - tail.load(std::memory_order_acquire) >= kRing) spin_wait(spins);
+    ring[h % kRing] = Item{a, b, c, d};
+    head.store(h + 1, std::memory_order_release);
+  }
+  void drain() {
+    const uint32_t h = head.load(std::memory_order_relaxed);
+    int spins = 0;
+    while (tail.load(std::memory_order_acquire) != h) spin_wait(spins);
+  }
+};
+
+constexpr size_t kThreadMinLimbs = 48;  // shorter inputs run on the calling thread alone
+
+// euclid() for rational_reconstruct (T0, T1 tracked, nbits >= 0) with the
+// cofactors on a second thread; false when that thread could not be started
+// (then nothing has changed).
+bool euclid_threads(Nat& r0, Nat& r1, Nat& T0, Nat& T1, size_t* steps, long nbits) {
+  std::unique_ptr<CofactorThread> ct(new CofactorThread);
+  ct->T0 = &T0;
+  ct->T1 = &T1;
+  std::thread tc;
+  try {
+    tc = std::thread([&] { ct->run(); });
+  } catch (...) {
+    return false;
+  }
+  auto done = [&](const Nat& x) { return le_pow2(x, (size_t)nbits); };
+  Nat n0, n1;
+  while (!done(r1)) {
+    if (r1.size() >= 3) {
+      const size_t bl0 = bitlen(r0);
+      const size_t sh = bl0 > 126 ? bl0 - 126 : 0;
+      __int128 stop = (__int128)1 << 63;
+      if ((size_t)nbits >= sh) {
+        const size_t e = (size_t)nbits - sh;
+        stop = e >= 126 ? ((__int128)1 << 126) : stop + ((__int128)1 << e);
+      }
+      const LMat Lm = lehmer_sim((__int128)bits128_at(r0, sh), (__int128)bits128_at(r1, sh), stop);
+      if (Lm.B != 0) {
+        const size_t len = std::max(r0.size(), r1.size());
+        n0.resize(len + 1);
+        n1.resize(len + 1);
+        const int code = sign_code(Lm.A, Lm.B, Lm.C, Lm.D);
+        const limb a = uabs(Lm.A), b = uabs(Lm.B), c = uabs(Lm.C), d = uabs(Lm.D);
+        __int128 h0, h1;
+        comb2_range(code, n0.data(), n1.data(), r0.data(), r0.size(), r1.data(), r1.size(), 0, len, a, b, c, d, &h0,
+                    &h1);
+        n0[len] = (limb)h0;
+        n1[len] = (limb)h1;
+        trim(n0);
+        trim(n1);
+        r0.swap(n0);
+        r1.swap(n1);
+        ct->push(a, b, c, d);
+        *steps += Lm.k;
+        continue;
+      }
+    }
+    // one division step; the cofactor thread has nothing left to do meanwhile
+    ct->drain();
+    Nat q, rem;
+    divmod(r0, r1, &q, &rem);
+    r0.swap(r1);
+    r1.swap(rem);
+    Nat t = mul(q, T1);
+    add_in(t, T0);
+    T0.swap(T1);
+    T1.swap(t);
+    ++*steps;
+  }
+  ct->quit.store(true, std::memory_order_release);
+  tc.join();
+  return true;
+}
+}  // namespace
+
+// ------------------------------------------------------------ half-gcd
+// A run of k Euclid quotient steps on (a, b) as the matrix
+//   Q = Q(q_1) ... Q(q_k),  Q(q) = [[q, 1], [1, 0]],  (a; b) = Q (alpha; beta),
+// entries >= 0, det Q = (-1)^k (odd = k odd).  Then
+//   alpha = (-1)^k (m11 a - m01 b),  beta = (-1)^k (m00 b - m10 a),
+// and m01, m00 are the magnitudes of the cofactors of b in alpha and beta.
+// If alpha > beta > 0, a / b = [q_1; ..., q_{k-1}, q_k + beta / alpha] with
+// every partial term strictly between q_i and q_i + 1, so the q_i are
+// exactly the first k quotients of Euclid on (a, b) and (alpha, beta) its
+// k-th remainder pair.  That check (qmat_apply_split) is the only thing trusted:
+// quotients are computed from leading parts of the numbers, and a matrix
+// that fails it is recomputed more conservatively or dropped.
+struct QMat {
+  Nat m00{1}, m01, m10, m11{1};
+  bool odd = false;
+  bool identity() const { return m01.empty() && m10.empty(); }
+};
+
+static Nat add_prod(const Nat& a, const Nat& b, const Nat& c, const Nat& d) {  // a b + c d
+  Nat r = mul(a, b);
+  add_in(r, mul(c, d));
+  return r;
+}
+static QMat qmat_mul(const QMat& x, const QMat& y) {
+  QMat r;
+  r.m00 = add_prod(x.m00, y.m00, x.m01, y.m10);
+  r.m01 = add_prod(x.m00, y.m01, x.m01, y.m11);
+  r.m10 = add_prod(x.m10, y.m00, x.m11, y.m10);
+  r.m11 = add_prod(x.m10, y.m01, x.m11, y.m11);
+  r.odd = x.odd != y.odd;
+  return r;
+}
+// (alpha, beta) = Q^{-1} (a, b), true when alpha > beta > 0, for
+// a = a1 2^h + a0, b = b1 2^h + b0 (0 <= a0, b0 < 2^h) when
+// (x, y) = Q^{-1} (a1, b1) is known already: alpha = x 2^h + (-1)^k (m11 a0 - m01 b0),
+// beta = y 2^h + (-1)^k (m00 b0 - m10 a0), so only the short low parts are
+// multiplied.
+static bool qmat_apply_split(const QMat& Q, const Nat& x, const Nat& y, const Nat& a0, const Nat& b0, size_t h,
+                             Nat* al, Nat* be) {
+  const Nat p = mul(Q.m11, a0), q = mul(Q.m01, b0), r = mul(Q.m00, b0), t = mul(Q.m10, a0);
+  Nat ap = shl(x, h), bp = shl(y, h);
+  add_in(ap, Q.odd ? q : p);
+  add_in(bp, Q.odd ? t : r);
+  const Nat& am = Q.odd ? p : q;
+  const Nat& bm = Q.odd ? r : t;
+  if (cmp(ap, am) <= 0 || cmp(bp, bm) <= 0) return false;
+  sub_in(ap, am);
+  sub_in(bp, bm);
+  al->swap(ap);
+  be->swap(bp);
+  return cmp(*al, *be) > 0;
+}
+static Nat low_bits(const Nat& a, size_t h) {  // a mod 2^h
+  const size_t w = (h + 63) / 64;
+  Nat r(a.begin(), a.begin() + (ptrdiff_t)std::min(w, a.size()));
+  if (h % 64 && r.size() == w) r[w - 1] &= (~0ull >> (64 - h % 64));
+  trim(r);
+  return r;
+}
+// One plain division step appended to Q: (x, y) -> (y, x mod y).
+static void qmat_step(QMat* Q, Nat* x, Nat* y) {
+  Nat q, rem;
+  divmod(*x, *y, &q, &rem);
+  Nat n00 = mul(Q->m00, q), n10 = mul(Q->m10, q);
+  add_in(n00, Q->m01);
+  add_in(n10, Q->m11);
+  Q->m01.swap(Q->m00);
+  Q->m00.swap(n00);
+  Q->m11.swap(Q->m10);
+  Q->m10.swap(n10);
+  Q->odd = !Q->odd;
+  x->swap(*y);
+  y->swap(rem);
+}
+
+constexpr size_t kHgcdBaseBits = 64 * 64;  // at most this: Lehmer batches on the numbers themselves
+constexpr size_t kHgcdShiftMin = 512;      // a leading part is at least this much shorter than the number
+constexpr size_t kHgcdMargin = 64;         // the leading part stops this far above its share of the target
+constexpr size_t kHgcdTol = 192;           // a stage is done within this many bits of its target
+
+// Euclid steps on (a, b), a > b > 0, while the remainders stay above about
+// 2^s: returns their matrix Q and the remainder pair (alpha, beta) reached
+// (alpha > beta > 0; Q may be the identity when no step is certain).
+//   - small numbers: Lehmer batches (euclid) on the numbers themselves;
+//   - target at most half of a's length away (2 s >= n + kHgcdShiftMin):
+//     the quotients of the leading 2 (n - s) bits, reduced to their own
+//     half (plus a margin), agree with those of (a, b) for all but possibly
+//     the last few; the matrix is checked against (a, b) and recomputed
+//     with a wider margin if the check fails;
+//   - farther: stages, each one reduction of the previous kind over the
+//     leading (n - s) bits, i.e. half of the remaining distance and then the
+//     rest, with one division step wherever a stage makes no progress.
+static void hgcd(const Nat& a, const Nat& b, size_t s, QMat* Q, Nat* al, Nat* be) {
+  const size_t n = bitlen(a);
+  *Q = QMat{};
+  if (bitlen(b) <= s) {
+    *al = a;
+    *be = b;
+    return;
+  }
+  if (n <= kHgcdBaseBits || s < kHgcdShiftMin) {
+    Nat r0 = a, r1 = b, T0, T1 = from_u64(1), S0 = from_u64(1), S1;
+    size_t steps = 0;
+    euclid(r0, r1, &T0, &T1, &steps, (long)s, &S0, &S1);
+    if (r1.empty()) {  // ran into the gcd: keep the pair before the last step (beta > 0)
+      *Q = QMat{};
+      *al = a;
+      *be = b;
+      return;
+    }
+    Q->m00.swap(T1);
+    Q->m01.swap(T0);
+    Q->m10.swap(S1);
+    Q->m11.swap(S0);
+    Q->odd = steps & 1;
+    al->swap(r0);
+    be->swap(r1);
+    return;
+  }
+  if (2 * s >= n + kHgcdShiftMin) {
+    const size_t h = 2 * s - n;
+    const Nat a1 = shr(a, h), b1 = shr(b, h);
+    if (b1.empty() || cmp(a1, b1) <= 0) {
+      *al = a;
+      *be = b;
+      return;
+    }
+    const Nat a0 = low_bits(a, h), b0 = low_bits(b, h);
+    for (size_t margin = kHgcdMargin; margin <= 3 * kHgcdMargin; margin += kHgcdMargin) {
+      QMat Q1;
+      Nat x, y;
+      hgcd(a1, b1, s - h + margin, &Q1, &x, &y);
+      if (Q1.identity()) break;
+      if (qmat_apply_split(Q1, x, y, a0, b0, h, al, be)) {
+        *Q = std::move(Q1);
+        return;
+      }
+    }
+    *Q = QMat{};
+    *al = a;
+    *be = b;
+    return;
+  }
+  Nat x = a, y = b;
+  while (bitlen(y) > s + kHgcdTol) {
+    const size_t nx = bitlen(x);
+    const size_t t = 2 * s >= nx + kHgcdShiftMin ? s : nx - (nx - s) / 2;
+    QMat Qs;
+    Nat x2, y2;
+    hgcd(x, y, t, &Qs, &x2, &y2);
+    if (Qs.identity()) {
+      qmat_step(Q, &x, &y);
+      if (y.empty()) break;  // the gcd: the caller's check rejects beta = 0
+      continue;
+    }
+    if (Q->identity())
+      *Q = std::move(Qs);
+    else
+      *Q = qmat_mul(*Q, Qs);
+    x.swap(x2);
+    y.swap(y2);
+  }
+  al->swap(x);
+  be->swap(y);
+}
+
+bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den,
+                          const ReconOpts& opts) {
   Nat r0 = M, r1 = u, T0, T1 = from_u64(1);
   size_t steps = 0;
-  euclid(r0, r1, &T0, &T1, &steps, (long)nbits);
+  // Long inputs: most of the way by half-gcd stages, kept above 2^nbits; the
+  // exact stopping point is then found by the Lehmer loop below.
+  if (bitlen(M) >= std::max(opts.hgcd_min_bits, kHgcdBaseBits + 1) && !u.empty() && cmp(M, u) > 0 &&
+      bitlen(u) > nbits + 4 * kHgcdTol) {
+    QMat Q;
+    Nat x, y;
+    hgcd(M, u, nbits + kHgcdTol, &Q, &x, &y);
+    if (!y.empty() && cmp(x, y) > 0 && !le_pow2(x, nbits)) {
+      r0.swap(x);
+      r1.swap(y);
+      T0.swap(Q.m01);
+      T1.swap(Q.m00);
+      steps = Q.odd ? 1 : 0;
+    }
+  }
+  const bool threaded = opts.helpers > 0 && r1.size() >= kThreadMinLimbs && !le_pow2(r1, nbits) &&
+                        euclid_threads(r0, r1, T0, T1, &steps, (long)nbits);
+  if (!threaded) euclid(r0, r1, &T0, &T1, &steps, (long)nbits);
   if (T1.empty()) return false;
   *num = r1;
   *num_neg = (steps & 1) && !r1.empty();

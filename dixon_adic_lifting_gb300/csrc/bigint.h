@@ -1,7 +1,7 @@
 // Minimal arbitrary-precision naturals for the host reconstruction stage
 // (64-bit limbs, little-endian, no leading zero limbs; zero = empty).
 // Schoolbook and Karatsuba multiplication, Knuth's Algorithm D division,
-// Lehmer's extended Euclid.
+// Lehmer's extended Euclid (optionally on helper threads), half-gcd stages.
 #pragma once
 
 #include <cstdint>
@@ -31,10 +31,19 @@ Nat shr(const Nat& a, size_t bits);
 // a <= 2^k
 bool le_pow2(const Nat& a, size_t k);
 
+// How rational_reconstruct runs.  helpers > 0: its Lehmer loop updates the
+// cofactors on a second thread.  hgcd_min_bits: from this length of M on,
+// half-gcd stages (subquadratic) do most of the reduction.
+struct ReconOpts {
+  int helpers = 0;
+  size_t hgcd_min_bits = 98304;
+};
 // Extended Euclid on (r0 = M, r1 = u) stopped at the first remainder <= 2^nbits
 // (Wang's rational reconstruction).  Returns den = |t| and num = r with its
-// sign (num_neg), or false when no remainder ever gets that small.
-bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den);
+// sign (num_neg), or false when no remainder ever gets that small.  The
+// result does not depend on opts.
+bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den,
+                          const ReconOpts& opts = ReconOpts());
 Nat gcd(const Nat& a, const Nat& b);
 
 }  // namespace big

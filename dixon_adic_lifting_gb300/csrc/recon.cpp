@@ -144,10 +144,13 @@ void lcm_in(Nat& d, const Nat& v) {
   d = big::mul(d, q);
 }
 
-bool component_denominator(const Nat& M, const Nat& u, int64_t num_bits, int64_t den_bits, Nat* den) {
+bool component_denominator(const Nat& M, const Nat& u, int64_t num_bits, int64_t den_bits, Nat* den, bool helper) {
   Nat num;
   bool neg;
-  return big::rational_reconstruct(M, u, (size_t)num_bits, &num, &neg, den) && big::le_pow2(*den, (size_t)den_bits);
+  big::ReconOpts o;
+  o.helpers = helper ? 1 : 0;
+  return big::rational_reconstruct(M, u, (size_t)num_bits, &num, &neg, den, o) &&
+         big::le_pow2(*den, (size_t)den_bits);
 }
 
 void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
@@ -209,8 +212,9 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
   const int64_t ns = (int64_t)sk.size();
   std::vector<Nat> sden((size_t)ns);
   std::atomic<int> fail(0);
+  const bool helper = denominator_helpers(ns, width);
   parallel_for(ns, threads, [&](int64_t t) {
-    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t])) fail = 1;
+    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t], helper)) fail = 1;
   });
   if (fail) return ES_ERR_INTERNAL;
   Nat d = big::from_u64(1);
@@ -245,8 +249,10 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     // lcm must grow d (a later one may already be covered by an earlier one).
     const Nat before = d;
     std::vector<Nat> fden(failed.size());
+    const bool fhelper = denominator_helpers((int64_t)failed.size(), width);
     parallel_for((int64_t)failed.size(), threads, [&](int64_t t) {
-      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t])) fail = 1;
+      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t], fhelper))
+        fail = 1;
     });
     if (fail) return ES_ERR_INTERNAL;
     for (auto& v : fden) lcm_in(d, v);
@@ -395,7 +401,10 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
     // so u = -num k (mod M) represents it; with 2^(nbits+1) den < M the stopped
     // Euclid must return exactly (num, den), sign included
     if (t % 4 == 1) {
-      Nat den = number(1 + rnd() % 40), k = number(1 + rnd() % 40);
+      // every eighth planted case long enough for the half-gcd stages and the
+      // cofactor thread
+      const size_t lmax = t % 32 == 1 ? 400 : 40;
+      Nat den = number(1 + rnd() % lmax), k = number(1 + rnd() % lmax);
       if (den.empty() || k.empty()) continue;
       Nat M = big::mul(den, k);
       big::add_in(M, big::from_u64(1));
@@ -413,9 +422,38 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
         big::divmod(Nat(num), g, &num, nullptr);
         big::divmod(Nat(den), g, &den, nullptr);
       }
-      Nat rn, rd;
-      bool rneg = false;
-      if (!big::rational_reconstruct(M, u, nbits, &rn, &rneg, &rd) || rn != num || rd != den || rneg != neg) ++bad;
+      // the same result on every way the reconstruction can run
+      for (int way = 0; way < 4; ++way) {
+        big::ReconOpts o;
+        o.helpers = way & 1;
+        if (way & 2) o.hgcd_min_bits = 0;
+        Nat rn, rd;
+        bool rneg = false;
+        if (!big::rational_reconstruct(M, u, nbits, &rn, &rneg, &rd, o) || rn != num || rd != den || rneg != neg)
+          ++bad;
+      }
+    }
+    // a residue with no small fraction behind it: the four ways agree with
+    // the plain one, failure included
+    if (t % 8 == 2) {
+      const size_t ml = 64 + rnd() % 400;
+      Nat M = number(ml);
+      if (M.empty()) continue;
+      Nat u;
+      big::divmod(number(ml), M, nullptr, &u);
+      const size_t nbits = big::bitlen(M) / 2 - rnd() % 64;
+      Nat n0, d0;
+      bool g0 = false;
+      const bool ok0 = big::rational_reconstruct(M, u, nbits, &n0, &g0, &d0);
+      for (int way = 1; way < 4; ++way) {
+        big::ReconOpts o;
+        o.helpers = way & 1;
+        if (way & 2) o.hgcd_min_bits = 0;
+        Nat n1, d1;
+        bool g1 = false;
+        const bool ok1 = big::rational_reconstruct(M, u, nbits, &n1, &g1, &d1, o);
+        if (ok1 != ok0 || (ok0 && (n1 != n0 || d1 != d0 || g1 != g0))) ++bad;
+      }
     }
   }
   return bad;

@@ -246,8 +246,11 @@ int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples);
  * schoolbook product, division (q v + r == u, r < v), shifts, and the
  * rational reconstruction's output (num == +-den u mod M, |num| <= 2^nbits,
  * den > 0), and its exact recovery of planted fractions num / den with
- * 2^(nbits+1) den < M (sign included).  Returns the number of failed checks (0 = pass), or -1 on bad
- * arguments. */
+ * 2^(nbits+1) den < M (sign included; planted denominators up to 400 limbs).
+ * The planted cases, and residues with no small fraction behind them, are
+ * reconstructed every way the library can (plain Lehmer loop, cofactors on a
+ * helper thread, half-gcd stages, both), which must agree exactly.  Returns
+ * the number of failed checks (0 = pass), or -1 on bad arguments. */
 int64_t es_selftest_bigint(uint64_t seed, int64_t rounds);
 
 /* Host self-check of the Gauss-Jordan kernels' f32 residue arithmetic (no
