@@ -4,6 +4,7 @@
 // Lehmer's extended Euclid (optionally on helper threads), half-gcd stages.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <vector>
 
@@ -33,10 +34,14 @@ bool le_pow2(const Nat& a, size_t k);
 
 // How rational_reconstruct runs.  helpers > 0: its Lehmer loop updates the
 // cofactors on a second thread.  hgcd_min_bits: from this length of M on,
-// half-gcd stages (subquadratic) do most of the reduction.
+// half-gcd stages (subquadratic) do most of the reduction.  They are off by
+// default: alone they beat the Lehmer loop only from about 10^5 bits (167 K
+// bits: 7.8 against 9.6 ms on the Grace host), and their many short-lived
+// products scale badly when a whole pool of reconstructions runs at once
+// (sixteen at 166 K bits took 52-75 ms each).
 struct ReconOpts {
   int helpers = 0;
-  size_t hgcd_min_bits = 98304;
+  size_t hgcd_min_bits = SIZE_MAX;
 };
 // Extended Euclid on (r0 = M, r1 = u) stopped at the first remainder <= 2^nbits
 // (Wang's rational reconstruction).  Returns den = |t| and num = r with its
