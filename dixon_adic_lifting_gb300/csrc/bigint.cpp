@@ -495,77 +495,113 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
   }
 }
 
-// ------------------------------------------------------------ threaded Lehmer
-// The Lehmer loop of rational_reconstruct with a helper thread: it applies
-// every batch's matrix to the cofactors (T0, T1), taking the matrices in order
-// from a single-producer ring, so the cofactors never hold up the remainders.
-// A plain division step first waits for the ring to drain and then updates
-// the cofactors itself.  (Splitting the remainder updates between threads as
-// well did not pay: the handoff per batch costs what the split saves.)
+// ------------------------------------------------------------ cofactor pipe
+// The Lehmer loop of rational_reconstruct can hand the cofactor updates to a
+// second thread: every batch's matrix goes, in order, into a single-producer
+// ring, and whoever claims the pipe first applies them to (T0, T1):
+//   - a thread that calls cofactor_pipe_serve() (a pool task beside the run)
+//     claims it and follows the ring until the run closes it;
+//   - the run itself claims it whenever it needs the cofactors and nobody has
+//     (a plain division step, a full ring, the end), and from then on applies
+//     its batches directly; a late serve() then returns at once.
+// So the run never waits for a thread that has not started, and a pool as
+// narrow as one thread still finishes.  A division step with the pipe served
+// waits for the ring to drain, then updates the cofactors itself.  (Splitting
+// the remainder updates between threads as well did not pay: the handoff per
+// batch costs what the split saves.)
 namespace {
 inline void spin_wait(int& spins) {
   if (++spins > 512) std::this_thread::yield();
 }
+}  // namespace
 
-struct CofactorThread {
+struct CofactorPipe {
   struct Item {
     limb a, b, c, d;
   };
-  static constexpr uint32_t kRing = 512;
+  static constexpr uint32_t kRing = 1024;
+  enum : int { kFree = 0, kServed = 1, kOwned = 2 };
   Item ring[kRing];
   std::atomic<uint32_t> head{0}, tail{0};
-  std::atomic<bool> quit{false};
-  Nat* T0 = nullptr;
-  Nat* T1 = nullptr;
+  std::atomic<int> claim{kFree};
+  std::atomic<bool> closed{false};
+  Nat T0, T1{1};  // magnitudes of the cofactors of u in r0 and r1
   Nat m0, m1;
-  void run() {
-    uint32_t t = 0;
+
+  void apply(const Item& it) {
+    // consecutive cofactors alternate in sign: the magnitudes add
+    comb2(m0, m1, (int64_t)it.a, (int64_t)it.b, (int64_t)it.c, (int64_t)it.d, T0, T1);
+    T0.swap(m0);
+    T1.swap(m1);
+  }
+  // the run's side: the cofactors are its own from here on
+  void own() {
+    int expect = kFree;
+    if (claim.compare_exchange_strong(expect, kOwned, std::memory_order_acq_rel)) {
+      const uint32_t h = head.load(std::memory_order_relaxed);
+      for (uint32_t t = tail.load(std::memory_order_relaxed); t != h; ++t) apply(ring[t % kRing]);
+      tail.store(h, std::memory_order_relaxed);
+    }
+  }
+  // the run's side: every batch handed over so far is applied
+  void sync() {
+    if (claim.load(std::memory_order_acquire) == kFree) own();
+    if (claim.load(std::memory_order_acquire) == kServed) {
+      const uint32_t h = head.load(std::memory_order_relaxed);
+      int spins = 0;
+      while (tail.load(std::memory_order_acquire) != h) spin_wait(spins);
+    }
+  }
+  void push(limb a, limb b, limb c, limb d) {
+    if (claim.load(std::memory_order_acquire) == kOwned) {
+      apply(Item{a, b, c, d});
+      return;
+    }
+    const uint32_t h = head.load(std::memory_order_relaxed);
+    if (h - tail.load(std::memory_order_acquire) >= kRing) {
+      own();  // a full ring nobody serves: the run takes the work over
+      if (claim.load(std::memory_order_acquire) == kOwned) {
+        apply(Item{a, b, c, d});
+        return;
+      }
+      int spins = 0;
+      while (h - tail.load(std::memory_order_acquire) >= kRing) spin_wait(spins);
+    }
+    ring[h % kRing] = Item{a, b, c, d};
+    head.store(h + 1, std::memory_order_release);
+  }
+  void serve() {
+    int expect = kFree;
+    if (!claim.compare_exchange_strong(expect, kServed, std::memory_order_acq_rel)) return;
+    uint32_t t = tail.load(std::memory_order_relaxed);
     for (;;) {
       int spins = 0;
       uint32_t h;
       while ((h = head.load(std::memory_order_acquire)) == t) {
-        if (quit.load(std::memory_order_acquire) && head.load(std::memory_order_acquire) == t) return;
+        if (closed.load(std::memory_order_acquire) && head.load(std::memory_order_acquire) == t) return;
         spin_wait(spins);
       }
       for (; t != h; ++t) {
-        const Item it = ring[t % kRing];
-        // consecutive cofactors alternate in sign: the magnitudes add
-        comb2(m0, m1, (int64_t)it.a, (int64_t)it.b, (int64_t)it.c, (int64_t)it.d, *T0, *T1);
-        T0->swap(m0);
-        T1->swap(m1);
+        apply(ring[t % kRing]);
         tail.store(t + 1, std::memory_order_release);
       }
     }
   }
-  void push(limb a, limb b, limb c, limb d) {
-    const uint32_t h = head.load(std::memory_order_relaxed);
-    int spins = 0;
-    while (h - tail.load(std::memory_order_acquire) >= kRing) spin_wait(spins);
-    ring[h % kRing] = Item{a, b, c, d};
-    head.store(h + 1, std::memory_order_release);
-  }
-  void drain() {
-    const uint32_t h = head.load(std::memory_order_relaxed);
-    int spins = 0;
-    while (tail.load(std::memory_order_acquire) != h) spin_wait(spins);
-  }
 };
 
-constexpr size_t kThreadMinLimbs = 48;  // shorter inputs run on the calling thread alone
+CofactorPipe* cofactor_pipe_new() { return new (std::nothrow) CofactorPipe; }
+void cofactor_pipe_free(CofactorPipe* p) { delete p; }
+void cofactor_pipe_serve(CofactorPipe* p) {
+  if (p) p->serve();
+}
 
-// euclid() for rational_reconstruct (T0, T1 tracked, nbits >= 0) with the
-// cofactors on a second thread; false when that thread could not be started
-// (then nothing has changed).
-bool euclid_threads(Nat& r0, Nat& r1, Nat& T0, Nat& T1, size_t* steps, long nbits) {
-  std::unique_ptr<CofactorThread> ct(new CofactorThread);
-  ct->T0 = &T0;
-  ct->T1 = &T1;
-  std::thread tc;
-  try {
-    tc = std::thread([&] { ct->run(); });
-  } catch (...) {
-    return false;
-  }
+namespace {
+constexpr size_t kPipeMinLimbs = 48;  // shorter inputs keep their cofactors on the run's thread
+
+// euclid() for rational_reconstruct (nbits >= 0) with the cofactors kept by
+// the pipe (its T0, T1 are the starting cofactors; on return they are final
+// and the run owns them or has seen every batch applied).
+void euclid_piped(Nat& r0, Nat& r1, CofactorPipe* P, size_t* steps, long nbits) {
   auto done = [&](const Nat& x) { return le_pow2(x, (size_t)nbits); };
   Nat n0, n1;
   while (!done(r1)) {
@@ -582,37 +618,34 @@ bool euclid_threads(Nat& r0, Nat& r1, Nat& T0, Nat& T1, size_t* steps, long nbit
         const size_t len = std::max(r0.size(), r1.size());
         n0.resize(len + 1);
         n1.resize(len + 1);
-        const int code = sign_code(Lm.A, Lm.B, Lm.C, Lm.D);
         const limb a = uabs(Lm.A), b = uabs(Lm.B), c = uabs(Lm.C), d = uabs(Lm.D);
         __int128 h0, h1;
-        comb2_range(code, n0.data(), n1.data(), r0.data(), r0.size(), r1.data(), r1.size(), 0, len, a, b, c, d, &h0,
-                    &h1);
+        comb2_range(sign_code(Lm.A, Lm.B, Lm.C, Lm.D), n0.data(), n1.data(), r0.data(), r0.size(), r1.data(),
+                    r1.size(), 0, len, a, b, c, d, &h0, &h1);
         n0[len] = (limb)h0;
         n1[len] = (limb)h1;
         trim(n0);
         trim(n1);
         r0.swap(n0);
         r1.swap(n1);
-        ct->push(a, b, c, d);
+        P->push(a, b, c, d);
         *steps += Lm.k;
         continue;
       }
     }
-    // one division step; the cofactor thread has nothing left to do meanwhile
-    ct->drain();
+    // one division step, with every earlier batch applied to the cofactors
+    P->sync();
     Nat q, rem;
     divmod(r0, r1, &q, &rem);
     r0.swap(r1);
     r1.swap(rem);
-    Nat t = mul(q, T1);
-    add_in(t, T0);
-    T0.swap(T1);
-    T1.swap(t);
+    Nat t = mul(q, P->T1);
+    add_in(t, P->T0);
+    P->T0.swap(P->T1);
+    P->T1.swap(t);
     ++*steps;
   }
-  ct->quit.store(true, std::memory_order_release);
-  tc.join();
-  return true;
+  P->sync();
 }
 }  // namespace
 
@@ -784,6 +817,13 @@ static void hgcd(const Nat& a, const Nat& b, size_t s, QMat* Q, Nat* al, Nat* be
 
 bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bool* num_neg, Nat* den,
                           const ReconOpts& opts) {
+  // a pipe is closed on every way out, so that a serve() waiting on it returns
+  struct Closer {
+    CofactorPipe* p;
+    ~Closer() {
+      if (p) p->closed.store(true, std::memory_order_release);
+    }
+  } closer{opts.pipe};
   Nat r0 = M, r1 = u, T0, T1 = from_u64(1);
   size_t steps = 0;
   // Long inputs: most of the way by half-gcd stages, kept above 2^nbits; the
@@ -801,9 +841,19 @@ bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bo
       steps = Q.odd ? 1 : 0;
     }
   }
-  const bool threaded = opts.helpers > 0 && r1.size() >= kThreadMinLimbs && !le_pow2(r1, nbits) &&
-                        euclid_threads(r0, r1, T0, T1, &steps, (long)nbits);
-  if (!threaded) euclid(r0, r1, &T0, &T1, &steps, (long)nbits);
+  CofactorPipe* P = opts.pipe;
+  if (P && r1.size() >= kPipeMinLimbs && !le_pow2(r1, nbits) && P->head.load() == 0 &&
+      P->claim.load() != CofactorPipe::kOwned) {
+    // the pipe starts from these cofactors; a server reads them only after
+    // the first batch is handed over
+    P->T0 = T0;
+    P->T1 = T1;
+    euclid_piped(r0, r1, P, &steps, (long)nbits);
+    T0 = P->T0;
+    T1 = P->T1;
+  } else {
+    euclid(r0, r1, &T0, &T1, &steps, (long)nbits);
+  }
   if (T1.empty()) return false;
   *num = r1;
   *num_neg = (steps & 1) && !r1.empty();

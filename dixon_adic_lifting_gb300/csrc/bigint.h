@@ -32,15 +32,25 @@ Nat shr(const Nat& a, size_t bits);
 // a <= 2^k
 bool le_pow2(const Nat& a, size_t k);
 
-// How rational_reconstruct runs.  helpers > 0: its Lehmer loop updates the
-// cofactors on a second thread.  hgcd_min_bits: from this length of M on,
+// A cofactor pipe lets a second thread follow the cofactors of one
+// rational_reconstruct run (ReconOpts::pipe): that thread calls
+// cofactor_pipe_serve() beside the run -- before, during or after it -- and
+// returns once the run is over.  Whichever side claims the work first does
+// it, so the run never waits for a server that has not started.  One pipe
+// per run; a pipe is used once.
+struct CofactorPipe;
+CofactorPipe* cofactor_pipe_new();  // null when out of memory
+void cofactor_pipe_free(CofactorPipe* p);
+void cofactor_pipe_serve(CofactorPipe* p);
+// How rational_reconstruct runs.  pipe: its Lehmer loop hands the cofactor
+// updates to whoever serves the pipe.  hgcd_min_bits: from this length of M on,
 // half-gcd stages (subquadratic) do most of the reduction.  They are off by
 // default: alone they beat the Lehmer loop only from about 10^5 bits (167 K
 // bits: 7.8 against 9.6 ms on the Grace host), and their many short-lived
 // products scale badly when a whole pool of reconstructions runs at once
 // (sixteen at 166 K bits took 52-75 ms each).
 struct ReconOpts {
-  int helpers = 0;
+  CofactorPipe* pipe = nullptr;
   size_t hgcd_min_bits = SIZE_MAX;
 };
 // Extended Euclid on (r0 = M, r1 = u) stopped at the first remainder <= 2^nbits

@@ -1146,11 +1146,10 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     ES_CHECK(cuda_status(cudaStreamSynchronize(st), "sample digits sync"));
     dens->assign(ks.size(), Nat{});
     std::atomic<int> fail(0);
-    const bool helper = denominator_helpers((int64_t)ks.size(), hw_threads);
-    parallel_for((int64_t)ks.size(), hw_threads, [&](int64_t t) {
+    denominators_parallel((int64_t)ks.size(), hw_threads, [&](int64_t t, big::CofactorPipe* pipe) {
       const Nat u = shifted_to_residue(
           assemble_shifted_dc(ps, R.ap, hd.data() + (size_t)t * m * kDigitLimbs, kDigitLimbs), Mhalf, Mhalf1);
-      if (!component_denominator(M, u, num_bits, den_bits, &(*dens)[(size_t)t], helper)) fail = 1;
+      if (!component_denominator(M, u, num_bits, den_bits, &(*dens)[(size_t)t], pipe)) fail = 1;
     });
     return fail ? ES_ERR_INTERNAL : ES_OK;
   };

@@ -144,13 +144,30 @@ void lcm_in(Nat& d, const Nat& v) {
   d = big::mul(d, q);
 }
 
-bool component_denominator(const Nat& M, const Nat& u, int64_t num_bits, int64_t den_bits, Nat* den, bool helper) {
+bool component_denominator(const Nat& M, const Nat& u, int64_t num_bits, int64_t den_bits, Nat* den,
+                           big::CofactorPipe* pipe) {
   Nat num;
   bool neg;
   big::ReconOpts o;
-  o.helpers = helper ? 1 : 0;
+  o.pipe = pipe;
   return big::rational_reconstruct(M, u, (size_t)num_bits, &num, &neg, den, o) &&
          big::le_pow2(*den, (size_t)den_bits);
+}
+
+void denominators_parallel(int64_t count, int width, const std::function<void(int64_t, big::CofactorPipe*)>& run) {
+  std::vector<big::CofactorPipe*> pipes;
+  if (count > 0 && 2 * count <= (int64_t)width) {
+    pipes.assign((size_t)count, nullptr);
+    for (auto& p : pipes) p = big::cofactor_pipe_new();
+  }
+  const int64_t tasks = pipes.empty() ? count : 2 * count;
+  parallel_for(tasks, width, [&](int64_t t) {
+    if (t < count)
+      run(t, pipes.empty() ? nullptr : pipes[(size_t)t]);
+    else
+      big::cofactor_pipe_serve(pipes[(size_t)(t - count)]);
+  });
+  for (auto* p : pipes) big::cofactor_pipe_free(p);
 }
 
 void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
@@ -212,9 +229,8 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
   const int64_t ns = (int64_t)sk.size();
   std::vector<Nat> sden((size_t)ns);
   std::atomic<int> fail(0);
-  const bool helper = denominator_helpers(ns, width);
-  parallel_for(ns, threads, [&](int64_t t) {
-    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t], helper)) fail = 1;
+  denominators_parallel(ns, width, [&](int64_t t, big::CofactorPipe* pipe) {
+    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t], pipe)) fail = 1;
   });
   if (fail) return ES_ERR_INTERNAL;
   Nat d = big::from_u64(1);
@@ -249,9 +265,8 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     // lcm must grow d (a later one may already be covered by an earlier one).
     const Nat before = d;
     std::vector<Nat> fden(failed.size());
-    const bool fhelper = denominator_helpers((int64_t)failed.size(), width);
-    parallel_for((int64_t)failed.size(), threads, [&](int64_t t) {
-      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t], fhelper))
+    denominators_parallel((int64_t)failed.size(), width, [&](int64_t t, big::CofactorPipe* pipe) {
+      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t], pipe))
         fail = 1;
     });
     if (fail) return ES_ERR_INTERNAL;
@@ -320,6 +335,32 @@ extern "C" int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples) 
     }
   }
   return bad;
+}
+
+// rational_reconstruct in one of the ways the library can run it: way & 1: a
+// cofactor pipe served by a second thread that starts before the run (way & 4:
+// after it, so the run keeps the work), way & 2: half-gcd stages from any length.
+static bool reconstruct_way(const es::big::Nat& M, const es::big::Nat& u, size_t nbits, int way, es::big::Nat* num,
+                            bool* neg, es::big::Nat* den) {
+  namespace big = es::big;
+  big::ReconOpts o;
+  if (way & 2) o.hgcd_min_bits = 0;
+  if (!(way & 1)) return big::rational_reconstruct(M, u, nbits, num, neg, den, o);
+  big::CofactorPipe* pipe = big::cofactor_pipe_new();
+  if (!pipe) return false;
+  o.pipe = pipe;
+  bool ok = false;
+  if (way & 4) {
+    ok = big::rational_reconstruct(M, u, nbits, num, neg, den, o);
+    std::thread th([&] { big::cofactor_pipe_serve(pipe); });
+    th.join();
+  } else {
+    std::thread th([&] { big::cofactor_pipe_serve(pipe); });
+    ok = big::rational_reconstruct(M, u, nbits, num, neg, den, o);
+    th.join();
+  }
+  big::cofactor_pipe_free(pipe);
+  return ok;
 }
 
 extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
@@ -423,17 +464,13 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
         big::divmod(Nat(den), g, &den, nullptr);
       }
       // the same result on every way the reconstruction can run
-      for (int way = 0; way < 4; ++way) {
-        big::ReconOpts o;
-        o.helpers = way & 1;
-        if (way & 2) o.hgcd_min_bits = 0;
+      for (int way = 0; way < 6; ++way) {
         Nat rn, rd;
         bool rneg = false;
-        if (!big::rational_reconstruct(M, u, nbits, &rn, &rneg, &rd, o) || rn != num || rd != den || rneg != neg)
-          ++bad;
+        if (!reconstruct_way(M, u, nbits, way, &rn, &rneg, &rd) || rn != num || rd != den || rneg != neg) ++bad;
       }
     }
-    // a residue with no small fraction behind it: the four ways agree with
+    // a residue with no small fraction behind it: the other ways agree with
     // the plain one, failure included
     if (t % 8 == 2) {
       const size_t ml = 64 + rnd() % 400;
@@ -445,13 +482,10 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
       Nat n0, d0;
       bool g0 = false;
       const bool ok0 = big::rational_reconstruct(M, u, nbits, &n0, &g0, &d0);
-      for (int way = 1; way < 4; ++way) {
-        big::ReconOpts o;
-        o.helpers = way & 1;
-        if (way & 2) o.hgcd_min_bits = 0;
+      for (int way = 1; way < 6; ++way) {
         Nat n1, d1;
         bool g1 = false;
-        const bool ok1 = big::rational_reconstruct(M, u, nbits, &n1, &g1, &d1, o);
+        const bool ok1 = reconstruct_way(M, u, nbits, way, &n1, &g1, &d1);
         if (ok1 != ok0 || (ok0 && (n1 != n0 || d1 != d0 || g1 != g0))) ++bad;
       }
     }

@@ -46,13 +46,18 @@ big::Nat shifted_to_residue(big::Nat X, const big::Nat& Mhalf, const big::Nat& M
 void lcm_in(big::Nat& d, const big::Nat& v);
 
 // Rational reconstruction of one component's denominator (Wang; bounds
-// Nb = 2^num_bits, Db = 2^den_bits); false when it does not exist.  With
-// helper = true its Lehmer loop keeps the cofactors on a second thread.
+// Nb = 2^num_bits, Db = 2^den_bits); false when it does not exist.  With a
+// pipe, a pool task serving it (big::cofactor_pipe_serve) can keep the
+// cofactors.
 bool component_denominator(const big::Nat& M, const big::Nat& u, int64_t num_bits, int64_t den_bits,
-                           big::Nat* den, bool helper = false);
-// Whether `count` reconstructions running at once on a pool `width` threads
-// wide leave a core for each one's helper thread.
-inline bool denominator_helpers(int64_t count, int width) { return count > 0 && 2 * count <= (int64_t)width; }
+                           big::Nat* den, big::CofactorPipe* pipe = nullptr);
+// Denominators of `count` components at once on the host pool: run(t, pipe)
+// reconstructs component t (passing the pipe on).  When the pool is at least
+// twice as wide as count, each run gets a pipe and a second pool task serves
+// it (the tasks are taken in index order: the runs come first, so a narrower
+// pool than planned only makes the servers return at once).
+void denominators_parallel(int64_t count, int width,
+                           const std::function<void(int64_t, big::CofactorPipe*)>& run);
 
 // Two's complement little-endian limbs of +-mag into out[0..W).
 void to_limbs(const big::Nat& mag, bool neg, int64_t W, uint64_t* out);
