@@ -23,9 +23,17 @@
 //               barriers, residual update of that row (its row of A stays in
 //               registers for the whole launch when A fits in int32).
 //   warp 7      one thread: producer.  B never changes, so it streams the
-//               CTA's rows of every B_j with cp.async.bulk into a ring of
-//               slots (up to 14 KB) and runs ahead into the next step while the
-//               consumers sit in the grid barriers.
+//               CTA's rows of the streamed B_j with cp.async.bulk into a ring
+//               of slots (up to 14 KB) and runs ahead into the next step while
+//               the consumers sit in the grid barriers.
+// Resident slots.  Most of the CTA's rows of B never leave the SM: the first
+// two slots of every consumer warp (all four of warp 3, the only warp on its
+// lane quarter) sit in tensor memory, written once at the start (each lane
+// keeps the 16-byte chunks it multiplies, 56 words per slot and chunk column:
+// two primes x seven rows), and each step reads them back with tcgen05.ld.
+// Only the other slots (21 of 53 primes at E' = 53) are streamed, which takes
+// about 60 % of the shared-memory traffic (bulk writes plus reads) and of the
+// L2 reads off the product phase.
 // Before the launch, k_lift_relayout copies B once into the order of
 // ownership: CTA g's rows of all primes form one contiguous block, prime-major
 // ([e][t][ld]), so every ring slot (all owned rows of two primes) is filled by
@@ -131,6 +139,48 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// Tensor-memory residency of ring slot s (slot j = s / 7 of consumer warp
+// w = s % 7): the first kResSlots slots of every warp, all slots of warp 3.
+constexpr int kResSlots = 2;
+constexpr int kTmCols = 512;        // allocated tensor-memory columns
+constexpr int kTmSlotCols = 2 * 56;  // two chunk columns x (2 primes x 7 rows x 4 words)
+__device__ __forceinline__ int res_slots(int w) { return w == 3 ? kSlotsPerWarp : kResSlots; }
+__device__ __forceinline__ bool resident(int s) { return s / kConsumerWarps < res_slots(s % kConsumerWarps); }
+// Streamed slots before slot s (the ring's fill order within a step).
+__device__ __forceinline__ int stream_rank(int s) {
+  int k = 0;
+  for (int x = 0; x < s; ++x) k += resident(x) ? 0 : 1;
+  return k;
+}
+// First tensor-memory column of warp w's resident slots (warps w and w + 4
+// share a lane quarter: the second takes the upper columns).
+__device__ __forceinline__ uint32_t tm_col0(int w) { return w >= 4 ? (uint32_t)(kResSlots * kTmSlotCols) : 0u; }
+static_assert(2 * kResSlots * kTmSlotCols <= kTmCols && kSlotsPerWarp * kTmSlotCols <= kTmCols, "tensor memory");
+// 56 consecutive 32-bit tensor-memory columns of this thread's lane (x32 + x16 + x8).
+__device__ __forceinline__ void tm_ld56(uint32_t taddr, uint32_t (&r)[56]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr + 0));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47])
+               : "r"(taddr + 32));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55])
+               : "r"(taddr + 48));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tm_st56(uint32_t taddr, const uint32_t (&r)[56]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               ::"r"(taddr + 0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               ::"r"(taddr + 32), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47])
+               : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               ::"r"(taddr + 48), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55])
+               : "memory");
+}
+
 // Named barrier 1 over the consumer warps only (the producer never joins).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
 // The same barrier, returning the OR of `v` over the consumer threads: every
@@ -272,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
   int32_t* Vs = reinterpret_cast<int32_t*>(xs + a.ld);
   uint64_t* full = reinterpret_cast<uint64_t*>(Vs + kConsumerWarps * kVStride);
   uint64_t* empty = full + a.slots;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(empty + a.slots);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x, G = a.G, n = a.n, ld = a.ld, E = a.E;
@@ -290,7 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(kTmCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -303,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
     bool ok = true;
     for (int step = 0; step < a.m && ok; ++step) {
       for (int s = 0; s < sps; ++s) {
+        if (resident(s)) continue;
         if (use > 0 && !mbar_wait(empty + r, (use - 1) & 1, a.err, kErrEmpty, true)) {
           ok = false;
           break;
@@ -347,8 +406,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
   const uint64_t f0 = h0 ? K->t56[e0] : 0, f1 = h1 ? K->t56[e1] : 0;
   const uint64_t m0 = h0 ? lo64(K->Mq[e0]) : 0, m1 = h1 ? lo64(K->Mq[e1]) : 0;
   const uint64_t P64 = lo64(K->P), Pinv = K->Pinv64;
+  // this warp's resident slots into tensor memory: lane l keeps chunks l and
+  // l + 32 of both primes' rows, 56 words per chunk column
+  const int nres = res_slots(warp);
+  const uint32_t tm_warp = *s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tm_col0(warp);
+  const int8_t* Bg = a.Bf + own_start(g, n, G) * E * ld;  // this CTA's rows, all primes, [e][t][ld]
+  for (int j = 0; j < nres; ++j) {
+    const int s = warp + kConsumerWarps * j;
+#pragma unroll
+    for (int cc = 0; cc < kChunksPerLane; ++cc) {
+      const int ch = lane + 32 * cc;
+      uint32_t w[56];
+#pragma unroll
+      for (int pe = 0; pe < kPP; ++pe)
+#pragma unroll
+        for (int t = 0; t < kConsumerWarps; ++t) {
+          const int e = kPP * s + pe;
+          int4 v = make_int4(0, 0, 0, 0);
+          if (s < sps && e < E && t < rows && ch < bchunks)
+            v = __ldg(reinterpret_cast<const int4*>(Bg + ((int64_t)e * rows + t) * ld) + ch);
+          const int o = (pe * kConsumerWarps + t) * 4;
+          w[o] = (uint32_t)v.x, w[o + 1] = (uint32_t)v.y, w[o + 2] = (uint32_t)v.z, w[o + 3] = (uint32_t)v.w;
+        }
+      tm_st56(tm_warp + (uint32_t)(j * kTmSlotCols + cc * 56), w);
+    }
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  int sstream = 0;  // streamed slots per step
+  for (int s = 0; s < sps; ++s) sstream += resident(s) ? 0 : 1;
   unsigned target = 0;
   unsigned gs = 0;  // fills of all earlier steps
+  // the steps; every way out (the end, or an error that all consumers leave
+  // on together) comes back here to free tensor memory
+  [&]() {
   for (int step = 0; step < a.m; ++step) {
     // This warp's slots are s = warp + 7 j; their primes' residues of r_i go
     // straight to registers (chunks lane and lane + 32 of each row).
@@ -372,8 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
     for (int j = 0; j < kSlotsPerWarp; ++j) {
       const int s = warp + kConsumerWarps * j;
       if (s >= sps) break;
-      const unsigned q = gs + (unsigned)s, r = q % slots, use = q / slots;
-      if (!fail) fail = !mbar_wait(full + r, use & 1, a.err, kErrFull, true);
+      const bool res = j < nres;  // warp-uniform
+      unsigned r = 0;
+      if (!res) {
+        const unsigned q = gs + (unsigned)stream_rank(s), use = q / slots;
+        r = q % slots;
+        if (!fail) fail = !mbar_wait(full + r, use & 1, a.err, kErrFull, true);
+      }
       fail = __any_sync(0xffffffffu, fail);  // warp-uniform: the code below shuffles
       if (fail) break;
       const int eb = kPP * s, np = min(kPP, E - eb);
@@ -386,13 +481,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
 #pragma unroll
       for (int cc = 0; cc < kChunksPerLane; ++cc) {
         const int ch = lane + 32 * cc;
-        if (ch < bchunks) {
-          int4 x[kPP][kConsumerWarps];
+        int4 x[kPP][kConsumerWarps];
+        if (res) {  // every lane: tcgen05.ld is warp-wide
+          uint32_t w[56];
+          tm_ld56(tm_warp + (uint32_t)(j * kTmSlotCols + cc * 56), w);
 #pragma unroll
           for (int pe = 0; pe < kPP; ++pe)
 #pragma unroll
-            for (int t = 0; t < kConsumerWarps; ++t)
-              x[pe][t] = (pe < np && t < rows) ? src[(pe * rows + t) * bchunks + ch] : make_int4(0, 0, 0, 0);
+            for (int t = 0; t < kConsumerWarps; ++t) {
+              const int o = (pe * kConsumerWarps + t) * 4;
+              x[pe][t] = make_int4((int)w[o], (int)w[o + 1], (int)w[o + 2], (int)w[o + 3]);
+            }
+        }
+        if (ch < bchunks) {
+          if (!res) {
+#pragma unroll
+            for (int pe = 0; pe < kPP; ++pe)
+#pragma unroll
+              for (int t = 0; t < kConsumerWarps; ++t)
+                x[pe][t] = (pe < np && t < rows) ? src[(pe * rows + t) * bchunks + ch] : make_int4(0, 0, 0, 0);
+          }
 #pragma unroll
           for (int pe = 0; pe < kPP; ++pe) {
             const int4 y = Rr[j][pe][cc];
@@ -407,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty + r);  // the slot's bytes are in registers now
+      if (!res && lane == 0) mbar_arrive(empty + r);  // the slot's bytes are in registers now
       const int t = (lane >> 2) & 7;           // the row whose total this lane ends with
 #pragma unroll
       for (int pe = 0; pe < kPP; ++pe) {
@@ -415,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
         if ((lane & 3) == 0 && t < rows && pe < np) Vs[t * kVStride + eb + pe] = v;
       }
     }
-    gs += (unsigned)sps;
+    gs += (unsigned)sstream;
     if (csync_or(fail)) return;
     // x_i mod 2^64 of this warp's row, on the short path (see fast_digit_lo),
     // published before the full digit is formed
@@ -493,9 +601,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
     target += G;
     if (grid_sync(a.bar, target, a.err)) return;
   }
+  }();
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  csync();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*s_tmem), "r"(kTmCols));
+  }
 }
 
-size_t fused_smem_fixed(int64_t ld) { return 128 + (size_t)ld * 8 + (size_t)kConsumerWarps * kVStride * 4; }
+size_t fused_smem_fixed(int64_t ld) { return 144 + (size_t)ld * 8 + (size_t)kConsumerWarps * kVStride * 4; }
 
 }  // namespace
 
