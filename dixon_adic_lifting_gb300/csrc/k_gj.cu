@@ -65,9 +65,10 @@ constexpr QInvTable make_qinv_table() {
 }
 __constant__ QInvTable c_qinv = make_qinv_table();
 
-// Exact residue arithmetic in f32 for |x| < 2^20: bal(x) = x - q rint(x fl(1/q))
-// (the quotient estimate errs by less than 1/(16 q), and x / q is never
-// within 1/(2 q) of a half-integer since q is odd).
+// Exact residue arithmetic in f32 for |x| < 2^22: bal(x) = x - q rint(x fl(1/q))
+// (the quotient estimate errs by less than |x| 2^-24 / q < 1/(4 q), and x / q
+// is never within 1/(2 q) of a half-integer since q is odd); the updates keep
+// |x| below 2^21 + 2^10, the range es_selftest_gj_reduction checks.
 struct ModF {
   float q, qinv;
 };
@@ -1285,6 +1286,172 @@ __global__ void __launch_bounds__(256, 2) k_gj_update_mma(GJParams p, const int8
   }
 }
 
+// Depth-128 update (blocks of 128 columns, 1024 < n): as k_gj_update_mma, with
+// two changes.  The sums reach 128 * 125^2 + 125 < 2^21; the f32 accumulator
+// (started at -(2^23 + 128)) stays an exact integer below 2^24 in magnitude,
+// and the residue step is exact up to |v| < 2^22 (its quotient estimate errs
+// by less than 1/(4q) there; es_selftest_gj_reduction checks it exhaustively
+// to 2^21 + 2^10).  U^T's fragments (128 columns x 128 k) no longer fit in
+// registers next to the accumulators at two CTAs per SM, so U^T is widened
+// once into a shared f16 tile laid out like the widened F (256-byte rows,
+// chunk c of row r at c ^ (r & 7)) and read with ldmatrix every tile.
+constexpr int kUpd128Smem = 128 * 256 + 2 * 64 * 128 + 2 * 64 * 128 + 64 * 256;  // Bh, As, Os, Af
+__device__ __forceinline__ int swz256(int r, int c) { return r * 256 + 16 * (c ^ (r & 7)); }
+__global__ void __launch_bounds__(256, 2) k_gj_update_mma128(GJParams p, const int8_t* __restrict__ UT, int utw,
+                                                            int64_t k0, int64_t cbase, int64_t cend, int64_t xb,
+                                                            int64_t xe) {
+  constexpr int KW = 128, KC = KW / 16;
+  const int j = blockIdx.z;
+  if (p.bad[j]) return;
+  const int64_t n = p.n, ld = p.ld;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t colc = cbase + (int64_t)blockIdx.x * 128;
+  const int64_t rowc0 = (int64_t)blockIdx.y * (64 * kUpdRowTiles);
+  const int ntile = (int)min((int64_t)kUpdRowTiles, (n - rowc0 + 63) / 64);
+  int8_t* Wj = p.W + (int64_t)j * n * ld;
+  const int8_t* UTj = UT + (int64_t)j * ld * utw;
+  extern __shared__ __align__(128) uint8_t upd_smem[];
+  uint8_t* Bh = upd_smem;                    // [128][256]: U^T widened to f16
+  uint8_t* As0 = Bh + 128 * 256;             // [2][64][128]: s8 F
+  uint8_t* Os0 = As0 + 2 * 64 * 128;         // [2][64][128]: old tile
+  uint8_t* Af = Os0 + 2 * 64 * 128;          // [64][256]: F widened to f16
+  auto seg_ok = [&](int sg) {
+    const int64_t c0 = colc + 32 * sg;
+    return c0 < ld && c0 < cend && (c0 < xb || c0 >= xe);
+  };
+  auto issue_tile = [&](int k) {
+    const int buf = k & 1;
+    const int64_t rowc = rowc0 + 64 * k;
+    for (int i = tid; i < 64 * KC; i += 256) {
+      const int r = i / KC, c = i % KC;
+      const int64_t row = rowc + r, col = k0 + 16 * c;
+      const bool ok = row < n && col < ld;
+      cp_async16(As0 + buf * 64 * 128 + swz128(r, c), ok ? Wj + row * ld + col : Wj, ok);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + 256 * i, r = idx >> 3, c = idx & 7;
+      const int64_t row = rowc + r, col = colc + 16 * c;
+      const bool ok = row < n && col < ld && seg_ok(c >> 1);
+      cp_async16(Os0 + buf * 64 * 128 + swz128(r, c), ok ? Wj + row * ld + col : Wj, ok);
+    }
+    cp_async_commit();
+  };
+  // U^T as s8 into Af's space first, then widened into Bh
+  for (int i = tid; i < 128 * KC; i += 256) {
+    const int r = i / KC, c = i % KC;
+    const int64_t col = colc + r;
+    cp_async16(Af + r * 128 + 16 * c, col < ld ? UTj + col * utw + 16 * c : UTj, col < ld);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  for (int i = tid; i < 128 * KC; i += 256) {
+    const int r = i / KC, c = i % KC;
+    const int4 w = *reinterpret_cast<const int4*>(Af + r * 128 + 16 * c);
+    uint32_t lo[4], hi[4];
+    s8x4_to_f16((uint32_t)w.x, lo[0], hi[0]);
+    s8x4_to_f16((uint32_t)w.y, lo[1], hi[1]);
+    s8x4_to_f16((uint32_t)w.z, lo[2], hi[2]);
+    s8x4_to_f16((uint32_t)w.w, lo[3], hi[3]);
+    *reinterpret_cast<int4*>(Bh + swz256(r, 2 * c)) = make_int4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<int4*>(Bh + swz256(r, 2 * c + 1)) = make_int4(hi[0], hi[1], hi[2], hi[3]);
+  }
+  __syncthreads();  // Af's space is free again
+  issue_tile(0);
+  if (ntile > 1) issue_tile(1);
+  const int mi8 = lane >> 3, rr8 = lane & 7;
+  const int g = lane >> 2, t = lane & 3;
+  const int wr = (warp >> 2) * 32, wc = (warp & 3) * 32;
+  const bool wok = seg_ok(warp & 3);
+  const float qf = (float)c_modq.v[j].q, qinv = c_qinv.v[j];
+  const ModF mf{qf, qinv};
+#pragma unroll 1
+  for (int k = 0; k < ntile; ++k) {
+    const int buf = k & 1;
+    uint8_t* As = As0 + buf * 64 * 128;
+    uint8_t* Os = Os0 + buf * 64 * 128;
+    if (k + 1 < ntile)
+      cp_async_wait<1>();
+    else
+      cp_async_wait<0>();
+    __syncthreads();
+    for (int i = tid; i < 64 * KC; i += 256) {
+      const int r = i / KC, c = i % KC;
+      const int4 w = *reinterpret_cast<const int4*>(As + swz128(r, c));
+      uint32_t lo[4], hi[4];
+      s8x4_to_f16((uint32_t)w.x, lo[0], hi[0]);
+      s8x4_to_f16((uint32_t)w.y, lo[1], hi[1]);
+      s8x4_to_f16((uint32_t)w.z, lo[2], hi[2]);
+      s8x4_to_f16((uint32_t)w.w, lo[3], hi[3]);
+      *reinterpret_cast<int4*>(Af + swz256(r, 2 * c)) = make_int4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<int4*>(Af + swz256(r, 2 * c + 1)) = make_int4(hi[0], hi[1], hi[2], hi[3]);
+    }
+    __syncthreads();
+    if (wok) {
+      float acc[2][4][4];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[mi][ni][r] = -8388736.0f;
+#pragma unroll 2
+      for (int G = 0; G < KW / 16; ++G) {  // 16-k group G: f16 chunks 2G (low halves) and 2G + 1 (high halves)
+        uint32_t af[2][4];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+          ldsm_x4(af[mi], Af + swz256(wr + 16 * mi + rr8 + 8 * (mi8 & 1), 2 * G + (mi8 >> 1)));
+        uint32_t bfr[4][2];
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          uint32_t b4[4];  // reg i: column tile 2 np + (i >> 1), chunk 2 G + (i & 1)
+          ldsm_x4(b4, Bh + swz256(wc + 8 * (2 * np + (mi8 >> 1)) + rr8, 2 * G + (mi8 & 1)));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) bfr[2 * np + (i >> 1)][i & 1] = b4[i];
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int ni = 0; ni < 4; ++ni) mma_f16_16x8x16(acc[mi][ni], af[mi], bfr[ni]);
+      }
+      const bool full = colc + wc + 32 <= n;
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int r = wr + 16 * mi + g + 8 * rr, c = wc + 8 * ni + 2 * t;
+            uint16_t* o = reinterpret_cast<uint16_t*>(Os + swz128(r, c >> 4) + (c & 15));
+            const uint32_t ov = *o;
+            const float v0 = __fadd_rn(acc[mi][ni][2 * rr], sbyte_fb(ov, 0));
+            const float v1 = __fadd_rn(acc[mi][ni][2 * rr + 1], sbyte_fb(ov, 1));
+            uint32_t nb = __byte_perm((uint32_t)__float_as_int(__fadd_rn(fred(v0, mf), 12582912.0f)),
+                                      (uint32_t)__float_as_int(__fadd_rn(fred(v1, mf), 12582912.0f)), 0x0040);
+            if (!full) {
+              const int64_t gc = colc + c;
+              if (gc + 1 >= n) nb = gc >= n ? ov : ((nb & 0xFFu) | (ov & 0xFF00u));
+            }
+            *o = (uint16_t)nb;
+          }
+    }
+    __syncthreads();
+    const int64_t rowc = rowc0 + 64 * k;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + 256 * i, r = idx >> 3, c = idx & 7;
+      const int64_t row = rowc + r, col = colc + 16 * c;
+      if (row < n && col < ld && seg_ok(c >> 1))
+        *reinterpret_cast<int4*>(Wj + row * ld + col) = *reinterpret_cast<const int4*>(Os + swz128(r, c));
+    }
+    if (k + 2 < ntile) {
+      __syncthreads();
+      issue_tile(k + 2);
+    }
+  }
+}
+
 // The wide update of the two-partition schedule, with the staging of U folded
 // in.  A CTA owns one 64-column strip of one prime for every row, so it can
 // read U straight from the block's pivot rows before anything writes them:
@@ -1566,7 +1733,8 @@ InvLayout inverse_layout(int64_t n) {
   Layout L;
   InvLayout r;
   r.W = L.add((size_t)kNumPrimes * n * ld);
-  r.UT = L.add((size_t)kNumPrimes * ld * (nbp == 32 ? 64 : nbp));  // NB = 32: two panels' U^T side by side
+  // NB = 32: two panels' U^T side by side (four beyond n = 1024: 128-column blocks)
+  r.UT = L.add((size_t)kNumPrimes * ld * (nbp == 32 ? (n > 1024 ? 128 : 64) : nbp));
   r.piv = L.add((size_t)kNumPrimes * n * 4);
   r.pinv = L.add((size_t)kNumPrimes * n * 4);
   r.used = L.add((size_t)kNumPrimes * n);
@@ -1630,6 +1798,13 @@ es_status run_blocks16(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) 
 //   update every column outside [k0, k0+64) by W[:, k0..k0+64) U^T
 // R2's entries outside the block are staged before any update reached them,
 // as the formula needs.  The number of full passes over W halves.
+//
+// Beyond n = 1024 the blocks are 128 columns wide, two such halves H0, H1 of
+// 64 in turn: H0 as above (its U^T staged for every column outside each
+// panel), then H1 brought up to date by F_H0 U_H0, H1 as above, then H0's
+// columns by F_H1 U_H1 (H1's pivot rows staged from them after H0 was done),
+// and every column outside the block gets ONE depth-128 update
+// (k_gj_update_mma128): half the passes over W of 64-column blocks.
 es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) {
   ES_CHECK(cuda_status(cudaFuncSetAttribute(k_gj_panel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)kPanelSmemLimit + 1024),
@@ -1638,9 +1813,38 @@ es_status run_blocks64(GJParams& gp, int64_t n, bool use_smem, cudaStream_t st) 
   const int64_t ld = gp.ld;
   const unsigned rtiles = (unsigned)((n + 64 * kUpdRowTiles - 1) / (64 * kUpdRowTiles));
   const dim3 wide((unsigned)((ld + 127) / 128), rtiles, kNumPrimes);
+  const dim3 narrow(1, rtiles, kNumPrimes);
   const bool reg_block = n <= 1024;  // the whole block in one launch, panel in registers
+  int64_t kstart = 0;
+  if (!reg_block) {
+    ES_CHECK(cuda_status(cudaFuncSetAttribute(k_gj_update_mma128, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              kUpd128Smem),
+                         "update128 smem attribute"));
+    gp.utw = 128;
+    for (; kstart + 128 <= n; kstart += 128) {
+      const int64_t k0 = kstart, k1 = k0 + 32, k2 = k0 + 64, k3 = k0 + 96;
+      gp.UT = UT;
+      panel<32>(gp, n, k0, 32, use_smem, st);
+      k_gj_update_mma<32><<<narrow, 256, 0, st>>>(gp, UT, 128, k0, k1, k1 + 32, k0, k1);
+      gp.UT = UT + 32;
+      panel<32>(gp, n, k1, 32, use_smem, st);
+      k_gj_update_mma<32><<<narrow, 256, 0, st>>>(gp, UT + 32, 128, k1, k0, k0 + 32, k1, k1 + 32);
+      k_gj_update_mma<64><<<narrow, 256, 0, st>>>(gp, UT, 128, k0, k2, k2 + 64, k0, k2);
+      gp.UT = UT + 64;
+      panel<32>(gp, n, k2, 32, use_smem, st);
+      k_gj_update_mma<32><<<narrow, 256, 0, st>>>(gp, UT + 64, 128, k2, k3, k3 + 32, k2, k3);
+      gp.UT = UT + 96;
+      panel<32>(gp, n, k3, 32, use_smem, st);
+      k_gj_update_mma<32><<<narrow, 256, 0, st>>>(gp, UT + 96, 128, k3, k2, k2 + 32, k3, k3 + 32);
+      k_gj_update_mma<64><<<narrow, 256, 0, st>>>(gp, UT + 64, 128, k2, k0, k0 + 64, k2, k2 + 64);
+      gp.UT = UT;
+      k_gj_update_mma128<<<wide, 256, kUpd128Smem, st>>>(gp, UT, 128, k0, 0, ld, k0, k0 + 128);
+      count_launch(7);
+    }
+  }
+  gp.UT = UT;
   gp.utw = 64;
-  for (int64_t k0 = 0; k0 < n; k0 += 64) {
+  for (int64_t k0 = kstart; k0 < n; k0 += 64) {
     const int kb1 = (int)((n - k0) < 32 ? (n - k0) : 32);
     const int64_t k1 = k0 + 32;
     const bool two = k1 < n;
@@ -1907,7 +2111,7 @@ extern "C" int64_t es_selftest_gj_reduction(void) {
   for (int j = 0; j < kNumPrimes; ++j) {
     const int32_t q = (int32_t)kPrimes[j], h = (q - 1) / 2;
     const ModF mf{(float)q, qi.v[j]};
-    for (int32_t x = -(1 << 20) + 1; x < (1 << 20); ++x) {
+    for (int32_t x = -(1 << 21) - 1024; x <= (1 << 21) + 1024; ++x) {
       int32_t r = x % q;
       if (r > h) r -= q;
       if (r < -h) r += q;

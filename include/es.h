@@ -256,12 +256,13 @@ int64_t es_selftest_bigint(uint64_t seed, int64_t rounds);
 
 /* Host self-check of the Gauss-Jordan kernels' f32 residue arithmetic (no
  * GPU; card §Method: the inverse's modular reduction).  The kernels keep row
- * entries as exact f32 integers below 2^20 in magnitude and reduce them as
- * x - q rint(x fl(1/q)) (one fused multiply-add against 1.5 * 2^23, one add,
- * one fused multiply-add); the same source function is run here for every
- * odd prime q < 256 and every integer |x| < 2^20 and compared with the
- * balanced residue by the % operator, together with the byte extraction
- * that stores the result.  Returns the number of mismatches (0 = pass). */
+ * entries as exact f32 integers below 2^20 in magnitude (2^21 + 128 in the
+ * depth-128 update) and reduce them as x - q rint(x fl(1/q)) (one fused
+ * multiply-add against 1.5 * 2^23, one add, one fused multiply-add); the
+ * same source function is run here for every odd prime q < 256 and every
+ * integer |x| <= 2^21 + 2^10 and compared with the balanced residue by the %
+ * operator, together with the byte extraction that stores the result.
+ * Returns the number of mismatches (0 = pass). */
 int64_t es_selftest_gj_reduction(void);
 
 #ifdef __cplusplus

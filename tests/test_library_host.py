@@ -40,8 +40,9 @@ def test_barrett_reduction_matches_mod(lib):
 
 
 def test_gauss_jordan_f32_reduction_is_exact(lib):
-    """The inverse kernels reduce exact f32 integers |x| < 2^20 as
-    x - q rint(x fl(1/q)); every such x and every prime, against %."""
+    """The inverse kernels reduce exact f32 integers (|x| < 2^20, and up to
+    2^21 + 128 in the depth-128 update) as x - q rint(x fl(1/q)); every
+    |x| <= 2^21 + 2^10 and every prime, against %."""
     assert api.selftest_gj_reduction() == 0
 
 
