@@ -117,13 +117,25 @@ struct LiftRun {
   LiftRun& operator=(const LiftRun&) = delete;
   ~LiftRun();  // destroys the events
 };
+// Digits of a few components (c == 1) handed to the host while the fused lift
+// forms them: `host` is a page-locked block mapped into the device's address
+// space (dev, its device address), kStreamRows entries of 8 words per step:
+// entry (i, s) at (i kStreamRows + s) 8 holds the digit of step i of
+// component rows[s] in its first 6 words, and word 7 becomes i + 1 once they
+// are in place (zero before the lift).  Other lift paths leave it untouched.
+constexpr int kStreamRows = 4;
+struct DigitStream {
+  uint64_t* dev = nullptr;
+  const volatile uint64_t* host = nullptr;
+  int64_t rows[kStreamRows] = {-1, -1, -1, -1};
+};
 // stall_barrier: start the fused lift's grid-barrier counter 11 short of
 // wrapping around, so that its first barrier never completes (fault injection
 // of an expiring bounded wait).
 es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                          const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a,
                          char* scratch, void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run,
-                         bool stall_barrier = false);
+                         bool stall_barrier = false, const DigitStream* stream_digits = nullptr);
 es_status run_lift_finish(LiftRun* run);
 es_status run_lift(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                    const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a, char* scratch,
@@ -176,8 +188,25 @@ struct ReconPlan;
 void recon_plan_free(ReconPlan* p);
 es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, const uint8_t* good, int64_t num_bits,
                                int64_t den_bits, const Stats& stats, ReconPlan** out);
+// The components whose denominators seed the common denominator (the first
+// round's sample), for `threads` host threads (0: all cores).
+std::vector<int64_t> recon_samples(int64_t n, int64_t c, int threads);
+// recon_device_prepare, and with a digit stream (ds, its first ns rows the
+// samples) the samples' shifted sums formed from the low digit up as the
+// digits arrive, both on the host pool while the lift runs.  lift_done: an
+// event recorded after the lift's launches; a sample whose digits stop
+// coming once it has completed leaves *pre empty (the reconstruction then
+// reads the digits from the device as usual).
+es_status recon_prepare_overlapped(int64_t n, int64_t c, int32_t m, int32_t mp, const uint8_t* good,
+                                   int64_t num_bits, int64_t den_bits, const Stats& stats, int threads,
+                                   const DigitStream* ds, int ns, void* lift_done, ReconPlan** out,
+                                   std::vector<std::vector<uint64_t>>* pre);
+// pre: the shifted sums (assemble_shifted) of the first round's sampled
+// components, in the order sample_components gives, when they were formed
+// already (from a DigitStream); null or empty: formed here from D_dev.
 es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads, char* scratch,
-                             size_t scratch_bytes, void* stream, struct Solution* out);
+                             size_t scratch_bytes, void* stream, struct Solution* out,
+                             const std::vector<std::vector<uint64_t>>* pre = nullptr);
 
 // Host reconstruction (recon.cpp).  digits [m][n*c][6].
 es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, const uint8_t* good,

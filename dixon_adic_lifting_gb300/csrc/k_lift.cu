@@ -855,7 +855,7 @@ es_status create_events(LiftRun* run, size_t count) {
 es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, int64_t c, const int8_t* B_dev,
                          const uint8_t* good_host, int32_t m, uint64_t* digits_dev, uint64_t max_abs_a,
                          char* scratch, void* stream, KernelTiming* kt, bool allow_fused, LiftRun* run,
-                         bool stall_barrier) {
+                         bool stall_barrier, const DigitStream* stream_digits) {
   cudaStream_t st = (cudaStream_t)stream;
   const bool a32 = max_abs_a < (uint64_t(1) << 31);
   LiftConst hK;
@@ -931,7 +931,7 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
     count_launch();
     if (!run->ev.empty()) cudaEventRecord(ev(0), st);
     es_status fs = fused_lift_launch(fp, Bf, A32, a32 ? nullptr : A_dev, b_dev, K, R, xl, digits_dev, bar, err,
-                                     n, E, m, st);
+                                     n, E, m, st, stream_digits);
     if (fs == ES_OK) {
       if (!run->ev.empty()) cudaEventRecord(ev(1), st);
       count_launch();

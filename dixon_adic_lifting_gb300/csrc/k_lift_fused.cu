@@ -78,6 +78,8 @@ struct FusedArgs {
   int8_t* R;            // [E'][ld] residues of r_i (zero padded), row owners write
   uint64_t* xl;         // [ld] x_i mod 2^64 (zero padded), row owners write
   uint64_t* D;          // [m][n][6] digits
+  uint64_t* hs;         // digit stream into mapped host memory (null: none), see DigitStream
+  int64_t hsrow[kStreamRows];
   unsigned* bar;        // grid barrier arrivals, zero at launch
   int* err;
   int n, ld, E, m, G, slots, slot_bytes;
@@ -552,6 +554,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
         if (lane == l) limb = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
       if (lane < kDigitLimbs) a.D[((int64_t)step * n + k) * kDigitLimbs + lane] = limb;
       if (lane == 0 && limb != xlo) atomicCAS(a.err, 0, kErrDigit);
+      if (a.hs) {  // a streamed row: the limbs, then (after a system-wide fence) the step tag
+        int si = -1;
+#pragma unroll
+        for (int q = 0; q < kStreamRows; ++q)
+          if (a.hsrow[q] == k) si = q;
+        if (si >= 0) {
+          uint64_t* e = a.hs + ((int64_t)step * kStreamRows + si) * 8;
+          if (lane < kDigitLimbs) e[lane] = limb;
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence_system();
+            asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(e + 7), "l"((uint64_t)step + 1) : "memory");
+          }
+        }
+      }
     }
     if (last) break;
     target += G;
@@ -652,7 +669,8 @@ es_status fused_lift_relayout(const FusedPlan& p, const int8_t* B, const LiftCon
 
 es_status fused_lift_launch(const FusedPlan& p, const int8_t* Bf, const int32_t* A32, const int64_t* A64,
                             const int64_t* b, const LiftConst* K, int8_t* R, uint64_t* xl, uint64_t* D,
-                            unsigned* bar, int* err, int64_t n, int E, int32_t m, void* stream) {
+                            unsigned* bar, int* err, int64_t n, int E, int32_t m, void* stream,
+                            const DigitStream* ds) {
   FusedArgs a;
   a.Bf = Bf;
   a.A32 = A32;
@@ -662,6 +680,8 @@ es_status fused_lift_launch(const FusedPlan& p, const int8_t* Bf, const int32_t*
   a.R = R;
   a.xl = xl;
   a.D = D;
+  a.hs = ds ? ds->dev : nullptr;
+  for (int q = 0; q < kStreamRows; ++q) a.hsrow[q] = ds ? ds->rows[q] : -1;
   a.bar = bar;
   a.err = err;
   a.n = (int)n;

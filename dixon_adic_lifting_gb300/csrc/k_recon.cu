@@ -1126,8 +1126,42 @@ static es_status tc_numerator_pass(const ReconPlan& R, const std::vector<uint32_
   return ES_OK;
 }
 
+std::vector<int64_t> recon_samples(int64_t n, int64_t c, int threads) {
+  const int width = threads > 0 ? threads : std::max(1, (int)std::thread::hardware_concurrency());
+  return sample_components(n, c, sample_count(c, width));
+}
+
+es_status recon_prepare_overlapped(int64_t n, int64_t c, int32_t m, int32_t mp, const uint8_t* good,
+                                   int64_t num_bits, int64_t den_bits, const Stats& stats, int threads,
+                                   const DigitStream* ds, int ns, void* lift_done, ReconPlan** out,
+                                   std::vector<std::vector<uint64_t>>* pre) {
+  const int width = threads > 0 ? threads : std::max(1, (int)std::thread::hardware_concurrency());
+  const int nsamp = ds && ds->host ? ns : 0;
+  std::vector<Nat> sums((size_t)nsamp);
+  std::atomic<int> missing(0);
+  es_status ps = ES_OK;
+  const PrimeSet pset = make_prime_set(good);
+  auto lift_over = [&]() {
+    const cudaError_t q = cudaEventQuery((cudaEvent_t)lift_done);
+    if (q == cudaErrorNotReady) return false;
+    if (q != cudaSuccess) cudaGetLastError();
+    return true;
+  };
+  parallel_for(1 + nsamp, width, [&](int64_t t) {
+    if (t == 0) {
+      ps = recon_device_prepare(n, c, m, mp, good, num_bits, den_bits, stats, out);
+    } else if (!assemble_streamed(pset, ds->host, (int)t - 1, kStreamRows, m, lift_over, &sums[(size_t)t - 1])) {
+      missing = 1;
+    }
+  });
+  pre->clear();
+  if (nsamp && !missing) pre->assign(sums.begin(), sums.end());
+  return ps;
+}
+
 es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads, char* scratch,
-                             size_t scratch_bytes, void* stream, Solution* out) {
+                             size_t scratch_bytes, void* stream, Solution* out,
+                             const std::vector<std::vector<uint64_t>>* pre) {
   cudaStream_t st = (cudaStream_t)stream;
   const ReconPlan& R = *plan;
   const int64_t n = R.n, c = R.c, nc = R.nc, num_bits = R.num_bits, den_bits = R.den_bits;
@@ -1156,7 +1190,18 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
   const int64_t per_round = sample_count(c, hw_threads);
   const std::vector<int64_t> sk = sample_components(n, c, per_round);
   std::vector<Nat> sden;
-  ES_CHECK(denominators(sk, &sden));
+  if (pre && pre->size() == sk.size()) {
+    // the samples' shifted sums came in while the lift ran
+    sden.assign(sk.size(), Nat{});
+    std::atomic<int> fail(0);
+    denominators_parallel((int64_t)sk.size(), hw_threads, [&](int64_t t, big::CofactorPipe* pipe) {
+      const Nat u = shifted_to_residue((*pre)[(size_t)t], Mhalf, Mhalf1);
+      if (!component_denominator(M, u, num_bits, den_bits, &sden[(size_t)t], pipe)) fail = 1;
+    });
+    if (fail) return ES_ERR_INTERNAL;
+  } else {
+    ES_CHECK(denominators(sk, &sden));
+  }
   Nat d = big::from_u64(1);
   for (auto& v : sden) lcm_in(d, v);
 

@@ -88,6 +88,7 @@ es_status fused_lift_relayout(const FusedPlan& p, const int8_t* B, const LiftCon
 // ES_ERR_RANGE when the cooperative launch is refused (then nothing ran).
 es_status fused_lift_launch(const FusedPlan& p, const int8_t* Bf, const int32_t* A32, const int64_t* A64,
                             const int64_t* b, const LiftConst* K, int8_t* R, uint64_t* xl, uint64_t* D,
-                            unsigned* bar, int* err, int64_t n, int E, int32_t m, void* stream);
+                            unsigned* bar, int* err, int64_t n, int E, int32_t m, void* stream,
+                            const DigitStream* ds = nullptr);
 
 }  // namespace es

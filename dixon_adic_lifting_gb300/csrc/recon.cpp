@@ -81,6 +81,38 @@ Nat assemble_shifted(const PrimeSet& ps, const uint64_t* base, size_t stride, in
   return X;
 }
 
+bool assemble_streamed(const PrimeSet& ps, const volatile uint64_t* host, int s, int rows, int32_t m,
+                       const std::function<bool()>& lift_over, Nat* out) {
+  Nat X, pw = big::from_u64(1);
+  auto last = std::chrono::steady_clock::now();
+  for (int32_t i = 0; i < m; ++i) {
+    const volatile uint64_t* e = host + ((size_t)i * rows + (size_t)s) * 8;
+    for (uint32_t spins = 1; e[7] != (uint64_t)i + 1; ++spins) {
+      if ((spins & 1023) == 0) {
+        if (lift_over() && e[7] != (uint64_t)i + 1) return false;
+        const auto now = std::chrono::steady_clock::now();
+        if (now - last > std::chrono::seconds(60)) return false;
+        std::this_thread::yield();
+      }
+    }
+    std::atomic_thread_fence(std::memory_order_acquire);
+    uint64_t xp[kDigitLimbs];
+    unsigned __int128 carry = 0;
+    for (int l = 0; l < kDigitLimbs; ++l) {
+      const unsigned __int128 v = (unsigned __int128)e[l] + ps.half6[l] + carry;
+      xp[l] = (uint64_t)v;
+      carry = v >> 64;
+    }
+    int alen = kDigitLimbs;
+    while (alen && xp[alen - 1] == 0) --alen;
+    if (alen) big::add_in(X, big::mul(Nat(xp, xp + alen), pw));
+    if (i + 1 < m) pw = big::mul(pw, ps.P);
+    last = std::chrono::steady_clock::now();
+  }
+  *out = std::move(X);
+  return true;
+}
+
 namespace {
 constexpr int32_t kAssembleLeaf = 24;
 void split_lengths(int32_t len, std::vector<int32_t>& out) {

@@ -47,6 +47,9 @@ struct DeviceState {
   size_t hdigits_size = 0;
   char* recon = nullptr;  // device reconstruction buffers (grow-only)
   size_t recon_size = 0;
+  uint64_t* hstream = nullptr;  // page-locked, mapped: the fused lift's digit stream (grow-only)
+  size_t hstream_words = 0;
+  cudaEvent_t lift_done = nullptr;
   cudaStream_t stream = nullptr;
   int sms = 0;
 };
@@ -56,6 +59,29 @@ int current_device() {
   int d = 0;
   cudaGetDevice(&d);
   return d < kMaxDevices ? d : 0;
+}
+
+// The digit-stream block (page-locked, mapped into the device's address
+// space) and the event that marks the lift's end; false when unavailable.
+bool stream_buffer(DeviceState& dev, size_t words) {
+  if (!dev.lift_done) {
+    if (cudaEventCreateWithFlags(&dev.lift_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      dev.lift_done = nullptr;
+      return false;
+    }
+  }
+  if (words <= dev.hstream_words) return true;
+  if (dev.hstream) cudaFreeHost(dev.hstream);
+  dev.hstream = nullptr;
+  dev.hstream_words = 0;
+  if (cudaHostAlloc((void**)&dev.hstream, words * 8, cudaHostAllocMapped) != cudaSuccess) {
+    cudaGetLastError();
+    dev.hstream = nullptr;
+    return false;
+  }
+  dev.hstream_words = words;
+  return true;
 }
 
 es_status grow_device(void** p, size_t* have, size_t need, size_t cap_left, bool inject) {
@@ -257,16 +283,41 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   int32_t mp = 0;
   const bool on_device = !o.host_recon && recon_device_applicable(n, m, good, num_bits, den_bits, stats, &mp);
   std::unique_ptr<ReconPlan, void (*)(ReconPlan*)> rplan(nullptr, recon_plan_free);
+  // c == 1: the fused lift hands the sampled components' digits to the host
+  // as it forms them, so that their sums are ready when it ends
+  DigitStream ds;
+  int ns = 0;
+  std::vector<std::vector<uint64_t>> pre;
+  if (on_device && c == 1 && !o.step_lift) {
+    const std::vector<int64_t> sk = recon_samples(n, c, o.threads);
+    const size_t words = (size_t)m * kStreamRows * 8;
+    if (sk.size() <= (size_t)kStreamRows && stream_buffer(dev, words)) {
+      std::memset(dev.hstream, 0, words * 8);
+      ds.host = dev.hstream;
+      void* dp = nullptr;
+      if (cudaHostGetDevicePointer(&dp, dev.hstream, 0) == cudaSuccess) {
+        ds.dev = static_cast<uint64_t*>(dp);
+        ns = (int)sk.size();
+        for (int q = 0; q < ns; ++q) ds.rows[q] = sk[(size_t)q];
+      } else {
+        cudaGetLastError();
+        ds.host = nullptr;
+      }
+    }
+  }
   {
     LiftRun lr;
     ES_CHECK(run_lift_start(A, b, n, c, B, good, m, dev.digits, stats.max_abs_a, ws + SL.work, st, &kt,
-                            !o.step_lift, &lr,
-                            o.fault == ES_FAULT_LIFT_WAIT));
+                            !o.step_lift, &lr, o.fault == ES_FAULT_LIFT_WAIT, ns ? &ds : nullptr));
     // while the GPU lifts: the reconstruction's digit-independent constants
+    // and (fused lift) the streamed samples' sums
     es_status ps = ES_OK;
     if (on_device) {
+      const bool streamed = ns && lr.fused &&
+                            cudaEventRecord(dev.lift_done, st) == cudaSuccess;
       ReconPlan* rp = nullptr;
-      ps = recon_device_prepare(n, c, m, mp, good, num_bits, den_bits, stats, &rp);
+      ps = recon_prepare_overlapped(n, c, m, mp, good, num_bits, den_bits, stats, o.threads,
+                                    streamed ? &ds : nullptr, ns, dev.lift_done, &rp, &pre);
       rplan.reset(rp);
     }
     ES_CHECK(run_lift_finish(&lr));
@@ -289,7 +340,8 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
     rs = grow_device(&p, &dev.recon_size, rbytes, 0, false);
     dev.recon = (char*)p;
     t_rec = std::chrono::steady_clock::now();
-    if (rs == ES_OK) rs = reconstruct_device(rplan.get(), dev.digits, o.threads, dev.recon, dev.recon_size, st, &sol->s);
+    if (rs == ES_OK)
+      rs = reconstruct_device(rplan.get(), dev.digits, o.threads, dev.recon, dev.recon_size, st, &sol->s, &pre);
   } else {
     // all digits to the host, reconstruction on the host
     if (dbytes > dev.hdigits_size) {
@@ -527,6 +579,9 @@ es_status es_release_workspace(void) {
   if (d.recon) cudaFree(d.recon);
   d.recon = nullptr;
   d.recon_size = 0;
+  if (d.hstream) cudaFreeHost(d.hstream);
+  d.hstream = nullptr;
+  d.hstream_words = 0;
   d.ws = nullptr;
   d.digits = nullptr;
   d.hdigits = nullptr;
