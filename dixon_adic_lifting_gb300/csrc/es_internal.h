@@ -119,11 +119,15 @@ struct LiftRun {
 };
 // Digits of a few components (c == 1) handed to the host while the fused lift
 // forms them: `host` is a page-locked block mapped into the device's address
-// space (dev, its device address), kStreamRows entries of 8 words per step:
-// entry (i, s) at (i kStreamRows + s) 8 holds the digit of step i of
-// component rows[s] in its first 6 words, and word 7 becomes i + 1 once they
-// are in place (zero before the lift).  Other lift paths leave it untouched.
+// space (dev, its device address), kStreamRows entries of kStreamWords words
+// per step: entry (i, s) at (i kStreamRows + s) kStreamWords holds the digit
+// of step i of component rows[s] as 12 words, word j = 32-bit part j of the
+// digit's six limbs (little-endian) in its low half and the tag i + 1 in its
+// high half.  Each 8-byte store is single-copy atomic, so a word whose tag
+// reads i + 1 holds its part; no fence is needed (zero before the lift).
+// Other lift paths leave the block untouched.
 constexpr int kStreamRows = 4;
+constexpr int kStreamWords = 16;
 struct DigitStream {
   uint64_t* dev = nullptr;
   const volatile uint64_t* host = nullptr;

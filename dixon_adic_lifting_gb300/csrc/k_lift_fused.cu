@@ -554,20 +554,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
         if (lane == l) limb = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
       if (lane < kDigitLimbs) a.D[((int64_t)step * n + k) * kDigitLimbs + lane] = limb;
       if (lane == 0 && limb != xlo) atomicCAS(a.err, 0, kErrDigit);
-      if (a.hs) {  // a streamed row: lane 0 writes the limbs, then the step tag with release semantics
+      if (a.hs) {  // a streamed row: twelve self-tagged words (32 bits of the digit, 32 of tag)
         int si = -1;
 #pragma unroll
         for (int q = 0; q < kStreamRows; ++q)
           if (a.hsrow[q] == k) si = q;
         if (si >= 0) {
-          uint64_t w[kDigitLimbs];
-#pragma unroll
-          for (int l = 0; l < kDigitLimbs; ++l) w[l] = __shfl_sync(0xffffffffu, limb, l);
-          if (lane == 0) {
-            uint64_t* e = a.hs + ((int64_t)step * kStreamRows + si) * 8;
-#pragma unroll
-            for (int l = 0; l < kDigitLimbs; ++l) e[l] = w[l];
-            asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(e + 7), "l"((uint64_t)step + 1) : "memory");
+          const uint64_t part = __shfl_sync(0xffffffffu, limb, (lane >> 1) % kDigitLimbs);
+          if (lane < 2 * kDigitLimbs) {
+            const uint64_t w = ((lane & 1) ? part >> 32 : part & 0xffffffffull) | ((uint64_t)(step + 1) << 32);
+            asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(a.hs + ((int64_t)step * kStreamRows + si) *
+                                                                                 kStreamWords + lane),
+                         "l"(w)
+                         : "memory");
           }
         }
       }

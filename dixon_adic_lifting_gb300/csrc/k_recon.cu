@@ -1150,7 +1150,8 @@ es_status recon_prepare_overlapped(int64_t n, int64_t c, int32_t m, int32_t mp, 
   parallel_for(1 + nsamp, width, [&](int64_t t) {
     if (t == 0) {
       ps = recon_device_prepare(n, c, m, mp, good, num_bits, den_bits, stats, out);
-    } else if (!assemble_streamed(pset, ds->host, (int)t - 1, kStreamRows, m, lift_over, &sums[(size_t)t - 1])) {
+    } else if (!assemble_streamed(pset, ds->host, (int)t - 1, kStreamRows, kStreamWords, m, lift_over,
+                                  &sums[(size_t)t - 1])) {
       missing = 1;
     }
   });

@@ -81,25 +81,29 @@ Nat assemble_shifted(const PrimeSet& ps, const uint64_t* base, size_t stride, in
   return X;
 }
 
-bool assemble_streamed(const PrimeSet& ps, const volatile uint64_t* host, int s, int rows, int32_t m,
+bool assemble_streamed(const PrimeSet& ps, const volatile uint64_t* host, int s, int rows, int words, int32_t m,
                        const std::function<bool()>& lift_over, Nat* out) {
   Nat X, pw = big::from_u64(1);
   auto last = std::chrono::steady_clock::now();
   for (int32_t i = 0; i < m; ++i) {
-    const volatile uint64_t* e = host + ((size_t)i * rows + (size_t)s) * 8;
-    for (uint32_t spins = 1; e[7] != (uint64_t)i + 1; ++spins) {
-      if ((spins & 1023) == 0) {
-        if (lift_over() && e[7] != (uint64_t)i + 1) return false;
-        const auto now = std::chrono::steady_clock::now();
-        if (now - last > std::chrono::seconds(60)) return false;
-        std::this_thread::yield();
+    const volatile uint64_t* e = host + ((size_t)i * rows + (size_t)s) * words;
+    const uint64_t tag = (uint64_t)i + 1;
+    uint64_t w[2 * kDigitLimbs];
+    for (int j = 0; j < 2 * kDigitLimbs; ++j) {
+      for (uint32_t spins = 1; ((w[j] = e[j]) >> 32) != tag; ++spins) {
+        if ((spins & 1023) == 0) {
+          if (lift_over() && (e[j] >> 32) != tag) return false;
+          if (std::chrono::steady_clock::now() - last > std::chrono::seconds(60)) return false;
+          std::this_thread::yield();
+        }
       }
     }
-    std::atomic_thread_fence(std::memory_order_acquire);
+    uint64_t dg[kDigitLimbs];
+    for (int l = 0; l < kDigitLimbs; ++l) dg[l] = (w[2 * l] & 0xffffffffull) | (w[2 * l + 1] << 32);
     uint64_t xp[kDigitLimbs];
     unsigned __int128 carry = 0;
     for (int l = 0; l < kDigitLimbs; ++l) {
-      const unsigned __int128 v = (unsigned __int128)e[l] + ps.half6[l] + carry;
+      const unsigned __int128 v = (unsigned __int128)dg[l] + ps.half6[l] + carry;
       xp[l] = (uint64_t)v;
       carry = v >> 64;
     }

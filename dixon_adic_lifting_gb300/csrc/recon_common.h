@@ -38,11 +38,12 @@ void assemble_plan_init(const PrimeSet& ps, int32_t m, AssemblePlan* ap,
                         const std::vector<big::Nat>* table = nullptr);
 big::Nat assemble_shifted_dc(const PrimeSet& ps, const AssemblePlan& ap, const uint64_t* base, size_t stride);
 // The shifted sum of one streamed component (entry s of every step's `rows`
-// entries of 8 words in `host`: 6 limbs, then the tag step + 1), formed from
-// the low digit up as the digits arrive: X' += (x_i + (P'-1)/2) P'^i, the
-// same value as assemble_shifted.  False when lift_over() says the lift has
-// ended and a digit is still missing (or after a minute without progress).
-bool assemble_streamed(const PrimeSet& ps, const volatile uint64_t* host, int s, int rows, int32_t m,
+// entries of `words` words in `host`: twelve words, each a 32-bit part of the
+// digit's six limbs under the tag step + 1 in its high half), formed from the
+// low digit up as the digits arrive: X' += (x_i + (P'-1)/2) P'^i, the same
+// value as assemble_shifted.  False when lift_over() says the lift has ended
+// and a digit is still missing (or after a minute without progress).
+bool assemble_streamed(const PrimeSet& ps, const volatile uint64_t* host, int s, int rows, int words, int32_t m,
                        const std::function<bool()>& lift_over, big::Nat* out);
 // P'^k for k = 0 .. kmax, one multiplication by P' each
 void power_table(const PrimeSet& ps, int32_t kmax, std::vector<big::Nat>* pw);

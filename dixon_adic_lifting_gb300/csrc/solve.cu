@@ -290,7 +290,7 @@ es_status solve_impl(const int64_t* A_in, const int64_t* b_in, bool host_inputs,
   std::vector<std::vector<uint64_t>> pre;
   if (on_device && c == 1 && !o.step_lift) {
     const std::vector<int64_t> sk = recon_samples(n, c, o.threads);
-    const size_t words = (size_t)m * kStreamRows * 8;
+    const size_t words = (size_t)m * kStreamRows * kStreamWords;
     if (sk.size() <= (size_t)kStreamRows && stream_buffer(dev, words)) {
       std::memset(dev.hstream, 0, words * 8);
       ds.host = dev.hstream;
