@@ -441,7 +441,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
   // the steps; every way out (the end, or an error that all consumers leave
   // on together) comes back here to free tensor memory
   [&]() {
+  // this warp's row in the digit stream (-1: none), and its pending words
+  int si_stream = -1;
+  if (a.hs && own) {
+#pragma unroll
+    for (int q = 0; q < kStreamRows; ++q)
+      if (a.hsrow[q] == k) si_stream = q;
+  }
+  uint64_t hs_part = 0;
+  int hs_step = -1;
+  auto stream_out = [&]() {  // twelve 8-byte words: 32 bits of the digit, 32 of tag
+    if (hs_step >= 0 && lane < 2 * kDigitLimbs) {
+      const uint64_t w = ((lane & 1) ? hs_part >> 32 : hs_part & 0xffffffffull) | ((uint64_t)(hs_step + 1) << 32);
+      asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(a.hs + ((int64_t)hs_step * kStreamRows + si_stream) *
+                                                                           kStreamWords + lane),
+                   "l"(w)
+                   : "memory");
+    }
+    hs_step = -1;
+  };
   for (int step = 0; step < a.m; ++step) {
+    if (si_stream >= 0) stream_out();  // the previous step's digit
     // This warp's slots are s = warp + 7 j; their primes' residues of r_i go
     // straight to registers (chunks lane and lane + 32 of each row).
     int4 Rr[kSlotsPerWarp][kPP][kChunksPerLane];
@@ -554,21 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_lift_fused(const FusedArgs a) {
         if (lane == l) limb = (uint64_t)S[2 * l] | ((uint64_t)S[2 * l + 1] << 32);
       if (lane < kDigitLimbs) a.D[((int64_t)step * n + k) * kDigitLimbs + lane] = limb;
       if (lane == 0 && limb != xlo) atomicCAS(a.err, 0, kErrDigit);
-      if (a.hs) {  // a streamed row: twelve self-tagged words (32 bits of the digit, 32 of tag)
-        int si = -1;
-#pragma unroll
-        for (int q = 0; q < kStreamRows; ++q)
-          if (a.hsrow[q] == k) si = q;
-        if (si >= 0) {
-          const uint64_t part = __shfl_sync(0xffffffffu, limb, (lane >> 1) % kDigitLimbs);
-          if (lane < 2 * kDigitLimbs) {
-            const uint64_t w = ((lane & 1) ? part >> 32 : part & 0xffffffffull) | ((uint64_t)(step + 1) << 32);
-            asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(a.hs + ((int64_t)step * kStreamRows + si) *
-                                                                                 kStreamWords + lane),
-                         "l"(w)
-                         : "memory");
-          }
-        }
+      if (si_stream >= 0) {
+        // a streamed row: its twelve self-tagged words go out at the start of
+        // the next step's products (the last step's at once), so that the
+        // stores to host memory do not hold up this step's second barrier
+        hs_part = __shfl_sync(0xffffffffu, limb, (lane >> 1) % kDigitLimbs);
+        hs_step = step;
+        if (last) stream_out();
       }
     }
     if (last) break;
