@@ -116,6 +116,14 @@ class Clocks:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # the sampler's start-up takes host cores for a while: let it reach its
+        # first sample before the timed region begins (it keeps sampling there)
+        t0 = time.time()
+        while time.time() - t0 < 3.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -431,10 +439,13 @@ def run_gb300(args, rank, local_rank, world):
             s = api.solve_canonical(An, bn)
             times.append((time.perf_counter() - t0) * 1e3)
         e2e_ms = max_over_ranks(sum(times) / len(times), dist, "cuda")
-        # device->host: sampled components' digits (4 x m x 48 B), the numerators
-        # (n c limbs x 8 B), the acceptance flags (n c B) and the good-prime flags
+        # device->host: sampled components' digits (4 x m digits: 48 B each as a
+        # copy, 96 B each as the fused lift's self-tagged stream for c = 1,
+        # n <= 1024), the numerators (n c limbs x 8 B), the acceptance flags
+        # (n c B) and the good-prime flags
+        per_digit = 96 if (c == 1 and n <= 1024) else 48
         e2e = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": int(8 * (n * n + n * c)),
-               "d2h_bytes_per_step": int(min(4, n * c) * s.m * 48 + n * c * s.limbs * 8 + n * c + 53)}
+               "d2h_bytes_per_step": int(min(4, n * c) * s.m * per_digit + n * c * s.limbs * 8 + n * c + 53)}
         s = None
 
     many = None

@@ -123,16 +123,20 @@ void build_lift_const(const uint8_t* good, LiftConst* K) {
 
 // ------------------------------------------------------------ kernels
 // r0 = b, R = residues of b.  Thread per entry, row fastest.
+// r_0 = b and its residues: one thread per entry and prime (the primes'
+// reductions are independent, so they run side by side rather than 53 in a
+// row); the threads of prime 0 also copy the entry.
 __global__ void k_lift_init(const int64_t* __restrict__ b, int64_t n, int64_t c, int64_t ld,
                             const LiftConst* __restrict__ K, int64_t* __restrict__ r, int8_t* __restrict__ R,
                             int col_major) {
-  int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= n * c) return;
-  int64_t row = t % n, col = t / n;
-  int64_t v = b[row * c + col];
-  r[col_major ? t : row * c + col] = v;
-  const int E = K->E;
-  for (int e = 0; e < E; ++e) R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
+  const int64_t nc = n * c;
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= nc * K->E) return;
+  const int e = (int)(u / nc);
+  const int64_t t = u - (int64_t)e * nc, row = t % n, col = t / n;
+  const int64_t v = b[row * c + col];
+  if (e == 0) r[col_major ? t : row * c + col] = v;
+  R[((int64_t)e * c + col) * ld + row] = (int8_t)reduce_i64_bal(v, K->mq[e]);
 }
 
 // 16-byte load with an L2 cache-hint policy (createpolicy).
@@ -919,7 +923,7 @@ es_status run_lift_start(const int64_t* A_dev, const int64_t* b_dev, int64_t n, 
   }
   // the tensor-core residual keeps r column by column ([c][n]), so that forming
   // r_{i+1} and its residues reads and writes whole columns
-  k_lift_init<<<(unsigned)((nc + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R, na ? 1 : 0);
+  k_lift_init<<<(unsigned)((nc * E + 255) / 256), 256, 0, st>>>(b_dev, n, c, ld, K, r[0], R, na ? 1 : 0);
   ES_CHECK(cuda_status(cudaGetLastError(), "k_lift_init"));
   count_launch(a32 && !na ? 2 : 1);
   run->stream = stream;

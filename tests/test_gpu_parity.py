@@ -345,6 +345,21 @@ def test_solve_device_matches_host_and_is_deterministic(torch_cuda):
     assert all(t >= 0 for t in s3.phase_ms) and s3.phase_ms[2] > 0
 
 
+@pytest.mark.parametrize("threads", [1, 2, 5])
+def test_streamed_samples_with_narrow_pools(torch_cuda, threads):
+    """c = 1, n <= 1024: the fused lift streams the sampled components' digits
+    to host pool tasks that assemble them while it runs.  Pools narrower than
+    the task count (one thread: every task in turn on the caller, after the
+    lift has ended) give the same canonical solution."""
+    A, b = inputs.uniform(300, 1, -(1 << 23), 1 << 23, seed=301)
+    At, bt = dev(torch_cuda, A), dev(torch_cuda, b)
+    ref = api.solve_device(At, bt, timing=2)
+    assert ref.top_kernel == "k_lift_fused"
+    s = api.solve_device(At, bt, threads=threads)
+    assert (s.N, s.d) == (ref.N, ref.d)
+    check_identity(A, b, s.N, s.d)
+
+
 def test_edge_cases(torch_cuda):
     # zero right-hand side
     A, _ = inputs.uniform(20, 1, -99, 100, seed=2)
