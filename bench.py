@@ -299,10 +299,10 @@ def roofline_of(fig, workload, hbm_peak, tensor_peak, peak_kind):
 def time_solves(api, torch, At, bt, steps, warmup, one_stream, flush):
     """Warm-up solves, then `steps` solves each bracketed by CUDA events on the
     solve's stream (L2 flushed before each); returns (ms per step, figures)."""
-    for _ in range(warmup):
-        s = api.solve_device(At, bt, one_stream=one_stream)
-    s = None
     stream = torch.cuda.current_stream()
+    for _ in range(warmup):  # the same call as the timed ones
+        s = api.solve_device(At, bt, stream=stream, timing=2, one_stream=one_stream)
+    s = None
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     fig = []
     torch.cuda.synchronize()
@@ -410,10 +410,13 @@ def run_gb300(args, rank, local_rank, world):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     hbm_peak, tensor_peak, peak_kind = load_peaks()
     clocks = Clocks(local_rank)
-    for _ in range(args.warmup):
-        api.solve_device(At, bt, one_stream=args.one_stream)
-    barrier()
+    # the sampler starts before the warm-up, so that the timed solves follow
+    # the warm-up ones with no idle gap (after one the host pool's workers and
+    # the cores are asleep) and still run with the sampler going
     clocks.start()
+    for _ in range(args.warmup):  # the same call as the timed ones
+        api.solve_device(At, bt, stream=torch.cuda.current_stream(), timing=2, one_stream=args.one_stream)
+    barrier()
     step_ms, sols = time_solves(api, torch, At, bt, args.steps, 0, args.one_stream, flush)
     barrier()
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dist, "cuda")
