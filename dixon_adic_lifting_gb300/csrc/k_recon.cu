@@ -70,12 +70,6 @@ struct RParams {
   uint8_t* ok;            // [nc]
 };
 
-__device__ __forceinline__ void mac(uint64_t& lo, uint32_t& hi, uint32_t a, uint32_t b) {
-  uint64_t p = (uint64_t)a * b;
-  lo += p;
-  hi += (lo < p) ? 1u : 0u;
-}
-
 // acc (96 bits, little-endian words) += x y, one carry chain
 __device__ __forceinline__ void mac96(uint32_t (&acc)[3], uint32_t x, uint32_t y) {
   asm("mad.lo.cc.u32 %0, %3, %4, %0;\n\tmadc.hi.cc.u32 %1, %3, %4, %1;\n\taddc.u32 %2, %2, 0;"
@@ -83,116 +77,232 @@ __device__ __forceinline__ void mac96(uint32_t (&acc)[3], uint32_t x, uint32_t y
       : "r"(x), "r"(y));
 }
 
-// From the normalised words Zn[0 .. LG + kZExtra) of Z (in shared memory, Z <
-// b^(LG + 11)): N = bal_Q(Z mod Q) by Barrett's method with the 13-word
-// reciprocal, the acceptance test |N| <= 2^nb, and the two's complement
-// output of component k.  Zlo / Zhi are shared scratch of LG + 1 entries.
-// Called by every thread of the CTA (it synchronises).
-__device__ __forceinline__ void numerator_tail(const RParams& p, int64_t k, uint32_t* Zn, uint64_t* Zlo,
-                                               uint32_t* Zhi) {
+// ---- block-parallel multi-word arithmetic
+// The numerator's big integers live in shared memory as 32-bit words, cut into
+// groups of four (16 bytes) that one thread owns in each round of blockDim
+// groups.  A carry (or borrow) between groups is resolved by a block-wide
+// carry lookahead: a group generates a carry when its own sum overflows and
+// propagates one when its sum is all ones (a borrow: when its difference is
+// zero); with G and P the warp's ballots of the two, the carry into lane l is
+// bit l of 2G + P + c_in, xor P's bit l, and bit 32 of that sum is the carry
+// out of the warp.
+constexpr int kGroup = 4;
+
+struct Scratch {
+  uint32_t g[32], pr[32];
+  int hi[32], lo[32];
+};
+
+// Carry into this thread's group of the current round; *cin is the carry into
+// the round's first group on entry and into the next round's on return.  gen
+// and prop must not both hold.  Called by every thread of the block.
+__device__ __forceinline__ uint32_t carry_in(bool gen, bool prop, uint32_t* cin, Scratch& sc) {
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const uint32_t G = __ballot_sync(~0u, gen), P = __ballot_sync(~0u, prop);
+  if (lane == 0) {
+    sc.g[wp] = G;
+    sc.pr[wp] = P;
+  }
+  __syncthreads();
+  uint64_t c = *cin;
+  uint32_t mine = 0;
+  for (int w = 0; w < nw; ++w) {
+    const uint64_t gw = sc.g[w], pw = sc.pr[w];
+    const uint64_t s = 2 * gw + pw + c;
+    if (w == wp) mine = (uint32_t)(((s ^ pw) >> lane) & 1u);
+    c = (s >> 32) & 1u;
+  }
+  __syncthreads();
+  *cin = (uint32_t)c;
+  return mine;
+}
+
+__device__ __forceinline__ unsigned __int128 ld_group(const uint32_t* Y, int g) {
+  const uint4 v = reinterpret_cast<const uint4*>(Y)[g];
+  return (unsigned __int128)v.x | ((unsigned __int128)v.y << 32) | ((unsigned __int128)v.z << 64) |
+         ((unsigned __int128)v.w << 96);
+}
+
+__device__ __forceinline__ void st_group(uint32_t* Y, int g, unsigned __int128 v) {
+  reinterpret_cast<uint4*>(Y)[g] = make_uint4((uint32_t)v, (uint32_t)(v >> 32), (uint32_t)(v >> 64), (uint32_t)(v >> 96));
+}
+
+// Y holds ng groups, each normalised on its own, and Cg[g] the carry out of
+// group g (below 2^64); adds Cg[g - 1] into group g and resolves the ripple,
+// so that Y becomes the normalised sum mod b^(4 ng).  Every thread calls it.
+__device__ void settle(uint32_t* Y, int ng, const uint64_t* Cg, Scratch& sc) {
+  uint32_t cin = 0;
+  for (int r0 = 0; r0 < ng; r0 += blockDim.x) {
+    const int g = r0 + threadIdx.x;
+    unsigned __int128 v = 0;
+    bool gen = false, prop = false;
+    if (g < ng) {
+      const unsigned __int128 y = ld_group(Y, g);
+      v = y + (g ? Cg[g - 1] : 0ull);
+      gen = v < y;
+      prop = v == ~(unsigned __int128)0;
+    }
+    const uint32_t c = carry_in(gen, prop, &cin, sc);
+    if (g < ng) st_group(Y, g, v + c);
+  }
+}
+
+// Y = X - S mod b^L over words w < L (X, S word sources; Y may be either's
+// storage: each thread reads and writes only its own groups).  Y has whole
+// groups of storage; its words from L up to the group end are left as they are.
+template <class FX, class FS>
+__device__ void sub_words(uint32_t* Y, int L, FX x, FS s, Scratch& sc) {
+  const int ng = (L + kGroup - 1) / kGroup;
+  uint32_t bin = 0;
+  for (int r0 = 0; r0 < ng; r0 += blockDim.x) {
+    const int g = r0 + threadIdx.x;
+    uint32_t d[kGroup] = {0u, 0u, 0u, 0u};
+    bool gen = false, prop = false;
+    if (g < ng) {
+      int64_t br = 0;
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        const int w = kGroup * g + j;
+        const int64_t t = (w < L ? (int64_t)x(w) - (int64_t)s(w) : 0) + br;
+        d[j] = (uint32_t)t;
+        br = t >> 32;
+      }
+      gen = br != 0;
+      prop = (d[0] | d[1] | d[2] | d[3]) == 0u;
+    }
+    uint32_t b = carry_in(gen, prop, &bin, sc);
+    if (g < ng) {
+#pragma unroll
+      for (int j = 0; j < kGroup; ++j) {
+        const int w = kGroup * g + j;
+        const uint32_t v = d[j] - b;
+        b = d[j] < b ? 1u : 0u;
+        if (w < L) Y[w] = v;
+      }
+    }
+  }
+}
+
+// Highest w < L with a(w) != b(w), or -1; the same value in every thread.
+template <class FA, class FB>
+__device__ int top_diff(int L, FA a, FB b, Scratch& sc) {
+  int best = -1;
+  for (int w = threadIdx.x; w < L; w += blockDim.x)
+    if (a(w) != b(w)) best = w;
+  best = __reduce_max_sync(~0u, best);
+  if ((threadIdx.x & 31) == 0) sc.hi[threadIdx.x >> 5] = best;
+  __syncthreads();
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) best = max(best, sc.hi[w]);
+  __syncthreads();
+  return best;
+}
+
+// From Z's words Zn[0 .. LG + kZExtra), normalised (Z < b^(LG + 11)): N =
+// bal_Q(Z mod Q) by Barrett's method with the 13-word reciprocal, the
+// acceptance test |N| <= 2^nb, and the two's complement output of component k.
+// QQ is shared scratch of whole groups covering LG + 1 words, Cg one 64-bit
+// carry per group.  Every thread calls it.
+__device__ __forceinline__ void numerator_tail(const RParams& p, int64_t k, uint32_t* Zn, uint32_t* QQ, uint64_t* Cg,
+                                               Scratch& sc) {
   const int LG = p.LG;
   const int tid = threadIdx.x, nt = blockDim.x;
+  __shared__ uint32_t qc[2 * kMuWords][3];
   __shared__ uint32_t qh[kMuWords];
-  __shared__ int s_ok, s_neg, s_z;
-  __syncthreads();
-  if (tid == 0) {
-    // q^ = floor(Z1 MU / b^13) with Z1 = floor(Z / b^(LG-1)) (13 words)
-    uint32_t prod[2 * kMuWords];
-    for (int t = 0; t < 2 * kMuWords; ++t) prod[t] = 0;
-    for (int a = 0; a < kMuWords; ++a) {
-      uint64_t c = 0;
-      const uint64_t za = Zn[LG - 1 + a];
-      for (int b = 0; b < kMuWords; ++b) {
-        uint64_t t = za * p.MU[b] + prod[a + b] + c;
-        prod[a + b] = (uint32_t)t;
-        c = t >> 32;
-      }
-      prod[a + kMuWords] = (uint32_t)c;
-    }
-    for (int t = 0; t < kMuWords; ++t) qh[t] = prod[kMuWords + t];
-  }
-  __syncthreads();
-  // q^ Q, words 0 .. LG (enough: the remainder is below 3Q < b^(LG+1))
-  for (int w = tid; w <= LG; w += nt) {
-    uint64_t lo = 0;
-    uint32_t hi = 0;
-    for (int j = 0; j < kMuWords; ++j) {
-      const int t = w - j;
-      if (t >= 0 && t < LG) mac(lo, hi, qh[j], p.Q[t]);
-    }
-    Zlo[w] = lo;
-    Zhi[w] = hi;
+  // q^ = floor(Z1 MU / b^13) with Z1 = floor(Z / b^(LG-1)): 26 column sums,
+  // then one short carry chain
+  if (tid < 2 * kMuWords) {
+    uint32_t acc[3] = {0u, 0u, 0u};
+    for (int a = max(0, tid - (kMuWords - 1)); a <= min(kMuWords - 1, tid); ++a)
+      mac96(acc, Zn[LG - 1 + a], p.MU[tid - a]);
+    qc[tid][0] = acc[0];
+    qc[tid][1] = acc[1];
+    qc[tid][2] = acc[2];
   }
   __syncthreads();
   if (tid == 0) {
-    // r = Z - q^ Q  (mod b^(LG+1))
-    uint64_t carry = 0;
-    int64_t borrow = 0;
-    for (int w = 0; w <= LG; ++w) {
-      unsigned __int128 s = (unsigned __int128)Zlo[w] + ((unsigned __int128)Zhi[w] << 64) + carry;
-      const uint32_t qq = (uint32_t)s;
-      carry = (uint64_t)(s >> 32);
-      const int64_t d = (int64_t)Zn[w] - (int64_t)qq + borrow;
-      Zn[w] = (uint32_t)d;
-      borrow = d >> 32;
+    unsigned __int128 s = 0;
+    for (int t = 0; t < 2 * kMuWords; ++t) {
+      s += (unsigned __int128)qc[t][0] | ((unsigned __int128)qc[t][1] << 32) | ((unsigned __int128)qc[t][2] << 64);
+      if (t >= kMuWords) qh[t - kMuWords] = (uint32_t)s;
+      s >>= 32;
     }
-    // at most two subtractions of Q
-    for (int rep = 0; rep < 3; ++rep) {
-      bool ge = Zn[LG] != 0;
-      if (!ge) {
-        ge = true;
-        for (int w = LG - 1; w >= 0; --w)
-          if (Zn[w] != p.Q[w]) {
-            ge = Zn[w] > p.Q[w];
-            break;
-          }
-      }
-      if (!ge) break;
-      borrow = 0;
-      for (int w = 0; w <= LG; ++w) {
-        const int64_t d = (int64_t)Zn[w] - (int64_t)(w < LG ? p.Q[w] : 0u) + borrow;
-        Zn[w] = (uint32_t)d;
-        borrow = d >> 32;
-      }
-    }
-    // balanced: r > (Q-1)/2 -> N = r - Q, magnitude Q - r
-    bool neg = false;
-    for (int w = LG - 1; w >= 0; --w)
-      if (Zn[w] != p.Qhalf[w]) {
-        neg = Zn[w] > p.Qhalf[w];
-        break;
-      }
-    if (neg) {
-      borrow = 0;
-      for (int w = 0; w < LG; ++w) {
-        const int64_t d = (int64_t)p.Q[w] - (int64_t)Zn[w] + borrow;
-        Zn[w] = (uint32_t)d;
-        borrow = d >> 32;
-      }
-    }
-    Zn[LG] = 0;
-    // |N| <= 2^nb ?
-    int top = LG - 1;
-    while (top >= 0 && Zn[top] == 0) --top;
-    bool ok = true;
-    if (top >= 0) {
-      const int64_t bl = 32 * (int64_t)top + (32 - __clz(Zn[top]));
-      if (bl > p.nb + 1) {
-        ok = false;
-      } else if (bl == p.nb + 1) {  // equal to 2^nb only
-        ok = Zn[top] == (1u << (p.nb % 32));
-        for (int w = 0; ok && w < top; ++w) ok = Zn[w] == 0;
-      }
-    }
-    int z = 0;
-    while (z < LG && Zn[z] == 0) ++z;
-    s_ok = ok ? 1 : 0;
-    s_neg = neg ? 1 : 0;
-    s_z = z;
   }
   __syncthreads();
+  // q^ Q mod b^(LG+1) (the remainder is below 3Q < b^(LG+1)): each group's four
+  // column sums, normalised within the group, then settled
+  const int nq = (LG + 1 + kGroup - 1) / kGroup;
+  for (int g = tid; g < nq; g += nt) {
+    unsigned __int128 s = 0;
+    uint32_t v[kGroup];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+      const int w = kGroup * g + j;
+      uint32_t acc[3] = {0u, 0u, 0u};
+      if (w <= LG)
+        for (int i = max(0, w - LG + 1); i <= min(kMuWords - 1, w); ++i) mac96(acc, qh[i], p.Q[w - i]);
+      s += (unsigned __int128)acc[0] | ((unsigned __int128)acc[1] << 32) | ((unsigned __int128)acc[2] << 64);
+      v[j] = (uint32_t)s;
+      s >>= 32;
+    }
+    reinterpret_cast<uint4*>(QQ)[g] = make_uint4(v[0], v[1], v[2], v[3]);
+    Cg[g] = (uint64_t)s;
+  }
+  __syncthreads();
+  settle(QQ, nq, Cg, sc);
+  __syncthreads();
+  // r = Z - q^ Q  (mod b^(LG+1))
+  auto zw = [&](int w) { return Zn[w]; };
+  auto qw = [&](int w) { return w < LG ? p.Q[w] : 0u; };
+  sub_words(Zn, LG + 1, zw, [&](int w) { return QQ[w]; }, sc);
+  __syncthreads();
+  // at most two subtractions of Q
+  for (int rep = 0; rep < 3; ++rep) {
+    const int t = top_diff(LG + 1, zw, qw, sc);
+    if (t >= 0 && Zn[t] < qw(t)) break;  // r < Q
+    if (t < 0) {                         // r == Q
+      for (int w = tid; w <= LG; w += nt) Zn[w] = 0u;
+      __syncthreads();
+      break;
+    }
+    sub_words(Zn, LG + 1, zw, qw, sc);
+    __syncthreads();
+  }
+  // balanced: r > (Q-1)/2 -> N = r - Q, magnitude Q - r
+  const int th = top_diff(LG, zw, [&](int w) { return p.Qhalf[w]; }, sc);
+  const bool neg = th >= 0 && Zn[th] > p.Qhalf[th];
+  if (neg) {
+    sub_words(Zn, LG, qw, zw, sc);
+    __syncthreads();
+  }
+  // highest and lowest nonzero words
+  int hi = -1, lo = LG;
+  for (int w = tid; w < LG; w += nt)
+    if (Zn[w] != 0u) {
+      hi = w;
+      lo = min(lo, w);
+    }
+  hi = __reduce_max_sync(~0u, hi);
+  lo = __reduce_min_sync(~0u, lo);
+  if ((tid & 31) == 0) {
+    sc.hi[tid >> 5] = hi;
+    sc.lo[tid >> 5] = lo;
+  }
+  __syncthreads();
+  for (int w = 0; w < (nt >> 5); ++w) {
+    hi = max(hi, sc.hi[w]);
+    lo = min(lo, sc.lo[w]);
+  }
+  // |N| <= 2^nb ?
+  bool ok = true;
+  if (hi >= 0) {
+    const int64_t bl = 32 * (int64_t)hi + (32 - __clz(Zn[hi]));
+    if (bl > p.nb + 1)
+      ok = false;
+    else if (bl == p.nb + 1)  // equal to 2^nb only
+      ok = Zn[hi] == (1u << (p.nb % 32)) && lo == hi;
+  }
   // two's complement output: -mag = ~mag + 1 (words below the lowest nonzero stay 0)
-  const int neg = s_neg, z = s_z;
+  const int z = lo;
   uint64_t* out = p.N + (size_t)k * p.W;
   for (int t = tid; t < p.W; t += nt) {
     uint32_t wv[2];
@@ -204,19 +314,29 @@ __device__ __forceinline__ void numerator_tail(const RParams& p, int64_t k, uint
     }
     out[t] = (uint64_t)wv[0] | ((uint64_t)wv[1] << 32);
   }
-  if (tid == 0) p.ok[k] = (uint8_t)s_ok;
+  if (tid == 0) p.ok[k] = ok ? 1 : 0;
 }
 
+// Shared memory of k_recon_numerators, in 32-bit words unless stated: Zn
+// (whole groups over LG + kZExtra words), QQ (whole groups over LG + 1), the
+// shifted digits (mp * 12), then one 64-bit carry per group of Zn.
+__host__ __device__ inline int64_t zn_groups(int64_t LG) { return (LG + kZExtra + kGroup - 1) / kGroup; }
+__host__ __device__ inline int64_t qq_groups(int64_t LG) { return (LG + 1 + kGroup - 1) / kGroup; }
+inline int64_t numerator_smem(int64_t LG, int64_t mp) {
+  return 4 * kGroup * (zn_groups(LG) + qq_groups(LG)) + 4 * mp * kDigitWords + 8 * zn_groups(LG);
+}
 
-__global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
+__global__ void __launch_bounds__(256, 5) k_recon_numerators(RParams p) {
   const int64_t k = blockIdx.x;
-  const int mp = p.mp, LG = p.LG, LZ = LG + kZExtra;
+  const int mp = p.mp, LG = p.LG;
   const int tid = threadIdx.x, nt = blockDim.x;
+  const int nz = (int)zn_groups(LG);
   extern __shared__ __align__(16) unsigned char sm[];
-  uint64_t* Zlo = reinterpret_cast<uint64_t*>(sm);          // LZ + 1
-  uint32_t* Zhi = reinterpret_cast<uint32_t*>(Zlo + LZ + 1);  // LZ + 1
-  uint32_t* Zn = Zhi + LZ + 1;                              // LZ + 1
-  uint32_t* xs = Zn + LZ + 1;                               // mp * 12
+  __shared__ Scratch sc;
+  uint32_t* Zn = reinterpret_cast<uint32_t*>(sm);             // kGroup nz
+  uint32_t* QQ = Zn + kGroup * nz;                            // kGroup qq_groups(LG)
+  uint32_t* xs = QQ + kGroup * qq_groups(LG);                 // mp * 12
+  uint64_t* Cg = reinterpret_cast<uint64_t*>(xs + mp * kDigitWords);  // nz
 
   // shifted digits x'_i = x_i + (P'-1)/2  (384-bit two's complement add)
   for (int i = tid; i < mp; i += nt) {
@@ -231,9 +351,12 @@ __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
   }
   __syncthreads();
   // Z word columns: Z[w] = OFF[w] + sum_i sum_l x'_i[l] G_i[w - l].  A thread
-  // owns 4 consecutive columns: per digit it loads the 16 words of G_i they
-  // need (4 aligned 16-byte loads) and the digit's 12 words, then 48 96-bit MACs.
-  for (int w0 = 4 * tid; w0 < LZ; w0 += 4 * nt) {
+  // owns a group of 4 consecutive columns: per digit it loads the 16 words of
+  // G_i they need (4 aligned 16-byte loads) and the digit's 12 words, then 48
+  // 96-bit MACs; the four sums are normalised into words in registers and the
+  // group's carry out (below 2^64: every column is below 2^95) is kept apart.
+  for (int g = tid; g < nz; g += nt) {
+    const int w0 = kGroup * g;
     uint32_t acc[4][3];
 #pragma unroll
     for (int o = 0; o < 4; ++o) {
@@ -244,11 +367,11 @@ __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
     for (int i = 0; i < mp; ++i) {
       const uint4* gr = reinterpret_cast<const uint4*>(p.G + (size_t)i * p.GS + kGPad + w0 - 12);
       const uint4* xr = reinterpret_cast<const uint4*>(xs + i * kDigitWords);
-      uint32_t g[16], x[kDigitWords];
+      uint32_t g16[16], x[kDigitWords];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const uint4 v = __ldg(gr + h);
-        g[4 * h] = v.x, g[4 * h + 1] = v.y, g[4 * h + 2] = v.z, g[4 * h + 3] = v.w;
+        g16[4 * h] = v.x, g16[4 * h + 1] = v.y, g16[4 * h + 2] = v.z, g16[4 * h + 3] = v.w;
       }
 #pragma unroll
       for (int h = 0; h < kDigitWords / 4; ++h) {
@@ -258,26 +381,23 @@ __global__ void __launch_bounds__(256) k_recon_numerators(RParams p) {
 #pragma unroll
       for (int o = 0; o < 4; ++o)
 #pragma unroll
-        for (int l = 0; l < kDigitWords; ++l) mac96(acc[o], x[l], g[o + 12 - l]);
+        for (int l = 0; l < kDigitWords; ++l) mac96(acc[o], x[l], g16[o + 12 - l]);
     }
+    unsigned __int128 s = 0;
+    uint32_t v[4];
 #pragma unroll
-    for (int o = 0; o < 4; ++o)
-      if (w0 + o < LZ) {
-        Zlo[w0 + o] = (uint64_t)acc[o][0] | ((uint64_t)acc[o][1] << 32);
-        Zhi[w0 + o] = acc[o][2];
-      }
+    for (int o = 0; o < 4; ++o) {
+      s += (unsigned __int128)acc[o][0] | ((unsigned __int128)acc[o][1] << 32) | ((unsigned __int128)acc[o][2] << 64);
+      v[o] = (uint32_t)s;
+      s >>= 32;
+    }
+    reinterpret_cast<uint4*>(Zn)[g] = make_uint4(v[0], v[1], v[2], v[3]);
+    Cg[g] = (uint64_t)s;
   }
   __syncthreads();
-  if (tid == 0) {
-    // normalise the columns into 32-bit words
-    uint64_t carry = 0;
-    for (int w = 0; w < LZ; ++w) {
-      unsigned __int128 s = (unsigned __int128)Zlo[w] + ((unsigned __int128)Zhi[w] << 64) + carry;
-      Zn[w] = (uint32_t)s;
-      carry = (uint64_t)(s >> 32);
-    }
-  }
-  numerator_tail(p, k, Zn, Zlo, Zhi);
+  settle(Zn, nz, Cg, sc);  // Z < b^(LG + 11): nothing carries out of the top group
+  __syncthreads();
+  numerator_tail(p, k, Zn, QQ, Cg, sc);
 }
 
 // ------------------------------------------------------------------ tensor cores
@@ -1033,7 +1153,7 @@ es_status recon_device_prepare(int64_t n, int64_t c, int32_t m, int32_t mp, cons
   if ((int64_t)((big::bitlen(mu) + 31) / 32) > kMuWords) return ES_ERR_INTERNAL;
   to_words(mu, kMuWords, R.hM.data());
   to_words(R.ps.half, kDigitWords, R.hM.data() + kMuWords);
-  R.dyn = (int)((3 * (LG + kZExtra + 1)) * 4 + (LG + kZExtra + 1) * 4 + (size_t)mp * kDigitWords * 4);
+  R.dyn = (int)numerator_smem(LG, mp);
   *out = rp.release();
   return ES_OK;
 }
