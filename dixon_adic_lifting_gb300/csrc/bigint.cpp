@@ -525,6 +525,7 @@ struct CofactorPipe {
   std::atomic<uint32_t> head{0}, tail{0};
   std::atomic<int> claim{kFree};
   std::atomic<bool> closed{false};
+  uint32_t tail_seen = 0;  // the run's last look at tail
   Nat T0, T1{1};  // magnitudes of the cofactors of u in r0 and r1
   Nat m0, m1;
 
@@ -558,7 +559,9 @@ struct CofactorPipe {
       return;
     }
     const uint32_t h = head.load(std::memory_order_relaxed);
-    if (h - tail.load(std::memory_order_acquire) >= kRing) {
+    // the consumer's position is read only when the last one seen leaves no room
+    if (h - tail_seen >= kRing) tail_seen = tail.load(std::memory_order_acquire);
+    if (h - tail_seen >= kRing) {
       own();  // a full ring nobody serves: the run takes the work over
       if (claim.load(std::memory_order_acquire) == kOwned) {
         apply(Item{a, b, c, d});
@@ -595,16 +598,338 @@ void cofactor_pipe_serve(CofactorPipe* p) {
   if (p) p->serve();
 }
 
+// ------------------------------------------------------------ low-limb pipe
+// The remainder updates of the Lehmer loop split by limbs between the run and
+// up to kLowSlots more threads.  At a round's start the run cuts both
+// remainders at limb h and the part below into one range [lo_j, hi_j) per
+// server: r = t 2^(64h) + sum_j l_j 2^(64 lo_j), 0 <= l_j < 2^(64(hi_j - lo_j)).
+// The run keeps the high parts t (a copy) and updates them with each batch's
+// matrix M as if nothing carried in from below; server j follows the same
+// matrices over l_j in place, up to a ring's length behind, and keeps what
+// carries out of its range as a small signed correction e_j (two's complement,
+// at most kLowCorr limbs): a batch maps (l_j, e_j) to
+// (M l_j mod 2^(64(hi_j - lo_j)), M e_j + floor(M l_j / 2^(64(hi_j - lo_j)))),
+// so that throughout
+//     r = t 2^(64h) + sum_j (l_j 2^(64 lo_j) + e_j 2^(64 hi_j)).
+// Every |e_j| < 2^ebits, which grows by at most the bits of the batch's largest
+// row sum plus one per batch, and the part below t is then below
+// 2^(64h + ebits + 1) in magnitude; so as long as ebits + 3 <= sh' (the shift
+// at which the run reads the leading 126 bits of t) the true leading parts
+// differ from the simulated ones by less than 1/2, and a batch certified over
+// the box [a0 - 1, a0 + 2] x [b0 - 1, b0 + 2] (lehmer_sim_wide) holds for the
+// true remainders.  When that margin runs out (or no step is certain) the run
+// waits for the servers, folds the corrections in from the bottom up, and
+// starts the next round.  The run splits only while a server serves the pipe,
+// and takes in servers that arrive late at the next round's start, so a pool
+// narrower than planned changes nothing but the speed.
+constexpr size_t kLowCorr = 64;        // limbs of a correction e_j
+constexpr int kLowSlots = 4;            // servers one pipe takes
+constexpr size_t kSplitMinLimbs = 160;  // shorter remainders stay on the run's thread
+
+// As lehmer_sim, for leading parts known only to lie in (a - 1, a + 2) and
+// (b - 1, b + 2).  The quotient steps are run plainly on (a, b), keeping every
+// step's remainders (alpha, beta) and cofactors; then the longest prefix is
+// taken whose matrix has alpha > beta > 0 at all four corners of the box
+// [a - 1, a + 2] x [b - 1, b + 2]: that makes its quotients the first ones of
+// Euclid's algorithm at every point of the box (the continued fraction
+// argument of the half-gcd below; alpha and beta are linear, so the corners
+// decide), hence on the true remainders.  The stop condition is checked the
+// same way.  Every divisor stays at least 2^66 and every cofactor below 2^61,
+// so no product overflows and the row sums stay below 2^62.
+static LMat lehmer_sim_wide(__int128 a, __int128 b, __int128 stop) {
+  const __int128 kMin = (__int128)1 << 66;
+  const __int128 kCap = (__int128)1 << 61;
+  constexpr int kMax = 96;
+  struct Step {
+    __int128 a, b;
+    int64_t A, B, C, D;
+  };
+  Step st[kMax];
+  int n = 0;
+  int64_t A = 1, B = 0, C = 0, D = 1;
+  while (n < kMax && b >= kMin && a >= b) {
+    // q = floor(a / b): the small quotients (two in three) by subtraction,
+    // the others from a double-precision estimate (relative error below
+    // 2^-50, so at most one off for q < 2^61) and one correction
+    int64_t q = 1;
+    __int128 r = a - b;
+    if (r >= b) {
+      r -= b;
+      q = 2;
+      if (r >= b) {
+        r -= b;
+        q = 3;
+        if (r >= b) {
+          const double ad = (double)(uint64_t)(a >> 64) * 0x1p64 + (double)(uint64_t)a;
+          const double bd = (double)(uint64_t)(b >> 64) * 0x1p64 + (double)(uint64_t)b;
+          const double qd = ad / bd;
+          if (!(qd < 0x1p60)) break;
+          q = (int64_t)qd;
+          r = a - (__int128)q * b;
+          while (r < 0) {
+            --q;
+            r += b;
+          }
+          while (r >= b) {
+            ++q;
+            r -= b;
+          }
+        }
+      }
+    }
+    if (q >= kCap) break;
+    const __int128 nC = (__int128)A - (__int128)q * C, nD = (__int128)B - (__int128)q * D;
+    if (nC >= kCap || -nC >= kCap || nD >= kCap || -nD >= kCap) break;
+    A = C;
+    B = D;
+    C = (int64_t)nC;
+    D = (int64_t)nD;
+    a = b;
+    b = r;
+    st[n++] = Step{a, b, A, B, C, D};
+  }
+  for (int k = n - 1; k >= 0; --k) {
+    const Step& s = st[k];
+    bool ok = true;
+    for (int j = 0; j < 4 && ok; ++j) {
+      const int da = (j & 1) ? 2 : -1, db = (j & 2) ? 2 : -1;
+      const __int128 al = s.a + (__int128)s.A * da + (__int128)s.B * db;
+      const __int128 be = s.b + (__int128)s.C * da + (__int128)s.D * db;
+      ok = be > 0 && al > be && be >= stop;
+    }
+    if (ok) {
+      LMat M;
+      M.A = s.A, M.B = s.B, M.C = s.C, M.D = s.D, M.k = (size_t)k + 1;
+      return M;
+    }
+  }
+  return LMat{};
+}
+
+// x += c on a w-limb two's complement number (the result must fit).
+static void add_carry_signed(limb* x, size_t w, __int128 c) {
+  for (size_t i = 0; i < w && c != 0; ++i) {
+    const __int128 s = c + (__int128)x[i];
+    x[i] = (limb)s;
+    c = s >> 64;
+  }
+}
+// (x, y) <- (A x + B y + c0, C x + D y + c1) on w-limb two's complement numbers
+// (in place; the results must fit): the unsigned limbs by comb2_range, the
+// signed top limb apart, then the carries.
+static void lin2x2_signed(limb* x, limb* y, size_t w, int64_t A, int64_t B, int64_t C, int64_t D, __int128 c0,
+                          __int128 c1) {
+  if (w == 0) return;
+  __int128 h0 = 0, h1 = 0;
+  if (w > 1)
+    comb2_range(sign_code(A, B, C, D), x, y, x, w - 1, y, w - 1, 0, w - 1, uabs(A), uabs(B), uabs(C), uabs(D), &h0,
+                &h1);
+  const __int128 xt = (int64_t)x[w - 1], yt = (int64_t)y[w - 1];
+  x[w - 1] = (limb)(h0 + (__int128)A * xt + (__int128)B * yt);
+  y[w - 1] = (limb)(h1 + (__int128)C * xt + (__int128)D * yt);
+  add_carry_signed(x, w, c0);
+  add_carry_signed(y, w, c1);
+}
+
+struct LowPipe {
+  struct Item {
+    int64_t A, B, C, D;
+    size_t w;  // limbs of the corrections that can be nonzero after this batch
+  };
+  static constexpr uint32_t kRing = 256;
+  struct alignas(64) Slot {
+    std::atomic<uint32_t> tail{0};
+    std::atomic<bool> joined{false};
+    // the round: set by the run while the slot is idle, published by the
+    // release of the round's first item
+    limb* x = nullptr;
+    limb* y = nullptr;
+    size_t lo = 0, hi = 0;
+    size_t ew = 0;  // limbs of e in use (the ones above are its sign)
+    limb e0[kLowCorr], e1[kLowCorr];
+
+    void apply(const Item& it) {
+      __int128 c0 = 0, c1 = 0;
+      if (hi > lo)
+        comb2_range(sign_code(it.A, it.B, it.C, it.D), x, y, x, hi, y, hi, lo, hi, uabs(it.A), uabs(it.B),
+                    uabs(it.C), uabs(it.D), &c0, &c1);
+      for (; ew < it.w; ++ew) {
+        e0[ew] = ew && (e0[ew - 1] >> 63) ? ~(limb)0 : 0;
+        e1[ew] = ew && (e1[ew - 1] >> 63) ? ~(limb)0 : 0;
+      }
+      lin2x2_signed(e0, e1, ew, it.A, it.B, it.C, it.D, c0, c1);
+    }
+  };
+  Item ring[kRing];
+  std::atomic<uint32_t> head{0};
+  std::atomic<int> claimed{0};
+  std::atomic<bool> closed{false};
+  int joined = 0;           // the run's count of slots taken into rounds
+  uint32_t tail_seen = 0;   // the run's last look at the slowest server
+  Slot slot[kLowSlots];
+
+  bool served() const { return claimed.load(std::memory_order_acquire) > 0; }
+  // the run, between rounds: takes in the servers that have arrived
+  int begin_round() {
+    const int n = std::min(claimed.load(std::memory_order_acquire), kLowSlots);
+    const uint32_t hd = head.load(std::memory_order_relaxed);
+    for (; joined < n; ++joined) {
+      slot[joined].tail.store(hd, std::memory_order_relaxed);
+      slot[joined].joined.store(true, std::memory_order_release);
+    }
+    tail_seen = hd;  // every joined server has drained
+    return joined;
+  }
+  uint32_t min_tail() const {
+    const uint32_t hd = head.load(std::memory_order_relaxed);
+    uint32_t lag = 0;
+    for (int j = 0; j < joined; ++j) lag = std::max(lag, hd - slot[j].tail.load(std::memory_order_acquire));
+    return hd - lag;
+  }
+  void push(const LMat& L, size_t w) {
+    const uint32_t hd = head.load(std::memory_order_relaxed);
+    int spins = 0;
+    // the servers' positions are read only when the last ones seen leave no room
+    while (hd - tail_seen >= kRing) {
+      tail_seen = min_tail();
+      if (hd - tail_seen >= kRing) spin_wait(spins);
+    }
+    ring[hd % kRing] = Item{L.A, L.B, L.C, L.D, w};
+    head.store(hd + 1, std::memory_order_release);
+  }
+  void drain() {
+    const uint32_t hd = head.load(std::memory_order_relaxed);
+    int spins = 0;
+    while (min_tail() != hd) spin_wait(spins);
+  }
+  void serve() {
+    const int j = claimed.fetch_add(1, std::memory_order_acq_rel);
+    if (j >= kLowSlots) return;
+    Slot& s = slot[j];
+    int spins = 0;
+    while (!s.joined.load(std::memory_order_acquire)) {
+      if (closed.load(std::memory_order_acquire)) return;
+      spin_wait(spins);
+    }
+    uint32_t t = s.tail.load(std::memory_order_relaxed);
+    for (;;) {
+      spins = 0;
+      uint32_t hd;
+      while ((hd = head.load(std::memory_order_acquire)) == t) {
+        if (closed.load(std::memory_order_acquire) && head.load(std::memory_order_acquire) == t) return;
+        spin_wait(spins);
+      }
+      for (; t != hd; ++t) {
+        s.apply(ring[t % kRing]);
+        s.tail.store(t + 1, std::memory_order_release);
+      }
+    }
+  }
+};
+
+LowPipe* low_pipe_new() { return new (std::nothrow) LowPipe; }
+void low_pipe_free(LowPipe* p) { delete p; }
+void low_pipe_serve(LowPipe* p) {
+  if (p) p->serve();
+}
+
+namespace {
+size_t bitlen_n(const limb* x, size_t n) {
+  while (n && !x[n - 1]) --n;
+  return n ? 64 * (n - 1) + (64 - (size_t)__builtin_clzll(x[n - 1])) : 0;
+}
+size_t bits_u64(uint64_t v) { return v ? 64 - (size_t)__builtin_clzll(v) : 0; }
+
+// One round of split batches (see LowPipe); false when none was taken.
+bool split_round(Nat& r0, Nat& r1, CofactorPipe* P, LowPipe* S, size_t* steps, long nbits) {
+  const int ns = S->begin_round();
+  const size_t len = r0.size();
+  // the run also simulates each batch: it keeps the top eighth
+  const size_t h = len * 7 / 8;
+  const size_t lt = len - h + 1;
+  if (ns < 1 || r1.size() < h + 8 || lt < 16 || h < (size_t)ns * (kLowCorr + 2)) return false;
+  Nat t0(lt, 0), t1(lt, 0);
+  std::copy(r0.begin() + (ptrdiff_t)h, r0.end(), t0.begin());
+  std::copy(r1.begin() + (ptrdiff_t)h, r1.end(), t1.begin());
+  for (int j = 0; j < ns; ++j) {
+    LowPipe::Slot& sl = S->slot[j];
+    sl.x = r0.data();
+    sl.y = r1.data();
+    sl.lo = h * (size_t)j / (size_t)ns;
+    sl.hi = h * (size_t)(j + 1) / (size_t)ns;
+    sl.ew = 0;
+  }
+  size_t ebits = 0, taken = 0;
+  for (;;) {
+    const size_t tb = bitlen_n(t0.data(), lt);
+    if (tb < 126 + 64) break;
+    const size_t shp = tb - 126;
+    if (ebits + 3 > shp || ebits + 70 > 64 * kLowCorr) break;
+    const size_t sh = shp + 64 * h;
+    __int128 stop = (__int128)1 << 63;
+    if ((size_t)nbits >= sh) {
+      const size_t e = (size_t)nbits - sh;
+      stop = e >= 126 ? ((__int128)1 << 126) : stop + ((__int128)1 << e);
+    }
+    const LMat L = lehmer_sim_wide((__int128)bits128_at(t0, shp), (__int128)bits128_at(t1, shp), stop);
+    if (L.B == 0) break;
+    const limb a = uabs(L.A), b = uabs(L.B), c = uabs(L.C), d = uabs(L.D);
+    __int128 h0, h1;
+    comb2_range(sign_code(L.A, L.B, L.C, L.D), t0.data(), t1.data(), t0.data(), lt, t1.data(), lt, 0, lt, a, b, c,
+                d, &h0, &h1);
+    ebits = std::max(ebits + bits_u64(std::max(a + b, c + d)), (size_t)64) + 1;
+    S->push(L, ebits / 64 + 1);
+    P->push(a, b, c, d);
+    *steps += L.k;
+    ++taken;
+  }
+  S->drain();
+  // r = t 2^(64h) + sum_j (l_j 2^(64 lo_j) + e_j 2^(64 hi_j)), folded from the
+  // bottom up with one signed carry; the total is below 2^(64(h + lt)) and at
+  // least 0, so the top part's two's complement sum mod 2^(64 lt) is exact
+  r0.resize(h + lt, 0);
+  r1.resize(h + lt, 0);
+  for (int q = 0; q < 2; ++q) {
+    limb* r = q ? r1.data() : r0.data();
+    const limb* t = q ? t1.data() : t0.data();
+    __int128 carry = 0;
+    const limb* e = nullptr;  // the correction entering the current range at its bottom
+    size_t ew = 0;
+    for (int j = 0; j <= ns; ++j) {
+      const size_t lo = j < ns ? S->slot[j].lo : h, hi = j < ns ? S->slot[j].hi : h + lt;
+      for (size_t i = lo; i < hi; ++i) {
+        const size_t k = i - lo;
+        __int128 s = carry + (__int128)(j < ns ? r[i] : t[i - h]);
+        if (k + 1 < ew)
+          s += (__int128)e[k];
+        else if (k + 1 == ew)
+          s += (__int128)(int64_t)e[k];
+        r[i] = (limb)s;
+        carry = s >> 64;
+      }
+      if (j < ns) {
+        e = q ? S->slot[j].e1 : S->slot[j].e0;
+        ew = S->slot[j].ew;
+      }
+    }
+  }
+  trim(r0);
+  trim(r1);
+  return taken > 0;
+}
+}  // namespace
+
 namespace {
 constexpr size_t kPipeMinLimbs = 48;  // shorter inputs keep their cofactors on the run's thread
 
 // euclid() for rational_reconstruct (nbits >= 0) with the cofactors kept by
 // the pipe (its T0, T1 are the starting cofactors; on return they are final
 // and the run owns them or has seen every batch applied).
-void euclid_piped(Nat& r0, Nat& r1, CofactorPipe* P, size_t* steps, long nbits) {
+void euclid_piped(Nat& r0, Nat& r1, CofactorPipe* P, LowPipe* S, size_t* steps, long nbits) {
   auto done = [&](const Nat& x) { return le_pow2(x, (size_t)nbits); };
   Nat n0, n1;
   while (!done(r1)) {
+    if (S && r1.size() >= kSplitMinLimbs && S->served() && split_round(r0, r1, P, S, steps, nbits)) continue;
     if (r1.size() >= 3) {
       const size_t bl0 = bitlen(r0);
       const size_t sh = bl0 > 126 ? bl0 - 126 : 0;
@@ -820,10 +1145,12 @@ bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bo
   // a pipe is closed on every way out, so that a serve() waiting on it returns
   struct Closer {
     CofactorPipe* p;
+    LowPipe* l;
     ~Closer() {
       if (p) p->closed.store(true, std::memory_order_release);
+      if (l) l->closed.store(true, std::memory_order_release);
     }
-  } closer{opts.pipe};
+  } closer{opts.pipe, opts.low};
   Nat r0 = M, r1 = u, T0, T1 = from_u64(1);
   size_t steps = 0;
   // Long inputs: most of the way by half-gcd stages, kept above 2^nbits; the
@@ -848,7 +1175,7 @@ bool rational_reconstruct(const Nat& M, const Nat& u, size_t nbits, Nat* num, bo
     // the first batch is handed over
     P->T0 = T0;
     P->T1 = T1;
-    euclid_piped(r0, r1, P, &steps, (long)nbits);
+    euclid_piped(r0, r1, P, opts.low, &steps, (long)nbits);
     T0 = P->T0;
     T1 = P->T1;
   } else {

@@ -42,8 +42,19 @@ struct CofactorPipe;
 CofactorPipe* cofactor_pipe_new();  // null when out of memory
 void cofactor_pipe_free(CofactorPipe* p);
 void cofactor_pipe_serve(CofactorPipe* p);
+// A low-limb pipe lets a further thread take the low limbs of the remainders
+// of one run that has a cofactor pipe (ReconOpts::low): the run updates the
+// high limbs from each batch's matrix and that thread follows over the low
+// ones, a bounded number of batches behind.  The run splits the work only
+// while a thread serves the pipe (low_pipe_serve, before, during or after the
+// run; it returns once the run is over).  One pipe per run, used once.
+struct LowPipe;
+LowPipe* low_pipe_new();  // null when out of memory
+void low_pipe_free(LowPipe* p);
+void low_pipe_serve(LowPipe* p);
 // How rational_reconstruct runs.  pipe: its Lehmer loop hands the cofactor
-// updates to whoever serves the pipe.  hgcd_min_bits: from this length of M on,
+// updates to whoever serves the pipe; low (with pipe only): the low limbs of
+// the remainders likewise.  hgcd_min_bits: from this length of M on,
 // half-gcd stages (subquadratic) do most of the reduction.  They are off by
 // default: alone they beat the Lehmer loop only from about 10^5 bits (167 K
 // bits: 7.8 against 9.6 ms on the Grace host), and their many short-lived
@@ -51,6 +62,7 @@ void cofactor_pipe_serve(CofactorPipe* p);
 // (sixteen at 166 K bits took 52-75 ms each).
 struct ReconOpts {
   CofactorPipe* pipe = nullptr;
+  LowPipe* low = nullptr;
   size_t hgcd_min_bits = SIZE_MAX;
 };
 // Extended Euclid on (r0 = M, r1 = u) stopped at the first remainder <= 2^nbits

@@ -1301,10 +1301,10 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     ES_CHECK(cuda_status(cudaStreamSynchronize(st), "sample digits sync"));
     dens->assign(ks.size(), Nat{});
     std::atomic<int> fail(0);
-    denominators_parallel((int64_t)ks.size(), hw_threads, [&](int64_t t, big::CofactorPipe* pipe) {
+    denominators_parallel((int64_t)ks.size(), hw_threads, [&](int64_t t, const big::ReconOpts& ro) {
       const Nat u = shifted_to_residue(
           assemble_shifted_dc(ps, R.ap, hd.data() + (size_t)t * m * kDigitLimbs, kDigitLimbs), Mhalf, Mhalf1);
-      if (!component_denominator(M, u, num_bits, den_bits, &(*dens)[(size_t)t], pipe)) fail = 1;
+      if (!component_denominator(M, u, num_bits, den_bits, &(*dens)[(size_t)t], ro)) fail = 1;
     });
     return fail ? ES_ERR_INTERNAL : ES_OK;
   };
@@ -1315,9 +1315,9 @@ es_status reconstruct_device(ReconPlan* plan, const uint64_t* D_dev, int threads
     // the samples' shifted sums came in while the lift ran
     sden.assign(sk.size(), Nat{});
     std::atomic<int> fail(0);
-    denominators_parallel((int64_t)sk.size(), hw_threads, [&](int64_t t, big::CofactorPipe* pipe) {
+    denominators_parallel((int64_t)sk.size(), hw_threads, [&](int64_t t, const big::ReconOpts& ro) {
       const Nat u = shifted_to_residue((*pre)[(size_t)t], Mhalf, Mhalf1);
-      if (!component_denominator(M, u, num_bits, den_bits, &sden[(size_t)t], pipe)) fail = 1;
+      if (!component_denominator(M, u, num_bits, den_bits, &sden[(size_t)t], ro)) fail = 1;
     });
     if (fail) return ES_ERR_INTERNAL;
   } else {

@@ -181,29 +181,36 @@ void lcm_in(Nat& d, const Nat& v) {
 }
 
 bool component_denominator(const Nat& M, const Nat& u, int64_t num_bits, int64_t den_bits, Nat* den,
-                           big::CofactorPipe* pipe) {
+                           const big::ReconOpts& o) {
   Nat num;
   bool neg;
-  big::ReconOpts o;
-  o.pipe = pipe;
   return big::rational_reconstruct(M, u, (size_t)num_bits, &num, &neg, den, o) &&
          big::le_pow2(*den, (size_t)den_bits);
 }
 
-void denominators_parallel(int64_t count, int width, const std::function<void(int64_t, big::CofactorPipe*)>& run) {
-  std::vector<big::CofactorPipe*> pipes;
+void denominators_parallel(int64_t count, int width, const std::function<void(int64_t, const big::ReconOpts&)>& run) {
+  std::vector<big::ReconOpts> opts((size_t)std::max<int64_t>(count, 0));
+  int64_t low = 0;  // low-limb servers per run
   if (count > 0 && 2 * count <= (int64_t)width) {
-    pipes.assign((size_t)count, nullptr);
-    for (auto& p : pipes) p = big::cofactor_pipe_new();
+    low = std::min<int64_t>(kLowServers, ((int64_t)width - 2 * count) / count);
+    for (auto& o : opts) {
+      o.pipe = big::cofactor_pipe_new();
+      if (low > 0) o.low = big::low_pipe_new();
+    }
   }
-  const int64_t tasks = pipes.empty() ? count : 2 * count;
+  const int64_t tasks = opts.empty() || !opts[0].pipe ? count : (2 + low) * count;
   parallel_for(tasks, width, [&](int64_t t) {
     if (t < count)
-      run(t, pipes.empty() ? nullptr : pipes[(size_t)t]);
+      run(t, opts[(size_t)t]);
+    else if (t < 2 * count)
+      big::cofactor_pipe_serve(opts[(size_t)(t - count)].pipe);
     else
-      big::cofactor_pipe_serve(pipes[(size_t)(t - count)]);
+      big::low_pipe_serve(opts[(size_t)((t - 2 * count) % count)].low);
   });
-  for (auto* p : pipes) big::cofactor_pipe_free(p);
+  for (auto& o : opts) {
+    big::cofactor_pipe_free(o.pipe);
+    big::low_pipe_free(o.low);
+  }
 }
 
 void to_limbs(const Nat& mag, bool neg, int64_t W, uint64_t* out) {
@@ -265,8 +272,8 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
   const int64_t ns = (int64_t)sk.size();
   std::vector<Nat> sden((size_t)ns);
   std::atomic<int> fail(0);
-  denominators_parallel(ns, width, [&](int64_t t, big::CofactorPipe* pipe) {
-    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t], pipe)) fail = 1;
+  denominators_parallel(ns, width, [&](int64_t t, const big::ReconOpts& ro) {
+    if (!component_denominator(M, residue(sk[(size_t)t]), num_bits, den_bits, &sden[(size_t)t], ro)) fail = 1;
   });
   if (fail) return ES_ERR_INTERNAL;
   Nat d = big::from_u64(1);
@@ -301,8 +308,8 @@ es_status reconstruct(const uint64_t* digits, int64_t n, int64_t c, int32_t m, c
     // lcm must grow d (a later one may already be covered by an earlier one).
     const Nat before = d;
     std::vector<Nat> fden(failed.size());
-    denominators_parallel((int64_t)failed.size(), width, [&](int64_t t, big::CofactorPipe* pipe) {
-      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t], pipe))
+    denominators_parallel((int64_t)failed.size(), width, [&](int64_t t, const big::ReconOpts& ro) {
+      if (!component_denominator(M, residue(failed[(size_t)t]), num_bits, den_bits, &fden[(size_t)t], ro))
         fail = 1;
     });
     if (fail) return ES_ERR_INTERNAL;
@@ -375,7 +382,10 @@ extern "C" int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples) 
 
 // rational_reconstruct in one of the ways the library can run it: way & 1: a
 // cofactor pipe served by a second thread that starts before the run (way & 4:
-// after it, so the run keeps the work), way & 2: half-gcd stages from any length.
+// after it, so the run keeps the work), way & 8 (with way & 1): a low-limb
+// pipe as well, served by two more threads started at the same point, way & 2:
+// half-gcd stages from any length.
+static const int kWays[] = {0, 1, 2, 3, 5, 9, 11, 13};
 static bool reconstruct_way(const es::big::Nat& M, const es::big::Nat& u, size_t nbits, int way, es::big::Nat* num,
                             bool* neg, es::big::Nat* den) {
   namespace big = es::big;
@@ -383,19 +393,32 @@ static bool reconstruct_way(const es::big::Nat& M, const es::big::Nat& u, size_t
   if (way & 2) o.hgcd_min_bits = 0;
   if (!(way & 1)) return big::rational_reconstruct(M, u, nbits, num, neg, den, o);
   big::CofactorPipe* pipe = big::cofactor_pipe_new();
-  if (!pipe) return false;
+  big::LowPipe* low = (way & 8) ? big::low_pipe_new() : nullptr;
+  if (!pipe || ((way & 8) && !low)) {
+    big::cofactor_pipe_free(pipe);
+    big::low_pipe_free(low);
+    return false;
+  }
   o.pipe = pipe;
+  o.low = low;
+  auto serve = [&] {
+    std::vector<std::thread> th;
+    th.emplace_back([&] { big::cofactor_pipe_serve(pipe); });
+    if (low)
+      for (int i = 0; i < 2; ++i) th.emplace_back([&] { big::low_pipe_serve(low); });
+    return th;
+  };
   bool ok = false;
   if (way & 4) {
     ok = big::rational_reconstruct(M, u, nbits, num, neg, den, o);
-    std::thread th([&] { big::cofactor_pipe_serve(pipe); });
-    th.join();
+    for (auto& t : serve()) t.join();
   } else {
-    std::thread th([&] { big::cofactor_pipe_serve(pipe); });
+    std::vector<std::thread> th = serve();
     ok = big::rational_reconstruct(M, u, nbits, num, neg, den, o);
-    th.join();
+    for (auto& t : th) t.join();
   }
   big::cofactor_pipe_free(pipe);
+  big::low_pipe_free(low);
   return ok;
 }
 
@@ -500,7 +523,7 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
         big::divmod(Nat(den), g, &den, nullptr);
       }
       // the same result on every way the reconstruction can run
-      for (int way = 0; way < 6; ++way) {
+      for (int way : kWays) {
         Nat rn, rd;
         bool rneg = false;
         if (!reconstruct_way(M, u, nbits, way, &rn, &rneg, &rd) || rn != num || rd != den || rneg != neg) ++bad;
@@ -518,7 +541,8 @@ extern "C" int64_t es_selftest_bigint(uint64_t seed, int64_t rounds) {
       Nat n0, d0;
       bool g0 = false;
       const bool ok0 = big::rational_reconstruct(M, u, nbits, &n0, &g0, &d0);
-      for (int way = 1; way < 6; ++way) {
+      for (int way : kWays) {
+        if (way == 0) continue;
         Nat n1, d1;
         bool g1 = false;
         const bool ok1 = reconstruct_way(M, u, nbits, way, &n1, &g1, &d1);

@@ -54,18 +54,22 @@ big::Nat shifted_to_residue(big::Nat X, const big::Nat& Mhalf, const big::Nat& M
 void lcm_in(big::Nat& d, const big::Nat& v);
 
 // Rational reconstruction of one component's denominator (Wang; bounds
-// Nb = 2^num_bits, Db = 2^den_bits); false when it does not exist.  With a
-// pipe, a pool task serving it (big::cofactor_pipe_serve) can keep the
-// cofactors.
+// Nb = 2^num_bits, Db = 2^den_bits); false when it does not exist.  With the
+// pipes of `o`, pool tasks serving them (big::cofactor_pipe_serve,
+// big::low_pipe_serve) can keep the cofactors and the remainders' low limbs.
 bool component_denominator(const big::Nat& M, const big::Nat& u, int64_t num_bits, int64_t den_bits,
-                           big::Nat* den, big::CofactorPipe* pipe = nullptr);
-// Denominators of `count` components at once on the host pool: run(t, pipe)
-// reconstructs component t (passing the pipe on).  When the pool is at least
-// twice as wide as count, each run gets a pipe and a second pool task serves
-// it (the tasks are taken in index order: the runs come first, so a narrower
-// pool than planned only makes the servers return at once).
+                           big::Nat* den, const big::ReconOpts& o = big::ReconOpts());
+// Low-limb servers per reconstruction when the pool is wide enough.
+constexpr int64_t kLowServers = 2;
+// Denominators of `count` components at once on the host pool: run(t, opts)
+// reconstructs component t (passing the options on).  When the pool is at
+// least twice as wide as count, each run gets a cofactor pipe and a second
+// pool task serves it; when it is wider still, a low-limb pipe as well with up
+// to kLowServers more tasks (the tasks are taken in index order: the runs come
+// first, then the cofactor servers, so a narrower pool than planned only makes
+// the servers return at once).
 void denominators_parallel(int64_t count, int width,
-                           const std::function<void(int64_t, big::CofactorPipe*)>& run);
+                           const std::function<void(int64_t, const big::ReconOpts&)>& run);
 
 // Two's complement little-endian limbs of +-mag into out[0..W).
 void to_limbs(const big::Nat& mag, bool neg, int64_t W, uint64_t* out);
