@@ -520,12 +520,14 @@ struct CofactorPipe {
     limb a, b, c, d;
   };
   static constexpr uint32_t kRing = 1024;
+  static constexpr uint32_t kPublish = 4;
   enum : int { kFree = 0, kServed = 1, kOwned = 2 };
   Item ring[kRing];
   std::atomic<uint32_t> head{0}, tail{0};
   std::atomic<int> claim{kFree};
   std::atomic<bool> closed{false};
   uint32_t tail_seen = 0;  // the run's last look at tail
+  uint32_t next = 0;       // the run's next ring slot (head trails it by under kPublish)
   Nat T0, T1{1};  // magnitudes of the cofactors of u in r0 and r1
   Nat m0, m1;
 
@@ -539,18 +541,21 @@ struct CofactorPipe {
   void own() {
     int expect = kFree;
     if (claim.compare_exchange_strong(expect, kOwned, std::memory_order_acq_rel)) {
-      const uint32_t h = head.load(std::memory_order_relaxed);
-      for (uint32_t t = tail.load(std::memory_order_relaxed); t != h; ++t) apply(ring[t % kRing]);
-      tail.store(h, std::memory_order_relaxed);
+      for (uint32_t t = tail.load(std::memory_order_relaxed); t != next; ++t) apply(ring[t % kRing]);
+      tail.store(next, std::memory_order_relaxed);
+      head.store(next, std::memory_order_relaxed);
     }
+  }
+  void publish() {
+    if (head.load(std::memory_order_relaxed) != next) head.store(next, std::memory_order_release);
   }
   // the run's side: every batch handed over so far is applied
   void sync() {
     if (claim.load(std::memory_order_acquire) == kFree) own();
     if (claim.load(std::memory_order_acquire) == kServed) {
-      const uint32_t h = head.load(std::memory_order_relaxed);
+      publish();
       int spins = 0;
-      while (tail.load(std::memory_order_acquire) != h) spin_wait(spins);
+      while (tail.load(std::memory_order_acquire) != next) spin_wait(spins);
     }
   }
   void push(limb a, limb b, limb c, limb d) {
@@ -558,7 +563,7 @@ struct CofactorPipe {
       apply(Item{a, b, c, d});
       return;
     }
-    const uint32_t h = head.load(std::memory_order_relaxed);
+    const uint32_t h = next;
     // the consumer's position is read only when the last one seen leaves no room
     if (h - tail_seen >= kRing) tail_seen = tail.load(std::memory_order_acquire);
     if (h - tail_seen >= kRing) {
@@ -567,11 +572,15 @@ struct CofactorPipe {
         apply(Item{a, b, c, d});
         return;
       }
+      publish();
       int spins = 0;
       while (h - tail.load(std::memory_order_acquire) >= kRing) spin_wait(spins);
     }
     ring[h % kRing] = Item{a, b, c, d};
-    head.store(h + 1, std::memory_order_release);
+    next = h + 1;
+    // batches go out a few at a time: every store of head takes its cache
+    // line away from the spinning server
+    if (next - head.load(std::memory_order_relaxed) >= kPublish) head.store(next, std::memory_order_release);
   }
   void serve() {
     int expect = kFree;
@@ -627,83 +636,94 @@ constexpr int kLowSlots = 4;            // servers one pipe takes
 constexpr size_t kSplitMinLimbs = 160;  // shorter remainders stay on the run's thread
 
 // As lehmer_sim, for leading parts known only to lie in (a - 1, a + 2) and
-// (b - 1, b + 2).  The quotient steps are run plainly on (a, b), keeping every
-// step's remainders (alpha, beta) and cofactors; then the longest prefix is
-// taken whose matrix has alpha > beta > 0 at all four corners of the box
-// [a - 1, a + 2] x [b - 1, b + 2]: that makes its quotients the first ones of
-// Euclid's algorithm at every point of the box (the continued fraction
-// argument of the half-gcd below; alpha and beta are linear, so the corners
-// decide), hence on the true remainders.  The stop condition is checked the
-// same way.  Every divisor stays at least 2^66 and every cofactor below 2^61,
-// so no product overflows and the row sums stay below 2^62.
+// (b - 1, b + 2).  Candidates come from plain quotient steps on the leading
+// 64 bits of the current remainders (cofactors below 2^32 per level, at most
+// three levels); a candidate is taken only when the composite matrix has
+// alpha > beta > 0 at all four corners of the box [a - 1, a + 2] x
+// [b - 1, b + 2], with alpha, beta its remainders: that makes its quotients
+// the first ones of Euclid's algorithm at every point of the box (the
+// continued fraction argument of the half-gcd below; alpha and beta are
+// linear, so the corners decide), hence on the true remainders.  The longest
+// such prefix of each level is kept; the stop condition is checked the same
+// way.  Composite cofactors stay below 2^61 (row sums below 2^62), and every
+// remainder at the base point fits in 127 bits (the steps only reduce them).
 static LMat lehmer_sim_wide(__int128 a, __int128 b, __int128 stop) {
   const __int128 kMin = (__int128)1 << 66;
   const __int128 kCap = (__int128)1 << 61;
-  constexpr int kMax = 96;
-  struct Step {
-    __int128 a, b;
-    int64_t A, B, C, D;
-  };
-  Step st[kMax];
-  int n = 0;
+  const int64_t kLevelCap = (int64_t)1 << 32;
+  constexpr int kSteps = 64;
   int64_t A = 1, B = 0, C = 0, D = 1;
-  while (n < kMax && b >= kMin && a >= b) {
-    // q = floor(a / b): the small quotients (two in three) by subtraction,
-    // the others from a double-precision estimate (relative error below
-    // 2^-50, so at most one off for q < 2^61) and one correction
-    int64_t q = 1;
-    __int128 r = a - b;
-    if (r >= b) {
-      r -= b;
-      q = 2;
-      if (r >= b) {
-        r -= b;
-        q = 3;
-        if (r >= b) {
-          const double ad = (double)(uint64_t)(a >> 64) * 0x1p64 + (double)(uint64_t)a;
-          const double bd = (double)(uint64_t)(b >> 64) * 0x1p64 + (double)(uint64_t)b;
-          const double qd = ad / bd;
-          if (!(qd < 0x1p60)) break;
-          q = (int64_t)qd;
-          r = a - (__int128)q * b;
-          while (r < 0) {
-            --q;
-            r += b;
-          }
-          while (r >= b) {
-            ++q;
-            r -= b;
+  __int128 al = a, be = b;  // the composite's remainders at the base point
+  size_t k = 0;
+  for (int level = 0; level < 3; ++level) {
+    if (be < kMin || al < be) break;
+    const int sh = 64 - __builtin_clzll((uint64_t)(al >> 64));  // al >= 2^66: bitlen(al) - 64
+    int64_t h[kSteps][4];
+    int n = 0;
+    {
+      uint64_t x = (uint64_t)(al >> sh), y = (uint64_t)(be >> sh);
+      int64_t a2 = 1, b2 = 0, c2 = 0, d2 = 1;
+      while (n < kSteps && y >= ((uint64_t)1 << 34)) {
+        uint64_t q = 1, r = x - y;
+        if (r >= y) {
+          r -= y;
+          q = 2;
+          if (r >= y) {
+            r -= y;
+            q = 3;
+            if (r >= y) {
+              q = x / y;
+              r = x - q * y;
+            }
           }
         }
+        if (q >= (uint64_t)kLevelCap) break;
+        const int64_t nc = a2 - (int64_t)q * c2, nd = b2 - (int64_t)q * d2;
+        if (nc >= kLevelCap || -nc >= kLevelCap || nd >= kLevelCap || -nd >= kLevelCap) break;
+        a2 = c2;
+        b2 = d2;
+        c2 = nc;
+        d2 = nd;
+        x = y;
+        y = r;
+        h[n][0] = a2, h[n][1] = b2, h[n][2] = c2, h[n][3] = d2;
+        ++n;
       }
     }
-    if (q >= kCap) break;
-    const __int128 nC = (__int128)A - (__int128)q * C, nD = (__int128)B - (__int128)q * D;
-    if (nC >= kCap || -nC >= kCap || nD >= kCap || -nD >= kCap) break;
-    A = C;
-    B = D;
-    C = (int64_t)nC;
-    D = (int64_t)nD;
-    a = b;
-    b = r;
-    st[n++] = Step{a, b, A, B, C, D};
-  }
-  for (int k = n - 1; k >= 0; --k) {
-    const Step& s = st[k];
-    bool ok = true;
-    for (int j = 0; j < 4 && ok; ++j) {
-      const int da = (j & 1) ? 2 : -1, db = (j & 2) ? 2 : -1;
-      const __int128 al = s.a + (__int128)s.A * da + (__int128)s.B * db;
-      const __int128 be = s.b + (__int128)s.C * da + (__int128)s.D * db;
-      ok = be > 0 && al > be && be >= stop;
+    const int64_t alh = (int64_t)(al >> 64), beh = (int64_t)(be >> 64);
+    const uint64_t all = (uint64_t)al, bel = (uint64_t)be;
+    int got = -1;
+    for (int j = n - 1; j >= 0 && got < 0; --j) {
+      const int64_t a2 = h[j][0], b2 = h[j][1], c2 = h[j][2], d2 = h[j][3];
+      const __int128 cA = (__int128)a2 * A + (__int128)b2 * C, cB = (__int128)a2 * B + (__int128)b2 * D;
+      const __int128 cC = (__int128)c2 * A + (__int128)d2 * C, cD = (__int128)c2 * B + (__int128)d2 * D;
+      if (cA >= kCap || -cA >= kCap || cB >= kCap || -cB >= kCap || cC >= kCap || -cC >= kCap || cD >= kCap ||
+          -cD >= kCap)
+        continue;
+      // (a2 al + b2 be, c2 al + d2 be) with al, be split at 2^64: the high
+      // parts nearly cancel, so no partial sum overflows
+      const __int128 ra = ((__int128)a2 * alh + (__int128)b2 * beh) * ((__int128)1 << 64) +
+                          ((__int128)a2 * (__int128)all + (__int128)b2 * (__int128)bel);
+      const __int128 rb = ((__int128)c2 * alh + (__int128)d2 * beh) * ((__int128)1 << 64) +
+                          ((__int128)c2 * (__int128)all + (__int128)d2 * (__int128)bel);
+      bool ok = true;
+      for (int c = 0; c < 4 && ok; ++c) {
+        const int da = (c & 1) ? 2 : -1, db = (c & 2) ? 2 : -1;
+        const __int128 x = ra + cA * da + cB * db, y = rb + cC * da + cD * db;
+        ok = y > 0 && x > y && y >= stop;
+      }
+      if (!ok) continue;
+      got = j;
+      A = (int64_t)cA, B = (int64_t)cB, C = (int64_t)cC, D = (int64_t)cD;
+      al = ra;
+      be = rb;
+      k += (size_t)j + 1;
     }
-    if (ok) {
-      LMat M;
-      M.A = s.A, M.B = s.B, M.C = s.C, M.D = s.D, M.k = (size_t)k + 1;
-      return M;
-    }
+    if (got < 0) break;
   }
-  return LMat{};
+  LMat M;
+  M.A = A, M.B = B, M.C = C, M.D = D, M.k = k;
+  return M;
 }
 
 // x += c on a w-limb two's complement number (the result must fit).
@@ -766,13 +786,15 @@ struct LowPipe {
   std::atomic<bool> closed{false};
   int joined = 0;           // the run's count of slots taken into rounds
   uint32_t tail_seen = 0;   // the run's last look at the slowest server
+  uint32_t next = 0;        // the run's next ring slot (head trails it by under kPublish)
+  static constexpr uint32_t kPublish = 4;
   Slot slot[kLowSlots];
 
   bool served() const { return claimed.load(std::memory_order_acquire) > 0; }
   // the run, between rounds: takes in the servers that have arrived
   int begin_round() {
     const int n = std::min(claimed.load(std::memory_order_acquire), kLowSlots);
-    const uint32_t hd = head.load(std::memory_order_relaxed);
+    const uint32_t hd = next;  // every item so far is published and done
     for (; joined < n; ++joined) {
       slot[joined].tail.store(hd, std::memory_order_relaxed);
       slot[joined].joined.store(true, std::memory_order_release);
@@ -781,26 +803,31 @@ struct LowPipe {
     return joined;
   }
   uint32_t min_tail() const {
-    const uint32_t hd = head.load(std::memory_order_relaxed);
     uint32_t lag = 0;
-    for (int j = 0; j < joined; ++j) lag = std::max(lag, hd - slot[j].tail.load(std::memory_order_acquire));
-    return hd - lag;
+    for (int j = 0; j < joined; ++j) lag = std::max(lag, next - slot[j].tail.load(std::memory_order_acquire));
+    return next - lag;
+  }
+  void publish() {
+    if (head.load(std::memory_order_relaxed) != next) head.store(next, std::memory_order_release);
   }
   void push(const LMat& L, size_t w) {
-    const uint32_t hd = head.load(std::memory_order_relaxed);
     int spins = 0;
     // the servers' positions are read only when the last ones seen leave no room
-    while (hd - tail_seen >= kRing) {
+    while (next - tail_seen >= kRing) {
+      publish();
       tail_seen = min_tail();
-      if (hd - tail_seen >= kRing) spin_wait(spins);
+      if (next - tail_seen >= kRing) spin_wait(spins);
     }
-    ring[hd % kRing] = Item{L.A, L.B, L.C, L.D, w};
-    head.store(hd + 1, std::memory_order_release);
+    ring[next % kRing] = Item{L.A, L.B, L.C, L.D, w};
+    ++next;
+    // a few batches at a time: every store of head takes its cache line away
+    // from the spinning servers
+    if (next - head.load(std::memory_order_relaxed) >= kPublish) head.store(next, std::memory_order_release);
   }
   void drain() {
-    const uint32_t hd = head.load(std::memory_order_relaxed);
+    publish();
     int spins = 0;
-    while (min_tail() != hd) spin_wait(spins);
+    while (min_tail() != next) spin_wait(spins);
   }
   void serve() {
     const int j = claimed.fetch_add(1, std::memory_order_acq_rel);
@@ -844,8 +871,8 @@ size_t bits_u64(uint64_t v) { return v ? 64 - (size_t)__builtin_clzll(v) : 0; }
 bool split_round(Nat& r0, Nat& r1, CofactorPipe* P, LowPipe* S, size_t* steps, long nbits) {
   const int ns = S->begin_round();
   const size_t len = r0.size();
-  // the run also simulates each batch: it keeps the top eighth
-  const size_t h = len * 7 / 8;
+  // the run also simulates each batch: it keeps the top 3/16
+  const size_t h = len * 13 / 16;
   const size_t lt = len - h + 1;
   if (ns < 1 || r1.size() < h + 8 || lt < 16 || h < (size_t)ns * (kLowCorr + 2)) return false;
   Nat t0(lt, 0), t1(lt, 0);
