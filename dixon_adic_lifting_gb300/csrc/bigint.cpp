@@ -331,21 +331,54 @@ static u128 bits128_at(const Nat& x, size_t sh) {  // floor(x / 2^sh) mod 2^128
 // with no carry coming in at lo; the carries out of limb hi - 1 are returned.
 // Each product |coef| * limb is below 2^126, so one signed 128-bit accumulator
 // per output holds the limb sum and a signed carry; the signs are template
-// parameters so the loop has no branches.
+// parameters so the loop has no branches.  Where both inputs have limbs, the
+// range is cut in two halves that run as two independent carry chains side
+// by side (the chain through the carries, not the multiplies, bounds one
+// chain's speed); the lower half's carries are then added into the upper
+// half, which rarely takes them past a limb or two.  In place (o0 == x,
+// o1 == y) is allowed: every limb is read before it is written.
+template <bool NA, bool NB, bool NC, bool ND>
+static inline void lin2x2_limb(limb xi, limb yi, limb a, limb b, limb c, limb d, __int128& c0, __int128& c1,
+                               limb* o0, limb* o1) {
+  const __int128 pa = (__int128)((u128)a * xi), pb = (__int128)((u128)b * yi);
+  const __int128 pc = (__int128)((u128)c * xi), pd = (__int128)((u128)d * yi);
+  const __int128 t0 = c0 + (NA ? -pa : pa) + (NB ? -pb : pb);
+  const __int128 t1 = c1 + (NC ? -pc : pc) + (ND ? -pd : pd);
+  *o0 = (limb)t0;
+  *o1 = (limb)t1;
+  c0 = t0 >> 64;
+  c1 = t1 >> 64;
+}
+static __int128 carry_into(limb* o, size_t from, size_t to, __int128 c) {  // o[from, to) += c; the carry out
+  for (size_t k = from; k < to && c != 0; ++k) {
+    const __int128 s = c + (__int128)o[k];
+    o[k] = (limb)s;
+    c = s >> 64;
+  }
+  return c;
+}
 template <bool NA, bool NB, bool NC, bool ND>
 static void lin2x2_range(limb* o0, limb* o1, const limb* x, size_t xn, const limb* y, size_t yn, size_t lo,
                          size_t hi, limb a, limb b, limb c, limb d, __int128* cr0, __int128* cr1) {
   __int128 c0 = 0, c1 = 0;
-  for (size_t i = lo; i < hi; ++i) {
+  size_t i = lo;
+  const size_t full = std::min(hi, std::min(xn, yn));
+  if (full >= lo + 32) {
+    const size_t half = (full - lo) / 2, mid = lo + half;
+    __int128 e0 = 0, e1 = 0;
+    for (size_t k = 0; k < half; ++k) {
+      const limb xl = x[lo + k], yl = y[lo + k], xh = x[mid + k], yh = y[mid + k];
+      lin2x2_limb<NA, NB, NC, ND>(xl, yl, a, b, c, d, c0, c1, o0 + lo + k, o1 + lo + k);
+      lin2x2_limb<NA, NB, NC, ND>(xh, yh, a, b, c, d, e0, e1, o0 + mid + k, o1 + mid + k);
+    }
+    for (size_t k = mid + half; k < full; ++k) lin2x2_limb<NA, NB, NC, ND>(x[k], y[k], a, b, c, d, e0, e1, o0 + k, o1 + k);
+    c0 = e0 + carry_into(o0, mid, full, c0);
+    c1 = e1 + carry_into(o1, mid, full, c1);
+    i = full;
+  }
+  for (; i < hi; ++i) {
     const limb xi = i < xn ? x[i] : 0, yi = i < yn ? y[i] : 0;
-    const __int128 pa = (__int128)((u128)a * xi), pb = (__int128)((u128)b * yi);
-    const __int128 pc = (__int128)((u128)c * xi), pd = (__int128)((u128)d * yi);
-    const __int128 t0 = c0 + (NA ? -pa : pa) + (NB ? -pb : pb);
-    const __int128 t1 = c1 + (NC ? -pc : pc) + (ND ? -pd : pd);
-    o0[i] = (limb)t0;
-    o1[i] = (limb)t1;
-    c0 = t0 >> 64;
-    c1 = t1 >> 64;
+    lin2x2_limb<NA, NB, NC, ND>(xi, yi, a, b, c, d, c0, c1, o0 + i, o1 + i);
   }
   *cr0 = c0;
   *cr1 = c1;

@@ -175,6 +175,10 @@ Nat shifted_to_residue(Nat X, const Nat& Mhalf, const Nat& Mhalf1) {
 
 void lcm_in(Nat& d, const Nat& v) {
   if (big::cmp(d, v) == 0 || v.empty()) return;
+  if (d.size() == 1 && d[0] == 1) {  // lcm(1, v) = v
+    d = v;
+    return;
+  }
   Nat g = big::gcd(d, v), q;
   big::divmod(v, g, &q, nullptr);
   d = big::mul(d, q);
