@@ -539,9 +539,10 @@ static void euclid(Nat& r0, Nat& r1, Nat* T0, Nat* T1, size_t* steps, long nbits
 //     its batches directly; a late serve() then returns at once.
 // So the run never waits for a thread that has not started, and a pool as
 // narrow as one thread still finishes.  A division step with the pipe served
-// waits for the ring to drain, then updates the cofactors itself.  (Splitting
-// the remainder updates between threads as well did not pay: the handoff per
-// batch costs what the split saves.)
+// waits for the ring to drain, then updates the cofactors itself.  (The
+// remainder updates are split too, by the low-limb pipe below; a split that
+// waits for the other thread at every batch did not pay: that handoff costs
+// what the split saves.)
 namespace {
 inline void spin_wait(int& spins) {
   if (++spins > 512) std::this_thread::yield();

@@ -250,7 +250,8 @@ int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples);
  * The planted cases, and residues with no small fraction behind them, are
  * reconstructed every way the library can (plain Lehmer loop; cofactors
  * handed to a thread that serves the run's pipe, started before the run or
- * after it; half-gcd stages; both), which must agree exactly.  Returns
+ * after it; also the remainders' low limbs handed to two more threads;
+ * half-gcd stages; combinations), which must agree exactly.  Returns
  * the number of failed checks (0 = pass), or -1 on bad arguments. */
 int64_t es_selftest_bigint(uint64_t seed, int64_t rounds);
 
