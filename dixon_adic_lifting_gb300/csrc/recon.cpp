@@ -386,19 +386,22 @@ extern "C" int64_t es_selftest_modular(int64_t lo, int64_t hi, int64_t samples) 
 
 // rational_reconstruct in one of the ways the library can run it: way & 1: a
 // cofactor pipe served by a second thread that starts before the run (way & 4:
-// after it, so the run keeps the work), way & 8 (with way & 1): a low-limb
-// pipe as well, served by two more threads started at the same point, way & 2:
-// half-gcd stages from any length.
-static const int kWays[] = {0, 1, 2, 3, 5, 9, 11, 13};
+// after it, so the run keeps the work); with way & 1, a low-limb pipe as well,
+// served by two more threads (way & 8), one (way & 16) or five, one more than
+// a pipe takes (way & 32), started at the same point (way & 64: each after a
+// short delay of its own, so that they join while the run is under way);
+// way & 2: half-gcd stages from any length.
+static const int kWays[] = {0, 1, 2, 3, 5, 9, 11, 13, 17, 33, 73, 81};
 static bool reconstruct_way(const es::big::Nat& M, const es::big::Nat& u, size_t nbits, int way, es::big::Nat* num,
                             bool* neg, es::big::Nat* den) {
   namespace big = es::big;
   big::ReconOpts o;
   if (way & 2) o.hgcd_min_bits = 0;
   if (!(way & 1)) return big::rational_reconstruct(M, u, nbits, num, neg, den, o);
+  const int servers = (way & 8) ? 2 : (way & 16) ? 1 : (way & 32) ? 5 : 0;
   big::CofactorPipe* pipe = big::cofactor_pipe_new();
-  big::LowPipe* low = (way & 8) ? big::low_pipe_new() : nullptr;
-  if (!pipe || ((way & 8) && !low)) {
+  big::LowPipe* low = servers ? big::low_pipe_new() : nullptr;
+  if (!pipe || (servers && !low)) {
     big::cofactor_pipe_free(pipe);
     big::low_pipe_free(low);
     return false;
@@ -408,8 +411,11 @@ static bool reconstruct_way(const es::big::Nat& M, const es::big::Nat& u, size_t
   auto serve = [&] {
     std::vector<std::thread> th;
     th.emplace_back([&] { big::cofactor_pipe_serve(pipe); });
-    if (low)
-      for (int i = 0; i < 2; ++i) th.emplace_back([&] { big::low_pipe_serve(low); });
+    for (int i = 0; i < servers; ++i)
+      th.emplace_back([&, i] {
+        if (way & 64) std::this_thread::sleep_for(std::chrono::microseconds(20 + 40 * i));
+        big::low_pipe_serve(low);
+      });
     return th;
   };
   bool ok = false;
