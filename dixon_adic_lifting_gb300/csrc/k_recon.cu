@@ -326,6 +326,8 @@ inline int64_t numerator_smem(int64_t LG, int64_t mp) {
   return 4 * kGroup * (zn_groups(LG) + qq_groups(LG)) + 4 * mp * kDigitWords + 8 * zn_groups(LG);
 }
 
+// Five CTAs per SM (48 registers): 1024 components take 1.35 waves of 760 CTAs
+// rather than 1.7 waves of 608.
 __global__ void __launch_bounds__(256, 5) k_recon_numerators(RParams p) {
   const int64_t k = blockIdx.x;
   const int mp = p.mp, LG = p.LG;
