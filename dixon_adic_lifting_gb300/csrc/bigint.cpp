@@ -640,6 +640,9 @@ void cofactor_pipe_free(CofactorPipe* p) { delete p; }
 void cofactor_pipe_serve(CofactorPipe* p) {
   if (p) p->serve();
 }
+void cofactor_pipe_close(CofactorPipe* p) {
+  if (p) p->closed.store(true, std::memory_order_release);
+}
 
 // ------------------------------------------------------------ low-limb pipe
 // The remainder updates of the Lehmer loop split by limbs between the run and
@@ -892,6 +895,9 @@ LowPipe* low_pipe_new() { return new (std::nothrow) LowPipe; }
 void low_pipe_free(LowPipe* p) { delete p; }
 void low_pipe_serve(LowPipe* p) {
   if (p) p->serve();
+}
+void low_pipe_close(LowPipe* p) {
+  if (p) p->closed.store(true, std::memory_order_release);
 }
 
 namespace {

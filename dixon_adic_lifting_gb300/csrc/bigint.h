@@ -42,6 +42,9 @@ struct CofactorPipe;
 CofactorPipe* cofactor_pipe_new();  // null when out of memory
 void cofactor_pipe_free(CofactorPipe* p);
 void cofactor_pipe_serve(CofactorPipe* p);
+// Ends serve() calls once nothing is left for them (a run closes its pipes
+// itself on every way out; closing again is harmless).
+void cofactor_pipe_close(CofactorPipe* p);
 // A low-limb pipe lets a further thread take the low limbs of the remainders
 // of one run that has a cofactor pipe (ReconOpts::low): the run updates the
 // high limbs from each batch's matrix and that thread follows over the low
@@ -52,6 +55,7 @@ struct LowPipe;
 LowPipe* low_pipe_new();  // null when out of memory
 void low_pipe_free(LowPipe* p);
 void low_pipe_serve(LowPipe* p);
+void low_pipe_close(LowPipe* p);  // as cofactor_pipe_close
 // How rational_reconstruct runs.  pipe: its Lehmer loop hands the cofactor
 // updates to whoever serves the pipe; low (with pipe only): the low limbs of
 // the remainders likewise.  hgcd_min_bits: from this length of M on,

@@ -204,9 +204,12 @@ void denominators_parallel(int64_t count, int width, const std::function<void(in
   }
   const int64_t tasks = opts.empty() || !opts[0].pipe ? count : (2 + low) * count;
   parallel_for(tasks, width, [&](int64_t t) {
-    if (t < count)
+    if (t < count) {
       run(t, opts[(size_t)t]);
-    else if (t < 2 * count)
+      // the servers return even if the run never reached the reconstruction
+      big::cofactor_pipe_close(opts[(size_t)t].pipe);
+      big::low_pipe_close(opts[(size_t)t].low);
+    } else if (t < 2 * count)
       big::cofactor_pipe_serve(opts[(size_t)(t - count)].pipe);
     else
       big::low_pipe_serve(opts[(size_t)((t - 2 * count) % count)].low);
