@@ -200,3 +200,16 @@ def test_host_reconstruction_random_many_columns(lib, seed):
     for threads in (1, 4):
         s = api.reconstruct(digits_to_limbs(digits), n, c, m, good, nb, db, threads=threads)
         assert (s.N, s.d) == exact.solve(A, b)
+
+
+@pytest.mark.parametrize("threads", [8, 16])
+def test_host_reconstruction_through_the_pool_pipes(lib, threads):
+    # 64 x 64, 24-bit entries: M has about 55 limbs, so every sampled run hands
+    # its cofactors to a pool task (pools of 8 and more); with 16 tasks on a
+    # smaller machine the low-limb servers start only after their runs and must
+    # return at once
+    A, b = inputs.uniform(64, 1, -(1 << 23), 1 << 23, seed=64)
+    A, b = A.tolist(), b.tolist()
+    digits, good, nb, db, m = model_digits(A, b)
+    s = api.reconstruct(digits_to_limbs(digits), 64, 1, m, good, nb, db, threads=threads)
+    assert (s.N, s.d) == exact.solve(A, b)
